@@ -1,0 +1,384 @@
+// MoE-layer forward oracle: plain, slow, fp64 CPU code.
+//
+// TEST INFRASTRUCTURE. Only the test suite, the smoke check and the benchmark's
+// CPU-baseline leg load this library. The product path (the CUDA library under
+// mixture_experts_layer_gemv_gb300/csrc) shares no code, header, table or helper
+// with it, and neither side includes or links the other.
+//
+// What it computes, step by step, follows the DeepSeek-V2 MoE stages as described
+// on "DSV2-236B-MegaKernel" (README, stage flowchart, MoE subgraph, stages M..R):
+//   N  router GEMV            logits = W_router . x                      (fp64 here)
+//   O  softmax + group-limited greedy top-k, w = score * routed_scaling_factor
+//   P1 routed gate+up, FP8 block-scaled weights, SiLU(g) * u
+//   P2 routed down, times the routing weight w
+//   Q1/Q2 shared experts (fused into one MLP of width n_shared * moe_inter)
+//   R  combine: h = shared_out + sum of routed (+ residual when one is given)
+// The FP8 activation quantisation (one power-of-two scale per token and 128
+// channels) is this build's reading of the pages' "FP8 block-scaled MoE GEMMs"
+// (README "Results") and of "MXFP8 input quantization" (the DeepSeek-V4.1 Flash
+// lecture, "Rounds 12-15" table); the scale form follows the pages' quantiser with
+// UE8M0 (power-of-two) scale factors (README "Layout", quant/fp8_block_quant.py).
+//
+// Parity pins (tests/test_oracle_*.py) tie every function below to something other
+// than itself: the OCP E4M3 definition and torch's float8 conversion, closed forms,
+// brute-force enumeration, and fp64 library matmuls. The choice of activation
+// quantisation (on, power-of-two scale) is a reading of the pages, not something
+// the pages print a number for: that choice itself is parity unpinned.
+//
+// Build: g++ -std=c++17 -O3 -fopenmp -shared -fPIC moe_oracle.cpp -o libmoe_oracle.so
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+extern "C" {
+
+typedef struct {
+    int32_t hidden;      // H
+    int32_t moe_inter;   // I, width of one routed expert
+    int32_t n_routed;    // E
+    int32_t n_group;     // G, experts form G contiguous groups of E/G
+    int32_t topk_group;  // Gk, groups kept per token
+    int32_t top_k;       // k, experts kept per token
+    int32_t n_shared;    // S, shared experts fused into one MLP of width S*I
+    int32_t act_quant;   // 1: FP8 activation quantisation (the method); 0: off
+    double routed_scaling_factor;  // s
+} orc_cfg_t;
+
+// ---------------------------------------------------------------- E4M3 format
+// OCP FP8 E4M3FN: bit 7 sign, bits 6..3 biased exponent (bias 7), bits 2..0
+// mantissa. Exponent field 0 encodes subnormals m/8 * 2^-6. S.1111.111 is NaN;
+// there is no infinity, so the largest finite magnitude is 1.75 * 2^8 = 448.
+double orc_e4m3_decode(uint8_t code) {
+    const int sign = code >> 7;
+    const int e = (code >> 3) & 0xF;
+    const int m = code & 0x7;
+    if (e == 0xF && m == 0x7) return std::numeric_limits<double>::quiet_NaN();
+    double mag;
+    if (e == 0)
+        mag = std::ldexp((double)m / 8.0, -6);
+    else
+        mag = std::ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+// Round to the nearest E4M3 value, ties to the even code (the code's last bit is
+// the mantissa's last bit), saturating to +-448. NaN maps to 0x7F.
+uint8_t orc_e4m3_encode(double v) {
+    if (std::isnan(v)) return 0x7F;
+    const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+    const double a = std::fabs(v);
+    // The 127 finite non-negative codes 0x00..0x7E are increasing in value.
+    struct Grid {
+        double v[127];
+        Grid() {
+            for (int c = 0; c < 127; ++c) v[c] = orc_e4m3_decode((uint8_t)c);
+        }
+    };
+    static const Grid G;  // thread-safe one-time initialisation
+    const double* grid = G.v;
+    if (a >= grid[126]) return sign | 0x7E;
+    // first code whose value is >= a
+    int hi = (int)(std::lower_bound(grid, grid + 127, a) - grid);
+    if (grid[hi] == a) return sign | (uint8_t)hi;
+    int lo = hi - 1;
+    const double dlo = a - grid[lo], dhi = grid[hi] - a;
+    int c;
+    if (dlo < dhi)
+        c = lo;
+    else if (dhi < dlo)
+        c = hi;
+    else
+        c = (lo % 2 == 0) ? lo : hi;
+    return sign | (uint8_t)c;
+}
+
+// ------------------------------------------------------ activation quantisation
+// One block of 128 values: scale = the smallest power of two 2^k with
+// amax <= 448 * 2^k (amax = 0 gives scale 1 and all-zero codes), then
+// q = RNE-to-E4M3(v / scale). v / scale is exact because the scale is 2^k.
+void orc_quant_block(const double* v, int n, uint8_t* q, double* scale_out) {
+    double amax = 0.0;
+    for (int i = 0; i < n; ++i) amax = std::max(amax, std::fabs(v[i]));
+    double scale = 1.0;
+    if (amax > 0.0) {
+        int k = (int)std::ceil(std::log2(amax / 448.0));
+        while (amax > 448.0 * std::ldexp(1.0, k)) ++k;
+        while (amax <= 448.0 * std::ldexp(1.0, k - 1)) --k;
+        scale = std::ldexp(1.0, k);
+    }
+    for (int i = 0; i < n; ++i) q[i] = (amax > 0.0) ? orc_e4m3_encode(v[i] / scale) : 0;
+    *scale_out = scale;
+}
+
+// Quantise a length-n vector (n a multiple of 128) block by block, and write the
+// dequantised values q * scale to vhat (the operand the FP8 GEMM actually sees).
+static void quant_dequant(const double* v, int n, double* vhat, uint8_t* q, double* s) {
+    for (int b = 0; b < n / 128; ++b) {
+        orc_quant_block(v + b * 128, 128, q + b * 128, s + b);
+        for (int i = 0; i < 128; ++i) vhat[b * 128 + i] = orc_e4m3_decode(q[b * 128 + i]) * s[b];
+    }
+}
+
+void orc_quant_rows(const double* v, int rows, int n, uint8_t* q, double* s) {
+    std::vector<double> tmp(n);
+    for (int r = 0; r < rows; ++r)
+        quant_dequant(v + (size_t)r * n, n, tmp.data(), q + (size_t)r * n, s + (size_t)r * (n / 128));
+}
+
+static double bf16_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+// ------------------------------------------------------------------ N: router
+// logits[t][e] = sum_h x[t][h] * W_router[e][h]  (+ bias[e] when given)
+void orc_router_logits(const orc_cfg_t* c, const uint16_t* x_bf16, int T, const float* w_router,
+                       const float* bias, double* logits) {
+    const int H = c->hidden, E = c->n_routed;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += bf16_to_double(x_bf16[(size_t)t * H + h]) * (double)w_router[(size_t)e * H + h];
+            if (bias) acc += (double)bias[e];
+            logits[(size_t)t * E + e] = acc;
+        }
+}
+
+// ------------------------------------------- O: softmax + group-limited top-k
+// p = softmax over all E experts. Group j holds experts [j*E/G, (j+1)*E/G) and
+// scores max(p) over its members. The topk_group best groups are kept (ties: lower
+// group index), the top_k best experts among them are selected (ties: lower expert
+// index), listed by score descending then index ascending, and weighted
+// w = p * routed_scaling_factor with no renormalisation.
+// margin[t] = smallest gap, in probability units, that decided token t: between
+// the last kept and first dropped group, between the last selected and first
+// unselected eligible expert, and between adjacent selected experts.
+void orc_topk(const orc_cfg_t* c, const double* logits, int T, int32_t* ids, double* w,
+              double* probs_out, double* margin) {
+    const int E = c->n_routed, G = c->n_group, Gk = c->topk_group, k = c->top_k;
+    const int per = E / G;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const double* l = logits + (size_t)t * E;
+        std::vector<double> p(E);
+        double mx = -std::numeric_limits<double>::infinity();
+        for (int e = 0; e < E; ++e) mx = std::max(mx, l[e]);
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) {
+            p[e] = std::exp(l[e] - mx);
+            z += p[e];
+        }
+        for (int e = 0; e < E; ++e) p[e] /= z;
+        if (probs_out)
+            for (int e = 0; e < E; ++e) probs_out[(size_t)t * E + e] = p[e];
+
+        std::vector<double> gs(G);
+        for (int g = 0; g < G; ++g) {
+            double m = p[g * per];
+            for (int i = 1; i < per; ++i) m = std::max(m, p[g * per + i]);
+            gs[g] = m;
+        }
+        std::vector<int> gord(G);
+        for (int g = 0; g < G; ++g) gord[g] = g;
+        std::stable_sort(gord.begin(), gord.end(), [&](int a, int b) { return gs[a] > gs[b]; });
+
+        std::vector<int> cand;
+        for (int r = 0; r < Gk; ++r)
+            for (int i = 0; i < per; ++i) cand.push_back(gord[r] * per + i);
+        std::sort(cand.begin(), cand.end());
+        std::stable_sort(cand.begin(), cand.end(), [&](int a, int b) { return p[a] > p[b]; });
+
+        double mg = std::numeric_limits<double>::infinity();
+        if (Gk < G) mg = std::min(mg, gs[gord[Gk - 1]] - gs[gord[Gk]]);
+        if (k < (int)cand.size()) mg = std::min(mg, p[cand[k - 1]] - p[cand[k]]);
+        for (int j = 0; j + 1 < k; ++j) mg = std::min(mg, p[cand[j]] - p[cand[j + 1]]);
+        if (margin) margin[t] = mg;
+
+        for (int j = 0; j < k; ++j) {
+            ids[(size_t)t * k + j] = cand[j];
+            w[(size_t)t * k + j] = p[cand[j]] * c->routed_scaling_factor;
+        }
+    }
+}
+
+// ------------------------------------------------------------- permutation
+// Stable counting sort of the T*k (token, slot) pairs by expert id. The pair
+// (t, j) has flat index f = t*k + j; pairs of one expert keep ascending f.
+//   expert_offsets[e] = number of pairs routed to experts < e  (E+1 entries)
+//   perm_src[pos]     = f of the pair at permuted position pos
+//   inv_pos[f]        = permuted position of pair f
+void orc_permute(const orc_cfg_t* c, const int32_t* ids, int T, int32_t* expert_offsets,
+                 int32_t* perm_src, int32_t* inv_pos) {
+    const int E = c->n_routed, k = c->top_k;
+    const int n = T * k;
+    std::vector<int32_t> count(E, 0);
+    for (int f = 0; f < n; ++f) count[ids[f]]++;
+    expert_offsets[0] = 0;
+    for (int e = 0; e < E; ++e) expert_offsets[e + 1] = expert_offsets[e] + count[e];
+    std::vector<int32_t> next(expert_offsets, expert_offsets + E);
+    for (int f = 0; f < n; ++f) {
+        const int pos = next[ids[f]]++;
+        perm_src[pos] = f;
+        inv_pos[f] = pos;
+    }
+}
+
+// ------------------------------------------------------- P1/P2: one expert MLP
+// For one token's dequantised activation xhat[H] and one expert's weights:
+//   g = Wg . xhat, u = Wu . xhat           (Wg, Wu: [N, H], block scales [N/128, H/128])
+//   a = SiLU(g) * u = g / (1 + e^-g) * u
+//   ahat = a, or its FP8 quantise-dequantise when act_quant is on
+//   y = w * (Wd . ahat)                    (Wd: [H, N], block scales [H/128, N/128])
+// with every weight dequantised as W[o][i] = dec(code[o][i]) * scale[o/128][i/128].
+// Writes y[H] (accumulated into y when accumulate != 0).
+static void expert_mlp(const double* dec_tab, int H, int N, int act_quant, const double* xhat,
+                       const uint8_t* wg, const float* sg, const uint8_t* wu, const float* su,
+                       const uint8_t* wd, const float* sd, double w, double* y, int accumulate,
+                       double* a_out) {
+    const int Hb = H / 128, Nb = N / 128;
+    std::vector<double> a(N);
+    for (int o = 0; o < N; ++o) {
+        double g = 0.0, u = 0.0;
+        const uint8_t* rg = wg + (size_t)o * H;
+        const uint8_t* ru = wu + (size_t)o * H;
+        for (int i = 0; i < H; ++i) {
+            g += dec_tab[rg[i]] * (double)sg[(size_t)(o / 128) * Hb + i / 128] * xhat[i];
+            u += dec_tab[ru[i]] * (double)su[(size_t)(o / 128) * Hb + i / 128] * xhat[i];
+        }
+        a[o] = g / (1.0 + std::exp(-g)) * u;
+    }
+    std::vector<double> ahat(N);
+    if (act_quant) {
+        std::vector<uint8_t> q(N);
+        std::vector<double> s(Nb);
+        quant_dequant(a.data(), N, ahat.data(), q.data(), s.data());
+    } else {
+        ahat = a;
+    }
+    if (a_out)
+        for (int o = 0; o < N; ++o) a_out[o] = ahat[o];
+    for (int o = 0; o < H; ++o) {
+        const uint8_t* rd = wd + (size_t)o * N;
+        double acc = 0.0;
+        for (int i = 0; i < N; ++i)
+            acc += dec_tab[rd[i]] * (double)sd[(size_t)(o / 128) * Nb + i / 128] * ahat[i];
+        y[o] = (accumulate ? y[o] : 0.0) + w * acc;
+    }
+}
+
+static void make_dec_tab(double* tab) {
+    for (int c = 0; c < 256; ++c) tab[c] = orc_e4m3_decode((uint8_t)c);
+}
+
+// The activation the expert GEMMs see for token row x: its FP8 quantise-dequantise
+// (act_quant on) or the bf16 value itself.
+static void token_xhat(const orc_cfg_t* c, const uint16_t* xrow, double* xhat) {
+    const int H = c->hidden;
+    std::vector<double> xv(H);
+    for (int h = 0; h < H; ++h) xv[h] = bf16_to_double(xrow[h]);
+    if (c->act_quant) {
+        std::vector<uint8_t> q(H);
+        std::vector<double> s(H / 128);
+        quant_dequant(xv.data(), H, xhat, q.data(), s.data());
+    } else {
+        for (int h = 0; h < H; ++h) xhat[h] = xv[h];
+    }
+}
+
+typedef struct {
+    const uint8_t *w_gate, *w_up, *w_down;   // [E,I,H], [E,I,H], [E,H,I] E4M3 codes
+    const float *s_gate, *s_up, *s_down;     // [E,I/128,H/128], same, [E,H/128,I/128]
+    const uint8_t *ws_gate, *ws_up, *ws_down;  // shared [Is,H], [Is,H], [H,Is]; NULL if S=0
+    const float *ss_gate, *ss_up, *ss_down;    // [Is/128,H/128], same, [H/128,Is/128]
+} orc_weights_t;
+
+// One routed (token, expert, weight) row: y[H] = w * expert_e(xhat(token)).
+// Also writes the expert's (dequantised) intermediate activation to a_out[I] if given.
+void orc_expert_row(const orc_cfg_t* c, const orc_weights_t* W, const uint16_t* x_row, int expert,
+                    double w, double* y, double* a_out) {
+    const int H = c->hidden, I = c->moe_inter, Hb = H / 128, Ib = I / 128;
+    double tab[256];
+    make_dec_tab(tab);
+    std::vector<double> xhat(H);
+    token_xhat(c, x_row, xhat.data());
+    const size_t e = (size_t)expert;
+    expert_mlp(tab, H, I, c->act_quant, xhat.data(), W->w_gate + e * I * H, W->s_gate + e * Ib * Hb,
+               W->w_up + e * I * H, W->s_up + e * Ib * Hb, W->w_down + e * H * I,
+               W->s_down + e * Hb * Ib, w, y, 0, a_out);
+}
+
+// The shared experts for one token: y[H] = shared_MLP(xhat(token)), weight 1.
+void orc_shared_row(const orc_cfg_t* c, const orc_weights_t* W, const uint16_t* x_row, double* y) {
+    const int H = c->hidden, Is = c->n_shared * c->moe_inter;
+    double tab[256];
+    make_dec_tab(tab);
+    std::vector<double> xhat(H);
+    token_xhat(c, x_row, xhat.data());
+    if (c->n_shared == 0) {
+        for (int h = 0; h < H; ++h) y[h] = 0.0;
+        return;
+    }
+    expert_mlp(tab, H, Is, c->act_quant, xhat.data(), W->ws_gate, W->ss_gate, W->ws_up, W->ss_up,
+               W->ws_down, W->ss_down, 1.0, y, 0, nullptr);
+}
+
+// R: the layer output for the listed tokens, in fp64.
+//   out[i][:] = sum_j w[t][j] * expert_{ids[t][j]}(xhat_t) + shared(xhat_t) (+ residual[t])
+// for t = tokens[i]. ids / w are the routing of all T tokens ([T,k], from orc_topk
+// or given by the caller); residual is bf16 [T,H] or NULL.
+void orc_forward_tokens(const orc_cfg_t* c, const orc_weights_t* W, const uint16_t* x_bf16,
+                        const int32_t* ids, const double* w, const uint16_t* residual_bf16,
+                        const int32_t* tokens, int n_tokens, double* out) {
+    const int H = c->hidden, I = c->moe_inter, k = c->top_k, Hb = H / 128, Ib = I / 128;
+    const int Is = c->n_shared * I;
+    double tab[256];
+    make_dec_tab(tab);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < n_tokens; ++i) {
+        const int t = tokens[i];
+        std::vector<double> xhat(H);
+        token_xhat(c, x_bf16 + (size_t)t * H, xhat.data());
+        double* o = out + (size_t)i * H;
+        for (int h = 0; h < H; ++h) o[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const size_t e = (size_t)ids[(size_t)t * k + j];
+            expert_mlp(tab, H, I, c->act_quant, xhat.data(), W->w_gate + e * I * H,
+                       W->s_gate + e * Ib * Hb, W->w_up + e * I * H, W->s_up + e * Ib * Hb,
+                       W->w_down + e * H * I, W->s_down + e * Hb * Ib, w[(size_t)t * k + j], o, 1,
+                       nullptr);
+        }
+        if (c->n_shared > 0)
+            expert_mlp(tab, H, Is, c->act_quant, xhat.data(), W->ws_gate, W->ss_gate, W->ws_up,
+                       W->ss_up, W->ws_down, W->ss_down, 1.0, o, 1, nullptr);
+        if (residual_bf16)
+            for (int h = 0; h < H; ++h) o[h] += bf16_to_double(residual_bf16[(size_t)t * H + h]);
+    }
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+}  // extern "C"
