@@ -1,0 +1,182 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) MoE-layer forward library (libmoe_gb300.so).
+ *
+ * The layer is the DeepSeek-style mixture-of-experts block described on
+ * "DSV2-236B-MegaKernel" (README, stage flowchart, MoE subgraph, stages M..R):
+ *   router GEMV -> softmax + group-limited greedy top-k, w = score * routed_scaling_factor
+ *   -> routed experts: FP8 block-scaled gate/up, SiLU(g) * u, down, times w
+ *   -> shared experts (same MLP, weight 1) -> h = shared_out + sum of routed (+ residual).
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_bf16, *_ids, *_w, weights and ws are DEVICE pointers, owned by
+ *     the caller; the library allocates no memory. All of them must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream). A returned MOE_OK means the work was enqueued.
+ *   - Arguments are validated on the host before anything is launched; a failed check
+ *     returns an error code and launches nothing.
+ *   - T = 0 is a valid no-op that returns MOE_OK.
+ *   - Row-major layouts everywhere. E4M3 = OCP FP8 E4M3FN, one byte per value.
+ *   - The library keeps no state between calls; concurrent calls need distinct workspaces.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The layer's arguments, named as in the DeepSeek-V2 configuration the README's
+ * "Model geometry" paragraph quotes (hidden 5120, moe_intermediate_size 1536, 160 routed
+ * experts in 8 groups, top-3 groups, top-6 experts, x16.0, 2 shared experts).
+ * Constraints (checked, MOE_ERR_UNSUPPORTED_SHAPE otherwise):
+ *   hidden % 128 == 0 and moe_inter % 128 == 0 (the 128-wide FP8 scale block,
+ *   README "Results": a TP=8 shard of 1536 is 192, not a multiple of 128);
+ *   1 <= n_routed <= 256; n_routed % n_group == 0; 1 <= n_group <= 32;
+ *   1 <= topk_group <= n_group; 1 <= top_k <= min(16, topk_group * n_routed / n_group);
+ *   0 <= n_shared; the shared experts are fused into one MLP of width n_shared*moe_inter. */
+typedef struct moe_config {
+    int32_t hidden;                /* H */
+    int32_t moe_inter;             /* I */
+    int32_t n_routed;              /* E */
+    int32_t n_group;               /* G */
+    int32_t topk_group;            /* Gk */
+    int32_t top_k;                 /* k */
+    int32_t n_shared;              /* S; shared width Is = S * I */
+    float routed_scaling_factor;   /* s; w = softmax score * s, no renormalisation */
+} moe_config_t;
+
+/* One layer's weights (device pointers). Expert weights are E4M3 codes with one fp32
+ * scale per 128x128 block: value[o][i] = e4m3(code[o][i]) * scale[o/128][i/128].
+ *   w_gate, w_up   [E, I, H]  codes     s_gate, s_up  [E, I/128, H/128] fp32
+ *   w_down         [E, H, I]  codes     s_down        [E, H/128, I/128] fp32
+ *   ws_gate, ws_up [Is, H]    codes     ss_gate, ss_up [Is/128, H/128]  fp32
+ *   ws_down        [H, Is]    codes     ss_down        [H/128, Is/128]  fp32
+ *   w_router       [E, H]     fp32      router_bias    [E] fp32 or NULL
+ * The shared pointers may be NULL when n_shared == 0. */
+typedef struct moe_weights {
+    const uint8_t *w_gate, *w_up, *w_down;
+    const float *s_gate, *s_up, *s_down;
+    const uint8_t *ws_gate, *ws_up, *ws_down;
+    const float *ss_gate, *ss_up, *ss_down;
+    const float *w_router, *router_bias;
+} moe_weights_t;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,       /* NULL / misaligned pointer, negative T */
+    MOE_ERR_UNSUPPORTED_SHAPE = -2, /* config outside the constraints above */
+    MOE_ERR_WORKSPACE = -3,         /* ws NULL or ws_bytes < moe_workspace_size(cfg, T) */
+    MOE_ERR_CUDA = -4,              /* a CUDA launch or runtime call failed */
+    MOE_ERR_DEVICE_TIMEOUT = -5     /* a bounded device-side wait ran out (see below) */
+} moe_status_t;
+
+/* Which kernel launch moe_forward_profiled brackets with CUDA events. */
+typedef enum moe_stage {
+    MOE_STAGE_ROUTE = 0,    /* router + top-k (+ permutation when fused) */
+    MOE_STAGE_PERMUTE = 1,  /* permutation (large T) */
+    MOE_STAGE_GATE_UP = 2,  /* routed + shared gate/up, SiLU(g) * u */
+    MOE_STAGE_DOWN = 3,     /* routed + shared down, times w */
+    MOE_STAGE_COMBINE = 4,  /* sum into the hidden vector */
+    MOE_STAGE_COUNT = 5
+} moe_stage_t;
+
+/* cudaEvent_t handles (or NULL) recorded on the call's stream immediately before and
+ * after the named stage's kernels. */
+typedef struct moe_stage_events {
+    void* start[MOE_STAGE_COUNT];
+    void* stop[MOE_STAGE_COUNT];
+} moe_stage_events_t;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t status);
+
+/* Bytes of device workspace every entry point below needs for up to max_tokens tokens
+ * (0 if the config is invalid). Workspace contents need no initialisation except its
+ * first 256 bytes (control words), which moe_workspace_init zeroes; the library returns
+ * them to zero at the end of every call, so one init after allocation suffices. */
+size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_tokens);
+
+/* Zero the control words at the start of ws (asynchronous memset on stream). */
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Device-side error word of ws: copies it to the host (synchronising `stream`), clears
+ * it, and returns MOE_OK or the recorded error (MOE_ERR_DEVICE_TIMEOUT when a bounded
+ * wait inside a kernel gave up; such a kernel skips its remaining work and returns
+ * instead of hanging). Every bounded wait has an iteration budget; none traps. */
+moe_status_t moe_read_device_status(void* ws, void* stream);
+
+/* Activation quantisation, the FP8 operand of the expert GEMMs: per token and block of
+ * 128 channels, scale = the smallest power of two 2^k with amax <= 448 * 2^k
+ * (amax = 0 -> scale 1), code = round-to-nearest-even E4M3 of x / scale.
+ * This is the reading of the pages' FP8 block-scaled expert GEMMs ("Results") with
+ * UE8M0 (power-of-two) scale factors (README "Layout", quant/fp8_block_quant.py).
+ *   x_bf16 [T, H] -> xq [T, H] E4M3 codes, xs [T, H/128] fp32 scales. */
+moe_status_t moe_quant_act(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq, float* xs,
+                           void* stream);
+
+/* Stage N + O: router GEMV/GEMM and group-limited greedy top-k.
+ *   logits[t][e] = sum_h x[t][h] * w_router[e][h] (+ router_bias[e])   (fp32)
+ *   p = softmax over all E; group j = experts [j*E/G, (j+1)*E/G) scores max p;
+ *   the topk_group best groups are kept (ties: lower group index); the top_k best
+ *   experts inside them are selected (ties: lower expert index).
+ * Outputs: topk_ids int32 [T, k] (score-descending), topk_w fp32 [T, k] = p * s.
+ * README, stage flowchart "N" and "O"; per-stage table rows "M+N" and "O". */
+moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                       const float* w_router, const float* router_bias, int32_t* topk_ids,
+                       float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/* Token permutation by expert: a stable counting sort of the T*k (token, slot) pairs.
+ * Pair (t, j) has flat index f = t*k + j.
+ *   expert_offsets int32 [E+1]: pairs routed to experts < e (exclusive prefix sum)
+ *   perm_src       int32 [T*k]: flat index of the pair at each permuted position
+ *   inv_pos        int32 [T*k]: permuted position of each flat index
+ * Within one expert the pairs keep ascending f. Ids outside [0, E) are an error the
+ * library does not check on the device: they must come from moe_route.
+ * ("router emits the layout the experts need": DeepSeek-V4.1 Flash lecture, "Rounds
+ * 12-15" table; MoK's GPU-side dispatch scheduling, abstract.) */
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32_t T,
+                         int32_t* expert_offsets, int32_t* perm_src, int32_t* inv_pos,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Stages P1/P2 and Q1/Q2: the expert MLPs on FP8 block-scaled weights.
+ * For permuted row r of expert e (token t = perm_src[r] / k, weight w = topk_w[perm_src[r]]):
+ *   g = Wg_e . xhat_t, u = Wu_e . xhat_t, a = SiLU(g) * u, ahat = FP8-quantised a
+ *   (as in moe_quant_act), y_perm[r] = w * (Wd_e . ahat)            -> bf16 [T*k, H]
+ * and for the shared experts (width Is, weight 1): y_shared[t]     -> bf16 [T, H]
+ * xhat is the moe_quant_act quantisation of x. y_shared may be NULL only if
+ * n_shared == 0. */
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                            const moe_weights_t* weights, const int32_t* expert_offsets,
+                            const int32_t* perm_src, const float* topk_w, void* y_perm_bf16,
+                            void* y_shared_bf16, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage R's local part: out[t] = sum_j y_perm[inv_pos[t*k + j]] + y_shared[t] (+ residual[t]),
+ * summed in fp32, rounded once to bf16 (README flowchart: "h += shared_out + routed").
+ * y_shared / residual may be NULL (treated as zero). out must not alias the inputs. */
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm_bf16, const int32_t* inv_pos,
+                         const void* y_shared_bf16, const void* residual_bf16, int32_t T,
+                         void* out_bf16, void* stream);
+
+/* The whole layer: route, permute, expert MLPs, shared experts, combine.
+ *   x_bf16 [T, H] -> out_bf16 [T, H]; residual_bf16 [T, H] or NULL;
+ *   topk_ids_out int32 [T, k] or NULL (a copy of the routing decision).
+ * No host synchronisation: expert counts and offsets never leave the device.
+ * (MoK abstract: "no CPU-GPU synchronisation".) */
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                         const moe_weights_t* weights, const void* residual_bf16, void* out_bf16,
+                         int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward with CUDA events recorded around each stage (events may be NULL). */
+moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                                  const moe_weights_t* weights, const void* residual_bf16,
+                                  void* out_bf16, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
+                                  void* stream, const moe_stage_events_t* events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,113 @@
+// Device helpers shared by the MoE kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kBlk = 128;       // FP8 scale block (weights: 128x128, activations: 1x128)
+constexpr float kE4M3Max = 448.f;
+
+// ---------------------------------------------------------------- loads
+// Streaming 16-byte load for weights that are read exactly once: bypass L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 16-byte load of data that other CTAs also read (activations): normal caching.
+__device__ __forceinline__ uint4 ld_v4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// ------------------------------------------------------------ warp helpers
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// ------------------------------------------------ activation quantisation
+// Power-of-two block scale: the smallest 2^k with amax <= 448 * 2^k. With
+// amax = m * 2^e (m in [0.5, 1)) and 448 = 0.875 * 2^9 this is k = e - 9 when
+// m <= 0.875 and k = e - 8 otherwise. amax = 0 gives scale 1. k is clamped at
+// -126 so both the scale and its inverse stay normal fp32 numbers.
+__device__ __forceinline__ float act_scale_pow2(float amax, float* inv_scale) {
+    if (!(amax > 0.f)) {
+        *inv_scale = 1.f;
+        return 1.f;
+    }
+    int e;
+    const float m = frexpf(amax, &e);
+    int k = (m <= 0.875f) ? e - 9 : e - 8;
+    k = k < -126 ? -126 : k;
+    *inv_scale = ldexpf(1.f, -k);
+    return ldexpf(1.f, k);
+}
+
+// Four fp32 values -> four E4M3 codes (round to nearest even, saturating), packed
+// little-endian in one 32-bit word (value 0 in the low byte).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// One 128-value block held by a warp, four consecutive values per lane
+// (lane l holds values 4l..4l+3): returns the packed codes of this lane and
+// writes the block scale (identical in every lane).
+__device__ __forceinline__ uint32_t warp_quant_block128(float v0, float v1, float v2, float v3,
+                                                        float* scale_out) {
+    float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+    amax = warp_max(amax);
+    float inv;
+    const float s = act_scale_pow2(amax, &inv);
+    *scale_out = s;
+    return pack_e4m3x4(v0 * inv, v1 * inv, v2 * inv, v3 * inv);
+}
+
+// ------------------------------------------------------------- FP8 MMA
+// D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col). Used as a dequantising
+// dot-product engine for weight-streaming GEMVs with up to 8 activation columns.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float((uint32_t)b << 16);
+}
+
+// ----------------------------------------------------------- status word
+// kStatusTimeout: a bounded wait gave up; kStatusBadId: an expert id outside [0, E)
+// reached the permutation (the offending item is skipped).
+enum : int { kStatusTimeout = 1, kStatusBadId = 2 };
+
+__device__ __forceinline__ void set_status(int* status, int bit) { atomicOr(status, bit); }
+
+}  // namespace moe

@@ -1,0 +1,381 @@
+// The C ABI of include/moe.h: host-side argument checks, workspace carving and
+// the launch sequence of each entry point. No entry point allocates memory or
+// synchronises the host, except moe_read_device_status (documented).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+int num_sms() {
+    static const int n = [] {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 152;
+        return v;
+    }();
+    return n;
+}
+
+static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+int router_splits_for(const moe_config_t& c, int64_t T) {
+    if (T <= kSmallT) return 1;
+    const int64_t tiles = ((T + 63) / 64) * ((c.n_routed + 63) / 64);
+    int64_t s = (304 + tiles - 1) / tiles;  // aim at two CTAs per SM of a 152-SM part
+    const int64_t hb = c.hidden / 128;
+    if (s > 8) s = 8;
+    if (s > hb) s = hb;
+    return (int)(s < 1 ? 1 : s);
+}
+
+int max_routed_groups(const moe_config_t& c, int64_t T) {
+    const int64_t n = T * c.top_k;
+    const int64_t touched = n < c.n_routed ? n : c.n_routed;
+    return (int)(n / kGroupRows + touched + 1);
+}
+
+WsLayout ws_layout(const moe_config_t& c, int64_t T) {
+    WsLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    const size_t H = c.hidden, I = c.moe_inter, E = c.n_routed, k = c.top_k;
+    const size_t Is = (size_t)c.n_shared * c.moe_inter;
+    const size_t t = (size_t)T;
+    L.router_splits = router_splits_for(c, T);
+    L.max_groups = max_routed_groups(c, T);
+    L.ctrl = take(sizeof(Ctrl));
+    L.logits = take((size_t)L.router_splits * t * E * 4);
+    L.ids = take(t * k * 4);
+    L.w = take(t * k * 4);
+    L.xq = take(t * H);
+    L.xs = take(t * (H / 128) * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm_src = take(t * k * 4);
+    L.inv_pos = take(t * k * 4);
+    L.groups = take((size_t)L.max_groups * sizeof(RowGroup));
+    L.a_routed = take(t * k * I * 4);
+    L.a_shared = take(t * Is * 4);
+    L.y_perm = take(t * k * H * 2);
+    L.y_shared = take(t * H * 2);
+    L.total = off;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
+
+moe_status_t check_cfg(const moe_config_t* c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->hidden <= 0 || c->hidden % 128 || c->hidden > 32768) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->moe_inter <= 0 || c->moe_inter % 128 || c->moe_inter > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->n_routed < 1 || c->n_routed > 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->n_group < 1 || c->n_group > 32 || c->n_routed % c->n_group) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->topk_group * (c->n_routed / c->n_group))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->n_shared < 0 || (int64_t)c->n_shared * c->moe_inter > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!std::isfinite(c->routed_scaling_factor)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+moe_status_t check_T(const moe_config_t* c, int32_t T) {
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    // flat (token, slot) indices and row offsets are int32
+    if ((int64_t)T * c->top_k > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_config_t* c, int32_t T, const void* ws, size_t ws_bytes) {
+    if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(*c, T).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w, bool need_router) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    const void* req[] = {w->w_gate, w->w_up, w->w_down, w->s_gate, w->s_up, w->s_down};
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (c->n_shared > 0) {
+        const void* sh[] = {w->ws_gate, w->ws_up, w->ws_down, w->ss_gate, w->ss_up, w->ss_down};
+        for (const void* p : sh)
+            if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    }
+    if (need_router) {
+        if (!w->w_router || !aligned16(w->w_router)) return MOE_ERR_INVALID_ARG;
+        if (w->router_bias && !aligned4(w->router_bias)) return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+#define MOE_TRY(expr)                         \
+    do {                                      \
+        const moe_status_t _s = (expr);       \
+        if (_s != MOE_OK) return _s;          \
+    } while (0)
+
+#define MOE_CUDA(expr)                                   \
+    do {                                                 \
+        if ((expr) != cudaSuccess) return MOE_ERR_CUDA;  \
+    } while (0)
+
+template <class T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+ExpertArgs expert_args(const moe_config_t* c, int32_t T, const moe_weights_t* W, const WsLayout& L, void* ws,
+                       const int32_t* perm_src, const float* topk_w, void* y_perm, void* y_shared) {
+    ExpertArgs a;
+    a.H = c->hidden;
+    a.I = c->moe_inter;
+    a.Is = c->n_shared * c->moe_inter;
+    a.T = T;
+    a.k = c->top_k;
+    a.n_shared_groups = c->n_shared > 0 ? (T + kGroupRows - 1) / kGroupRows : 0;
+    a.w_gate = W->w_gate;
+    a.w_up = W->w_up;
+    a.w_down = W->w_down;
+    a.s_gate = W->s_gate;
+    a.s_up = W->s_up;
+    a.s_down = W->s_down;
+    a.ws_gate = W->ws_gate;
+    a.ws_up = W->ws_up;
+    a.ws_down = W->ws_down;
+    a.ss_gate = W->ss_gate;
+    a.ss_up = W->ss_up;
+    a.ss_down = W->ss_down;
+    a.xq = at<uint8_t>(ws, L.xq);
+    a.xs = at<float>(ws, L.xs);
+    a.perm_src = perm_src;
+    a.topk_w = topk_w;
+    a.groups = at<RowGroup>(ws, L.groups);
+    a.ctrl = at<Ctrl>(ws, L.ctrl);
+    a.a_routed = at<float>(ws, L.a_routed);
+    a.a_shared = at<float>(ws, L.a_shared);
+    a.y_perm = static_cast<__nv_bfloat16*>(y_perm);
+    a.y_shared = static_cast<__nv_bfloat16*>(y_shared);
+    a.max_groups = L.max_groups;
+    return a;
+}
+
+struct StageMark {
+    const moe_stage_events_t* ev;
+    cudaStream_t st;
+    moe_status_t begin(moe_stage_t s) const {
+        if (ev && ev->start[s] && cudaEventRecord((cudaEvent_t)ev->start[s], st) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    moe_status_t end(moe_stage_t s) const {
+        if (ev && ev->stop[s] && cudaEventRecord((cudaEvent_t)ev->stop[s], st) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_tokens) {
+    if (check_cfg(cfg) != MOE_OK || max_tokens < 0 || check_T(cfg, max_tokens) != MOE_OK) return 0;
+    return ws_layout(*cfg, max_tokens).total;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
+    MOE_CUDA(cudaMemsetAsync(ws, 0, sizeof(Ctrl), (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status_t moe_read_device_status(void* ws, void* stream) {
+    if (!ws) return MOE_ERR_WORKSPACE;
+    int h = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    MOE_CUDA(cudaMemcpyAsync(&h, ws, sizeof(int), cudaMemcpyDeviceToHost, st));
+    MOE_CUDA(cudaStreamSynchronize(st));
+    if (h == 0) return MOE_OK;
+    MOE_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), st));
+    MOE_CUDA(cudaStreamSynchronize(st));
+    if (h & kStatusTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+    return MOE_ERR_INVALID_ARG;
+}
+
+moe_status_t moe_quant_act(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq, float* xs, void* stream) {
+    if (T < 0 || H <= 0 || H % 128) return T < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !xq || !xs || !aligned16(x_bf16) || !aligned16(xq) || !aligned16(xs)) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_quant_act(x_bf16, T, H, xq, xs, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, int32_t T, const float* w_router,
+                       const float* router_bias, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                       void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_T(cfg, T));
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !w_router || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(w_router) || !aligned16(topk_ids) || !aligned16(topk_w))
+        return MOE_ERR_INVALID_ARG;
+    if (router_bias && !aligned4(router_bias)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+    const WsLayout L = ws_layout(*cfg, T);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T <= kSmallT) {
+        MOE_CUDA(launch_route_small(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
+                                    at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), nullptr, nullptr, nullptr, nullptr,
+                                    at<Ctrl>(ws, L.ctrl), st));
+    } else {
+        MOE_CUDA(launch_route_large(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
+                                    L.router_splits, st));
+    }
+    return MOE_OK;
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32_t T, int32_t* expert_offsets,
+                         int32_t* perm_src, int32_t* inv_pos, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_T(cfg, T));
+    if (T == 0) return MOE_OK;
+    const void* req[] = {topk_ids, expert_offsets, perm_src, inv_pos};
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+    const WsLayout L = ws_layout(*cfg, T);
+    MOE_CUDA(launch_permute(*cfg, topk_ids, T, expert_offsets, perm_src, inv_pos, nullptr, at<Ctrl>(ws, L.ctrl),
+                            (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_t* weights,
+                            const int32_t* expert_offsets, const int32_t* perm_src, const float* topk_w,
+                            void* y_perm_bf16, void* y_shared_bf16, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_T(cfg, T));
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(cfg, weights, false));
+    const void* req[] = {x_bf16, expert_offsets, perm_src, topk_w, y_perm_bf16};
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared > 0 && (!y_shared_bf16 || !aligned16(y_shared_bf16))) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+    const WsLayout L = ws_layout(*cfg, T);
+    cudaStream_t st = (cudaStream_t)stream;
+    MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), st));
+    MOE_CUDA(launch_build_groups(*cfg, expert_offsets, T * cfg->top_k, at<RowGroup>(ws, L.groups), at<Ctrl>(ws, L.ctrl), st));
+    const ExpertArgs a = expert_args(cfg, T, weights, L, ws, perm_src, topk_w, y_perm_bf16, y_shared_bf16);
+    MOE_CUDA(launch_gateup_gemv(a, st));
+    MOE_CUDA(launch_down_gemv(a, st));
+    return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm_bf16, const int32_t* inv_pos,
+                         const void* y_shared_bf16, const void* residual_bf16, int32_t T, void* out_bf16,
+                         void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_T(cfg, T));
+    if (T == 0) return MOE_OK;
+    const void* req[] = {y_perm_bf16, inv_pos, out_bf16};
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if ((y_shared_bf16 && !aligned16(y_shared_bf16)) || (residual_bf16 && !aligned16(residual_bf16)))
+        return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_combine(T, cfg->hidden, cfg->top_k, static_cast<const __nv_bfloat16*>(y_perm_bf16), inv_pos,
+                            static_cast<const __nv_bfloat16*>(y_shared_bf16),
+                            static_cast<const __nv_bfloat16*>(residual_bf16), static_cast<__nv_bfloat16*>(out_bf16),
+                            (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                                  const moe_weights_t* weights, const void* residual_bf16, void* out_bf16,
+                                  int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream,
+                                  const moe_stage_events_t* events) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_T(cfg, T));
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(cfg, weights, true));
+    if (!x_bf16 || !out_bf16 || !aligned16(x_bf16) || !aligned16(out_bf16)) return MOE_ERR_INVALID_ARG;
+    if ((residual_bf16 && !aligned16(residual_bf16)) || (topk_ids_out && !aligned4(topk_ids_out)))
+        return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
+    const WsLayout L = ws_layout(*cfg, T);
+    cudaStream_t st = (cudaStream_t)stream;
+    const StageMark mark{events, st};
+    int32_t* ids = at<int32_t>(ws, L.ids);
+    float* w = at<float>(ws, L.w);
+    int32_t* perm_src = at<int32_t>(ws, L.perm_src);
+    int32_t* inv_pos = at<int32_t>(ws, L.inv_pos);
+    Ctrl* ctrl = at<Ctrl>(ws, L.ctrl);
+    RowGroup* groups = at<RowGroup>(ws, L.groups);
+
+    MOE_TRY(mark.begin(MOE_STAGE_ROUTE));
+    if (T <= kSmallT) {
+        MOE_CUDA(launch_route_small(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
+                                    at<float>(ws, L.logits), at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
+                                    at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups, ctrl, st));
+        MOE_TRY(mark.end(MOE_STAGE_ROUTE));
+    } else {
+        MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
+                                    at<float>(ws, L.logits), L.router_splits, st));
+        MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), st));
+        MOE_TRY(mark.end(MOE_STAGE_ROUTE));
+        MOE_TRY(mark.begin(MOE_STAGE_PERMUTE));
+        MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups, ctrl, st));
+        MOE_TRY(mark.end(MOE_STAGE_PERMUTE));
+    }
+    void* y_perm = at<void>(ws, L.y_perm);
+    void* y_shared = cfg->n_shared > 0 ? at<void>(ws, L.y_shared) : nullptr;
+    const ExpertArgs a = expert_args(cfg, T, weights, L, ws, perm_src, w, y_perm, y_shared);
+    MOE_TRY(mark.begin(MOE_STAGE_GATE_UP));
+    MOE_CUDA(launch_gateup_gemv(a, st));
+    MOE_TRY(mark.end(MOE_STAGE_GATE_UP));
+    MOE_TRY(mark.begin(MOE_STAGE_DOWN));
+    MOE_CUDA(launch_down_gemv(a, st));
+    MOE_TRY(mark.end(MOE_STAGE_DOWN));
+    MOE_TRY(mark.begin(MOE_STAGE_COMBINE));
+    MOE_CUDA(launch_combine(T, cfg->hidden, cfg->top_k, static_cast<const __nv_bfloat16*>(y_perm), inv_pos,
+                            static_cast<const __nv_bfloat16*>(y_shared),
+                            static_cast<const __nv_bfloat16*>(residual_bf16), static_cast<__nv_bfloat16*>(out_bf16),
+                            st));
+    MOE_TRY(mark.end(MOE_STAGE_COMBINE));
+    if (topk_ids_out)
+        MOE_CUDA(cudaMemcpyAsync(topk_ids_out, ids, (size_t)T * cfg->top_k * sizeof(int32_t),
+                                 cudaMemcpyDeviceToDevice, st));
+    return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_t* weights,
+                         const void* residual_bf16, void* out_bf16, int32_t* topk_ids_out, void* ws,
+                         size_t ws_bytes, void* stream) {
+    return moe_forward_profiled(cfg, x_bf16, T, weights, residual_bf16, out_bf16, topk_ids_out, ws, ws_bytes,
+                                stream, nullptr);
+}
+
+}  // extern "C"

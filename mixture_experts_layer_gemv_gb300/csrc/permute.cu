@@ -1,0 +1,211 @@
+// Token permutation by expert: a deterministic, stable counting sort of the
+// T*k (token, slot) pairs, done on the device so that expert counts and offsets
+// never travel to the host (MoK abstract: no CPU-GPU synchronisation; the
+// DeepSeek-V4.1 Flash lecture's "router emits the layout the experts need").
+//
+// One CTA of 32 warps: warp w owns a contiguous segment of flat indices,
+// counts its experts into a private shared-memory histogram, the histograms are
+// scanned expert-major / warp-minor, and each warp then walks its segment in
+// order, ranking equal experts inside each 32-wide chunk with __match_any_sync.
+// The same kernel emits the row-group work list of the expert GEMVs.
+#include "common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kPermWarps = 32;
+constexpr int kMaxE = 256;
+
+__device__ int scan_exclusive_warp256(int* v, int n) {
+    const int lane = threadIdx.x & 31;
+    int loc[8];
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = lane * 8 + i;
+        loc[i] = idx < n ? v[idx] : 0;
+        s += loc[i];
+    }
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int run = incl - s;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = lane * 8 + i;
+        if (idx < n) v[idx] = run;
+        run += loc[i];
+    }
+    __syncwarp();
+    return total;
+}
+
+// Write the row groups (<= kGroupRows rows of one expert each) from per-expert
+// counts in s_cnt and exclusive offsets in s_off. s_gcnt/s_goff are scratch.
+__device__ void write_groups(const int* s_cnt, const int* s_off, int* s_goff, int E, RowGroup* groups,
+                             Ctrl* ctrl) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_goff[e] = (s_cnt[e] + kGroupRows - 1) / kGroupRows;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int gtot = scan_exclusive_warp256(s_goff, E);
+        if (threadIdx.x == 0) ctrl->n_routed_groups = gtot;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int c = s_cnt[e];
+        const int ng = (c + kGroupRows - 1) / kGroupRows;
+        for (int g = 0; g < ng; ++g) {
+            RowGroup rg;
+            rg.expert = e;
+            rg.row_begin = s_off[e] + g * kGroupRows;
+            rg.nrows = min(kGroupRows, c - g * kGroupRows);
+            rg.pad = 0;
+            groups[s_goff[e] + g] = rg;
+        }
+    }
+}
+
+struct PermuteParams {
+    int E, n;
+    const int32_t* ids;
+    int32_t* offsets;
+    int32_t* perm_src;
+    int32_t* inv_pos;
+    RowGroup* groups;
+    Ctrl* ctrl;
+};
+
+__global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(PermuteParams p) {
+    __shared__ int hist[kPermWarps][kMaxE];
+    __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_goff[kMaxE];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E, n = p.n;
+    const int seg = (n + kPermWarps - 1) / kPermWarps;
+    const int f_begin = min(n, warp * seg), f_end = min(n, f_begin + seg);
+
+    for (int i = threadIdx.x; i < kPermWarps * kMaxE; i += blockDim.x) (&hist[0][0])[i] = 0;
+    __syncthreads();
+    for (int f = f_begin + lane; f < f_end; f += 32) {
+        const int e = p.ids[f];
+        if (e >= 0 && e < E)
+            atomicAdd(&hist[warp][e], 1);
+        else
+            set_status(&p.ctrl->status, kStatusBadId);
+    }
+    __syncthreads();
+    // hist[w][e] <- pairs of expert e in segments before w; s_cnt[e] <- total
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < kPermWarps; ++w) {
+            const int c = hist[w][e];
+            hist[w][e] = run;
+            run += c;
+        }
+        s_cnt[e] = run;
+        s_off[e] = run;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int tot = scan_exclusive_warp256(s_off, E);
+        if (lane == 0) s_off[E] = tot;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) p.offsets[e] = s_off[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        for (int w = 0; w < kPermWarps; ++w) hist[w][e] += s_off[e];
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int base = f_begin; base < f_end; base += 32) {
+        const int f = base + lane;
+        int e = -1;
+        if (f < f_end) {
+            e = p.ids[f];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & lt_mask);
+        if (e >= 0) {
+            const int pos = hist[warp][e] + rank;
+            p.perm_src[pos] = f;
+            p.inv_pos[f] = pos;
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) hist[warp][e] += __popc(peers);
+        __syncwarp();
+    }
+    if (p.groups) {
+        __syncthreads();
+        write_groups(s_cnt, s_off, s_goff, E, p.groups, p.ctrl);
+    }
+}
+
+struct BuildGroupsParams {
+    int E, n_rows;
+    const int32_t* offsets;
+    RowGroup* groups;
+    Ctrl* ctrl;
+};
+
+// Row groups from caller-supplied offsets. Offsets that are not a non-decreasing
+// sequence inside [0, T*k] would make the work list point outside the buffers, so
+// they are rejected on the device: the error bit is set and no work is listed.
+__global__ void __launch_bounds__(256) build_groups_kernel(BuildGroupsParams p) {
+    __shared__ int s_cnt[kMaxE], s_off[kMaxE], s_goff[kMaxE];
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+        const int a = p.offsets[e], b = p.offsets[e + 1];
+        if (a < 0 || b < a || b > p.n_rows) s_bad = 1;
+        s_off[e] = a;
+        s_cnt[e] = b - a;
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (threadIdx.x == 0) {
+            p.ctrl->n_routed_groups = 0;
+            set_status(&p.ctrl->status, kStatusBadId);
+        }
+        return;
+    }
+    write_groups(s_cnt, s_off, s_goff, p.E, p.groups, p.ctrl);
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int32_t* offsets,
+                           int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, Ctrl* ctrl,
+                           cudaStream_t st) {
+    PermuteParams p;
+    p.E = c.n_routed;
+    p.n = T * c.top_k;
+    p.ids = ids;
+    p.offsets = offsets;
+    p.perm_src = perm_src;
+    p.inv_pos = inv_pos;
+    p.groups = groups;
+    p.ctrl = ctrl;
+    permute_kernel<<<1, kPermWarps * 32, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, int n_rows, RowGroup* groups,
+                                Ctrl* ctrl, cudaStream_t st) {
+    BuildGroupsParams p;
+    p.E = c.n_routed;
+    p.n_rows = n_rows;
+    p.offsets = offsets;
+    p.groups = groups;
+    p.ctrl = ctrl;
+    build_groups_kernel<<<1, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
