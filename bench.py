@@ -95,6 +95,15 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def wait_first_sample(self, timeout_s: float = 10.0):
+        """Block until nvidia-smi has written its first sample (its start-up takes a moment)."""
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < timeout_s:
+            self.f.flush()
+            if os.path.getsize(self.f.name) > 0:
+                break
+            time.sleep(0.02)
+
     def __exit__(self, *a):
         if self.proc is not None:
             self.proc.terminate()
@@ -150,12 +159,15 @@ def _launches_per_step(T: int) -> int:
 
 
 def run_ours(args, dist, rank, world):
+    import ctypes
+
     from mixture_experts_layer_gemv_gb300 import binding as B
     from mixture_experts_layer_gemv_gb300 import build as lib_build
 
     if rank == 0 or not os.path.exists(lib_build.LIB):
         lib_build.build()
     _barrier(dist)
+    lib = B.lib()
     dev = torch.device("cuda", torch.cuda.current_device())
     wl = WORKLOADS[args.workload]
     cfg, T = wl.cfg, wl.T
@@ -170,6 +182,24 @@ def run_ours(args, dist, rank, world):
     out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=dev)
     ids = torch.empty((T, cfg.top_k), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
+    st = stream.cuda_stream
+
+    # argument structs built once: the timed loop is one C call per step
+    cstruct = B.config_struct(cfg)
+    wstructs = [B.weights_struct(Wl) for Wl in layers]
+    c_ref = ctypes.byref(cstruct)
+    w_refs = [ctypes.byref(w) for w in wstructs]
+    x_ptrs = [x.data_ptr() for x in xs]
+    out_p, ws_p, ws_n = out.data_ptr(), ws.data_ptr(), ws.numel()
+
+    def step(i, ev=None):
+        if ev is None:
+            r = lib.moe_forward(c_ref, x_ptrs[i % P], T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st)
+        else:
+            r = lib.moe_forward_profiled(c_ref, x_ptrs[i % P], T, w_refs[i % R], None, out_p, None, ws_p, ws_n,
+                                         st, ctypes.byref(ev))
+        if r != 0:
+            raise B.MoeError("moe_forward", r, B.status_string(r))
 
     # touched experts per step (for the roofline numerator): from the routing itself
     touched = []
@@ -178,49 +208,69 @@ def run_ours(args, dist, rank, world):
         touched.append(int(torch.unique(ids).numel()))
     torch.cuda.synchronize()
 
-    ev_gu = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in ev_gu:
-        a.record()
-        b.record()
+    # per-stage CUDA events on every `stride`-th timed step
+    stride = max(1, args.steps // 256)
+    n_prof = (args.steps + stride - 1) // stride
+    prof = []
+    for _ in range(n_prof):
+        evs = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in B.STAGES}
+        for a, b in evs.values():
+            a.record()
+            b.record()
+        s_ev = B.moe_stage_events_t()
+        for j, n in enumerate(B.STAGES):
+            s_ev.start[j] = evs[n][0].cuda_event
+            s_ev.stop[j] = evs[n][1].cuda_event
+        prof.append((evs, s_ev))
     torch.cuda.synchronize()
 
-    for i in range(args.warmup):
-        B.moe_forward(cfg, xs[i % P], layers[i % R], out, ws=ws)
-    torch.cuda.synchronize()
-    _barrier(dist)
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
+        clk.wait_first_sample()
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        _barrier(dist)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for i in range(args.steps):
-            B.moe_forward(cfg, xs[i % P], layers[i % R], out, ws=ws, events={"gate_up": ev_gu[i]})
+            step(i, prof[i // stride][1] if i % stride == 0 else None)
         t1.record()
         torch.cuda.synchronize()
     _barrier(dist)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / args.steps
-    ms = _max_over_ranks(dist, ms)
-    gu_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_gu)
+    ms = _max_over_ranks(dist, t0.elapsed_time(t1) / args.steps)
+    stage_us = {}
+    for n in B.STAGES:
+        v = [evs[n][0].elapsed_time(evs[n][1]) * 1e3 for evs, _ in prof]
+        if max(v) > 0:
+            stage_us[n] = round(statistics.mean(v), 3)
+    gu_ms = stage_us["gate_up"] / 1e3
     status = B.moe_read_device_status(ws)
 
     # end to end through the C ABI with host buffers: pinned x in, out back, every step
     xh = [x.cpu().pin_memory() for x in xs]
     oh = torch.empty((T, cfg.hidden), dtype=torch.bfloat16).pin_memory()
     xd = torch.empty_like(xs[0])
-    for i in range(args.warmup):
+    xd_p = xd.data_ptr()
+
+    def e2e_step(i):
         xd.copy_(xh[i % P], non_blocking=True)
-        B.moe_forward(cfg, xd, layers[i % R], out, ws=ws)
+        r = lib.moe_forward(c_ref, xd_p, T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st)
+        if r != 0:
+            raise B.MoeError("moe_forward", r, B.status_string(r))
         oh.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     _barrier(dist)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(args.steps):
-        xd.copy_(xh[i % P], non_blocking=True)
-        B.moe_forward(cfg, xd, layers[i % R], out, ws=ws)
-        oh.copy_(out, non_blocking=True)
+        e2e_step(i)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / args.steps)
@@ -237,6 +287,7 @@ def run_ours(args, dist, rank, world):
         "achieved": achieved, "peak": peak_gbs, "peak_src": "measured" if peaks else "fallback",
         "layer_bytes": layer_bytes, "tokens_per_s": tokens_per_s, "clocks": clk.summary(), "status": status,
         "replicas": R, "n_touched": n_touched, "launches": _launches_per_step(T) * args.steps, "weights": W0,
+        "stage_us": stage_us, "prof_steps": n_prof,
     }
 
 
@@ -270,7 +321,7 @@ def cpu_oracle_rate(wl, budget_s: float, weights=None):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (default: ~1 s of work)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="dsv2_decode_t1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -284,6 +335,8 @@ def main():
     dist, rank, world = _dist()
     wl = WORKLOADS[args.workload]
     cfg, T = wl.cfg, wl.T
+    if args.steps <= 0:
+        args.steps = {1: 20000, 8: 20000, 64: 2000}.get(T, 200)
     t1_metric = T <= 64
     metric = "MoE layer µs at T=1 (% HBM roofline); tokens/s at T=4096 (% FP8 TC peak)"
     config = {"workload": f"{wl.name}: {wl.description}", "T": T, "hidden": cfg.hidden,
@@ -334,6 +387,7 @@ def main():
                      "launch_us": round(r["gu_ms"] * 1e3, 3), "bytes_per_launch": r["gu_bytes"]},
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": T * cfg.hidden * 2,
                 "d2h_bytes_per_step": T * cfg.hidden * 2},
+        "stages_us": r["stage_us"], "stage_events_on_steps": r["prof_steps"],
         "gpu_launches": r["launches"], "clocks": r["clocks"], "device_status": r["status"],
     }
     if not args.no_cpu_baseline:
