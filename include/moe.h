@@ -128,6 +128,22 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, int32_t T,
                        const float* w_router, const float* router_bias, int32_t* topk_ids,
                        float* topk_w, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_route without a workspace, for callers that cannot allocate device memory:
+ * a framework that owns the whole device memory pool and forbids cudaMalloc while it
+ * serves (cudaMalloc can synchronise the device and stall other streams), or a plugin
+ * inside one with no allocator hook. The pages have no counterpart of this call; it
+ * computes exactly what moe_route computes, with the same arguments minus ws.
+ * Its scratch is one fixed device array of 606,464 bytes inside the library, held by
+ * every GPU that loads it until the process exits; it covers T <= 64, n_routed <= 256
+ * and hidden <= 8192, and larger sizes return MOE_ERR_UNSUPPORTED_SHAPE.
+ * The first call on a device looks up that array's device address (once per device,
+ * with the device current); make that first call before any stream capture.
+ * Every call shares the array: calls whose work overlaps on the GPU (other streams,
+ * other host threads) race and may return wrong results; serialise them. */
+moe_status_t moe_route_noalloc(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                               const float* w_router, const float* router_bias, int32_t* topk_ids,
+                               float* topk_w, void* stream);
+
 /* Token permutation by expert: a stable counting sort of the T*k (token, slot) pairs.
  * Pair (t, j) has flat index f = t*k + j.
  *   expert_offsets int32 [E+1]: pairs routed to experts < e (exclusive prefix sum)

@@ -57,6 +57,7 @@ _SIGNATURES = {
     "moe_read_device_status": (ctypes.c_int, [_P, _P]),
     "moe_quant_act": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "moe_route": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_route_noalloc": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_ffn": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P]),
@@ -150,6 +151,16 @@ def moe_route(cfg, x, w_router, router_bias, topk_ids, topk_w, ws, stream=None) 
     c = config_struct(cfg)
     _check("moe_route", lib().moe_route(ctypes.byref(c), _ptr(x), x.shape[0], _ptr(w_router), _ptr(router_bias),
                                         _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_route_noalloc(cfg, x, w_router, router_bias, topk_ids, topk_w, stream=None) -> None:
+    """moe_route for callers that cannot allocate: no workspace argument; the library's
+    fixed internal scratch (T <= 64, n_routed <= 256, hidden <= 8192) is used instead.
+    Calls that overlap on the GPU share that scratch and must be serialised."""
+    c = config_struct(cfg)
+    _check("moe_route_noalloc", lib().moe_route_noalloc(ctypes.byref(c), _ptr(x), x.shape[0], _ptr(w_router),
+                                                        _ptr(router_bias), _ptr(topk_ids), _ptr(topk_w),
+                                                        _stream(stream)))
 
 
 def moe_permute(cfg, topk_ids, expert_offsets, perm_src, inv_pos, ws, stream=None) -> None:
