@@ -153,9 +153,9 @@ def _algorithmic_layer_bytes(cfg, n_experts_touched: int, T: int) -> int:
 
 
 def _launches_per_step(T: int) -> int:
-    # small T: fused route, gate/up, down, combine; large T: router GEMM, top-k,
+    # small T: fused route, gate/up, down with the combine fused in; large T: router GEMM, top-k,
     # activation quant, permutation, gate/up, down, combine
-    return 4 if T <= 64 else 7
+    return 3 if T <= 64 else 7
 
 
 def run_ours(args, dist, rank, world):
@@ -242,7 +242,8 @@ def run_ours(args, dist, rank, world):
     torch.cuda.synchronize()
     ms = _max_over_ranks(dist, t0.elapsed_time(t1) / args.steps)
     stage_us = {}
-    for n in B.STAGES:
+    recorded = ("route", "gate_up", "down") if T <= 64 else B.STAGES  # small T: permutation and combine are fused
+    for n in recorded:
         v = [evs[n][0].elapsed_time(evs[n][1]) * 1e3 for evs, _ in prof]
         if max(v) > 0:
             stage_us[n] = round(statistics.mean(v), 3)

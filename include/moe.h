@@ -94,12 +94,13 @@ typedef struct moe_stage_events {
 const char* moe_status_string(moe_status_t status);
 
 /* Bytes of device workspace every entry point below needs for up to max_tokens tokens
- * (0 if the config is invalid). Workspace contents need no initialisation except its
- * first 256 bytes (control words), which moe_workspace_init zeroes; the library returns
- * them to zero at the end of every call, so one init after allocation suffices. */
+ * (0 if the config is invalid). Workspace contents need no initialisation except the
+ * control region at its start (status word and hand-off counters), which
+ * moe_workspace_init zeroes; the library returns the counters to zero by the end of
+ * every call, so one init after allocation suffices. */
 size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_tokens);
 
-/* Zero the control words at the start of ws (asynchronous memset on stream). */
+/* Zero the control region at the start of ws (asynchronous memset on stream). */
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Device-side error word of ws: copies it to the host (synchronising `stream`), clears

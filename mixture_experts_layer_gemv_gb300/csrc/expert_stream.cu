@@ -1,0 +1,603 @@
+// Stages P1/P2 and Q1/Q2 of the DeepSeek-V2 MoE layer ("DSV2-236B-MegaKernel",
+// README stage flowchart, MoE subgraph) in the weight-streaming regime, where each
+// expert sees at most a few tokens and every FP8 weight byte is used by at most 8
+// activation rows: bound by HBM bandwidth ("decode is a GEMV", the DeepSeek-V4.1
+// Flash Kernel Journey lecture, "Skill 5").
+//
+// Work decomposition (stream-K). A tile is 128 output rows of one matrix (gate and up
+// together for P1/Q1) for one row group of <= 8 activation rows; a unit is one tile
+// times one 128-wide K block (one FP8 scale block). All units of a stage are laid out
+// in one sequence and every CTA (one per SM) takes an equal contiguous range of it, so
+// every SM streams the same number of bytes whatever the routing.
+//
+// No CTA waits for another. The K range of every output row block is split into P
+// parts, P just large enough that no part (a tile) is longer than a CTA's range, so a
+// tile has at most two contributors. Partial sums go to two dense fp32 buffers with
+// the layout of the output: the CTA holding a tile's first unit stores into A (and, if
+// it also holds the last unit, zeros into B); when the tile is cut by a range boundary
+// the next CTA stores the rest into B. A reader adds A + B over the P parts in a fixed
+// order: deterministic, with no fence, atomic, spin, counter or zero-initialisation.
+//
+// Data movement. One producer thread streams weight boxes of 128 rows x 128 bytes with
+// 2-D TMA (128-byte swizzle) into a ring of shared-memory stages guarded by mbarriers;
+// eight consumer warps each own 16 rows of the tile and run mma.m16n8k32
+// (E4M3 x E4M3 -> fp32) as a dequantising dot-product engine. Block scales are applied
+// once per unit: acc += partial * s_w[rowblock][kblock] * s_x[token][kblock].
+//
+// The down kernel builds its FP8 operand itself: for each row group it sums the gate/up
+// tiles, forms a = SiLU(g) * u and quantises every 128 values (one gate/up tile, one
+// down K block) to E4M3 with a power-of-two scale, in shared memory, while its producer
+// is already streaming down weights (which depend only on the routing).
+//
+// Launch chaining. The kernels are launched with programmatic stream serialisation.
+// The gate/up kernel prefetches the shared experts' weights (independent of the
+// routing) into L2 before it waits for the router.
+#include "stream_common.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace stream;
+
+__device__ __forceinline__ TileSpace gateup_space(const StreamArgs& a, int P) {
+    return TileSpace{a.ctrl->n_routed_groups * (a.I / kTile), a.H / kBlk, a.n_shared_groups * (a.Is / kTile),
+                     a.H / kBlk, P};
+}
+__device__ __forceinline__ Plan gateup_plan(const StreamArgs& a) {
+    const TileSpace t = gateup_space(a, 1);
+    return make_plan(t.n_r, t.kc_r, t.n_s, t.kc_s, a.grid_gu, a.max_parts);
+}
+__device__ __forceinline__ TileSpace down_space(const StreamArgs& a, int P) {
+    const int slices = a.H / kTile;
+    return TileSpace{a.ctrl->n_routed_groups * slices, a.I / kBlk, a.n_shared_groups * slices, a.Is / kBlk, P};
+}
+__device__ __forceinline__ Plan down_plan(const StreamArgs& a) {
+    const TileSpace t = down_space(a, 1);
+    return make_plan(t.n_r, t.kc_r, t.n_s, t.kc_s, a.grid_d, a.max_parts);
+}
+
+// ================================================================== gate / up
+__global__ void __launch_bounds__(kThreads, 1)
+    gateup_stream_kernel(const StreamArgs a, const __grid_constant__ TmaMap tm_g, const __grid_constant__ TmaMap tm_u,
+                         const __grid_constant__ TmaMap tm_sg, const __grid_constant__ TmaMap tm_su) {
+    extern __shared__ uint8_t smem_raw[];
+    constexpr int S = kStagesGU;
+    constexpr int SB = 2 * kBox + kBRows;
+    uint8_t* smem = align1024(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
+    uint64_t* empty = full + S;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int H = a.H, Hb = H / kBlk;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCons);
+        }
+        fence_mbar_init();
+    }
+    for (int s = 0; s < S; ++s)  // activation rows beyond a group's size are read but masked
+        for (int i = tid; i < kBRows / 16; i += kThreads)
+            reinterpret_cast<uint4*>(smem + s * SB + 2 * kBox)[i] = make_uint4(0, 0, 0, 0);
+    if (warp == kCons && lane == 0) {
+        prefetch_tmap(&tm_g);
+        prefetch_tmap(&tm_u);
+        if (a.Is > 0) {
+            prefetch_tmap(&tm_sg);
+            prefetch_tmap(&tm_su);
+            // the shared experts' gate/up weights do not depend on the routing:
+            // pull this CTA's slice of them into L2 while the router runs
+            const size_t bytes = (size_t)a.Is * H;
+            const size_t per = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~size_t(15);
+            const size_t lo = std::min(bytes, per * blockIdx.x), hi = std::min(bytes, lo + per);
+            for (size_t o = lo; o < hi; o += 65536) {
+                const uint32_t n = (uint32_t)std::min<size_t>(65536, hi - o);
+                bulk_prefetch_l2(a.ws_gate + o, n);
+                bulk_prefetch_l2(a.ws_up + o, n);
+            }
+        }
+    }
+    __syncthreads();
+    pdl_wait();  // routing, activation codes and the work list are complete
+    pdl_launch_dependents();
+
+    const int slices_r = a.I / kTile, slices_s = a.Is / kTile;
+    const Plan pl = gateup_plan(a);
+    const TileSpace ts = gateup_space(a, pl.P);
+    const Range rg = make_range(ts, pl.nb, blockIdx.x);
+    if (blockIdx.x >= pl.nb || rg.u1 <= rg.u0) return;
+    const Partials pt{{a.g_r, a.u_r}, {a.gb_r, a.ub_r}, (long)a.T * a.k, a.I};
+    const Partials pts{{a.g_s, a.u_s}, {a.gb_s, a.ub_s}, (long)a.T, a.Is};
+
+    if (warp == kCons) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        long cur = -1;
+        TileInfo ti{};
+        const uint8_t* xrow[kGroupRows];
+        long t = rg.first_tile;
+        int kb = rg.kb0;
+        int left = (int)(ts.start(t) + ts.len(t) - rg.u0);  // units left in the current tile
+        int s = 0, ph = 0;
+        for (long u = rg.u0; u < rg.u1; ++u) {
+            if (u - rg.u0 >= S && !mbar_wait_bounded(&empty[s], ph ^ 1, kWaitPolls)) {
+                set_status(a.status, kStatusTimeout);
+                break;
+            }
+            if (t != cur) {
+                cur = t;
+                ti = decode_tile(ts, t, slices_r, slices_s, a.groups, a.T);
+                for (int c = 0; c < kGroupRows; ++c) {
+                    int tok = -1;
+                    if (c < ti.nrows) {
+                        if (ti.shared) {
+                            tok = ti.row_begin + c;
+                        } else {
+                            const int f = a.perm_src[ti.row_begin + c];
+                            tok = ((unsigned)f < (unsigned)(a.T * a.k)) ? f / a.k : -1;
+                        }
+                    }
+                    xrow[c] = tok >= 0 ? a.xq + (size_t)tok * H : nullptr;
+                }
+            }
+            uint8_t* st = smem + s * SB;
+            int nrow = 0;
+            for (int c = 0; c < ti.nrows; ++c) nrow += xrow[c] != nullptr;
+            mbar_arrive_expect_tx(&full[s], 2 * kBox + nrow * kBlk);
+            const int y = ti.shared ? ti.slice * kTile : ti.expert * a.I + ti.slice * kTile;
+            tma_load_2d(st, ti.shared ? (const void*)&tm_sg : (const void*)&tm_g, kb * kBlk, y, &full[s]);
+            tma_load_2d(st + kBox, ti.shared ? (const void*)&tm_su : (const void*)&tm_u, kb * kBlk, y, &full[s]);
+            for (int c = 0; c < ti.nrows; ++c)
+                if (xrow[c]) bulk_load(st + 2 * kBox + c * kBlk, xrow[c] + kb * kBlk, kBlk, &full[s]);
+            ++kb;
+            if (--left == 0) {
+                ++t;
+                if (u + 1 < rg.u1) {
+                    left = ts.len(t);
+                    const long stt = ts.start(t);
+                    int kbn;
+                    ts.tile_of(stt, &kbn);
+                    kb = kbn;
+                }
+            }
+            if (++s == S) {
+                s = 0;
+                ph ^= 1;
+            }
+        }
+        return;  // the consumers wait for every copy issued here before the CTA exits
+    }
+
+    // ---------------------------------------------------------------- consumers
+    float acc[2][4] = {};
+    long cur = -1;
+    TileInfo ti{};
+    const float *sgr = nullptr, *sur = nullptr, *xs0 = nullptr, *xs1 = nullptr;
+    bool failed = false;
+    long t = rg.first_tile;
+    int kb = rg.kb0;
+    int left = (int)(ts.start(t) + ts.len(t) - rg.u0);
+    int s = 0, ph = 0;
+    for (long u = rg.u0; u < rg.u1; ++u) {
+        if (t != cur) {
+            cur = t;
+            ti = decode_tile(ts, t, slices_r, slices_s, a.groups, a.T);
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[m][j] = 0.f;
+            if (ti.shared) {
+                sgr = a.ss_gate + (size_t)ti.slice * Hb;
+                sur = a.ss_up + (size_t)ti.slice * Hb;
+            } else {
+                const size_t e = (size_t)ti.expert;
+                sgr = a.s_gate + (e * (a.I / kBlk) + ti.slice) * Hb;
+                sur = a.s_up + (e * (a.I / kBlk) + ti.slice) * Hb;
+            }
+            int tok[2] = {-1, -1};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int c = 2 * t4 + q;
+                if (c < ti.nrows) {
+                    if (ti.shared) {
+                        tok[q] = ti.row_begin + c;
+                    } else {
+                        const int f = a.perm_src[ti.row_begin + c];
+                        tok[q] = ((unsigned)f < (unsigned)(a.T * a.k)) ? f / a.k : -1;
+                    }
+                }
+            }
+            xs0 = tok[0] >= 0 ? a.xs + (size_t)tok[0] * Hb : nullptr;
+            xs1 = tok[1] >= 0 ? a.xs + (size_t)tok[1] * Hb : nullptr;
+        }
+        const float swg = __ldg(sgr + kb), swu = __ldg(sur + kb);
+        const float sx0 = xs0 ? __ldg(xs0 + kb) : 0.f;
+        const float sx1 = xs1 ? __ldg(xs1 + kb) : 0.f;
+        // after a timed-out wait this warp keeps walking the units (so its control flow
+        // matches its siblings') but waits for and computes nothing more
+        if (!failed && !mbar_wait_bounded(&full[s], ph, kWaitPolls)) {
+            set_status(a.status, kStatusTimeout);
+            failed = true;
+        }
+        const uint8_t* st = smem + s * SB;
+        float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!failed) {
+            box_dot(cg, st, st + 2 * kBox + g * kBlk, warp, g, t4);
+            box_dot(cu, st + kBox, st + 2 * kBox + g * kBlk, warp, g, t4);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        acc[0][0] = fmaf(cg[0], swg * sx0, acc[0][0]);
+        acc[0][1] = fmaf(cg[1], swg * sx1, acc[0][1]);
+        acc[0][2] = fmaf(cg[2], swg * sx0, acc[0][2]);
+        acc[0][3] = fmaf(cg[3], swg * sx1, acc[0][3]);
+        acc[1][0] = fmaf(cu[0], swu * sx0, acc[1][0]);
+        acc[1][1] = fmaf(cu[1], swu * sx1, acc[1][1]);
+        acc[1][2] = fmaf(cu[2], swu * sx0, acc[1][2]);
+        acc[1][3] = fmaf(cu[3], swu * sx1, acc[1][3]);
+        ++kb;
+        if (--left == 0 || u + 1 == rg.u1) {  // end of this CTA's share of tile t
+            if (!failed) store_tile<2>(acc, ts, rg, t, ti, ti.shared ? pts : pt);
+            if (left == 0 && u + 1 < rg.u1) {
+                ++t;
+                left = ts.len(t);
+                int kbn;
+                ts.tile_of(ts.start(t), &kbn);
+                kb = kbn;
+            }
+        }
+        if (++s == S) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+}
+
+// ======================================================================= down
+__global__ void __launch_bounds__(kThreads, 1)
+    down_stream_kernel(const StreamArgs a, const __grid_constant__ TmaMap tm_d, const __grid_constant__ TmaMap tm_sd) {
+    extern __shared__ uint8_t smem_raw[];
+    const int S = a.stages_d;
+    constexpr int SB = kBox;
+    uint8_t* smem = align1024(smem_raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
+    uint64_t* empty = full + S;
+    const int Nmax = max(a.I, a.Is);
+    uint8_t* s_hq = reinterpret_cast<uint8_t*>(empty + S);               // [8][Nmax] FP8 operand
+    float* s_hs = reinterpret_cast<float*>(s_hq + kGroupRows * Nmax);    // [8][Nmax/128] its scales
+    __shared__ float s_w[kGroupRows];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int H = a.H, Ib = a.I / kBlk, Isb = a.Is / kBlk;
+    const int slices = H / kTile;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCons);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // The work list comes from the router, which completed before the gate/up kernel
+    // (this kernel's predecessor) got past its own wait; down weights depend on nothing
+    // else, so the producer streams them before the gate/up results exist.
+    const Plan pl = down_plan(a);
+    const TileSpace ts = down_space(a, pl.P);
+    const Range rg = make_range(ts, pl.nb, blockIdx.x);
+    const bool active = blockIdx.x < pl.nb && rg.u1 > rg.u0;
+
+    if (warp == kCons) {
+        if (lane == 0 && active) {
+            prefetch_tmap(&tm_d);
+            if (a.Is > 0) prefetch_tmap(&tm_sd);
+            long cur = -1;
+            TileInfo ti{};
+            long t = rg.first_tile;
+            int kb = rg.kb0;
+            int left = (int)(ts.start(t) + ts.len(t) - rg.u0);
+            int s = 0, ph = 0;
+            for (long u = rg.u0; u < rg.u1; ++u) {
+                if (u - rg.u0 >= S && !mbar_wait_bounded(&empty[s], ph ^ 1, kWaitPolls)) {
+                    set_status(a.status, kStatusTimeout);
+                    break;
+                }
+                if (t != cur) {
+                    cur = t;
+                    ti = decode_tile(ts, t, slices, slices, a.groups, a.T);
+                }
+                mbar_arrive_expect_tx(&full[s], kBox);
+                const int y = ti.shared ? ti.slice * kTile : ti.expert * H + ti.slice * kTile;
+                tma_load_2d(smem + s * SB, ti.shared ? (const void*)&tm_sd : (const void*)&tm_d, kb * kBlk, y,
+                            &full[s]);
+                ++kb;
+                if (--left == 0 && u + 1 < rg.u1) {
+                    ++t;
+                    left = ts.len(t);
+                    int kbn;
+                    ts.tile_of(ts.start(t), &kbn);
+                    kb = kbn;
+                }
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+        pdl_wait();
+        pdl_launch_dependents();
+        return;
+    }
+
+    pdl_wait();  // the gate/up tiles are complete
+    pdl_launch_dependents();
+    if (!active) return;
+
+    const Plan pl_gu = gateup_plan(a);
+    const Partials gu_r{{a.g_r, a.u_r}, {a.gb_r, a.ub_r}, (long)a.T * a.k, a.I};
+    const Partials gu_s{{a.g_s, a.u_s}, {a.gb_s, a.ub_s}, (long)a.T, a.Is};
+    const Partials pt{{a.y_r, nullptr}, {a.yb_r, nullptr}, (long)a.T * a.k, H};
+    const Partials pts{{a.y_s, nullptr}, {a.yb_s, nullptr}, (long)a.T, H};
+    float acc[1][4] = {};
+    long cur = -1;
+    // routed group index, or -1 - shared group index; INT_MIN: no operand built yet
+    int cur_group = INT_MIN;
+    TileInfo ti{};
+    const float* swr = nullptr;
+    bool failed = false;
+
+    // FP8 operand of one row group: a = SiLU(g) * u from the gate/up tiles, quantised
+    // per 128 values (one gate/up slice = one down K block)
+    auto build_operand = [&](const TileInfo& q) {
+        const int N = q.shared ? a.Is : a.I;
+        const int Nb = N / kBlk;
+        const Partials& src = q.shared ? gu_s : gu_r;
+        for (int task = warp; task < q.nrows * Nb; task += kCons) {
+            const int col = task / Nb, kbq = task % Nb;
+            const long orow = q.row_begin + col;
+            const float4 gv = read4(src, pl_gu.P, 0, orow, kbq * kTile + 4 * lane);
+            const float4 uv = read4(src, pl_gu.P, 1, orow, kbq * kTile + 4 * lane);
+            float sc;
+            const uint32_t code = warp_quant_block128(silu_mul(gv.x, uv.x), silu_mul(gv.y, uv.y), silu_mul(gv.z, uv.z),
+                                                      silu_mul(gv.w, uv.w), &sc);
+            reinterpret_cast<uint32_t*>(s_hq + col * Nmax + kbq * kBlk)[lane] = code;
+            if (lane == 0) s_hs[col * (Nmax / kBlk) + kbq] = sc;
+        }
+        if (tid < kGroupRows) {
+            float wc = 0.f;
+            if (tid < q.nrows) {
+                if (q.shared) {
+                    wc = 1.f;
+                } else {
+                    const int f = a.perm_src[q.row_begin + tid];
+                    wc = ((unsigned)f < (unsigned)(a.T * a.k)) ? a.topk_w[f] : 0.f;
+                }
+            }
+            s_w[tid] = wc;
+        }
+        named_bar(1, kConsThreads);
+    };
+
+    long t = rg.first_tile;
+    int kb = rg.kb0;
+    int left = (int)(ts.start(t) + ts.len(t) - rg.u0);
+    int s = 0, ph = 0;
+    for (long u = rg.u0; u < rg.u1; ++u) {
+        if (t != cur) {
+            cur = t;
+            ti = decode_tile(ts, t, slices, slices, a.groups, a.T);
+            const int grp = ti.shared ? -1 - ti.row_begin / kGroupRows : ti.group;
+            if (grp != cur_group) {
+                named_bar(1, kConsThreads);  // every warp is done with the previous operand
+                build_operand(ti);
+                cur_group = grp;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[0][j] = 0.f;
+            swr = ti.shared ? a.ss_down + (size_t)ti.slice * Isb
+                            : a.s_down + ((size_t)ti.expert * slices + ti.slice) * Ib;
+        }
+        const float sw = __ldg(swr + kb);
+        const int nsb = Nmax / kBlk;
+        const float sx0 = s_hs[(2 * t4) * nsb + kb];
+        const float sx1 = s_hs[(2 * t4 + 1) * nsb + kb];
+        if (!failed && !mbar_wait_bounded(&full[s], ph, kWaitPolls)) {
+            set_status(a.status, kStatusTimeout);
+            failed = true;  // keep walking the units so every named barrier is still reached
+        }
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!failed) {
+            box_dot(c, smem + s * SB, s_hq + g * Nmax + kb * kBlk, warp, g, t4);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        const bool v0 = 2 * t4 < ti.nrows, v1 = 2 * t4 + 1 < ti.nrows;
+        acc[0][0] = fmaf(c[0], v0 ? sw * sx0 : 0.f, acc[0][0]);
+        acc[0][1] = fmaf(c[1], v1 ? sw * sx1 : 0.f, acc[0][1]);
+        acc[0][2] = fmaf(c[2], v0 ? sw * sx0 : 0.f, acc[0][2]);
+        acc[0][3] = fmaf(c[3], v1 ? sw * sx1 : 0.f, acc[0][3]);
+        ++kb;
+        if (--left == 0 || u + 1 == rg.u1) {
+            if (!failed) {
+                float vals[1][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vals[0][i] = acc[0][i] * s_w[2 * t4 + (i & 1)];
+                store_tile<1>(vals, ts, rg, t, ti, ti.shared ? pts : pt);
+            }
+            if (left == 0 && u + 1 < rg.u1) {
+                ++t;
+                left = ts.len(t);
+                int kbn;
+                ts.tile_of(ts.start(t), &kbn);
+                kb = kbn;
+            }
+        }
+        if (++s == S) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+}
+
+// ==================================================================== combine
+// out[t] = sum_j y(row inv_pos[t*k+j]) + y_shared(t) (+ residual[t]), fp32, one bf16
+// rounding; or, for the stage API, the bf16 expert rows y_perm / y_shared themselves.
+// Each thread owns 4 consecutive hidden channels of one token (or one row).
+__global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a) {
+    pdl_wait();  // the down tiles are complete
+    pdl_launch_dependents();
+    const int H = a.H;
+    const Plan pl = down_plan(a);
+    const int H4 = H / 4;
+    const int Tk = a.T * a.k;
+    const Partials pt{{a.y_r, nullptr}, {a.yb_r, nullptr}, (long)Tk, H};
+    const Partials pts{{a.y_s, nullptr}, {a.yb_s, nullptr}, (long)a.T, H};
+    // the down output of permuted row r (routed) or token tok (shared), channels h..h+3
+    auto routed4 = [&](int r, int h) -> float4 { return read4(pt, pl.P, 0, r, h); };
+    auto shared4 = [&](int tok, int h) -> float4 { return read4(pts, pl.P, 0, tok, h); };
+    auto store4 = [](__nv_bfloat16* dst, float4 v) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(dst) = o;
+    };
+
+    if (a.fuse_combine) {
+        const long n = (long)a.T * H4;
+        for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+            const int tok = (int)(i / H4), h = (int)(i % H4) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < a.k; ++j) {
+                const int r = a.inv_pos[tok * a.k + j];
+                if ((unsigned)r >= (unsigned)Tk) continue;
+                const float4 y = routed4(r, h);
+                v.x += y.x;
+                v.y += y.y;
+                v.z += y.z;
+                v.w += y.w;
+            }
+            if (a.n_shared_groups > 0) {
+                const float4 y = shared4(tok, h);
+                v.x += y.x;
+                v.y += y.y;
+                v.z += y.z;
+                v.w += y.w;
+            }
+            if (a.residual) {
+                const uint2 rr = *reinterpret_cast<const uint2*>(a.residual + (size_t)tok * H + h);
+                v.x += __uint_as_float(rr.x << 16);
+                v.y += __uint_as_float(rr.x & 0xFFFF0000u);
+                v.z += __uint_as_float(rr.y << 16);
+                v.w += __uint_as_float(rr.y & 0xFFFF0000u);
+            }
+            store4(a.out + (size_t)tok * H + h, v);
+        }
+    } else {
+        const long nr = (long)Tk * H4, ns = a.n_shared_groups > 0 ? (long)a.T * H4 : 0;
+        for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nr + ns; i += (long)gridDim.x * blockDim.x) {
+            if (i < nr) {
+                const int r = (int)(i / H4), h = (int)(i % H4) * 4;
+                store4(a.y_perm + (size_t)r * H + h, routed4(r, h));
+            } else {
+                const long j = i - nr;
+                const int tok = (int)(j / H4), h = (int)(j % H4) * 4;
+                store4(a.y_shared + (size_t)tok * H + h, shared4(tok, h));
+            }
+        }
+    }
+}
+
+size_t smem_gateup() { return (size_t)kStagesGU * (2 * kBox + kBRows) + 2 * kStagesGU * 8 + 1024; }
+// Down-kernel ring depth: as many 16 KB stages (up to 10) as fit beside the FP8 operand.
+int stages_down(int Nmax) {
+    const long operand = (long)kGroupRows * Nmax + (long)kGroupRows * (Nmax / kBlk) * 4;
+    const long room = 227L * 1024 - 1024 - operand;
+    return (int)std::max<long>(2, std::min<long>(kMaxStagesD, room / (kBox + 16)));
+}
+size_t smem_down(int Nmax) {
+    const int S = stages_down(Nmax);
+    return (size_t)S * kBox + 2 * S * 8 + (size_t)kGroupRows * Nmax + (size_t)kGroupRows * (Nmax / kBlk) * 4 + 1024;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+cudaError_t set_smem(const void* fn, size_t bytes, size_t* done) {
+    if (*done >= bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) *done = bytes;
+    return e;
+}
+
+}  // namespace
+
+int stream_grid() { return std::min(num_sms(), kMaxStreamCtas); }
+
+int down_stages(int I, int Is) { return stages_down(std::max(I, Is)); }
+
+int stream_max_parts(const moe_config_t& c, int64_t T) {
+    // fewest units either streaming stage can have for T tokens, spread over the most
+    // CTAs the kernels may use: the longest part must still fit in a range
+    const int64_t Hb = c.hidden / kBlk, Ib = c.moe_inter / kBlk, Isb = (int64_t)c.n_shared * Ib;
+    const int64_t groups = (T * c.top_k + kGroupRows - 1) / kGroupRows;
+    const int64_t sgroups = c.n_shared > 0 ? (T + kGroupRows - 1) / kGroupRows : 0;
+    const int64_t U = groups * Ib * Hb + sgroups * Isb * Hb;  // same count for gate/up and down
+    const int64_t L = std::max<int64_t>(1, U / kMaxStreamCtas);
+    const int64_t kcmax = std::max<int64_t>(Hb, std::max(Ib, Isb));
+    return (int)std::max<int64_t>(1, std::min<int64_t>(kMaxParts, (kcmax + L - 1) / L));
+}
+
+cudaError_t launch_gateup_stream(const StreamArgs& a, const uint8_t* w_gate, const uint8_t* w_up, int E,
+                                 cudaStream_t st) {
+    static size_t smem_set = 0;
+    cudaError_t e = set_smem((const void*)gateup_stream_kernel, smem_gateup(), &smem_set);
+    if (e != cudaSuccess) return e;
+    TmaMap tg{}, tu{}, tsg{}, tsu{};
+    if (!tmap_u8_2d(&tg, w_gate, (uint64_t)E * a.I, a.H, kBlk, kTile) ||
+        !tmap_u8_2d(&tu, w_up, (uint64_t)E * a.I, a.H, kBlk, kTile))
+        return cudaErrorInvalidValue;
+    if (a.Is > 0 && (!tmap_u8_2d(&tsg, a.ws_gate, a.Is, a.H, kBlk, kTile) ||
+                     !tmap_u8_2d(&tsu, a.ws_up, a.Is, a.H, kBlk, kTile)))
+        return cudaErrorInvalidValue;
+    return launch_pdl(gateup_stream_kernel, a.grid_gu, kThreads, smem_gateup(), st, a, tg, tu, tsg, tsu);
+}
+
+cudaError_t launch_down_stream(const StreamArgs& a, const uint8_t* w_down, const uint8_t* ws_down, int E,
+                               cudaStream_t st) {
+    static size_t smem_set = 0;
+    const size_t smem = smem_down(std::max(a.I, a.Is));
+    cudaError_t e = set_smem((const void*)down_stream_kernel, smem, &smem_set);
+    if (e != cudaSuccess) return e;
+    TmaMap td{}, tsd{};
+    if (!tmap_u8_2d(&td, w_down, (uint64_t)E * a.H, a.I, kBlk, kTile)) return cudaErrorInvalidValue;
+    if (a.Is > 0 && !tmap_u8_2d(&tsd, ws_down, a.H, a.Is, kBlk, kTile)) return cudaErrorInvalidValue;
+    return launch_pdl(down_stream_kernel, a.grid_d, kThreads, smem, st, a, td, tsd);
+}
+
+cudaError_t launch_stream_combine(const StreamArgs& a, cudaStream_t st) {
+    const long n = a.fuse_combine ? (long)a.T * (a.H / 4)
+                                  : (long)a.T * a.k * (a.H / 4) + (a.n_shared_groups > 0 ? (long)a.T * (a.H / 4) : 0);
+    if (n == 0) return cudaSuccess;
+    const int grid = (int)std::min<long>((n + 255) / 256, (long)num_sms() * 8);
+    return launch_pdl(stream_combine_kernel, grid, 256, 0, st, a);
+}
+
+}  // namespace moe

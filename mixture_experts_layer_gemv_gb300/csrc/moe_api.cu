@@ -51,7 +51,7 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     const size_t t = (size_t)T;
     L.router_splits = router_splits_for(c, T);
     L.max_groups = max_routed_groups(c, T);
-    L.ctrl = take(sizeof(Ctrl));
+    L.ctrl = take(kCtrlRegionBytes);
     L.logits = take((size_t)L.router_splits * t * E * 4);
     L.ids = take(t * k * 4);
     L.w = take(t * k * 4);
@@ -61,8 +61,20 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     L.perm_src = take(t * k * 4);
     L.inv_pos = take(t * k * 4);
     L.groups = take((size_t)L.max_groups * sizeof(RowGroup));
-    L.a_routed = take(t * k * I * 4);
-    L.a_shared = take(t * Is * 4);
+    L.group_of_row = take(t * k * 4);
+    const size_t P = (size_t)stream_max_parts(c, T);
+    L.g_r = take(P * t * k * I * 4);
+    L.u_r = take(P * t * k * I * 4);
+    L.gb_r = take(P * t * k * I * 4);
+    L.ub_r = take(P * t * k * I * 4);
+    L.g_s = take(P * t * Is * 4);
+    L.u_s = take(P * t * Is * 4);
+    L.gb_s = take(P * t * Is * 4);
+    L.ub_s = take(P * t * Is * 4);
+    L.y_r = take(P * t * k * H * 4);
+    L.yb_r = take(P * t * k * H * 4);
+    L.y_s = take(P * t * H * 4);
+    L.yb_s = take(P * t * H * 4);
     L.y_perm = take(t * k * H * 2);
     L.y_shared = take(t * H * 2);
     L.total = off;
@@ -138,38 +150,48 @@ T* at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
-ExpertArgs expert_args(const moe_config_t* c, int32_t T, const moe_weights_t* W, const WsLayout& L, void* ws,
-                       const int32_t* perm_src, const float* topk_w, void* y_perm, void* y_shared) {
-    ExpertArgs a;
+StreamArgs stream_args(const moe_config_t* c, int32_t T, const moe_weights_t* W, const WsLayout& L, void* ws,
+                       const int32_t* perm_src, const float* topk_w) {
+    StreamArgs a = {};
     a.H = c->hidden;
     a.I = c->moe_inter;
     a.Is = c->n_shared * c->moe_inter;
     a.T = T;
     a.k = c->top_k;
     a.n_shared_groups = c->n_shared > 0 ? (T + kGroupRows - 1) / kGroupRows : 0;
-    a.w_gate = W->w_gate;
-    a.w_up = W->w_up;
-    a.w_down = W->w_down;
-    a.s_gate = W->s_gate;
-    a.s_up = W->s_up;
-    a.s_down = W->s_down;
-    a.ws_gate = W->ws_gate;
-    a.ws_up = W->ws_up;
-    a.ws_down = W->ws_down;
-    a.ss_gate = W->ss_gate;
-    a.ss_up = W->ss_up;
-    a.ss_down = W->ss_down;
-    a.xq = at<uint8_t>(ws, L.xq);
-    a.xs = at<float>(ws, L.xs);
+    a.grid_gu = stream_grid();
+    a.grid_d = stream_grid();
+    a.stages_d = down_stages(a.I, a.Is);
+    a.max_parts = stream_max_parts(*c, T);
+    a.ctrl = at<Ctrl>(ws, L.ctrl);
+    a.groups = at<RowGroup>(ws, L.groups);
+    a.group_of_row = at<int32_t>(ws, L.group_of_row);
     a.perm_src = perm_src;
     a.topk_w = topk_w;
-    a.groups = at<RowGroup>(ws, L.groups);
-    a.ctrl = at<Ctrl>(ws, L.ctrl);
-    a.a_routed = at<float>(ws, L.a_routed);
-    a.a_shared = at<float>(ws, L.a_shared);
-    a.y_perm = static_cast<__nv_bfloat16*>(y_perm);
-    a.y_shared = static_cast<__nv_bfloat16*>(y_shared);
-    a.max_groups = L.max_groups;
+    a.inv_pos = at<int32_t>(ws, L.inv_pos);
+    a.s_gate = W->s_gate;
+    a.s_up = W->s_up;
+    a.ss_gate = W->ss_gate;
+    a.ss_up = W->ss_up;
+    a.ws_gate = W->ws_gate;
+    a.ws_up = W->ws_up;
+    a.xq = at<uint8_t>(ws, L.xq);
+    a.xs = at<float>(ws, L.xs);
+    a.g_r = at<float>(ws, L.g_r);
+    a.u_r = at<float>(ws, L.u_r);
+    a.gb_r = at<float>(ws, L.gb_r);
+    a.ub_r = at<float>(ws, L.ub_r);
+    a.g_s = at<float>(ws, L.g_s);
+    a.u_s = at<float>(ws, L.u_s);
+    a.gb_s = at<float>(ws, L.gb_s);
+    a.ub_s = at<float>(ws, L.ub_s);
+    a.s_down = W->s_down;
+    a.ss_down = W->ss_down;
+    a.y_r = at<float>(ws, L.y_r);
+    a.yb_r = at<float>(ws, L.yb_r);
+    a.y_s = at<float>(ws, L.y_s);
+    a.yb_s = at<float>(ws, L.yb_s);
+    a.status = &at<Ctrl>(ws, L.ctrl)->status;
     return a;
 }
 
@@ -209,7 +231,8 @@ size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_tokens) {
 
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
-    MOE_CUDA(cudaMemsetAsync(ws, 0, sizeof(Ctrl), (cudaStream_t)stream));
+    MOE_CUDA(cudaMemsetAsync(ws, 0, ws_bytes < kCtrlRegionBytes ? ws_bytes : kCtrlRegionBytes,
+                             (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -250,7 +273,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, int32_t T, c
     if (T <= kSmallT) {
         MOE_CUDA(launch_route_small(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
                                     at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), nullptr, nullptr, nullptr, nullptr,
-                                    at<Ctrl>(ws, L.ctrl), st));
+                                    nullptr, at<Ctrl>(ws, L.ctrl), st));
     } else {
         MOE_CUDA(launch_route_large(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
                                     L.router_splits, st));
@@ -268,8 +291,8 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32
         if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
     MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
     const WsLayout L = ws_layout(*cfg, T);
-    MOE_CUDA(launch_permute(*cfg, topk_ids, T, expert_offsets, perm_src, inv_pos, nullptr, at<Ctrl>(ws, L.ctrl),
-                            (cudaStream_t)stream));
+    MOE_CUDA(launch_permute(*cfg, topk_ids, T, expert_offsets, perm_src, inv_pos, nullptr, nullptr,
+                            at<Ctrl>(ws, L.ctrl), (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -288,10 +311,15 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_bf16, int32_t
     const WsLayout L = ws_layout(*cfg, T);
     cudaStream_t st = (cudaStream_t)stream;
     MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), st));
-    MOE_CUDA(launch_build_groups(*cfg, expert_offsets, T * cfg->top_k, at<RowGroup>(ws, L.groups), at<Ctrl>(ws, L.ctrl), st));
-    const ExpertArgs a = expert_args(cfg, T, weights, L, ws, perm_src, topk_w, y_perm_bf16, y_shared_bf16);
-    MOE_CUDA(launch_gateup_gemv(a, st));
-    MOE_CUDA(launch_down_gemv(a, st));
+    MOE_CUDA(launch_build_groups(*cfg, expert_offsets, T * cfg->top_k, at<RowGroup>(ws, L.groups),
+                                 at<int32_t>(ws, L.group_of_row), at<Ctrl>(ws, L.ctrl), st));
+    StreamArgs a = stream_args(cfg, T, weights, L, ws, perm_src, topk_w);
+    a.fuse_combine = 0;
+    a.y_perm = static_cast<__nv_bfloat16*>(y_perm_bf16);
+    a.y_shared = static_cast<__nv_bfloat16*>(y_shared_bf16);
+    MOE_CUDA(launch_gateup_stream(a, weights->w_gate, weights->w_up, cfg->n_routed, st));
+    MOE_CUDA(launch_down_stream(a, weights->w_down, weights->ws_down, cfg->n_routed, st));
+    MOE_CUDA(launch_stream_combine(a, st));
     return MOE_OK;
 }
 
@@ -339,7 +367,8 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
     if (T <= kSmallT) {
         MOE_CUDA(launch_route_small(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
                                     at<float>(ws, L.logits), at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
-                                    at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups, ctrl, st));
+                                    at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups,
+                                    at<int32_t>(ws, L.group_of_row), ctrl, st));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
     } else {
         MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
@@ -347,23 +376,22 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
         MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), st));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
         MOE_TRY(mark.begin(MOE_STAGE_PERMUTE));
-        MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups, ctrl, st));
+        MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups,
+                                at<int32_t>(ws, L.group_of_row), ctrl, st));
         MOE_TRY(mark.end(MOE_STAGE_PERMUTE));
     }
-    void* y_perm = at<void>(ws, L.y_perm);
-    void* y_shared = cfg->n_shared > 0 ? at<void>(ws, L.y_shared) : nullptr;
-    const ExpertArgs a = expert_args(cfg, T, weights, L, ws, perm_src, w, y_perm, y_shared);
+    StreamArgs a = stream_args(cfg, T, weights, L, ws, perm_src, w);
+    a.fuse_combine = 1;
+    a.residual = static_cast<const __nv_bfloat16*>(residual_bf16);
+    a.out = static_cast<__nv_bfloat16*>(out_bf16);
     MOE_TRY(mark.begin(MOE_STAGE_GATE_UP));
-    MOE_CUDA(launch_gateup_gemv(a, st));
+    MOE_CUDA(launch_gateup_stream(a, weights->w_gate, weights->w_up, cfg->n_routed, st));
     MOE_TRY(mark.end(MOE_STAGE_GATE_UP));
     MOE_TRY(mark.begin(MOE_STAGE_DOWN));
-    MOE_CUDA(launch_down_gemv(a, st));
+    MOE_CUDA(launch_down_stream(a, weights->w_down, weights->ws_down, cfg->n_routed, st));
     MOE_TRY(mark.end(MOE_STAGE_DOWN));
     MOE_TRY(mark.begin(MOE_STAGE_COMBINE));
-    MOE_CUDA(launch_combine(T, cfg->hidden, cfg->top_k, static_cast<const __nv_bfloat16*>(y_perm), inv_pos,
-                            static_cast<const __nv_bfloat16*>(y_shared),
-                            static_cast<const __nv_bfloat16*>(residual_bf16), static_cast<__nv_bfloat16*>(out_bf16),
-                            st));
+    MOE_CUDA(launch_stream_combine(a, st));
     MOE_TRY(mark.end(MOE_STAGE_COMBINE));
     if (topk_ids_out)
         MOE_CUDA(cudaMemcpyAsync(topk_ids_out, ids, (size_t)T * cfg->top_k * sizeof(int32_t),

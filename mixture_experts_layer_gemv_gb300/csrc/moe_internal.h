@@ -6,7 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/moe.h"
+#include "moe.h"  // include/ (on the include path)
 
 namespace moe {
 
@@ -48,8 +48,11 @@ struct WsLayout {
     size_t perm_src;   // int32 [T*k]
     size_t inv_pos;    // int32 [T*k]
     size_t groups;     // RowGroup [max_groups]
-    size_t a_routed;   // fp32 [T*k, I]
-    size_t a_shared;   // fp32 [T, Is]
+    size_t group_of_row;  // int32 [T*k]
+    size_t g_r, u_r, gb_r, ub_r;  // fp32 [P][T*k, I] each
+    size_t g_s, u_s, gb_s, ub_s;  // fp32 [P][T, Is] each
+    size_t y_r, yb_r;             // fp32 [P][T*k, H] each
+    size_t y_s, yb_s;             // fp32 [P][T, H] each
     size_t y_perm;     // bf16 [T*k, H]
     size_t y_shared;   // bf16 [T, H]
     size_t total;
@@ -70,7 +73,8 @@ cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs
 cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits,
                                uint8_t* xq, float* xs, int32_t* offsets, int32_t* perm_src,
-                               int32_t* inv_pos, RowGroup* groups, Ctrl* ctrl, cudaStream_t st);
+                               int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl,
+                               cudaStream_t st);
 
 // Large-T route: tiled fp32 router (split-K partials) + softmax/top-k per token.
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
@@ -79,34 +83,67 @@ cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, cons
 
 // Stable counting sort of the T*k pairs by expert; writes row groups when groups != nullptr.
 cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int32_t* offsets,
-                           int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, Ctrl* ctrl,
-                           cudaStream_t st);
+                           int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row,
+                           Ctrl* ctrl, cudaStream_t st);
 
 // Row groups from existing expert offsets (stage API path).
 cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, int n_rows, RowGroup* groups,
-                                Ctrl* ctrl, cudaStream_t st);
+                                int32_t* group_of_row, Ctrl* ctrl, cudaStream_t st);
 
-struct ExpertArgs {
-    int H, I, Is, T, k, n_shared_groups;
-    const uint8_t *w_gate, *w_up, *w_down;
-    const float *s_gate, *s_up, *s_down;
-    const uint8_t *ws_gate, *ws_up, *ws_down;
-    const float *ss_gate, *ss_up, *ss_down;
-    const uint8_t* xq;
-    const float* xs;
-    const int32_t* perm_src;
-    const float* topk_w;
-    const RowGroup* groups;
-    const Ctrl* ctrl;
-    float* a_routed;
-    float* a_shared;
-    __nv_bfloat16* y_perm;
-    __nv_bfloat16* y_shared;
-    int max_groups;
+// Opaque 128-byte TMA descriptor (a CUtensorMap), passed to kernels by value.
+struct alignas(64) TmaMap {
+    unsigned char bytes[128];
 };
 
-cudaError_t launch_gateup_gemv(const ExpertArgs& a, cudaStream_t st);
-cudaError_t launch_down_gemv(const ExpertArgs& a, cudaStream_t st);
+// 2-D tensor map of an 8-bit row-major [rows, cols] tensor with a box of
+// box_rows x box_cols bytes and 128-byte swizzle (cached per address/shape/box).
+bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows);
+
+// Upper bound on the CTAs of the weight-streaming kernels (sizes the hand-off slots).
+constexpr int kMaxStreamCtas = 512;
+
+constexpr size_t kCtrlRegionBytes = sizeof(Ctrl);
+
+struct StreamArgs {
+    int H, I, Is, T, k, n_shared_groups;
+    int grid_gu, grid_d, stages_d;  // launch shapes (the readers of partial tiles need them)
+    int max_parts;                  // K parts the A buffers have room for
+    const Ctrl* ctrl;
+    const RowGroup* groups;
+    const int32_t* group_of_row;  // [T*k] row group of each permuted row
+    const int32_t* perm_src;
+    const float* topk_w;
+    const int32_t* inv_pos;
+    // gate/up
+    const float *s_gate, *s_up, *ss_gate, *ss_up;
+    const uint8_t *ws_gate, *ws_up;  // raw pointers of the shared weights (L2 prefetch)
+    const uint8_t* xq;
+    const float* xs;
+    float *g_r, *u_r;    // fp32 gate/up partial sums of routed rows [P][T*k, I]: A buffers
+    float *gb_r, *ub_r;  // and B buffers (rest of a cut tile, or zeros)
+    float *g_s, *u_s;    // shared rows [P][T, Is]
+    float *gb_s, *ub_s;
+    // down
+    const float *s_down, *ss_down;
+    float *y_r, *yb_r;  // fp32 weighted expert rows [P][T*k, H]: A and B buffers
+    float *y_s, *yb_s;  // shared rows [P][T, H]
+    // combine
+    int fuse_combine;  // 1: out (bf16) = sum of rows + shared (+ residual); 0: y_perm / y_shared (bf16)
+    __nv_bfloat16* y_perm;
+    __nv_bfloat16* y_shared;
+    const __nv_bfloat16* residual;
+    __nv_bfloat16* out;
+    int* status;
+};
+
+int stream_grid();
+int down_stages(int I, int Is);
+int stream_max_parts(const moe_config_t& c, int64_t T);  // K parts the workspace provides for
+cudaError_t launch_gateup_stream(const StreamArgs& a, const uint8_t* w_gate, const uint8_t* w_up, int E,
+                                 cudaStream_t st);
+cudaError_t launch_down_stream(const StreamArgs& a, const uint8_t* w_down, const uint8_t* ws_down, int E,
+                               cudaStream_t st);
+cudaError_t launch_stream_combine(const StreamArgs& a, cudaStream_t st);
 
 cudaError_t launch_combine(int T, int H, int k, const __nv_bfloat16* y_perm, const int32_t* inv_pos,
                            const __nv_bfloat16* y_shared, const __nv_bfloat16* residual,

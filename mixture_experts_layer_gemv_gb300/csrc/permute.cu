@@ -50,7 +50,7 @@ __device__ int scan_exclusive_warp256(int* v, int n) {
 // Write the row groups (<= kGroupRows rows of one expert each) from per-expert
 // counts in s_cnt and exclusive offsets in s_off. s_gcnt/s_goff are scratch.
 __device__ void write_groups(const int* s_cnt, const int* s_off, int* s_goff, int E, RowGroup* groups,
-                             Ctrl* ctrl) {
+                             int32_t* group_of_row, Ctrl* ctrl) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_goff[e] = (s_cnt[e] + kGroupRows - 1) / kGroupRows;
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -68,6 +68,7 @@ __device__ void write_groups(const int* s_cnt, const int* s_off, int* s_goff, in
             rg.nrows = min(kGroupRows, c - g * kGroupRows);
             rg.pad = 0;
             groups[s_goff[e] + g] = rg;
+            for (int r = 0; r < rg.nrows; ++r) group_of_row[rg.row_begin + r] = s_goff[e] + g;
         }
     }
 }
@@ -79,6 +80,7 @@ struct PermuteParams {
     int32_t* perm_src;
     int32_t* inv_pos;
     RowGroup* groups;
+    int32_t* group_of_row;
     Ctrl* ctrl;
 };
 
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(PermuteParams 
     }
     if (p.groups) {
         __syncthreads();
-        write_groups(s_cnt, s_off, s_goff, E, p.groups, p.ctrl);
+        write_groups(s_cnt, s_off, s_goff, E, p.groups, p.group_of_row, p.ctrl);
     }
 }
 
@@ -150,6 +152,7 @@ struct BuildGroupsParams {
     int E, n_rows;
     const int32_t* offsets;
     RowGroup* groups;
+    int32_t* group_of_row;
     Ctrl* ctrl;
 };
 
@@ -175,14 +178,14 @@ __global__ void __launch_bounds__(256) build_groups_kernel(BuildGroupsParams p) 
         }
         return;
     }
-    write_groups(s_cnt, s_off, s_goff, p.E, p.groups, p.ctrl);
+    write_groups(s_cnt, s_off, s_goff, p.E, p.groups, p.group_of_row, p.ctrl);
 }
 
 }  // namespace
 
 cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int32_t* offsets,
-                           int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, Ctrl* ctrl,
-                           cudaStream_t st) {
+                           int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row,
+                           Ctrl* ctrl, cudaStream_t st) {
     PermuteParams p;
     p.E = c.n_routed;
     p.n = T * c.top_k;
@@ -191,18 +194,20 @@ cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int
     p.perm_src = perm_src;
     p.inv_pos = inv_pos;
     p.groups = groups;
+    p.group_of_row = group_of_row;
     p.ctrl = ctrl;
     permute_kernel<<<1, kPermWarps * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, int n_rows, RowGroup* groups,
-                                Ctrl* ctrl, cudaStream_t st) {
+                                int32_t* group_of_row, Ctrl* ctrl, cudaStream_t st) {
     BuildGroupsParams p;
     p.E = c.n_routed;
     p.n_rows = n_rows;
     p.offsets = offsets;
     p.groups = groups;
+    p.group_of_row = group_of_row;
     p.ctrl = ctrl;
     build_groups_kernel<<<1, 256, 0, st>>>(p);
     return cudaGetLastError();

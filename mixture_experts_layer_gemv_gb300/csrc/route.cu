@@ -24,19 +24,21 @@ namespace {
 constexpr int kRouteWarps = 8;
 constexpr int kMaxE = 256;
 
-// 64-bit selection key: larger score first, then lower index. Scores are
-// non-negative probabilities, so their IEEE bits order like the values.
-__device__ __forceinline__ unsigned long long sel_key(float score, int idx) {
-    return ((unsigned long long)__float_as_uint(score) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)idx);
-}
-__device__ __forceinline__ int key_idx(unsigned long long key) { return (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFu)); }
-
 // Softmax over E logits and group-limited greedy top-k for one token, computed by
-// one warp. lg[i] is the logit of expert lane + 32*i (-inf beyond E). gscratch
-// holds kMaxE floats of shared memory private to this warp.
+// one warp. lg[i] is the logit of expert lane + 32*i (-inf beyond E). scratch holds
+// 2*kMaxE + 32 words of shared memory private to this warp.
+//
+// Selection by ranks instead of repeated arg-max rounds: a group is kept when fewer
+// than topk_group groups beat it (higher score, or equal score and lower index); the
+// candidates of kept groups are compacted with a ballot, and a candidate is selected
+// when fewer than top_k candidates beat it, its rank being its output slot. Same
+// result as the greedy rounds (ties to the lower index), with no serial dependency.
 __device__ void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, int Gk, int k, float scale,
-                          float* gscratch, int32_t* ids_out, float* w_out, int32_t* ids_smem) {
+                          float* scratch, int32_t* ids_out, float* w_out, int32_t* ids_smem) {
     const int lane = threadIdx.x & 31;
+    float* sp = scratch;                                          // [E] probabilities
+    int* cand = reinterpret_cast<int*>(scratch + kMaxE);          // [<= E] candidate ids
+    float* gsc = scratch + 2 * kMaxE;                             // [G] group scores
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) mx = fmaxf(mx, lg[i]);
@@ -54,47 +56,55 @@ __device__ void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, int Gk, i
     for (int i = 0; i < kMaxE / 32; ++i) {
         p[i] = p[i] / z;
         const int e = lane + 32 * i;
-        if (e < E) gscratch[e] = p[i];
+        if (e < E) sp[e] = p[i];
     }
     __syncwarp();
     // group score = max member score; groups are contiguous blocks of E/G experts
     const int per = E / G;
-    unsigned long long gkey = 0ull;
     if (lane < G) {
-        float m = gscratch[lane * per];
-        for (int i = 1; i < per; ++i) m = fmaxf(m, gscratch[lane * per + i]);
-        gkey = sel_key(m, lane) | (1ull << 63);  // bit 63 marks "present" so a 0 score still wins over empty lanes
+        float m = sp[lane * per];
+        for (int i = 1; i < per; ++i) m = fmaxf(m, sp[lane * per + i]);
+        gsc[lane] = m;
     }
     __syncwarp();
-    unsigned kept = 0u;
-    for (int r = 0; r < Gk; ++r) {
-        const unsigned long long best = warp_max_u64(gkey);
-        const int g = key_idx(best);
-        kept |= 1u << g;
-        if (lane == g) gkey = 0ull;
+    bool keep_g = false;
+    if (lane < G) {
+        const float mine = gsc[lane];
+        int beaten = 0;
+        for (int h = 0; h < G; ++h) {
+            const float o = gsc[h];
+            beaten += (o > mine) || (o == mine && h < lane);
+        }
+        keep_g = beaten < Gk;
     }
-    unsigned long long ck[kMaxE / 32];
+    const unsigned kept = __ballot_sync(0xffffffffu, keep_g);
+    // compact the candidates (experts of kept groups), in expert order
+    int n = 0;
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) {
         const int e = lane + 32 * i;
-        ck[i] = (e < E && ((kept >> (e / per)) & 1u)) ? (sel_key(p[i], e) | (1ull << 63)) : 0ull;
+        const bool c = e < E && ((kept >> (e / per)) & 1u);
+        const unsigned m = __ballot_sync(0xffffffffu, c);
+        if (c) cand[n + __popc(m & ((1u << lane) - 1u))] = e;
+        n += __popc(m);
     }
-    for (int j = 0; j < k; ++j) {
-        unsigned long long loc = 0ull;
-#pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i) loc = ck[i] > loc ? ck[i] : loc;
-        const unsigned long long best = warp_max_u64(loc);
-        const int e = key_idx(best);
-        const float pe = __uint_as_float((unsigned)((best >> 32) & 0x7FFFFFFFu));
-#pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i)
-            if (lane + 32 * i == e) ck[i] = 0ull;
-        if (lane == 0) {
-            ids_out[j] = e;
-            w_out[j] = pe * scale;
-            if (ids_smem) ids_smem[j] = e;
+    __syncwarp();
+    for (int j = lane; j < n; j += 32) {
+        const int e = cand[j];
+        const float pe = sp[e];
+        int beaten = 0;
+        for (int q = 0; q < n; ++q) {
+            const int o = cand[q];
+            const float po = sp[o];
+            beaten += (po > pe) || (po == pe && o < e);
+        }
+        if (beaten < k) {
+            ids_out[beaten] = e;
+            w_out[beaten] = pe * scale;
+            if (ids_smem) ids_smem[beaten] = e;
         }
     }
+    __syncwarp();
 }
 
 // Exclusive scan of n (<= 256) ints in shared memory by one warp; returns the total.
@@ -131,7 +141,7 @@ __device__ int warp_exclusive_scan256(int* v, int n) {
 // plus row groups of at most kGroupRows rows per expert.
 __device__ void small_permute(const int32_t* s_ids, int n, int E, int* s_cnt, int* s_off, int* s_gcnt,
                               int* s_goff, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
-                              RowGroup* groups, Ctrl* ctrl) {
+                              RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int c = 0;
         for (int f = 0; f < n; ++f) c += (s_ids[f] == e);
@@ -168,6 +178,7 @@ __device__ void small_permute(const int32_t* s_ids, int n, int E, int* s_cnt, in
             rg.nrows = min(kGroupRows, c - g * kGroupRows);
             rg.pad = 0;
             groups[s_goff[e] + g] = rg;
+            for (int r = 0; r < rg.nrows; ++r) group_of_row[rg.row_begin + r] = s_goff[e] + g;
         }
     }
 }
@@ -187,12 +198,13 @@ struct RouteSmallParams {
     int32_t* perm_src;
     int32_t* inv_pos;
     RowGroup* groups;
+    int32_t* group_of_row;
     Ctrl* ctrl;
 };
 
 __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmallParams p) {
     __shared__ float s_part[kRouteWarps][kSmallT];
-    __shared__ float s_gs[kRouteWarps][kMaxE];
+    __shared__ float s_gs[kRouteWarps][2 * kMaxE + 32];
     __shared__ int32_t s_ids[kSmallT * 16];
     __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_gcnt[kMaxE], s_goff[kMaxE];
     __shared__ int s_last;
@@ -200,6 +212,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x;
     const int H = p.H, T = p.T, Hb = H / kBlk;
+    pdl_wait();  // x and the workspace are free (the previous kernel in the stream is done)
+    pdl_launch_dependents();
 
     // ---- N: logits[:, e], K split over the CTA's warps (H/8 is a multiple of 16)
     const int slice = H / kRouteWarps;
@@ -263,7 +277,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     __syncthreads();
     if (p.offsets)
         small_permute(s_ids, T * p.k, p.E, s_cnt, s_off, s_gcnt, s_goff, p.offsets, p.perm_src, p.inv_pos,
-                      p.groups, p.ctrl);
+                      p.groups, p.group_of_row, p.ctrl);
     if (threadIdx.x == 0) p.ctrl->route_arrived = 0u;
 }
 
@@ -350,7 +364,7 @@ struct TopkParams {
 };
 
 __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
-    __shared__ float s_gs[8][kMaxE];
+    __shared__ float s_gs[8][2 * kMaxE + 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.T) return;
@@ -401,7 +415,7 @@ cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs
 cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, uint8_t* xq,
                                float* xs, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
-                               RowGroup* groups, Ctrl* ctrl, cudaStream_t st) {
+                               RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl, cudaStream_t st) {
     RouteSmallParams p;
     p.H = c.hidden;
     p.E = c.n_routed;
@@ -422,9 +436,18 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
     p.perm_src = perm_src;
     p.inv_pos = inv_pos;
     p.groups = groups;
+    p.group_of_row = group_of_row;
     p.ctrl = ctrl;
-    route_small_kernel<<<c.n_routed, kRouteWarps * 32, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c.n_routed);
+    cfg.blockDim = dim3(kRouteWarps * 32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, route_small_kernel, p);
 }
 
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,

@@ -96,6 +96,6 @@ def test_workspace_covers_the_largest_workload(L):
     wl = WORKLOADS["prefill_t4096"]
     n = B.moe_workspace_size(wl.cfg, wl.T)
     c = wl.cfg
-    # at least the permuted intermediate and outputs: fp32 a [T*k, I] + bf16 y [T*k, H]
-    assert n >= wl.T * c.top_k * (4 * c.moe_inter + 2 * c.hidden)
-    assert n < 2 * 1024 ** 3
+    # at least the permuted FP8 intermediate [T*k, I] and the bf16 expert outputs [T*k, H]
+    assert n >= wl.T * c.top_k * (c.moe_inter + 2 * c.hidden)
+    assert n < 4 * 1024 ** 3  # fp32 partial sums of the weight-streaming path dominate

@@ -280,3 +280,19 @@ def test_invalid_expert_id_is_reported_not_faulted():
     B.moe_permute(cfg, ids, off, ps, ip, ws)
     assert B.moe_read_device_status(ws) == -1  # MOE_ERR_INVALID_ARG
     assert B.moe_read_device_status(ws) == 0   # cleared by the read
+
+
+@pytest.mark.parametrize("T", [9, 16, 24])
+def test_second_shared_row_group_on_the_dsv2_layer(T):
+    # several 8-token groups of the shared experts: every CTA, wherever its range
+    # starts, must build the operand of the group it begins in
+    wl, W, x64, Wc = _layer("dsv2_decode_t64")
+    x = x64[:T].contiguous()
+    out, ids = B.forward(wl.cfg, x, W, return_ids=True)
+    torch.cuda.synchronize()
+    ids_o, w_o, p_o, margin = oracle.route(wl.cfg, x.cpu(), Wc["w_router"], Wc["router_bias"])
+    ids_eff, w_eff, _ = effective_routing(wl.cfg, ids.cpu().numpy(), ids_o, p_o, margin)
+    tokens = np.array([0, 7, 8, T - 1], dtype=np.int32)
+    ref = oracle.forward_tokens(wl.cfg, oracle.Weights(Wc), x.cpu(), ids_eff, w_eff, tokens)
+    assert_out_close(out[torch.from_numpy(tokens).long().cuda()], ref, f"T={T}")
+    assert torch.isfinite(out.float()).all()
