@@ -52,7 +52,7 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     L.router_splits = router_splits_for(c, T);
     L.max_groups = max_routed_groups(c, T);
     L.ctrl = take(kCtrlRegionBytes);
-    L.logits = take((size_t)L.router_splits * t * E * 4);
+    L.logits = take((size_t)L.router_splits * t * E * 4);  // router split-K partials
     L.ids = take(t * k * 4);
     L.w = take(t * k * 4);
     L.xq = take(t * H);

@@ -73,8 +73,13 @@ __device__ __forceinline__ Plan make_plan(int n_r, int kc_r, int n_s, int kc_s, 
     const long U = (long)n_r * kc_r + (long)n_s * kc_s;
     Plan pl;
     pl.nb = (int)std::max<long>(1, std::min<long>(grid, U));
-    const int kcmax = n_s > 0 ? std::max(kc_r, kc_s) : kc_r;
-    const int kcmin = n_s > 0 ? std::min(kc_r, kc_s) : kc_r;
+    int kcmax = 0, kcmin = INT_MAX;  // over the kinds that have rows
+    if (n_r > 0) kcmax = kcmin = kc_r;
+    if (n_s > 0) {
+        kcmax = std::max(kcmax, kc_s);
+        kcmin = std::min(kcmin, kc_s);
+    }
+    if (kcmax == 0) kcmax = kcmin = 1;
     const long L = std::max<long>(1, U / pl.nb);
     int P = (int)((kcmax + L - 1) / L);
     P = std::max(1, std::min(P, std::min(max_parts, kcmin)));
