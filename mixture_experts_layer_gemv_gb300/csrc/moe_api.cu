@@ -1,6 +1,7 @@
 // The C ABI of include/moe.h: host-side argument checks, workspace carving and
 // the launch sequence of each entry point. No entry point allocates memory or
 // synchronises the host, except moe_read_device_status (documented).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -38,6 +39,9 @@ int max_routed_groups(const moe_config_t& c, int64_t T) {
     return (int)(n / kGroupRows + touched + 1);
 }
 
+// Many tokens per expert: the grouped tensor-core GEMM instead of the streaming GEMVs.
+bool use_gemm(const moe_config_t& c, int64_t T) { return T > kSmallT && gemm_supported(c); }
+
 WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     WsLayout L;
     size_t off = 0;
@@ -62,7 +66,13 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     L.inv_pos = take(t * k * 4);
     L.groups = take((size_t)L.max_groups * sizeof(RowGroup));
     L.group_of_row = take(t * k * 4);
-    const size_t P = (size_t)stream_max_parts(c, T);
+    // the streaming GEMVs' partial sums; on the GEMM path they stay sized for kSmallT
+    // tokens so that the workspace size never shrinks as T grows
+    const bool gemm = use_gemm(c, T);
+    const size_t ts = gemm ? (size_t)kSmallT : t;
+    const size_t P = (size_t)stream_max_parts(c, (int64_t)ts);
+    {
+        const size_t t = ts;
     L.g_r = take(P * t * k * I * 4);
     L.u_r = take(P * t * k * I * 4);
     L.gb_r = take(P * t * k * I * 4);
@@ -75,6 +85,24 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     L.yb_r = take(P * t * k * H * 4);
     L.y_s = take(P * t * H * 4);
     L.yb_s = take(P * t * H * 4);
+    }
+    L.ld_r = L.ld_s = 0;
+    L.max_mtiles = 0;
+    L.xq_perm = L.xsT_r = L.xsT_s = L.hq_r = L.hq_s = L.hsT_r = L.hsT_s = L.mtiles = 0;
+    if (gemm) {
+        const size_t Hb = H / 128, Ib = I / 128, Isb = Is / 128;
+        L.ld_r = (long)((t * k + 3) & ~size_t(3));  // 16-byte rows for the scale tensor maps
+        L.ld_s = (long)((t + 3) & ~size_t(3));
+        L.max_mtiles = (int)((t * k + 127) / 128 + std::min(E, t * k));
+        L.xq_perm = take(t * k * H);
+        L.xsT_r = take(Hb * L.ld_r * 4);
+        L.xsT_s = take(Hb * L.ld_s * 4);
+        L.hq_r = take(t * k * I);
+        L.hq_s = take(t * Is);
+        L.hsT_r = take(Ib * L.ld_r * 4);
+        L.hsT_s = take(Isb * L.ld_s * 4);
+        L.mtiles = take((size_t)L.max_mtiles * sizeof(MTile));
+    }
     L.y_perm = take(t * k * H * 2);
     L.y_shared = take(t * H * 2);
     L.total = off;
@@ -208,6 +236,86 @@ struct StageMark {
     }
 };
 
+// Both grouped-GEMM launches of the large-T path: gate/up (x -> FP8 SiLU(g)*u) and
+// down (-> routing-weighted bf16 rows in y_perm, shared experts' rows in y_shared).
+cudaError_t run_expert_gemms(const moe_config_t* c, int32_t T, const moe_weights_t* W, const WsLayout& L, void* ws,
+                             const int32_t* perm_src, const float* topk_w, __nv_bfloat16* y_perm,
+                             __nv_bfloat16* y_shared, const StageMark* mark) {
+    const int H = c->hidden, I = c->moe_inter, E = c->n_routed, k = c->top_k;
+    const int Is = c->n_shared * c->moe_inter;
+    const bool sh = Is > 0;
+    const uint64_t n = (uint64_t)T * k;
+    cudaStream_t st = mark->st;
+    GemmArgs g = {};
+    g.H = H;
+    g.I = I;
+    g.Is = Is;
+    g.T = T;
+    g.k = k;
+    g.n_mt_s = sh ? (T + 127) / 128 : 0;
+    g.ld_r = L.ld_r;
+    g.ld_s = L.ld_s;
+    g.ctrl = at<Ctrl>(ws, L.ctrl);
+    g.mtiles = at<MTile>(ws, L.mtiles);
+    g.perm_src = perm_src;
+    g.topk_w = topk_w;
+    g.s_gate = W->s_gate;
+    g.s_up = W->s_up;
+    g.s_down = W->s_down;
+    g.ss_gate = W->ss_gate;
+    g.ss_up = W->ss_up;
+    g.ss_down = W->ss_down;
+    g.hq_r = at<uint8_t>(ws, L.hq_r);
+    g.hq_s = at<uint8_t>(ws, L.hq_s);
+    g.hsT_r = at<float>(ws, L.hsT_r);
+    g.hsT_s = at<float>(ws, L.hsT_s);
+    g.y_perm = y_perm;
+    g.y_shared = y_shared;
+    g.status = &at<Ctrl>(ws, L.ctrl)->status;
+
+    TmaMaps m = {};
+    // gate/up: A = permuted activation codes (routed) / token-order codes (shared)
+    g.mode = 0;
+    g.K_r = g.K_s = H;
+    g.nt_r = I / 128;
+    g.nt_s = Is / 128;
+    if (!tmap_u8_2d(&m.a_r, at<uint8_t>(ws, L.xq_perm), n, H, 128, 128) ||
+        !tmap_u8_2d(&m.b0_r, W->w_gate, (uint64_t)E * I, H, 128, 128) ||
+        !tmap_u8_2d(&m.b1_r, W->w_up, (uint64_t)E * I, H, 128, 128) ||
+        !tmap_f32_2d(&m.sx_r, at<float>(ws, L.xsT_r), H / 128, n, L.ld_r, 132, 1))
+        return cudaErrorInvalidValue;
+    if (sh && (!tmap_u8_2d(&m.a_s, at<uint8_t>(ws, L.xq), T, H, 128, 128) ||
+               !tmap_u8_2d(&m.b0_s, W->ws_gate, Is, H, 128, 128) ||
+               !tmap_u8_2d(&m.b1_s, W->ws_up, Is, H, 128, 128) ||
+               !tmap_f32_2d(&m.sx_s, at<float>(ws, L.xsT_s), H / 128, T, L.ld_s, 132, 1)))
+        return cudaErrorInvalidValue;
+    if (mark->begin(MOE_STAGE_GATE_UP) != MOE_OK) return cudaErrorUnknown;
+    cudaError_t e = launch_expert_gemm(g, m, st);
+    if (e != cudaSuccess) return e;
+    if (mark->end(MOE_STAGE_GATE_UP) != MOE_OK) return cudaErrorUnknown;
+
+    // down: A = the FP8 intermediate, B = 256 hidden rows per tile
+    g.mode = 1;
+    g.K_r = I;
+    g.K_s = Is;
+    g.nt_r = g.nt_s = H / 256;
+    m = TmaMaps{};
+    if (!tmap_u8_2d(&m.a_r, g.hq_r, n, I, 128, 128) ||
+        !tmap_u8_2d(&m.b0_r, W->w_down, (uint64_t)E * H, I, 128, 128) ||
+        !tmap_f32_2d(&m.sx_r, g.hsT_r, I / 128, n, L.ld_r, 132, 1))
+        return cudaErrorInvalidValue;
+    m.b1_r = m.b0_r;
+    if (sh && (!tmap_u8_2d(&m.a_s, g.hq_s, T, Is, 128, 128) || !tmap_u8_2d(&m.b0_s, W->ws_down, H, Is, 128, 128) ||
+               !tmap_f32_2d(&m.sx_s, g.hsT_s, Is / 128, T, L.ld_s, 132, 1)))
+        return cudaErrorInvalidValue;
+    m.b1_s = m.b0_s;
+    if (mark->begin(MOE_STAGE_DOWN) != MOE_OK) return cudaErrorUnknown;
+    e = launch_expert_gemm(g, m, st);
+    if (e != cudaSuccess) return e;
+    if (mark->end(MOE_STAGE_DOWN) != MOE_OK) return cudaErrorUnknown;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -291,7 +399,7 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32
         if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
     MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
     const WsLayout L = ws_layout(*cfg, T);
-    MOE_CUDA(launch_permute(*cfg, topk_ids, T, expert_offsets, perm_src, inv_pos, nullptr, nullptr,
+    MOE_CUDA(launch_permute(*cfg, topk_ids, T, expert_offsets, perm_src, inv_pos, nullptr, nullptr, nullptr,
                             at<Ctrl>(ws, L.ctrl), (cudaStream_t)stream));
     return MOE_OK;
 }
@@ -311,8 +419,20 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_bf16, int32_t
     const WsLayout L = ws_layout(*cfg, T);
     cudaStream_t st = (cudaStream_t)stream;
     MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), st));
+    if (use_gemm(*cfg, T)) {
+        MOE_CUDA(launch_build_groups(*cfg, expert_offsets, T * cfg->top_k, nullptr, nullptr, at<MTile>(ws, L.mtiles),
+                                     at<Ctrl>(ws, L.ctrl), st));
+        MOE_CUDA(launch_gather_rows(T, cfg->hidden, cfg->top_k, perm_src, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
+                                    at<uint8_t>(ws, L.xq_perm), at<float>(ws, L.xsT_r), L.ld_r,
+                                    cfg->n_shared > 0 ? at<float>(ws, L.xsT_s) : nullptr, L.ld_s,
+                                    &at<Ctrl>(ws, L.ctrl)->status, st));
+        const StageMark mark{nullptr, st};
+        MOE_CUDA(run_expert_gemms(cfg, T, weights, L, ws, perm_src, topk_w, static_cast<__nv_bfloat16*>(y_perm_bf16),
+                                  static_cast<__nv_bfloat16*>(y_shared_bf16), &mark));
+        return MOE_OK;
+    }
     MOE_CUDA(launch_build_groups(*cfg, expert_offsets, T * cfg->top_k, at<RowGroup>(ws, L.groups),
-                                 at<int32_t>(ws, L.group_of_row), at<Ctrl>(ws, L.ctrl), st));
+                                 at<int32_t>(ws, L.group_of_row), nullptr, at<Ctrl>(ws, L.ctrl), st));
     StreamArgs a = stream_args(cfg, T, weights, L, ws, perm_src, topk_w);
     a.fuse_combine = 0;
     a.y_perm = static_cast<__nv_bfloat16*>(y_perm_bf16);
@@ -376,8 +496,29 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
         MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), st));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
         MOE_TRY(mark.begin(MOE_STAGE_PERMUTE));
+        if (use_gemm(*cfg, T)) {
+            MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, nullptr, nullptr,
+                                    at<MTile>(ws, L.mtiles), ctrl, st));
+            MOE_CUDA(launch_gather_rows(T, cfg->hidden, cfg->top_k, perm_src, at<uint8_t>(ws, L.xq),
+                                        at<float>(ws, L.xs), at<uint8_t>(ws, L.xq_perm), at<float>(ws, L.xsT_r),
+                                        L.ld_r, cfg->n_shared > 0 ? at<float>(ws, L.xsT_s) : nullptr, L.ld_s,
+                                        &ctrl->status, st));
+            MOE_TRY(mark.end(MOE_STAGE_PERMUTE));
+            __nv_bfloat16* y_perm = at<__nv_bfloat16>(ws, L.y_perm);
+            __nv_bfloat16* y_shared = cfg->n_shared > 0 ? at<__nv_bfloat16>(ws, L.y_shared) : nullptr;
+            MOE_CUDA(run_expert_gemms(cfg, T, weights, L, ws, perm_src, w, y_perm, y_shared, &mark));
+            MOE_TRY(mark.begin(MOE_STAGE_COMBINE));
+            MOE_CUDA(launch_combine(T, cfg->hidden, cfg->top_k, y_perm, inv_pos, y_shared,
+                                    static_cast<const __nv_bfloat16*>(residual_bf16),
+                                    static_cast<__nv_bfloat16*>(out_bf16), st));
+            MOE_TRY(mark.end(MOE_STAGE_COMBINE));
+            if (topk_ids_out)
+                MOE_CUDA(cudaMemcpyAsync(topk_ids_out, ids, (size_t)T * cfg->top_k * sizeof(int32_t),
+                                         cudaMemcpyDeviceToDevice, st));
+            return MOE_OK;
+        }
         MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups,
-                                at<int32_t>(ws, L.group_of_row), ctrl, st));
+                                at<int32_t>(ws, L.group_of_row), nullptr, ctrl, st));
         MOE_TRY(mark.end(MOE_STAGE_PERMUTE));
     }
     StreamArgs a = stream_args(cfg, T, weights, L, ws, perm_src, w);

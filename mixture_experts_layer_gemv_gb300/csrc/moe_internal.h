@@ -22,7 +22,8 @@ struct Ctrl {
     int status;              // device error bits (kStatusTimeout ...)
     unsigned route_arrived;  // last-block-done counter of the fused router
     int n_routed_groups;     // work descriptors written by the permutation
-    int pad[61];
+    int n_mtiles;            // 128-row token tiles of the routed experts (grouped GEMM)
+    int pad[60];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 
@@ -35,6 +36,17 @@ struct RowGroup {
     int nrows;
     int pad;
 };
+
+// One 128-row tile of an expert's permuted token rows (grouped GEMM work list).
+struct MTile {
+    int expert;
+    int row0;
+    int nrows;
+    int pad;
+};
+
+// The grouped FP8 GEMM (tcgen05) of the large-T path; mode 0: gate/up -> SiLU(g)*u
+// quantised to FP8, mode 1: down -> routing-weighted bf16 rows.
 
 // Byte offsets of every workspace region for a given (config, T).
 struct WsLayout {
@@ -53,6 +65,13 @@ struct WsLayout {
     size_t g_s, u_s, gb_s, ub_s;  // fp32 [P][T, Is] each
     size_t y_r, yb_r;             // fp32 [P][T*k, H] each
     size_t y_s, yb_s;             // fp32 [P][T, H] each
+    size_t xq_perm;    // u8 [T*k, H]                 (grouped GEMM path)
+    size_t xsT_r, xsT_s; // fp32 [H/128][ld_r], [H/128][ld_s]
+    size_t hq_r, hq_s;   // u8 [T*k, I], [T, Is]
+    size_t hsT_r, hsT_s; // fp32 [I/128][ld_r], [Is/128][ld_s]
+    size_t mtiles;       // MTile [max_mtiles]
+    long ld_r, ld_s;
+    int max_mtiles;
     size_t y_perm;     // bf16 [T*k, H]
     size_t y_shared;   // bf16 [T, H]
     size_t total;
@@ -84,11 +103,11 @@ cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, cons
 // Stable counting sort of the T*k pairs by expert; writes row groups when groups != nullptr.
 cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int32_t* offsets,
                            int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row,
-                           Ctrl* ctrl, cudaStream_t st);
+                           MTile* mtiles, Ctrl* ctrl, cudaStream_t st);
 
 // Row groups from existing expert offsets (stage API path).
 cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, int n_rows, RowGroup* groups,
-                                int32_t* group_of_row, Ctrl* ctrl, cudaStream_t st);
+                                int32_t* group_of_row, MTile* mtiles, Ctrl* ctrl, cudaStream_t st);
 
 // Opaque 128-byte TMA descriptor (a CUtensorMap), passed to kernels by value.
 struct alignas(64) TmaMap {
@@ -135,6 +154,40 @@ struct StreamArgs {
     __nv_bfloat16* out;
     int* status;
 };
+
+struct GemmArgs {
+    int mode;
+    int H, I, Is, T, k;
+    int K_r, K_s;      // reduction length of routed / shared tiles
+    int nt_r, nt_s;    // weight tiles per token tile (routed / shared)
+    int n_mt_s;        // shared token tiles
+    long ld_r, ld_s;   // leading dimension of the transposed scale arrays
+    const Ctrl* ctrl;
+    const MTile* mtiles;
+    const int32_t* perm_src;
+    const float* topk_w;
+    const float *s_gate, *s_up, *s_down, *ss_gate, *ss_up, *ss_down;
+    uint8_t *hq_r, *hq_s;   // FP8 intermediate (gate/up output, down input)
+    float *hsT_r, *hsT_s;   // its scales, transposed [blocks][rows]
+    __nv_bfloat16* y_perm;
+    __nv_bfloat16* y_shared;
+    int* status;
+};
+struct TmaMaps {
+    TmaMap a_r, a_s, b0_r, b1_r, b0_s, b1_s, sx_r, sx_s;
+};
+bool gemm_supported(const moe_config_t& c);
+cudaError_t launch_expert_gemm(const GemmArgs& g, const TmaMaps& m, cudaStream_t st);
+// 2-D tensor map of a row-major fp32 [rows, cols] array with leading dimension ld (elements),
+// box of box_rows x box_cols, no swizzle.
+bool tmap_f32_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_cols,
+                 uint32_t box_rows);
+// xq_perm[r] = xq[token of r], xsT_r[kb][r] = xs[token of r][kb] for the routed rows and
+// xsT_s[kb][t] = xs[t][kb] for the shared experts' rows (skipped when xsT_s is null).
+// A row whose perm_src entry is outside [0, T*k) is written as zeros and sets kStatusBadId.
+cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, const float* xs,
+                               uint8_t* xq_perm, float* xsT_r, long ld_r, float* xsT_s, long ld_s, int* status,
+                               cudaStream_t st);
 
 int stream_grid();
 int down_stages(int I, int Is);

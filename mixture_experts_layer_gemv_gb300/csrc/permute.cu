@@ -7,7 +7,8 @@
 // counts its experts into a private shared-memory histogram, the histograms are
 // scanned expert-major / warp-minor, and each warp then walks its segment in
 // order, ranking equal experts inside each 32-wide chunk with __match_any_sync.
-// The same kernel emits the row-group work list of the expert GEMVs.
+// The same kernel emits the work list of the expert kernels: row groups of <= 8
+// rows for the streaming GEMVs, or 128-row tiles for the grouped GEMM.
 #include "common.cuh"
 #include "moe_internal.h"
 
@@ -73,6 +74,29 @@ __device__ void write_groups(const int* s_cnt, const int* s_off, int* s_goff, in
     }
 }
 
+// Write the 128-row token tiles of every expert segment (the grouped GEMM's work
+// list) from per-expert counts and offsets; s_tmp is scratch.
+__device__ void write_mtiles(const int* s_cnt, const int* s_off, int* s_tmp, int E, MTile* mtiles, Ctrl* ctrl) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_tmp[e] = (s_cnt[e] + 127) / 128;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int tot = scan_exclusive_warp256(s_tmp, E);
+        if (threadIdx.x == 0) ctrl->n_mtiles = tot;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int c = s_cnt[e];
+        for (int j = 0; 128 * j < c; ++j) {
+            MTile m;
+            m.expert = e;
+            m.row0 = s_off[e] + 128 * j;
+            m.nrows = min(128, c - 128 * j);
+            m.pad = 0;
+            mtiles[s_tmp[e] + j] = m;
+        }
+    }
+}
+
 struct PermuteParams {
     int E, n;
     const int32_t* ids;
@@ -81,6 +105,7 @@ struct PermuteParams {
     int32_t* inv_pos;
     RowGroup* groups;
     int32_t* group_of_row;
+    MTile* mtiles;
     Ctrl* ctrl;
 };
 
@@ -146,6 +171,10 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(PermuteParams 
         __syncthreads();
         write_groups(s_cnt, s_off, s_goff, E, p.groups, p.group_of_row, p.ctrl);
     }
+    if (p.mtiles) {
+        __syncthreads();
+        write_mtiles(s_cnt, s_off, s_goff, E, p.mtiles, p.ctrl);
+    }
 }
 
 struct BuildGroupsParams {
@@ -153,10 +182,11 @@ struct BuildGroupsParams {
     const int32_t* offsets;
     RowGroup* groups;
     int32_t* group_of_row;
+    MTile* mtiles;
     Ctrl* ctrl;
 };
 
-// Row groups from caller-supplied offsets. Offsets that are not a non-decreasing
+// Work lists from caller-supplied offsets. Offsets that are not a non-decreasing
 // sequence inside [0, T*k] would make the work list point outside the buffers, so
 // they are rejected on the device: the error bit is set and no work is listed.
 __global__ void __launch_bounds__(256) build_groups_kernel(BuildGroupsParams p) {
@@ -174,18 +204,88 @@ __global__ void __launch_bounds__(256) build_groups_kernel(BuildGroupsParams p) 
     if (s_bad) {
         if (threadIdx.x == 0) {
             p.ctrl->n_routed_groups = 0;
+            p.ctrl->n_mtiles = 0;
             set_status(&p.ctrl->status, kStatusBadId);
         }
         return;
     }
-    write_groups(s_cnt, s_off, s_goff, p.E, p.groups, p.group_of_row, p.ctrl);
+    if (p.groups) write_groups(s_cnt, s_off, s_goff, p.E, p.groups, p.group_of_row, p.ctrl);
+    if (p.mtiles) {
+        __syncthreads();
+        write_mtiles(s_cnt, s_off, s_goff, p.E, p.mtiles, p.ctrl);
+    }
+}
+
+// Rows of the grouped GEMM's operands in permuted order (see launch_gather_rows).
+constexpr int kGatherRows = 32;
+constexpr int kMaxHb = 256;
+
+struct GatherParams {
+    int T, H, k, n_blocks_r;
+    const int32_t* perm_src;
+    const uint8_t* xq;
+    const float* xs;
+    uint8_t* xq_perm;
+    float* xsT_r;
+    long ld_r;
+    float* xsT_s;
+    long ld_s;
+    int* status;
+};
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(GatherParams p) {
+    __shared__ float s_sc[kMaxHb][kGatherRows + 1];
+    __shared__ int s_tok[kGatherRows];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool shared = (int)blockIdx.x >= p.n_blocks_r;
+    const long r0 = (long)(shared ? (int)blockIdx.x - p.n_blocks_r : (int)blockIdx.x) * kGatherRows;
+    const long n = shared ? p.T : (long)p.T * p.k;
+    const int Hb = p.H / kBlk;
+    if (tid < kGatherRows) {
+        const long r = r0 + tid;
+        int tok = -1;
+        if (r < n) {
+            if (shared) {
+                tok = (int)r;
+            } else {
+                const int f = p.perm_src[r];
+                if ((unsigned)f < (unsigned)n)
+                    tok = f / p.k;
+                else
+                    set_status(p.status, kStatusBadId);
+            }
+        }
+        s_tok[tid] = tok;
+    }
+    __syncthreads();
+    if (!shared) {  // the shared experts read the activation codes in token order
+        const int H16 = p.H / 16;
+        for (int i = warp; i < kGatherRows && r0 + i < n; i += 8) {
+            const int tok = s_tok[i];
+            uint4* dst = reinterpret_cast<uint4*>(p.xq_perm + (size_t)(r0 + i) * p.H);
+            const uint4* src = reinterpret_cast<const uint4*>(p.xq + (size_t)(tok < 0 ? 0 : tok) * p.H);
+            for (int c = lane; c < H16; c += 32) dst[c] = tok >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    for (int i = tid; i < kGatherRows * Hb; i += blockDim.x) {
+        const int rr = i / Hb, kb = i % Hb;
+        const int tok = s_tok[rr];
+        s_sc[kb][rr] = tok >= 0 ? p.xs[(size_t)tok * Hb + kb] : 0.f;
+    }
+    __syncthreads();
+    float* dstT = shared ? p.xsT_s : p.xsT_r;
+    const long ld = shared ? p.ld_s : p.ld_r;
+    for (int i = tid; i < kGatherRows * Hb; i += blockDim.x) {
+        const int kb = i / kGatherRows, rr = i % kGatherRows;
+        if (r0 + rr < n) dstT[kb * ld + r0 + rr] = s_sc[kb][rr];
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int32_t* offsets,
                            int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row,
-                           Ctrl* ctrl, cudaStream_t st) {
+                           MTile* mtiles, Ctrl* ctrl, cudaStream_t st) {
     PermuteParams p;
     p.E = c.n_routed;
     p.n = T * c.top_k;
@@ -195,21 +295,46 @@ cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int
     p.inv_pos = inv_pos;
     p.groups = groups;
     p.group_of_row = group_of_row;
+    p.mtiles = mtiles;
     p.ctrl = ctrl;
     permute_kernel<<<1, kPermWarps * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, int n_rows, RowGroup* groups,
-                                int32_t* group_of_row, Ctrl* ctrl, cudaStream_t st) {
+                                int32_t* group_of_row, MTile* mtiles, Ctrl* ctrl, cudaStream_t st) {
     BuildGroupsParams p;
     p.E = c.n_routed;
     p.n_rows = n_rows;
     p.offsets = offsets;
     p.groups = groups;
     p.group_of_row = group_of_row;
+    p.mtiles = mtiles;
     p.ctrl = ctrl;
     build_groups_kernel<<<1, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, const float* xs,
+                               uint8_t* xq_perm, float* xsT_r, long ld_r, float* xsT_s, long ld_s, int* status,
+                               cudaStream_t st) {
+    if (H / kBlk > kMaxHb) return cudaErrorInvalidValue;
+    GatherParams p;
+    p.T = T;
+    p.H = H;
+    p.k = k;
+    p.n_blocks_r = (int)(((long)T * k + kGatherRows - 1) / kGatherRows);
+    p.perm_src = perm_src;
+    p.xq = xq;
+    p.xs = xs;
+    p.xq_perm = xq_perm;
+    p.xsT_r = xsT_r;
+    p.ld_r = ld_r;
+    p.xsT_s = xsT_s;
+    p.ld_s = ld_s;
+    p.status = status;
+    const int n_blocks_s = xsT_s ? (T + kGatherRows - 1) / kGatherRows : 0;
+    gather_rows_kernel<<<p.n_blocks_r + n_blocks_s, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 

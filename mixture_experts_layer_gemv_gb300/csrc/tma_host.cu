@@ -29,20 +29,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint32_t, uint32_t>;
+// (address, rows, cols, row pitch in bytes, box, element kind)
+using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint64_t, uint32_t, uint32_t, int>;
 std::mutex g_mu;
 std::map<Key, CUtensorMap> g_cache;
 
-}  // namespace
-
-bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                uint32_t box_rows) {
-    const Key key{(uintptr_t)base, rows, cols, box_cols, box_rows};
+bool encode_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch_bytes, uint32_t box_cols,
+               uint32_t box_rows, bool f32) {
+    static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "opaque map size");
+    const Key key{(uintptr_t)base, rows, cols, pitch_bytes, box_cols, box_rows, f32 ? 1 : 0};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_cache.find(key);
         if (it != g_cache.end()) {
-            static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "opaque map size");
             *reinterpret_cast<CUtensorMap*>(out) = it->second;
             return true;
         }
@@ -51,12 +50,13 @@ bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uin
     if (!fn) return false;
     CUtensorMap m;
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols};  // bytes between rows
+    const cuuint64_t strides[1] = {pitch_bytes};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r =
+        fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -65,6 +65,20 @@ bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uin
     }
     *reinterpret_cast<CUtensorMap*>(out) = m;
     return true;
+}
+
+}  // namespace
+
+// u8 [rows, cols], dense rows, 128-byte swizzle (box_cols must be 128)
+bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                uint32_t box_rows) {
+    return encode_2d(out, base, rows, cols, cols, box_cols, box_rows, false);
+}
+
+// fp32 [rows, cols] with row pitch ld elements, no swizzle; reads beyond cols or rows return zeros
+bool tmap_f32_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_cols,
+                 uint32_t box_rows) {
+    return encode_2d(out, base, rows, cols, ld * 4, box_cols, box_rows, true);
 }
 
 }  // namespace moe

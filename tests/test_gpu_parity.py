@@ -224,7 +224,7 @@ def test_group_and_topk_degenerate_cases(G, Gk, k):
     _run_and_check(cfg, W, x)
 
 
-@pytest.mark.parametrize("T", [5, 200])
+@pytest.mark.parametrize("T", [5, 200, 300])
 def test_one_expert_receives_every_token(T):
     cfg = MoEConfig(256, 256, 8, 2, 1, 2, 1.0, 1)
     W = make_weights(cfg, 40, "cuda")
@@ -296,3 +296,55 @@ def test_second_shared_row_group_on_the_dsv2_layer(T):
     ref = oracle.forward_tokens(wl.cfg, oracle.Weights(Wc), x.cpu(), ids_eff, w_eff, tokens)
     assert_out_close(out[torch.from_numpy(tokens).long().cuda()], ref, f"T={T}")
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------- grouped tensor-core GEMM path (T > 64 tokens)
+GEMM_CFG = MoEConfig(512, 256, 16, 4, 2, 4, 1.0, 2)
+
+
+@pytest.mark.parametrize("T", [65, 129, 257, 600])
+def test_grouped_gemm_path_every_token(T):
+    # 128-row token tiles: several per expert, ragged last tiles, and a shared-expert
+    # tile with a single row at T = 129 and T = 257
+    W = make_weights(GEMM_CFG, 70, "cuda")
+    x = make_tokens(GEMM_CFG, T, 71 + T, "cuda")
+    res = make_tokens(GEMM_CFG, T, 72, "cuda", name="residual")
+    _run_and_check(GEMM_CFG, W, x, residual=res)
+
+
+def test_grouped_gemm_expert_segments_on_tile_boundaries():
+    """moe_permute -> moe_expert_ffn with hand-made ids: expert segments of exactly 128,
+    256, 1 and 0 rows, so tiles start and end on every kind of boundary; every
+    permuted row is checked against the oracle's expert row."""
+    cfg = MoEConfig(512, 256, 16, 4, 2, 4, 1.0, 1)
+    T, k = 160, 4
+    t = np.arange(T)
+    ids = np.stack([np.where(t < 128, 0, 3),                 # expert 0: 128 rows
+                    np.full(T, 1),                           # expert 1: 160 + 96 = 256 rows
+                    np.where(t < 64, 2, 1),                  # expert 2: 64 rows
+                    np.where(t == 5, 4, 5 + t % 11)], 1)     # expert 4: 1 row; experts 5..15
+    assert (np.bincount(ids.ravel(), minlength=16)[[0, 1, 4]] == [128, 256, 1]).all()
+    rng = np.random.default_rng(80)
+    w = rng.uniform(0.1, 2.0, (T, k))
+    W = make_weights(cfg, 81, "cuda")
+    x = make_tokens(cfg, T, 82, "cuda")
+    ws = B.alloc_workspace(cfg, T)
+    ids_d = torch.from_numpy(ids.astype(np.int32)).cuda()
+    w_d = torch.from_numpy(w.astype(np.float32)).cuda()
+    off = torch.empty(cfg.n_routed + 1, dtype=torch.int32, device="cuda")
+    ps = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    ip = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    B.moe_permute(cfg, ids_d, off, ps, ip, ws)
+    y_perm = torch.empty((T * k, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    y_sh = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device="cuda")
+    B.moe_expert_ffn(cfg, x, W, off, ps, w_d.float(), y_perm, y_sh, ws)
+    torch.cuda.synchronize()
+    assert B.moe_read_device_status(ws) == 0
+    OW = oracle.Weights(host_weights(W))
+    xc = x.cpu()
+    inv = ip.cpu().numpy()
+    for tok in range(T):
+        for j in range(k):
+            y_ref, _ = oracle.expert_row(cfg, OW, xc[tok], int(ids[tok, j]), float(w[tok, j]))
+            assert_out_close(y_perm[inv[tok * k + j]], y_ref, f"row ({tok},{j}) expert {ids[tok, j]}")
+        assert_out_close(y_sh[tok], oracle.shared_row(cfg, OW, xc[tok]), f"shared {tok}")
