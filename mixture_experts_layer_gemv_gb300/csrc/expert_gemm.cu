@@ -10,17 +10,21 @@
 // Block scales. The weights carry arbitrary fp32 scales per 128x128 block and the
 // activations a power-of-two scale per (row, 128 channels), so the tensor core cannot
 // apply them: every 128-wide K block is accumulated on its own (4 MMAs of K=32) into
-// one of two TMEM accumulators, and the epilogue warps promote it,
+// one of two TMEM accumulators, and the epilogue promotes it into registers,
 //     acc[m][n] += D_kb[m][n] * s_x[m][kb] * s_w[n-block][kb],
-// while the MMA warp fills the other accumulator with the next K block.
+// while the tensor core fills the other accumulator with the next K block.
 //
-// Warp roles (one CTA per SM, persistent over tiles):
-//   warp 9      TMA producer: A box (128 rows x 128 B), B boxes (2 x 128 rows x 128 B),
-//               the tile rows' activation scales for this K block, into a 4-stage ring
-//   warp 8      MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 per K block,
-//               commits to the stage's "empty" barrier and the accumulator's "full"
-//   warps 0-7   epilogue: warpgroup g covers columns [64g, 64g+64) of gate and of up
-//               (or [128g, 128g+128) of down); TMEM lanes 32*(warp%4).. are its rows
+// One CTA of 10 warps per SM, persistent over tiles, warp-specialised:
+//   warp 9      TMA producer: per K block an A box (128 rows x 128 B) and two B boxes
+//               (128 rows x 128 B) into a 4-stage ring; a stage is refilled as soon as
+//               the MMAs that read it have completed
+//   warp 8      MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 per K block into
+//               accumulator n%2 once the epilogue has drained it
+//   warps 0-7   epilogue: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and, with
+//               g = w/4, columns [64g, 64g+64) of gate and of up (or [128g, 128g+128) of
+//               down), so each thread keeps a 128-float accumulator row in registers
+// Activation scales come from global memory (row-major, one row per thread) and the
+// weight scales of the tile's row blocks too; both are loaded one K block ahead.
 // Epilogue at the end of a tile: gate/up -> a = SiLU(g) * u, quantised per 128 values
 // to E4M3 with a power-of-two scale (the down GEMM's operand); down -> w * y in bf16.
 #include <algorithm>
@@ -36,15 +40,13 @@ constexpr int kGM = 128;                  // token rows per tile (MMA M)
 constexpr int kGN = 256;                  // weight rows per tile (MMA N)
 constexpr int kGStages = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kGThreads = (kEpiWarps + 2) * 32;
-constexpr int kProducerWarp = kEpiWarps + 1;
 constexpr int kMmaWarp = kEpiWarps;
+constexpr int kProducerWarp = kEpiWarps + 1;
+constexpr int kGThreads = (kEpiWarps + 2) * 32;
 constexpr int kSA = kGM * kBlk;           // 16 KB A tile
 constexpr int kSB = kGN * kBlk;           // 32 KB B tile
-constexpr int kSXF = 132;                 // activation scales loaded per stage (floats)
-constexpr int kStageBytes = ((kSA + kSB + kSXF * 4) + 1023) & ~1023;
+constexpr int kStageBytes = kSA + kSB;    // a multiple of 1024 (128-byte swizzle atoms)
 constexpr uint32_t kTmemCols = 512;       // two 128 x 256 fp32 accumulators
-constexpr uint32_t kPolls = 1u << 22;
 constexpr uint32_t kIdesc = idesc_f8_f32(kGM, kGN);
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -68,31 +70,75 @@ __device__ __forceinline__ Item decode_item(const GemmArgs& a, int n_mt_r, int i
         it.expert = mt.expert;
         it.row0 = mt.row0;
         it.nrows = mt.nrows;
-        it.ntile = (int)(item % a.nt_r);
+        it.ntile = item % a.nt_r;
     } else {
         const int v = item - n_r;
-        const int m = (int)(v / a.nt_s);
         it.shared = 1;
         it.expert = -1;
-        it.row0 = m * kGM;
+        it.row0 = (v / a.nt_s) * kGM;
         it.nrows = min(kGM, a.T - it.row0);
-        it.ntile = (int)(v % a.nt_s);
+        it.ntile = v % a.nt_s;
     }
     return it;
+}
+
+// Number of this CTA's items (blockIdx.x, blockIdx.x + gridDim.x, ...) in [from, to).
+__device__ __forceinline__ int items_in(int from, int to) {
+    const int b = blockIdx.x, g = gridDim.x;
+    const int first = from <= b ? b : b + ((from - b + g - 1) / g) * g;
+    return first < to ? (to - 1 - first) / g + 1 : 0;
+}
+
+// Walks this CTA's K blocks in order (the TMA side of the pipeline).
+struct LoadCursor {
+    int item, kb, Kb, shared, row0, yb0, yb1;
+    __device__ __forceinline__ void set(const GemmArgs& a, int n_mt_r, int n_items, bool gateup) {
+        if (item >= n_items) return;
+        const Item it = decode_item(a, n_mt_r, item);
+        Kb = (it.shared ? a.K_s : a.K_r) / kBlk;
+        shared = it.shared;
+        row0 = it.row0;
+        if (gateup) {  // 128 gate rows and the same 128 rows of up
+            yb0 = (it.shared ? 0 : it.expert * a.I) + it.ntile * kBlk;
+            yb1 = yb0;
+        } else {       // 256 consecutive rows of down
+            yb0 = (it.shared ? 0 : it.expert * a.H) + it.ntile * kGN;
+            yb1 = yb0 + kBlk;
+        }
+    }
+    __device__ __forceinline__ void next(const GemmArgs& a, int n_mt_r, int n_items, bool gateup) {
+        if (++kb == Kb) {
+            kb = 0;
+            item += gridDim.x;
+            set(a, n_mt_r, n_items, gateup);
+        }
+    }
+};
+
+struct Maps {
+    const void *a_r, *a_s, *b0_r, *b1_r, *b0_s, *b1_s;
+};
+
+__device__ __forceinline__ void issue_loads(uint8_t* stage, uint64_t* bar, const LoadCursor& c, const Maps& m) {
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    const int x = c.kb * kBlk;
+    tma_load_2d(stage, c.shared ? m.a_s : m.a_r, x, c.row0, bar);
+    tma_load_2d(stage + kSA, c.shared ? m.b0_s : m.b0_r, x, c.yb0, bar);
+    tma_load_2d(stage + kSA + kSB / 2, c.shared ? m.b1_s : m.b1_r, x, c.yb1, bar);
 }
 
 template <int kMode>  // 0: gate/up, 1: down
 __global__ void __launch_bounds__(kGThreads, 1)
     expert_gemm_kernel(const GemmArgs a, const __grid_constant__ TmaMap tm_a_r, const __grid_constant__ TmaMap tm_a_s,
                        const __grid_constant__ TmaMap tm_b0_r, const __grid_constant__ TmaMap tm_b1_r,
-                       const __grid_constant__ TmaMap tm_b0_s, const __grid_constant__ TmaMap tm_b1_s,
-                       const __grid_constant__ TmaMap tm_sx_r, const __grid_constant__ TmaMap tm_sx_s) {
+                       const __grid_constant__ TmaMap tm_b0_s, const __grid_constant__ TmaMap tm_b1_s) {
+    constexpr bool gateup = kMode == 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGStages * kStageBytes);
     uint64_t* empty = full + kGStages;
-    uint64_t* acc_full = empty + kGStages;   // [2]
-    uint64_t* acc_empty = acc_full + 2;      // [2]
+    uint64_t* acc_full = empty + kGStages;  // [2]
+    uint64_t* acc_empty = acc_full + 2;     // [2]
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + 2);
     float* s_amax = reinterpret_cast<float*>(s_tmem + 4);  // [2][128]
 
@@ -100,7 +146,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kGStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + kEpiWarps);  // MMA commit + every epilogue warp (activation scales read)
+            mbar_init(&empty[s], 1);  // the MMA warp's commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -120,135 +166,121 @@ __global__ void __launch_bounds__(kGThreads, 1)
     pdl_launch_dependents();
 
     const int n_mt_r = a.ctrl->n_mtiles;
-    const int n_items = n_mt_r * a.nt_r + a.n_mt_s * a.nt_s;
-    constexpr bool gateup = kMode == 0;
+    const int n_r = n_mt_r * a.nt_r;
+    const int n_items = n_r + a.n_mt_s * a.nt_s;
+    // K blocks this CTA runs, over all its items
+    const int total = items_in(0, n_r) * (a.K_r / kBlk) + items_in(n_r, n_items) * (a.K_s / kBlk);
 
     if (warp == kProducerWarp) {
         // ----------------------------------------------------------- TMA producer
-        if (lane == 0) {
+        if (lane == 0 && total > 0) {
+            const Maps maps{&tm_a_r, &tm_a_s, &tm_b0_r, &tm_b1_r, &tm_b0_s, &tm_b1_s};
             prefetch_tmap(&tm_a_r);
             prefetch_tmap(&tm_b0_r);
-            prefetch_tmap(&tm_sx_r);
+            prefetch_tmap(&tm_b1_r);
             if (a.n_mt_s > 0) {
                 prefetch_tmap(&tm_a_s);
                 prefetch_tmap(&tm_b0_s);
-                prefetch_tmap(&tm_sx_s);
+                prefetch_tmap(&tm_b1_s);
             }
-            int n = 0;  // K blocks issued
-            bool ok = true;
-            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-                const Item it = decode_item(a, n_mt_r, item);
-                const int Kb = (it.shared ? a.K_s : a.K_r) / kBlk;
-                const void* ma = it.shared ? (const void*)&tm_a_s : (const void*)&tm_a_r;
-                const void* mb0 = it.shared ? (const void*)&tm_b0_s : (const void*)&tm_b0_r;
-                const void* mb1 = it.shared ? (const void*)&tm_b1_s : (const void*)&tm_b1_r;
-                const void* msx = it.shared ? (const void*)&tm_sx_s : (const void*)&tm_sx_r;
-                // weight rows of this tile in the 2-D [E * rows_per_expert, K] view
-                int yb0, yb1;
-                if (gateup) {
-                    const int base = it.shared ? 0 : it.expert * a.I;
-                    yb0 = base + it.ntile * kBlk;  // gate rows
-                    yb1 = yb0;                     // the same rows of up
-                } else {
-                    const int base = it.shared ? 0 : it.expert * a.H;
-                    yb0 = base + it.ntile * kGN;
-                    yb1 = yb0 + kBlk;
+            LoadCursor lc;
+            lc.item = blockIdx.x;
+            lc.kb = 0;
+            lc.set(a, n_mt_r, n_items, gateup);
+            int n = 0;
+            for (; n < total; ++n) {
+                const int s = n % kGStages;
+                if (n >= kGStages && !mbar_wait_bounded(&empty[s], ((n / kGStages) - 1) & 1)) {
+                    set_status(a.status, kStatusTimeout);
+                    break;
                 }
-                const int x0 = it.row0 & ~3;  // TMA inner coordinate must be 16-byte aligned
-                for (int kb = 0; kb < Kb; ++kb, ++n) {
-                    const int s = (int)(n % kGStages);
-                    if (n >= kGStages && !mbar_wait_bounded(&empty[s], ((n / kGStages) - 1) & 1, kPolls)) {
-                        set_status(a.status, kStatusTimeout);
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* st = smem + s * kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], kSA + kSB + kSXF * 4);
-                    tma_load_2d(st, ma, kb * kBlk, it.row0, &full[s]);
-                    tma_load_2d(st + kSA, mb0, kb * kBlk, yb0, &full[s]);
-                    tma_load_2d(st + kSA + kSB / 2, mb1, kb * kBlk, yb1, &full[s]);
-                    tma_load_2d(st + kSA + kSB, msx, x0, kb, &full[s]);
-                }
+                issue_loads(smem + s * kStageBytes, &full[s], lc, maps);
+                lc.next(a, n_mt_r, n_items, gateup);
             }
             // copies still in flight land before this CTA may exit
-            const int done_from = n > kGStages ? n - kGStages : 0;
-            for (int q = done_from; q < n; ++q)
-                mbar_wait_bounded(&full[q % kGStages], (q / kGStages) & 1, kPolls);
+            for (int q = n > kGStages ? n - kGStages : 0; q < n; ++q)
+                mbar_wait_bounded(&full[q % kGStages], (q / kGStages) & 1);
         }
     } else if (warp == kMmaWarp) {
         // -------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             int n = 0;
-            bool ok = true;
-            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-                const Item it = decode_item(a, n_mt_r, item);
-                const int Kb = (it.shared ? a.K_s : a.K_r) / kBlk;
-                for (int kb = 0; kb < Kb; ++kb, ++n) {
-                    const int s = (int)(n % kGStages);
-                    const int b = (int)(n & 1);
-                    if (n >= 2 && !mbar_wait_bounded(&acc_empty[b], ((n >> 1) - 1) & 1, kPolls)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!mbar_wait_bounded(&full[s], (n / kGStages) & 1, kPolls)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint8_t* st = smem + s * kStageBytes;
-                    const uint64_t da = smem_desc_sw128(st);
-                    const uint64_t db = smem_desc_sw128(st + kSA);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)  // 4 x K=32 bytes inside the 128-byte swizzled rows
-                        tc_mma_f8(tmem + b * kGN, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), kIdesc, k > 0);
-                    tc_commit(&empty[s]);
-                    tc_commit(&acc_full[b]);
+            for (; n < total; ++n) {
+                const int s = n % kGStages, b = n & 1;
+                if ((n >= 2 && !mbar_wait_bounded(&acc_empty[b], ((n >> 1) - 1) & 1)) ||
+                    !mbar_wait_bounded(&full[s], (n / kGStages) & 1)) {
+                    set_status(a.status, kStatusTimeout);
+                    break;
                 }
+                tc_fence_after();
+                const uint8_t* st = smem + s * kStageBytes;
+                const uint64_t da = smem_desc_sw128(st);
+                const uint64_t db = smem_desc_sw128(st + kSA);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // 4 x K=32 bytes inside the 128-byte swizzled rows
+                    tc_mma_f8(tmem + b * kGN, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), kIdesc, k > 0);
+                tc_commit(&empty[s]);
+                tc_commit(&acc_full[b]);
             }
-            if (!ok) set_status(a.status, kStatusTimeout);
             // every MMA issued has completed before the CTA frees tensor memory
-            if (n > 0) mbar_wait_bounded(&acc_full[(n - 1) & 1], ((n - 1) >> 1) & 1, kPolls);
+            if (n > 0) mbar_wait_bounded(&acc_full[(n - 1) & 1], ((n - 1) >> 1) & 1);
         }
     } else {
         // ---------------------------------------------------------------- epilogue
-        const int q = warp & 3;          // TMEM lane quadrant: rows 32q .. 32q+31
-        const int wg = warp >> 2;        // column half
-        const int row = 32 * q + lane;   // tile row of this thread
-        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        int n = 0;
+        const int q4 = warp & 3;          // TMEM lane quadrant: rows 32q .. 32q+31
+        const int wg = warp >> 2;         // column half
+        const int row = 32 * q4 + lane;   // tile row of this thread
+        const uint32_t t_row = tmem + ((uint32_t)(32 * q4) << 16);
+        int n = 0;  // K blocks consumed
         bool ok = true;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-            const Item it = decode_item(a, n_mt_r, item);
-            const int Kb = (it.shared ? a.K_s : a.K_r) / kBlk;
-            // weight block scales of this tile's rows, one per K block
-            const float* sw0;
-            const float* sw1;
-            if (gateup) {
-                const size_t r = it.shared ? (size_t)it.ntile : (size_t)it.expert * (a.I / kBlk) + it.ntile;
-                sw0 = (it.shared ? a.ss_gate : a.s_gate) + r * Kb;
-                sw1 = (it.shared ? a.ss_up : a.s_up) + r * Kb;
-            } else {
-                const size_t r = (it.shared ? 0 : (size_t)it.expert * (a.H / kBlk)) + (size_t)it.ntile * 2 + wg;
-                sw0 = (it.shared ? a.ss_down : a.s_down) + r * Kb;
-                sw1 = sw0;
+            int Kb, grow;
+            bool valid_row;
+            const float *sxp, *sw0, *sw1;
+            {
+                const Item it = decode_item(a, n_mt_r, item);
+                Kb = (it.shared ? a.K_s : a.K_r) / kBlk;
+                valid_row = row < it.nrows;
+                grow = it.row0 + row;  // row in the A tensor and the output tensors
+                // this row's activation scales (row-major, Kb per row) and the weight scales
+                if (gateup) {
+                    int tok = grow;
+                    if (!it.shared) {
+                        const int f = valid_row ? a.perm_src[grow] : 0;
+                        tok = ((unsigned)f < (unsigned)(a.T * a.k)) ? f / a.k : 0;
+                    }
+                    sxp = a.xs + (size_t)(valid_row ? tok : 0) * Kb;
+                    const size_t r = it.shared ? (size_t)it.ntile : (size_t)it.expert * (a.I / kBlk) + it.ntile;
+                    sw0 = (it.shared ? a.ss_gate : a.s_gate) + r * Kb;
+                    sw1 = (it.shared ? a.ss_up : a.s_up) + r * Kb;
+                } else {
+                    sxp = (it.shared ? a.hs_s : a.hs_r) + (size_t)(valid_row ? grow : 0) * Kb;
+                    const size_t r = (it.shared ? 0 : (size_t)it.expert * (a.H / kBlk)) + (size_t)it.ntile * 2 + wg;
+                    sw0 = (it.shared ? a.ss_down : a.s_down) + r * Kb;
+                    sw1 = sw0;
+                }
             }
+            // raw scales of the next K block, loaded one block ahead of their use
+            float nx = __ldg(sxp), nw0 = __ldg(sw0), nw1 = gateup ? __ldg(sw1) : 0.f;
+
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.f;
-            const int sx_off = it.row0 - (it.row0 & ~3) + row;
+
             for (int kb = 0; kb < Kb; ++kb, ++n) {
-                const int s = (int)(n % kGStages);
-                const int b = (int)(n & 1);
-                if (ok && !mbar_wait_bounded(&acc_full[b], (n >> 1) & 1, kPolls)) ok = false;
-                if (ok && !mbar_wait_bounded(&full[s], (n / kGStages) & 1, kPolls)) ok = false;
+                const int b = n & 1;
+                const float c0 = nx * nw0, c1 = gateup ? nx * nw1 : c0;
+                if (kb + 1 < Kb) {
+                    nx = __ldg(sxp + kb + 1);
+                    nw0 = __ldg(sw0 + kb + 1);
+                    if (gateup) nw1 = __ldg(sw1 + kb + 1);
+                }
+                if (ok && !mbar_wait_bounded(&acc_full[b], (n >> 1) & 1)) ok = false;
+                // tcgen05.ld is warp-collective: the whole warp reads, or none of it
+                ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
-                const float sx = ok ? reinterpret_cast<const float*>(smem + s * kStageBytes + kSA + kSB)[sx_off] : 0.f;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                const float c0 = sx * __ldg(sw0 + kb);
-                const float c1 = sx * __ldg(sw1 + kb);
                 if (ok) {
-                    const uint32_t tb = tmem + lane_off + (uint32_t)(b * kGN);
+                    const uint32_t tb = t_row + (uint32_t)(b * kGN);
 #pragma unroll
                     for (int h = 0; h < 8; ++h) {
                         // gate/up: chunks 0-3 = gate cols 64wg.., chunks 4-7 = up cols 128+64wg..
@@ -267,13 +299,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (lane == 0) mbar_arrive(&acc_empty[b]);
             }
             if (!ok) set_status(a.status, kStatusTimeout);
-            // after a timeout this warp still takes every named barrier below (its sibling
-            // warpgroup waits there) but writes nothing
-            const bool valid = ok && row < it.nrows;
-            const int grow = it.row0 + row;  // row in the output tensors
+            // after a timeout every warp still takes the named barriers below, but writes nothing
+            const bool valid = ok && valid_row;
+            const Item it = decode_item(a, n_mt_r, item);
             if (gateup) {
-                // a = SiLU(g) * u for 64 intermediate channels; the 128-channel scale
-                // block spans both warpgroups: combine their maxima through shared memory
+                // a = SiLU(g) * u for 64 intermediate channels; the 128-channel scale block
+                // spans both column halves: combine their maxima through shared memory
                 float amax = 0.f;
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
@@ -301,11 +332,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                                           acc[16 * c + 15] * inv);
                         reinterpret_cast<uint4*>(dst)[c] = w;
                     }
-                    if (wg == 0) {  // transposed scales: [I/128][rows] (the down GEMM's TMA layout)
-                        float* hsT = it.shared ? a.hsT_s : a.hsT_r;
-                        const long ld = it.shared ? a.ld_s : a.ld_r;
-                        hsT[(size_t)it.ntile * ld + grow] = scale;
-                    }
+                    if (wg == 0)  // row-major [rows, N/128]: the down GEMM's activation scales
+                        (it.shared ? a.hs_s : a.hs_r)[(size_t)grow * (N / kBlk) + it.ntile] = scale;
                 }
                 named_bar(1, kEpiWarps * 32);  // s_amax is reused by the next tile
             } else if (valid) {
@@ -314,7 +342,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     const int f = a.perm_src[grow];
                     wrow = ((unsigned)f < (unsigned)(a.T * a.k)) ? a.topk_w[f] : 0.f;
                 }
-                __nv_bfloat16* dst = (it.shared ? a.y_shared : a.y_perm) + (size_t)grow * a.H + it.ntile * kGN + 128 * wg;
+                __nv_bfloat16* dst =
+                    (it.shared ? a.y_shared : a.y_perm) + (size_t)grow * a.H + it.ntile * kGN + 128 * wg;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     uint4 o;
@@ -343,10 +372,8 @@ size_t gemm_smem() { return (size_t)kGStages * kStageBytes + 1024 + 2 * kGStages
 }  // namespace
 
 bool gemm_supported(const moe_config_t& c) {
-    // 256-row down tiles, whole 128-row intermediate tiles, and the scale rows of a
-    // K block must fit the epilogue's per-lane registers (K <= 256 blocks)
-    const int Is = c.n_shared * c.moe_inter;
-    return c.hidden % kGN == 0 && c.hidden / kBlk <= 256 && c.moe_inter / kBlk <= 256 && Is / kBlk <= 256;
+    // 256-row down tiles; intermediate tiles are whole 128-row blocks by the ABI's checks
+    return c.hidden % kGN == 0;
 }
 
 cudaError_t launch_expert_gemm(const GemmArgs& g, const TmaMaps& m, cudaStream_t st) {
@@ -370,7 +397,7 @@ cudaError_t launch_expert_gemm(const GemmArgs& g, const TmaMaps& m, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, g, m.a_r, m.a_s, m.b0_r, m.b1_r, m.b0_s, m.b1_s, m.sx_r, m.sx_s);
+    return cudaLaunchKernelEx(&cfg, kern, g, m.a_r, m.a_s, m.b0_r, m.b1_r, m.b0_s, m.b1_s);
 }
 
 }  // namespace moe

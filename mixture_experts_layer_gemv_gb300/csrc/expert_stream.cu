@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int left = (int)(ts.start(t) + ts.len(t) - rg.u0);  // units left in the current tile
         int s = 0, ph = 0;
         for (long u = rg.u0; u < rg.u1; ++u) {
-            if (u - rg.u0 >= S && !mbar_wait_bounded(&empty[s], ph ^ 1, kWaitPolls)) {
+            if (u - rg.u0 >= S && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
                 set_status(a.status, kStatusTimeout);
                 break;
             }
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sx1 = xs1 ? __ldg(xs1 + kb) : 0.f;
         // after a timed-out wait this warp keeps walking the units (so its control flow
         // matches its siblings') but waits for and computes nothing more
-        if (!failed && !mbar_wait_bounded(&full[s], ph, kWaitPolls)) {
+        if (!failed && !mbar_wait_bounded(&full[s], ph)) {
             set_status(a.status, kStatusTimeout);
             failed = true;
         }
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int left = (int)(ts.start(t) + ts.len(t) - rg.u0);
             int s = 0, ph = 0;
             for (long u = rg.u0; u < rg.u1; ++u) {
-                if (u - rg.u0 >= S && !mbar_wait_bounded(&empty[s], ph ^ 1, kWaitPolls)) {
+                if (u - rg.u0 >= S && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
                     set_status(a.status, kStatusTimeout);
                     break;
                 }
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nsb = Nmax / kBlk;
         const float sx0 = s_hs[(2 * t4) * nsb + kb];
         const float sx1 = s_hs[(2 * t4 + 1) * nsb + kb];
-        if (!failed && !mbar_wait_bounded(&full[s], ph, kWaitPolls)) {
+        if (!failed && !mbar_wait_bounded(&full[s], ph)) {
             set_status(a.status, kStatusTimeout);
             failed = true;  // keep walking the units so every named barrier is still reached
         }

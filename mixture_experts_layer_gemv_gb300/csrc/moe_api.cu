@@ -86,21 +86,15 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     L.y_s = take(P * t * H * 4);
     L.yb_s = take(P * t * H * 4);
     }
-    L.ld_r = L.ld_s = 0;
     L.max_mtiles = 0;
-    L.xq_perm = L.xsT_r = L.xsT_s = L.hq_r = L.hq_s = L.hsT_r = L.hsT_s = L.mtiles = 0;
+    L.xq_perm = L.hq_r = L.hq_s = L.hs_r = L.hs_s = L.mtiles = 0;
     if (gemm) {
-        const size_t Hb = H / 128, Ib = I / 128, Isb = Is / 128;
-        L.ld_r = (long)((t * k + 3) & ~size_t(3));  // 16-byte rows for the scale tensor maps
-        L.ld_s = (long)((t + 3) & ~size_t(3));
         L.max_mtiles = (int)((t * k + 127) / 128 + std::min(E, t * k));
         L.xq_perm = take(t * k * H);
-        L.xsT_r = take(Hb * L.ld_r * 4);
-        L.xsT_s = take(Hb * L.ld_s * 4);
         L.hq_r = take(t * k * I);
         L.hq_s = take(t * Is);
-        L.hsT_r = take(Ib * L.ld_r * 4);
-        L.hsT_s = take(Isb * L.ld_s * 4);
+        L.hs_r = take(t * k * (I / 128) * 4);
+        L.hs_s = take(t * (Is / 128) * 4);
         L.mtiles = take((size_t)L.max_mtiles * sizeof(MTile));
     }
     L.y_perm = take(t * k * H * 2);
@@ -253,12 +247,11 @@ cudaError_t run_expert_gemms(const moe_config_t* c, int32_t T, const moe_weights
     g.T = T;
     g.k = k;
     g.n_mt_s = sh ? (T + 127) / 128 : 0;
-    g.ld_r = L.ld_r;
-    g.ld_s = L.ld_s;
     g.ctrl = at<Ctrl>(ws, L.ctrl);
     g.mtiles = at<MTile>(ws, L.mtiles);
     g.perm_src = perm_src;
     g.topk_w = topk_w;
+    g.xs = at<float>(ws, L.xs);
     g.s_gate = W->s_gate;
     g.s_up = W->s_up;
     g.s_down = W->s_down;
@@ -267,8 +260,8 @@ cudaError_t run_expert_gemms(const moe_config_t* c, int32_t T, const moe_weights
     g.ss_down = W->ss_down;
     g.hq_r = at<uint8_t>(ws, L.hq_r);
     g.hq_s = at<uint8_t>(ws, L.hq_s);
-    g.hsT_r = at<float>(ws, L.hsT_r);
-    g.hsT_s = at<float>(ws, L.hsT_s);
+    g.hs_r = at<float>(ws, L.hs_r);
+    g.hs_s = at<float>(ws, L.hs_s);
     g.y_perm = y_perm;
     g.y_shared = y_shared;
     g.status = &at<Ctrl>(ws, L.ctrl)->status;
@@ -281,13 +274,11 @@ cudaError_t run_expert_gemms(const moe_config_t* c, int32_t T, const moe_weights
     g.nt_s = Is / 128;
     if (!tmap_u8_2d(&m.a_r, at<uint8_t>(ws, L.xq_perm), n, H, 128, 128) ||
         !tmap_u8_2d(&m.b0_r, W->w_gate, (uint64_t)E * I, H, 128, 128) ||
-        !tmap_u8_2d(&m.b1_r, W->w_up, (uint64_t)E * I, H, 128, 128) ||
-        !tmap_f32_2d(&m.sx_r, at<float>(ws, L.xsT_r), H / 128, n, L.ld_r, 132, 1))
+        !tmap_u8_2d(&m.b1_r, W->w_up, (uint64_t)E * I, H, 128, 128))
         return cudaErrorInvalidValue;
     if (sh && (!tmap_u8_2d(&m.a_s, at<uint8_t>(ws, L.xq), T, H, 128, 128) ||
                !tmap_u8_2d(&m.b0_s, W->ws_gate, Is, H, 128, 128) ||
-               !tmap_u8_2d(&m.b1_s, W->ws_up, Is, H, 128, 128) ||
-               !tmap_f32_2d(&m.sx_s, at<float>(ws, L.xsT_s), H / 128, T, L.ld_s, 132, 1)))
+               !tmap_u8_2d(&m.b1_s, W->ws_up, Is, H, 128, 128)))
         return cudaErrorInvalidValue;
     if (mark->begin(MOE_STAGE_GATE_UP) != MOE_OK) return cudaErrorUnknown;
     cudaError_t e = launch_expert_gemm(g, m, st);
@@ -301,12 +292,10 @@ cudaError_t run_expert_gemms(const moe_config_t* c, int32_t T, const moe_weights
     g.nt_r = g.nt_s = H / 256;
     m = TmaMaps{};
     if (!tmap_u8_2d(&m.a_r, g.hq_r, n, I, 128, 128) ||
-        !tmap_u8_2d(&m.b0_r, W->w_down, (uint64_t)E * H, I, 128, 128) ||
-        !tmap_f32_2d(&m.sx_r, g.hsT_r, I / 128, n, L.ld_r, 132, 1))
+        !tmap_u8_2d(&m.b0_r, W->w_down, (uint64_t)E * H, I, 128, 128))
         return cudaErrorInvalidValue;
     m.b1_r = m.b0_r;
-    if (sh && (!tmap_u8_2d(&m.a_s, g.hq_s, T, Is, 128, 128) || !tmap_u8_2d(&m.b0_s, W->ws_down, H, Is, 128, 128) ||
-               !tmap_f32_2d(&m.sx_s, g.hsT_s, Is / 128, T, L.ld_s, 132, 1)))
+    if (sh && (!tmap_u8_2d(&m.a_s, g.hq_s, T, Is, 128, 128) || !tmap_u8_2d(&m.b0_s, W->ws_down, H, Is, 128, 128)))
         return cudaErrorInvalidValue;
     m.b1_s = m.b0_s;
     if (mark->begin(MOE_STAGE_DOWN) != MOE_OK) return cudaErrorUnknown;
@@ -422,10 +411,8 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_bf16, int32_t
     if (use_gemm(*cfg, T)) {
         MOE_CUDA(launch_build_groups(*cfg, expert_offsets, T * cfg->top_k, nullptr, nullptr, at<MTile>(ws, L.mtiles),
                                      at<Ctrl>(ws, L.ctrl), st));
-        MOE_CUDA(launch_gather_rows(T, cfg->hidden, cfg->top_k, perm_src, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
-                                    at<uint8_t>(ws, L.xq_perm), at<float>(ws, L.xsT_r), L.ld_r,
-                                    cfg->n_shared > 0 ? at<float>(ws, L.xsT_s) : nullptr, L.ld_s,
-                                    &at<Ctrl>(ws, L.ctrl)->status, st));
+        MOE_CUDA(launch_gather_rows(T, cfg->hidden, cfg->top_k, perm_src, at<uint8_t>(ws, L.xq),
+                                    at<uint8_t>(ws, L.xq_perm), &at<Ctrl>(ws, L.ctrl)->status, st));
         const StageMark mark{nullptr, st};
         MOE_CUDA(run_expert_gemms(cfg, T, weights, L, ws, perm_src, topk_w, static_cast<__nv_bfloat16*>(y_perm_bf16),
                                   static_cast<__nv_bfloat16*>(y_shared_bf16), &mark));
@@ -500,9 +487,7 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
             MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, nullptr, nullptr,
                                     at<MTile>(ws, L.mtiles), ctrl, st));
             MOE_CUDA(launch_gather_rows(T, cfg->hidden, cfg->top_k, perm_src, at<uint8_t>(ws, L.xq),
-                                        at<float>(ws, L.xs), at<uint8_t>(ws, L.xq_perm), at<float>(ws, L.xsT_r),
-                                        L.ld_r, cfg->n_shared > 0 ? at<float>(ws, L.xsT_s) : nullptr, L.ld_s,
-                                        &ctrl->status, st));
+                                        at<uint8_t>(ws, L.xq_perm), &ctrl->status, st));
             MOE_TRY(mark.end(MOE_STAGE_PERMUTE));
             __nv_bfloat16* y_perm = at<__nv_bfloat16>(ws, L.y_perm);
             __nv_bfloat16* y_shared = cfg->n_shared > 0 ? at<__nv_bfloat16>(ws, L.y_shared) : nullptr;

@@ -66,11 +66,9 @@ struct WsLayout {
     size_t y_r, yb_r;             // fp32 [P][T*k, H] each
     size_t y_s, yb_s;             // fp32 [P][T, H] each
     size_t xq_perm;    // u8 [T*k, H]                 (grouped GEMM path)
-    size_t xsT_r, xsT_s; // fp32 [H/128][ld_r], [H/128][ld_s]
     size_t hq_r, hq_s;   // u8 [T*k, I], [T, Is]
-    size_t hsT_r, hsT_s; // fp32 [I/128][ld_r], [Is/128][ld_s]
+    size_t hs_r, hs_s;   // fp32 [T*k, I/128], [T, Is/128]
     size_t mtiles;       // MTile [max_mtiles]
-    long ld_r, ld_s;
     int max_mtiles;
     size_t y_perm;     // bf16 [T*k, H]
     size_t y_shared;   // bf16 [T, H]
@@ -161,33 +159,27 @@ struct GemmArgs {
     int K_r, K_s;      // reduction length of routed / shared tiles
     int nt_r, nt_s;    // weight tiles per token tile (routed / shared)
     int n_mt_s;        // shared token tiles
-    long ld_r, ld_s;   // leading dimension of the transposed scale arrays
     const Ctrl* ctrl;
     const MTile* mtiles;
     const int32_t* perm_src;
     const float* topk_w;
+    const float* xs;   // activation scales [T, H/128] (token order)
     const float *s_gate, *s_up, *s_down, *ss_gate, *ss_up, *ss_down;
     uint8_t *hq_r, *hq_s;   // FP8 intermediate (gate/up output, down input)
-    float *hsT_r, *hsT_s;   // its scales, transposed [blocks][rows]
+    float *hs_r, *hs_s;     // its scales, row-major [rows, width/128]
     __nv_bfloat16* y_perm;
     __nv_bfloat16* y_shared;
     int* status;
 };
 struct TmaMaps {
-    TmaMap a_r, a_s, b0_r, b1_r, b0_s, b1_s, sx_r, sx_s;
+    TmaMap a_r, a_s, b0_r, b1_r, b0_s, b1_s;
 };
 bool gemm_supported(const moe_config_t& c);
 cudaError_t launch_expert_gemm(const GemmArgs& g, const TmaMaps& m, cudaStream_t st);
-// 2-D tensor map of a row-major fp32 [rows, cols] array with leading dimension ld (elements),
-// box of box_rows x box_cols, no swizzle.
-bool tmap_f32_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_cols,
-                 uint32_t box_rows);
-// xq_perm[r] = xq[token of r], xsT_r[kb][r] = xs[token of r][kb] for the routed rows and
-// xsT_s[kb][t] = xs[t][kb] for the shared experts' rows (skipped when xsT_s is null).
-// A row whose perm_src entry is outside [0, T*k) is written as zeros and sets kStatusBadId.
-cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, const float* xs,
-                               uint8_t* xq_perm, float* xsT_r, long ld_r, float* xsT_s, long ld_s, int* status,
-                               cudaStream_t st);
+// xq_perm[r] = xq[token of r] (the routed rows in expert order). A row whose perm_src
+// entry is outside [0, T*k) is written as zeros and sets kStatusBadId.
+cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, uint8_t* xq_perm,
+                               int* status, cudaStream_t st);
 
 int stream_grid();
 int down_stages(int I, int Is);

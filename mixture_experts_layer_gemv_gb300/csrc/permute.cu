@@ -216,68 +216,21 @@ __global__ void __launch_bounds__(256) build_groups_kernel(BuildGroupsParams p) 
     }
 }
 
-// Rows of the grouped GEMM's operands in permuted order (see launch_gather_rows).
+// Activation-code rows of the grouped GEMM in permuted order: one warp per row.
 constexpr int kGatherRows = 32;
-constexpr int kMaxHb = 256;
 
-struct GatherParams {
-    int T, H, k, n_blocks_r;
-    const int32_t* perm_src;
-    const uint8_t* xq;
-    const float* xs;
-    uint8_t* xq_perm;
-    float* xsT_r;
-    long ld_r;
-    float* xsT_s;
-    long ld_s;
-    int* status;
-};
-
-__global__ void __launch_bounds__(256) gather_rows_kernel(GatherParams p) {
-    __shared__ float s_sc[kMaxHb][kGatherRows + 1];
-    __shared__ int s_tok[kGatherRows];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool shared = (int)blockIdx.x >= p.n_blocks_r;
-    const long r0 = (long)(shared ? (int)blockIdx.x - p.n_blocks_r : (int)blockIdx.x) * kGatherRows;
-    const long n = shared ? p.T : (long)p.T * p.k;
-    const int Hb = p.H / kBlk;
-    if (tid < kGatherRows) {
-        const long r = r0 + tid;
-        int tok = -1;
-        if (r < n) {
-            if (shared) {
-                tok = (int)r;
-            } else {
-                const int f = p.perm_src[r];
-                if ((unsigned)f < (unsigned)n)
-                    tok = f / p.k;
-                else
-                    set_status(p.status, kStatusBadId);
-            }
-        }
-        s_tok[tid] = tok;
-    }
-    __syncthreads();
-    if (!shared) {  // the shared experts read the activation codes in token order
-        const int H16 = p.H / 16;
-        for (int i = warp; i < kGatherRows && r0 + i < n; i += 8) {
-            const int tok = s_tok[i];
-            uint4* dst = reinterpret_cast<uint4*>(p.xq_perm + (size_t)(r0 + i) * p.H);
-            const uint4* src = reinterpret_cast<const uint4*>(p.xq + (size_t)(tok < 0 ? 0 : tok) * p.H);
-            for (int c = lane; c < H16; c += 32) dst[c] = tok >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        }
-    }
-    for (int i = tid; i < kGatherRows * Hb; i += blockDim.x) {
-        const int rr = i / Hb, kb = i % Hb;
-        const int tok = s_tok[rr];
-        s_sc[kb][rr] = tok >= 0 ? p.xs[(size_t)tok * Hb + kb] : 0.f;
-    }
-    __syncthreads();
-    float* dstT = shared ? p.xsT_s : p.xsT_r;
-    const long ld = shared ? p.ld_s : p.ld_r;
-    for (int i = tid; i < kGatherRows * Hb; i += blockDim.x) {
-        const int kb = i / kGatherRows, rr = i % kGatherRows;
-        if (r0 + rr < n) dstT[kb * ld + r0 + rr] = s_sc[kb][rr];
+__global__ void __launch_bounds__(256) gather_rows_kernel(int T, int H, int k, const int32_t* perm_src,
+                                                          const uint8_t* xq, uint8_t* xq_perm, int* status) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long n = (long)T * k;
+    const int H16 = H / 16;
+    for (long r = (long)blockIdx.x * kGatherRows + warp; r < n && r < (long)(blockIdx.x + 1) * kGatherRows; r += 8) {
+        const int f = perm_src[r];
+        const bool good = (unsigned)f < (unsigned)n;
+        if (!good && lane == 0) set_status(status, kStatusBadId);
+        const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)(good ? f / k : 0) * H);
+        uint4* dst = reinterpret_cast<uint4*>(xq_perm + (size_t)r * H);
+        for (int c = lane; c < H16; c += 32) dst[c] = good ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -315,26 +268,12 @@ cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, i
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, const float* xs,
-                               uint8_t* xq_perm, float* xsT_r, long ld_r, float* xsT_s, long ld_s, int* status,
-                               cudaStream_t st) {
-    if (H / kBlk > kMaxHb) return cudaErrorInvalidValue;
-    GatherParams p;
-    p.T = T;
-    p.H = H;
-    p.k = k;
-    p.n_blocks_r = (int)(((long)T * k + kGatherRows - 1) / kGatherRows);
-    p.perm_src = perm_src;
-    p.xq = xq;
-    p.xs = xs;
-    p.xq_perm = xq_perm;
-    p.xsT_r = xsT_r;
-    p.ld_r = ld_r;
-    p.xsT_s = xsT_s;
-    p.ld_s = ld_s;
-    p.status = status;
-    const int n_blocks_s = xsT_s ? (T + kGatherRows - 1) / kGatherRows : 0;
-    gather_rows_kernel<<<p.n_blocks_r + n_blocks_s, 256, 0, st>>>(p);
+cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, uint8_t* xq_perm,
+                               int* status, cudaStream_t st) {
+    const long n = (long)T * k;
+    if (n == 0) return cudaSuccess;
+    gather_rows_kernel<<<(unsigned)((n + kGatherRows - 1) / kGatherRows), 256, 0, st>>>(T, H, k, perm_src, xq,
+                                                                                        xq_perm, status);
     return cudaGetLastError();
 }
 

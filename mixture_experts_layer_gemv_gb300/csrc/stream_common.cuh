@@ -20,7 +20,6 @@ constexpr int kBox = kTile * kBlk;          // 16 KB: 128 rows x 128 bytes
 constexpr int kBRows = kGroupRows * kBlk;   // 1 KB: the unit's activation rows
 constexpr int kStagesGU = 5;
 constexpr int kMaxStagesD = 10;
-constexpr uint32_t kWaitPolls = 1u << 22;
 
 // The unit sequence of a stage. Output rows come in "rows" of 128 (row group x 128-row
 // slice): n_r routed rows with kc_r K blocks each, then n_s shared rows with kc_s.

@@ -75,10 +75,5 @@ bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uin
     return encode_2d(out, base, rows, cols, cols, box_cols, box_rows, false);
 }
 
-// fp32 [rows, cols] with row pitch ld elements, no swizzle; reads beyond cols or rows return zeros
-bool tmap_f32_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_cols,
-                 uint32_t box_rows) {
-    return encode_2d(out, base, rows, cols, ld * 4, box_cols, box_rows, true);
-}
 
 }  // namespace moe
