@@ -111,148 +111,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (blockIdx.x >= pl.nb || rg.u1 <= rg.u0) return;
     const Partials pt{{a.g_r, a.u_r}, {a.gb_r, a.ub_r}, (long)a.T * a.k, a.I};
     const Partials pts{{a.g_s, a.u_s}, {a.gb_s, a.ub_s}, (long)a.T, a.Is};
+    // this CTA's tiles, with the token of every activation row
+    __shared__ TileRec s_tab[kMaxTab];
+    const int ntiles = build_table(s_tab, ts, rg, slices_r, slices_s, a.groups, a.T, a.k, a.perm_src, nullptr,
+                                   tid, kThreads);
+    __syncthreads();
+    auto rec = [&](int i) {
+        return i < kMaxTab ? s_tab[i]
+                           : make_rec(ts, rg, rg.first_tile + i, slices_r, slices_s, a.groups, a.T, a.k, a.perm_src,
+                                      nullptr);
+    };
 
     if (warp == kCons) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        long cur = -1;
-        TileInfo ti{};
-        const uint8_t* xrow[kGroupRows];
-        long t = rg.first_tile;
-        int kb = rg.kb0;
-        int left = (int)(ts.start(t) + ts.len(t) - rg.u0);  // units left in the current tile
         int s = 0, ph = 0;
-        for (long u = rg.u0; u < rg.u1; ++u) {
-            if (u - rg.u0 >= S && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
-                set_status(a.status, kStatusTimeout);
-                break;
-            }
-            if (t != cur) {
-                cur = t;
-                ti = decode_tile(ts, t, slices_r, slices_s, a.groups, a.T);
-                for (int c = 0; c < kGroupRows; ++c) {
-                    int tok = -1;
-                    if (c < ti.nrows) {
-                        if (ti.shared) {
-                            tok = ti.row_begin + c;
-                        } else {
-                            const int f = a.perm_src[ti.row_begin + c];
-                            tok = ((unsigned)f < (unsigned)(a.T * a.k)) ? f / a.k : -1;
-                        }
-                    }
-                    xrow[c] = tok >= 0 ? a.xq + (size_t)tok * H : nullptr;
-                }
-            }
-            uint8_t* st = smem + s * SB;
+        long q = 0;  // units issued
+        bool stop = false;
+        for (int i = 0; i < ntiles && !stop; ++i) {
+            const TileRec r = rec(i);
+            const uint8_t* xrow[kGroupRows];
             int nrow = 0;
-            for (int c = 0; c < ti.nrows; ++c) nrow += xrow[c] != nullptr;
-            mbar_arrive_expect_tx(&full[s], 2 * kBox + nrow * kBlk);
-            const int y = ti.shared ? ti.slice * kTile : ti.expert * a.I + ti.slice * kTile;
-            tma_load_2d(st, ti.shared ? (const void*)&tm_sg : (const void*)&tm_g, kb * kBlk, y, &full[s]);
-            tma_load_2d(st + kBox, ti.shared ? (const void*)&tm_su : (const void*)&tm_u, kb * kBlk, y, &full[s]);
-            for (int c = 0; c < ti.nrows; ++c)
-                if (xrow[c]) bulk_load(st + 2 * kBox + c * kBlk, xrow[c] + kb * kBlk, kBlk, &full[s]);
-            ++kb;
-            if (--left == 0) {
-                ++t;
-                if (u + 1 < rg.u1) {
-                    left = ts.len(t);
-                    const long stt = ts.start(t);
-                    int kbn;
-                    ts.tile_of(stt, &kbn);
-                    kb = kbn;
-                }
+#pragma unroll
+            for (int c = 0; c < kGroupRows; ++c) {
+                xrow[c] = r.tok[c] >= 0 ? a.xq + (size_t)r.tok[c] * H : nullptr;
+                nrow += xrow[c] != nullptr;
             }
-            if (++s == S) {
-                s = 0;
-                ph ^= 1;
+            const int y = r.shared ? r.slice * kTile : r.expert * a.I + r.slice * kTile;
+            const void* mg = r.shared ? (const void*)&tm_sg : (const void*)&tm_g;
+            const void* mu = r.shared ? (const void*)&tm_su : (const void*)&tm_u;
+            for (int j = 0; j < r.n; ++j, ++q) {
+                if (q >= S && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
+                    set_status(a.status, kStatusTimeout);
+                    stop = true;
+                    break;
+                }
+                const int kb = r.kb0 + j;
+                uint8_t* st = smem + s * SB;
+                mbar_arrive_expect_tx(&full[s], 2 * kBox + nrow * kBlk);
+                tma_load_2d(st, mg, kb * kBlk, y, &full[s]);
+                tma_load_2d(st + kBox, mu, kb * kBlk, y, &full[s]);
+#pragma unroll
+                for (int c = 0; c < kGroupRows; ++c)
+                    if (xrow[c]) bulk_load(st + 2 * kBox + c * kBlk, xrow[c] + kb * kBlk, kBlk, &full[s]);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
+                }
             }
         }
         return;  // the consumers wait for every copy issued here before the CTA exits
     }
 
     // ---------------------------------------------------------------- consumers
-    float acc[2][4] = {};
-    long cur = -1;
-    TileInfo ti{};
-    const float *sgr = nullptr, *sur = nullptr, *xs0 = nullptr, *xs1 = nullptr;
     bool failed = false;
-    long t = rg.first_tile;
-    int kb = rg.kb0;
-    int left = (int)(ts.start(t) + ts.len(t) - rg.u0);
     int s = 0, ph = 0;
-    for (long u = rg.u0; u < rg.u1; ++u) {
-        if (t != cur) {
-            cur = t;
-            ti = decode_tile(ts, t, slices_r, slices_s, a.groups, a.T);
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[m][j] = 0.f;
-            if (ti.shared) {
-                sgr = a.ss_gate + (size_t)ti.slice * Hb;
-                sur = a.ss_up + (size_t)ti.slice * Hb;
-            } else {
-                const size_t e = (size_t)ti.expert;
-                sgr = a.s_gate + (e * (a.I / kBlk) + ti.slice) * Hb;
-                sur = a.s_up + (e * (a.I / kBlk) + ti.slice) * Hb;
+    for (int i = 0; i < ntiles; ++i) {
+        const TileRec r = rec(i);
+        const float *sgr, *sur;
+        if (r.shared) {
+            sgr = a.ss_gate + (size_t)r.slice * Hb;
+            sur = a.ss_up + (size_t)r.slice * Hb;
+        } else {
+            const size_t e = (size_t)r.expert;
+            sgr = a.s_gate + (e * (a.I / kBlk) + r.slice) * Hb;
+            sur = a.s_up + (e * (a.I / kBlk) + r.slice) * Hb;
+        }
+        const int tok0 = r.tok[2 * t4], tok1 = r.tok[2 * t4 + 1];
+        const float* xs0 = tok0 >= 0 ? a.xs + (size_t)tok0 * Hb : nullptr;
+        const float* xs1 = tok1 >= 0 ? a.xs + (size_t)tok1 * Hb : nullptr;
+        float acc[2][4] = {};
+        for (int j = 0; j < r.n; ++j) {
+            const int kb = r.kb0 + j;
+            const float swg = __ldg(sgr + kb), swu = __ldg(sur + kb);
+            const float sx0 = xs0 ? __ldg(xs0 + kb) : 0.f;
+            const float sx1 = xs1 ? __ldg(xs1 + kb) : 0.f;
+            // after a timed-out wait this warp keeps walking the units (so its control flow
+            // matches its siblings') but waits for and computes nothing more
+            if (!failed && !mbar_wait_bounded(&full[s], ph)) {
+                set_status(a.status, kStatusTimeout);
+                failed = true;
             }
-            int tok[2] = {-1, -1};
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int c = 2 * t4 + q;
-                if (c < ti.nrows) {
-                    if (ti.shared) {
-                        tok[q] = ti.row_begin + c;
-                    } else {
-                        const int f = a.perm_src[ti.row_begin + c];
-                        tok[q] = ((unsigned)f < (unsigned)(a.T * a.k)) ? f / a.k : -1;
-                    }
-                }
+            const uint8_t* st = smem + s * SB;
+            float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+            if (!failed) {
+                box_dot(cg, st, st + 2 * kBox + g * kBlk, warp, g, t4);
+                box_dot(cu, st + kBox, st + 2 * kBox + g * kBlk, warp, g, t4);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
             }
-            xs0 = tok[0] >= 0 ? a.xs + (size_t)tok[0] * Hb : nullptr;
-            xs1 = tok[1] >= 0 ? a.xs + (size_t)tok[1] * Hb : nullptr;
-        }
-        const float swg = __ldg(sgr + kb), swu = __ldg(sur + kb);
-        const float sx0 = xs0 ? __ldg(xs0 + kb) : 0.f;
-        const float sx1 = xs1 ? __ldg(xs1 + kb) : 0.f;
-        // after a timed-out wait this warp keeps walking the units (so its control flow
-        // matches its siblings') but waits for and computes nothing more
-        if (!failed && !mbar_wait_bounded(&full[s], ph)) {
-            set_status(a.status, kStatusTimeout);
-            failed = true;
-        }
-        const uint8_t* st = smem + s * SB;
-        float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
-        if (!failed) {
-            box_dot(cg, st, st + 2 * kBox + g * kBlk, warp, g, t4);
-            box_dot(cu, st + kBox, st + 2 * kBox + g * kBlk, warp, g, t4);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-        }
-        acc[0][0] = fmaf(cg[0], swg * sx0, acc[0][0]);
-        acc[0][1] = fmaf(cg[1], swg * sx1, acc[0][1]);
-        acc[0][2] = fmaf(cg[2], swg * sx0, acc[0][2]);
-        acc[0][3] = fmaf(cg[3], swg * sx1, acc[0][3]);
-        acc[1][0] = fmaf(cu[0], swu * sx0, acc[1][0]);
-        acc[1][1] = fmaf(cu[1], swu * sx1, acc[1][1]);
-        acc[1][2] = fmaf(cu[2], swu * sx0, acc[1][2]);
-        acc[1][3] = fmaf(cu[3], swu * sx1, acc[1][3]);
-        ++kb;
-        if (--left == 0 || u + 1 == rg.u1) {  // end of this CTA's share of tile t
-            if (!failed) store_tile<2>(acc, ts, rg, t, ti, ti.shared ? pts : pt);
-            if (left == 0 && u + 1 < rg.u1) {
-                ++t;
-                left = ts.len(t);
-                int kbn;
-                ts.tile_of(ts.start(t), &kbn);
-                kb = kbn;
+            acc[0][0] = fmaf(cg[0], swg * sx0, acc[0][0]);
+            acc[0][1] = fmaf(cg[1], swg * sx1, acc[0][1]);
+            acc[0][2] = fmaf(cg[2], swg * sx0, acc[0][2]);
+            acc[0][3] = fmaf(cg[3], swg * sx1, acc[0][3]);
+            acc[1][0] = fmaf(cu[0], swu * sx0, acc[1][0]);
+            acc[1][1] = fmaf(cu[1], swu * sx1, acc[1][1]);
+            acc[1][2] = fmaf(cu[2], swu * sx0, acc[1][2]);
+            acc[1][3] = fmaf(cu[3], swu * sx1, acc[1][3]);
+            if (++s == S) {
+                s = 0;
+                ph ^= 1;
             }
         }
-        if (++s == S) {
-            s = 0;
-            ph ^= 1;
-        }
+        if (!failed) store_rec<2>(acc, r, r.shared ? pts : pt);
     }
 }
 
@@ -286,46 +247,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // The work list comes from the router, which completed before the gate/up kernel
     // (this kernel's predecessor) got past its own wait; down weights depend on nothing
-    // else, so the producer streams them before the gate/up results exist.
+    // else, so the tile table is built and the producer streams weights before the
+    // gate/up results exist.
     const Plan pl = down_plan(a);
     const TileSpace ts = down_space(a, pl.P);
     const Range rg = make_range(ts, pl.nb, blockIdx.x);
     const bool active = blockIdx.x < pl.nb && rg.u1 > rg.u0;
+    __shared__ TileRec s_tab[kMaxTab];
+    const int ntiles = active ? build_table(s_tab, ts, rg, slices, slices, a.groups, a.T, a.k, a.perm_src,
+                                            a.topk_w, tid, kThreads)
+                              : 0;
+    __syncthreads();
+    auto rec = [&](int i) {
+        return i < kMaxTab ? s_tab[i]
+                           : make_rec(ts, rg, rg.first_tile + i, slices, slices, a.groups, a.T, a.k, a.perm_src,
+                                      a.topk_w);
+    };
 
     if (warp == kCons) {
         if (lane == 0 && active) {
             prefetch_tmap(&tm_d);
             if (a.Is > 0) prefetch_tmap(&tm_sd);
-            long cur = -1;
-            TileInfo ti{};
-            long t = rg.first_tile;
-            int kb = rg.kb0;
-            int left = (int)(ts.start(t) + ts.len(t) - rg.u0);
             int s = 0, ph = 0;
-            for (long u = rg.u0; u < rg.u1; ++u) {
-                if (u - rg.u0 >= S && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
-                    set_status(a.status, kStatusTimeout);
-                    break;
-                }
-                if (t != cur) {
-                    cur = t;
-                    ti = decode_tile(ts, t, slices, slices, a.groups, a.T);
-                }
-                mbar_arrive_expect_tx(&full[s], kBox);
-                const int y = ti.shared ? ti.slice * kTile : ti.expert * H + ti.slice * kTile;
-                tma_load_2d(smem + s * SB, ti.shared ? (const void*)&tm_sd : (const void*)&tm_d, kb * kBlk, y,
-                            &full[s]);
-                ++kb;
-                if (--left == 0 && u + 1 < rg.u1) {
-                    ++t;
-                    left = ts.len(t);
-                    int kbn;
-                    ts.tile_of(ts.start(t), &kbn);
-                    kb = kbn;
-                }
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1;
+            long q = 0;  // units issued
+            bool stop = false;
+            for (int i = 0; i < ntiles && !stop; ++i) {
+                const TileRec r = rec(i);
+                const int y = r.shared ? r.slice * kTile : r.expert * H + r.slice * kTile;
+                const void* md = r.shared ? (const void*)&tm_sd : (const void*)&tm_d;
+                for (int j = 0; j < r.n; ++j, ++q) {
+                    if (q >= S && !mbar_wait_bounded(&empty[s], ph ^ 1)) {
+                        set_status(a.status, kStatusTimeout);
+                        stop = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], kBox);
+                    tma_load_2d(smem + s * SB, md, (r.kb0 + j) * kBlk, y, &full[s]);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1;
+                    }
                 }
             }
         }
@@ -343,17 +304,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Partials gu_s{{a.g_s, a.u_s}, {a.gb_s, a.ub_s}, (long)a.T, a.Is};
     const Partials pt{{a.y_r, nullptr}, {a.yb_r, nullptr}, (long)a.T * a.k, H};
     const Partials pts{{a.y_s, nullptr}, {a.yb_s, nullptr}, (long)a.T, H};
-    float acc[1][4] = {};
-    long cur = -1;
-    // routed group index, or -1 - shared group index; INT_MIN: no operand built yet
-    int cur_group = INT_MIN;
-    TileInfo ti{};
-    const float* swr = nullptr;
     bool failed = false;
 
     // FP8 operand of one row group: a = SiLU(g) * u from the gate/up tiles, quantised
     // per 128 values (one gate/up slice = one down K block)
-    auto build_operand = [&](const TileInfo& q) {
+    auto build_operand = [&](const TileRec& q) {
         const int N = q.shared ? a.Is : a.I;
         const int Nb = N / kBlk;
         const Partials& src = q.shared ? gu_s : gu_r;
@@ -368,78 +323,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<uint32_t*>(s_hq + col * Nmax + kbq * kBlk)[lane] = code;
             if (lane == 0) s_hs[col * (Nmax / kBlk) + kbq] = sc;
         }
-        if (tid < kGroupRows) {
-            float wc = 0.f;
-            if (tid < q.nrows) {
-                if (q.shared) {
-                    wc = 1.f;
-                } else {
-                    const int f = a.perm_src[q.row_begin + tid];
-                    wc = ((unsigned)f < (unsigned)(a.T * a.k)) ? a.topk_w[f] : 0.f;
-                }
-            }
-            s_w[tid] = wc;
-        }
+        if (tid < kGroupRows) s_w[tid] = q.w[tid];
         named_bar(1, kConsThreads);
     };
 
-    long t = rg.first_tile;
-    int kb = rg.kb0;
-    int left = (int)(ts.start(t) + ts.len(t) - rg.u0);
+    // routed group index, or -1 - shared group index; INT_MIN: no operand built yet
+    int cur_group = INT_MIN;
     int s = 0, ph = 0;
-    for (long u = rg.u0; u < rg.u1; ++u) {
-        if (t != cur) {
-            cur = t;
-            ti = decode_tile(ts, t, slices, slices, a.groups, a.T);
-            const int grp = ti.shared ? -1 - ti.row_begin / kGroupRows : ti.group;
-            if (grp != cur_group) {
-                named_bar(1, kConsThreads);  // every warp is done with the previous operand
-                build_operand(ti);
-                cur_group = grp;
+    const int nsb = Nmax / kBlk;
+    for (int i = 0; i < ntiles; ++i) {
+        const TileRec r = rec(i);
+        const int grp = r.shared ? -1 - r.row_begin / kGroupRows : r.group;
+        if (grp != cur_group) {
+            named_bar(1, kConsThreads);  // every warp is done with the previous operand
+            build_operand(r);
+            cur_group = grp;
+        }
+        const float* swr =
+            r.shared ? a.ss_down + (size_t)r.slice * Isb : a.s_down + ((size_t)r.expert * slices + r.slice) * Ib;
+        const bool v0 = 2 * t4 < r.nrows, v1 = 2 * t4 + 1 < r.nrows;
+        float acc[1][4] = {};
+        for (int j = 0; j < r.n; ++j) {
+            const int kb = r.kb0 + j;
+            const float sw = __ldg(swr + kb);
+            const float sx0 = s_hs[(2 * t4) * nsb + kb];
+            const float sx1 = s_hs[(2 * t4 + 1) * nsb + kb];
+            if (!failed && !mbar_wait_bounded(&full[s], ph)) {
+                set_status(a.status, kStatusTimeout);
+                failed = true;  // keep walking the units so every named barrier is still reached
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[0][j] = 0.f;
-            swr = ti.shared ? a.ss_down + (size_t)ti.slice * Isb
-                            : a.s_down + ((size_t)ti.expert * slices + ti.slice) * Ib;
-        }
-        const float sw = __ldg(swr + kb);
-        const int nsb = Nmax / kBlk;
-        const float sx0 = s_hs[(2 * t4) * nsb + kb];
-        const float sx1 = s_hs[(2 * t4 + 1) * nsb + kb];
-        if (!failed && !mbar_wait_bounded(&full[s], ph)) {
-            set_status(a.status, kStatusTimeout);
-            failed = true;  // keep walking the units so every named barrier is still reached
-        }
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        if (!failed) {
-            box_dot(c, smem + s * SB, s_hq + g * Nmax + kb * kBlk, warp, g, t4);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-        }
-        const bool v0 = 2 * t4 < ti.nrows, v1 = 2 * t4 + 1 < ti.nrows;
-        acc[0][0] = fmaf(c[0], v0 ? sw * sx0 : 0.f, acc[0][0]);
-        acc[0][1] = fmaf(c[1], v1 ? sw * sx1 : 0.f, acc[0][1]);
-        acc[0][2] = fmaf(c[2], v0 ? sw * sx0 : 0.f, acc[0][2]);
-        acc[0][3] = fmaf(c[3], v1 ? sw * sx1 : 0.f, acc[0][3]);
-        ++kb;
-        if (--left == 0 || u + 1 == rg.u1) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
             if (!failed) {
-                float vals[1][4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) vals[0][i] = acc[0][i] * s_w[2 * t4 + (i & 1)];
-                store_tile<1>(vals, ts, rg, t, ti, ti.shared ? pts : pt);
+                box_dot(c, smem + s * SB, s_hq + g * Nmax + kb * kBlk, warp, g, t4);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
             }
-            if (left == 0 && u + 1 < rg.u1) {
-                ++t;
-                left = ts.len(t);
-                int kbn;
-                ts.tile_of(ts.start(t), &kbn);
-                kb = kbn;
+            acc[0][0] = fmaf(c[0], v0 ? sw * sx0 : 0.f, acc[0][0]);
+            acc[0][1] = fmaf(c[1], v1 ? sw * sx1 : 0.f, acc[0][1]);
+            acc[0][2] = fmaf(c[2], v0 ? sw * sx0 : 0.f, acc[0][2]);
+            acc[0][3] = fmaf(c[3], v1 ? sw * sx1 : 0.f, acc[0][3]);
+            if (++s == S) {
+                s = 0;
+                ph ^= 1;
             }
         }
-        if (++s == S) {
-            s = 0;
-            ph ^= 1;
+        if (!failed) {
+            float vals[1][4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) vals[0][q] = acc[0][q] * s_w[2 * t4 + (q & 1)];
+            store_rec<1>(vals, r, r.shared ? pts : pt);
         }
     }
 }
@@ -473,14 +405,44 @@ __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a)
         for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
             const int tok = (int)(i / H4), h = (int)(i % H4) * 4;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < a.k; ++j) {
-                const int r = a.inv_pos[tok * a.k + j];
-                if ((unsigned)r >= (unsigned)Tk) continue;
-                const float4 y = routed4(r, h);
-                v.x += y.x;
-                v.y += y.y;
-                v.z += y.z;
-                v.w += y.w;
+            // up to 8 expert rows at a time: their positions, then all their loads, then
+            // the sums in slot order
+            for (int j0 = 0; j0 < a.k; j0 += 8) {
+                int r[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    r[jj] = j0 + jj < a.k ? a.inv_pos[tok * a.k + j0 + jj] : -1;
+                    if ((unsigned)r[jj] >= (unsigned)Tk) r[jj] = -1;
+                }
+                float4 y[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) y[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int p = 0; p < pl.P; ++p) {
+                    float4 ya[8], yb[8];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        if (r[jj] >= 0) {
+                            const size_t o = ((size_t)p * pt.rows + r[jj]) * pt.N + h;
+                            ya[jj] = __ldcg(reinterpret_cast<const float4*>(pt.A[0] + o));
+                            yb[jj] = __ldcg(reinterpret_cast<const float4*>(pt.B[0] + o));
+                        }
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        if (r[jj] >= 0) {
+                            y[jj].x += ya[jj].x + yb[jj].x;
+                            y[jj].y += ya[jj].y + yb[jj].y;
+                            y[jj].z += ya[jj].z + yb[jj].z;
+                            y[jj].w += ya[jj].w + yb[jj].w;
+                        }
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    if (r[jj] >= 0) {
+                        v.x += y[jj].x;
+                        v.y += y[jj].y;
+                        v.z += y[jj].z;
+                        v.w += y[jj].w;
+                    }
             }
             if (a.n_shared_groups > 0) {
                 const float4 y = shared4(tok, h);
@@ -517,7 +479,7 @@ size_t smem_gateup() { return (size_t)kStagesGU * (2 * kBox + kBRows) + 2 * kSta
 // Down-kernel ring depth: as many 16 KB stages (up to 10) as fit beside the FP8 operand.
 int stages_down(int Nmax) {
     const long operand = (long)kGroupRows * Nmax + (long)kGroupRows * (Nmax / kBlk) * 4;
-    const long room = 227L * 1024 - 1024 - operand;
+    const long room = 227L * 1024 - 1024 - operand - (long)kTabBytes - 64;
     return (int)std::max<long>(2, std::min<long>(kMaxStagesD, room / (kBox + 16)));
 }
 size_t smem_down(int Nmax) {

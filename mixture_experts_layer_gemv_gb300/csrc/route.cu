@@ -45,7 +45,7 @@ struct RouteSmallParams {
 
 __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmallParams p) {
     __shared__ float s_part[kRouteWarps][kSmallT];
-    __shared__ float s_gs[kRouteWarps][2 * kMaxE + 32];
+    __shared__ float s_gs[kRouteWarps][kMaxE];
     __shared__ int32_t s_ids[kSmallT * 16];
     __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_gcnt[kMaxE], s_goff[kMaxE];
     __shared__ int s_last;
@@ -56,22 +56,48 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     pdl_wait();  // x and the workspace are free (the previous kernel in the stream is done)
     pdl_launch_dependents();
 
-    // ---- N: logits[:, e], K split over the CTA's warps (H/8 is a multiple of 16)
+    // ---- N: logits[:, e], K split over the CTA's warps (H/8 is a multiple of 16).
+    // A warp's router slice sits in registers (up to 8 float4 per lane per chunk) and
+    // four tokens' activations are loaded before any FMA, so a warp waits for one
+    // memory round trip per chunk and four tokens, not one per load.
     const int slice = H / kRouteWarps;
-    const float* wrow = p.wr + (size_t)e * H + warp * slice;
-    for (int t = 0; t < T; ++t) {
-        const uint16_t* xrow = p.x + (size_t)t * H + warp * slice;
-        float acc = 0.f;
-        for (int i = lane; i < slice / 4; i += 32) {
-            const float4 wv = __ldg(reinterpret_cast<const float4*>(wrow) + i);
-            const uint2 xv = __ldg(reinterpret_cast<const uint2*>(xrow) + i);
-            acc = fmaf(bf16_bits_to_float((uint16_t)(xv.x & 0xFFFF)), wv.x, acc);
-            acc = fmaf(bf16_bits_to_float((uint16_t)(xv.x >> 16)), wv.y, acc);
-            acc = fmaf(bf16_bits_to_float((uint16_t)(xv.y & 0xFFFF)), wv.z, acc);
-            acc = fmaf(bf16_bits_to_float((uint16_t)(xv.y >> 16)), wv.w, acc);
+    const int n4 = slice / 4;  // float4 per warp slice
+    const float4* wrow = reinterpret_cast<const float4*>(p.wr + (size_t)e * H + warp * slice);
+    for (int t = lane; t < T; t += 32) s_part[warp][t] = 0.f;
+    __syncwarp();
+    for (int c0 = 0; c0 < n4; c0 += 32 * 8) {
+        float4 wv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = c0 + lane + 32 * j;
+            wv[j] = i < n4 ? __ldg(wrow + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        acc = warp_sum(acc);
-        if (lane == 0) s_part[warp][t] = acc;
+        for (int t = 0; t < T; t += 4) {
+            uint2 xv[4][8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint2* xr =
+                    reinterpret_cast<const uint2*>(p.x + (size_t)min(t + q, T - 1) * H + warp * slice);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int i = c0 + lane + 32 * j;
+                    xv[q][j] = i < n4 ? __ldg(xr + i) : make_uint2(0, 0);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    acc = fmaf(bf16_bits_to_float((uint16_t)(xv[q][j].x & 0xFFFF)), wv[j].x, acc);
+                    acc = fmaf(bf16_bits_to_float((uint16_t)(xv[q][j].x >> 16)), wv[j].y, acc);
+                    acc = fmaf(bf16_bits_to_float((uint16_t)(xv[q][j].y & 0xFFFF)), wv[j].z, acc);
+                    acc = fmaf(bf16_bits_to_float((uint16_t)(xv[q][j].y >> 16)), wv[j].w, acc);
+                }
+                acc = warp_sum(acc);
+                if (lane == 0 && t + q < T) s_part[warp][t + q] += acc;
+            }
+        }
     }
     __syncthreads();
     for (int t = threadIdx.x; t < T; t += blockDim.x) {
@@ -205,7 +231,7 @@ struct TopkParams {
 };
 
 __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
-    __shared__ float s_gs[8][2 * kMaxE + 32];
+    __shared__ float s_gs[8][kMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.T) return;

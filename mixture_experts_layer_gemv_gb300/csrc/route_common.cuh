@@ -3,6 +3,8 @@
 // top-k of one token by one warp, and the in-CTA counting-sort permutation.
 #pragma once
 
+#include <climits>
+
 #include "common.cuh"
 #include "moe_internal.h"
 
@@ -13,19 +15,16 @@ constexpr int kMaxE = 256;
 
 // Softmax over E logits and group-limited greedy top-k for one token, computed by
 // one warp. lg[i] is the logit of expert lane + 32*i (-inf beyond E). scratch holds
-// 2*kMaxE + 32 words of shared memory private to this warp.
+// kMaxE words of shared memory private to this warp.
 //
-// Selection by ranks instead of repeated arg-max rounds: a group is kept when fewer
-// than topk_group groups beat it (higher score, or equal score and lower index); the
-// candidates of kept groups are compacted with a ballot, and a candidate is selected
-// when fewer than top_k candidates beat it, its rank being its output slot. Same
-// result as the greedy rounds (ties to the lower index), with no serial dependency.
+// A group is kept when fewer than topk_group groups beat it (higher score, or equal
+// score and lower index). The experts are then taken in top_k rounds of a warp-wide
+// arg-max over the candidates of kept groups (highest probability, ties to the lower
+// index), so slot j holds the j-th best: the greedy order, with no serial scan.
 __device__ inline void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, int Gk, int k, float scale,
-                          float* scratch, int32_t* ids_out, float* w_out, int32_t* ids_smem) {
+                                 float* scratch, int32_t* ids_out, float* w_out, int32_t* ids_smem) {
     const int lane = threadIdx.x & 31;
-    float* sp = scratch;                                          // [E] probabilities
-    int* cand = reinterpret_cast<int*>(scratch + kMaxE);          // [<= E] candidate ids
-    float* gsc = scratch + 2 * kMaxE;                             // [G] group scores
+    float* sp = scratch;  // [E] probabilities
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) mx = fmaxf(mx, lg[i]);
@@ -48,47 +47,52 @@ __device__ inline void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, in
     __syncwarp();
     // group score = max member score; groups are contiguous blocks of E/G experts
     const int per = E / G;
+    float gs = -INFINITY;
     if (lane < G) {
-        float m = sp[lane * per];
-        for (int i = 1; i < per; ++i) m = fmaxf(m, sp[lane * per + i]);
-        gsc[lane] = m;
+        gs = sp[lane * per];
+        for (int i = 1; i < per; ++i) gs = fmaxf(gs, sp[lane * per + i]);
     }
-    __syncwarp();
-    bool keep_g = false;
-    if (lane < G) {
-        const float mine = gsc[lane];
-        int beaten = 0;
-        for (int h = 0; h < G; ++h) {
-            const float o = gsc[h];
-            beaten += (o > mine) || (o == mine && h < lane);
-        }
-        keep_g = beaten < Gk;
+    int beaten = 0;
+    for (int h = 0; h < G; ++h) {
+        const float o = __shfl_sync(0xffffffffu, gs, h);
+        beaten += (o > gs) || (o == gs && h < lane);
     }
-    const unsigned kept = __ballot_sync(0xffffffffu, keep_g);
-    // compact the candidates (experts of kept groups), in expert order
-    int n = 0;
+    const unsigned kept = __ballot_sync(0xffffffffu, lane < G && beaten < Gk);
+    // candidates: experts of kept groups (probabilities are >= 0; -1 marks "none")
+    float cv[kMaxE / 32];
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) {
         const int e = lane + 32 * i;
-        const bool c = e < E && ((kept >> (e / per)) & 1u);
-        const unsigned m = __ballot_sync(0xffffffffu, c);
-        if (c) cand[n + __popc(m & ((1u << lane) - 1u))] = e;
-        n += __popc(m);
+        cv[i] = (e < E && ((kept >> (e / per)) & 1u)) ? p[i] : -1.f;
     }
-    __syncwarp();
-    for (int j = lane; j < n; j += 32) {
-        const int e = cand[j];
-        const float pe = sp[e];
-        int beaten = 0;
-        for (int q = 0; q < n; ++q) {
-            const int o = cand[q];
-            const float po = sp[o];
-            beaten += (po > pe) || (po == pe && o < e);
+    for (int j = 0; j < k; ++j) {
+        // this lane's best (lowest index on ties: e grows with i), then the warp's
+        float bv = -2.f;
+        int be = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i)
+            if (cv[i] > bv) {
+                bv = cv[i];
+                be = lane + 32 * i;
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
         }
-        if (beaten < k) {
-            ids_out[beaten] = e;
-            w_out[beaten] = pe * scale;
-            if (ids_smem) ids_smem[beaten] = e;
+        if ((be & 31) == lane) {  // the owner removes the winner from its candidates
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i)
+                if (lane + 32 * i == be) cv[i] = -1.f;
+        }
+        if (lane == 0) {
+            ids_out[j] = be;
+            w_out[j] = bv * scale;
+            if (ids_smem) ids_smem[j] = be;
         }
     }
     __syncwarp();

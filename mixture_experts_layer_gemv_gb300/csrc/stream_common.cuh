@@ -178,6 +178,74 @@ __device__ __forceinline__ Range make_range(const TileSpace& ts, int nb, int b) 
     return r;
 }
 
+// One tile of a CTA's unit range, decoded once before the streaming loops so that
+// neither the producer nor the consumers stall on descriptor loads or 64-bit index
+// arithmetic at tile boundaries.
+struct TileRec {
+    int shared, expert, group, row_begin, nrows, slice, part;
+    int kb0;  // absolute K block of this range's first unit of the tile
+    int n;    // units of the tile in this range
+    int hs;   // 1: the range holds the tile's first unit
+    int he;   // 1: the range holds the tile's last unit
+    int pad;
+    union {
+        int tok[kGroupRows];  // gate/up: token of each activation row, -1 if none
+        float w[kGroupRows];  // down: routing weight of each row (1 for the shared experts)
+    };
+};
+constexpr int kMaxTab = 96;
+constexpr size_t kTabBytes = (size_t)kMaxTab * sizeof(TileRec);
+
+__device__ inline TileRec make_rec(const TileSpace& ts, const Range& rg, long t, int slices_r, int slices_s,
+                                   const RowGroup* groups, int T, int k, const int32_t* perm_src,
+                                   const float* topk_w) {
+    TileRec r;
+    const TileInfo ti = decode_tile(ts, t, slices_r, slices_s, groups, T);
+    r.shared = ti.shared;
+    r.expert = ti.expert;
+    r.group = ti.group;
+    r.row_begin = ti.row_begin;
+    r.nrows = ti.nrows;
+    r.slice = ti.slice;
+    r.part = ti.part;
+    const long st = ts.start(t), len = ts.len(t);
+    const long lo = st > rg.u0 ? st : rg.u0, hi = st + len < rg.u1 ? st + len : rg.u1;
+    int kbs;
+    ts.tile_of(st, &kbs);
+    r.kb0 = kbs + (int)(lo - st);
+    r.n = (int)(hi - lo);
+    r.hs = st >= rg.u0;
+    r.he = st + len <= rg.u1;
+    r.pad = 0;
+    const int Tk = T * k;
+    int f[kGroupRows];
+#pragma unroll
+    for (int c = 0; c < kGroupRows; ++c)
+        f[c] = (c < ti.nrows && !ti.shared) ? perm_src[ti.row_begin + c] : -1;
+#pragma unroll
+    for (int c = 0; c < kGroupRows; ++c) {
+        if (topk_w) {
+            r.w[c] = c >= ti.nrows ? 0.f : ti.shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? topk_w[f[c]] : 0.f);
+        } else {
+            r.tok[c] = c >= ti.nrows ? -1 : ti.shared ? ti.row_begin + c : ((unsigned)f[c] < (unsigned)Tk ? f[c] / k : -1);
+        }
+    }
+    return r;
+}
+
+// Decode the tiles of range rg into tab (cooperatively, threads tid of nthreads); the
+// first kMaxTab are stored, the rest are decoded when reached. Returns the tile count.
+__device__ inline int build_table(TileRec* tab, const TileSpace& ts, const Range& rg, int slices_r, int slices_s,
+                                  const RowGroup* groups, int T, int k, const int32_t* perm_src, const float* topk_w,
+                                  int tid, int nthreads) {
+    int kbl;
+    const long last = ts.tile_of(rg.u1 - 1, &kbl);
+    const int n = (int)(last - rg.first_tile + 1);
+    for (int i = tid; i < n && i < kMaxTab; i += nthreads)
+        tab[i] = make_rec(ts, rg, rg.first_tile + i, slices_r, slices_s, groups, T, k, perm_src, topk_w);
+    return n;
+}
+
 // Partial results of a stage: dense buffers A[m] and B[m], both [P][rows][N] with the
 // output's row order (permuted rows for routed experts, tokens for the shared ones).
 struct Partials {
@@ -216,17 +284,47 @@ __device__ __forceinline__ void store_tile(const float (&vals)[NMAT][4], const T
 
 // Sum over the P parts of A + B at four consecutive channels col4.. of output row
 // `orow` of matrix m.
-__device__ __forceinline__ float4 read4(const Partials& pt, int P, int m, long orow, int col4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = 0; p < P; ++p) {
-        const size_t o = ((size_t)p * pt.rows + orow) * pt.N + col4;
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(pt.A[m] + o));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(pt.B[m] + o));
-        acc.x += a.x + b.x;
-        acc.y += a.y + b.y;
-        acc.z += a.z + b.z;
-        acc.w += a.w + b.w;
+// store_tile with the tile described by a TileRec
+template <int NMAT>
+__device__ __forceinline__ void store_rec(const float (&vals)[NMAT][4], const TileRec& r, const Partials& pt) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int col = 2 * t4 + (i & 1);
+        if (col >= r.nrows) continue;
+        const int row = warp * 16 + g + (i >= 2 ? 8 : 0);
+        const size_t o = ((size_t)r.part * pt.rows + r.row_begin + col) * pt.N + r.slice * kTile + row;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            if (r.hs) {
+                pt.A[m][o] = vals[m][i];
+                if (r.he) pt.B[m][o] = 0.f;
+            } else {
+                pt.B[m][o] = vals[m][i];
+            }
+        }
     }
+}
+
+__device__ __forceinline__ float4 read4(const Partials& pt, int P, int m, long orow, int col4) {
+    // all 2P loads first, then the sums in part order: one memory round trip
+    float4 a[kMaxParts], b[kMaxParts];
+#pragma unroll
+    for (int p = 0; p < kMaxParts; ++p)
+        if (p < P) {
+            const size_t o = ((size_t)p * pt.rows + orow) * pt.N + col4;
+            a[p] = __ldcg(reinterpret_cast<const float4*>(pt.A[m] + o));
+            b[p] = __ldcg(reinterpret_cast<const float4*>(pt.B[m] + o));
+        }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < kMaxParts; ++p)
+        if (p < P) {
+            acc.x += a[p].x + b[p].x;
+            acc.y += a[p].y + b[p].y;
+            acc.z += a[p].z + b[p].z;
+            acc.w += a[p].w + b[p].w;
+        }
     return acc;
 }
 
