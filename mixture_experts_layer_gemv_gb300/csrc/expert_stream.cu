@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(st + kBox, mu, kb * kBlk, y, &full[s]);
 #pragma unroll
                 for (int c = 0; c < kGroupRows; ++c)
-                    if (xrow[c]) bulk_load(st + 2 * kBox + c * kBlk, xrow[c] + kb * kBlk, kBlk, &full[s]);
+                    if (xrow[c]) bulk_load(st + 2 * kBox + c * kRowPitch, xrow[c] + kb * kBlk, kBlk, &full[s]);
                 if (++s == S) {
                     s = 0;
                     ph ^= 1;
@@ -180,6 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok0 = r.tok[2 * t4], tok1 = r.tok[2 * t4 + 1];
         const float* xs0 = tok0 >= 0 ? a.xs + (size_t)tok0 * Hb : nullptr;
         const float* xs1 = tok1 >= 0 ? a.xs + (size_t)tok1 * Hb : nullptr;
+        int tokg = -1;  // this lane's B column: activation row g
+#pragma unroll
+        for (int c = 0; c < kGroupRows; ++c)
+            if (c == g) tokg = r.tok[c];
+        const bool bv = tokg >= 0;
         float acc[2][4] = {};
         for (int j = 0; j < r.n; ++j) {
             const int kb = r.kb0 + j;
@@ -195,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t* st = smem + s * SB;
             float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
             if (!failed) {
-                box_dot(cg, st, st + 2 * kBox + g * kBlk, warp, g, t4);
-                box_dot(cu, st + kBox, st + 2 * kBox + g * kBlk, warp, g, t4);
+                box_dot(cg, st, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
+                box_dot(cu, st + kBox, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
@@ -227,8 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
     uint64_t* empty = full + S;
     const int Nmax = max(a.I, a.Is);
-    uint8_t* s_hq = reinterpret_cast<uint8_t*>(empty + S);               // [8][Nmax] FP8 operand
-    float* s_hs = reinterpret_cast<float*>(s_hq + kGroupRows * Nmax);    // [8][Nmax/128] its scales
+    const int hp = Nmax + 16;  // operand row pitch: the rows of a B fragment in distinct banks
+    uint8_t* s_hq = reinterpret_cast<uint8_t*>(empty + S);               // [8][hp] FP8 operand
+    float* s_hs = reinterpret_cast<float*>(s_hq + kGroupRows * hp);      // [8][Nmax/128] its scales
     __shared__ float s_w[kGroupRows];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float sc;
             const uint32_t code = warp_quant_block128(silu_mul(gv.x, uv.x), silu_mul(gv.y, uv.y), silu_mul(gv.z, uv.z),
                                                       silu_mul(gv.w, uv.w), &sc);
-            reinterpret_cast<uint32_t*>(s_hq + col * Nmax + kbq * kBlk)[lane] = code;
+            reinterpret_cast<uint32_t*>(s_hq + col * hp + kbq * kBlk)[lane] = code;
             if (lane == 0) s_hs[col * (Nmax / kBlk) + kbq] = sc;
         }
         if (tid < kGroupRows) s_w[tid] = q.w[tid];
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float c[4] = {0.f, 0.f, 0.f, 0.f};
             if (!failed) {
-                box_dot(c, smem + s * SB, s_hq + g * Nmax + kb * kBlk, warp, g, t4);
+                box_dot(c, smem + s * SB, s_hq + g * hp + kb * kBlk, g < r.nrows, warp, g, t4);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
@@ -478,13 +484,14 @@ __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a)
 size_t smem_gateup() { return (size_t)kStagesGU * (2 * kBox + kBRows) + 2 * kStagesGU * 8 + 1024; }
 // Down-kernel ring depth: as many 16 KB stages (up to 10) as fit beside the FP8 operand.
 int stages_down(int Nmax) {
-    const long operand = (long)kGroupRows * Nmax + (long)kGroupRows * (Nmax / kBlk) * 4;
+    const long operand = (long)kGroupRows * (Nmax + 16) + (long)kGroupRows * (Nmax / kBlk) * 4;
     const long room = 227L * 1024 - 1024 - operand - (long)kTabBytes - 64;
     return (int)std::max<long>(2, std::min<long>(kMaxStagesD, room / (kBox + 16)));
 }
 size_t smem_down(int Nmax) {
     const int S = stages_down(Nmax);
-    return (size_t)S * kBox + 2 * S * 8 + (size_t)kGroupRows * Nmax + (size_t)kGroupRows * (Nmax / kBlk) * 4 + 1024;
+    return (size_t)S * kBox + 2 * S * 8 + (size_t)kGroupRows * (Nmax + 16) + (size_t)kGroupRows * (Nmax / kBlk) * 4 +
+           1024;
 }
 
 template <typename... KArgs, typename... Args>

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     __shared__ float s_part[kRouteWarps][kSmallT];
     __shared__ float s_gs[kRouteWarps][kMaxE];
     __shared__ int32_t s_ids[kSmallT * 16];
+    __shared__ int s_rank[kSmallT * 16];
     __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_gcnt[kMaxE], s_goff[kMaxE];
     __shared__ int s_last;
 
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     }
     __syncthreads();
     if (p.offsets)
-        small_permute(s_ids, T * p.k, p.E, s_cnt, s_off, s_gcnt, s_goff, p.offsets, p.perm_src, p.inv_pos,
+        small_permute(s_ids, T * p.k, p.E, s_cnt, s_off, s_gcnt, s_goff, s_rank, p.offsets, p.perm_src, p.inv_pos,
                       p.groups, p.group_of_row, p.ctrl);
     if (threadIdx.x == 0) p.ctrl->route_arrived = 0u;
 }

@@ -13,88 +13,88 @@ namespace routing {
 
 constexpr int kMaxE = 256;
 
+// Total order of floats as unsigned keys (larger float -> larger key).
+__device__ __forceinline__ unsigned float_key(float f) {
+    const unsigned b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 // Softmax over E logits and group-limited greedy top-k for one token, computed by
-// one warp. lg[i] is the logit of expert lane + 32*i (-inf beyond E). scratch holds
-// kMaxE words of shared memory private to this warp.
+// one warp. lg[i] is the logit of expert lane + 32*i (-inf beyond E). scratch is
+// unused (kept for the callers' shared-memory layout).
 //
-// A group is kept when fewer than topk_group groups beat it (higher score, or equal
-// score and lower index). The experts are then taken in top_k rounds of a warp-wide
-// arg-max over the candidates of kept groups (highest probability, ties to the lower
-// index), so slot j holds the j-th best: the greedy order, with no serial scan.
+// The softmax is monotonic, so groups and experts are ranked on the logits themselves
+// and probabilities are formed only for the chosen experts: p = exp(l - max) / sum.
+// A group's score is its best member; a group is kept when fewer than topk_group
+// groups beat it (higher score, or equal score and lower index). The experts are then
+// taken in top_k rounds of a warp-wide arg-max over the members of kept groups (ties
+// to the lower index), so slot j holds the j-th best: the greedy order.
 __device__ inline void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, int Gk, int k, float scale,
                                  float* scratch, int32_t* ids_out, float* w_out, int32_t* ids_smem) {
+    (void)scratch;
     const int lane = threadIdx.x & 31;
-    float* sp = scratch;  // [E] probabilities
+    const int per = E / G;
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) mx = fmaxf(mx, lg[i]);
     mx = warp_max(mx);
-    float p[kMaxE / 32];
-    float z = 0.f;
+    // group scores: lane g keeps the best key of group g
+    int gid[kMaxE / 32];
 #pragma unroll
     for (int i = 0; i < kMaxE / 32; ++i) {
         const int e = lane + 32 * i;
-        p[i] = (e < E) ? expf(lg[i] - mx) : 0.f;
-        z += p[i];
+        gid[i] = e < E ? e / per : -1;
     }
-    z = warp_sum(z);
+    unsigned gkey = 0u;
+    for (int gi = 0; gi < G; ++gi) {
+        unsigned m = 0u;
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-        p[i] = p[i] / z;
-        const int e = lane + 32 * i;
-        if (e < E) sp[e] = p[i];
-    }
-    __syncwarp();
-    // group score = max member score; groups are contiguous blocks of E/G experts
-    const int per = E / G;
-    float gs = -INFINITY;
-    if (lane < G) {
-        gs = sp[lane * per];
-        for (int i = 1; i < per; ++i) gs = fmaxf(gs, sp[lane * per + i]);
+        for (int i = 0; i < kMaxE / 32; ++i)
+            if (gid[i] == gi) m = max(m, float_key(lg[i]));
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == gi) gkey = m;
     }
     int beaten = 0;
     for (int h = 0; h < G; ++h) {
-        const float o = __shfl_sync(0xffffffffu, gs, h);
-        beaten += (o > gs) || (o == gs && h < lane);
+        const unsigned o = __shfl_sync(0xffffffffu, gkey, h);
+        beaten += (o > gkey) || (o == gkey && h < lane);
     }
     const unsigned kept = __ballot_sync(0xffffffffu, lane < G && beaten < Gk);
-    // candidates: experts of kept groups (probabilities are >= 0; -1 marks "none")
-    float cv[kMaxE / 32];
+    // candidates: experts of kept groups, as keys (0: none; a real key is never 0)
+    unsigned ck[kMaxE / 32];
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-        const int e = lane + 32 * i;
-        cv[i] = (e < E && ((kept >> (e / per)) & 1u)) ? p[i] : -1.f;
-    }
+    for (int i = 0; i < kMaxE / 32; ++i) ck[i] = (gid[i] >= 0 && ((kept >> gid[i]) & 1u)) ? float_key(lg[i]) : 0u;
+    float lsel = 0.f;  // lane j < k: logit of the j-th choice
     for (int j = 0; j < k; ++j) {
-        // this lane's best (lowest index on ties: e grows with i), then the warp's
-        float bv = -2.f;
-        int be = INT_MAX;
+        unsigned bk = 0u;
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i) bk = max(bk, ck[i]);
+        const unsigned top = __reduce_max_sync(0xffffffffu, bk);
+        unsigned be = 0xffffffffu;  // this lane's lowest expert holding the top key
+#pragma unroll
+        for (int i = kMaxE / 32 - 1; i >= 0; --i)
+            if (ck[i] == top) be = (unsigned)(lane + 32 * i);
+        be = __reduce_min_sync(0xffffffffu, be);
 #pragma unroll
         for (int i = 0; i < kMaxE / 32; ++i)
-            if (cv[i] > bv) {
-                bv = cv[i];
-                be = lane + 32 * i;
-            }
+            if ((unsigned)(lane + 32 * i) == be) ck[i] = 0u;  // the owner removes the winner
+        const int owner = (int)(be & 31u), slot = (int)(be >> 5);
+        float lw = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if ((be & 31) == lane) {  // the owner removes the winner from its candidates
-#pragma unroll
-            for (int i = 0; i < kMaxE / 32; ++i)
-                if (lane + 32 * i == be) cv[i] = -1.f;
-        }
+        for (int i = 0; i < kMaxE / 32; ++i)
+            if (i == slot) lw = lg[i];
+        lw = __shfl_sync(0xffffffffu, lw, owner);
+        if (lane == j) lsel = lw;
         if (lane == 0) {
-            ids_out[j] = be;
-            w_out[j] = bv * scale;
-            if (ids_smem) ids_smem[j] = be;
+            ids_out[j] = (int)be;
+            if (ids_smem) ids_smem[j] = (int)be;
         }
     }
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) z += (lane + 32 * i < E) ? expf(lg[i] - mx) : 0.f;
+    z = warp_sum(z);
+    if (lane < k) w_out[lane] = expf(lsel - mx) / z * scale;
     __syncwarp();
 }
 
@@ -128,15 +128,32 @@ __device__ inline int warp_exclusive_scan256(int* v, int n) {
     return total;
 }
 
-// Stable counting sort of n = T*k ids held in shared memory (n small) by one CTA,
-// plus row groups of at most kGroupRows rows per expert.
+// Stable counting sort of n = T*k (<= 1024) ids held in shared memory by one CTA,
+// plus row groups of at most kGroupRows rows per expert. The rank of each id among the
+// earlier equal ids comes from one warp walking 32-id chunks in order (__match_any_sync
+// inside a chunk, a running count per expert across chunks); the scatter is parallel.
+// s_rank holds n ints of scratch.
 __device__ inline void small_permute(const int32_t* s_ids, int n, int E, int* s_cnt, int* s_off, int* s_gcnt,
-                              int* s_goff, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
-                              RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl) {
+                                     int* s_goff, int* s_rank, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
+                                     RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl) {
+    const int lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const unsigned lt = (1u << lane) - 1u;
+        for (int c0 = 0; c0 < n; c0 += 32) {
+            const int f = c0 + lane;
+            const int e = f < n ? s_ids[f] : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            if (e >= 0) s_rank[f] = s_cnt[e] + __popc(peers & lt);
+            __syncwarp();
+            if (e >= 0 && (peers & lt) == 0u) s_cnt[e] += __popc(peers);  // one leader per expert
+            __syncwarp();
+        }
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int c = 0;
-        for (int f = 0; f < n; ++f) c += (s_ids[f] == e);
-        s_cnt[e] = c;
+        const int c = s_cnt[e];
         s_off[e] = c;
         s_gcnt[e] = (c + kGroupRows - 1) / kGroupRows;
         s_goff[e] = s_gcnt[e];
@@ -152,15 +169,16 @@ __device__ inline void small_permute(const int32_t* s_ids, int n, int E, int* s_
     }
     __syncthreads();
     for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+    for (int f = threadIdx.x; f < n; f += blockDim.x) {
+        const int e = s_ids[f];
+        if (e < 0) continue;
+        const int r = s_rank[f];
+        const int pos = s_off[e] + r;
+        perm_src[pos] = f;
+        inv_pos[f] = pos;
+        group_of_row[pos] = s_goff[e] + r / kGroupRows;
+    }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int pos = s_off[e];
-        for (int f = 0; f < n; ++f) {
-            if (s_ids[f] == e) {
-                perm_src[pos] = f;
-                inv_pos[f] = pos;
-                ++pos;
-            }
-        }
         const int c = s_cnt[e];
         for (int g = 0; g < s_gcnt[e]; ++g) {
             RowGroup rg;
@@ -169,7 +187,6 @@ __device__ inline void small_permute(const int32_t* s_ids, int n, int E, int* s_
             rg.nrows = min(kGroupRows, c - g * kGroupRows);
             rg.pad = 0;
             groups[s_goff[e] + g] = rg;
-            for (int r = 0; r < rg.nrows; ++r) group_of_row[rg.row_begin + r] = s_goff[e] + g;
         }
     }
 }

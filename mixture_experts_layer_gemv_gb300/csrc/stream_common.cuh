@@ -17,7 +17,10 @@ constexpr int kThreads = (kCons + 1) * 32;  // + one producer warp
 constexpr int kConsThreads = kCons * 32;
 constexpr int kTile = 128;
 constexpr int kBox = kTile * kBlk;          // 16 KB: 128 rows x 128 bytes
-constexpr int kBRows = kGroupRows * kBlk;   // 1 KB: the unit's activation rows
+// Activation rows of a unit sit kRowPitch bytes apart: 16 bytes more than a K block, so
+// that the 8 rows of an mma B fragment fall in different shared-memory banks.
+constexpr int kRowPitch = kBlk + 16;
+constexpr int kBRows = 2048;                // the unit's activation rows (8 x kRowPitch, 1 KB-rounded)
 constexpr int kStagesGU = 5;
 constexpr int kMaxStagesD = 10;
 
@@ -147,15 +150,16 @@ __device__ __forceinline__ void mma_step64(float (&c)[4], const uint4& ar, const
 }
 
 // One 128 x 128-byte box times 8 activation rows (brow: this lane's row g, 128 bytes
-// of K): the fp32 16x8 partial of this warp (rows 16w..16w+15).
-__device__ __forceinline__ void box_dot(float (&c)[4], const uint8_t* box, const uint8_t* brow, int warp, int g,
-                                        int t4) {
+// of K; bvalid: row g exists): the fp32 16x8 partial of this warp (rows 16w..16w+15).
+// Columns of missing rows are zero and are not read from shared memory.
+__device__ __forceinline__ void box_dot(float (&c)[4], const uint8_t* box, const uint8_t* brow, bool bvalid, int warp,
+                                        int g, int t4) {
     const int r = warp * 16 + g;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
         uint4 lo, hi;
         load_a(box, r, g, 4 * s + t4, lo, hi);
-        const uint4 b = lds128(brow + s * 64 + 16 * t4);
+        const uint4 b = bvalid ? lds128(brow + s * 64 + 16 * t4) : make_uint4(0, 0, 0, 0);
         mma_step64(c, lo, hi, b, 0);
         mma_step64(c, lo, hi, b, 1);
     }
