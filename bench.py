@@ -152,10 +152,41 @@ def _algorithmic_layer_bytes(cfg, n_experts_touched: int, T: int) -> int:
     return w + s + E * H * 4 + 2 * T * H * 2
 
 
-def _launches_per_step(T: int) -> int:
-    # small T: fused route + permutation, gate/up, down, combine; large T: router GEMM, top-k,
-    # activation quant, permutation, gate/up, down, combine
-    return 4 if T <= 64 else 7
+def _gemm_path(cfg, T: int) -> bool:
+    """The library runs the grouped tensor-core GEMM when T > 64 and hidden % 256 == 0."""
+    return T > 64 and cfg.hidden % 256 == 0
+
+
+def _launches_per_step(cfg, T: int) -> int:
+    # small T: fused route + permutation, gate/up, down, combine
+    if T <= 64:
+        return 4
+    # grouped GEMM: router GEMM, top-k, activation quant, permutation, row gather, gate/up, down, combine
+    if _gemm_path(cfg, T):
+        return 8
+    # streaming fallback: router GEMM, top-k, activation quant, permutation, gate/up, down, combine
+    return 7
+
+
+def _gateup_flops(cfg, T: int) -> int:
+    """FP8 tensor work of the gate/up stage: 2 x rows x (gate + up rows) x hidden."""
+    H, I, Is = cfg.hidden, cfg.moe_inter, cfg.shared_inter
+    return 2 * T * cfg.top_k * 2 * I * H + 2 * T * 2 * Is * H
+
+
+def _layer_flops(cfg, T: int) -> int:
+    """FP8 tensor work of the layer (gate/up and down of routed and shared experts)."""
+    H, I, Is = cfg.hidden, cfg.moe_inter, cfg.shared_inter
+    return _gateup_flops(cfg, T) + 2 * T * cfg.top_k * H * I + 2 * T * H * Is
+
+
+# DRAM traffic of the dominant kernel per launch, from ncu captures of the current
+# kernels (the summaries under profiles/ give the commands); None where no capture of
+# the current kernel exists.
+NCU_TRAFFIC_BYTES = {
+    ("dsv2_decode_t1", "gateup_stream_kernel"): 138_390_000,   # 133.98 MB read + 4.41 MB written
+    ("prefill_t4096", "expert_gemm_kernel<0>"): 2_577_560_000,  # 2.4976 GB read + 80.0 MB written
+}
 
 
 def run_ours(args, dist, rank, world):
@@ -287,7 +318,7 @@ def run_ours(args, dist, rank, world):
         "cfg": cfg, "T": T, "ms": ms, "e2e_ms": e2e_ms, "gu_ms": gu_ms, "gu_bytes": gu_bytes,
         "achieved": achieved, "peak": peak_gbs, "peak_src": "measured" if peaks else "fallback",
         "layer_bytes": layer_bytes, "tokens_per_s": tokens_per_s, "clocks": clk.summary(), "status": status,
-        "replicas": R, "n_touched": n_touched, "launches": _launches_per_step(T) * args.steps, "weights": W0,
+        "replicas": R, "n_touched": n_touched, "launches": _launches_per_step(cfg, T) * args.steps, "weights": W0,
         "stage_us": stage_us, "prof_steps": n_prof,
     }
 
@@ -374,6 +405,26 @@ def main():
         value, unit, hib = r["tokens_per_s"], "tokens/s", True
         e2e_value = world * T / (r["e2e_ms"] * 1e-3)
     config["l2"] = f"{r['replicas']} stacked layer replicas rotated so weights stream from HBM (inputs > L2)"
+    peaks = _peaks()
+    if _gemm_path(cfg, T):
+        # contraction on the FP8 tensor cores: peak = measured bf16 burst x nominal FP8/bf16 ratio (2)
+        fp8_peak = 2.0 * peaks["bf16_tflops"] if peaks else 2.0 * 1900.0
+        gu_tflops = _gateup_flops(cfg, T) / (r["gu_ms"] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "expert_gemm_kernel<0> (gate/up grouped GEMM)",
+                    "achieved": round(gu_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                    "frac": round(gu_tflops / fp8_peak, 4),
+                    "traffic": NCU_TRAFFIC_BYTES.get((wl.name, "expert_gemm_kernel<0>")),
+                    "peak_source": ("measured bf16 burst x2 (nominal fp8/bf16)" if peaks else "fallback x2"),
+                    "launch_us": round(r["gu_ms"] * 1e3, 3), "flops_per_launch": _gateup_flops(cfg, T)}
+        layer_tflops = _layer_flops(cfg, T) / (r["ms"] * 1e-3) / 1e12
+        extra = {"layer_tflops": round(layer_tflops, 1), "layer_tensor_frac": round(layer_tflops / fp8_peak, 4)}
+    else:
+        roofline = {"bound": "hbm", "kernel": "gateup_stream_kernel", "achieved": round(r["achieved"], 1),
+                    "peak": r["peak"], "unit": "GB/s", "frac": round(r["achieved"] / r["peak"], 4),
+                    "traffic": NCU_TRAFFIC_BYTES.get((wl.name, "gateup_stream_kernel")),
+                    "peak_source": r["peak_src"], "launch_us": round(r["gu_ms"] * 1e3, 3),
+                    "bytes_per_launch": r["gu_bytes"]}
+        extra = {}
     line = {
         "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms"], 5), "higher_is_better": hib, "scaling": "weak",
@@ -382,12 +433,10 @@ def main():
         "layer_hbm_frac": round(r["layer_bytes"] / (r["ms"] * 1e-3) / 1e9 / r["peak"], 4),
         "tokens_per_s": round(r["tokens_per_s"], 1),
         "experts_touched_per_step": r["n_touched"],
-        "roofline": {"bound": "hbm", "kernel": "gateup_stream_kernel", "achieved": round(r["achieved"], 1),
-                     "peak": r["peak"], "unit": "GB/s", "frac": round(r["achieved"] / r["peak"], 4),
-                     "traffic": None, "peak_source": r["peak_src"],
-                     "launch_us": round(r["gu_ms"] * 1e3, 3), "bytes_per_launch": r["gu_bytes"]},
+        "roofline": roofline,
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": T * cfg.hidden * 2,
                 "d2h_bytes_per_step": T * cfg.hidden * 2},
+        **extra,
         "stages_us": r["stage_us"], "stage_events_on_steps": r["prof_steps"],
         "gpu_launches": r["launches"], "clocks": r["clocks"], "device_status": r["status"],
     }
