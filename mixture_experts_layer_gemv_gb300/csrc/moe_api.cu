@@ -25,7 +25,7 @@ static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 int router_splits_for(const moe_config_t& c, int64_t T) {
     if (T <= kSmallT) return 1;
-    const int64_t tiles = ((T + 63) / 64) * ((c.n_routed + 63) / 64);
+    const int64_t tiles = (T + 63) / 64;     // router CTAs: 64 tokens x all experts each
     int64_t s = (304 + tiles - 1) / tiles;  // aim at two CTAs per SM of a 152-SM part
     const int64_t hb = c.hidden / 128;
     if (s > 8) s = 8;

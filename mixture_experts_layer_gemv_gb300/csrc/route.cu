@@ -150,74 +150,144 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
 }
 
 // ---------------------------------------------------------------- large T
-constexpr int kBM = 64, kBN = 64, kBK = 32;
+// ---- large T: router GEMM on the tensor cores. x is exact in bf16; each fp32 router
+// weight is split as w = hi + mid + lo, three bf16 values (|w - hi - mid - lo| <=
+// 2^-27 |w|, the precision of the fp32 weight itself), and the three products go
+// through mma.m16n8k16 (bf16 x bf16, fp32 accumulation). A CTA takes 64 tokens x all
+// experts over a range of K (split-K partials, summed in fixed order by topk_kernel),
+// in 64-wide K steps: the next step's x and router values are loaded into registers
+// while the current step's MMAs run.
+constexpr int kRM = 64;      // token rows per CTA
+constexpr int kRK = 64;      // K per step
+constexpr int kRPitch = 72;  // bf16 per shared-memory row: 64 + 8 (rows in distinct banks)
 
-struct RouterGemmParams {
-    int H, E, T, kchunk;
+struct RouterMmaParams {
+    int H, E, Ep, T, k_per_split;
     const uint16_t* x;
     const float* wr;
     float* part;  // [splits, T, E]
 };
 
-// part[s][t][e] = sum over this split's K range of x[t][h] * wr[e][h]; 256 threads,
-// each owns a 4x4 register tile (rows ty+16i, cols tx+16j).
-__global__ void __launch_bounds__(256) router_gemm_kernel(RouterGemmParams p) {
-    __shared__ float As[kBK][kBM + 4];
-    __shared__ float Bs[kBK][kBN + 4];
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
-    const int k_begin = blockIdx.z * p.kchunk;
-    const int k_end = min(p.H, k_begin + p.kchunk);
-    float acc[4][4] = {};
-    for (int k0 = k_begin; k0 < k_end; k0 += kBK) {
-        {   // A: 64 rows x 32 bf16, 8 per thread
-            const int r = tid >> 2, c = (tid & 3) * 8;
-            const int t = m0 + r;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t < p.T) v = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H + k0 + c));
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// w -> (hi, mid, lo), each the bf16 rounding of what the previous parts leave
+__device__ __forceinline__ void split3(float w, uint16_t& hi, uint16_t& mid, uint16_t& lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(h);
+    const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(m);
+    hi = __bfloat16_as_ushort(h);
+    mid = __bfloat16_as_ushort(m);
+    lo = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+}
+
+template <int NTW>  // 8-wide expert tiles per warp: Ep = 16 * NTW
+__global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
+    extern __shared__ uint4 smem_r[];
+    uint16_t* sx = reinterpret_cast<uint16_t*>(smem_r);  // [64][kRPitch]
+    uint16_t* sw = sx + kRM * kRPitch;                    // [3][Ep][kRPitch]: hi, mid, lo
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+    const int m0 = blockIdx.x * kRM;
+    const int k0 = blockIdx.y * p.k_per_split, k1 = min(p.H, k0 + p.k_per_split);
+    const int mt = warp & 3, nh = warp >> 2;  // 16-row tile, half of the experts
+    constexpr int nw4 = NTW;                  // router float4 per thread per step: Ep * 16 / 256
+    const size_t wplane = (size_t)p.Ep * kRPitch;
+    float acc[NTW][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                As[c + 2 * i][r] = bf16_bits_to_float((uint16_t)(w4[i] & 0xFFFF));
-                As[c + 2 * i + 1][r] = bf16_bits_to_float((uint16_t)(w4[i] >> 16));
-            }
+    for (int j = 0; j < NTW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+    uint4 xr[2];       // x tile: 64 rows x 64 bf16 = 512 uint4, 2 per thread
+    float4 wv[nw4];    // router tile: Ep rows x 64 fp32
+    auto load = [&](int kk) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = tid + 256 * q, r = i >> 3, c = i & 7, t = m0 + r;
+            xr[q] = t < p.T ? __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H + kk) + c)
+                            : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // B: 64 rows x 32 fp32, 2 float4 per thread
-            const int idx = tid + h * 256;
-            const int r = idx >> 3, c = (idx & 7) * 4;
-            const int e = n0 + r;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < p.E) v = __ldg(reinterpret_cast<const float4*>(p.wr + (size_t)e * p.H + k0 + c));
-            Bs[c + 0][r] = v.x;
-            Bs[c + 1][r] = v.y;
-            Bs[c + 2][r] = v.z;
-            Bs[c + 3][r] = v.w;
+        for (int q = 0; q < nw4; ++q) {
+            const int i = tid + 256 * q, e = i >> 4, c = i & 15;
+            wv[q] = e < p.E ? __ldg(reinterpret_cast<const float4*>(p.wr + (size_t)e * p.H + kk) + c)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    auto store = [&]() {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = tid + 256 * q, r = i >> 3, c = i & 7;
+            *reinterpret_cast<uint4*>(sx + r * kRPitch + c * 8) = xr[q];
+        }
+#pragma unroll
+        for (int q = 0; q < nw4; ++q) {
+            const int i = tid + 256 * q, e = i >> 4, c = i & 15;
+            const float w4[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
+            uint16_t h[4], m[4], l[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) split3(w4[u], h[u], m[u], l[u]);
+            uint16_t* d = sw + e * kRPitch + c * 4;
+            *reinterpret_cast<uint2*>(d) = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+            *reinterpret_cast<uint2*>(d + wplane) =
+                make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
+            *reinterpret_cast<uint2*>(d + 2 * wplane) =
+                make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
+        }
+    };
+
+    if (k0 < k1) load(k0);
+    for (int kk = k0; kk < k1; kk += kRK) {
+        store();
         __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < kBK; ++kk) {
-            float a[4], b[4];
+        if (kk + kRK < k1) load(kk + kRK);  // in flight during this step's MMAs
+        // The tensor core aligns the products of one MMA to its accumulator's exponent and
+        // truncates, so each K step accumulates in a fresh (small) register block that is
+        // then added to the running sum with an ordinary fp32 add.
+        uint32_t af[kRK / 16][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int k16 = 0; k16 < kRK / 16; ++k16) {
+            const uint16_t* ar = sx + (mt * 16 + g) * kRPitch + k16 * 16 + 2 * t4;
+            af[k16][0] = lds32(ar);
+            af[k16][1] = lds32(ar + 8 * kRPitch);
+            af[k16][2] = lds32(ar + 8);
+            af[k16][3] = lds32(ar + 8 * kRPitch + 8);
         }
+        float d[NTW][4];
+#pragma unroll
+        for (int j = 0; j < NTW; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll
+        for (int k16 = 0; k16 < kRK / 16; ++k16)
+#pragma unroll
+            for (int part = 2; part >= 0; --part)  // small parts first
+#pragma unroll
+                for (int j = 0; j < NTW; ++j) {  // independent accumulators interleave
+                    const uint16_t* b = sw + part * wplane + ((nh * NTW + j) * 8 + g) * kRPitch + k16 * 16 + 2 * t4;
+                    mma_bf16_16816(d[j], af[k16][0], af[k16][1], af[k16][2], af[k16][3], lds32(b), lds32(b + 8));
+                }
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[j][q] += d[j][q];
         __syncthreads();
     }
-    float* out = p.part + (size_t)blockIdx.z * p.T * p.E;
+    float* out = p.part + (size_t)blockIdx.y * p.T * p.E;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = m0 + ty + 16 * i;
-        if (t >= p.T) continue;
+    for (int j = 0; j < NTW; ++j) {
+        const int e0 = (nh * NTW + j) * 8 + 2 * t4;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = n0 + tx + 16 * j;
-            if (e < p.E) out[(size_t)t * p.E + e] = acc[i][j];
+        for (int h = 0; h < 2; ++h) {
+            const int t = m0 + mt * 16 + g + 8 * h;
+            if (t >= p.T) continue;
+            if (e0 < p.E) out[(size_t)t * p.E + e0] = acc[j][2 * h];
+            if (e0 + 1 < p.E) out[(size_t)t * p.E + e0 + 1] = acc[j][2 * h + 1];
         }
     }
 }
@@ -253,29 +323,59 @@ __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
               nullptr);
 }
 
-// x [T, H] bf16 -> xq codes, xs scales; one warp per 128-block.
+// x [T, H] bf16 -> xq codes, xs scales. Four threads share a 128-value block (32 values
+// each, two shuffles for the block maximum), so the per-block work is spread thinly.
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, int T, int H, uint8_t* xq, float* xs) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hb = H / kBlk;
-    const long nb = (long)T * Hb;
-    for (long b = (long)blockIdx.x * 8 + warp; b < nb; b += (long)gridDim.x * 8) {
+    const long nq = (long)T * Hb * 4;  // quarters; a group of 4 threads = one block
+    // the loop condition is the same for every lane of a warp (the shuffles need all 32)
+    for (long base = (long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < nq;
+         base += (long)gridDim.x * blockDim.x) {
+        const long i = base + (threadIdx.x & 31);
+        const bool ok = i < nq;
+        const long b = (ok ? i : nq - 1) >> 2;
+        const int q = (int)(i & 3);
         const long t = b / Hb;
         const int kb = (int)(b % Hb);
-        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + t * H + kb * kBlk) + lane);
-        float s;
-        const uint32_t q = warp_quant_block128(
-            bf16_bits_to_float((uint16_t)(xv.x & 0xFFFF)), bf16_bits_to_float((uint16_t)(xv.x >> 16)),
-            bf16_bits_to_float((uint16_t)(xv.y & 0xFFFF)), bf16_bits_to_float((uint16_t)(xv.y >> 16)), &s);
-        reinterpret_cast<uint32_t*>(xq + t * H + kb * kBlk)[lane] = q;
-        if (lane == 0) xs[t * Hb + kb] = s;
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * H + kb * kBlk + q * 32);
+        uint4 u[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) u[c] = __ldg(src + c);
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                v[8 * c + 2 * h] = bf16_bits_to_float((uint16_t)(w[h] & 0xFFFF));
+                v[8 * c + 2 * h + 1] = bf16_bits_to_float((uint16_t)(w[h] >> 16));
+            }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        float inv;
+        const float sc = act_scale_pow2(amax, &inv);
+        if (ok) {
+            uint32_t code[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                code[j] = pack_e4m3x4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv);
+            uint4* dst = reinterpret_cast<uint4*>(xq + t * H + kb * kBlk + q * 32);
+            dst[0] = make_uint4(code[0], code[1], code[2], code[3]);
+            dst[1] = make_uint4(code[4], code[5], code[6], code[7]);
+            if (q == 0) xs[t * Hb + kb] = sc;
+        }
     }
 }
 
 }  // namespace
 
 cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs, cudaStream_t st) {
-    const long nb = (long)T * (H / kBlk);
-    const int grid = (int)std::min<long>((nb + 7) / 8, (long)num_sms() * 8);
+    const long nq = (long)T * (H / kBlk) * 4;
+    const int grid = (int)std::min<long>((nq + 255) / 256, (long)num_sms() * 8);
     quant_act_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, xq, xs);
     return cudaGetLastError();
 }
@@ -321,17 +421,44 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, int splits,
                                cudaStream_t st) {
-    RouterGemmParams g;
+    RouterMmaParams g;
     g.H = c.hidden;
     g.E = c.n_routed;
+    g.Ep = (c.n_routed + 15) & ~15;
     g.T = T;
     const int Hb = c.hidden / kBlk;
-    g.kchunk = ((Hb + splits - 1) / splits) * kBlk;
+    g.k_per_split = ((Hb + splits - 1) / splits) * kBlk;
     g.x = static_cast<const uint16_t*>(x);
     g.wr = w_router;
     g.part = logits;
-    dim3 grid((T + kBM - 1) / kBM, (c.n_routed + kBN - 1) / kBN, splits);
-    router_gemm_kernel<<<grid, 256, 0, st>>>(g);
+    const size_t smem = ((size_t)kRM + 3 * (size_t)g.Ep) * kRPitch * sizeof(uint16_t);
+    const dim3 grid((T + kRM - 1) / kRM, splits);
+    auto run = [&](auto kern) -> cudaError_t {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, 256, smem, st>>>(g);
+        return cudaGetLastError();
+    };
+    cudaError_t e2 = cudaErrorInvalidValue;
+    switch (g.Ep / 16) {  // n_routed <= 256
+        case 1: e2 = run(router_mma_kernel<1>); break;
+        case 2: e2 = run(router_mma_kernel<2>); break;
+        case 3: e2 = run(router_mma_kernel<3>); break;
+        case 4: e2 = run(router_mma_kernel<4>); break;
+        case 5: e2 = run(router_mma_kernel<5>); break;
+        case 6: e2 = run(router_mma_kernel<6>); break;
+        case 7: e2 = run(router_mma_kernel<7>); break;
+        case 8: e2 = run(router_mma_kernel<8>); break;
+        case 9: e2 = run(router_mma_kernel<9>); break;
+        case 10: e2 = run(router_mma_kernel<10>); break;
+        case 11: e2 = run(router_mma_kernel<11>); break;
+        case 12: e2 = run(router_mma_kernel<12>); break;
+        case 13: e2 = run(router_mma_kernel<13>); break;
+        case 14: e2 = run(router_mma_kernel<14>); break;
+        case 15: e2 = run(router_mma_kernel<15>); break;
+        case 16: e2 = run(router_mma_kernel<16>); break;
+    }
+    if (e2 != cudaSuccess) return e2;
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     TopkParams t;
