@@ -67,6 +67,8 @@ def _load():
             lib.orc_e4m3_encode.restype = ctypes.c_uint8
             lib.orc_e4m3_encode.argtypes = [ctypes.c_double]
             lib.orc_quant_rows.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P]
+            lib.orc_round_bf16.argtypes = [_P, ctypes.c_int, _P]
+            lib.orc_rmsnorm.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, ctypes.c_double, _P, _P]
             lib.orc_router_logits.argtypes = [_P, _P, ctypes.c_int, _P, _P, _P]
             lib.orc_topk.argtypes = [_P, _P, ctypes.c_int, _P, _P, _P, _P]
             lib.orc_permute.argtypes = [_P, _P, ctypes.c_int, _P, _P, _P]
@@ -156,6 +158,30 @@ def quant_rows(v) -> tuple:
     return q, s
 
 
+def round_bf16(values) -> np.ndarray:
+    """fp64 values -> bf16 bit patterns (uint16), rounded once to nearest, ties to even."""
+    lib = _load()
+    v = np.ascontiguousarray(np.asarray(values, dtype=np.float64))
+    out = np.empty(v.shape, np.uint16)
+    lib.orc_round_bf16(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def rmsnorm(h_bf16, gamma_bf16, eps: float, return_exact=False):
+    """Stage M: x = h / sqrt(mean(h^2) + eps) * gamma per row, rounded once to bf16.
+
+    -> x as bf16 bit patterns uint16 [T, H] (and the fp64 values before rounding)."""
+    lib = _load()
+    h = _np(h_bf16, np.uint16)
+    g = _np(gamma_bf16, np.uint16).reshape(-1)
+    T, H = h.shape
+    assert g.shape == (H,)
+    x = np.empty((T, H), np.uint16)
+    ex = np.empty((T, H), np.float64)
+    lib.orc_rmsnorm(_ptr(h), T, H, _ptr(g), float(eps), _ptr(x), _ptr(ex))
+    return (x, ex) if return_exact else x
+
+
 def router_logits(cfg, x_bf16, w_router, bias=None) -> np.ndarray:
     lib = _load()
     x = _np(x_bf16, np.uint16)
@@ -238,6 +264,13 @@ def forward_tokens(cfg, weights: Weights, x_bf16, ids, w, tokens=None, residual_
     lib.orc_forward_tokens(ctypes.byref(c), ctypes.byref(weights.struct), _ptr(x), _ptr(ids), _ptr(w),
                            _ptr(r), _ptr(tokens), len(tokens), _ptr(out))
     return out
+
+
+def forward_rmsnorm(cfg, weights_dict, h_bf16, gamma_bf16, eps: float, tokens=None, act_quant=True):
+    """Stage M in front of the layer, the residual after it: out = h + layer(RMSNorm(h))."""
+    x = rmsnorm(h_bf16, gamma_bf16, eps)
+    return forward(cfg, weights_dict, x, tokens=tokens, residual_bf16=_np(h_bf16, np.uint16),
+                   act_quant=act_quant)
 
 
 def forward(cfg, weights_dict, x_bf16, bias=None, w_router=None, tokens=None, residual_bf16=None,

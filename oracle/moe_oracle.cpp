@@ -7,6 +7,7 @@
 //
 // What it computes, step by step, follows the DeepSeek-V2 MoE stages as described
 // on "DSV2-236B-MegaKernel" (README, stage flowchart, MoE subgraph, stages M..R):
+//   M  RMSNorm in front of the router (optional: the fused-norm entry points)
 //   N  router GEMV            logits = W_router . x                      (fp64 here)
 //   O  softmax + group-limited greedy top-k, w = score * routed_scaling_factor
 //   P1 routed gate+up, FP8 block-scaled weights, SiLU(g) * u
@@ -136,6 +137,58 @@ static double bf16_to_double(uint16_t b) {
     float f;
     std::memcpy(&f, &u, 4);
     return (double)f;
+}
+
+// -------------------------------------------------------------- bf16 rounding
+// Round v to the nearest bf16 value (8 significant bits, exponent range of fp32),
+// ties to the even significand, in one step from the double (no detour through
+// float, which would round twice). Values at or beyond the overflow threshold give
+// infinity, NaN gives the canonical quiet NaN 0x7FC0.
+static uint16_t round_bf16(double v) {
+    if (std::isnan(v)) return 0x7FC0;
+    const uint16_t sign = std::signbit(v) ? 0x8000 : 0;
+    const double a = std::fabs(v);
+    if (a == 0.0) return sign;
+    int e = 0;
+    std::frexp(a, &e);       // a in [2^(e-1), 2^e)
+    int lead = e - 1;        // exponent of the leading bit
+    if (lead < -126) lead = -126;  // subnormals share the smallest normal binade's spacing
+    const double quantum = std::ldexp(1.0, lead - 7);  // distance between neighbours here
+    const double r = std::nearbyint(a / quantum) * quantum;  // a / quantum is exact
+    if (r >= std::ldexp(1.0, 128)) return sign | 0x7F80;
+    const float f = (float)r;  // exact: r has at most 8 significant bits
+    uint32_t bits;
+    std::memcpy(&bits, &f, 4);
+    return sign | (uint16_t)(bits >> 16);
+}
+
+void orc_round_bf16(const double* v, int n, uint16_t* out) {
+    for (int i = 0; i < n; ++i) out[i] = round_bf16(v[i]);
+}
+
+// ------------------------------------------------------------------ M: RMSNorm
+// Stage M in front of the router ("RMSNorm h x gamma4", DSV2-236B-MegaKernel stage
+// flowchart, MoE subgraph): per token row,
+//   x[h] = h[h] / sqrt(mean over the row of h^2 + eps) * gamma[h],
+// computed in fp64 and rounded once to bf16. x_exact (optional) receives the value
+// before that rounding.
+void orc_rmsnorm(const uint16_t* h_bf16, int T, int H, const uint16_t* gamma_bf16, double eps,
+                 uint16_t* x_bf16, double* x_exact) {
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const uint16_t* row = h_bf16 + (size_t)t * H;
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) {
+            const double v = bf16_to_double(row[h]);
+            ss += v * v;
+        }
+        const double rms = std::sqrt(ss / H + eps);
+        for (int h = 0; h < H; ++h) {
+            const double v = bf16_to_double(row[h]) / rms * bf16_to_double(gamma_bf16[h]);
+            if (x_exact) x_exact[(size_t)t * H + h] = v;
+            x_bf16[(size_t)t * H + h] = round_bf16(v);
+        }
+    }
 }
 
 // ------------------------------------------------------------------ N: router
