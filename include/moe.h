@@ -118,6 +118,16 @@ moe_status_t moe_read_device_status(void* ws, void* stream);
 moe_status_t moe_quant_act(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq, float* xs,
                            void* stream);
 
+/* Stage M: RMSNorm in front of the router ("M . RMSNorm h x gamma4 -> 5120",
+ * DSV2-236B-MegaKernel stage flowchart, MoE subgraph). Per token row t:
+ *   x[t][i] = bf16( h[t][i] * rstd[t] * gamma[i] ),  rstd[t] = 1 / sqrt(mean_i h[t][i]^2 + eps),
+ * the mean and 1/rms in fp32, one round-to-nearest-even to bf16 per element.
+ *   h_bf16 [T, H], gamma_bf16 [H] -> x_bf16 [T, H] (must not alias h).
+ * H % 8 == 0 (MOE_ERR_UNSUPPORTED_SHAPE otherwise); eps >= 0 and finite. The fused
+ * entry points below compute exactly these x values inside their own kernels. */
+moe_status_t moe_rmsnorm(const void* h_bf16, int32_t T, int32_t H, const void* gamma_bf16, float eps,
+                         void* x_bf16, void* stream);
+
 /* Stage N + O: router GEMV/GEMM and group-limited greedy top-k.
  *   logits[t][e] = sum_h x[t][h] * w_router[e][h] (+ router_bias[e])   (fp32)
  *   p = softmax over all E; group j = experts [j*E/G, (j+1)*E/G) scores max p;
@@ -128,6 +138,13 @@ moe_status_t moe_quant_act(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq
 moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, int32_t T,
                        const float* w_router, const float* router_bias, int32_t* topk_ids,
                        float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_route on RMSNorm(h) (stage M fused into the router's kernels: the normalised
+ * activation never goes to memory). Same outputs as moe_rmsnorm followed by moe_route;
+ * the workspace afterwards holds the FP8 codes of the normalised rows. */
+moe_status_t moe_route_rmsnorm(const moe_config_t* cfg, const void* h_bf16, int32_t T, const void* gamma_bf16,
+                               float eps, const float* w_router, const float* router_bias, int32_t* topk_ids,
+                               float* topk_w, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_route without a workspace, for callers that cannot allocate device memory:
  * a framework that owns the whole device memory pool and forbids cudaMalloc while it
@@ -191,6 +208,22 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
                                   const moe_weights_t* weights, const void* residual_bf16,
                                   void* out_bf16, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
                                   void* stream, const moe_stage_events_t* events);
+
+/* Stages M..R of the MoE block in one call, the residual stream in and out:
+ *   out = h + layer(RMSNorm(h))      (stage M as in moe_rmsnorm, the layer as in
+ *                                     moe_forward with residual = h)
+ * h_bf16 [T, H] is the hidden state before the norm; out_bf16 must not alias it.
+ * The normalised activation is formed inside the router and quantisation kernels
+ * (README flowchart: "M . RMSNorm h x gamma4", then N..R, "h += shared_out + routed"). */
+moe_status_t moe_forward_rmsnorm(const moe_config_t* cfg, const void* h_bf16, int32_t T, const void* gamma_bf16,
+                                 float eps, const moe_weights_t* weights, void* out_bf16, int32_t* topk_ids_out,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward_rmsnorm with CUDA events around each stage (stage M counts as routing). */
+moe_status_t moe_forward_rmsnorm_profiled(const moe_config_t* cfg, const void* h_bf16, int32_t T,
+                                          const void* gamma_bf16, float eps, const moe_weights_t* weights,
+                                          void* out_bf16, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
+                                          void* stream, const moe_stage_events_t* events);
 
 #ifdef __cplusplus
 }

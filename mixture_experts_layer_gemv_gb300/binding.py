@@ -56,6 +56,11 @@ _SIGNATURES = {
     "moe_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_read_device_status": (ctypes.c_int, [_P, _P]),
     "moe_quant_act": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
+    "moe_rmsnorm": (ctypes.c_int, [_P, _I32, _I32, _P, ctypes.c_float, _P, _P]),
+    "moe_route_rmsnorm": (ctypes.c_int, [_P, _P, _I32, _P, ctypes.c_float, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_rmsnorm": (ctypes.c_int, [_P, _P, _I32, _P, ctypes.c_float, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_rmsnorm_profiled": (ctypes.c_int, [_P, _P, _I32, _P, ctypes.c_float, _P, _P, _P, _P, _SZ, _P,
+                                                    _P]),
     "moe_route": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_route_noalloc": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -147,6 +152,20 @@ def moe_quant_act(x: torch.Tensor, xq: torch.Tensor, xs: torch.Tensor, stream=No
     _check("moe_quant_act", lib().moe_quant_act(_ptr(x), T, H, _ptr(xq), _ptr(xs), _stream(stream)))
 
 
+def moe_rmsnorm(h: torch.Tensor, gamma: torch.Tensor, eps: float, x_out: torch.Tensor, stream=None) -> None:
+    """Stage M: x_out = bf16(h / sqrt(mean(h^2) + eps) * gamma) per row."""
+    T, H = h.shape
+    _check("moe_rmsnorm", lib().moe_rmsnorm(_ptr(h), T, H, _ptr(gamma), float(eps), _ptr(x_out), _stream(stream)))
+
+
+def moe_route_rmsnorm(cfg, h, gamma, eps, w_router, router_bias, topk_ids, topk_w, ws, stream=None) -> None:
+    c = config_struct(cfg)
+    _check("moe_route_rmsnorm", lib().moe_route_rmsnorm(ctypes.byref(c), _ptr(h), h.shape[0], _ptr(gamma),
+                                                        float(eps), _ptr(w_router), _ptr(router_bias),
+                                                        _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel(),
+                                                        _stream(stream)))
+
+
 def moe_route(cfg, x, w_router, router_bias, topk_ids, topk_w, ws, stream=None) -> None:
     c = config_struct(cfg)
     _check("moe_route", lib().moe_route(ctypes.byref(c), _ptr(x), x.shape[0], _ptr(w_router), _ptr(router_bias),
@@ -195,11 +214,7 @@ def moe_forward(cfg, x, weights, out, residual=None, topk_ids_out=None, ws=None,
     c = config_struct(cfg)
     W = weights_struct(weights)
     if events:
-        ev = moe_stage_events_t()
-        for name, (a, b) in events.items():
-            i = STAGES.index(name)
-            ev.start[i] = a.cuda_event
-            ev.stop[i] = b.cuda_event
+        ev = _events_struct(events)
         st = lib().moe_forward_profiled(ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W), _ptr(residual),
                                         _ptr(out), _ptr(topk_ids_out), _ptr(ws), ws.numel(), _stream(stream),
                                         ctypes.byref(ev))
@@ -207,6 +222,33 @@ def moe_forward(cfg, x, weights, out, residual=None, topk_ids_out=None, ws=None,
         return
     _check("moe_forward", lib().moe_forward(ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W), _ptr(residual),
                                             _ptr(out), _ptr(topk_ids_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def _events_struct(events):
+    ev = moe_stage_events_t()
+    for name, (a, b) in events.items():
+        i = STAGES.index(name)
+        ev.start[i] = a.cuda_event
+        ev.stop[i] = b.cuda_event
+    return ev
+
+
+def moe_forward_rmsnorm(cfg, h, gamma, eps, weights, out, topk_ids_out=None, ws=None, stream=None,
+                        events: Optional[Dict[str, tuple]] = None) -> None:
+    """out[T, H] = h + MoE layer(RMSNorm(h) * gamma); ws from alloc_workspace(cfg, >= T)."""
+    c = config_struct(cfg)
+    W = weights_struct(weights)
+    if events:
+        ev = _events_struct(events)
+        st = lib().moe_forward_rmsnorm_profiled(ctypes.byref(c), _ptr(h), h.shape[0], _ptr(gamma), float(eps),
+                                                ctypes.byref(W), _ptr(out), _ptr(topk_ids_out), _ptr(ws),
+                                                ws.numel(), _stream(stream), ctypes.byref(ev))
+        _check("moe_forward_rmsnorm_profiled", st)
+        return
+    _check("moe_forward_rmsnorm", lib().moe_forward_rmsnorm(ctypes.byref(c), _ptr(h), h.shape[0], _ptr(gamma),
+                                                            float(eps), ctypes.byref(W), _ptr(out),
+                                                            _ptr(topk_ids_out), _ptr(ws), ws.numel(),
+                                                            _stream(stream)))
 
 
 def forward(cfg: MoEConfig, x: torch.Tensor, weights, residual=None, ws=None, return_ids=False):

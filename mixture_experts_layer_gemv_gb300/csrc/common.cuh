@@ -103,6 +103,61 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
     return __uint_as_float((uint32_t)b << 16);
 }
 
+// ------------------------------------------------- stage M: RMSNorm x gamma
+// x = h * rstd * gamma with rstd = 1 / sqrt(mean(h^2) + eps), rounded once to bf16
+// ("M . RMSNorm h x gamma4", DSV2-236B-MegaKernel stage flowchart, MoE subgraph).
+// Every kernel that reads a normalised activation derives it from the raw row with
+// these functions (rstd always from warp_row_sumsq), so all of them see the same
+// bf16 values.
+
+// Sum of squares of one bf16 row of H values (H a multiple of 8), by one warp in
+// a fixed order: lane l accumulates the 8-value chunks l, l+32, ... in order, then
+// a xor-shuffle tree. Returns the sum in every lane.
+__device__ __forceinline__ float warp_row_sumsq(const uint16_t* row, int H) {
+    const uint4* r = reinterpret_cast<const uint4*>(row);
+    const int lane = threadIdx.x & 31, n8 = H / 8;
+    float ss = 0.f;
+    for (int c0 = 0; c0 < n8; c0 += 32 * 8) {  // up to 8 loads in flight per lane
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = c0 + lane + 32 * j;
+            v[j] = c < n8 ? __ldg(r + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float a = bf16_bits_to_float((uint16_t)(w[q] & 0xFFFF));
+                const float b = bf16_bits_to_float((uint16_t)(w[q] >> 16));
+                ss = fmaf(a, a, ss);
+                ss = fmaf(b, b, ss);
+            }
+        }
+    }
+    return warp_sum(ss);
+}
+
+__device__ __forceinline__ float rms_rstd(float sumsq, int H, float eps) {
+    return 1.f / sqrtf(sumsq / (float)H + eps);
+}
+
+// Two packed bf16 values (low half first) normalised, repacked as bf16 bits.
+__device__ __forceinline__ uint32_t rms_apply2(uint32_t h2, float rstd, uint32_t g2) {
+    const __nv_bfloat16 lo = __float2bfloat16_rn(bf16_bits_to_float((uint16_t)(h2 & 0xFFFF)) * rstd *
+                                                 bf16_bits_to_float((uint16_t)(g2 & 0xFFFF)));
+    const __nv_bfloat16 hi = __float2bfloat16_rn(bf16_bits_to_float((uint16_t)(h2 >> 16)) * rstd *
+                                                 bf16_bits_to_float((uint16_t)(g2 >> 16)));
+    return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
+
+__device__ __forceinline__ uint4 rms_apply8(uint4 h8, float rstd, uint4 g8) {
+    return make_uint4(rms_apply2(h8.x, rstd, g8.x), rms_apply2(h8.y, rstd, g8.y), rms_apply2(h8.z, rstd, g8.z),
+                      rms_apply2(h8.w, rstd, g8.w));
+}
+
+
 
 // ------------------------------------------------------ mbarrier / TMA (sm_90+)
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

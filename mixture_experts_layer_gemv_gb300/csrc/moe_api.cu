@@ -61,6 +61,7 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     L.w = take(t * k * 4);
     L.xq = take(t * H);
     L.xs = take(t * (H / 128) * 4);
+    L.rstd = take(t * 4);
     L.offsets = take((E + 1) * 4);
     L.perm_src = take(t * k * 4);
     L.inv_pos = take(t * k * 4);
@@ -350,13 +351,28 @@ moe_status_t moe_quant_act(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq
     if (T < 0 || H <= 0 || H % 128) return T < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;
     if (!x_bf16 || !xq || !xs || !aligned16(x_bf16) || !aligned16(xq) || !aligned16(xs)) return MOE_ERR_INVALID_ARG;
-    MOE_CUDA(launch_quant_act(x_bf16, T, H, xq, xs, (cudaStream_t)stream));
+    MOE_CUDA(launch_quant_act(x_bf16, T, H, xq, xs, NormArgs{}, (cudaStream_t)stream));
     return MOE_OK;
 }
 
-moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, int32_t T, const float* w_router,
-                       const float* router_bias, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
-                       void* stream) {
+moe_status_t moe_rmsnorm(const void* h_bf16, int32_t T, int32_t H, const void* gamma_bf16, float eps,
+                         void* x_bf16, void* stream) {
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (H <= 0 || H % 8 || H > 65536) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!std::isfinite(eps) || eps < 0.f) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!h_bf16 || !gamma_bf16 || !x_bf16 || !aligned16(h_bf16) || !aligned16(gamma_bf16) || !aligned16(x_bf16))
+        return MOE_ERR_INVALID_ARG;
+    NormArgs nm;
+    nm.gamma = static_cast<const uint16_t*>(gamma_bf16);
+    nm.eps = eps;
+    MOE_CUDA(launch_rmsnorm(h_bf16, T, H, nm, x_bf16, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+static moe_status_t route_impl(const moe_config_t* cfg, const void* x_bf16, int32_t T, const float* w_router,
+                               const float* router_bias, int32_t* topk_ids, float* topk_w, void* ws,
+                               size_t ws_bytes, void* stream, NormArgs nm) {
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_T(cfg, T));
     if (T == 0) return MOE_OK;
@@ -370,12 +386,32 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, int32_t T, c
     if (T <= kSmallT) {
         MOE_CUDA(launch_route_small(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
                                     at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), nullptr, nullptr, nullptr, nullptr,
-                                    nullptr, at<Ctrl>(ws, L.ctrl), st));
+                                    nullptr, at<Ctrl>(ws, L.ctrl), nm, st));
     } else {
+        if (nm.gamma) {
+            nm.rstd = at<float>(ws, L.rstd);
+            MOE_CUDA(launch_rmsnorm(x_bf16, T, cfg->hidden, nm, nullptr, st));
+        }
         MOE_CUDA(launch_route_large(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
-                                    L.router_splits, st));
+                                    L.router_splits, nm, st));
     }
     return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, int32_t T, const float* w_router,
+                       const float* router_bias, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                       void* stream) {
+    return route_impl(cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, ws, ws_bytes, stream, NormArgs{});
+}
+
+moe_status_t moe_route_rmsnorm(const moe_config_t* cfg, const void* h_bf16, int32_t T, const void* gamma_bf16,
+                               float eps, const float* w_router, const float* router_bias, int32_t* topk_ids,
+                               float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+    if (!gamma_bf16 || !aligned16(gamma_bf16) || !std::isfinite(eps) || eps < 0.f) return MOE_ERR_INVALID_ARG;
+    NormArgs nm;
+    nm.gamma = static_cast<const uint16_t*>(gamma_bf16);
+    nm.eps = eps;
+    return route_impl(cfg, h_bf16, T, w_router, router_bias, topk_ids, topk_w, ws, ws_bytes, stream, nm);
 }
 
 moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32_t T, int32_t* expert_offsets,
@@ -407,7 +443,7 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_bf16, int32_t
     MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
     const WsLayout L = ws_layout(*cfg, T);
     cudaStream_t st = (cudaStream_t)stream;
-    MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), st));
+    MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), NormArgs{}, st));
     if (use_gemm(*cfg, T)) {
         MOE_CUDA(launch_build_groups(*cfg, expert_offsets, T * cfg->top_k, nullptr, nullptr, at<MTile>(ws, L.mtiles),
                                      at<Ctrl>(ws, L.ctrl), st));
@@ -448,10 +484,10 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm_bf16, const
     return MOE_OK;
 }
 
-moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, int32_t T,
-                                  const moe_weights_t* weights, const void* residual_bf16, void* out_bf16,
-                                  int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream,
-                                  const moe_stage_events_t* events) {
+static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                                 const moe_weights_t* weights, const void* residual_bf16, void* out_bf16,
+                                 int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream,
+                                 const moe_stage_events_t* events, NormArgs nm) {
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_T(cfg, T));
     if (T == 0) return MOE_OK;
@@ -475,12 +511,16 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
         MOE_CUDA(launch_route_small(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
                                     at<float>(ws, L.logits), at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
                                     at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups,
-                                    at<int32_t>(ws, L.group_of_row), ctrl, st));
+                                    at<int32_t>(ws, L.group_of_row), ctrl, nm, st));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
     } else {
+        if (nm.gamma) {
+            nm.rstd = at<float>(ws, L.rstd);
+            MOE_CUDA(launch_rmsnorm(x_bf16, T, cfg->hidden, nm, nullptr, st));
+        }
         MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
-                                    at<float>(ws, L.logits), L.router_splits, st));
-        MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), st));
+                                    at<float>(ws, L.logits), L.router_splits, nm, st));
+        MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), nm, st));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
         MOE_TRY(mark.begin(MOE_STAGE_PERMUTE));
         if (use_gemm(*cfg, T)) {
@@ -525,11 +565,38 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
     return MOE_OK;
 }
 
+moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                                  const moe_weights_t* weights, const void* residual_bf16, void* out_bf16,
+                                  int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream,
+                                  const moe_stage_events_t* events) {
+    return forward_impl(cfg, x_bf16, T, weights, residual_bf16, out_bf16, topk_ids_out, ws, ws_bytes, stream,
+                        events, NormArgs{});
+}
+
 moe_status_t moe_forward(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_t* weights,
                          const void* residual_bf16, void* out_bf16, int32_t* topk_ids_out, void* ws,
                          size_t ws_bytes, void* stream) {
-    return moe_forward_profiled(cfg, x_bf16, T, weights, residual_bf16, out_bf16, topk_ids_out, ws, ws_bytes,
-                                stream, nullptr);
+    return forward_impl(cfg, x_bf16, T, weights, residual_bf16, out_bf16, topk_ids_out, ws, ws_bytes, stream,
+                        nullptr, NormArgs{});
+}
+
+moe_status_t moe_forward_rmsnorm_profiled(const moe_config_t* cfg, const void* h_bf16, int32_t T,
+                                          const void* gamma_bf16, float eps, const moe_weights_t* weights,
+                                          void* out_bf16, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
+                                          void* stream, const moe_stage_events_t* events) {
+    if (!gamma_bf16 || !aligned16(gamma_bf16) || !std::isfinite(eps) || eps < 0.f) return MOE_ERR_INVALID_ARG;
+    if (out_bf16 == h_bf16) return MOE_ERR_INVALID_ARG;  // h is also the residual
+    NormArgs nm;
+    nm.gamma = static_cast<const uint16_t*>(gamma_bf16);
+    nm.eps = eps;
+    return forward_impl(cfg, h_bf16, T, weights, h_bf16, out_bf16, topk_ids_out, ws, ws_bytes, stream, events, nm);
+}
+
+moe_status_t moe_forward_rmsnorm(const moe_config_t* cfg, const void* h_bf16, int32_t T, const void* gamma_bf16,
+                                 float eps, const moe_weights_t* weights, void* out_bf16, int32_t* topk_ids_out,
+                                 void* ws, size_t ws_bytes, void* stream) {
+    return moe_forward_rmsnorm_profiled(cfg, h_bf16, T, gamma_bf16, eps, weights, out_bf16, topk_ids_out, ws,
+                                        ws_bytes, stream, nullptr);
 }
 
 }  // extern "C"

@@ -56,6 +56,7 @@ struct WsLayout {
     size_t w;          // fp32 [T, k]
     size_t xq;         // u8 [T, H]
     size_t xs;         // fp32 [T, H/128]
+    size_t rstd;       // fp32 [T] 1/rms of each token (stage M, large T)
     size_t offsets;    // int32 [E+1]
     size_t perm_src;   // int32 [T*k]
     size_t inv_pos;    // int32 [T*k]
@@ -81,22 +82,38 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T);
 int router_splits_for(const moe_config_t& c, int64_t T);
 int max_routed_groups(const moe_config_t& c, int64_t T);
 
+// Optional stage M in front of a kernel: gamma == nullptr means the input is used
+// as it is. rstd: per-token 1/rms computed by rms_kernel (large T) or in-kernel.
+struct NormArgs {
+    const uint16_t* gamma = nullptr;  // bf16 [H]
+    float eps = 0.f;
+    float* rstd = nullptr;            // fp32 [T] workspace
+};
+
 // ------------------------------------------------------------ launchers
 // All launchers enqueue on `st` and return cudaGetLastError().
-cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs, cudaStream_t st);
+// nm.gamma != nullptr: x is first normalised (stage M) with the 1/rms values in nm.rstd.
+cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs, const NormArgs& nm,
+                             cudaStream_t st);
 
-// Fused small-T route: logits, x quantisation, softmax + top-k, and (when
-// offsets != nullptr) the permutation and row-group descriptors.
+// Stage M alone: nm.rstd[t] = 1/rms of row t (if nm.rstd) and x_out = the normalised
+// rows in bf16 (if x_out).
+cudaError_t launch_rmsnorm(const void* x, int T, int H, const NormArgs& nm, void* x_out, cudaStream_t st);
+
+// Fused small-T route: (stage M when nm.gamma, computed in-kernel), logits, x
+// quantisation, softmax + top-k, and (when offsets != nullptr) the permutation and
+// row-group descriptors.
 cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits,
                                uint8_t* xq, float* xs, int32_t* offsets, int32_t* perm_src,
                                int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl,
-                               cudaStream_t st);
+                               const NormArgs& nm, cudaStream_t st);
 
-// Large-T route: tiled fp32 router (split-K partials) + softmax/top-k per token.
+// Large-T route: router GEMM (split-K partials) + softmax/top-k per token. With
+// nm.gamma the router reads stage M's output on the fly (nm.rstd from launch_rmsnorm).
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, int splits,
-                               cudaStream_t st);
+                               const NormArgs& nm, cudaStream_t st);
 
 // Stable counting sort of the T*k pairs by expert; writes row groups when groups != nullptr.
 cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int32_t* offsets,

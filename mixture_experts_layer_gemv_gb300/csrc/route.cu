@@ -41,6 +41,8 @@ struct RouteSmallParams {
     RowGroup* groups;
     int32_t* group_of_row;
     Ctrl* ctrl;
+    const uint16_t* gamma;  // stage M in front of the router when not null
+    float eps;
 };
 
 __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmallParams p) {
@@ -50,12 +52,23 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     __shared__ int s_rank[kSmallT * 16];
     __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_gcnt[kMaxE], s_goff[kMaxE];
     __shared__ int s_last;
+    __shared__ float s_rstd[kSmallT];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x;
     const int H = p.H, T = p.T, Hb = H / kBlk;
+    const bool norm = p.gamma != nullptr;
     pdl_wait();  // x and the workspace are free (the previous kernel in the stream is done)
     pdl_launch_dependents();
+
+    // ---- M (optional): every CTA derives the same 1/rms of each token itself
+    if (norm) {
+        for (int t = warp; t < T; t += kRouteWarps) {
+            const float r = rms_rstd(warp_row_sumsq(p.x + (size_t)t * H, H), H, p.eps);
+            if (lane == 0) s_rstd[t] = r;
+        }
+        __syncthreads();
+    }
 
     // ---- N: logits[:, e], K split over the CTA's warps (H/8 is a multiple of 16).
     // A warp's router slice sits in registers (up to 8 float4 per lane per chunk) and
@@ -66,12 +79,15 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     const float4* wrow = reinterpret_cast<const float4*>(p.wr + (size_t)e * H + warp * slice);
     for (int t = lane; t < T; t += 32) s_part[warp][t] = 0.f;
     __syncwarp();
+    const uint2* grow = norm ? reinterpret_cast<const uint2*>(p.gamma + warp * slice) : nullptr;
     for (int c0 = 0; c0 < n4; c0 += 32 * 8) {
         float4 wv[8];
+        uint2 gv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int i = c0 + lane + 32 * j;
             wv[j] = i < n4 ? __ldg(wrow + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[j] = norm && i < n4 ? __ldg(grow + i) : make_uint2(0, 0);
         }
         for (int t = 0; t < T; t += 4) {
             uint2 xv[4][8];
@@ -83,6 +99,15 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
                 for (int j = 0; j < 8; ++j) {
                     const int i = c0 + lane + 32 * j;
                     xv[q][j] = i < n4 ? __ldg(xr + i) : make_uint2(0, 0);
+                }
+            }
+            if (norm) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float r = s_rstd[min(t + q, T - 1)];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        xv[q][j] = make_uint2(rms_apply2(xv[q][j].x, r, gv[j].x), rms_apply2(xv[q][j].y, r, gv[j].y));
                 }
             }
 #pragma unroll
@@ -112,7 +137,11 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     // ---- activation quantisation: this CTA's share of the T*H/128 blocks
     for (int b = blockIdx.x * kRouteWarps + warp; b < T * Hb; b += gridDim.x * kRouteWarps) {
         const int t = b / Hb, kb = b % Hb;
-        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(p.x + (size_t)t * H + kb * kBlk) + lane);
+        uint2 xv = __ldg(reinterpret_cast<const uint2*>(p.x + (size_t)t * H + kb * kBlk) + lane);
+        if (norm) {
+            const uint2 g = __ldg(reinterpret_cast<const uint2*>(p.gamma + kb * kBlk) + lane);
+            xv = make_uint2(rms_apply2(xv.x, s_rstd[t], g.x), rms_apply2(xv.y, s_rstd[t], g.y));
+        }
         float s;
         const uint32_t q = warp_quant_block128(
             bf16_bits_to_float((uint16_t)(xv.x & 0xFFFF)), bf16_bits_to_float((uint16_t)(xv.x >> 16)),
@@ -165,7 +194,9 @@ struct RouterMmaParams {
     int H, E, Ep, T, k_per_split;
     const uint16_t* x;
     const float* wr;
-    float* part;  // [splits, T, E]
+    float* part;            // [splits, T, E]
+    const uint16_t* gamma;  // stage M applied to x when not null (with rstd [T])
+    const float* rstd;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -206,13 +237,22 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
     for (int j = 0; j < NTW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
     uint4 xr[2];       // x tile: 64 rows x 64 bf16 = 512 uint4, 2 per thread
+    uint4 gx[2];       // gamma of those columns (stage M)
+    float rs[2];       // 1/rms of those rows
     float4 wv[nw4];    // router tile: Ep rows x 64 fp32
+    const bool norm = p.gamma != nullptr;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int t = m0 + ((tid + 256 * q) >> 3);
+        rs[q] = norm && t < p.T ? p.rstd[t] : 0.f;
+    }
     auto load = [&](int kk) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int i = tid + 256 * q, r = i >> 3, c = i & 7, t = m0 + r;
             xr[q] = t < p.T ? __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H + kk) + c)
                             : make_uint4(0, 0, 0, 0);
+            if (norm) gx[q] = __ldg(reinterpret_cast<const uint4*>(p.gamma + kk) + c);
         }
 #pragma unroll
         for (int q = 0; q < nw4; ++q) {
@@ -225,7 +265,7 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int i = tid + 256 * q, r = i >> 3, c = i & 7;
-            *reinterpret_cast<uint4*>(sx + r * kRPitch + c * 8) = xr[q];
+            *reinterpret_cast<uint4*>(sx + r * kRPitch + c * 8) = norm ? rms_apply8(xr[q], rs[q], gx[q]) : xr[q];
         }
 #pragma unroll
         for (int q = 0; q < nw4; ++q) {
@@ -325,7 +365,8 @@ __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
 
 // x [T, H] bf16 -> xq codes, xs scales. Four threads share a 128-value block (32 values
 // each, two shuffles for the block maximum), so the per-block work is spread thinly.
-__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, int T, int H, uint8_t* xq, float* xs) {
+__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, int T, int H, uint8_t* xq, float* xs,
+                                                        const uint16_t* gamma, const float* rstd) {
     const int Hb = H / kBlk;
     const long nq = (long)T * Hb * 4;  // quarters; a group of 4 threads = one block
     // the loop condition is the same for every lane of a warp (the shuffles need all 32)
@@ -341,6 +382,12 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, int T
         uint4 u[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) u[c] = __ldg(src + c);
+        if (gamma) {  // stage M applied on the fly
+            const uint4* gs = reinterpret_cast<const uint4*>(gamma + kb * kBlk + q * 32);
+            const float r = rstd[t];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) u[c] = rms_apply8(u[c], r, __ldg(gs + c));
+        }
         float v[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -371,19 +418,46 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, int T
     }
 }
 
+// ---- stage M as a kernel of its own (large T, and the stand-alone moe_rmsnorm):
+// one warp per token row writes 1/rms (rstd != nullptr) and/or the normalised row.
+__global__ void __launch_bounds__(256) rms_kernel(const uint16_t* x, int T, int H, const uint16_t* gamma, float eps,
+                                                  float* rstd, uint16_t* x_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    const uint16_t* row = x + (size_t)t * H;
+    const float r = rms_rstd(warp_row_sumsq(row, H), H, eps);
+    if (rstd && lane == 0) rstd[t] = r;
+    if (x_out) {
+        const uint4* src = reinterpret_cast<const uint4*>(row);
+        const uint4* g = reinterpret_cast<const uint4*>(gamma);
+        uint4* dst = reinterpret_cast<uint4*>(x_out + (size_t)t * H);
+        for (int c = lane; c < H / 8; c += 32) dst[c] = rms_apply8(__ldg(src + c), r, __ldg(g + c));
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs, cudaStream_t st) {
+cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs, const NormArgs& nm,
+                             cudaStream_t st) {
     const long nq = (long)T * (H / kBlk) * 4;
     const int grid = (int)std::min<long>((nq + 255) / 256, (long)num_sms() * 8);
-    quant_act_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, xq, xs);
+    quant_act_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, xq, xs, nm.gamma, nm.rstd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const void* x, int T, int H, const NormArgs& nm, void* x_out, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    rms_kernel<<<(T + 7) / 8, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, nm.gamma, nm.eps, nm.rstd,
+                                            static_cast<uint16_t*>(x_out));
     return cudaGetLastError();
 }
 
 cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, uint8_t* xq,
                                float* xs, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
-                               RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl, cudaStream_t st) {
+                               RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl, const NormArgs& nm,
+                               cudaStream_t st) {
     RouteSmallParams p;
     p.H = c.hidden;
     p.E = c.n_routed;
@@ -406,6 +480,8 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
     p.groups = groups;
     p.group_of_row = group_of_row;
     p.ctrl = ctrl;
+    p.gamma = nm.gamma;
+    p.eps = nm.eps;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.n_routed);
     cfg.blockDim = dim3(kRouteWarps * 32);
@@ -420,7 +496,7 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
 
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, int splits,
-                               cudaStream_t st) {
+                               const NormArgs& nm, cudaStream_t st) {
     RouterMmaParams g;
     g.H = c.hidden;
     g.E = c.n_routed;
@@ -431,6 +507,8 @@ cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, cons
     g.x = static_cast<const uint16_t*>(x);
     g.wr = w_router;
     g.part = logits;
+    g.gamma = nm.gamma;
+    g.rstd = nm.rstd;
     const size_t smem = ((size_t)kRM + 3 * (size_t)g.Ep) * kRPitch * sizeof(uint16_t);
     const dim3 grid((T + kRM - 1) / kRM, splits);
     auto run = [&](auto kern) -> cudaError_t {

@@ -87,7 +87,7 @@ extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const void* x
     uint8_t* xq = base + kCtrlBytes + kLogitsBytes;
     float* xs = reinterpret_cast<float*>(base + kCtrlBytes + kLogitsBytes + kXqBytes);
     if (launch_route_small(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, logits, xq, xs, nullptr,
-                           nullptr, nullptr, nullptr, nullptr, ctrl, st) != cudaSuccess)
+                           nullptr, nullptr, nullptr, nullptr, ctrl, NormArgs{}, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
