@@ -37,6 +37,7 @@ __all__ = [
     "Workload",
     "WORKLOADS",
     "make_weights",
+    "make_weights_mx",
     "make_router",
     "make_tokens",
     "replicate_weights",
@@ -127,11 +128,34 @@ def _quantise_blocks(w: torch.Tensor):
     return codes.contiguous(), scale.to(torch.float32).contiguous()
 
 
-def _expert_stack(E, R, C, seed, name, device, std=0.02):
+def _quantise_mx(w: torch.Tensor):
+    """w fp32 [..., R, C] -> (E4M3 codes uint8 [..., R, C], E8M0 scale bytes uint8 [..., R, C/32]).
+
+    MXFP8 data preparation: per row and 32 consecutive columns, the scale is the smallest
+    power of two 2^k with amax <= 448 * 2^k (k >= -126; amax = 0 gives 2^0), stored as the
+    byte k + 127; codes are torch's float8_e4m3fn conversion (round to nearest even) of
+    the clamped quotient. Both sides receive the same codes and scale bytes."""
+    *lead, R, C = w.shape
+    blk = w.reshape(*lead, R, C // 32, 32)
+    amax = blk.abs().amax(dim=-1)
+    m, e = torch.frexp(amax)  # amax = m * 2^e, m in [0.5, 1); 448 = 0.875 * 2^9
+    k = torch.where(m <= 0.875, e - 9, e - 8)
+    k = torch.where(amax > 0, k, torch.zeros_like(k)).clamp(min=-126)
+    scale = torch.ldexp(torch.ones_like(amax), k)
+    q = (blk / scale[..., None]).clamp_(-448.0, 448.0)
+    codes = q.reshape(*lead, R, C).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), (k + 127).to(torch.uint8).contiguous()
+
+
+def _expert_stack(E, R, C, seed, name, device, std=0.02, mx=False):
     codes = torch.empty((E, R, C), dtype=torch.uint8, device=device)
-    scales = torch.empty((E, R // 128, C // 128), dtype=torch.float32, device=device)
+    if mx:
+        scales = torch.empty((E, R, C // 32), dtype=torch.uint8, device=device)
+    else:
+        scales = torch.empty((E, R // 128, C // 128), dtype=torch.float32, device=device)
+    quant = _quantise_mx if mx else _quantise_blocks
     for e in range(E):  # one expert at a time keeps the fp32 temporaries small
-        c, s = _quantise_blocks(_randn((R, C), seed, f"{name}[{e}]", device, std))
+        c, s = quant(_randn((R, C), seed, f"{name}[{e}]", device, std))
         codes[e].copy_(c)
         scales[e].copy_(s)
     return codes, scales
@@ -170,6 +194,31 @@ def make_weights(cfg: MoEConfig, seed: int, device="cpu", zipf: bool = False,
     if cfg.n_shared > 0:
         for nm, (R, C) in (("gate", (Is, H)), ("up", (Is, H)), ("down", (H, Is))):
             c, s = _quantise_blocks(_randn((R, C), seed, f"ws_{nm}", device, 0.02))
+            out[f"ws_{nm}"], out[f"ss_{nm}"] = c, s
+    else:
+        for nm in ("gate", "up", "down"):
+            out[f"ws_{nm}"] = out[f"ss_{nm}"] = None
+    return out
+
+
+def make_weights_mx(cfg: MoEConfig, seed: int, device="cpu", zipf: bool = False,
+                    zipf_beta: Optional[float] = None) -> Dict[str, Optional[torch.Tensor]]:
+    """The layer of make_weights (the same fp32 draws) quantised to MXFP8 instead.
+
+    w_gate, w_up  uint8 (E4M3 codes) [E, I, H]   s_gate, s_up  uint8 (E8M0) [E, I, H/32]
+    w_down        uint8 [E, H, I]                s_down        uint8 (E8M0) [E, H, I/32]
+    ws_gate/ws_up uint8 [Is, H], ws_down [H, Is] with E8M0 scales [Is, H/32], [H, Is/32]
+    w_router      fp32 [E, H]                    router_bias   fp32 [E] or None
+    """
+    H, I, E, Is = cfg.hidden, cfg.moe_inter, cfg.n_routed, cfg.shared_inter
+    out: Dict[str, Optional[torch.Tensor]] = {}
+    out["w_router"], out["router_bias"] = make_router(cfg, seed, device, zipf, zipf_beta)
+    out["w_gate"], out["s_gate"] = _expert_stack(E, I, H, seed, "w_gate", device, mx=True)
+    out["w_up"], out["s_up"] = _expert_stack(E, I, H, seed, "w_up", device, mx=True)
+    out["w_down"], out["s_down"] = _expert_stack(E, H, I, seed, "w_down", device, mx=True)
+    if cfg.n_shared > 0:
+        for nm, (R, C) in (("gate", (Is, H)), ("up", (Is, H)), ("down", (H, Is))):
+            c, s = _quantise_mx(_randn((R, C), seed, f"ws_{nm}", device, 0.02))
             out[f"ws_{nm}"], out[f"ss_{nm}"] = c, s
     else:
         for nm in ("gate", "up", "down"):

@@ -75,6 +75,10 @@ def _load():
             lib.orc_expert_row.argtypes = [_P, _P, _P, ctypes.c_int, ctypes.c_double, _P, _P]
             lib.orc_shared_row.argtypes = [_P, _P, _P, _P]
             lib.orc_forward_tokens.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P]
+            lib.orc_e8m0_decode.restype = ctypes.c_double
+            lib.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_quant_rows_mx.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P]
+            lib.orc_forward_tokens_mx.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P]
             lib.orc_num_threads.restype = ctypes.c_int
             lib.orc_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -124,6 +128,17 @@ class Weights:
         self.struct = _Weights(*[_ptr(self.arrays[k]) for k in
                                  ("w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down",
                                   "ws_gate", "ws_up", "ws_down", "ss_gate", "ss_up", "ss_down")])
+
+
+class WeightsMX:
+    """Host copies of one layer's MXFP8 weights (same keys as synth.make_weights_mx):
+    E4M3 codes and E8M0 scale bytes per (row, 32 consecutive K)."""
+
+    KEYS = Weights.KEYS
+
+    def __init__(self, weights: dict):
+        self.arrays = {k: _np(weights.get(k), np.uint8) for k in self.KEYS}
+        self.struct = _Weights(*[_ptr(self.arrays[k]) for k in self.KEYS])
 
 
 def num_threads() -> int:
@@ -180,6 +195,24 @@ def rmsnorm(h_bf16, gamma_bf16, eps: float, return_exact=False):
     ex = np.empty((T, H), np.float64)
     lib.orc_rmsnorm(_ptr(h), T, H, _ptr(g), float(eps), _ptr(x), _ptr(ex))
     return (x, ex) if return_exact else x
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.orc_e8m0_decode(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def quant_rows_mx(v) -> tuple:
+    """Per (row, 32-column block) MXFP8 quantisation: (codes uint8 [R,N], E8M0 scales uint8 [R,N/32])."""
+    lib = _load()
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+    R, N = v.shape
+    assert N % 32 == 0
+    q = np.empty((R, N), np.uint8)
+    s = np.empty((R, N // 32), np.uint8)
+    lib.orc_quant_rows_mx(_ptr(v), R, N, _ptr(q), _ptr(s))
+    return q, s
 
 
 def router_logits(cfg, x_bf16, w_router, bias=None) -> np.ndarray:
@@ -263,6 +296,24 @@ def forward_tokens(cfg, weights: Weights, x_bf16, ids, w, tokens=None, residual_
     c = _cfg(cfg, act_quant)
     lib.orc_forward_tokens(ctypes.byref(c), ctypes.byref(weights.struct), _ptr(x), _ptr(ids), _ptr(w),
                            _ptr(r), _ptr(tokens), len(tokens), _ptr(out))
+    return out
+
+
+def forward_tokens_mx(cfg, weights: WeightsMX, x_bf16, ids, w, tokens=None, residual_bf16=None,
+                      act_quant=True) -> np.ndarray:
+    """MXFP8 layer output (fp64) for the listed tokens, given the routing of all tokens."""
+    lib = _load()
+    x = _np(x_bf16, np.uint16)
+    T = x.shape[0]
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(
+        np.asarray(tokens, dtype=np.int32))
+    r = _np(residual_bf16, np.uint16)
+    out = np.empty((len(tokens), cfg.hidden), np.float64)
+    c = _cfg(cfg, act_quant)
+    lib.orc_forward_tokens_mx(ctypes.byref(c), ctypes.byref(weights.struct), _ptr(x), _ptr(ids), _ptr(w),
+                              _ptr(r), _ptr(tokens), len(tokens), _ptr(out))
     return out
 
 

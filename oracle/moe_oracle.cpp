@@ -418,6 +418,122 @@ void orc_forward_tokens(const orc_cfg_t* c, const orc_weights_t* W, const uint16
     }
 }
 
+// ------------------------------------------------------------------ MXFP8
+// The MXFP8 variant of the expert MLPs: E4M3 codes with one UE8M0 (power-of-two)
+// scale per 32 consecutive values along K, for the weights (per output row) and the
+// activations (per token) alike ("MXFP8 routed experts", Mixture-of-Kittens Table 2;
+// the "block_fp8 -> mxfp8" load-time scale conversion and "MXFP8 input quantization"
+// of the DeepSeek-V4.1 Flash lecture, "Round 1->2" and "Rounds 12-15").
+// An E8M0 byte b encodes 2^(b-127); 0xFF is NaN.
+double orc_e8m0_decode(uint8_t b) {
+    if (b == 0xFF) return std::numeric_limits<double>::quiet_NaN();
+    return std::ldexp(1.0, (int)b - 127);
+}
+
+// One block of 32 values: the scale rule of orc_quant_block (the smallest 2^k with
+// amax <= 448 * 2^k; amax = 0 gives 2^0), with k kept >= -126 (a block whose amax is
+// below 448 * 2^-127 still gets 2^-126), stored as the byte k + 127.
+static void quant_block_mx(const double* v, uint8_t* q, uint8_t* s) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(v[i]));
+    int k = 0;
+    if (amax > 0.0) {
+        k = (int)std::ceil(std::log2(amax / 448.0));
+        while (amax > 448.0 * std::ldexp(1.0, k)) ++k;
+        while (amax <= 448.0 * std::ldexp(1.0, k - 1)) --k;
+        if (k < -126) k = -126;
+    }
+    const double scale = std::ldexp(1.0, k);
+    for (int i = 0; i < 32; ++i) q[i] = (amax > 0.0) ? orc_e4m3_encode(v[i] / scale) : 0;
+    *s = (uint8_t)(k + 127);
+}
+
+// Rows of n values (n a multiple of 32) -> codes [rows, n] and E8M0 scales [rows, n/32].
+void orc_quant_rows_mx(const double* v, int rows, int n, uint8_t* q, uint8_t* s) {
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < n / 32; ++b)
+            quant_block_mx(v + (size_t)r * n + b * 32, q + (size_t)r * n + b * 32, s + (size_t)r * (n / 32) + b);
+}
+
+static void quant_dequant_mx(const double* v, int n, double* vhat) {
+    uint8_t q[32], s;
+    for (int b = 0; b < n / 32; ++b) {
+        quant_block_mx(v + b * 32, q, &s);
+        for (int i = 0; i < 32; ++i) vhat[b * 32 + i] = orc_e4m3_decode(q[i]) * orc_e8m0_decode(s);
+    }
+}
+
+// One MXFP8 expert MLP (the steps of expert_mlp with per-32 E8M0 scales):
+//   W[o][i] = dec(code[o][i]) * 2^(s[o][i/32] - 127)   for Wg, Wu [N, H] and Wd [H, N]
+//   g = Wg . xhat, u = Wu . xhat, a = SiLU(g) * u, ahat = MX quantise-dequantise of a,
+//   y (+)= w * (Wd . ahat)
+static void expert_mlp_mx(const double* dec_tab, int H, int N, int act_quant, const double* xhat,
+                          const uint8_t* wg, const uint8_t* sg, const uint8_t* wu, const uint8_t* su,
+                          const uint8_t* wd, const uint8_t* sd, double w, double* y, int accumulate) {
+    const int H32 = H / 32, N32 = N / 32;
+    std::vector<double> a(N), ahat(N);
+    for (int o = 0; o < N; ++o) {
+        double g = 0.0, u = 0.0;
+        for (int i = 0; i < H; ++i) {
+            g += dec_tab[wg[(size_t)o * H + i]] * orc_e8m0_decode(sg[(size_t)o * H32 + i / 32]) * xhat[i];
+            u += dec_tab[wu[(size_t)o * H + i]] * orc_e8m0_decode(su[(size_t)o * H32 + i / 32]) * xhat[i];
+        }
+        a[o] = g / (1.0 + std::exp(-g)) * u;
+    }
+    if (act_quant)
+        quant_dequant_mx(a.data(), N, ahat.data());
+    else
+        ahat = a;
+    for (int o = 0; o < H; ++o) {
+        double acc = 0.0;
+        for (int i = 0; i < N; ++i)
+            acc += dec_tab[wd[(size_t)o * N + i]] * orc_e8m0_decode(sd[(size_t)o * N32 + i / 32]) * ahat[i];
+        y[o] = (accumulate ? y[o] : 0.0) + w * acc;
+    }
+}
+
+typedef struct {
+    const uint8_t *w_gate, *w_up, *w_down;     // E4M3 codes, layouts as orc_weights_t
+    const uint8_t *s_gate, *s_up, *s_down;     // E8M0 [E,I,H/32], [E,I,H/32], [E,H,I/32]
+    const uint8_t *ws_gate, *ws_up, *ws_down;  // shared codes [Is,H], [Is,H], [H,Is]
+    const uint8_t *ss_gate, *ss_up, *ss_down;  // E8M0 [Is,H/32], [Is,H/32], [H,Is/32]
+} orc_weights_mx_t;
+
+// R with MXFP8 experts, for the listed tokens (as orc_forward_tokens):
+//   out[i] = sum_j w[t][j] * expert_mx_{ids[t][j]}(xhat_t) + shared_mx(xhat_t) (+ residual[t])
+// where xhat_t is the MX quantise-dequantise of the bf16 row (act_quant on).
+void orc_forward_tokens_mx(const orc_cfg_t* c, const orc_weights_mx_t* W, const uint16_t* x_bf16,
+                           const int32_t* ids, const double* w, const uint16_t* residual_bf16,
+                           const int32_t* tokens, int n_tokens, double* out) {
+    const int H = c->hidden, I = c->moe_inter, k = c->top_k;
+    const int Is = c->n_shared * I;
+    double tab[256];
+    make_dec_tab(tab);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < n_tokens; ++i) {
+        const int t = tokens[i];
+        std::vector<double> xv(H), xhat(H);
+        for (int h = 0; h < H; ++h) xv[h] = bf16_to_double(x_bf16[(size_t)t * H + h]);
+        if (c->act_quant)
+            quant_dequant_mx(xv.data(), H, xhat.data());
+        else
+            xhat = xv;
+        double* o = out + (size_t)i * H;
+        for (int h = 0; h < H; ++h) o[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const size_t e = (size_t)ids[(size_t)t * k + j];
+            expert_mlp_mx(tab, H, I, c->act_quant, xhat.data(), W->w_gate + e * I * H,
+                          W->s_gate + e * I * (H / 32), W->w_up + e * I * H, W->s_up + e * I * (H / 32),
+                          W->w_down + e * H * I, W->s_down + e * H * (I / 32), w[(size_t)t * k + j], o, 1);
+        }
+        if (c->n_shared > 0)
+            expert_mlp_mx(tab, H, Is, c->act_quant, xhat.data(), W->ws_gate, W->ss_gate, W->ws_up, W->ss_up,
+                          W->ws_down, W->ss_down, 1.0, o, 1);
+        if (residual_bf16)
+            for (int h = 0; h < H; ++h) o[h] += bf16_to_double(residual_bf16[(size_t)t * H + h]);
+    }
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
