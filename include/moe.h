@@ -64,6 +64,20 @@ typedef struct moe_weights {
     const float *w_router, *router_bias;
 } moe_weights_t;
 
+/* One layer's weights in the MXFP8 variant ("MXFP8 routed experts", Mixture-of-Kittens
+ * Table 2; "block_fp8 -> mxfp8", DeepSeek-V4.1 Flash lecture): E4M3 codes as in
+ * moe_weights_t, with one UE8M0 scale byte b (value 2^(b-127)) per row and 32
+ * consecutive K instead of the fp32 128x128 block scales:
+ *   s_gate, s_up   [E, I, H/32]   s_down [E, H, I/32]
+ *   ss_gate, ss_up [Is, H/32]     ss_down [H, Is/32]        (u8, row-major) */
+typedef struct moe_weights_mx {
+    const uint8_t *w_gate, *w_up, *w_down;
+    const uint8_t *s_gate, *s_up, *s_down;
+    const uint8_t *ws_gate, *ws_up, *ws_down;
+    const uint8_t *ss_gate, *ss_up, *ss_down;
+    const float *w_router, *router_bias;
+} moe_weights_mx_t;
+
 typedef enum moe_status {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = -1,       /* NULL / misaligned pointer, negative T */
@@ -224,6 +238,32 @@ moe_status_t moe_forward_rmsnorm_profiled(const moe_config_t* cfg, const void* h
                                           const void* gamma_bf16, float eps, const moe_weights_t* weights,
                                           void* out_bf16, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
                                           void* stream, const moe_stage_events_t* events);
+
+/* ------------------------------------------------------------ MXFP8 variant
+ * The layer with moe_weights_mx_t weights and MXFP8 activations: x and the
+ * intermediate a = SiLU(g) * u are quantised per token and 32 consecutive values
+ * (scale = the smallest 2^k, k >= -126, with amax <= 448 * 2^k; codes RNE E4M3), and
+ * the expert GEMMs apply all scales inside the tensor core (tcgen05.mma
+ * kind::mxf8f6f4). Routing is that of moe_route. Shapes: hidden % 512 == 0 and
+ * moe_inter % 512 == 0 (MOE_ERR_UNSUPPORTED_SHAPE otherwise; moe_workspace_size_mx
+ * returns 0). Every T runs the grouped tensor-core GEMM. */
+size_t moe_workspace_size_mx(const moe_config_t* cfg, int32_t max_tokens);
+
+/* MXFP8 activation quantisation: x_bf16 [T, H] -> xq [T, H] E4M3 codes and
+ * xs_e8m0 [T, H/32] scale bytes. */
+moe_status_t moe_quant_act_mx(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq, uint8_t* xs_e8m0,
+                              void* stream);
+
+/* moe_forward in the MXFP8 variant (workspace from moe_workspace_size_mx). */
+moe_status_t moe_forward_mx(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_mx_t* weights,
+                            const void* residual_bf16, void* out_bf16, int32_t* topk_ids_out, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/* moe_forward_mx with CUDA events around each stage. */
+moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                                     const moe_weights_mx_t* weights, const void* residual_bf16, void* out_bf16,
+                                     int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream,
+                                     const moe_stage_events_t* events);
 
 #ifdef __cplusplus
 }

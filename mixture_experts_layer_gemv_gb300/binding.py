@@ -45,6 +45,10 @@ class moe_weights_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in _WEIGHT_FIELDS]
 
 
+class moe_weights_mx_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _WEIGHT_FIELDS]
+
+
 class moe_stage_events_t(ctypes.Structure):
     _fields_ = [("start", ctypes.c_void_p * 5), ("stop", ctypes.c_void_p * 5)]
 
@@ -68,6 +72,10 @@ _SIGNATURES = {
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P]),
     "moe_forward": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_profiled": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "moe_workspace_size_mx": (_SZ, [_P, _I32]),
+    "moe_quant_act_mx": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
+    "moe_forward_mx": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_mx_profiled": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P, _P]),
 }
 
 _lib = None
@@ -249,6 +257,55 @@ def moe_forward_rmsnorm(cfg, h, gamma, eps, weights, out, topk_ids_out=None, ws=
                                                             float(eps), ctypes.byref(W), _ptr(out),
                                                             _ptr(topk_ids_out), _ptr(ws), ws.numel(),
                                                             _stream(stream)))
+
+
+# ------------------------------------------------------------ MXFP8 variant
+def weights_mx_struct(weights: Dict[str, Optional[torch.Tensor]]) -> moe_weights_mx_t:
+    return moe_weights_mx_t(*[_ptr(weights.get(n)) for n in _WEIGHT_FIELDS])
+
+
+def moe_workspace_size_mx(cfg: MoEConfig, max_tokens: int) -> int:
+    c = config_struct(cfg)
+    return int(lib().moe_workspace_size_mx(ctypes.byref(c), int(max_tokens)))
+
+
+def alloc_workspace_mx(cfg: MoEConfig, max_tokens: int, device="cuda") -> torch.Tensor:
+    n = moe_workspace_size_mx(cfg, max_tokens)
+    if n == 0:
+        raise MoeError("moe_workspace_size_mx", -2, "config not supported by the MXFP8 variant")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws)
+    return ws
+
+
+def moe_quant_act_mx(x: torch.Tensor, xq: torch.Tensor, xs8: torch.Tensor, stream=None) -> None:
+    T, H = x.shape
+    _check("moe_quant_act_mx", lib().moe_quant_act_mx(_ptr(x), T, H, _ptr(xq), _ptr(xs8), _stream(stream)))
+
+
+def moe_forward_mx(cfg, x, weights, out, residual=None, topk_ids_out=None, ws=None, stream=None,
+                   events: Optional[Dict[str, tuple]] = None) -> None:
+    """out[T, H] = MoE layer(x) with MXFP8 experts (weights from synth.make_weights_mx)."""
+    c = config_struct(cfg)
+    W = weights_mx_struct(weights)
+    if events:
+        st = lib().moe_forward_mx_profiled(ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W), _ptr(residual),
+                                           _ptr(out), _ptr(topk_ids_out), _ptr(ws), ws.numel(), _stream(stream),
+                                           ctypes.byref(_events_struct(events)))
+        _check("moe_forward_mx_profiled", st)
+        return
+    _check("moe_forward_mx", lib().moe_forward_mx(ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W),
+                                                  _ptr(residual), _ptr(out), _ptr(topk_ids_out), _ptr(ws),
+                                                  ws.numel(), _stream(stream)))
+
+
+def forward_mx(cfg: MoEConfig, x: torch.Tensor, weights, residual=None, ws=None, return_ids=False):
+    T = x.shape[0]
+    ws = alloc_workspace_mx(cfg, T, x.device) if ws is None else ws
+    out = torch.empty_like(x)
+    ids = torch.empty((T, cfg.top_k), dtype=torch.int32, device=x.device) if return_ids else None
+    moe_forward_mx(cfg, x, weights, out, residual, ids, ws)
+    return (out, ids) if return_ids else out
 
 
 def forward(cfg: MoEConfig, x: torch.Tensor, weights, residual=None, ws=None, return_ids=False):

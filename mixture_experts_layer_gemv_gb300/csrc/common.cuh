@@ -64,6 +64,20 @@ __device__ __forceinline__ float act_scale_pow2(float amax, float* inv_scale) {
     return ldexpf(1.f, k);
 }
 
+// The same scale as an E8M0 byte (k + 127) for the MXFP8 variant.
+__device__ __forceinline__ uint32_t act_scale_e8m0(float amax, float* inv_scale) {
+    if (!(amax > 0.f)) {
+        *inv_scale = 1.f;
+        return 127u;
+    }
+    int e;
+    const float m = frexpf(amax, &e);
+    int k = (m <= 0.875f) ? e - 9 : e - 8;
+    k = k < -126 ? -126 : k;
+    *inv_scale = ldexpf(1.f, -k);
+    return (uint32_t)(k + 127);
+}
+
 // Four fp32 values -> four E4M3 codes (round to nearest even, saturating), packed
 // little-endian in one 32-bit word (value 0 in the low byte).
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
@@ -348,6 +362,58 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(const void* p) {
     d |= (uint64_t)1 << 46;           // descriptor version
     d |= (uint64_t)2 << 61;           // layout: 128-byte swizzle
     return d;
+}
+
+// Shared-memory descriptor of a plain row-major matrix of 16-byte rows (no swizzle):
+// 8-row core matrices 128 bytes apart. The source of a 128x128b tcgen05.cp.
+__device__ __forceinline__ uint64_t smem_desc_rows16(const void* p) {
+    const uint64_t addr = smem_u32(p);
+    uint64_t d = 0;
+    d |= (addr & 0x3FFFFull) >> 4;    // start address
+    d |= (uint64_t)1 << 16;           // leading byte offset (one core matrix along K: unused)
+    d |= (uint64_t)(128 >> 4) << 32;  // stride byte offset: 8-row group pitch
+    d |= (uint64_t)1 << 46;           // descriptor version
+    return d;                         // layout field 0: no swizzle
+}
+
+// Copy 32 rows x 16 bytes of shared memory into tensor memory, the same data into each
+// of the four 32-lane quadrants: row i -> lane 32q + i of 4 consecutive 32-bit columns
+// from taddr (q = 0..3). Ordered with the issuing thread's later tcgen05.mma; its
+// completion is tracked by tcgen05.commit like an MMA's.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+// Make this thread's generic shared-memory writes visible to the async proxy
+// (tcgen05.cp / tcgen05.mma operand reads) that a later barrier hand-off orders.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// D(tmem, fp32) (+)= (A * 2^(sfA-127)) * (B * 2^(sfB-127))^T with E4M3 operands and one
+// UE8M0 scale factor per row and 32-wide K step, read from tensor memory. A scale
+// group of 128 rows occupies 4 columns from sfa_tmem (sfb_tmem, a multiple of 4): the
+// rows of lane quadrant q are read from column q, lane 32q + i holding the four K-step
+// bytes of row 32q + i; the descriptor's scale-factor ids pick the byte.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4: E4M3 x E4M3 -> fp32, both K-major, M x N,
+// UE8M0 scale factors, byte sf_id of the A and B scale words.
+__host__ __device__ constexpr uint32_t idesc_mx_f32(int M, int N, int sf_id) {
+    return ((uint32_t)sf_id << 4)           // B scale-factor byte
+           | (0u << 7) | (0u << 10)         // A, B: E4M3
+           | ((uint32_t)(N >> 3) << 17)     // N / 8
+           | (1u << 23)                     // scale factors: UE8M0
+           | ((uint32_t)(M >> 4) << 24)     // M / 16
+           | ((uint32_t)sf_id << 29);       // A scale-factor byte
 }
 
 // Instruction descriptor: E4M3 x E4M3 -> fp32, both operands K-major, M x N.

@@ -23,8 +23,8 @@ int num_sms() {
 
 static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
-int router_splits_for(const moe_config_t& c, int64_t T) {
-    if (T <= kSmallT) return 1;
+int router_splits_for(const moe_config_t& c, int64_t T, bool large_route) {
+    if (T <= kSmallT && !large_route) return 1;  // the fused small-T route kernel
     const int64_t tiles = (T + 63) / 64;     // router CTAs: 64 tokens x all experts each
     int64_t s = (304 + tiles - 1) / tiles;  // aim at two CTAs per SM of a 152-SM part
     const int64_t hb = c.hidden / 128;
@@ -42,7 +42,7 @@ int max_routed_groups(const moe_config_t& c, int64_t T) {
 // Many tokens per expert: the grouped tensor-core GEMM instead of the streaming GEMVs.
 bool use_gemm(const moe_config_t& c, int64_t T) { return T > kSmallT && gemm_supported(c); }
 
-WsLayout ws_layout(const moe_config_t& c, int64_t T) {
+WsLayout ws_layout(const moe_config_t& c, int64_t T, bool mx) {
     WsLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -53,7 +53,7 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     const size_t H = c.hidden, I = c.moe_inter, E = c.n_routed, k = c.top_k;
     const size_t Is = (size_t)c.n_shared * c.moe_inter;
     const size_t t = (size_t)T;
-    L.router_splits = router_splits_for(c, T);
+    L.router_splits = router_splits_for(c, T, mx);
     L.max_groups = max_routed_groups(c, T);
     L.ctrl = take(kCtrlRegionBytes);
     L.logits = take((size_t)L.router_splits * t * E * 4);  // router split-K partials
@@ -69,9 +69,9 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
     L.group_of_row = take(t * k * 4);
     // the streaming GEMVs' partial sums; on the GEMM path they stay sized for kSmallT
     // tokens so that the workspace size never shrinks as T grows
-    const bool gemm = use_gemm(c, T);
-    const size_t ts = gemm ? (size_t)kSmallT : t;
-    const size_t P = (size_t)stream_max_parts(c, (int64_t)ts);
+    const bool gemm = mx || use_gemm(c, T);
+    const size_t ts = mx ? 0 : gemm ? (size_t)kSmallT : t;
+    const size_t P = mx ? 0 : (size_t)stream_max_parts(c, (int64_t)ts);
     {
         const size_t t = ts;
     L.g_r = take(P * t * k * I * 4);
@@ -97,6 +97,13 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T) {
         L.hs_r = take(t * k * (I / 128) * 4);
         L.hs_s = take(t * (Is / 128) * 4);
         L.mtiles = take((size_t)L.max_mtiles * sizeof(MTile));
+    }
+    L.xs8 = L.xs8_perm = L.hs8_r = L.hs8_s = 0;
+    if (mx) {
+        L.xs8 = take(t * (H / 32));
+        L.xs8_perm = take(t * k * (H / 32));
+        L.hs8_r = take(t * k * (I / 32));
+        L.hs8_s = take(t * (Is / 32));
     }
     L.y_perm = take(t * k * H * 2);
     L.y_shared = take(t * H * 2);
@@ -304,6 +311,95 @@ cudaError_t run_expert_gemms(const moe_config_t* c, int32_t T, const moe_weights
     if (e != cudaSuccess) return e;
     if (mark->end(MOE_STAGE_DOWN) != MOE_OK) return cudaErrorUnknown;
     return cudaSuccess;
+}
+
+// The MXFP8 variant's two grouped-GEMM launches (scales through the tensor core).
+cudaError_t run_expert_gemms_mx(const moe_config_t* c, int32_t T, const moe_weights_mx_t* W, const WsLayout& L,
+                                void* ws, const int32_t* perm_src, const float* topk_w, __nv_bfloat16* y_perm,
+                                __nv_bfloat16* y_shared, const StageMark* mark) {
+    const int H = c->hidden, I = c->moe_inter, E = c->n_routed, k = c->top_k;
+    const int Is = c->n_shared * c->moe_inter;
+    const bool sh = Is > 0;
+    const uint64_t n = (uint64_t)T * k;
+    cudaStream_t st = mark->st;
+    GemmArgs g = {};
+    g.H = H;
+    g.I = I;
+    g.Is = Is;
+    g.T = T;
+    g.k = k;
+    g.n_mt_s = sh ? (T + 127) / 128 : 0;
+    g.ctrl = at<Ctrl>(ws, L.ctrl);
+    g.mtiles = at<MTile>(ws, L.mtiles);
+    g.perm_src = perm_src;
+    g.topk_w = topk_w;
+    g.hq_r = at<uint8_t>(ws, L.hq_r);
+    g.hq_s = at<uint8_t>(ws, L.hq_s);
+    g.hs8_r = at<uint8_t>(ws, L.hs8_r);
+    g.hs8_s = at<uint8_t>(ws, L.hs8_s);
+    g.y_perm = y_perm;
+    g.y_shared = y_shared;
+    g.status = &at<Ctrl>(ws, L.ctrl)->status;
+
+    TmaMaps m = {};
+    // gate/up: A = permuted activation codes (routed) / token-order codes (shared)
+    g.mode = 0;
+    g.K_r = g.K_s = H;
+    g.nt_r = I / 128;
+    g.nt_s = Is / 128;
+    g.sfa_r = at<uint8_t>(ws, L.xs8_perm);
+    g.sfa_s = at<uint8_t>(ws, L.xs8);
+    g.sfb0_r = W->s_gate;
+    g.sfb1_r = W->s_up;
+    g.sfb0_s = W->ss_gate;
+    g.sfb1_s = W->ss_up;
+    if (!tmap_u8_2d(&m.a_r, at<uint8_t>(ws, L.xq_perm), n, H, 128, 128) ||
+        !tmap_u8_2d(&m.b0_r, W->w_gate, (uint64_t)E * I, H, 128, 128) ||
+        !tmap_u8_2d(&m.b1_r, W->w_up, (uint64_t)E * I, H, 128, 128))
+        return cudaErrorInvalidValue;
+    if (sh && (!tmap_u8_2d(&m.a_s, at<uint8_t>(ws, L.xq), T, H, 128, 128) ||
+               !tmap_u8_2d(&m.b0_s, W->ws_gate, Is, H, 128, 128) || !tmap_u8_2d(&m.b1_s, W->ws_up, Is, H, 128, 128)))
+        return cudaErrorInvalidValue;
+    if (mark->begin(MOE_STAGE_GATE_UP) != MOE_OK) return cudaErrorUnknown;
+    cudaError_t e = launch_expert_gemm_mx(g, m, st);
+    if (e != cudaSuccess) return e;
+    if (mark->end(MOE_STAGE_GATE_UP) != MOE_OK) return cudaErrorUnknown;
+
+    // down: A = the FP8 intermediate, B = 256 hidden rows per tile (two 128-row halves)
+    g.mode = 1;
+    g.K_r = I;
+    g.K_s = Is;
+    g.nt_r = g.nt_s = H / 256;
+    m = TmaMaps{};
+    g.sfa_r = g.hs8_r;
+    g.sfa_s = g.hs8_s;
+    g.sfb0_r = g.sfb1_r = W->s_down;  // the B halves are rows yb0 and yb0 + 128 of one tensor
+    g.sfb0_s = g.sfb1_s = W->ss_down;
+    if (!tmap_u8_2d(&m.a_r, g.hq_r, n, I, 128, 128) || !tmap_u8_2d(&m.b0_r, W->w_down, (uint64_t)E * H, I, 128, 128))
+        return cudaErrorInvalidValue;
+    m.b1_r = m.b0_r;
+    if (sh && (!tmap_u8_2d(&m.a_s, g.hq_s, T, Is, 128, 128) || !tmap_u8_2d(&m.b0_s, W->ws_down, H, Is, 128, 128)))
+        return cudaErrorInvalidValue;
+    m.b1_s = m.b0_s;
+    if (mark->begin(MOE_STAGE_DOWN) != MOE_OK) return cudaErrorUnknown;
+    e = launch_expert_gemm_mx(g, m, st);
+    if (e != cudaSuccess) return e;
+    if (mark->end(MOE_STAGE_DOWN) != MOE_OK) return cudaErrorUnknown;
+    return cudaSuccess;
+}
+
+moe_status_t check_weights_mx(const moe_config_t* c, const moe_weights_mx_t* w) {
+    if (!w) return MOE_ERR_INVALID_ARG;
+    const void* req[] = {w->w_gate, w->w_up, w->w_down, w->s_gate, w->s_up, w->s_down, w->w_router};
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (c->n_shared > 0) {
+        const void* sh[] = {w->ws_gate, w->ws_up, w->ws_down, w->ss_gate, w->ss_up, w->ss_down};
+        for (const void* p : sh)
+            if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    }
+    if (w->router_bias && !aligned4(w->router_bias)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
 }
 
 }  // namespace
@@ -597,6 +693,77 @@ moe_status_t moe_forward_rmsnorm(const moe_config_t* cfg, const void* h_bf16, in
                                  void* ws, size_t ws_bytes, void* stream) {
     return moe_forward_rmsnorm_profiled(cfg, h_bf16, T, gamma_bf16, eps, weights, out_bf16, topk_ids_out, ws,
                                         ws_bytes, stream, nullptr);
+}
+
+size_t moe_workspace_size_mx(const moe_config_t* cfg, int32_t max_tokens) {
+    if (check_cfg(cfg) != MOE_OK || max_tokens < 0 || check_T(cfg, max_tokens) != MOE_OK) return 0;
+    if (!gemm_mx_supported(*cfg)) return 0;
+    return ws_layout(*cfg, max_tokens, true).total;
+}
+
+moe_status_t moe_quant_act_mx(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq, uint8_t* xs_e8m0,
+                              void* stream) {
+    if (T < 0 || H <= 0 || H % 128) return T < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !xq || !xs_e8m0 || !aligned16(x_bf16) || !aligned16(xq)) return MOE_ERR_INVALID_ARG;
+    MOE_CUDA(launch_quant_act_mx(x_bf16, T, H, xq, xs_e8m0, NormArgs{}, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                                     const moe_weights_mx_t* weights, const void* residual_bf16, void* out_bf16,
+                                     int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream,
+                                     const moe_stage_events_t* events) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_T(cfg, T));
+    if (!gemm_mx_supported(*cfg)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights_mx(cfg, weights));
+    if (!x_bf16 || !out_bf16 || !aligned16(x_bf16) || !aligned16(out_bf16)) return MOE_ERR_INVALID_ARG;
+    if ((residual_bf16 && !aligned16(residual_bf16)) || (topk_ids_out && !aligned4(topk_ids_out)))
+        return MOE_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+    const WsLayout L = ws_layout(*cfg, T, true);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const StageMark mark{events, st};
+    int32_t* ids = at<int32_t>(ws, L.ids);
+    float* w = at<float>(ws, L.w);
+    int32_t* perm_src = at<int32_t>(ws, L.perm_src);
+    int32_t* inv_pos = at<int32_t>(ws, L.inv_pos);
+    Ctrl* ctrl = at<Ctrl>(ws, L.ctrl);
+
+    MOE_TRY(mark.begin(MOE_STAGE_ROUTE));
+    MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
+                                at<float>(ws, L.logits), L.router_splits, NormArgs{}, st));
+    MOE_CUDA(launch_quant_act_mx(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs8), NormArgs{},
+                                 st));
+    MOE_TRY(mark.end(MOE_STAGE_ROUTE));
+    MOE_TRY(mark.begin(MOE_STAGE_PERMUTE));
+    MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, nullptr, nullptr,
+                            at<MTile>(ws, L.mtiles), ctrl, st));
+    MOE_CUDA(launch_gather_rows(T, cfg->hidden, cfg->top_k, perm_src, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xq_perm),
+                                &ctrl->status, st, at<uint8_t>(ws, L.xs8), at<uint8_t>(ws, L.xs8_perm)));
+    MOE_TRY(mark.end(MOE_STAGE_PERMUTE));
+    __nv_bfloat16* y_perm = at<__nv_bfloat16>(ws, L.y_perm);
+    __nv_bfloat16* y_shared = cfg->n_shared > 0 ? at<__nv_bfloat16>(ws, L.y_shared) : nullptr;
+    MOE_CUDA(run_expert_gemms_mx(cfg, T, weights, L, ws, perm_src, w, y_perm, y_shared, &mark));
+    MOE_TRY(mark.begin(MOE_STAGE_COMBINE));
+    MOE_CUDA(launch_combine(T, cfg->hidden, cfg->top_k, y_perm, inv_pos, y_shared,
+                            static_cast<const __nv_bfloat16*>(residual_bf16), static_cast<__nv_bfloat16*>(out_bf16),
+                            st));
+    MOE_TRY(mark.end(MOE_STAGE_COMBINE));
+    if (topk_ids_out)
+        MOE_CUDA(cudaMemcpyAsync(topk_ids_out, ids, (size_t)T * cfg->top_k * sizeof(int32_t),
+                                 cudaMemcpyDeviceToDevice, st));
+    return MOE_OK;
+}
+
+moe_status_t moe_forward_mx(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_mx_t* weights,
+                            const void* residual_bf16, void* out_bf16, int32_t* topk_ids_out, void* ws,
+                            size_t ws_bytes, void* stream) {
+    return moe_forward_mx_profiled(cfg, x_bf16, T, weights, residual_bf16, out_bf16, topk_ids_out, ws, ws_bytes,
+                                   stream, nullptr);
 }
 
 }  // extern "C"

@@ -71,6 +71,8 @@ struct WsLayout {
     size_t hs_r, hs_s;   // fp32 [T*k, I/128], [T, Is/128]
     size_t mtiles;       // MTile [max_mtiles]
     int max_mtiles;
+    size_t xs8, xs8_perm;  // MXFP8 variant: E8M0 activation scales [T, H/32], [T*k, H/32]
+    size_t hs8_r, hs8_s;   //                and of the intermediate [T*k, I/32], [T, Is/32]
     size_t y_perm;     // bf16 [T*k, H]
     size_t y_shared;   // bf16 [T, H]
     size_t total;
@@ -78,8 +80,9 @@ struct WsLayout {
     int max_groups;
 };
 
-WsLayout ws_layout(const moe_config_t& c, int64_t T);
-int router_splits_for(const moe_config_t& c, int64_t T);
+// mx: the MXFP8 variant's layout (grouped-GEMM path at every T, no streaming partials)
+WsLayout ws_layout(const moe_config_t& c, int64_t T, bool mx = false);
+int router_splits_for(const moe_config_t& c, int64_t T, bool large_route = false);
 int max_routed_groups(const moe_config_t& c, int64_t T);
 
 // Optional stage M in front of a kernel: gamma == nullptr means the input is used
@@ -184,6 +187,10 @@ struct GemmArgs {
     const float *s_gate, *s_up, *s_down, *ss_gate, *ss_up, *ss_down;
     uint8_t *hq_r, *hq_s;   // FP8 intermediate (gate/up output, down input)
     float *hs_r, *hs_s;     // its scales, row-major [rows, width/128]
+    uint8_t *hs8_r, *hs8_s; // MXFP8 variant: its E8M0 scales, row-major [rows, width/32]
+    // MXFP8 variant: E8M0 scale rows [rows, K/32] of the A operand (routed, shared) and
+    // of the two 128-row halves of the B tile (routed, shared)
+    const uint8_t *sfa_r, *sfa_s, *sfb0_r, *sfb1_r, *sfb0_s, *sfb1_s;
     __nv_bfloat16* y_perm;
     __nv_bfloat16* y_shared;
     int* status;
@@ -193,10 +200,21 @@ struct TmaMaps {
 };
 bool gemm_supported(const moe_config_t& c);
 cudaError_t launch_expert_gemm(const GemmArgs& g, const TmaMaps& m, cudaStream_t st);
-// xq_perm[r] = xq[token of r] (the routed rows in expert order). A row whose perm_src
-// entry is outside [0, T*k) is written as zeros and sets kStatusBadId.
+
+// MXFP8 variant: the same tiles and operand maps, E8M0 scales (GemmArgs::sfa_*, sfb*_*)
+// through the tensor core.
+bool gemm_mx_supported(const moe_config_t& c);
+cudaError_t launch_expert_gemm_mx(const GemmArgs& g, const TmaMaps& m, cudaStream_t st);
+// MXFP8 activation quantisation: per (token, 32 values) one E8M0 scale byte.
+cudaError_t launch_quant_act_mx(const void* x, int T, int H, uint8_t* xq, uint8_t* xs8, const NormArgs& nm,
+                                cudaStream_t st);
+
+// xq_perm[r] = xq[token of r] (the routed rows in expert order); with xs8 != nullptr also
+// xs8_perm[r] = xs8[token of r] (E8M0 rows of H/32 bytes). A row whose perm_src entry is
+// outside [0, T*k) is written as zeros and sets kStatusBadId.
 cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, uint8_t* xq_perm,
-                               int* status, cudaStream_t st);
+                               int* status, cudaStream_t st, const uint8_t* xs8 = nullptr,
+                               uint8_t* xs8_perm = nullptr);
 
 int stream_grid();
 int down_stages(int I, int Is);

@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(256) build_groups_kernel(BuildGroupsParams p) 
 constexpr int kGatherRows = 32;
 
 __global__ void __launch_bounds__(256) gather_rows_kernel(int T, int H, int k, const int32_t* perm_src,
-                                                          const uint8_t* xq, uint8_t* xq_perm, int* status) {
+                                                          const uint8_t* xq, uint8_t* xq_perm, int* status,
+                                                          const uint8_t* xs8, uint8_t* xs8_perm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long n = (long)T * k;
     const int H16 = H / 16;
@@ -231,6 +232,11 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int T, int H, int k, c
         const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)(good ? f / k : 0) * H);
         uint4* dst = reinterpret_cast<uint4*>(xq_perm + (size_t)r * H);
         for (int c = lane; c < H16; c += 32) dst[c] = good ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        if (xs8) {  // the row's E8M0 scales: H/32 bytes, a multiple of 16 (H % 512 == 0)
+            const uint4* ss = reinterpret_cast<const uint4*>(xs8 + (size_t)(good ? f / k : 0) * (H / 32));
+            uint4* sd = reinterpret_cast<uint4*>(xs8_perm + (size_t)r * (H / 32));
+            for (int c = lane; c < H / 512; c += 32) sd[c] = good ? __ldg(ss + c) : make_uint4(0, 0, 0, 0);
+        }
     }
 }
 
@@ -269,11 +275,12 @@ cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, i
 }
 
 cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, uint8_t* xq_perm,
-                               int* status, cudaStream_t st) {
+                               int* status, cudaStream_t st, const uint8_t* xs8, uint8_t* xs8_perm) {
     const long n = (long)T * k;
     if (n == 0) return cudaSuccess;
     gather_rows_kernel<<<(unsigned)((n + kGatherRows - 1) / kGatherRows), 256, 0, st>>>(T, H, k, perm_src, xq,
-                                                                                        xq_perm, status);
+                                                                                        xq_perm, status, xs8,
+                                                                                        xs8_perm);
     return cudaGetLastError();
 }
 

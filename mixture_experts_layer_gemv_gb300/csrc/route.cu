@@ -363,12 +363,15 @@ __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
               nullptr);
 }
 
-// x [T, H] bf16 -> xq codes, xs scales. Four threads share a 128-value block (32 values
-// each, two shuffles for the block maximum), so the per-block work is spread thinly.
+// x [T, H] bf16 -> xq codes + scales. Each thread takes 32 consecutive values. Per-128
+// blocks (kMX false): four threads share a block (two shuffles for its maximum), one fp32
+// scale per block in xs. MXFP8 (kMX true): a thread's 32 values are one block, its E8M0
+// scale byte goes to xs8 [T, H/32].
+template <bool kMX>
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, int T, int H, uint8_t* xq, float* xs,
-                                                        const uint16_t* gamma, const float* rstd) {
+                                                        uint8_t* xs8, const uint16_t* gamma, const float* rstd) {
     const int Hb = H / kBlk;
-    const long nq = (long)T * Hb * 4;  // quarters; a group of 4 threads = one block
+    const long nq = (long)T * Hb * 4;  // quarters of a 128-value block
     // the loop condition is the same for every lane of a warp (the shuffles need all 32)
     for (long base = (long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < nq;
          base += (long)gridDim.x * blockDim.x) {
@@ -401,10 +404,15 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, int T
         float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        float inv;
-        const float sc = act_scale_pow2(amax, &inv);
+        float inv, sc = 0.f;
+        uint32_t s8 = 0;
+        if (kMX) {
+            s8 = act_scale_e8m0(amax, &inv);
+        } else {
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            sc = act_scale_pow2(amax, &inv);
+        }
         if (ok) {
             uint32_t code[8];
 #pragma unroll
@@ -413,7 +421,10 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* x, int T
             uint4* dst = reinterpret_cast<uint4*>(xq + t * H + kb * kBlk + q * 32);
             dst[0] = make_uint4(code[0], code[1], code[2], code[3]);
             dst[1] = make_uint4(code[4], code[5], code[6], code[7]);
-            if (q == 0) xs[t * Hb + kb] = sc;
+            if (kMX)
+                xs8[t * (H / 32) + kb * 4 + q] = (uint8_t)s8;
+            else if (q == 0)
+                xs[t * Hb + kb] = sc;
         }
     }
 }
@@ -442,7 +453,17 @@ cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs
                              cudaStream_t st) {
     const long nq = (long)T * (H / kBlk) * 4;
     const int grid = (int)std::min<long>((nq + 255) / 256, (long)num_sms() * 8);
-    quant_act_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, xq, xs, nm.gamma, nm.rstd);
+    quant_act_kernel<false><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, xq, xs, nullptr, nm.gamma,
+                                                   nm.rstd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_mx(const void* x, int T, int H, uint8_t* xq, uint8_t* xs8, const NormArgs& nm,
+                                cudaStream_t st) {
+    const long nq = (long)T * (H / kBlk) * 4;
+    const int grid = (int)std::min<long>((nq + 255) / 256, (long)num_sms() * 8);
+    quant_act_kernel<true><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), T, H, xq, nullptr, xs8, nm.gamma,
+                                                 nm.rstd);
     return cudaGetLastError();
 }
 

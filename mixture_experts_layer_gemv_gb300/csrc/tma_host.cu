@@ -34,10 +34,12 @@ using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint64_t, uint32_t, uint32
 std::mutex g_mu;
 std::map<Key, CUtensorMap> g_cache;
 
+// kind 0: u8 with 128-byte swizzle; 1: fp32, no swizzle
 bool encode_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch_bytes, uint32_t box_cols,
-               uint32_t box_rows, bool f32) {
+               uint32_t box_rows, int kind) {
     static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "opaque map size");
-    const Key key{(uintptr_t)base, rows, cols, pitch_bytes, box_cols, box_rows, f32 ? 1 : 0};
+    const bool f32 = kind == 1;
+    const Key key{(uintptr_t)base, rows, cols, pitch_bytes, box_cols, box_rows, kind};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_cache.find(key);
@@ -55,7 +57,7 @@ bool encode_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r =
         fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     {
@@ -72,7 +74,7 @@ bool encode_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint
 // u8 [rows, cols], dense rows, 128-byte swizzle (box_cols must be 128)
 bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
                 uint32_t box_rows) {
-    return encode_2d(out, base, rows, cols, cols, box_cols, box_rows, false);
+    return encode_2d(out, base, rows, cols, cols, box_cols, box_rows, 0);
 }
 
 
