@@ -28,7 +28,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from mixture_experts_layer_gemv_gb300.synth import WORKLOADS, make_tokens, make_weights, replicate_weights  # noqa: E402
+from mixture_experts_layer_gemv_gb300.synth import (WORKLOADS, make_tokens, make_weights, make_weights_mx,  # noqa: E402
+                                                    replicate_weights)
 
 L2_BYTES = 129 * 1024 * 1024
 
@@ -157,11 +158,14 @@ def _gemm_path(cfg, T: int) -> bool:
     return T > 64 and cfg.hidden % 256 == 0
 
 
-def _launches_per_step(cfg, T: int) -> int:
+def _launches_per_step(cfg, T: int, mx: bool = False) -> int:
+    # grouped GEMM: router GEMM, top-k, activation quant, permutation, row gather, gate/up, down, combine
+    # (the MXFP8 variant at every T)
+    if mx:
+        return 8
     # small T: fused route + permutation, gate/up, down, combine
     if T <= 64:
         return 4
-    # grouped GEMM: router GEMM, top-k, activation quant, permutation, row gather, gate/up, down, combine
     if _gemm_path(cfg, T):
         return 8
     # streaming fallback: router GEMM, top-k, activation quant, permutation, gate/up, down, combine
@@ -186,6 +190,7 @@ def _layer_flops(cfg, T: int) -> int:
 NCU_TRAFFIC_BYTES = {
     ("dsv2_decode_t1", "gateup_stream_kernel"): 138_390_000,   # 133.98 MB read + 4.41 MB written
     ("prefill_t4096", "expert_gemm_kernel<0>"): 2_577_560_000,  # 2.4976 GB read + 80.0 MB written
+    ("prefill_t4096", "expert_gemm_mx_kernel<0>"): 3_136_350_000,  # 3.0643 GB read + 72.1 MB written
 }
 
 
@@ -202,14 +207,15 @@ def run_ours(args, dist, rank, world):
     dev = torch.device("cuda", torch.cuda.current_device())
     wl = WORKLOADS[args.workload]
     cfg, T = wl.cfg, wl.T
-    W0 = make_weights(cfg, wl.seed, dev, zipf=wl.zipf_bias)
+    mx = args.mx
+    W0 = (make_weights_mx if mx else make_weights)(cfg, wl.seed, dev, zipf=wl.zipf_bias)
     touched_bytes = _algorithmic_layer_bytes(cfg, min(cfg.n_routed, T * cfg.top_k), T)
     # enough stacked layer replicas that consecutive steps never find their weights in L2
     R = args.replicas or max(1, min(8, (4 * L2_BYTES) // max(1, touched_bytes) + 1))
     layers = [W0] + [replicate_weights(W0) for _ in range(R - 1)]
     P = max(R, 8)
     xs = [make_tokens(cfg, T, wl.seed * 1000 + rank * 100 + i, dev, name=f"x_step{i}") for i in range(P)]
-    ws = B.alloc_workspace(cfg, T, dev)
+    ws = (B.alloc_workspace_mx if mx else B.alloc_workspace)(cfg, T, dev)
     out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=dev)
     ids = torch.empty((T, cfg.top_k), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
@@ -217,7 +223,10 @@ def run_ours(args, dist, rank, world):
 
     # argument structs built once: the timed loop is one C call per step
     cstruct = B.config_struct(cfg)
-    wstructs = [B.weights_struct(Wl) for Wl in layers]
+    wstructs = [(B.weights_mx_struct if mx else B.weights_struct)(Wl) for Wl in layers]
+    fwd = lib.moe_forward_mx if mx else lib.moe_forward
+    fwd_prof = lib.moe_forward_mx_profiled if mx else lib.moe_forward_profiled
+    fwd_py = B.moe_forward_mx if mx else B.moe_forward
     c_ref = ctypes.byref(cstruct)
     w_refs = [ctypes.byref(w) for w in wstructs]
     x_ptrs = [x.data_ptr() for x in xs]
@@ -225,17 +234,16 @@ def run_ours(args, dist, rank, world):
 
     def step(i, ev=None):
         if ev is None:
-            r = lib.moe_forward(c_ref, x_ptrs[i % P], T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st)
+            r = fwd(c_ref, x_ptrs[i % P], T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st)
         else:
-            r = lib.moe_forward_profiled(c_ref, x_ptrs[i % P], T, w_refs[i % R], None, out_p, None, ws_p, ws_n,
-                                         st, ctypes.byref(ev))
+            r = fwd_prof(c_ref, x_ptrs[i % P], T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st, ctypes.byref(ev))
         if r != 0:
             raise B.MoeError("moe_forward", r, B.status_string(r))
 
     # touched experts per step (for the roofline numerator): from the routing itself
     touched = []
     for i in range(P):
-        B.moe_forward(cfg, xs[i], layers[i % R], out, topk_ids_out=ids, ws=ws)
+        fwd_py(cfg, xs[i], layers[i % R], out, topk_ids_out=ids, ws=ws)
         touched.append(int(torch.unique(ids).numel()))
     torch.cuda.synchronize()
 
@@ -273,7 +281,8 @@ def run_ours(args, dist, rank, world):
     torch.cuda.synchronize()
     ms = _max_over_ranks(dist, t0.elapsed_time(t1) / args.steps)
     stage_us = {}
-    recorded = ("route", "gate_up", "down", "combine") if T <= 64 else B.STAGES  # small T: the router also permutes
+    # small T: the router also permutes (the MXFP8 variant permutes separately at every T)
+    recorded = ("route", "gate_up", "down", "combine") if T <= 64 and not mx else B.STAGES
     for n in recorded:
         v = [evs[n][0].elapsed_time(evs[n][1]) * 1e3 for evs, _ in prof]
         if max(v) > 0:
@@ -289,7 +298,7 @@ def run_ours(args, dist, rank, world):
 
     def e2e_step(i):
         xd.copy_(xh[i % P], non_blocking=True)
-        r = lib.moe_forward(c_ref, xd_p, T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st)
+        r = fwd(c_ref, xd_p, T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st)
         if r != 0:
             raise B.MoeError("moe_forward", r, B.status_string(r))
         oh.copy_(out, non_blocking=True)
@@ -318,12 +327,12 @@ def run_ours(args, dist, rank, world):
         "cfg": cfg, "T": T, "ms": ms, "e2e_ms": e2e_ms, "gu_ms": gu_ms, "gu_bytes": gu_bytes,
         "achieved": achieved, "peak": peak_gbs, "peak_src": "measured" if peaks else "fallback",
         "layer_bytes": layer_bytes, "tokens_per_s": tokens_per_s, "clocks": clk.summary(), "status": status,
-        "replicas": R, "n_touched": n_touched, "launches": _launches_per_step(cfg, T) * args.steps, "weights": W0,
+        "replicas": R, "n_touched": n_touched, "launches": _launches_per_step(cfg, T, mx) * args.steps, "weights": W0,
         "stage_us": stage_us, "prof_steps": n_prof,
     }
 
 
-def cpu_oracle_rate(wl, budget_s: float, weights=None):
+def cpu_oracle_rate(wl, budget_s: float, weights=None, mx: bool = False):
     """Time the oracle (as it stands) on a bounded sample of the workload: independent
     T-token layer calls' worth of tokens, all host cores. Returns (us per layer call, cores, sample)."""
     import oracle
@@ -331,9 +340,10 @@ def cpu_oracle_rate(wl, budget_s: float, weights=None):
     cfg = wl.cfg
     if weights is None:  # the same generator; on the GPU when there is one (much faster)
         dev = "cuda" if torch.cuda.is_available() else "cpu"
-        weights = make_weights(cfg, wl.seed, dev, zipf=wl.zipf_bias)
+        weights = (make_weights_mx if mx else make_weights)(cfg, wl.seed, dev, zipf=wl.zipf_bias)
     Wc = {k: (None if v is None else v.detach().cpu()) for k, v in weights.items()}
-    OW = oracle.Weights(Wc)
+    OW = (oracle.WeightsMX if mx else oracle.Weights)(Wc)
+    run_tokens = oracle.forward_tokens_mx if mx else oracle.forward_tokens
     cores = oracle.num_threads()
     n_tok = max(1, cores)
     x = make_tokens(cfg, n_tok, wl.seed, "cpu", name="x_cpu_sample")
@@ -341,7 +351,7 @@ def cpu_oracle_rate(wl, budget_s: float, weights=None):
     done = 0
     while True:
         ids, w, _, _ = oracle.route(cfg, x, Wc["w_router"], Wc["router_bias"])
-        oracle.forward_tokens(cfg, OW, x, ids, w)
+        run_tokens(cfg, OW, x, ids, w)
         done += n_tok
         if time.perf_counter() - t0 > budget_s:
             break
@@ -360,6 +370,7 @@ def main():
     ap.add_argument("--replicas", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mx", action="store_true", help="the MXFP8 variant (E8M0 scales per 32 K)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -375,13 +386,14 @@ def main():
               "moe_inter": cfg.moe_inter, "n_routed": cfg.n_routed, "n_group": cfg.n_group,
               "topk_group": cfg.topk_group, "top_k": cfg.top_k,
               "routed_scaling_factor": cfg.routed_scaling_factor, "n_shared": cfg.n_shared,
-              "weights": "FP8 E4M3, fp32 per-128x128 block scales", "parallelism": f"replicas x{world}"}
+              "weights": ("MXFP8: E4M3, E8M0 scale per row and 32 K" if args.mx else
+                          "FP8 E4M3, fp32 per-128x128 block scales"), "parallelism": f"replicas x{world}"}
 
     if args.impl == "reference":
         if rank != 0:
             return
         budget = max(5.0, min(60.0, args.cpu_budget))
-        us, cores, sample = cpu_oracle_rate(wl, budget)
+        us, cores, sample = cpu_oracle_rate(wl, budget, mx=args.mx)
         value = us if t1_metric else 1e6 / us * 1.0
         unit = "us/layer" if t1_metric else "tokens/s"
         line = {"impl": "reference", "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": 1,
@@ -406,14 +418,15 @@ def main():
         e2e_value = world * T / (r["e2e_ms"] * 1e-3)
     config["l2"] = f"{r['replicas']} stacked layer replicas rotated so weights stream from HBM (inputs > L2)"
     peaks = _peaks()
-    if _gemm_path(cfg, T):
+    if args.mx or _gemm_path(cfg, T):
         # contraction on the FP8 tensor cores: peak = measured bf16 burst x nominal FP8/bf16 ratio (2)
         fp8_peak = 2.0 * peaks["bf16_tflops"] if peaks else 2.0 * 1900.0
         gu_tflops = _gateup_flops(cfg, T) / (r["gu_ms"] * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "expert_gemm_kernel<0> (gate/up grouped GEMM)",
+        kname = "expert_gemm_mx_kernel<0>" if args.mx else "expert_gemm_kernel<0>"
+        roofline = {"bound": "tensor", "kernel": f"{kname} (gate/up grouped GEMM)",
                     "achieved": round(gu_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                     "frac": round(gu_tflops / fp8_peak, 4),
-                    "traffic": NCU_TRAFFIC_BYTES.get((wl.name, "expert_gemm_kernel<0>")),
+                    "traffic": NCU_TRAFFIC_BYTES.get((wl.name, kname)),
                     "peak_source": ("measured bf16 burst x2 (nominal fp8/bf16)" if peaks else "fallback x2"),
                     "launch_us": round(r["gu_ms"] * 1e3, 3), "flops_per_launch": _gateup_flops(cfg, T)}
         layer_tflops = _layer_flops(cfg, T) / (r["ms"] * 1e-3) / 1e12
@@ -441,7 +454,7 @@ def main():
         "gpu_launches": r["launches"], "clocks": r["clocks"], "device_status": r["status"],
     }
     if not args.no_cpu_baseline:
-        us_cpu, cores, sample = cpu_oracle_rate(wl, args.cpu_budget, r["weights"])
+        us_cpu, cores, sample = cpu_oracle_rate(wl, args.cpu_budget, r["weights"], mx=args.mx)
         cv = us_cpu if t1_metric else 1e6 / us_cpu
         line["cpu_baseline"] = {"value": round(cv, 3), "unit": unit, "cores": cores, "kind": "oracle",
                                 "sample": sample}
