@@ -13,6 +13,7 @@
 //  * large T: a tiled fp32 SIMT GEMM for the logits (split-K partials, summed in a
 //    fixed order), then one warp per token for softmax/top-k.
 #include <algorithm>
+#include <type_traits>
 
 #include "route_common.cuh"
 
@@ -45,6 +46,7 @@ struct RouteSmallParams {
     float eps;
 };
 
+template <bool kNorm>  // stage M in front of the router (p.gamma != nullptr)
 __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmallParams p) {
     __shared__ float s_part[kRouteWarps][kSmallT];
     __shared__ float s_gs[kRouteWarps][kMaxE];
@@ -57,7 +59,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x;
     const int H = p.H, T = p.T, Hb = H / kBlk;
-    const bool norm = p.gamma != nullptr;
+    constexpr bool norm = kNorm;
     pdl_wait();  // x and the workspace are free (the previous kernel in the stream is done)
     pdl_launch_dependents();
 
@@ -221,7 +223,7 @@ __device__ __forceinline__ void split3(float w, uint16_t& hi, uint16_t& mid, uin
     lo = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
 }
 
-template <int NTW>  // 8-wide expert tiles per warp: Ep = 16 * NTW
+template <int NTW, bool kNorm>  // 8-wide expert tiles per warp: Ep = 16 * NTW; stage M on load
 __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
     extern __shared__ uint4 smem_r[];
     uint16_t* sx = reinterpret_cast<uint16_t*>(smem_r);  // [64][kRPitch]
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
     uint4 gx[2];       // gamma of those columns (stage M)
     float rs[2];       // 1/rms of those rows
     float4 wv[nw4];    // router tile: Ep rows x 64 fp32
-    const bool norm = p.gamma != nullptr;
+    constexpr bool norm = kNorm;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
         const int t = m0 + ((tid + 256 * q) >> 3);
@@ -512,7 +514,8 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, route_small_kernel, p);
+    return nm.gamma ? cudaLaunchKernelEx(&cfg, route_small_kernel<true>, p)
+                    : cudaLaunchKernelEx(&cfg, route_small_kernel<false>, p);
 }
 
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
@@ -539,23 +542,27 @@ cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, cons
         return cudaGetLastError();
     };
     cudaError_t e2 = cudaErrorInvalidValue;
+    auto pick = [&](auto ntw) -> cudaError_t {
+        constexpr int N = decltype(ntw)::value;
+        return g.gamma ? run(router_mma_kernel<N, true>) : run(router_mma_kernel<N, false>);
+    };
     switch (g.Ep / 16) {  // n_routed <= 256
-        case 1: e2 = run(router_mma_kernel<1>); break;
-        case 2: e2 = run(router_mma_kernel<2>); break;
-        case 3: e2 = run(router_mma_kernel<3>); break;
-        case 4: e2 = run(router_mma_kernel<4>); break;
-        case 5: e2 = run(router_mma_kernel<5>); break;
-        case 6: e2 = run(router_mma_kernel<6>); break;
-        case 7: e2 = run(router_mma_kernel<7>); break;
-        case 8: e2 = run(router_mma_kernel<8>); break;
-        case 9: e2 = run(router_mma_kernel<9>); break;
-        case 10: e2 = run(router_mma_kernel<10>); break;
-        case 11: e2 = run(router_mma_kernel<11>); break;
-        case 12: e2 = run(router_mma_kernel<12>); break;
-        case 13: e2 = run(router_mma_kernel<13>); break;
-        case 14: e2 = run(router_mma_kernel<14>); break;
-        case 15: e2 = run(router_mma_kernel<15>); break;
-        case 16: e2 = run(router_mma_kernel<16>); break;
+        case 1: e2 = pick(std::integral_constant<int, 1>{}); break;
+        case 2: e2 = pick(std::integral_constant<int, 2>{}); break;
+        case 3: e2 = pick(std::integral_constant<int, 3>{}); break;
+        case 4: e2 = pick(std::integral_constant<int, 4>{}); break;
+        case 5: e2 = pick(std::integral_constant<int, 5>{}); break;
+        case 6: e2 = pick(std::integral_constant<int, 6>{}); break;
+        case 7: e2 = pick(std::integral_constant<int, 7>{}); break;
+        case 8: e2 = pick(std::integral_constant<int, 8>{}); break;
+        case 9: e2 = pick(std::integral_constant<int, 9>{}); break;
+        case 10: e2 = pick(std::integral_constant<int, 10>{}); break;
+        case 11: e2 = pick(std::integral_constant<int, 11>{}); break;
+        case 12: e2 = pick(std::integral_constant<int, 12>{}); break;
+        case 13: e2 = pick(std::integral_constant<int, 13>{}); break;
+        case 14: e2 = pick(std::integral_constant<int, 14>{}); break;
+        case 15: e2 = pick(std::integral_constant<int, 15>{}); break;
+        case 16: e2 = pick(std::integral_constant<int, 16>{}); break;
     }
     if (e2 != cudaSuccess) return e2;
     cudaError_t err = cudaGetLastError();
