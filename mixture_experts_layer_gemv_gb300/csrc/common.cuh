@@ -394,7 +394,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // UE8M0 scale factor per row and 32-wide K step, read from tensor memory. A scale
 // group of 128 rows occupies 4 columns from sfa_tmem (sfb_tmem, a multiple of 4): the
 // rows of lane quadrant q are read from column q, lane 32q + i holding the four K-step
-// bytes of row 32q + i; the descriptor's scale-factor ids pick the byte.
+// bytes of row 32q + i; with N = 256, B's rows 128.. are the next group of 4 columns.
+// The descriptor's scale-factor ids pick the byte.
 __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
     asm volatile(

@@ -9,8 +9,8 @@
 // the epilogue runs once per tile instead of once per 128-wide K block.
 //
 // Tiles as in expert_gemm.cu: 128 permuted token rows x 256 weight rows (gate/up: 128
-// gate rows and the same 128 up rows; down: 256 hidden rows), issued as two N=128 MMAs
-// per 32-wide K step, one per 128-row half of B. One CTA of 10 warps per SM:
+// gate rows and the same 128 up rows; down: 256 hidden rows), one M=128 N=256 MMA per
+// 32-wide K step. One CTA of 10 warps per SM:
 //   warp 9      producer: per 128-wide K block an A box and two B boxes by TMA (4-stage
 //               ring); per group of 4 K blocks the scale bytes of the tile's 128 A rows
 //               and 256 B rows, read by its 32 lanes from the row-major scale tensors
@@ -18,8 +18,8 @@
 //               the tensor core's scale layout (below), a 2-slot ring
 //   warp 8      MMA issuer (one thread): per group twelve tcgen05.cp 32x128b.warpx4
 //               (A, B half 0, B half 1; 4 K blocks each) into tensor memory, then per K
-//               block 4 steps x 2 tcgen05.mma, the descriptor's scale-factor ids picking
-//               the step's byte
+//               block 4 tcgen05.mma, the descriptor's scale-factor ids picking the step's
+//               byte
 //   warps 0-7   epilogue: drains the accumulator into registers (warp w: lanes
 //               32*(w%4).., column half w/4), releases it, then gate/up -> a = SiLU(g)*u
 //               quantised per 32 values to E4M3 + E8M0 (the down GEMM's operand), or
@@ -27,9 +27,10 @@
 // Scale layout. For one K block, the scales of 128 rows (A, or one half of B) form a
 // 512-byte atom: 16 bytes per i = 0..31 holding the 4-byte words (the 4 K steps) of
 // rows i, i+32, i+64, i+96. tcgen05.cp 32x128b.warpx4 puts the atom into 4 columns of
-// every lane quadrant, and the MMA reads row 32q + i from lane 32q + i of column q.
-// Tensor memory: columns 0-255 the accumulator; scale slot j at 256 + 64j: A at +0,
-// B half 0 at +16, B half 1 at +32, 4 columns per K block.
+// every lane quadrant, and the MMA reads row 32q + i from lane 32q + i of column q; the
+// 256 rows of B take two such groups side by side (rows 128.. in the next 4 columns).
+// Tensor memory: columns 0-255 the accumulator; scale slot j at 256 + 64j: A at +4kb
+// (4 columns per K block of the group), B at +16 + 8kb (8 columns per K block).
 #include <algorithm>
 
 #include "gemm_common.cuh"
@@ -241,8 +242,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
 #pragma unroll
                         for (int jj = 0; jj < kSfGroup; ++jj) {
                             tc_cp_32x128b_x4(sfc + 4 * jj, smem_desc_rows16(sf + jj * kSfAtom));
-                            tc_cp_32x128b_x4(sfc + 16 + 4 * jj, smem_desc_rows16(sf + kSfA + jj * kSfAtom));
-                            tc_cp_32x128b_x4(sfc + 32 + 4 * jj,
+                            tc_cp_32x128b_x4(sfc + 16 + 8 * jj, smem_desc_rows16(sf + kSfA + jj * kSfAtom));
+                            tc_cp_32x128b_x4(sfc + 16 + 8 * jj + 4,
                                              smem_desc_rows16(sf + kSfA + (kSfGroup + jj) * kSfAtom));
                         }
                         ++g;
@@ -259,12 +260,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
                     const uint64_t db = smem_desc_sw128(st + kXSA);
                     const uint32_t col = 4u * (uint32_t)(kb % kSfGroup);  // this K block's scale columns
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)      // 4 x K=32 inside the 128-byte swizzled rows
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)  // B rows 128h.. -> accumulator columns 128h..
-                            tc_mma_mx(tmem + 128 * h, da + (uint64_t)(2 * k),
-                                      db + (uint64_t)(h * (kXSB / 2 >> 4) + 2 * k), idesc_mx_f32(kGM, 128, k),
-                                      sfc + col, sfc + 16 + 16 * h + col, (kb | k) != 0);
+                    for (int k = 0; k < 4; ++k)      // one N=256 MMA per K step
+                        tc_mma_mx(tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc_mx_f32(kGM, 256, k),
+                                  sfc + col, sfc + 16 + 2 * col, (kb | k) != 0);
                     tc_commit(&empty[s]);
                     if (kb % kSfGroup == kSfGroup - 1 || kb == Kb - 1) tc_commit(&sf_empty[(g - 1) % kSfSlots]);
                 }
