@@ -10,12 +10,13 @@
 //
 // Tiles as in expert_gemm.cu: 128 permuted token rows x 256 weight rows (gate/up: 128
 // gate rows and the same 128 up rows; down: 256 hidden rows), one M=128 N=256 MMA per
-// 32-wide K step. One CTA of 10 warps per SM:
-//   warp 9      producer: per 128-wide K block an A box and two B boxes by TMA (4-stage
-//               ring); per group of 4 K blocks the scale bytes of the tile's 128 A rows
-//               and 256 B rows, read by its 32 lanes from the row-major scale tensors
-//               (16 bytes = 4 K blocks x 4 steps per row) and stored rearranged into
-//               the tensor core's scale layout (below), a 2-slot ring
+// 32-wide K step. One CTA of 11 warps per SM:
+//   warp 9      TMA producer: per 128-wide K block an A box and two B boxes (4-stage
+//               ring)
+//   warp 10     scale producer: per group of 4 K blocks the scale bytes of the tile's
+//               128 A rows and 256 B rows, read by its 32 lanes from the row-major scale
+//               tensors (16 bytes = 4 K blocks x 4 steps per row) and stored rearranged
+//               into the tensor core's scale layout (below), a 2-slot ring
 //   warp 8      MMA issuer (one thread): per group twelve tcgen05.cp 32x128b.warpx4
 //               (A, B half 0, B half 1; 4 K blocks each) into tensor memory, then per K
 //               block 4 tcgen05.mma, the descriptor's scale-factor ids picking the step's
@@ -45,7 +46,8 @@ constexpr int kXStages = 4;
 constexpr int kXEpiWarps = 8;
 constexpr int kXMmaWarp = kXEpiWarps;
 constexpr int kXProducerWarp = kXEpiWarps + 1;
-constexpr int kXThreads = (kXEpiWarps + 2) * 32;
+constexpr int kXScaleWarp = kXEpiWarps + 2;
+constexpr int kXThreads = (kXEpiWarps + 3) * 32;
 constexpr int kXSA = kGM * kBlk;           // 16 KB A tile
 constexpr int kXSB = kGN * kBlk;           // 32 KB B tile
 constexpr int kXStage = kXSA + kXSB;
@@ -116,23 +118,47 @@ __global__ void __launch_bounds__(kXThreads, 1)
     const int total = items_in(0, n_r) * (a.K_r / kBlk) + items_in(n_r, n_items) * (a.K_s / kBlk);
 
     if (warp == kXProducerWarp) {
-        // --------------------------------------------------------------- producer
-        if (total > 0) {  // all 32 lanes: scale rows; lane 0: TMA and barriers
+        // ----------------------------------------------------------- TMA producer
+        if (lane == 0 && total > 0) {
             const MapsMX m{&tm.a_r, &tm.a_s, &tm.b0_r, &tm.b1_r, &tm.b0_s, &tm.b1_s};
-            if (lane == 0) {
-                prefetch_tmap(m.a_r);
-                prefetch_tmap(m.b0_r);
-                prefetch_tmap(m.b1_r);
-            }
-            const int rows_r = a.T * a.k;
+            prefetch_tmap(m.a_r);
+            prefetch_tmap(m.b0_r);
+            prefetch_tmap(m.b1_r);
             LoadCursor lc;
             lc.item = blockIdx.x;
             lc.kb = 0;
             lc.set(a, n_mt_r, n_items, gateup);
+            int n = 0;
+            for (; n < total; ++n) {
+                const int s = n % kXStages;
+                if (n >= kXStages && !mbar_wait_bounded(&empty[s], ((n / kXStages) - 1) & 1)) {
+                    set_status(a.status, kStatusTimeout);
+                    break;
+                }
+                uint8_t* st = smem + s * kXStage;
+                const int x = lc.kb * kBlk;
+                mbar_arrive_expect_tx(&full[s], kXStage);
+                tma_load_2d(st, lc.shared ? m.a_s : m.a_r, x, lc.row0, &full[s]);
+                tma_load_2d(st + kXSA, lc.shared ? m.b0_s : m.b0_r, x, lc.yb0, &full[s]);
+                tma_load_2d(st + kXSA + kXSB / 2, lc.shared ? m.b1_s : m.b1_r, x, lc.yb1, &full[s]);
+                lc.next(a, n_mt_r, n_items, gateup);
+            }
+            // copies still in flight land before this CTA may exit
+            for (int q = n > kXStages ? n - kXStages : 0; q < n; ++q)
+                mbar_wait_bounded(&full[q % kXStages], (q / kXStages) & 1);
+        }
+    } else if (warp == kXScaleWarp) {
+        // ------------------------------------------------------- scale producer
+        // all 32 lanes; every tile's K blocks come in whole groups of 4 (K % 512 == 0)
+        if (total > 0) {
+            const int rows_r = a.T * a.k;
+            LoadCursor gc;
+            gc.item = blockIdx.x;
+            gc.kb = 0;
+            gc.set(a, n_mt_r, n_items, gateup);
             // scale rows of the next group, fetched one group ahead of their use:
             // A rows row0 + lane + 32*m1, B half h rows yb_h + lane + 32*m1 (16 bytes each)
             uint4 pa[4], pb[8];
-            LoadCursor gc = lc;
             auto fetch = [&]() {
                 if (gc.item >= n_items) return;
                 const int Kg = (gc.shared ? a.K_s : a.K_r) / 32;  // scale bytes per row
@@ -163,56 +189,31 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 }
             };
             fetch();
-            int n = 0, g = 0;  // K blocks and scale groups issued
-            for (; n < total; ++n) {
+            const int groups = total / kSfGroup;
+            for (int g = 0; g < groups; ++g) {
+                const int j = g % kSfSlots;
                 bool ok = true;
-                if (lc.kb % kSfGroup == 0) {
-                    const int j = g % kSfSlots;
-                    if (g >= kSfSlots && lane == 0) ok = mbar_wait_bounded(&sf_empty[j], ((g / kSfSlots) - 1) & 1);
-                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                        if (lane == 0) set_status(a.status, kStatusTimeout);
-                        break;
-                    }
-                    uint8_t* sf = sf_smem + j * kSfStage;
-#pragma unroll
-                    for (int jj = 0; jj < kSfGroup; ++jj) {
-                        reinterpret_cast<uint4*>(sf + jj * kSfAtom)[lane] =
-                            make_uint4(word(pa[0], jj), word(pa[1], jj), word(pa[2], jj), word(pa[3], jj));
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            reinterpret_cast<uint4*>(sf + kSfA + (h * kSfGroup + jj) * kSfAtom)[lane] =
-                                make_uint4(word(pb[4 * h], jj), word(pb[4 * h + 1], jj), word(pb[4 * h + 2], jj),
-                                           word(pb[4 * h + 3], jj));
-                    }
-                    fence_proxy_async_smem();  // the tensor core reads these through the async proxy
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sf_full[j]);
-                    ++g;
-                    fetch();
-                }
-                const int s = n % kXStages;
-                if (lane == 0) {
-                    if (n >= kXStages && !mbar_wait_bounded(&empty[s], ((n / kXStages) - 1) & 1)) {
-                        ok = false;
-                    } else {
-                        uint8_t* st = smem + s * kXStage;
-                        const int x = lc.kb * kBlk;
-                        mbar_arrive_expect_tx(&full[s], kXStage);
-                        tma_load_2d(st, lc.shared ? m.a_s : m.a_r, x, lc.row0, &full[s]);
-                        tma_load_2d(st + kXSA, lc.shared ? m.b0_s : m.b0_r, x, lc.yb0, &full[s]);
-                        tma_load_2d(st + kXSA + kXSB / 2, lc.shared ? m.b1_s : m.b1_r, x, lc.yb1, &full[s]);
-                    }
-                }
+                if (g >= kSfSlots && lane == 0) ok = mbar_wait_bounded(&sf_empty[j], ((g / kSfSlots) - 1) & 1);
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
                     if (lane == 0) set_status(a.status, kStatusTimeout);
                     break;
                 }
-                lc.next(a, n_mt_r, n_items, gateup);
+                uint8_t* sf = sf_smem + j * kSfStage;
+#pragma unroll
+                for (int jj = 0; jj < kSfGroup; ++jj) {
+                    reinterpret_cast<uint4*>(sf + jj * kSfAtom)[lane] =
+                        make_uint4(word(pa[0], jj), word(pa[1], jj), word(pa[2], jj), word(pa[3], jj));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        reinterpret_cast<uint4*>(sf + kSfA + (h * kSfGroup + jj) * kSfAtom)[lane] =
+                            make_uint4(word(pb[4 * h], jj), word(pb[4 * h + 1], jj), word(pb[4 * h + 2], jj),
+                                       word(pb[4 * h + 3], jj));
+                }
+                fence_proxy_async_smem();  // the tensor core reads these through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_full[j]);
+                fetch();
             }
-            // copies still in flight land before this CTA may exit
-            if (lane == 0)
-                for (int q = n > kXStages ? n - kXStages : 0; q < n; ++q)
-                    mbar_wait_bounded(&full[q % kXStages], (q / kXStages) & 1);
         }
     } else if (warp == kXMmaWarp) {
         // -------------------------------------------------------------- MMA issuer
