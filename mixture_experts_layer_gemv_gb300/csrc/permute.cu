@@ -9,6 +9,8 @@
 // order, ranking equal experts inside each 32-wide chunk with __match_any_sync.
 // The same kernel emits the work list of the expert kernels: row groups of <= 8
 // rows for the streaming GEMVs, or 128-row tiles for the grouped GEMM.
+#include <climits>
+
 #include "common.cuh"
 #include "moe_internal.h"
 
@@ -18,6 +20,7 @@ namespace {
 
 constexpr int kPermWarps = 32;
 constexpr int kMaxE = 256;
+constexpr int kBatch = 16;  // 32-id chunks a warp loads before using them
 
 __device__ int scan_exclusive_warp256(int* v, int n) {
     const int lane = threadIdx.x & 31;
@@ -119,12 +122,23 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(PermuteParams 
 
     for (int i = threadIdx.x; i < kPermWarps * kMaxE; i += blockDim.x) (&hist[0][0])[i] = 0;
     __syncthreads();
-    for (int f = f_begin + lane; f < f_end; f += 32) {
-        const int e = p.ids[f];
-        if (e >= 0 && e < E)
-            atomicAdd(&hist[warp][e], 1);
-        else
-            set_status(&p.ctrl->status, kStatusBadId);
+    // ids are read kBatch chunks of 32 at a time: one memory round trip per batch
+    for (int base = f_begin; base < f_end; base += 32 * kBatch) {
+        int ev[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int f = base + lane + 32 * u;
+            ev[u] = f < f_end ? __ldg(p.ids + f) : INT_MIN;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = ev[u];
+            if (e == INT_MIN) continue;
+            if (e >= 0 && e < E)
+                atomicAdd(&hist[warp][e], 1);
+            else
+                set_status(&p.ctrl->status, kStatusBadId);
+        }
     }
     __syncthreads();
     // hist[w][e] <- pairs of expert e in segments before w; s_cnt[e] <- total
@@ -149,23 +163,34 @@ __global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(PermuteParams 
         for (int w = 0; w < kPermWarps; ++w) hist[w][e] += s_off[e];
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = f_begin; base < f_end; base += 32) {
-        const int f = base + lane;
-        int e = -1;
-        if (f < f_end) {
-            e = p.ids[f];
-            if (e < 0 || e >= E) e = -1;
+    for (int base0 = f_begin; base0 < f_end; base0 += 32 * kBatch) {
+        int ev[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int f = base0 + lane + 32 * u;
+            int e = -1;
+            if (f < f_end) {
+                e = __ldg(p.ids + f);
+                if (e < 0 || e >= E) e = -1;
+            }
+            ev[u] = e;
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(peers & lt_mask);
-        if (e >= 0) {
-            const int pos = hist[warp][e] + rank;
-            p.perm_src[pos] = f;
-            p.inv_pos[f] = pos;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (base0 + 32 * u >= f_end) break;  // warp-uniform
+            const int f = base0 + lane + 32 * u;
+            const int e = ev[u];
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & lt_mask);
+            if (e >= 0) {
+                const int pos = hist[warp][e] + rank;
+                p.perm_src[pos] = f;
+                p.inv_pos[f] = pos;
+            }
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(peers) - 1) hist[warp][e] += __popc(peers);
+            __syncwarp();
         }
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) hist[warp][e] += __popc(peers);
-        __syncwarp();
     }
     if (p.groups) {
         __syncthreads();
@@ -231,7 +256,19 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int T, int H, int k, c
         if (!good && lane == 0) set_status(status, kStatusBadId);
         const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)(good ? f / k : 0) * H);
         uint4* dst = reinterpret_cast<uint4*>(xq_perm + (size_t)r * H);
-        for (int c = lane; c < H16; c += 32) dst[c] = good ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        for (int c0 = 0; c0 < H16; c0 += 32 * 8) {  // 8 loads in flight per lane, then the stores
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + lane + 32 * u;
+                v[u] = good && c < H16 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + lane + 32 * u;
+                if (c < H16) dst[c] = v[u];
+            }
+        }
         if (xs8) {  // the row's E8M0 scales: H/32 bytes, a multiple of 16 (H % 512 == 0)
             const uint4* ss = reinterpret_cast<const uint4*>(xs8 + (size_t)(good ? f / k : 0) * (H / 32));
             uint4* sd = reinterpret_cast<uint4*>(xs8_perm + (size_t)r * (H / 32));
