@@ -190,7 +190,7 @@ def _layer_flops(cfg, T: int) -> int:
 NCU_TRAFFIC_BYTES = {
     ("dsv2_decode_t1", "gateup_stream_kernel"): 138_390_000,   # 133.98 MB read + 4.41 MB written
     ("prefill_t4096", "expert_gemm_kernel<0>"): 2_577_560_000,  # 2.4976 GB read + 80.0 MB written
-    ("prefill_t4096", "expert_gemm_mx_kernel<0>"): 3_136_350_000,  # 3.0643 GB read + 72.1 MB written
+    ("prefill_t4096", "expert_gemm_mx_kernel<0>"): 2_705_107_000,  # 2.6330 GB read + 72.2 MB written
 }
 
 
