@@ -42,12 +42,18 @@ def _peaks():
 
 
 def _dist():
+    """(torch.distributed or None, rank, world size) from the torchrun environment.
+
+    Every rank is an independent replica of the layer on its own tokens (the layer has
+    no exchange step); the process group is used only for barriers and for reducing the
+    timings. NCCL with one GPU per rank, gloo where there is no GPU."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
         import torch.distributed as dist
         rank = int(os.environ["RANK"])
         local = int(os.environ.get("LOCAL_RANK", rank))
-        torch.cuda.set_device(local)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         return dist, rank, ws
     return None, 0, 1
@@ -58,10 +64,14 @@ def _barrier(dist):
         dist.barrier()
 
 
+def _reduce_device(dist):
+    return "cuda" if dist.get_backend() == "nccl" else "cpu"
+
+
 def _max_over_ranks(dist, v: float) -> float:
     if dist is None:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_reduce_device(dist))
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -69,9 +79,14 @@ def _max_over_ranks(dist, v: float) -> float:
 def _sum_over_ranks(dist, v: float) -> float:
     if dist is None:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_reduce_device(dist))
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def replica_seed(seed: int, rank: int, step: int) -> int:
+    """Token seed of step `step` on replica `rank`: every rank gets its own tokens."""
+    return seed * 1000 + rank * 100 + step
 
 
 class ClockSampler:
@@ -214,7 +229,7 @@ def run_ours(args, dist, rank, world):
     R = args.replicas or max(1, min(8, (4 * L2_BYTES) // max(1, touched_bytes) + 1))
     layers = [W0] + [replicate_weights(W0) for _ in range(R - 1)]
     P = max(R, 8)
-    xs = [make_tokens(cfg, T, wl.seed * 1000 + rank * 100 + i, dev, name=f"x_step{i}") for i in range(P)]
+    xs = [make_tokens(cfg, T, replica_seed(wl.seed, rank, i), dev, name=f"x_step{i}") for i in range(P)]
     ws = (B.alloc_workspace_mx if mx else B.alloc_workspace)(cfg, T, dev)
     out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=dev)
     ids = torch.empty((T, cfg.top_k), dtype=torch.int32, device=dev)
