@@ -149,22 +149,27 @@ class ClockSampler:
                 "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
 
 
-def _algorithmic_gateup_bytes(cfg, n_experts_touched: int, T: int) -> int:
+def _algorithmic_gateup_bytes(cfg, n_experts_touched: int, T: int, mx: bool = False) -> int:
     """Bytes the gate/up stage must move: FP8 gate+up of touched experts and the shared
-    experts, their fp32 block scales, the FP8 activations in and fp32 a out."""
+    experts, their scales (fp32 per 128x128 block, or MXFP8: one byte per 32 values), the
+    FP8 activations and their scales in, and fp32 a out."""
     H, I, Is = cfg.hidden, cfg.moe_inter, cfg.shared_inter
     w = n_experts_touched * 2 * I * H + 2 * Is * H
-    s = (n_experts_touched * 2 * (I // 128) * (H // 128) + 2 * (Is // 128) * (H // 128)) * 4
-    act = T * H + T * (H // 128) * 4 + T * (cfg.top_k * I + Is) * 4
+    if mx:
+        s = w // 32
+        act = T * H + T * (H // 32) + T * (cfg.top_k * I + Is) * 4
+    else:
+        s = (n_experts_touched * 2 * (I // 128) * (H // 128) + 2 * (Is // 128) * (H // 128)) * 4
+        act = T * H + T * (H // 128) * 4 + T * (cfg.top_k * I + Is) * 4
     return w + s + act
 
 
-def _algorithmic_layer_bytes(cfg, n_experts_touched: int, T: int) -> int:
+def _algorithmic_layer_bytes(cfg, n_experts_touched: int, T: int, mx: bool = False) -> int:
     """Bytes the whole layer must move: touched experts' and shared FP8 weights with
     scales, the fp32 router, x in and out (bf16)."""
     H, I, Is, E = cfg.hidden, cfg.moe_inter, cfg.shared_inter, cfg.n_routed
     w = n_experts_touched * 3 * I * H + 3 * Is * H
-    s = (n_experts_touched * 3 * (I // 128) * (H // 128) + 3 * (Is // 128) * (H // 128)) * 4
+    s = w // 32 if mx else (n_experts_touched * 3 * (I // 128) * (H // 128) + 3 * (Is // 128) * (H // 128)) * 4
     return w + s + E * H * 4 + 2 * T * H * 2
 
 
@@ -174,14 +179,11 @@ def _gemm_path(cfg, T: int) -> bool:
 
 
 def _launches_per_step(cfg, T: int, mx: bool = False) -> int:
-    # grouped GEMM: router GEMM, top-k, activation quant, permutation, row gather, gate/up, down, combine
-    # (the MXFP8 variant at every T)
-    if mx:
-        return 8
-    # small T: fused route + permutation, gate/up, down, combine
+    # small T: fused route + permutation, gate/up, down, combine (both variants)
     if T <= 64:
         return 4
-    if _gemm_path(cfg, T):
+    # grouped GEMM: router GEMM, top-k, activation quant, permutation, row gather, gate/up, down, combine
+    if mx or _gemm_path(cfg, T):
         return 8
     # streaming fallback: router GEMM, top-k, activation quant, permutation, gate/up, down, combine
     return 7
@@ -224,7 +226,7 @@ def run_ours(args, dist, rank, world):
     cfg, T = wl.cfg, wl.T
     mx = args.mx
     W0 = (make_weights_mx if mx else make_weights)(cfg, wl.seed, dev, zipf=wl.zipf_bias)
-    touched_bytes = _algorithmic_layer_bytes(cfg, min(cfg.n_routed, T * cfg.top_k), T)
+    touched_bytes = _algorithmic_layer_bytes(cfg, min(cfg.n_routed, T * cfg.top_k), T, args.mx)
     # enough stacked layer replicas that consecutive steps never find their weights in L2
     R = args.replicas or max(1, min(8, (4 * L2_BYTES) // max(1, touched_bytes) + 1))
     layers = [W0] + [replicate_weights(W0) for _ in range(R - 1)]
@@ -296,8 +298,8 @@ def run_ours(args, dist, rank, world):
     torch.cuda.synchronize()
     ms = _max_over_ranks(dist, t0.elapsed_time(t1) / args.steps)
     stage_us = {}
-    # small T: the router also permutes (the MXFP8 variant permutes separately at every T)
-    recorded = ("route", "gate_up", "down", "combine") if T <= 64 and not mx else B.STAGES
+    # small T: the router also permutes
+    recorded = ("route", "gate_up", "down", "combine") if T <= 64 else B.STAGES
     for n in recorded:
         v = [evs[n][0].elapsed_time(evs[n][1]) * 1e3 for evs, _ in prof]
         if max(v) > 0:
@@ -332,11 +334,11 @@ def run_ours(args, dist, rank, world):
     e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / args.steps)
 
     n_touched = statistics.mean(touched)
-    gu_bytes = _algorithmic_gateup_bytes(cfg, round(n_touched), T)
+    gu_bytes = _algorithmic_gateup_bytes(cfg, round(n_touched), T, mx)
     peaks = _peaks()
     peak_gbs = peaks["hbm_gbs"] if peaks else 6800.0
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
-    layer_bytes = _algorithmic_layer_bytes(cfg, round(n_touched), T)
+    layer_bytes = _algorithmic_layer_bytes(cfg, round(n_touched), T, mx)
     tokens_per_s = _sum_over_ranks(dist, T / (ms * 1e-3))
     return {
         "cfg": cfg, "T": T, "ms": ms, "e2e_ms": e2e_ms, "gu_ms": gu_ms, "gu_bytes": gu_bytes,
@@ -433,7 +435,7 @@ def main():
         e2e_value = world * T / (r["e2e_ms"] * 1e-3)
     config["l2"] = f"{r['replicas']} stacked layer replicas rotated so weights stream from HBM (inputs > L2)"
     peaks = _peaks()
-    if args.mx or _gemm_path(cfg, T):
+    if (args.mx and T > 64) or _gemm_path(cfg, T):
         # contraction on the FP8 tensor cores: peak = measured bf16 burst x nominal FP8/bf16 ratio (2)
         fp8_peak = 2.0 * peaks["bf16_tflops"] if peaks else 2.0 * 1900.0
         gu_tflops = _gateup_flops(cfg, T) / (r["gu_ms"] * 1e-3) / 1e12
@@ -447,9 +449,10 @@ def main():
         layer_tflops = _layer_flops(cfg, T) / (r["ms"] * 1e-3) / 1e12
         extra = {"layer_tflops": round(layer_tflops, 1), "layer_tensor_frac": round(layer_tflops / fp8_peak, 4)}
     else:
-        roofline = {"bound": "hbm", "kernel": "gateup_stream_kernel", "achieved": round(r["achieved"], 1),
+        kname = "gateup_stream_kernel<true>" if args.mx else "gateup_stream_kernel"
+        roofline = {"bound": "hbm", "kernel": kname, "achieved": round(r["achieved"], 1),
                     "peak": r["peak"], "unit": "GB/s", "frac": round(r["achieved"] / r["peak"], 4),
-                    "traffic": NCU_TRAFFIC_BYTES.get((wl.name, "gateup_stream_kernel")),
+                    "traffic": NCU_TRAFFIC_BYTES.get((wl.name, kname)),
                     "peak_source": r["peak_src"], "launch_us": round(r["gu_ms"] * 1e3, 3),
                     "bytes_per_launch": r["gu_bytes"]}
         extra = {}

@@ -243,10 +243,11 @@ moe_status_t moe_forward_rmsnorm_profiled(const moe_config_t* cfg, const void* h
  * The layer with moe_weights_mx_t weights and MXFP8 activations: x and the
  * intermediate a = SiLU(g) * u are quantised per token and 32 consecutive values
  * (scale = the smallest 2^k, k >= -126, with amax <= 448 * 2^k; codes RNE E4M3), and
- * the expert GEMMs apply all scales inside the tensor core (tcgen05.mma
- * kind::mxf8f6f4). Routing is that of moe_route. Shapes: hidden % 512 == 0 and
- * moe_inter % 512 == 0 (MOE_ERR_UNSUPPORTED_SHAPE otherwise; moe_workspace_size_mx
- * returns 0). Every T runs the grouped tensor-core GEMM. */
+ * for T > 64 the expert GEMMs apply all scales inside the tensor core (tcgen05.mma
+ * kind::mxf8f6f4); for T <= 64 the weight-streaming kernels apply each 32-wide block's
+ * scales to its own MMA partial. Routing is that of moe_route. Shapes: hidden % 512 == 0
+ * and moe_inter % 512 == 0 (MOE_ERR_UNSUPPORTED_SHAPE otherwise; moe_workspace_size_mx
+ * returns 0). */
 size_t moe_workspace_size_mx(const moe_config_t* cfg, int32_t max_tokens);
 
 /* MXFP8 activation quantisation: x_bf16 [T, H] -> xq [T, H] E4M3 codes and

@@ -78,6 +78,12 @@ __device__ __forceinline__ uint32_t act_scale_e8m0(float amax, float* inv_scale)
     return (uint32_t)(k + 127);
 }
 
+// E8M0 byte -> its value 2^(b-127) (b = 0: 2^-127, a subnormal; 0xFF, NaN, is not
+// expected here).
+__device__ __forceinline__ float e8m0_to_float(uint32_t b) {
+    return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
 // Four fp32 values -> four E4M3 codes (round to nearest even, saturating), packed
 // little-endian in one 32-bit word (value 0 in the low byte).
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
@@ -96,6 +102,18 @@ __device__ __forceinline__ uint32_t warp_quant_block128(float v0, float v1, floa
     float inv;
     const float s = act_scale_pow2(amax, &inv);
     *scale_out = s;
+    return pack_e4m3x4(v0 * inv, v1 * inv, v2 * inv, v3 * inv);
+}
+
+// MXFP8: the same 128 values, four per lane, as four blocks of 32 (8 lanes each):
+// returns this lane's packed codes and writes the E8M0 byte of its block.
+__device__ __forceinline__ uint32_t warp_quant_mx32(float v0, float v1, float v2, float v3, uint32_t* s8_out) {
+    float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    float inv;
+    *s8_out = act_scale_e8m0(amax, &inv);
     return pack_e4m3x4(v0 * inv, v1 * inv, v2 * inv, v3 * inv);
 }
 

@@ -57,7 +57,11 @@ __device__ __forceinline__ Plan down_plan(const StreamArgs& a) {
     return make_plan(t.n_r, t.kc_r, t.n_s, t.kc_s, a.grid_d, a.max_parts);
 }
 
+__device__ __forceinline__ uint32_t ldg32(const uint8_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
+
 // ================================================================== gate / up
+// kMX: MXFP8 weights and activations (E8M0 scales per row / token and 32 K)
+template <bool kMX>
 __global__ void __launch_bounds__(kThreads, 1)
     gateup_stream_kernel(const StreamArgs a, const __grid_constant__ TmaMap tm_g, const __grid_constant__ TmaMap tm_u,
                          const __grid_constant__ TmaMap tm_sg, const __grid_constant__ TmaMap tm_su) {
@@ -168,18 +172,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s = 0, ph = 0;
     for (int i = 0; i < ntiles; ++i) {
         const TileRec r = rec(i);
-        const float *sgr, *sur;
-        if (r.shared) {
-            sgr = a.ss_gate + (size_t)r.slice * Hb;
-            sur = a.ss_up + (size_t)r.slice * Hb;
-        } else {
-            const size_t e = (size_t)r.expert;
-            sgr = a.s_gate + (e * (a.I / kBlk) + r.slice) * Hb;
-            sur = a.s_up + (e * (a.I / kBlk) + r.slice) * Hb;
+        const float *sgr = nullptr, *sur = nullptr;
+        if constexpr (!kMX) {
+            if (r.shared) {
+                sgr = a.ss_gate + (size_t)r.slice * Hb;
+                sur = a.ss_up + (size_t)r.slice * Hb;
+            } else {
+                const size_t e = (size_t)r.expert;
+                sgr = a.s_gate + (e * (a.I / kBlk) + r.slice) * Hb;
+                sur = a.s_up + (e * (a.I / kBlk) + r.slice) * Hb;
+            }
         }
         const int tok0 = r.tok[2 * t4], tok1 = r.tok[2 * t4 + 1];
-        const float* xs0 = tok0 >= 0 ? a.xs + (size_t)tok0 * Hb : nullptr;
-        const float* xs1 = tok1 >= 0 ? a.xs + (size_t)tok1 * Hb : nullptr;
+        const float* xs0 = !kMX && tok0 >= 0 ? a.xs + (size_t)tok0 * Hb : nullptr;
+        const float* xs1 = !kMX && tok1 >= 0 ? a.xs + (size_t)tok1 * Hb : nullptr;
+        // MXFP8: E8M0 scale rows of this lane's two weight rows (tile rows warp*16 + g and
+        // + 8) and of its two tokens; 4 bytes (the 4 blocks of 32) per 128-wide K block
+        const int Hs = H / 32;
+        const uint8_t *wg8 = nullptr, *wu8 = nullptr, *x80 = nullptr, *x81 = nullptr;
+        if constexpr (kMX) {
+            const size_t row = (r.shared ? 0 : (size_t)r.expert * a.I) + (size_t)r.slice * kTile + warp * 16 + g;
+            wg8 = (r.shared ? a.ss_gate8 : a.s_gate8) + row * Hs;
+            wu8 = (r.shared ? a.ss_up8 : a.s_up8) + row * Hs;
+            x80 = tok0 >= 0 ? a.xs8 + (size_t)tok0 * Hs : nullptr;
+            x81 = tok1 >= 0 ? a.xs8 + (size_t)tok1 * Hs : nullptr;
+        }
         int tokg = -1;  // this lane's B column: activation row g
 #pragma unroll
         for (int c = 0; c < kGroupRows; ++c)
@@ -188,31 +205,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[2][4] = {};
         for (int j = 0; j < r.n; ++j) {
             const int kb = r.kb0 + j;
-            const float swg = __ldg(sgr + kb), swu = __ldg(sur + kb);
-            const float sx0 = xs0 ? __ldg(xs0 + kb) : 0.f;
-            const float sx1 = xs1 ? __ldg(xs1 + kb) : 0.f;
-            // after a timed-out wait this warp keeps walking the units (so its control flow
-            // matches its siblings') but waits for and computes nothing more
-            if (!failed && !mbar_wait_bounded(&full[s], ph)) {
-                set_status(a.status, kStatusTimeout);
-                failed = true;
+            if constexpr (kMX) {
+                const uint32_t g0 = ldg32(wg8 + kb * 4), g1 = ldg32(wg8 + 8 * Hs + kb * 4);
+                const uint32_t u0 = ldg32(wu8 + kb * 4), u1 = ldg32(wu8 + 8 * Hs + kb * 4);
+                const uint32_t s0 = x80 ? ldg32(x80 + kb * 4) : 0u, s1 = x81 ? ldg32(x81 + kb * 4) : 0u;
+                if (!failed && !mbar_wait_bounded(&full[s], ph)) {
+                    set_status(a.status, kStatusTimeout);
+                    failed = true;
+                }
+                const uint8_t* st = smem + s * SB;
+                float cg[4][4] = {}, cu[4][4] = {};
+                if (!failed) {
+                    box_dot_mx(cg, st, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
+                    box_dot_mx(cu, st + kBox, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float a0 = x80 ? e8m0_to_float((s0 >> (8 * q)) & 0xFF) : 0.f;
+                    const float a1 = x81 ? e8m0_to_float((s1 >> (8 * q)) & 0xFF) : 0.f;
+                    const float gs0 = e8m0_to_float((g0 >> (8 * q)) & 0xFF), gs1 = e8m0_to_float((g1 >> (8 * q)) & 0xFF);
+                    const float us0 = e8m0_to_float((u0 >> (8 * q)) & 0xFF), us1 = e8m0_to_float((u1 >> (8 * q)) & 0xFF);
+                    acc[0][0] = fmaf(cg[q][0], gs0 * a0, acc[0][0]);
+                    acc[0][1] = fmaf(cg[q][1], gs0 * a1, acc[0][1]);
+                    acc[0][2] = fmaf(cg[q][2], gs1 * a0, acc[0][2]);
+                    acc[0][3] = fmaf(cg[q][3], gs1 * a1, acc[0][3]);
+                    acc[1][0] = fmaf(cu[q][0], us0 * a0, acc[1][0]);
+                    acc[1][1] = fmaf(cu[q][1], us0 * a1, acc[1][1]);
+                    acc[1][2] = fmaf(cu[q][2], us1 * a0, acc[1][2]);
+                    acc[1][3] = fmaf(cu[q][3], us1 * a1, acc[1][3]);
+                }
+            } else {
+                const float swg = __ldg(sgr + kb), swu = __ldg(sur + kb);
+                const float sx0 = xs0 ? __ldg(xs0 + kb) : 0.f;
+                const float sx1 = xs1 ? __ldg(xs1 + kb) : 0.f;
+                // after a timed-out wait this warp keeps walking the units (so its control flow
+                // matches its siblings') but waits for and computes nothing more
+                if (!failed && !mbar_wait_bounded(&full[s], ph)) {
+                    set_status(a.status, kStatusTimeout);
+                    failed = true;
+                }
+                const uint8_t* st = smem + s * SB;
+                float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+                if (!failed) {
+                    box_dot(cg, st, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
+                    box_dot(cu, st + kBox, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                }
+                acc[0][0] = fmaf(cg[0], swg * sx0, acc[0][0]);
+                acc[0][1] = fmaf(cg[1], swg * sx1, acc[0][1]);
+                acc[0][2] = fmaf(cg[2], swg * sx0, acc[0][2]);
+                acc[0][3] = fmaf(cg[3], swg * sx1, acc[0][3]);
+                acc[1][0] = fmaf(cu[0], swu * sx0, acc[1][0]);
+                acc[1][1] = fmaf(cu[1], swu * sx1, acc[1][1]);
+                acc[1][2] = fmaf(cu[2], swu * sx0, acc[1][2]);
+                acc[1][3] = fmaf(cu[3], swu * sx1, acc[1][3]);
             }
-            const uint8_t* st = smem + s * SB;
-            float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
-            if (!failed) {
-                box_dot(cg, st, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
-                box_dot(cu, st + kBox, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-            acc[0][0] = fmaf(cg[0], swg * sx0, acc[0][0]);
-            acc[0][1] = fmaf(cg[1], swg * sx1, acc[0][1]);
-            acc[0][2] = fmaf(cg[2], swg * sx0, acc[0][2]);
-            acc[0][3] = fmaf(cg[3], swg * sx1, acc[0][3]);
-            acc[1][0] = fmaf(cu[0], swu * sx0, acc[1][0]);
-            acc[1][1] = fmaf(cu[1], swu * sx1, acc[1][1]);
-            acc[1][2] = fmaf(cu[2], swu * sx0, acc[1][2]);
-            acc[1][3] = fmaf(cu[3], swu * sx1, acc[1][3]);
             if (++s == S) {
                 s = 0;
                 ph ^= 1;
@@ -223,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ======================================================================= down
+template <bool kMX>
 __global__ void __launch_bounds__(kThreads, 1)
     down_stream_kernel(const StreamArgs a, const __grid_constant__ TmaMap tm_d, const __grid_constant__ TmaMap tm_sd) {
     extern __shared__ uint8_t smem_raw[];
@@ -323,11 +374,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long orow = q.row_begin + col;
             const float4 gv = read4(src, pl_gu.P, 0, orow, kbq * kTile + 4 * lane);
             const float4 uv = read4(src, pl_gu.P, 1, orow, kbq * kTile + 4 * lane);
-            float sc;
-            const uint32_t code = warp_quant_block128(silu_mul(gv.x, uv.x), silu_mul(gv.y, uv.y), silu_mul(gv.z, uv.z),
-                                                      silu_mul(gv.w, uv.w), &sc);
-            reinterpret_cast<uint32_t*>(s_hq + col * hp + kbq * kBlk)[lane] = code;
-            if (lane == 0) s_hs[col * (Nmax / kBlk) + kbq] = sc;
+            const float h0 = silu_mul(gv.x, uv.x), h1 = silu_mul(gv.y, uv.y);
+            const float h2 = silu_mul(gv.z, uv.z), h3 = silu_mul(gv.w, uv.w);
+            if constexpr (kMX) {  // per 32 values: E8M0 bytes [8][Nmax/32] in place of s_hs
+                uint32_t s8;
+                const uint32_t code = warp_quant_mx32(h0, h1, h2, h3, &s8);
+                reinterpret_cast<uint32_t*>(s_hq + col * hp + kbq * kBlk)[lane] = code;
+                if ((lane & 7) == 0)
+                    reinterpret_cast<uint8_t*>(s_hs)[col * (Nmax / 32) + kbq * 4 + (lane >> 3)] = (uint8_t)s8;
+            } else {
+                float sc;
+                const uint32_t code = warp_quant_block128(h0, h1, h2, h3, &sc);
+                reinterpret_cast<uint32_t*>(s_hq + col * hp + kbq * kBlk)[lane] = code;
+                if (lane == 0) s_hs[col * (Nmax / kBlk) + kbq] = sc;
+            }
         }
         if (tid < kGroupRows) s_w[tid] = q.w[tid];
         named_bar(1, kConsThreads);
@@ -345,29 +405,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             build_operand(r);
             cur_group = grp;
         }
-        const float* swr =
-            r.shared ? a.ss_down + (size_t)r.slice * Isb : a.s_down + ((size_t)r.expert * slices + r.slice) * Ib;
+        const float* swr = nullptr;
+        const uint8_t* wd8 = nullptr;  // MXFP8: E8M0 row of this lane's weight row warp*16 + g
+        const int Ns = (r.shared ? a.Is : a.I) / 32;
+        if constexpr (kMX) {
+            wd8 = (r.shared ? a.ss_down8 : a.s_down8 + (size_t)r.expert * H * Ns) +
+                  ((size_t)r.slice * kTile + warp * 16 + g) * Ns;
+        } else {
+            swr = r.shared ? a.ss_down + (size_t)r.slice * Isb : a.s_down + ((size_t)r.expert * slices + r.slice) * Ib;
+        }
         const bool v0 = 2 * t4 < r.nrows, v1 = 2 * t4 + 1 < r.nrows;
         float acc[1][4] = {};
         for (int j = 0; j < r.n; ++j) {
             const int kb = r.kb0 + j;
-            const float sw = __ldg(swr + kb);
-            const float sx0 = s_hs[(2 * t4) * nsb + kb];
-            const float sx1 = s_hs[(2 * t4 + 1) * nsb + kb];
-            if (!failed && !mbar_wait_bounded(&full[s], ph)) {
-                set_status(a.status, kStatusTimeout);
-                failed = true;  // keep walking the units so every named barrier is still reached
+            if constexpr (kMX) {
+                const uint32_t w0 = ldg32(wd8 + kb * 4), w1 = ldg32(wd8 + 8 * Ns + kb * 4);
+                const uint8_t* hs8 = reinterpret_cast<const uint8_t*>(s_hs);
+                const uint32_t x0 = v0 ? *reinterpret_cast<const uint32_t*>(hs8 + (2 * t4) * (Nmax / 32) + kb * 4) : 0u;
+                const uint32_t x1 =
+                    v1 ? *reinterpret_cast<const uint32_t*>(hs8 + (2 * t4 + 1) * (Nmax / 32) + kb * 4) : 0u;
+                if (!failed && !mbar_wait_bounded(&full[s], ph)) {
+                    set_status(a.status, kStatusTimeout);
+                    failed = true;  // keep walking the units so every named barrier is still reached
+                }
+                float c[4][4] = {};
+                if (!failed) {
+                    box_dot_mx(c, smem + s * SB, s_hq + g * hp + kb * kBlk, g < r.nrows, warp, g, t4);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float a0 = v0 ? e8m0_to_float((x0 >> (8 * q)) & 0xFF) : 0.f;
+                    const float a1 = v1 ? e8m0_to_float((x1 >> (8 * q)) & 0xFF) : 0.f;
+                    const float ws0 = e8m0_to_float((w0 >> (8 * q)) & 0xFF), ws1 = e8m0_to_float((w1 >> (8 * q)) & 0xFF);
+                    acc[0][0] = fmaf(c[q][0], ws0 * a0, acc[0][0]);
+                    acc[0][1] = fmaf(c[q][1], ws0 * a1, acc[0][1]);
+                    acc[0][2] = fmaf(c[q][2], ws1 * a0, acc[0][2]);
+                    acc[0][3] = fmaf(c[q][3], ws1 * a1, acc[0][3]);
+                }
+            } else {
+                const float sw = __ldg(swr + kb);
+                const float sx0 = s_hs[(2 * t4) * nsb + kb];
+                const float sx1 = s_hs[(2 * t4 + 1) * nsb + kb];
+                if (!failed && !mbar_wait_bounded(&full[s], ph)) {
+                    set_status(a.status, kStatusTimeout);
+                    failed = true;  // keep walking the units so every named barrier is still reached
+                }
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                if (!failed) {
+                    box_dot(c, smem + s * SB, s_hq + g * hp + kb * kBlk, g < r.nrows, warp, g, t4);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                }
+                acc[0][0] = fmaf(c[0], v0 ? sw * sx0 : 0.f, acc[0][0]);
+                acc[0][1] = fmaf(c[1], v1 ? sw * sx1 : 0.f, acc[0][1]);
+                acc[0][2] = fmaf(c[2], v0 ? sw * sx0 : 0.f, acc[0][2]);
+                acc[0][3] = fmaf(c[3], v1 ? sw * sx1 : 0.f, acc[0][3]);
             }
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            if (!failed) {
-                box_dot(c, smem + s * SB, s_hq + g * hp + kb * kBlk, g < r.nrows, warp, g, t4);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-            acc[0][0] = fmaf(c[0], v0 ? sw * sx0 : 0.f, acc[0][0]);
-            acc[0][1] = fmaf(c[1], v1 ? sw * sx1 : 0.f, acc[0][1]);
-            acc[0][2] = fmaf(c[2], v0 ? sw * sx0 : 0.f, acc[0][2]);
-            acc[0][3] = fmaf(c[3], v1 ? sw * sx1 : 0.f, acc[0][3]);
             if (++s == S) {
                 s = 0;
                 ph ^= 1;
@@ -536,8 +631,9 @@ int stream_max_parts(const moe_config_t& c, int64_t T) {
 
 cudaError_t launch_gateup_stream(const StreamArgs& a, const uint8_t* w_gate, const uint8_t* w_up, int E,
                                  cudaStream_t st) {
-    static size_t smem_set = 0;
-    cudaError_t e = set_smem((const void*)gateup_stream_kernel, smem_gateup(), &smem_set);
+    static size_t smem_set[2] = {0, 0};
+    const void* kern = a.mx ? (const void*)gateup_stream_kernel<true> : (const void*)gateup_stream_kernel<false>;
+    cudaError_t e = set_smem(kern, smem_gateup(), &smem_set[a.mx ? 1 : 0]);
     if (e != cudaSuccess) return e;
     TmaMap tg{}, tu{}, tsg{}, tsu{};
     if (!tmap_u8_2d(&tg, w_gate, (uint64_t)E * a.I, a.H, kBlk, kTile) ||
@@ -546,19 +642,22 @@ cudaError_t launch_gateup_stream(const StreamArgs& a, const uint8_t* w_gate, con
     if (a.Is > 0 && (!tmap_u8_2d(&tsg, a.ws_gate, a.Is, a.H, kBlk, kTile) ||
                      !tmap_u8_2d(&tsu, a.ws_up, a.Is, a.H, kBlk, kTile)))
         return cudaErrorInvalidValue;
-    return launch_pdl(gateup_stream_kernel, a.grid_gu, kThreads, smem_gateup(), st, a, tg, tu, tsg, tsu);
+    return a.mx ? launch_pdl(gateup_stream_kernel<true>, a.grid_gu, kThreads, smem_gateup(), st, a, tg, tu, tsg, tsu)
+                : launch_pdl(gateup_stream_kernel<false>, a.grid_gu, kThreads, smem_gateup(), st, a, tg, tu, tsg, tsu);
 }
 
 cudaError_t launch_down_stream(const StreamArgs& a, const uint8_t* w_down, const uint8_t* ws_down, int E,
                                cudaStream_t st) {
-    static size_t smem_set = 0;
+    static size_t smem_set[2] = {0, 0};
     const size_t smem = smem_down(std::max(a.I, a.Is));
-    cudaError_t e = set_smem((const void*)down_stream_kernel, smem, &smem_set);
+    const void* kern = a.mx ? (const void*)down_stream_kernel<true> : (const void*)down_stream_kernel<false>;
+    cudaError_t e = set_smem(kern, smem, &smem_set[a.mx ? 1 : 0]);
     if (e != cudaSuccess) return e;
     TmaMap td{}, tsd{};
     if (!tmap_u8_2d(&td, w_down, (uint64_t)E * a.H, a.I, kBlk, kTile)) return cudaErrorInvalidValue;
     if (a.Is > 0 && !tmap_u8_2d(&tsd, ws_down, a.H, a.Is, kBlk, kTile)) return cudaErrorInvalidValue;
-    return launch_pdl(down_stream_kernel, a.grid_d, kThreads, smem, st, a, td, tsd);
+    return a.mx ? launch_pdl(down_stream_kernel<true>, a.grid_d, kThreads, smem, st, a, td, tsd)
+                : launch_pdl(down_stream_kernel<false>, a.grid_d, kThreads, smem, st, a, td, tsd);
 }
 
 cudaError_t launch_stream_combine(const StreamArgs& a, cudaStream_t st) {

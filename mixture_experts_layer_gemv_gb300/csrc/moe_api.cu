@@ -23,8 +23,8 @@ int num_sms() {
 
 static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
-int router_splits_for(const moe_config_t& c, int64_t T, bool large_route) {
-    if (T <= kSmallT && !large_route) return 1;  // the fused small-T route kernel
+int router_splits_for(const moe_config_t& c, int64_t T) {
+    if (T <= kSmallT) return 1;  // the fused small-T route kernel
     const int64_t tiles = (T + 63) / 64;     // router CTAs: 64 tokens x all experts each
     int64_t s = (304 + tiles - 1) / tiles;  // aim at two CTAs per SM of a 152-SM part
     const int64_t hb = c.hidden / 128;
@@ -53,7 +53,7 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T, bool mx) {
     const size_t H = c.hidden, I = c.moe_inter, E = c.n_routed, k = c.top_k;
     const size_t Is = (size_t)c.n_shared * c.moe_inter;
     const size_t t = (size_t)T;
-    L.router_splits = router_splits_for(c, T, mx);
+    L.router_splits = router_splits_for(c, T);
     L.max_groups = max_routed_groups(c, T);
     L.ctrl = take(kCtrlRegionBytes);
     L.logits = take((size_t)L.router_splits * t * E * 4);  // router split-K partials
@@ -69,9 +69,10 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T, bool mx) {
     L.group_of_row = take(t * k * 4);
     // the streaming GEMVs' partial sums; on the GEMM path they stay sized for kSmallT
     // tokens so that the workspace size never shrinks as T grows
-    const bool gemm = mx || use_gemm(c, T);
-    const size_t ts = mx ? 0 : gemm ? (size_t)kSmallT : t;
-    const size_t P = mx ? 0 : (size_t)stream_max_parts(c, (int64_t)ts);
+    // the MXFP8 variant streams at T <= 64 too, and its GEMM needs no 256-multiple hidden
+    const bool gemm = mx ? T > kSmallT : use_gemm(c, T);
+    const size_t ts = gemm ? (size_t)kSmallT : t;
+    const size_t P = (size_t)stream_max_parts(c, (int64_t)ts);
     {
         const size_t t = ts;
     L.g_r = take(P * t * k * I * 4);
@@ -222,6 +223,28 @@ StreamArgs stream_args(const moe_config_t* c, int32_t T, const moe_weights_t* W,
     a.y_s = at<float>(ws, L.y_s);
     a.yb_s = at<float>(ws, L.yb_s);
     a.status = &at<Ctrl>(ws, L.ctrl)->status;
+    return a;
+}
+
+// The streaming kernels' arguments for MXFP8 weights (E8M0 scale rows).
+StreamArgs stream_args_mx(const moe_config_t* c, int32_t T, const moe_weights_mx_t* W, const WsLayout& L, void* ws,
+                          const int32_t* perm_src, const float* topk_w) {
+    moe_weights_t Wb = {};  // codes and router only; the fp32 scale pointers stay null
+    Wb.w_gate = W->w_gate;
+    Wb.w_up = W->w_up;
+    Wb.w_down = W->w_down;
+    Wb.ws_gate = W->ws_gate;
+    Wb.ws_up = W->ws_up;
+    Wb.ws_down = W->ws_down;
+    StreamArgs a = stream_args(c, T, &Wb, L, ws, perm_src, topk_w);
+    a.mx = 1;
+    a.s_gate8 = W->s_gate;
+    a.s_up8 = W->s_up;
+    a.s_down8 = W->s_down;
+    a.ss_gate8 = W->ss_gate;
+    a.ss_up8 = W->ss_up;
+    a.ss_down8 = W->ss_down;
+    a.xs8 = at<uint8_t>(ws, L.xs8);
     return a;
 }
 
@@ -734,6 +757,31 @@ moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16
     Ctrl* ctrl = at<Ctrl>(ws, L.ctrl);
 
     MOE_TRY(mark.begin(MOE_STAGE_ROUTE));
+    if (T <= kSmallT) {
+        // decode: the fused route (x quantised per 32), then the weight-streaming kernels
+        MOE_CUDA(launch_route_small(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
+                                    at<float>(ws, L.logits), at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
+                                    at<int32_t>(ws, L.offsets), perm_src, inv_pos, at<RowGroup>(ws, L.groups),
+                                    at<int32_t>(ws, L.group_of_row), ctrl, NormArgs{}, st, at<uint8_t>(ws, L.xs8)));
+        MOE_TRY(mark.end(MOE_STAGE_ROUTE));
+        StreamArgs a = stream_args_mx(cfg, T, weights, L, ws, perm_src, w);
+        a.fuse_combine = 1;
+        a.residual = static_cast<const __nv_bfloat16*>(residual_bf16);
+        a.out = static_cast<__nv_bfloat16*>(out_bf16);
+        MOE_TRY(mark.begin(MOE_STAGE_GATE_UP));
+        MOE_CUDA(launch_gateup_stream(a, weights->w_gate, weights->w_up, cfg->n_routed, st));
+        MOE_TRY(mark.end(MOE_STAGE_GATE_UP));
+        MOE_TRY(mark.begin(MOE_STAGE_DOWN));
+        MOE_CUDA(launch_down_stream(a, weights->w_down, weights->ws_down, cfg->n_routed, st));
+        MOE_TRY(mark.end(MOE_STAGE_DOWN));
+        MOE_TRY(mark.begin(MOE_STAGE_COMBINE));
+        MOE_CUDA(launch_stream_combine(a, st));
+        MOE_TRY(mark.end(MOE_STAGE_COMBINE));
+        if (topk_ids_out)
+            MOE_CUDA(cudaMemcpyAsync(topk_ids_out, ids, (size_t)T * cfg->top_k * sizeof(int32_t),
+                                     cudaMemcpyDeviceToDevice, st));
+        return MOE_OK;
+    }
     MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
                                 at<float>(ws, L.logits), L.router_splits, NormArgs{}, st));
     MOE_CUDA(launch_quant_act_mx(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs8), NormArgs{},

@@ -80,9 +80,9 @@ struct WsLayout {
     int max_groups;
 };
 
-// mx: the MXFP8 variant's layout (grouped-GEMM path at every T, no streaming partials)
+// mx: the MXFP8 variant's layout (E8M0 activation and intermediate scales added)
 WsLayout ws_layout(const moe_config_t& c, int64_t T, bool mx = false);
-int router_splits_for(const moe_config_t& c, int64_t T, bool large_route = false);
+int router_splits_for(const moe_config_t& c, int64_t T);
 int max_routed_groups(const moe_config_t& c, int64_t T);
 
 // Optional stage M in front of a kernel: gamma == nullptr means the input is used
@@ -104,13 +104,13 @@ cudaError_t launch_quant_act(const void* x, int T, int H, uint8_t* xq, float* xs
 cudaError_t launch_rmsnorm(const void* x, int T, int H, const NormArgs& nm, void* x_out, cudaStream_t st);
 
 // Fused small-T route: (stage M when nm.gamma, computed in-kernel), logits, x
-// quantisation, softmax + top-k, and (when offsets != nullptr) the permutation and
+// quantisation (MXFP8, per 32 values into xs8, when xs8 != nullptr), softmax + top-k, and (when offsets != nullptr) the permutation and
 // row-group descriptors.
 cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits,
                                uint8_t* xq, float* xs, int32_t* offsets, int32_t* perm_src,
                                int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl,
-                               const NormArgs& nm, cudaStream_t st);
+                               const NormArgs& nm, cudaStream_t st, uint8_t* xs8 = nullptr);
 
 // Large-T route: router GEMM (split-K partials) + softmax/top-k per token. With
 // nm.gamma the router reads stage M's output on the fly (nm.rstd from launch_rmsnorm).
@@ -164,6 +164,11 @@ struct StreamArgs {
     const float *s_down, *ss_down;
     float *y_r, *yb_r;  // fp32 weighted expert rows [P][T*k, H]: A and B buffers
     float *y_s, *yb_s;  // shared rows [P][T, H]
+    // MXFP8 variant (mx = 1): E8M0 scales, one byte per row and 32 K, replace the fp32
+    // block scales above; the activation scales xs8 [T, H/32] replace xs
+    int mx;
+    const uint8_t *s_gate8, *s_up8, *ss_gate8, *ss_up8, *s_down8, *ss_down8;
+    const uint8_t* xs8;
     // combine
     int fuse_combine;  // 1: out (bf16) = sum of rows + shared (+ residual); 0: y_perm / y_shared (bf16)
     __nv_bfloat16* y_perm;

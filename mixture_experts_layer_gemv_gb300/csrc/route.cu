@@ -44,9 +44,12 @@ struct RouteSmallParams {
     Ctrl* ctrl;
     const uint16_t* gamma;  // stage M in front of the router when not null
     float eps;
+    uint8_t* xs8;           // MXFP8: E8M0 scales [T, H/32] (xs unused)
 };
 
-template <bool kNorm>  // stage M in front of the router (p.gamma != nullptr)
+// kNorm: stage M in front of the router (p.gamma != nullptr); kMX: x quantised per 32
+// values with E8M0 scales (p.xs8) instead of per 128 with fp32 scales (p.xs)
+template <bool kNorm, bool kMX>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmallParams p) {
     __shared__ float s_part[kRouteWarps][kSmallT];
     __shared__ float s_gs[kRouteWarps][kMaxE];
@@ -144,12 +147,19 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
             const uint2 g = __ldg(reinterpret_cast<const uint2*>(p.gamma + kb * kBlk) + lane);
             xv = make_uint2(rms_apply2(xv.x, s_rstd[t], g.x), rms_apply2(xv.y, s_rstd[t], g.y));
         }
-        float s;
-        const uint32_t q = warp_quant_block128(
-            bf16_bits_to_float((uint16_t)(xv.x & 0xFFFF)), bf16_bits_to_float((uint16_t)(xv.x >> 16)),
-            bf16_bits_to_float((uint16_t)(xv.y & 0xFFFF)), bf16_bits_to_float((uint16_t)(xv.y >> 16)), &s);
-        reinterpret_cast<uint32_t*>(p.xq + (size_t)t * H + kb * kBlk)[lane] = q;
-        if (lane == 0) p.xs[(size_t)t * Hb + kb] = s;
+        const float v0 = bf16_bits_to_float((uint16_t)(xv.x & 0xFFFF)), v1 = bf16_bits_to_float((uint16_t)(xv.x >> 16));
+        const float v2 = bf16_bits_to_float((uint16_t)(xv.y & 0xFFFF)), v3 = bf16_bits_to_float((uint16_t)(xv.y >> 16));
+        if constexpr (kMX) {
+            uint32_t s8;
+            const uint32_t q = warp_quant_mx32(v0, v1, v2, v3, &s8);
+            reinterpret_cast<uint32_t*>(p.xq + (size_t)t * H + kb * kBlk)[lane] = q;
+            if ((lane & 7) == 0) p.xs8[(size_t)t * (H / 32) + kb * 4 + (lane >> 3)] = (uint8_t)s8;
+        } else {
+            float s;
+            const uint32_t q = warp_quant_block128(v0, v1, v2, v3, &s);
+            reinterpret_cast<uint32_t*>(p.xq + (size_t)t * H + kb * kBlk)[lane] = q;
+            if (lane == 0) p.xs[(size_t)t * Hb + kb] = s;
+        }
     }
 
     // ---- last CTA to arrive: O (softmax + top-k) and the permutation
@@ -480,7 +490,7 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
                                const float* bias, int32_t* ids, float* w, float* logits, uint8_t* xq,
                                float* xs, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
                                RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl, const NormArgs& nm,
-                               cudaStream_t st) {
+                               cudaStream_t st, uint8_t* xs8) {
     RouteSmallParams p;
     p.H = c.hidden;
     p.E = c.n_routed;
@@ -505,6 +515,7 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
     p.ctrl = ctrl;
     p.gamma = nm.gamma;
     p.eps = nm.eps;
+    p.xs8 = nullptr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.n_routed);
     cfg.blockDim = dim3(kRouteWarps * 32);
@@ -514,8 +525,13 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return nm.gamma ? cudaLaunchKernelEx(&cfg, route_small_kernel<true>, p)
-                    : cudaLaunchKernelEx(&cfg, route_small_kernel<false>, p);
+    if (xs8) {
+        p.xs8 = xs8;
+        return nm.gamma ? cudaLaunchKernelEx(&cfg, route_small_kernel<true, true>, p)
+                        : cudaLaunchKernelEx(&cfg, route_small_kernel<false, true>, p);
+    }
+    return nm.gamma ? cudaLaunchKernelEx(&cfg, route_small_kernel<true, false>, p)
+                    : cudaLaunchKernelEx(&cfg, route_small_kernel<false, false>, p);
 }
 
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,

@@ -165,6 +165,24 @@ __device__ __forceinline__ void box_dot(float (&c)[4], const uint8_t* box, const
     }
 }
 
+// MXFP8: the same box times 8 activation rows, one fp32 16x8 partial per 32-wide K block
+// (c[q], q = 0..3), so that each block's E8M0 scales can be applied to its own partial.
+// Lane (g, t4) supplies bytes [32q + 8t4, 32q + 8t4 + 8) of its A rows and B column for
+// the MMA of block q; the MMA pairs A's and B's K slots the same way, so the products
+// match and the sum runs over exactly that block.
+__device__ __forceinline__ void box_dot_mx(float (&c)[4][4], const uint8_t* box, const uint8_t* brow, bool bvalid,
+                                           int warp, int g, int t4) {
+    const int r = warp * 16 + g;  // rows r and r + 8 share the swizzle phase r % 8
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int off = (((2 * q + (t4 >> 1)) ^ (r & 7)) << 4) + 8 * (t4 & 1);
+        const uint2 lo = *reinterpret_cast<const uint2*>(box + r * kBlk + off);
+        const uint2 hi = *reinterpret_cast<const uint2*>(box + (r + 8) * kBlk + off);
+        const uint2 b = bvalid ? *reinterpret_cast<const uint2*>(brow + 32 * q + 8 * t4) : make_uint2(0, 0);
+        mma_e4m3_16832(c[q], lo.x, hi.x, lo.y, hi.y, b.x, b.y);
+    }
+}
+
 struct Range {
     long U, u0, u1, first_tile;
     int nb, b, kb0;

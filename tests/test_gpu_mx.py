@@ -1,6 +1,7 @@
 """The MXFP8 variant through the C ABI against the oracle: E4M3 codes with one UE8M0
-scale per row and 32 consecutive K for weights and activations, all scales applied
-inside the tensor core (tcgen05.mma kind::mxf8f6f4).
+scale per row and 32 consecutive K for weights and activations; the grouped GEMM (T > 64)
+applies the scales inside the tensor core (tcgen05.mma kind::mxf8f6f4), the
+weight-streaming kernels (T <= 64) per 32-wide MMA partial.
 
 Bars: activation codes and scale bytes bit-exact; expert ids bit-exact on unflagged
 tokens (routing is moe_route's); outputs within max|err| <= 2e-2 * max|ref| + 1e-3.
@@ -69,10 +70,10 @@ def test_forward_mx_ragged(T):
     _check(MX_CFG, W, x, residual=res)
 
 
-def test_forward_mx_scrambled_scales():
+@pytest.mark.parametrize("T", [7, 200])  # weight-streaming path, grouped GEMM
+def test_forward_mx_scrambled_scales(T):
     """Scale bytes that differ strongly between the 32-blocks of every row (weights and
     activations), so a scale applied to the wrong K step or row shows at once."""
-    T = 200
     W = make_weights_mx(MX_CFG, 120, "cuda")
     g = torch.Generator(device="cuda").manual_seed(121)
     for k in ("s_gate", "s_up", "s_down", "ss_gate", "ss_up", "ss_down"):
