@@ -57,7 +57,7 @@ constexpr int kSfAtom = 512;               // one K block of 128 rows
 constexpr int kSfA = kSfGroup * kSfAtom;   // 2 KB
 constexpr int kSfB = 2 * kSfGroup * kSfAtom;  // 4 KB: two 128-row halves
 constexpr int kSfStage = kSfA + kSfB;
-constexpr int kSfSlots = 2;
+constexpr int kSfSlots = 4;  // TMEM: 256 + 4 x 64 columns = 512
 constexpr uint32_t kXTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kSfSlotCols = 64;
@@ -156,10 +156,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
             gc.item = blockIdx.x;
             gc.kb = 0;
             gc.set(a, n_mt_r, n_items, gateup);
-            // scale rows of the next group, fetched one group ahead of their use:
-            // A rows row0 + lane + 32*m1, B half h rows yb_h + lane + 32*m1 (16 bytes each)
-            uint4 pa[4], pb[8];
-            auto fetch = [&]() {
+            // scale rows of a group: A rows row0 + lane + 32*m1, B half h rows yb_h + lane + 32*m1
+            // (16 bytes each). Two register sets: the loads of groups g+1 and g+2 are in flight
+            // while group g waits for its slot, so a group's load latency spans two groups' MMAs.
+            auto fetch = [&](uint4 (&pa)[4], uint4 (&pb)[8]) {
                 if (gc.item >= n_items) return;
                 const int Kg = (gc.shared ? a.K_s : a.K_r) / 32;  // scale bytes per row
                 const size_t off = (size_t)(gc.kb / kSfGroup) * kSfRow;
@@ -188,15 +188,14 @@ __global__ void __launch_bounds__(kXThreads, 1)
                     gc.set(a, n_mt_r, n_items, gateup);
                 }
             };
-            fetch();
-            const int groups = total / kSfGroup;
-            for (int g = 0; g < groups; ++g) {
+            // waits for slot g % kSfSlots, stores the group as 512-byte atoms, hands it over
+            auto publish = [&](int g, const uint4 (&pa)[4], const uint4 (&pb)[8]) -> bool {
                 const int j = g % kSfSlots;
                 bool ok = true;
                 if (g >= kSfSlots && lane == 0) ok = mbar_wait_bounded(&sf_empty[j], ((g / kSfSlots) - 1) & 1);
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
                     if (lane == 0) set_status(a.status, kStatusTimeout);
-                    break;
+                    return false;
                 }
                 uint8_t* sf = sf_smem + j * kSfStage;
 #pragma unroll
@@ -212,7 +211,19 @@ __global__ void __launch_bounds__(kXThreads, 1)
                 fence_proxy_async_smem();  // the tensor core reads these through the async proxy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sf_full[j]);
-                fetch();
+                return true;
+            };
+            uint4 pa0[4], pb0[8], pa1[4], pb1[8];
+            fetch(pa0, pb0);
+            fetch(pa1, pb1);
+            const int groups = total / kSfGroup;
+            for (int g = 0; g < groups; g += 2) {
+                if (!publish(g, pa0, pb0)) break;
+                fetch(pa0, pb0);
+                if (g + 1 < groups) {
+                    if (!publish(g + 1, pa1, pb1)) break;
+                    fetch(pa1, pb1);
+                }
             }
         }
     } else if (warp == kXMmaWarp) {
