@@ -67,6 +67,7 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T, bool mx) {
     L.inv_pos = take(t * k * 4);
     L.groups = take((size_t)L.max_groups * sizeof(RowGroup));
     L.group_of_row = take(t * k * 4);
+    L.perm_hist = take((size_t)permute_segments((int64_t)(t * k)) * E * 4);
     // the streaming GEMVs' partial sums; on the GEMM path they stay sized for kSmallT
     // tokens so that the workspace size never shrinks as T grows
     // the MXFP8 variant streams at T <= 64 too, and its GEMM needs no 256-multiple hidden
@@ -544,7 +545,7 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32
     MOE_TRY(check_ws(cfg, T, ws, ws_bytes));
     const WsLayout L = ws_layout(*cfg, T);
     MOE_CUDA(launch_permute(*cfg, topk_ids, T, expert_offsets, perm_src, inv_pos, nullptr, nullptr, nullptr,
-                            at<Ctrl>(ws, L.ctrl), (cudaStream_t)stream));
+                            at<int32_t>(ws, L.perm_hist), at<Ctrl>(ws, L.ctrl), (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -644,7 +645,7 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
         MOE_TRY(mark.begin(MOE_STAGE_PERMUTE));
         if (use_gemm(*cfg, T)) {
             MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, nullptr, nullptr,
-                                    at<MTile>(ws, L.mtiles), ctrl, st));
+                                    at<MTile>(ws, L.mtiles), at<int32_t>(ws, L.perm_hist), ctrl, st));
             MOE_CUDA(launch_gather_rows(T, cfg->hidden, cfg->top_k, perm_src, at<uint8_t>(ws, L.xq),
                                         at<uint8_t>(ws, L.xq_perm), &ctrl->status, st));
             MOE_TRY(mark.end(MOE_STAGE_PERMUTE));
@@ -662,7 +663,7 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
             return MOE_OK;
         }
         MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups,
-                                at<int32_t>(ws, L.group_of_row), nullptr, ctrl, st));
+                                at<int32_t>(ws, L.group_of_row), nullptr, at<int32_t>(ws, L.perm_hist), ctrl, st));
         MOE_TRY(mark.end(MOE_STAGE_PERMUTE));
     }
     StreamArgs a = stream_args(cfg, T, weights, L, ws, perm_src, w);
@@ -789,7 +790,7 @@ moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16
     MOE_TRY(mark.end(MOE_STAGE_ROUTE));
     MOE_TRY(mark.begin(MOE_STAGE_PERMUTE));
     MOE_CUDA(launch_permute(*cfg, ids, T, at<int32_t>(ws, L.offsets), perm_src, inv_pos, nullptr, nullptr,
-                            at<MTile>(ws, L.mtiles), ctrl, st));
+                            at<MTile>(ws, L.mtiles), at<int32_t>(ws, L.perm_hist), ctrl, st));
     MOE_CUDA(launch_gather_rows(T, cfg->hidden, cfg->top_k, perm_src, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xq_perm),
                                 &ctrl->status, st, at<uint8_t>(ws, L.xs8), at<uint8_t>(ws, L.xs8_perm)));
     MOE_TRY(mark.end(MOE_STAGE_PERMUTE));

@@ -62,6 +62,7 @@ struct WsLayout {
     size_t inv_pos;    // int32 [T*k]
     size_t groups;     // RowGroup [max_groups]
     size_t group_of_row;  // int32 [T*k]
+    size_t perm_hist;  // int32 [ceil(T*k/1024), E] per-segment expert counts of the permutation
     size_t g_r, u_r, gb_r, ub_r;  // fp32 [P][T*k, I] each
     size_t g_s, u_s, gb_s, ub_s;  // fp32 [P][T, Is] each
     size_t y_r, yb_r;             // fp32 [P][T*k, H] each
@@ -119,9 +120,11 @@ cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, cons
                                const NormArgs& nm, cudaStream_t st);
 
 // Stable counting sort of the T*k pairs by expert; writes row groups when groups != nullptr.
+// seg_hist: int32 [permute_segments(T*k), E] scratch.
+int permute_segments(int64_t n);
 cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int32_t* offsets,
                            int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row,
-                           MTile* mtiles, Ctrl* ctrl, cudaStream_t st);
+                           MTile* mtiles, int32_t* seg_hist, Ctrl* ctrl, cudaStream_t st);
 
 // Row groups from existing expert offsets (stage API path).
 cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, int n_rows, RowGroup* groups,

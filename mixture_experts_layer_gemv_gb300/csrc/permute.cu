@@ -3,12 +3,14 @@
 // never travel to the host (MoK abstract: no CPU-GPU synchronisation; the
 // DeepSeek-V4.1 Flash lecture's "router emits the layout the experts need").
 //
-// One CTA of 32 warps: warp w owns a contiguous segment of flat indices,
-// counts its experts into a private shared-memory histogram, the histograms are
-// scanned expert-major / warp-minor, and each warp then walks its segment in
-// order, ranking equal experts inside each 32-wide chunk with __match_any_sync.
-// The same kernel emits the work list of the expert kernels: row groups of <= 8
-// rows for the streaming GEMVs, or 128-row tiles for the grouped GEMM.
+// Two launches over segments of 1024 flat indices, one CTA of 8 warps each:
+// permute_count_kernel writes every segment's expert histogram; permute_scatter_kernel
+// turns the histograms into each segment's base per expert (totals scanned expert-major,
+// earlier segments first), recounts its segment per warp, and each warp then walks its
+// 128 indices in order, ranking equal experts inside each 32-wide chunk with
+// __match_any_sync. The result equals a sequential stable sort. CTA 0 also writes the
+// expert offsets and the work list of the expert kernels: row groups of <= 8 rows for
+// the streaming GEMVs, or 128-row tiles for the grouped GEMM.
 #include <climits>
 
 #include "common.cuh"
@@ -18,9 +20,10 @@ namespace moe {
 
 namespace {
 
-constexpr int kPermWarps = 32;
+constexpr int kPermWarps = 8;
+constexpr int kPermSeg = 1024;                     // flat indices per CTA
+constexpr int kWarpSeg = kPermSeg / kPermWarps;    // 128 per warp: 4 chunks of 32
 constexpr int kMaxE = 256;
-constexpr int kBatch = 16;  // 32-id chunks a warp loads before using them
 
 __device__ int scan_exclusive_warp256(int* v, int n) {
     const int lane = threadIdx.x & 31;
@@ -106,92 +109,106 @@ struct PermuteParams {
     int32_t* offsets;
     int32_t* perm_src;
     int32_t* inv_pos;
+    int32_t* seg_hist;  // [segments, E] expert counts of each segment
     RowGroup* groups;
     int32_t* group_of_row;
     MTile* mtiles;
     Ctrl* ctrl;
 };
 
-__global__ void __launch_bounds__(kPermWarps * 32) permute_kernel(PermuteParams p) {
-    __shared__ int hist[kPermWarps][kMaxE];
-    __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_goff[kMaxE];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int E = p.E, n = p.n;
-    const int seg = (n + kPermWarps - 1) / kPermWarps;
-    const int f_begin = min(n, warp * seg), f_end = min(n, f_begin + seg);
-
-    for (int i = threadIdx.x; i < kPermWarps * kMaxE; i += blockDim.x) (&hist[0][0])[i] = 0;
-    __syncthreads();
-    // ids are read kBatch chunks of 32 at a time: one memory round trip per batch
-    for (int base = f_begin; base < f_end; base += 32 * kBatch) {
-        int ev[kBatch];
+// The 4 x 32 expert ids of this warp's slice of a segment (-1 past the end or out of range).
+__device__ __forceinline__ void load_warp_ids(const PermuteParams& p, int f0, int (&ev)[kWarpSeg / 32], bool flag) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int f = base + lane + 32 * u;
-            ev[u] = f < f_end ? __ldg(p.ids + f) : INT_MIN;
+    for (int u = 0; u < kWarpSeg / 32; ++u) {
+        const int f = f0 + lane + 32 * u;
+        int e = -1;
+        if (f < p.n) {
+            e = __ldg(p.ids + f);
+            if (e < 0 || e >= p.E) {
+                if (flag) set_status(&p.ctrl->status, kStatusBadId);
+                e = -1;
+            }
         }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int e = ev[u];
-            if (e == INT_MIN) continue;
-            if (e >= 0 && e < E)
-                atomicAdd(&hist[warp][e], 1);
-            else
-                set_status(&p.ctrl->status, kStatusBadId);
-        }
+        ev[u] = e;
     }
+}
+
+__global__ void __launch_bounds__(kPermWarps * 32) permute_count_kernel(PermuteParams p) {
+    __shared__ int hist[kMaxE];
+    const int warp = threadIdx.x >> 5;
+    pdl_launch_dependents();  // the scatter kernel waits for this grid's completion itself
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) hist[e] = 0;
     __syncthreads();
-    // hist[w][e] <- pairs of expert e in segments before w; s_cnt[e] <- total
+    int ev[kWarpSeg / 32];
+    load_warp_ids(p, blockIdx.x * kPermSeg + warp * kWarpSeg, ev, true);
+#pragma unroll
+    for (int u = 0; u < kWarpSeg / 32; ++u)
+        if (ev[u] >= 0) atomicAdd(&hist[ev[u]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.seg_hist[(size_t)blockIdx.x * p.E + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(kPermWarps * 32) permute_scatter_kernel(PermuteParams p) {
+    __shared__ int hist[kPermWarps][kMaxE];
+    __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_pre[kMaxE], s_goff[kMaxE];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E, seg = blockIdx.x, n_seg = gridDim.x;
+    int ev[kWarpSeg / 32];
+    load_warp_ids(p, seg * kPermSeg + warp * kWarpSeg, ev, false);  // ids come from before the count kernel
+    for (int i = threadIdx.x; i < kPermWarps * kMaxE; i += blockDim.x) (&hist[0][0])[i] = 0;
+    pdl_wait();  // the segment histograms
+    // per expert: pairs in earlier segments (s_pre) and in all segments (s_cnt)
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-        for (int w = 0; w < kPermWarps; ++w) {
-            const int c = hist[w][e];
-            hist[w][e] = run;
-            run += c;
+        int pre = 0, tot = 0;
+        for (int c = 0; c < n_seg; ++c) {
+            const int h = p.seg_hist[(size_t)c * E + e];
+            pre += c < seg ? h : 0;
+            tot += h;
         }
-        s_cnt[e] = run;
-        s_off[e] = run;
+        s_pre[e] = pre;
+        s_cnt[e] = tot;
+        s_off[e] = tot;
     }
     __syncthreads();
     if (warp == 0) {
         const int tot = scan_exclusive_warp256(s_off, E);
         if (lane == 0) s_off[E] = tot;
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) p.offsets[e] = s_off[e];
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        for (int w = 0; w < kPermWarps; ++w) hist[w][e] += s_off[e];
-    __syncthreads();
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base0 = f_begin; base0 < f_end; base0 += 32 * kBatch) {
-        int ev[kBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int f = base0 + lane + 32 * u;
-            int e = -1;
-            if (f < f_end) {
-                e = __ldg(p.ids + f);
-                if (e < 0 || e >= E) e = -1;
-            }
-            ev[u] = e;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            if (base0 + 32 * u >= f_end) break;  // warp-uniform
-            const int f = base0 + lane + 32 * u;
-            const int e = ev[u];
-            const unsigned peers = __match_any_sync(0xffffffffu, e);
-            const int rank = __popc(peers & lt_mask);
-            if (e >= 0) {
-                const int pos = hist[warp][e] + rank;
-                p.perm_src[pos] = f;
-                p.inv_pos[f] = pos;
-            }
-            __syncwarp();
-            if (e >= 0 && lane == __ffs(peers) - 1) hist[warp][e] += __popc(peers);
-            __syncwarp();
+    for (int u = 0; u < kWarpSeg / 32; ++u)
+        if (ev[u] >= 0) atomicAdd(&hist[warp][ev[u]], 1);
+    __syncthreads();
+    if (seg == 0)
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) p.offsets[e] = s_off[e];
+    // hist[w][e] <- first row of expert e for warp w of this segment
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = s_off[e] + s_pre[e];
+        for (int w = 0; w < kPermWarps; ++w) {
+            const int c = hist[w][e];
+            hist[w][e] = run;
+            run += c;
         }
     }
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int f0 = seg * kPermSeg + warp * kWarpSeg;
+#pragma unroll
+    for (int u = 0; u < kWarpSeg / 32; ++u) {
+        const int f = f0 + lane + 32 * u;
+        const int e = ev[u];
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & lt_mask);
+        if (e >= 0) {
+            const int pos = hist[warp][e] + rank;
+            p.perm_src[pos] = f;
+            p.inv_pos[f] = pos;
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) hist[warp][e] += __popc(peers);
+        __syncwarp();
+    }
+    if (seg != 0) return;
     if (p.groups) {
         __syncthreads();
         write_groups(s_cnt, s_off, s_goff, E, p.groups, p.group_of_row, p.ctrl);
@@ -279,9 +296,11 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int T, int H, int k, c
 
 }  // namespace
 
+int permute_segments(int64_t n) { return n > 0 ? (int)((n + kPermSeg - 1) / kPermSeg) : 1; }
+
 cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int32_t* offsets,
                            int32_t* perm_src, int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row,
-                           MTile* mtiles, Ctrl* ctrl, cudaStream_t st) {
+                           MTile* mtiles, int32_t* seg_hist, Ctrl* ctrl, cudaStream_t st) {
     PermuteParams p;
     p.E = c.n_routed;
     p.n = T * c.top_k;
@@ -289,12 +308,26 @@ cudaError_t launch_permute(const moe_config_t& c, const int32_t* ids, int T, int
     p.offsets = offsets;
     p.perm_src = perm_src;
     p.inv_pos = inv_pos;
+    p.seg_hist = seg_hist;
     p.groups = groups;
     p.group_of_row = group_of_row;
     p.mtiles = mtiles;
     p.ctrl = ctrl;
-    permute_kernel<<<1, kPermWarps * 32, 0, st>>>(p);
-    return cudaGetLastError();
+    const int segs = permute_segments(p.n);
+    permute_count_kernel<<<segs, kPermWarps * 32, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the scatter's id loads and shared-memory set-up overlap the count kernel's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(segs);
+    cfg.blockDim = dim3(kPermWarps * 32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, permute_scatter_kernel, p);
 }
 
 cudaError_t launch_build_groups(const moe_config_t& c, const int32_t* offsets, int n_rows, RowGroup* groups,
