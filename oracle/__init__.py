@@ -79,6 +79,9 @@ def _load():
             lib.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
             lib.orc_quant_rows_mx.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P]
             lib.orc_forward_tokens_mx.argtypes = [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P]
+            lib.orc_forward_fixed_ids_d.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int, _P, _P]
+            lib.orc_backward_d.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P,
+                                           _P, _P, _P]
             lib.orc_num_threads.restype = ctypes.c_int
             lib.orc_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -332,3 +335,54 @@ def forward(cfg, weights_dict, x_bf16, bias=None, w_router=None, tokens=None, re
                          weights_dict.get("router_bias") if bias is None else bias)
     out = forward_tokens(cfg, W, x_bf16, ids, w, tokens, residual_bf16, act_quant)
     return out, ids, w, m
+
+
+def _bf16_to_f64(x) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64 values; float arrays pass through as float64."""
+    a = _np(x, np.uint16) if (hasattr(x, "dtype") and str(x.dtype) in ("torch.bfloat16", "uint16")) else None
+    if a is None:
+        return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def forward_fixed_ids(cfg, weights: Weights, x, ids, w_router, bias=None, act_quant=True) -> np.ndarray:
+    """Layer output (fp64, [T, H]) with the expert choice `ids` fixed and the routing
+    weights recomputed from x: the function the backward differentiates. x is fp64
+    [T, H] (or bf16 bit patterns), w_router / bias fp64 copies (any float array)."""
+    lib = _load()
+    xd = _bf16_to_f64(x)
+    T = xd.shape[0]
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    wr = np.ascontiguousarray(np.asarray(w_router, dtype=np.float64))
+    b = None if bias is None else np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
+    out = np.empty((T, cfg.hidden), np.float64)
+    c = _cfg(cfg, act_quant)
+    lib.orc_forward_fixed_ids_d(ctypes.byref(c), ctypes.byref(weights.struct), _ptr(wr), _ptr(b), _ptr(xd), T,
+                                _ptr(ids), _ptr(out))
+    return out
+
+
+def backward(cfg, weights: Weights, x, ids, w, dout, w_router, bias=None, act_quant=True) -> dict:
+    """Gradients of sum(dout * out) for the layer with the expert choice `ids` and the
+    routing weights `w` the forward applied ([T, k]). Returns fp64 arrays: dx [T,H],
+    dw_gate, dw_up [E,I,H], dw_down [E,H,I], dws_gate, dws_up [Is,H], dws_down [H,Is]
+    (zero-size when there are no shared experts), dw_router [E,H], dbias [E]."""
+    lib = _load()
+    xd = _bf16_to_f64(x)
+    T, H = xd.shape
+    E, I, k = cfg.n_routed, cfg.moe_inter, cfg.top_k
+    Is = cfg.n_shared * I
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    w = np.ascontiguousarray(np.asarray(w, dtype=np.float64))
+    do = np.ascontiguousarray(np.asarray(dout, dtype=np.float64))
+    wr = np.ascontiguousarray(np.asarray(w_router, dtype=np.float64))
+    b = None if bias is None else np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
+    g = {"dx": np.empty((T, H)), "dw_gate": np.empty((E, I, H)), "dw_up": np.empty((E, I, H)),
+         "dw_down": np.empty((E, H, I)), "dws_gate": np.zeros((Is, H)), "dws_up": np.zeros((Is, H)),
+         "dws_down": np.zeros((H, Is)), "dw_router": np.empty((E, H)), "dbias": np.empty(E)}
+    c = _cfg(cfg, act_quant)
+    lib.orc_backward_d(ctypes.byref(c), ctypes.byref(weights.struct), _ptr(wr), _ptr(b), _ptr(xd), T, _ptr(ids),
+                       _ptr(w), _ptr(do), _ptr(g["dx"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]), _ptr(g["dw_down"]),
+                       _ptr(g["dws_gate"]), _ptr(g["dws_up"]), _ptr(g["dws_down"]), _ptr(g["dw_router"]),
+                       _ptr(g["dbias"]))
+    return g

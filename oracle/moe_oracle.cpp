@@ -1,4 +1,4 @@
-// MoE-layer forward oracle: plain, slow, fp64 CPU code.
+// MoE-layer oracle (forward and backward): plain, slow, fp64 CPU code.
 //
 // TEST INFRASTRUCTURE. Only the test suite, the smoke check and the benchmark's
 // CPU-baseline leg load this library. The product path (the CUDA library under
@@ -531,6 +531,256 @@ void orc_forward_tokens_mx(const orc_cfg_t* c, const orc_weights_mx_t* W, const 
                           W->ws_down, W->ss_down, 1.0, o, 1);
         if (residual_bf16)
             for (int h = 0; h < H; ++h) o[h] += bf16_to_double(residual_bf16[(size_t)t * H + h]);
+    }
+}
+
+// ---------------------------------------------------------------- backward
+// The layer's backward for an output gradient dout[T][H]: the training workload of the
+// Mixture-of-Kittens page (Table 1, "Backward" columns; "expert FFNs" forward and
+// backward), for one layer on one device. The forward's expert choice (ids) is held
+// fixed: selection is piecewise constant in the inputs, so gradients reach the router
+// only through the routing weights of the kept experts, w = s * p_e.
+// Reading taken here (the pages give no formulas): the FP8 quantisers are
+// straight-through (the derivative of x -> xhat and of a -> ahat is taken as 1), the
+// weights are their dequantised FP8 values, and the forward values g, u, a, ahat are
+// those the forward computes (FP8 activations when act_quant is on). Per routed pair
+// (t, j) with expert e:
+//   z   = Wd_e . ahat                    (expert output before weighting)
+//   dw  = <dout_t, z>
+//   da  = w * Wd_e^T dout_t
+//   dg  = da * u * sig(g) * (1 + g * (1 - sig(g)))      (d/dg of g * sig(g), times u)
+//   du  = da * g * sig(g)
+//   dx_t  += Wg_e^T dg + Wu_e^T du
+//   dWd_e += (w * dout_t) (x) ahat,  dWg_e += dg (x) xhat_t,  dWu_e += du (x) xhat_t
+// The shared experts: the same with w = 1 and no routing term. The router
+// (logits = Wr . x + bias on the unquantised input x):
+//   dp_e = s * dw for the kept experts of the token, 0 for the others
+//   dlogit = p * (dp - <p, dp>)                       (softmax over all E)
+//   dx_t += Wr^T dlogit,  dWr += dlogit (x) x_t,  dbias += dlogit
+// Inputs and outputs are fp64 here so that finite differences can probe the function;
+// x is the layer input (bf16 values widened), w_router / bias fp64 copies.
+// The forward used by those finite differences (fixed ids, w recomputed from x):
+//   out_t = sum_j s * p_{e_j}(x_t) * z_{e_j}(xhat_t) + shared(xhat_t)
+void orc_forward_fixed_ids_d(const orc_cfg_t* c, const orc_weights_t* W, const double* w_router,
+                             const double* bias, const double* x, int T, const int32_t* ids, double* out) {
+    const int H = c->hidden, I = c->moe_inter, E = c->n_routed, k = c->top_k, Hb = H / 128, Ib = I / 128;
+    const int Is = c->n_shared * I;
+    double tab[256];
+    make_dec_tab(tab);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; ++t) {
+        const double* xt = x + (size_t)t * H;
+        std::vector<double> xhat(H), l(E);
+        if (c->act_quant) {
+            std::vector<uint8_t> q(H);
+            std::vector<double> sc(H / 128);
+            quant_dequant(xt, H, xhat.data(), q.data(), sc.data());
+        } else {
+            for (int h = 0; h < H; ++h) xhat[h] = xt[h];
+        }
+        double mx = -std::numeric_limits<double>::infinity();
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h) acc += xt[h] * w_router[(size_t)e * H + h];
+            l[e] = acc + (bias ? bias[e] : 0.0);
+            mx = std::max(mx, l[e]);
+        }
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += std::exp(l[e] - mx);
+        double* o = out + (size_t)t * H;
+        for (int h = 0; h < H; ++h) o[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const size_t e = (size_t)ids[(size_t)t * k + j];
+            const double w = c->routed_scaling_factor * std::exp(l[e] - mx) / z;
+            expert_mlp(tab, H, I, c->act_quant, xhat.data(), W->w_gate + e * I * H, W->s_gate + e * Ib * Hb,
+                       W->w_up + e * I * H, W->s_up + e * Ib * Hb, W->w_down + e * H * I,
+                       W->s_down + e * Hb * Ib, w, o, 1, nullptr);
+        }
+        if (c->n_shared > 0)
+            expert_mlp(tab, H, Is, c->act_quant, xhat.data(), W->ws_gate, W->ss_gate, W->ws_up, W->ss_up,
+                       W->ws_down, W->ss_down, 1.0, o, 1, nullptr);
+    }
+}
+
+// One expert MLP's backward for one token. Adds to dx[H] and, through the callback
+// arrays, hands back the per-row vectors the weight gradients need:
+//   ahat[N], dg[N], du[N]; returns dw = <dout, Wd . ahat>.
+static double expert_mlp_bwd(const double* dec_tab, int H, int N, int act_quant, const double* xhat,
+                             const uint8_t* wg, const float* sg, const uint8_t* wu, const float* su,
+                             const uint8_t* wd, const float* sd, double w, const double* dout, double* dx,
+                             double* ahat_out, double* dg_out, double* du_out) {
+    const int Hb = H / 128, Nb = N / 128;
+    std::vector<double> g(N), u(N), a(N), ahat(N);
+    for (int o = 0; o < N; ++o) {
+        double gg = 0.0, uu = 0.0;
+        for (int i = 0; i < H; ++i) {
+            gg += dec_tab[wg[(size_t)o * H + i]] * (double)sg[(size_t)(o / 128) * Hb + i / 128] * xhat[i];
+            uu += dec_tab[wu[(size_t)o * H + i]] * (double)su[(size_t)(o / 128) * Hb + i / 128] * xhat[i];
+        }
+        g[o] = gg;
+        u[o] = uu;
+        a[o] = gg / (1.0 + std::exp(-gg)) * uu;
+    }
+    if (act_quant) {
+        std::vector<uint8_t> q(N);
+        std::vector<double> s(Nb);
+        quant_dequant(a.data(), N, ahat.data(), q.data(), s.data());
+    } else {
+        ahat = a;
+    }
+    // z = Wd . ahat and da = w * Wd^T dout, one pass over Wd
+    double dw = 0.0;
+    std::vector<double> da(N, 0.0);
+    for (int o = 0; o < H; ++o) {
+        double zo = 0.0;
+        for (int i = 0; i < N; ++i) {
+            const double wv = dec_tab[wd[(size_t)o * N + i]] * (double)sd[(size_t)(o / 128) * Nb + i / 128];
+            zo += wv * ahat[i];
+            da[i] += w * wv * dout[o];
+        }
+        dw += dout[o] * zo;
+    }
+    std::vector<double> dg(N), du(N);
+    for (int o = 0; o < N; ++o) {
+        const double sg_ = 1.0 / (1.0 + std::exp(-g[o]));
+        dg[o] = da[o] * u[o] * sg_ * (1.0 + g[o] * (1.0 - sg_));
+        du[o] = da[o] * g[o] * sg_;
+    }
+    for (int o = 0; o < N; ++o)
+        for (int i = 0; i < H; ++i) {
+            const double wgv = dec_tab[wg[(size_t)o * H + i]] * (double)sg[(size_t)(o / 128) * Hb + i / 128];
+            const double wuv = dec_tab[wu[(size_t)o * H + i]] * (double)su[(size_t)(o / 128) * Hb + i / 128];
+            dx[i] += wgv * dg[o] + wuv * du[o];
+        }
+    for (int o = 0; o < N; ++o) {
+        ahat_out[o] = ahat[o];
+        dg_out[o] = dg[o];
+        du_out[o] = du[o];
+    }
+    return dw;
+}
+
+// Gradients of L = sum_t <dout_t, out_t>: dx [T,H]; dwg, dwu [E,I,H]; dwd [E,H,I];
+// dwsg, dwsu [Is,H], dwsd [H,Is] (ignored when S = 0); dwr [E,H]; dbias [E].
+// w [T,k] are the routing weights the forward applied (s * p of the kept experts).
+void orc_backward_d(const orc_cfg_t* c, const orc_weights_t* W, const double* w_router, const double* bias,
+                    const double* x, int T, const int32_t* ids, const double* w, const double* dout, double* dx,
+                    double* dwg, double* dwu, double* dwd, double* dwsg, double* dwsu, double* dwsd, double* dwr,
+                    double* dbias) {
+    const int H = c->hidden, I = c->moe_inter, E = c->n_routed, k = c->top_k, Hb = H / 128, Ib = I / 128;
+    const int Is = c->n_shared * I;
+    const double s = c->routed_scaling_factor;
+    double tab[256];
+    make_dec_tab(tab);
+    // per pair (t, j): ahat, dg, du; per token: xhat and the router gradient dlogit
+    std::vector<double> p_ahat((size_t)T * k * I), p_dg((size_t)T * k * I), p_du((size_t)T * k * I);
+    std::vector<double> xhat_all((size_t)T * H), dlogit((size_t)T * E);
+    std::vector<double> s_ahat((size_t)T * Is), s_dg((size_t)T * Is), s_du((size_t)T * Is);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; ++t) {
+        const double* xt = x + (size_t)t * H;
+        double* xhat = xhat_all.data() + (size_t)t * H;
+        if (c->act_quant) {
+            std::vector<uint8_t> q(H);
+            std::vector<double> sc(H / 128);
+            quant_dequant(xt, H, xhat, q.data(), sc.data());
+        } else {
+            for (int h = 0; h < H; ++h) xhat[h] = xt[h];
+        }
+        const double* dt = dout + (size_t)t * H;
+        double* dxt = dx + (size_t)t * H;
+        for (int h = 0; h < H; ++h) dxt[h] = 0.0;
+        std::vector<double> dp(E, 0.0);
+        for (int j = 0; j < k; ++j) {
+            const size_t f = (size_t)t * k + j, e = (size_t)ids[f];
+            const double dwj = expert_mlp_bwd(
+                tab, H, I, c->act_quant, xhat, W->w_gate + e * I * H, W->s_gate + e * Ib * Hb, W->w_up + e * I * H,
+                W->s_up + e * Ib * Hb, W->w_down + e * H * I, W->s_down + e * Hb * Ib, w[f], dt, dxt,
+                p_ahat.data() + f * I, p_dg.data() + f * I, p_du.data() + f * I);
+            dp[e] += s * dwj;
+        }
+        if (c->n_shared > 0)
+            expert_mlp_bwd(tab, H, Is, c->act_quant, xhat, W->ws_gate, W->ss_gate, W->ws_up, W->ss_up, W->ws_down,
+                           W->ss_down, 1.0, dt, dxt, s_ahat.data() + (size_t)t * Is, s_dg.data() + (size_t)t * Is,
+                           s_du.data() + (size_t)t * Is);
+        // router: softmax over all E of logits = Wr . x + bias
+        std::vector<double> l(E), p(E);
+        double mx = -std::numeric_limits<double>::infinity();
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h) acc += xt[h] * w_router[(size_t)e * H + h];
+            l[e] = acc + (bias ? bias[e] : 0.0);
+            mx = std::max(mx, l[e]);
+        }
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += (p[e] = std::exp(l[e] - mx));
+        double pdp = 0.0;
+        for (int e = 0; e < E; ++e) {
+            p[e] /= z;
+            pdp += p[e] * dp[e];
+        }
+        for (int e = 0; e < E; ++e) {
+            const double dl = p[e] * (dp[e] - pdp);
+            dlogit[(size_t)t * E + e] = dl;
+            for (int h = 0; h < H; ++h) dxt[h] += w_router[(size_t)e * H + h] * dl;
+        }
+    }
+    // weight gradients: sums over the token pairs of each expert, in token order
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int e = 0; e < E; ++e) {
+        double* gW = dwg + (size_t)e * I * H;
+        double* uW = dwu + (size_t)e * I * H;
+        double* dW = dwd + (size_t)e * H * I;
+        std::fill(gW, gW + (size_t)I * H, 0.0);
+        std::fill(uW, uW + (size_t)I * H, 0.0);
+        std::fill(dW, dW + (size_t)H * I, 0.0);
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j) {
+                const size_t f = (size_t)t * k + j;
+                if (ids[f] != e) continue;
+                const double* xh = xhat_all.data() + (size_t)t * H;
+                const double* dt = dout + (size_t)t * H;
+                const double* ah = p_ahat.data() + f * I;
+                const double* dg = p_dg.data() + f * I;
+                const double* du = p_du.data() + f * I;
+                for (int o = 0; o < I; ++o)
+                    for (int i = 0; i < H; ++i) {
+                        gW[(size_t)o * H + i] += dg[o] * xh[i];
+                        uW[(size_t)o * H + i] += du[o] * xh[i];
+                    }
+                for (int o = 0; o < H; ++o)
+                    for (int i = 0; i < I; ++i) dW[(size_t)o * I + i] += w[f] * dt[o] * ah[i];
+            }
+        double* rW = dwr + (size_t)e * H;
+        std::fill(rW, rW + H, 0.0);
+        double db = 0.0;
+        for (int t = 0; t < T; ++t) {
+            const double dl = dlogit[(size_t)t * E + e];
+            db += dl;
+            for (int h = 0; h < H; ++h) rW[h] += dl * x[(size_t)t * H + h];
+        }
+        if (dbias) dbias[e] = db;
+    }
+    if (c->n_shared > 0) {
+#pragma omp parallel for schedule(static)
+        for (int o = 0; o < Is; ++o) {
+            for (int i = 0; i < H; ++i) {
+                double ag = 0.0, au = 0.0;
+                for (int t = 0; t < T; ++t) {
+                    ag += s_dg[(size_t)t * Is + o] * xhat_all[(size_t)t * H + i];
+                    au += s_du[(size_t)t * Is + o] * xhat_all[(size_t)t * H + i];
+                }
+                dwsg[(size_t)o * H + i] = ag;
+                dwsu[(size_t)o * H + i] = au;
+            }
+        }
+#pragma omp parallel for schedule(static)
+        for (int o = 0; o < H; ++o)
+            for (int i = 0; i < Is; ++i) {
+                double acc = 0.0;
+                for (int t = 0; t < T; ++t) acc += dout[(size_t)t * H + o] * s_ahat[(size_t)t * Is + i];
+                dwsd[(size_t)o * Is + i] = acc;
+            }
     }
 }
 
