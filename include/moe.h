@@ -266,6 +266,30 @@ moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16
                                      int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream,
                                      const moe_stage_events_t* events);
 
+/* ---------------------------------------------------------------- backward
+ * The layer's backward (the Mixture-of-Kittens page's training workload, Table 1
+ * "Backward"): the gradients of L = sum(dout * out) for the layer of moe_forward
+ * (no residual, no stage M) with its expert choice held fixed. topk_ids / topk_w [T, k]
+ * are the forward's routing as moe_route returns it; dout_bf16 [T, H] is dL/d(out).
+ * Reading: the FP8 activation quantisers are straight-through, the weights enter at
+ * their dequantised FP8 values, and the router receives gradient through the kept
+ * experts' weights w = routed_scaling_factor * softmax(W_router x + bias)_e.
+ * Outputs: fp32 device arrays, overwritten:
+ *   dx [T, H]; dw_gate, dw_up [E, I, H]; dw_down [E, H, I];
+ *   dws_gate, dws_up [Is, H], dws_down [H, Is] (required when n_shared > 0, else ignored);
+ *   dw_router [E, H]; dbias [E] (NULL: not computed).
+ * Arithmetic: g and u are recomputed by the forward's FP8 grouped GEMM; the backward's
+ * contractions run in bf16 x bf16 -> fp32 (weights decoded from E4M3 x block scale to
+ * bf16). Needs hidden % 256 == 0 and n_routed % 16 == 0 (MOE_ERR_UNSUPPORTED_SHAPE
+ * otherwise, and moe_backward_workspace_size returns 0). T = 0 zeroes the weight gradients.
+ * Errors as for moe_forward; the workspace's status word is read by
+ * moe_read_device_status. */
+size_t moe_backward_workspace_size(const moe_config_t* cfg, int32_t max_tokens);
+moe_status_t moe_backward(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_t* weights,
+                          const int32_t* topk_ids, const float* topk_w, const void* dout_bf16, float* dx,
+                          float* dw_gate, float* dw_up, float* dw_down, float* dws_gate, float* dws_up,
+                          float* dws_down, float* dw_router, float* dbias, void* ws, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

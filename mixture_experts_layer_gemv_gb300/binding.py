@@ -59,6 +59,9 @@ _SIGNATURES = {
     "moe_workspace_size": (_SZ, [_P, _I32]),
     "moe_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_read_device_status": (ctypes.c_int, [_P, _P]),
+    "moe_backward_workspace_size": (_SZ, [_P, _I32]),
+    "moe_backward": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                    _P]),
     "moe_quant_act": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "moe_rmsnorm": (ctypes.c_int, [_P, _I32, _I32, _P, ctypes.c_float, _P, _P]),
     "moe_route_rmsnorm": (ctypes.c_int, [_P, _P, _I32, _P, ctypes.c_float, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -316,3 +319,52 @@ def forward(cfg: MoEConfig, x: torch.Tensor, weights, residual=None, ws=None, re
     ids = torch.empty((T, cfg.top_k), dtype=torch.int32, device=x.device) if return_ids else None
     moe_forward(cfg, x, weights, out, residual, ids, ws)
     return (out, ids) if return_ids else out
+
+
+def moe_backward_workspace_size(cfg: MoEConfig, max_tokens: int) -> int:
+    c = config_struct(cfg)
+    return lib().moe_backward_workspace_size(ctypes.byref(c), max_tokens)
+
+
+def alloc_workspace_backward(cfg: MoEConfig, max_tokens: int, device="cuda") -> torch.Tensor:
+    n = moe_backward_workspace_size(cfg, max_tokens)
+    if n == 0:
+        raise MoeError("moe_backward_workspace_size", -2, "config not supported by the backward")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws)
+    return ws
+
+
+def moe_backward(cfg, x, weights, topk_ids, topk_w, dout, grads: Dict[str, torch.Tensor], ws, stream=None) -> None:
+    """Fill grads (fp32 tensors: dx, dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down,
+    dw_router, dbias) with the layer's gradients for output gradient dout."""
+    c = config_struct(cfg)
+    W = weights_struct(weights)
+    g = grads
+    _check("moe_backward", lib().moe_backward(
+        ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W), _ptr(topk_ids), _ptr(topk_w), _ptr(dout),
+        _ptr(g["dx"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]), _ptr(g["dw_down"]), _ptr(g.get("dws_gate")),
+        _ptr(g.get("dws_up")), _ptr(g.get("dws_down")), _ptr(g["dw_router"]), _ptr(g.get("dbias")), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def alloc_grads(cfg: MoEConfig, T: int, device="cuda", bias=True) -> Dict[str, torch.Tensor]:
+    H, I, E, Is = cfg.hidden, cfg.moe_inter, cfg.n_routed, cfg.shared_inter
+    f = dict(dtype=torch.float32, device=device)
+    g = {"dx": torch.empty((T, H), **f), "dw_gate": torch.empty((E, I, H), **f), "dw_up": torch.empty((E, I, H), **f),
+         "dw_down": torch.empty((E, H, I), **f), "dw_router": torch.empty((E, H), **f)}
+    if Is > 0:
+        g.update(dws_gate=torch.empty((Is, H), **f), dws_up=torch.empty((Is, H), **f),
+                 dws_down=torch.empty((H, Is), **f))
+    if bias:
+        g["dbias"] = torch.empty((E,), **f)
+    return g
+
+
+def backward(cfg: MoEConfig, x: torch.Tensor, weights, topk_ids, topk_w, dout, ws=None) -> Dict[str, torch.Tensor]:
+    """Convenience: allocate the gradients (and ws if not given) and run moe_backward."""
+    T = x.shape[0]
+    ws = alloc_workspace_backward(cfg, T, x.device) if ws is None else ws
+    g = alloc_grads(cfg, T, x.device)
+    moe_backward(cfg, x, weights, topk_ids, topk_w, dout, g, ws)
+    return g

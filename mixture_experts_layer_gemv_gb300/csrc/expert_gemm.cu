@@ -60,12 +60,12 @@ __device__ __forceinline__ void issue_loads(uint8_t* stage, uint64_t* bar, const
     tma_load_2d(stage + kSA + kSB / 2, c.shared ? m.b1_s : m.b1_r, x, c.yb1, bar);
 }
 
-template <int kMode>  // 0: gate/up, 1: down
+template <int kMode>  // 0: gate/up, 1: down, 2: gate/up with g and u written as they are (fp32)
 __global__ void __launch_bounds__(kGThreads, 1)
     expert_gemm_kernel(const GemmArgs a, const __grid_constant__ TmaMap tm_a_r, const __grid_constant__ TmaMap tm_a_s,
                        const __grid_constant__ TmaMap tm_b0_r, const __grid_constant__ TmaMap tm_b1_r,
                        const __grid_constant__ TmaMap tm_b0_s, const __grid_constant__ TmaMap tm_b1_s) {
-    constexpr bool gateup = kMode == 0;
+    constexpr bool gateup = kMode != 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGStages * kStageBytes);
@@ -235,7 +235,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
             // after a timeout every warp still takes the named barriers below, but writes nothing
             const bool valid = ok && valid_row;
             const Item it = decode_item(a, n_mt_r, item);
-            if (gateup) {
+            if (kMode == 2) {
+                // the backward's recompute: g and u of 64 intermediate channels each
+                if (valid) {
+                    const int N = it.shared ? a.Is : a.I;
+                    const size_t o = (size_t)grow * N + it.ntile * kBlk + 64 * wg;
+                    float4* dg = reinterpret_cast<float4*>((it.shared ? a.g_out_s : a.g_out_r) + o);
+                    float4* du = reinterpret_cast<float4*>((it.shared ? a.u_out_s : a.u_out_r) + o);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        dg[c] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+                        du[c] = make_float4(acc[64 + 4 * c], acc[64 + 4 * c + 1], acc[64 + 4 * c + 2],
+                                            acc[64 + 4 * c + 3]);
+                    }
+                }
+            } else if (gateup) {
                 // a = SiLU(g) * u for 64 intermediate channels; the 128-channel scale block
                 // spans both column halves: combine their maxima through shared memory
                 float amax = 0.f;
@@ -310,10 +324,10 @@ bool gemm_supported(const moe_config_t& c) {
 }
 
 cudaError_t launch_expert_gemm(const GemmArgs& g, const TmaMaps& m, cudaStream_t st) {
-    static size_t smem_set[2] = {0, 0};
+    static size_t smem_set[3] = {0, 0, 0};
     const size_t smem = gemm_smem();
-    const int mode = g.mode == 0 ? 0 : 1;
-    auto kern = mode == 0 ? expert_gemm_kernel<0> : expert_gemm_kernel<1>;
+    const int mode = g.mode == 0 ? 0 : g.mode == 1 ? 1 : 2;
+    auto kern = mode == 0 ? expert_gemm_kernel<0> : mode == 1 ? expert_gemm_kernel<1> : expert_gemm_kernel<2>;
     if (smem_set[mode] < smem) {
         const cudaError_t e =
             cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -467,6 +467,70 @@ moe_status_t moe_read_device_status(void* ws, void* stream) {
     return MOE_ERR_INVALID_ARG;
 }
 
+size_t moe_backward_workspace_size(const moe_config_t* cfg, int32_t max_tokens) {
+    if (check_cfg(cfg) != MOE_OK || max_tokens < 0 || check_T(cfg, max_tokens) != MOE_OK || !gemm_supported(*cfg) ||
+        cfg->n_routed % 16)
+        return 0;
+    return bwd_layout(*cfg, max_tokens).total;
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_t* weights,
+                          const int32_t* topk_ids, const float* topk_w, const void* dout_bf16, float* dx,
+                          float* dw_gate, float* dw_up, float* dw_down, float* dws_gate, float* dws_up,
+                          float* dws_down, float* dw_router, float* dbias, void* ws, size_t ws_bytes, void* stream) {
+    MOE_TRY(check_cfg(cfg));
+    MOE_TRY(check_T(cfg, T));
+    if (!gemm_supported(*cfg) || cfg->n_routed % 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+    MOE_TRY(check_weights(cfg, weights, true));
+    const void* req[] = {dw_gate, dw_up, dw_down, dw_router};  // the per-token arrays only when T > 0
+    for (const void* p : req)
+        if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    const void* treq[] = {x_bf16, topk_ids, topk_w, dout_bf16, dx};
+    for (const void* p : treq)
+        if (T > 0 && (!p || !aligned16(p))) return MOE_ERR_INVALID_ARG;
+    const bool sh = cfg->n_shared > 0;
+    if (sh) {
+        const void* sreq[] = {dws_gate, dws_up, dws_down};
+        for (const void* p : sreq)
+            if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    }
+    if (dbias && !aligned4(dbias)) return MOE_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws) || ws_bytes < bwd_layout(*cfg, T).total) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t H = cfg->hidden, I = cfg->moe_inter, E = cfg->n_routed, Is = (size_t)cfg->n_shared * I;
+    if (T == 0) {  // sums over no tokens
+        MOE_CUDA(cudaMemsetAsync(dw_gate, 0, E * I * H * 4, st));
+        MOE_CUDA(cudaMemsetAsync(dw_up, 0, E * I * H * 4, st));
+        MOE_CUDA(cudaMemsetAsync(dw_down, 0, E * H * I * 4, st));
+        MOE_CUDA(cudaMemsetAsync(dw_router, 0, E * H * 4, st));
+        if (dbias) MOE_CUDA(cudaMemsetAsync(dbias, 0, E * 4, st));
+        if (sh) {
+            MOE_CUDA(cudaMemsetAsync(dws_gate, 0, Is * H * 4, st));
+            MOE_CUDA(cudaMemsetAsync(dws_up, 0, Is * H * 4, st));
+            MOE_CUDA(cudaMemsetAsync(dws_down, 0, H * Is * 4, st));
+        }
+        return MOE_OK;
+    }
+    BwdArgs a;
+    a.T = T;
+    a.x = x_bf16;
+    a.W = weights;
+    a.topk_ids = topk_ids;
+    a.topk_w = topk_w;
+    a.dout = dout_bf16;
+    a.dx = dx;
+    a.dw_gate = dw_gate;
+    a.dw_up = dw_up;
+    a.dw_down = dw_down;
+    a.dws_gate = sh ? dws_gate : nullptr;
+    a.dws_up = sh ? dws_up : nullptr;
+    a.dws_down = sh ? dws_down : nullptr;
+    a.dw_router = dw_router;
+    a.dbias = dbias;
+    MOE_CUDA(launch_backward(*cfg, a, ws, st));
+    return MOE_OK;
+}
+
 moe_status_t moe_quant_act(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq, float* xs, void* stream) {
     if (T < 0 || H <= 0 || H % 128) return T < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;

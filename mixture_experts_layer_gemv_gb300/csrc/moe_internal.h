@@ -46,7 +46,8 @@ struct MTile {
 };
 
 // The grouped FP8 GEMM (tcgen05) of the large-T path; mode 0: gate/up -> SiLU(g)*u
-// quantised to FP8, mode 1: down -> routing-weighted bf16 rows.
+// quantised to FP8, mode 1: down -> routing-weighted bf16 rows, mode 2: gate/up -> g and
+// u in fp32 (the backward's recompute of the forward's pre-activations).
 
 // Byte offsets of every workspace region for a given (config, T).
 struct WsLayout {
@@ -201,6 +202,7 @@ struct GemmArgs {
     const uint8_t *sfa_r, *sfa_s, *sfb0_r, *sfb1_r, *sfb0_s, *sfb1_s;
     __nv_bfloat16* y_perm;
     __nv_bfloat16* y_shared;
+    float *g_out_r, *u_out_r, *g_out_s, *u_out_s;  // mode 2: g and u [rows, width] fp32
     int* status;
 };
 struct TmaMaps {
@@ -223,6 +225,28 @@ cudaError_t launch_quant_act_mx(const void* x, int T, int H, uint8_t* xq, uint8_
 cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, const uint8_t* xq, uint8_t* xq_perm,
                                int* status, cudaStream_t st, const uint8_t* xs8 = nullptr,
                                uint8_t* xs8_perm = nullptr);
+
+// ------------------------------------------------------------------ backward
+// Workspace regions of the layer backward (byte offsets), for T tokens.
+struct BwdLayout {
+    size_t ctrl, logits, ids, w, xq, xs, offsets, perm_src, inv_pos, perm_hist, mtiles, xq_perm;
+    size_t g_r, u_r, dau_r, ahat_r, dgu_r, dx_perm;  // routed rows: fp32 [R, I] x3, bf16 [R, I], [R, 2I], fp32 [R, H]
+    size_t g_s, u_s, dau_s, ahat_s, dgu_s, dx_s;     // shared experts' tokens, the same with Is
+    size_t dw, dlogit;                               // fp32 [T k], [T, E]
+    size_t total;
+    int splits, max_mtiles;
+};
+BwdLayout bwd_layout(const moe_config_t& c, int64_t T);
+struct BwdArgs {
+    int T;
+    const void* x;                 // bf16 [T, H]
+    const moe_weights_t* W;
+    const int32_t* topk_ids;       // [T, k] the forward's expert choice
+    const float* topk_w;           // [T, k] the forward's routing weights
+    const void* dout;              // bf16 [T, H]
+    float *dx, *dw_gate, *dw_up, *dw_down, *dws_gate, *dws_up, *dws_down, *dw_router, *dbias;
+};
+cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, cudaStream_t st);
 
 int stream_grid();
 int down_stages(int I, int Is);

@@ -362,11 +362,12 @@ def forward_fixed_ids(cfg, weights: Weights, x, ids, w_router, bias=None, act_qu
     return out
 
 
-def backward(cfg, weights: Weights, x, ids, w, dout, w_router, bias=None, act_quant=True) -> dict:
+def backward(cfg, weights: Weights, x, ids, w, dout, w_router, bias=None, act_quant=True, dx_only=False) -> dict:
     """Gradients of sum(dout * out) for the layer with the expert choice `ids` and the
     routing weights `w` the forward applied ([T, k]). Returns fp64 arrays: dx [T,H],
     dw_gate, dw_up [E,I,H], dw_down [E,H,I], dws_gate, dws_up [Is,H], dws_down [H,Is]
-    (zero-size when there are no shared experts), dw_router [E,H], dbias [E]."""
+    (zero-size when there are no shared experts), dw_router [E,H], dbias [E].
+    dx_only: only dx (None for the rest), for a sample of tokens at large sizes."""
     lib = _load()
     xd = _bf16_to_f64(x)
     T, H = xd.shape
@@ -377,9 +378,13 @@ def backward(cfg, weights: Weights, x, ids, w, dout, w_router, bias=None, act_qu
     do = np.ascontiguousarray(np.asarray(dout, dtype=np.float64))
     wr = np.ascontiguousarray(np.asarray(w_router, dtype=np.float64))
     b = None if bias is None else np.ascontiguousarray(np.asarray(bias, dtype=np.float64))
-    g = {"dx": np.empty((T, H)), "dw_gate": np.empty((E, I, H)), "dw_up": np.empty((E, I, H)),
-         "dw_down": np.empty((E, H, I)), "dws_gate": np.zeros((Is, H)), "dws_up": np.zeros((Is, H)),
-         "dws_down": np.zeros((H, Is)), "dw_router": np.empty((E, H)), "dbias": np.empty(E)}
+    if dx_only:  # the listed tokens' dx only (exact for any subset of tokens)
+        g = {"dx": np.empty((T, H)), "dw_gate": None, "dw_up": None, "dw_down": None, "dws_gate": None,
+             "dws_up": None, "dws_down": None, "dw_router": None, "dbias": None}
+    else:
+        g = {"dx": np.empty((T, H)), "dw_gate": np.empty((E, I, H)), "dw_up": np.empty((E, I, H)),
+             "dw_down": np.empty((E, H, I)), "dws_gate": np.zeros((Is, H)), "dws_up": np.zeros((Is, H)),
+             "dws_down": np.zeros((H, Is)), "dw_router": np.empty((E, H)), "dbias": np.empty(E)}
     c = _cfg(cfg, act_quant)
     lib.orc_backward_d(ctypes.byref(c), ctypes.byref(weights.struct), _ptr(wr), _ptr(b), _ptr(xd), T, _ptr(ids),
                        _ptr(w), _ptr(do), _ptr(g["dx"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]), _ptr(g["dw_down"]),

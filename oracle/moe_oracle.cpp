@@ -661,7 +661,10 @@ static double expert_mlp_bwd(const double* dec_tab, int H, int N, int act_quant,
 }
 
 // Gradients of L = sum_t <dout_t, out_t>: dx [T,H]; dwg, dwu [E,I,H]; dwd [E,H,I];
-// dwsg, dwsu [Is,H], dwsd [H,Is] (ignored when S = 0); dwr [E,H]; dbias [E].
+// dwsg, dwsu [Is,H], dwsd [H,Is] (ignored when S = 0); dwr [E,H]; dbias [E]. The
+// weight-gradient outputs may be NULL (dwg: the routed ones; dwsg: the shared ones;
+// dwr: the router's): dx_t depends on token t alone, so dx of a sample of tokens is
+// exact when only their rows are passed.
 // w [T,k] are the routing weights the forward applied (s * p of the kept experts).
 void orc_backward_d(const orc_cfg_t* c, const orc_weights_t* W, const double* w_router, const double* bias,
                     const double* x, int T, const int32_t* ids, const double* w, const double* dout, double* dx,
@@ -726,8 +729,9 @@ void orc_backward_d(const orc_cfg_t* c, const orc_weights_t* W, const double* w_
         }
     }
     // weight gradients: sums over the token pairs of each expert, in token order
+    // (NULL outputs are skipped: dx alone is exact for any subset of tokens)
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int e = 0; e < E; ++e) {
+    for (int e = 0; e < (dwg ? E : 0); ++e) {
         double* gW = dwg + (size_t)e * I * H;
         double* uW = dwu + (size_t)e * I * H;
         double* dW = dwd + (size_t)e * H * I;
@@ -751,6 +755,9 @@ void orc_backward_d(const orc_cfg_t* c, const orc_weights_t* W, const double* w_
                 for (int o = 0; o < H; ++o)
                     for (int i = 0; i < I; ++i) dW[(size_t)o * I + i] += w[f] * dt[o] * ah[i];
             }
+    }
+#pragma omp parallel for schedule(static)
+    for (int e = 0; e < (dwr ? E : 0); ++e) {
         double* rW = dwr + (size_t)e * H;
         std::fill(rW, rW + H, 0.0);
         double db = 0.0;
@@ -761,7 +768,7 @@ void orc_backward_d(const orc_cfg_t* c, const orc_weights_t* W, const double* w_
         }
         if (dbias) dbias[e] = db;
     }
-    if (c->n_shared > 0) {
+    if (c->n_shared > 0 && dwsg) {
 #pragma omp parallel for schedule(static)
         for (int o = 0; o < Is; ++o) {
             for (int i = 0; i < H; ++i) {

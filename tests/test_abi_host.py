@@ -99,3 +99,18 @@ def test_workspace_covers_the_largest_workload(L):
     # at least the permuted FP8 intermediate [T*k, I] and the bf16 expert outputs [T*k, H]
     assert n >= wl.T * c.top_k * (c.moe_inter + 2 * c.hidden)
     assert n < 4 * 1024 ** 3  # fp32 partial sums of the weight-streaming path dominate
+
+
+def test_backward_workspace_and_argument_checks(L):
+    c = B.config_struct(MoEConfig(512, 256, 16, 4, 2, 4, 1.0, 1))
+    n = L.moe_backward_workspace_size(ctypes.byref(c), 64)
+    assert n > L.moe_backward_workspace_size(ctypes.byref(c), 8) > 0
+    # unsupported: hidden not a multiple of 256, n_routed not a multiple of 16
+    assert L.moe_backward_workspace_size(ctypes.byref(B.config_struct(MoEConfig(384, 256, 16, 4, 2, 4, 1.0, 1))), 8) == 0
+    assert L.moe_backward_workspace_size(ctypes.byref(B.config_struct(MoEConfig(512, 256, 8, 4, 2, 4, 1.0, 1))), 8) == 0
+    w = B.moe_weights_t()
+    # no weights / no gradient outputs: rejected before anything is launched
+    assert L.moe_backward(ctypes.byref(c), None, 8, None, None, None, None, None, None, None, None, None, None,
+                          None, None, None, None, 0, None) == -1
+    assert L.moe_backward(ctypes.byref(c), None, 8, ctypes.byref(w), None, None, None, None, None, None, None,
+                          None, None, None, None, None, None, 0, None) == -1
