@@ -378,6 +378,200 @@ def cpu_oracle_rate(wl, budget_s: float, weights=None, mx: bool = False):
     return us_per_token, cores, f"{done} tokens routed and run through the layer, {cores} tokens in parallel, {el:.1f} s"
 
 
+def _backward_launches(cfg) -> int:
+    """Kernels per moe_backward call: the forward recompute (activation quant, router GEMM,
+    top-k, permutation count + scatter, row gather, g/u GEMM), then dgrad of down, SwiGLU,
+    router and dbias backward, router dx, dgrad of gate/up, the dx sum and the three
+    weight-gradient GEMMs (down, gate/up, router); the shared experts add five."""
+    return 17 + (5 if cfg.n_shared > 0 else 0)
+
+
+def _backward_flops(cfg, T: int) -> dict:
+    H, I, E, k, Is = cfg.hidden, cfg.moe_inter, cfg.n_routed, cfg.top_k, cfg.shared_inter
+    R = T * k
+    dgrad_gu_routed = 2 * R * 2 * I * H
+    total = (2 * R * H * I + dgrad_gu_routed + 2 * R * H * I + 2 * R * 2 * I * H      # routed dgrad + wgrad
+             + 2 * T * (H * Is + 2 * Is * H) * 2                                       # shared dgrad + wgrad
+             + 2 * 2 * T * E * H)                                                      # router dx + dWr
+    return {"dgrad_gate_up_routed": dgrad_gu_routed, "backward_bf16": total}
+
+
+def cpu_oracle_backward_rate(wl, budget_s: float, weights, x, ids, w, dout):
+    """The oracle backward as it stands, dx of a bounded sample of tokens (the weight
+    gradients are sums over whole experts, whose fp64 arrays do not fit at this shape).
+    Returns (tokens/s, cores, sample description)."""
+    import oracle
+    oracle.build()
+    cfg = wl.cfg
+    Wo = oracle.Weights(weights)
+    wr = weights["w_router"].detach().cpu().double().numpy()
+    b = None if weights.get("router_bias") is None else weights["router_bias"].detach().cpu().double().numpy()
+    ids_h, w_h = ids.cpu().numpy(), w.cpu().double().numpy()
+    dout_h = dout.float().cpu().double().numpy()
+    n, done, t0 = 1, 0, time.perf_counter()
+    while True:
+        rows = np.arange(done, done + n) % wl.T
+        oracle.backward(cfg, Wo, x[rows], ids_h[rows], w_h[rows], dout_h[rows], wr, b, dx_only=True)
+        done += n
+        el = time.perf_counter() - t0
+        if el > budget_s or done >= wl.T:
+            break
+        n = max(1, min(2 * n, int(n * (budget_s - el) / max(el, 1e-3))))
+    return done / el, oracle.num_threads(), f"dx of {done} tokens of the workload (router, experts, shared)"
+
+
+def main_backward(args, dist, rank, world):
+    from mixture_experts_layer_gemv_gb300 import binding as B
+    from mixture_experts_layer_gemv_gb300 import build as lib_build
+
+    wl = WORKLOADS[args.workload]
+    cfg, T = wl.cfg, wl.T
+    metric = "MoE layer backward tokens/s (bf16 tensor-core fraction of the dominant kernel)"
+    config = {"workload": f"{wl.name}: {wl.description}; layer backward (dx, expert, shared and router weight "
+                          f"gradients) for a seeded dout", "T": T, "hidden": cfg.hidden, "moe_inter": cfg.moe_inter,
+              "n_routed": cfg.n_routed, "top_k": cfg.top_k, "n_shared": cfg.n_shared,
+              "parallelism": f"replicas x{world}",
+              "l2": "one layer's weights and the gradients (GBs) exceed L2 every step"}
+    if args.steps <= 0:
+        args.steps = 10
+    if args.impl == "reference":  # the oracle's backward on the host cores, rank 0 only
+        if rank != 0:
+            return
+        import oracle
+        Wc = make_weights(cfg, wl.seed, "cpu", zipf=wl.zipf_bias)
+        xc = make_tokens(cfg, T, replica_seed(wl.seed, 0, 0), "cpu", name="x_step0")
+        ids, w, _, _ = oracle.route(cfg, xc, Wc["w_router"], Wc["router_bias"])
+        g = torch.Generator(device="cpu").manual_seed(1234)
+        dout = torch.randn((T, cfg.hidden), generator=g).to(torch.bfloat16)
+        budget = max(5.0, min(60.0, args.cpu_budget))
+        rate, cores, sample = cpu_oracle_backward_rate(wl, budget, Wc, xc, torch.from_numpy(ids),
+                                                       torch.from_numpy(w), dout)
+        line = {"impl": "reference", "metric": metric, "value": round(rate, 3), "unit": "tokens/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(T / rate * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": round(rate, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+    if rank == 0 or not os.path.exists(lib_build.LIB):
+        lib_build.build()
+    _barrier(dist)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    W = make_weights(cfg, wl.seed, dev, zipf=wl.zipf_bias)
+    P = 4
+    xs = [make_tokens(cfg, T, replica_seed(wl.seed, rank, i), dev, name=f"x_step{i}") for i in range(P)]
+    g = torch.Generator(device="cpu").manual_seed(1234 + rank)
+    dout = torch.randn((T, cfg.hidden), generator=g).to(torch.bfloat16).to(dev)
+    wsf = B.alloc_workspace(cfg, T, dev)
+    routes = []
+    for x in xs:
+        ids = torch.empty((T, cfg.top_k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, cfg.top_k), dtype=torch.float32, device=dev)
+        B.moe_route(cfg, x, W["w_router"], W["router_bias"], ids, w, wsf)
+        routes.append((ids, w))
+    ws = B.alloc_workspace_backward(cfg, T, dev)
+    grads = B.alloc_grads(cfg, T, dev)
+    names = {"recompute": "route", "dgrad_down": "permute", "dgrad_gate_up_routed": "gate_up",
+             "dx_rest": "combine", "wgrad": "down"}
+    prof = []
+    for _ in range(args.steps):
+        evs = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in B.STAGES}
+        for a, b in evs.values():  # torch only times events it has recorded itself
+            a.record()
+            b.record()
+        prof.append(evs)
+    torch.cuda.synchronize()
+
+    def step(i, evs=None):
+        ids, w = routes[i % P]
+        B.moe_backward(cfg, xs[i % P], W, ids, w, dout, grads, ws, events=evs)
+
+    with ClockSampler(dev.index) as clk:
+        clk.wait_first_sample()
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        _barrier(dist)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(args.steps):
+            step(i, prof[i])
+        t1.record()
+        torch.cuda.synchronize()
+    _barrier(dist)
+    ms = _max_over_ranks(dist, t0.elapsed_time(t1) / args.steps)
+    stages = {k: round(statistics.mean(e[v][0].elapsed_time(e[v][1]) * 1e3 for e in prof), 1)
+              for k, v in names.items()}
+    status = B.moe_read_device_status(ws)
+
+    # end to end: pinned x, dout, routing in; dbias (the step's result) back
+    xh = [x.cpu().pin_memory() for x in xs]
+    rh = [(i_.cpu().pin_memory(), w_.cpu().pin_memory()) for i_, w_ in routes]
+    dh = dout.cpu().pin_memory()
+    xd, dd = torch.empty_like(xs[0]), torch.empty_like(dout)
+    idd, wdd = torch.empty_like(routes[0][0]), torch.empty_like(routes[0][1])
+    bh = torch.empty_like(grads["dbias"], device="cpu").pin_memory()
+
+    def e2e_step(i):
+        xd.copy_(xh[i % P], non_blocking=True)
+        dd.copy_(dh, non_blocking=True)
+        idd.copy_(rh[i % P][0], non_blocking=True)
+        wdd.copy_(rh[i % P][1], non_blocking=True)
+        B.moe_backward(cfg, xd, W, idd, wdd, dd, grads, ws)
+        bh.copy_(grads["dbias"], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / args.steps)
+    if rank != 0:
+        return
+    fl = _backward_flops(cfg, T)
+    peaks = _peaks()
+    bf16_peak = peaks["bf16_tflops"] if peaks else 1900.0
+    k_us = stages["dgrad_gate_up_routed"]
+    k_tf = fl["dgrad_gate_up_routed"] / (k_us * 1e-6) / 1e12
+    tok_s = world * T / (ms * 1e-3)
+    line = {
+        "metric": metric, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 x bf16 -> f32 (g, u recomputed e4m3 x e4m3 -> f32)",
+        "data": "synthetic", "config": config,
+        "roofline": {"bound": "tensor", "kernel": "bwd_gemm_kernel<1> (dgrad of gate/up, routed experts)",
+                     "achieved": round(k_tf, 1), "peak": round(bf16_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(k_tf / bf16_peak, 4), "traffic": None,
+                     "peak_source": "measured bf16 burst" if peaks else "fallback",
+                     "launch_us": k_us, "flops_per_launch": fl["dgrad_gate_up_routed"]},
+        "backward_tflops": round(fl["backward_bf16"] / (ms * 1e-3) / 1e12, 1),
+        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * cfg.hidden * 2 * 2 + T * cfg.top_k * 8,
+                "d2h_bytes_per_step": cfg.n_routed * 4},
+        "stages_us": stages, "gpu_launches": _backward_launches(cfg) * args.steps, "clocks": clk.summary(),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        rate, cores, sample = cpu_oracle_backward_rate(wl, args.cpu_budget, W, xs[0], routes[0][0], routes[0][1],
+                                                       dout)
+        line["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -389,11 +583,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mx", action="store_true", help="the MXFP8 variant (E8M0 scales per 32 K)")
+    ap.add_argument("--backward", action="store_true",
+                    help="the layer backward (moe_backward) instead of the forward; use with --workload prefill_t4096")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     dist, rank, world = _dist()
+    if args.backward:
+        return main_backward(args, dist, rank, world)
     wl = WORKLOADS[args.workload]
     cfg, T = wl.cfg, wl.T
     if args.steps <= 0:

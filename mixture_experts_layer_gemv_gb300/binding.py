@@ -62,6 +62,8 @@ _SIGNATURES = {
     "moe_backward_workspace_size": (_SZ, [_P, _I32]),
     "moe_backward": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                     _P]),
+    "moe_backward_profiled": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                             _P, _SZ, _P, _P]),
     "moe_quant_act": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "moe_rmsnorm": (ctypes.c_int, [_P, _I32, _I32, _P, ctypes.c_float, _P, _P]),
     "moe_route_rmsnorm": (ctypes.c_int, [_P, _P, _I32, _P, ctypes.c_float, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -335,17 +337,22 @@ def alloc_workspace_backward(cfg: MoEConfig, max_tokens: int, device="cuda") -> 
     return ws
 
 
-def moe_backward(cfg, x, weights, topk_ids, topk_w, dout, grads: Dict[str, torch.Tensor], ws, stream=None) -> None:
+def moe_backward(cfg, x, weights, topk_ids, topk_w, dout, grads: Dict[str, torch.Tensor], ws, stream=None,
+                 events: Optional[Dict[str, tuple]] = None) -> None:
     """Fill grads (fp32 tensors: dx, dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down,
-    dw_router, dbias) with the layer's gradients for output gradient dout."""
+    dw_router, dbias) with the layer's gradients for output gradient dout. events: as
+    for moe_forward, in the backward's slots (see moe.h, moe_backward_profiled)."""
     c = config_struct(cfg)
     W = weights_struct(weights)
     g = grads
-    _check("moe_backward", lib().moe_backward(
-        ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W), _ptr(topk_ids), _ptr(topk_w), _ptr(dout),
-        _ptr(g["dx"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]), _ptr(g["dw_down"]), _ptr(g.get("dws_gate")),
-        _ptr(g.get("dws_up")), _ptr(g.get("dws_down")), _ptr(g["dw_router"]), _ptr(g.get("dbias")), _ptr(ws),
-        ws.numel(), _stream(stream)))
+    args = [ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W), _ptr(topk_ids), _ptr(topk_w), _ptr(dout),
+            _ptr(g["dx"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]), _ptr(g["dw_down"]), _ptr(g.get("dws_gate")),
+            _ptr(g.get("dws_up")), _ptr(g.get("dws_down")), _ptr(g["dw_router"]), _ptr(g.get("dbias")), _ptr(ws),
+            ws.numel(), _stream(stream)]
+    if events:
+        _check("moe_backward_profiled", lib().moe_backward_profiled(*args, ctypes.byref(_events_struct(events))))
+    else:
+        _check("moe_backward", lib().moe_backward(*args))
 
 
 def alloc_grads(cfg: MoEConfig, T: int, device="cuda", bias=True) -> Dict[str, torch.Tensor]:

@@ -32,6 +32,7 @@ namespace {
 
 constexpr int kBM = 128, kBN = 128, kBK = 32;
 constexpr int kAPitch = kBK + 8;  // bf16 per A row in shared memory (k contiguous)
+constexpr int kATPitch = kBM + 8; // bf16 per A row of the transposed layout (m contiguous, one row per k)
 constexpr int kBPitch = kBN + 8;  // bf16 per B row in shared memory (n contiguous)
 constexpr int kGThr = 256;        // 8 warps: 2 along M (64 rows) x 4 along N (32 columns)
 
@@ -137,10 +138,12 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 }
 
 // One 128 x 128 output tile of one group. A tile element (m, kk) and B tile element
-// (kk, n) are read as 16 contiguous values per thread and staged as bf16: A as
-// [m][k] (A_s), B as [k][n] (B_s), two buffers each; fragments come from ldmatrix.
+// (kk, n) are read as 16 contiguous values per thread and staged as bf16: B as [k][n],
+// A as [m][k] when its rows run along k (dgrad) and as [k][m] when they run along m
+// (wgrad), two buffers each; fragments come from ldmatrix (.trans for the [k][*] ones).
 template <int F>
 __global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const BwdGemm p) {
+    static_assert(kBM * kAPitch >= kBK * kATPitch, "one A buffer holds either layout");
     __shared__ __align__(16) __nv_bfloat16 A_s[2][kBM * kAPitch];
     __shared__ __align__(16) __nv_bfloat16 B_s[2][kBK * kBPitch];
     constexpr bool a_cols = F >= F_WDOWN;  // A(m, kk) contiguous along m (its rows are the K index)
@@ -278,14 +281,10 @@ __global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const BwdGemm p) {
             uint4* d = reinterpret_cast<uint4*>(&A_s[buf][am * kAPitch + ak]);
             d[0] = ra0;
             d[1] = ra1;
-        } else {  // transpose: 16 m values of one k
-            const uint32_t w[8] = {ra0.x, ra0.y, ra0.z, ra0.w, ra1.x, ra1.y, ra1.z, ra1.w};
-            __nv_bfloat16* d = &A_s[buf][am * kAPitch + ak];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                d[(2 * i) * kAPitch] = __ushort_as_bfloat16((unsigned short)(w[i] & 0xFFFF));
-                d[(2 * i + 1) * kAPitch] = __ushort_as_bfloat16((unsigned short)(w[i] >> 16));
-            }
+        } else {  // row kk of the [k][m] layout: 16 consecutive m
+            uint4* d = reinterpret_cast<uint4*>(&A_s[buf][ak * kATPitch + am]);
+            d[0] = ra0;
+            d[1] = ra1;
         }
         uint4* d = reinterpret_cast<uint4*>(&B_s[buf][bk * kBPitch + bn]);
         d[0] = rb0;
@@ -311,8 +310,13 @@ __global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const BwdGemm p) {
         for (int ks = 0; ks < kBK; ks += 16) {
             uint32_t af[4][4], bf[2][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                ldsm_x4(af[i], &A_s[buf][(wm * 64 + i * 16 + (lane & 15)) * kAPitch + ks + (lane >> 4) * 8]);
+            for (int i = 0; i < 4; ++i) {
+                if (a_cols)  // matrices (m 0-7 | 8-15) x (k 0-7 | 8-15) from rows k of [k][m]
+                    ldsm_x4_t(af[i], &A_s[buf][(ks + (lane & 7) + ((lane >> 4) & 1) * 8) * kATPitch + wm * 64 +
+                                              i * 16 + ((lane >> 3) & 1) * 8]);
+                else
+                    ldsm_x4(af[i], &A_s[buf][(wm * 64 + i * 16 + (lane & 15)) * kAPitch + ks + (lane >> 4) * 8]);
+            }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
                 ldsm_x4_t(bf[j], &B_s[buf][(ks + (lane & 15)) * kBPitch + wn * 32 + j * 16 + (lane >> 4) * 8]);
@@ -474,13 +478,22 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd p) {
     }
 }
 
-// dbias[e] = sum over tokens of dlogit[t, e], in token order.
-__global__ void __launch_bounds__(256) dbias_kernel(int T, int E, const float* dlogit, float* dbias) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
+// dbias[e] = sum over tokens of dlogit[t, e]: 32 experts per block, 32 token slices
+// (t = slice, slice + 32, ...) summed in slice order, so the result is deterministic.
+__global__ void __launch_bounds__(1024) dbias_kernel(int T, int E, const float* dlogit, float* dbias) {
+    __shared__ float part[32][33];
+    const int le = threadIdx.x & 31, ts = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + le;
     float s = 0.f;
-    for (int t = 0; t < T; ++t) s += dlogit[(size_t)t * E + e];
-    dbias[e] = s;
+    if (e < E)
+        for (int t = ts; t < T; t += 32) s += dlogit[(size_t)t * E + e];
+    part[ts][le] = s;
+    __syncthreads();
+    if (ts == 0 && e < E) {
+        float tot = 0.f;
+        for (int i = 0; i < 32; ++i) tot += part[i][le];
+        dbias[e] = tot;
+    }
 }
 
 // dx[t, :] += sum_j dx_perm[inv_pos[t k + j], :] + dx_s[t, :], four channels per thread.
@@ -573,6 +586,12 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
     do {                                       \
         if ((e = (x)) != cudaSuccess) return e; \
     } while (0)
+    // optional events around the parts (slots of moe_stage_events_t, see moe.h)
+    auto mark = [&](int slot, bool begin) -> cudaError_t {
+        void* ev = a.ev ? (begin ? a.ev->start[slot] : a.ev->stop[slot]) : nullptr;
+        return ev ? cudaEventRecord((cudaEvent_t)ev, st) : cudaSuccess;
+    };
+    BWD_TRY(mark(MOE_STAGE_ROUTE, true));
 
     // forward quantities: activation codes, the router's logits, the permutation, g and u
     BWD_TRY(launch_quant_act(a.x, T, H, xq, xs, NormArgs{}, st));
@@ -618,6 +637,8 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
             return cudaErrorInvalidValue;
         BWD_TRY(launch_expert_gemm(g, m, st));
     }
+    BWD_TRY(mark(MOE_STAGE_ROUTE, false));
+    BWD_TRY(mark(MOE_STAGE_PERMUTE, true));
 
     BwdGemm b = {};
     b.T = T;
@@ -709,12 +730,14 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         router_bwd_kernel<<<cdiv(T, 8), 256, 0, st>>>(r);
         BWD_TRY(cudaGetLastError());
         if (a.dbias) {
-            dbias_kernel<<<cdiv(E, 256), 256, 0, st>>>(T, E, b.dlogit, a.dbias);
+            dbias_kernel<<<cdiv(E, 32), 1024, 0, st>>>(T, E, b.dlogit, a.dbias);
             BWD_TRY(cudaGetLastError());
         }
     }
+    BWD_TRY(mark(MOE_STAGE_PERMUTE, false));
     // dx: router term, then the routed rows and the shared experts
     {
+        BWD_TRY(mark(MOE_STAGE_COMBINE, true));
         BwdGemm x = b;
         x.grouping = 0;
         x.M = T;
@@ -736,7 +759,9 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         g.w_estride = (size_t)I * H;
         g.s_estride = (size_t)(I / 128) * (H / 128);
         g.c0 = reinterpret_cast<float*>(at(L.dx_perm));
+        BWD_TRY(mark(MOE_STAGE_GATE_UP, true));
         BWD_TRY(run_gemm<F_DGU>(g, dim3(mt_grid, cdiv(H, kBN)), st));
+        BWD_TRY(mark(MOE_STAGE_GATE_UP, false));
         if (sh) {
             BwdGemm gs = b;
             gs.routed = 0;
@@ -757,7 +782,9 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         dx_combine_kernel<<<cdiv(n4, 256), 256, 0, st>>>(T, H, k, inv_pos, reinterpret_cast<float*>(at(L.dx_perm)),
                                                         sh ? reinterpret_cast<float*>(at(L.dx_s)) : nullptr, a.dx);
         BWD_TRY(cudaGetLastError());
+        BWD_TRY(mark(MOE_STAGE_COMBINE, false));
     }
+    BWD_TRY(mark(MOE_STAGE_DOWN, true));
     // weight gradients: down, gate/up (routed per expert, shared over all tokens), router
     {
         BwdGemm w = b;
@@ -812,6 +839,7 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         r.c0 = a.dw_router;
         BWD_TRY(run_gemm<F_WR>(r, dim3(cdiv(H, kBN), cdiv(E, kBM), 1), st));
     }
+    BWD_TRY(mark(MOE_STAGE_DOWN, false));
 #undef BWD_TRY
     return cudaSuccess;
 }

@@ -474,10 +474,11 @@ size_t moe_backward_workspace_size(const moe_config_t* cfg, int32_t max_tokens) 
     return bwd_layout(*cfg, max_tokens).total;
 }
 
-moe_status_t moe_backward(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_t* weights,
-                          const int32_t* topk_ids, const float* topk_w, const void* dout_bf16, float* dx,
-                          float* dw_gate, float* dw_up, float* dw_down, float* dws_gate, float* dws_up,
-                          float* dws_down, float* dw_router, float* dbias, void* ws, size_t ws_bytes, void* stream) {
+moe_status_t moe_backward_profiled(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                                   const moe_weights_t* weights, const int32_t* topk_ids, const float* topk_w,
+                                   const void* dout_bf16, float* dx, float* dw_gate, float* dw_up, float* dw_down,
+                                   float* dws_gate, float* dws_up, float* dws_down, float* dw_router, float* dbias,
+                                   void* ws, size_t ws_bytes, void* stream, const moe_stage_events_t* events) {
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_T(cfg, T));
     if (!gemm_supported(*cfg) || cfg->n_routed % 16) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -527,8 +528,17 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x_bf16, int32_t T
     a.dws_down = sh ? dws_down : nullptr;
     a.dw_router = dw_router;
     a.dbias = dbias;
+    a.ev = events;
     MOE_CUDA(launch_backward(*cfg, a, ws, st));
     return MOE_OK;
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_t* weights,
+                          const int32_t* topk_ids, const float* topk_w, const void* dout_bf16, float* dx,
+                          float* dw_gate, float* dw_up, float* dw_down, float* dws_gate, float* dws_up,
+                          float* dws_down, float* dw_router, float* dbias, void* ws, size_t ws_bytes, void* stream) {
+    return moe_backward_profiled(cfg, x_bf16, T, weights, topk_ids, topk_w, dout_bf16, dx, dw_gate, dw_up, dw_down,
+                                 dws_gate, dws_up, dws_down, dw_router, dbias, ws, ws_bytes, stream, nullptr);
 }
 
 moe_status_t moe_quant_act(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq, float* xs, void* stream) {

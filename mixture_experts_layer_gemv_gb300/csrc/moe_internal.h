@@ -245,6 +245,7 @@ struct BwdArgs {
     const float* topk_w;           // [T, k] the forward's routing weights
     const void* dout;              // bf16 [T, H]
     float *dx, *dw_gate, *dw_up, *dw_down, *dws_gate, *dws_up, *dws_down, *dw_router, *dbias;
+    const moe_stage_events_t* ev = nullptr;  // optional: events around the parts (moe_backward_profiled)
 };
 cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, cudaStream_t st);
 
