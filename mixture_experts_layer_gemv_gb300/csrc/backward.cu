@@ -30,51 +30,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 32;
-constexpr int kAPitch = kBK + 8;  // bf16 per A row in shared memory (k contiguous)
-constexpr int kATPitch = kBM + 8; // bf16 per A row of the transposed layout (m contiguous, one row per k)
-constexpr int kBPitch = kBN + 8;  // bf16 per B row in shared memory (n contiguous)
-constexpr int kGThr = 256;        // 8 warps: 2 along M (64 rows) x 4 along N (32 columns)
-
-// The contractions (F_*) and how each reads its operands; C is fp32 [M, N] per group.
-enum : int {
-    F_DDOWN = 0,  // dau[r, i]   = sum_h dout[tok r, h] Wd_e[h, i]          rows r of a tile, K = H
-    F_DGU = 1,    // dx_r[r, h]  = sum_i dgu[r, i] [Wg_e; Wu_e][i, h]       rows r of a tile, K = 2 Iw
-    F_DXR = 2,    // dx[t, h]    = sum_e dlogit[t, e] Wr[e, h]              K = E
-    F_WDOWN = 3,  // dWd_e[h, i] = sum_r w_r dout[tok r, h] ahat[r, i]      K = rows of e
-    F_WGU = 4,    // [dWg_e; dWu_e][i, h] = sum_r dgu[r, i] xhat[tok r, h]  K = rows of e
-    F_WR = 5,     // dWr[e, h]   = sum_t dlogit[t, e] x[t, h]               K = T
-};
-
-struct BwdGemm {
-    int M, N, K;       // output extent; K of single-group problems
-    int T, k, E;
-    int Iw;            // intermediate width of the experts involved (I routed, Is shared)
-    int H;
-    int routed;        // rows are permuted rows (token via perm_src) or tokens
-    const int32_t* perm_src;
-    const MTile* mtiles;
-    const Ctrl* ctrl;
-    const int32_t* offsets;  // per-expert row ranges (wgrad of routed experts)
-    int grouping;            // 0: one group; 1: the permutation's 128-row tiles; 2: per expert
-    const __nv_bfloat16* dout;  // [T, H]
-    const __nv_bfloat16* dgu;   // [rows, 2 Iw]
-    const __nv_bfloat16* ahat;  // [rows, Iw]
-    const float* topk_w;        // [T k] routing weights
-    const float* dlogit;        // [T, E]
-    const __nv_bfloat16* x;     // [T, H]
-    const uint8_t* xq;          // [T, H] e4m3
-    const float* xs;            // [T, H / 128]
-    const uint8_t *w0, *w1;     // FP8 weights: w1 stacked under w0 along K (F_DGU)
-    const float *s0, *s1;       // their block scales
-    size_t w_estride, s_estride;  // per-expert strides (elements) of w0/w1 and s0/s1
-    const float* wr;              // [E, H]
-    float *c0, *c1;             // outputs; F_WGU rows >= Iw go to c1
-    size_t c_estride;           // per-expert stride of c0/c1 (elements)
-};
-
-__device__ __forceinline__ int tok_of(const BwdGemm& p, int r) { return p.routed ? p.perm_src[r] / p.k : r; }
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -96,29 +51,6 @@ __device__ __forceinline__ void e4m3x16_to_bf16(uint4 q, float s, uint4& lo, uin
     hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-__device__ __forceinline__ void f32x16_to_bf16(const float* v, float mul, uint4& lo, uint4& hi) {
-    lo = make_uint4(pack_bf16x2(v[0] * mul, v[1] * mul), pack_bf16x2(v[2] * mul, v[3] * mul),
-                    pack_bf16x2(v[4] * mul, v[5] * mul), pack_bf16x2(v[6] * mul, v[7] * mul));
-    hi = make_uint4(pack_bf16x2(v[8] * mul, v[9] * mul), pack_bf16x2(v[10] * mul, v[11] * mul),
-                    pack_bf16x2(v[12] * mul, v[13] * mul), pack_bf16x2(v[14] * mul, v[15] * mul));
-}
-
-__device__ __forceinline__ void bf16x16_scaled(uint4 a, uint4 b, float mul, uint4& lo, uint4& hi) {
-    if (mul == 1.f) {
-        lo = a;
-        hi = b;
-        return;
-    }
-    float v[16];
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-    f32x16_to_bf16(v, mul, lo, hi);
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -137,158 +69,121 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// One 128 x 128 output tile of one group. A tile element (m, kk) and B tile element
-// (kk, n) are read as 16 contiguous values per thread and staged as bf16: B as [k][n],
-// A as [m][k] when its rows run along k (dgrad) and as [k][m] when they run along m
-// (wgrad), two buffers each; fragments come from ldmatrix (.trans for the [k][*] ones).
-template <int F>
-__global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const BwdGemm p) {
-    static_assert(kBM * kAPitch >= kBK * kATPitch, "one A buffer holds either layout");
-    __shared__ __align__(16) __nv_bfloat16 A_s[2][kBM * kAPitch];
-    __shared__ __align__(16) __nv_bfloat16 B_s[2][kBK * kBPitch];
-    constexpr bool a_cols = F >= F_WDOWN;  // A(m, kk) contiguous along m (its rows are the K index)
+constexpr int kBM = 128, kBN = 128, kBK = 32;
+constexpr int kStages = 4;
+constexpr int kAPitch = kBK + 8;   // bf16 per A row, [m][k] layout (k contiguous)
+constexpr int kTPitch = kBN + 8;   // bf16 per row of the [k][m] and [k][n] layouts
+constexpr int kGThr = 256;         // 8 warps: 2 along M (64 rows) x 4 along N (32 columns)
+constexpr int kAStage = kBM * kAPitch;  // bf16 per A stage (the larger of the two layouts)
+constexpr int kBStage = kBK * kTPitch;
+static_assert(kAStage >= kBK * kTPitch, "an A stage holds either layout");
+constexpr size_t kGemmSmem = (size_t)kStages * (kAStage + kBStage) * 2;
+
+// A bf16 GEMM over row-major operands, per group: C[m, n] = sum_k A(m, k) B(k, n).
+// A is [rows][lda] with k contiguous (dgrad: rows are the output rows) or, with
+// kACols, [k rows][lda] with m contiguous (wgrad: the K index runs over token rows);
+// B is [k][ldb] with n contiguous, its rows >= ksplit taken from B2 (two stacked
+// matrices). Groups: one (grouping 0), the permutation's 128-row tiles of an expert
+// (1: rows row0.., B of that expert), or one expert's K range of rows (2: C of that
+// expert).
+struct Gemm {
+    int M, N, K;
+    int grouping;
+    const MTile* mtiles;
+    const Ctrl* ctrl;
+    const int32_t* offsets;
+    const __nv_bfloat16* A;
+    long lda;
+    const __nv_bfloat16 *B, *B2;
+    int ksplit;
+    long ldb;
+    size_t b_estride;
+    float *C, *C2;  // output rows m >= msplit go to C2 (row m - msplit)
+    int msplit;
+    long ldc;
+    size_t c_estride;
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(pred ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// One 128 x 128 output tile: a kStages-deep ring of cp.async copies (16 bytes each, out of
+// range chunks zero-filled) and ldmatrix fragments (.trans for the [k][*] layouts).
+template <bool kACols>
+__global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const Gemm p) {
+    extern __shared__ __align__(16) uint8_t smem_g[];
+    __nv_bfloat16* As = reinterpret_cast<__nv_bfloat16*>(smem_g);
+    __nv_bfloat16* Bs = As + kStages * kAStage;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // ---- the group: output rows [m0, m0 + mv), columns [n0, N), K range [k0, k0 + kv)
-    int e = 0, m0, mv, n0 = blockIdx.y * kBN, k0 = 0, kv = p.K, row0 = 0;
-    if (p.grouping == 1) {  // a 128-row tile of the permutation (rows r = row0 + m)
-        if ((int)blockIdx.x >= p.ctrl->n_mtiles) return;
-        const MTile t = p.mtiles[blockIdx.x];
-        e = t.expert;
-        row0 = t.row0;
-        m0 = 0;
-        mv = t.nrows;
-    } else {
-        m0 = blockIdx.x * kBM;
+    int e = 0, m0, mv, n0, kbase = 0, kv = p.K, rowbase;
+    if (kACols) {  // wgrad: N tiles on x, M tiles on y, the group on z
+        n0 = blockIdx.x * kBN;
+        m0 = blockIdx.y * kBM;
         mv = min(kBM, p.M - m0);
-        if (a_cols) {  // wgrad: M, N tiles on x, y, the group on z
-            m0 = blockIdx.y * kBM;
-            mv = min(kBM, p.M - m0);
-            n0 = blockIdx.x * kBN;
-        }
+        rowbase = 0;
         if (p.grouping == 2) {
             e = blockIdx.z;
-            k0 = p.offsets[e];
-            kv = p.offsets[e + 1] - k0;
+            kbase = p.offsets[e];
+            kv = p.offsets[e + 1] - kbase;
+        }
+    } else {
+        n0 = blockIdx.y * kBN;
+        if (p.grouping == 1) {
+            if ((int)blockIdx.x >= p.ctrl->n_mtiles) return;
+            const MTile t = p.mtiles[blockIdx.x];
+            e = t.expert;
+            m0 = 0;
+            mv = t.nrows;
+            rowbase = t.row0;
+        } else {
+            m0 = blockIdx.x * kBM;
+            mv = min(kBM, p.M - m0);
+            rowbase = m0;
         }
     }
     if (mv <= 0 || n0 >= p.N) return;
+    const __nv_bfloat16* Bm = p.B + (size_t)e * p.b_estride;
+    const __nv_bfloat16* Bm2 = p.B2 ? p.B2 + (size_t)e * p.b_estride : nullptr;
 
-    // ---- loader coordinates: 16 contiguous values per thread
-    // A rows mode: m = tid / 2, k chunk (tid % 2) * 16; A cols mode: kk = tid / 8, m chunk (tid % 8) * 16
-    // B: kk = tid / 8, n chunk (tid % 8) * 16
-    const int am = a_cols ? (tid & 7) * 16 : tid >> 1;
-    const int ak = a_cols ? tid >> 3 : (tid & 1) * 16;
-    const int bk = tid >> 3, bn = (tid & 7) * 16;
-
-    // A rows mode: the source row of this thread's m (fixed over the K loop)
-    const __nv_bfloat16* arow_b = nullptr;
-    const float* arow_f = nullptr;
-    if (!a_cols && am < mv) {
-        if (F == F_DDOWN) arow_b = p.dout + (size_t)tok_of(p, row0 + m0 + am) * p.H;
-        if (F == F_DGU) arow_b = p.dgu + (size_t)(row0 + m0 + am) * (2 * p.Iw);
-        if (F == F_DXR) arow_f = p.dlogit + (size_t)(m0 + am) * p.E;
-    }
-    const uint8_t* wq0 = p.w0 ? p.w0 + (size_t)e * p.w_estride : nullptr;
-    const uint8_t* wq1 = p.w1 ? p.w1 + (size_t)e * p.w_estride : nullptr;
-    const float* ws0 = p.s0 ? p.s0 + (size_t)e * p.s_estride : nullptr;
-    const float* ws1 = p.s1 ? p.s1 + (size_t)e * p.s_estride : nullptr;
-
-    uint4 ra0, ra1, rb0, rb1;  // staged bf16 (16 values each for A and B)
-    auto load = [&](int kt) {
+    auto load_stage = [&](int slot, int kt) {
         const int kb = kt * kBK;
-        // ---------------- A
-        ra0 = ra1 = make_uint4(0, 0, 0, 0);
-        if (!a_cols) {
-            const int kk = kb + ak;
-            if (am < mv && kk < kv) {
-                if (F == F_DXR) {
-                    float v[16];
+        __nv_bfloat16* as = As + slot * kAStage;
+        __nv_bfloat16* bs = Bs + slot * kBStage;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 f = __ldg(reinterpret_cast<const float4*>(arow_f + kk) + q);
-                        v[4 * q] = f.x, v[4 * q + 1] = f.y, v[4 * q + 2] = f.z, v[4 * q + 3] = f.w;
-                    }
-                    f32x16_to_bf16(v, 1.f, ra0, ra1);
-                } else {
-                    ra0 = __ldg(reinterpret_cast<const uint4*>(arow_b + kk));
-                    ra1 = __ldg(reinterpret_cast<const uint4*>(arow_b + kk) + 1);
-                }
+        for (int q = 0; q < 2; ++q) {
+            const int c = tid + kGThr * q;
+            if (!kACols) {  // 128 rows x 4 chunks of 8 k
+                const int m = c >> 2, kc = (c & 3) * 8;
+                const bool ok = m < mv && kb + kc < kv;
+                const __nv_bfloat16* src = ok ? p.A + (size_t)(rowbase + m) * p.lda + kb + kc : p.A;
+                cp_async16(as + m * kAPitch + kc, src, ok);
+            } else {        // 32 k rows x 16 chunks of 8 m
+                const int kk = c >> 4, mc = (c & 15) * 8;
+                const bool ok = kb + kk < kv && m0 + mc < p.M;
+                const __nv_bfloat16* src = ok ? p.A + (size_t)(kbase + kb + kk) * p.lda + m0 + mc : p.A;
+                cp_async16(as + kk * kTPitch + mc, src, ok);
             }
-        } else {
-            const int kk = kb + ak;  // a row of the group
-            const int m = m0 + am;
-            if (kk < kv && m < p.M) {
-                const int r = k0 + kk;
-                if (F == F_WDOWN) {
-                    const float wmul = p.routed ? p.topk_w[p.perm_src[r]] : 1.f;
-                    const uint4* src = reinterpret_cast<const uint4*>(p.dout + (size_t)tok_of(p, r) * p.H + m);
-                    bf16x16_scaled(__ldg(src), __ldg(src + 1), wmul, ra0, ra1);
-                } else if (F == F_WGU) {
-                    const uint4* src = reinterpret_cast<const uint4*>(p.dgu + (size_t)r * (2 * p.Iw) + m);
-                    ra0 = __ldg(src);
-                    ra1 = __ldg(src + 1);
-                } else {  // F_WR
-                    float v[16];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 f = __ldg(reinterpret_cast<const float4*>(p.dlogit + (size_t)r * p.E + m) + q);
-                        v[4 * q] = f.x, v[4 * q + 1] = f.y, v[4 * q + 2] = f.z, v[4 * q + 3] = f.w;
-                    }
-                    f32x16_to_bf16(v, 1.f, ra0, ra1);
-                }
+            {  // B: 32 k rows x 16 chunks of 8 n
+                const int kk = c >> 4, nc = (c & 15) * 8;
+                const int kr = kb + kk;
+                const bool ok = kr < kv && n0 + nc < p.N;
+                const bool second = Bm2 && kr >= p.ksplit;
+                const __nv_bfloat16* src =
+                    ok ? (second ? Bm2 + (size_t)(kbase + kr - p.ksplit) * p.ldb : Bm + (size_t)(kbase + kr) * p.ldb) +
+                             n0 + nc
+                       : p.B;
+                cp_async16(bs + kk * kTPitch + nc, src, ok);
             }
         }
-        // ---------------- B: row kk of the K range, columns n0 + bn .. + 15
-        rb0 = rb1 = make_uint4(0, 0, 0, 0);
-        const int kk = kb + bk, n = n0 + bn;
-        if (kk < kv && n < p.N) {
-            if (F == F_DDOWN) {  // Wd_e [H, Iw]: row kk = h
-                const uint4 q = __ldg(reinterpret_cast<const uint4*>(wq0 + (size_t)kk * p.N + n));
-                const float s = __ldg(ws0 + (size_t)(kk / kBlk) * (p.N / kBlk) + n / kBlk);
-                e4m3x16_to_bf16(q, s, rb0, rb1);
-            } else if (F == F_DGU) {  // [Wg_e; Wu_e], each [Iw, H]
-                const bool up = kk >= p.Iw;
-                const int kr = up ? kk - p.Iw : kk;
-                const uint4 q = __ldg(reinterpret_cast<const uint4*>((up ? wq1 : wq0) + (size_t)kr * p.N + n));
-                const float s = __ldg((up ? ws1 : ws0) + (size_t)(kr / kBlk) * (p.N / kBlk) + n / kBlk);
-                e4m3x16_to_bf16(q, s, rb0, rb1);
-            } else if (F == F_DXR) {  // Wr [E, H]
-                float v[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 f = __ldg(reinterpret_cast<const float4*>(p.wr + (size_t)kk * p.N + n) + q);
-                    v[4 * q] = f.x, v[4 * q + 1] = f.y, v[4 * q + 2] = f.z, v[4 * q + 3] = f.w;
-                }
-                f32x16_to_bf16(v, 1.f, rb0, rb1);
-            } else if (F == F_WDOWN) {  // ahat [rows, Iw]
-                const uint4* src = reinterpret_cast<const uint4*>(p.ahat + (size_t)(k0 + kk) * p.N + n);
-                rb0 = __ldg(src);
-                rb1 = __ldg(src + 1);
-            } else if (F == F_WGU) {  // xhat of the row's token: codes x per-128 scale (exact in bf16)
-                const int t = tok_of(p, k0 + kk);
-                const uint4 q = __ldg(reinterpret_cast<const uint4*>(p.xq + (size_t)t * p.N + n));
-                e4m3x16_to_bf16(q, __ldg(p.xs + (size_t)t * (p.N / kBlk) + n / kBlk), rb0, rb1);
-            } else {  // F_WR: x [T, H]
-                const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)(k0 + kk) * p.N + n);
-                rb0 = __ldg(src);
-                rb1 = __ldg(src + 1);
-            }
-        }
-    };
-    auto store = [&](int buf) {
-        if (!a_cols) {
-            uint4* d = reinterpret_cast<uint4*>(&A_s[buf][am * kAPitch + ak]);
-            d[0] = ra0;
-            d[1] = ra1;
-        } else {  // row kk of the [k][m] layout: 16 consecutive m
-            uint4* d = reinterpret_cast<uint4*>(&A_s[buf][ak * kATPitch + am]);
-            d[0] = ra0;
-            d[1] = ra1;
-        }
-        uint4* d = reinterpret_cast<uint4*>(&B_s[buf][bk * kBPitch + bn]);
-        d[0] = rb0;
-        d[1] = rb1;
     };
 
     float acc[4][4][4];
@@ -298,36 +193,41 @@ __global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const BwdGemm p) {
         for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
     const int wm = warp & 1, wn = warp >> 1;
     const int nk = (kv + kBK - 1) / kBK;
-    if (nk > 0) {
-        load(0);
-        store(0);
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < nk) load_stage(s, s);
+        cp_async_commit();
     }
-    __syncthreads();
     for (int kt = 0; kt < nk; ++kt) {
-        const int buf = kt & 1;
-        if (kt + 1 < nk) load(kt + 1);  // global loads in flight during the MMAs
+        cp_async_wait<kStages - 2>();  // stage kt has landed (this thread's copies)
+        __syncthreads();               // ... and everyone's; stage kt-1 is free again
+        const int nxt = kt + kStages - 1;
+        if (nxt < nk) load_stage(nxt % kStages, nxt);
+        cp_async_commit();
+        const __nv_bfloat16* as = As + (kt % kStages) * kAStage;
+        const __nv_bfloat16* bs = Bs + (kt % kStages) * kBStage;
 #pragma unroll
         for (int ks = 0; ks < kBK; ks += 16) {
             uint32_t af[4][4], bf[2][4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if (a_cols)  // matrices (m 0-7 | 8-15) x (k 0-7 | 8-15) from rows k of [k][m]
-                    ldsm_x4_t(af[i], &A_s[buf][(ks + (lane & 7) + ((lane >> 4) & 1) * 8) * kATPitch + wm * 64 +
-                                              i * 16 + ((lane >> 3) & 1) * 8]);
+                if (kACols)  // matrices (m 0-7 | 8-15) x (k 0-7 | 8-15) from rows k of [k][m]
+                    ldsm_x4_t(af[i], as + (ks + (lane & 7) + ((lane >> 4) & 1) * 8) * kTPitch + wm * 64 + i * 16 +
+                                         ((lane >> 3) & 1) * 8);
                 else
-                    ldsm_x4(af[i], &A_s[buf][(wm * 64 + i * 16 + (lane & 15)) * kAPitch + ks + (lane >> 4) * 8]);
+                    ldsm_x4(af[i], as + (wm * 64 + i * 16 + (lane & 15)) * kAPitch + ks + (lane >> 4) * 8);
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-                ldsm_x4_t(bf[j], &B_s[buf][(ks + (lane & 15)) * kBPitch + wn * 32 + j * 16 + (lane >> 4) * 8]);
+                ldsm_x4_t(bf[j], bs + (ks + (lane & 15)) * kTPitch + wn * 32 + j * 16 + (lane >> 4) * 8);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) mma_bf16(acc[i][j], af[i], bf[j >> 1][2 * (j & 1)], bf[j >> 1][2 * (j & 1) + 1]);
+                for (int j = 0; j < 4; ++j)
+                    mma_bf16(acc[i][j], af[i], bf[j >> 1][2 * (j & 1)], bf[j >> 1][2 * (j & 1) + 1]);
         }
-        if (kt + 1 < nk) store(buf ^ 1);
-        __syncthreads();
     }
+    cp_async_wait<0>();
 
     // ---- epilogue: fp32 rows of C
 #pragma unroll
@@ -337,14 +237,12 @@ __global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const BwdGemm p) {
             const int m = wm * 64 + i * 16 + (lane >> 2) + 8 * h;
             if (m >= mv) continue;
             float* crow;
-            if (F == F_DDOWN || F == F_DGU) {
-                crow = p.c0 + (size_t)(row0 + m0 + m) * p.N;
-            } else if (F == F_WGU) {
-                const int mm = m0 + m;
-                crow = mm < p.Iw ? p.c0 + (size_t)e * p.c_estride + (size_t)mm * p.N
-                                 : p.c1 + (size_t)e * p.c_estride + (size_t)(mm - p.Iw) * p.N;
+            if (!kACols) {
+                crow = p.C + (size_t)(rowbase + m) * p.ldc;
             } else {
-                crow = p.c0 + (size_t)e * p.c_estride + (size_t)(m0 + m) * p.N;
+                const int mm = m0 + m;
+                crow = (p.C2 && mm >= p.msplit) ? p.C2 + (size_t)e * p.c_estride + (size_t)(mm - p.msplit) * p.ldc
+                                                : p.C + (size_t)e * p.c_estride + (size_t)mm * p.ldc;
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -354,17 +252,69 @@ __global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const BwdGemm p) {
         }
 }
 
+// ---------------------------------------------------------------- operand preparation
+// nmat matrices [rows, cols] of E4M3 codes with fp32 scales per 128 x 128 block ->
+// bf16 (dec(code) * scale, one rounding), 16 values per thread.
+__global__ void __launch_bounds__(256) dequant_bf16_kernel(const uint8_t* q, const float* s, long nmat, int rows,
+                                                           int cols, __nv_bfloat16* out) {
+    const long per = (long)rows * cols / 16;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nmat * per; i += (long)gridDim.x * blockDim.x) {
+        const long mat = i / per, off = (i % per) * 16;
+        const int r = (int)(off / cols), c = (int)(off % cols);
+        const float sc = s[(size_t)mat * (rows / kBlk) * (cols / kBlk) + (size_t)(r / kBlk) * (cols / kBlk) + c / kBlk];
+        uint4 lo, hi;
+        e4m3x16_to_bf16(*reinterpret_cast<const uint4*>(q + (size_t)mat * rows * cols + off), sc, lo, hi);
+        uint4* d = reinterpret_cast<uint4*>(out + (size_t)mat * rows * cols + off);
+        d[0] = lo;
+        d[1] = hi;
+    }
+}
+
+// xhat[t, :] = dec(xq[t, :]) * xs[t, block] in bf16 (exact: a 3-bit significand times 2^k).
+__global__ void __launch_bounds__(256) xhat_kernel(const uint8_t* xq, const float* xs, long T, int H,
+                                                   __nv_bfloat16* out) {
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < T * H / 16; i += (long)gridDim.x * blockDim.x) {
+        const long off = i * 16;
+        const long t = off / H;
+        const int h = (int)(off % H);
+        uint4 lo, hi;
+        e4m3x16_to_bf16(*reinterpret_cast<const uint4*>(xq + off), xs[t * (H / kBlk) + h / kBlk], lo, hi);
+        reinterpret_cast<uint4*>(out + off)[0] = lo;
+        reinterpret_cast<uint4*>(out + off)[1] = hi;
+    }
+}
+
+// dst[r, :] = src[perm_src[r] / k, :] for the n_rows permuted rows (bf16 rows of H), a warp per row.
+__global__ void __launch_bounds__(256) gather_bf16_kernel(const __nv_bfloat16* src, int H, const int32_t* perm_src,
+                                                          int k, int n_rows, __nv_bfloat16* dst) {
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (r >= n_rows) return;
+    const int f = perm_src[r];
+    const bool good = (unsigned)f < (unsigned)n_rows;  // else a row no valid id reached: zeros
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)(good ? f / k : 0) * H);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)r * H);
+    for (int c = lane; c < H / 8; c += 32) d4[c] = good ? __ldg(s4 + c) : make_uint4(0, 0, 0, 0);
+}
+
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* src, long n, __nv_bfloat16* dst) {
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n / 2; i += (long)gridDim.x * blockDim.x) {
+        const float2 v = reinterpret_cast<const float2*>(src)[i];
+        reinterpret_cast<uint32_t*>(dst)[i] = pack_bf16x2(v.x, v.y);
+    }
+}
+
 // SwiGLU backward and the quantised intermediate, one warp per row (routed rows or
 // tokens): ahat = the forward's FP8 intermediate (same arithmetic as its epilogue),
-// dw = <dau, ahat> (routed rows: written at the row's (token, slot) index), and
-// dgu = [dg | du] with da = w dau.
+// dw = <dau, ahat> (routed rows: written at the row's (token, slot) index),
+// dgu = [dg | du] with da = w dau, and wahat = w ahat in bf16 (the operand of the down
+// weight gradient, which then reads dout rows as they are).
 struct SwigluBwd {
     int rows, Iw, routed;
     const float *g, *u, *dau;
     const int32_t* perm_src;
     const float* topk_w;
-    __nv_bfloat16* ahat;  // [rows, Iw]
-    __nv_bfloat16* dgu;   // [rows, 2 Iw]
+    __nv_bfloat16* wahat;  // [rows, Iw]
+    __nv_bfloat16* dgu;    // [rows, 2 Iw]
     float* dw;            // [T k]
 };
 
@@ -372,7 +322,9 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const SwigluBwd p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + warp;
     if (r >= p.rows) return;
-    const float w = p.routed ? p.topk_w[p.perm_src[r]] : 1.f;
+    const int f = p.routed ? p.perm_src[r] : 0;
+    const bool good = !p.routed || (unsigned)f < (unsigned)p.rows;  // rows no valid id reached: weight 0
+    const float w = p.routed ? (good ? p.topk_w[f] : 0.f) : 1.f;
     const size_t base = (size_t)r * p.Iw;
     float dw = 0.f;
     for (int b = 0; b < p.Iw; b += kBlk) {
@@ -406,14 +358,15 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const SwigluBwd p) {
             dg[q] = da * u[q] * sg * (1.f + g[q] * (1.f - sg));
             du[q] = da * g[q] * sg;
         }
-        *reinterpret_cast<uint2*>(p.ahat + base + i) = make_uint2(pack_bf16x2(ah[0], ah[1]), pack_bf16x2(ah[2], ah[3]));
+        *reinterpret_cast<uint2*>(p.wahat + base + i) =
+            make_uint2(pack_bf16x2(w * ah[0], w * ah[1]), pack_bf16x2(w * ah[2], w * ah[3]));
         __nv_bfloat16* drow = p.dgu + (size_t)r * 2 * p.Iw;
         *reinterpret_cast<uint2*>(drow + i) = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
         *reinterpret_cast<uint2*>(drow + p.Iw + i) =
             make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
     }
     dw = warp_sum(dw);
-    if (p.routed && lane == 0) p.dw[p.perm_src[r]] = dw;
+    if (p.routed && good && lane == 0) p.dw[f] = dw;
 }
 
 // Router backward, one warp per token: the forward's logits (split-K partials summed in
@@ -427,6 +380,7 @@ struct RouterBwd {
     const int32_t* ids;
     const float* dw;    // [T k]
     float* dlogit;      // [T, E]
+    __nv_bfloat16* dlogit_bf;  // [T, E], the GEMMs' operand
 };
 
 __global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd p) {
@@ -474,7 +428,11 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const RouterBwd p) {
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
         const int e = lane + 32 * q;
-        if (e < p.E) p.dlogit[(size_t)t * p.E + e] = l[q] * (dp[q] - pdp);
+        if (e < p.E) {
+            const float v = l[q] * (dp[q] - pdp);
+            p.dlogit[(size_t)t * p.E + e] = v;
+            p.dlogit_bf[(size_t)t * p.E + e] = __float2bfloat16_rn(v);
+        }
     }
 }
 
@@ -505,7 +463,9 @@ __global__ void __launch_bounds__(256) dx_combine_kernel(int T, int H, int k, co
     const int t = (int)(i / (H / 4)), h = (int)(i % (H / 4)) * 4;
     float4 acc = *reinterpret_cast<const float4*>(dx + (size_t)t * H + h);
     for (int j = 0; j < k; ++j) {
-        const float4 v = *reinterpret_cast<const float4*>(dx_perm + (size_t)inv_pos[(size_t)t * k + j] * H + h);
+        const int pos = inv_pos[(size_t)t * k + j];
+        if ((unsigned)pos >= (unsigned)(T * k)) continue;  // an invalid id: no row (status reported)
+        const float4 v = *reinterpret_cast<const float4*>(dx_perm + (size_t)pos * H + h);
         acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
     }
     if (dx_s) {
@@ -515,14 +475,22 @@ __global__ void __launch_bounds__(256) dx_combine_kernel(int T, int H, int k, co
     *reinterpret_cast<float4*>(dx + (size_t)t * H + h) = acc;
 }
 
-template <int F>
-cudaError_t run_gemm(const BwdGemm& p, dim3 grid, cudaStream_t st) {
+template <bool kACols>
+cudaError_t run_gemm(const Gemm& p, dim3 grid, cudaStream_t st) {
     if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-    bwd_gemm_kernel<F><<<grid, kGThr, 0, st>>>(p);
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[kACols]) {
+        const cudaError_t e = cudaFuncSetAttribute((const void*)bwd_gemm_kernel<kACols>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[kACols] = true;
+    }
+    bwd_gemm_kernel<kACols><<<grid, kGThr, kGemmSmem, st>>>(p);
     return cudaGetLastError();
 }
 
 unsigned cdiv(long a, long b) { return (unsigned)((a + b - 1) / b); }
+unsigned grid_for(long n, int per_thread) { return (unsigned)std::min<long>(4096, std::max<long>(1, cdiv(n / per_thread, 256))); }
 
 }  // namespace
 
@@ -553,17 +521,28 @@ BwdLayout bwd_layout(const moe_config_t& c, int64_t T) {
     L.g_r = take(R * I * 4);
     L.u_r = take(R * I * 4);
     L.dau_r = take(R * I * 4);
-    L.ahat_r = take(R * I * 2);
+    L.wahat_r = take(R * I * 2);
     L.dgu_r = take(R * 2 * I * 2);
     L.dx_perm = take(R * H * 4);
     L.g_s = take(t * Is * 4);
     L.u_s = take(t * Is * 4);
     L.dau_s = take(t * Is * 4);
-    L.ahat_s = take(t * Is * 2);
+    L.wahat_s = take(t * Is * 2);
     L.dgu_s = take(t * 2 * Is * 2);
     L.dx_s = take(t * H * 4);
     L.dw = take(R * 4);
     L.dlogit = take(t * E * 4);
+    L.dlogit_bf = take(t * E * 2);
+    L.wg_bf = take(E * I * H * 2);
+    L.wu_bf = take(E * I * H * 2);
+    L.wd_bf = take(E * H * I * 2);
+    L.wsg_bf = take(Is * H * 2);
+    L.wsu_bf = take(Is * H * 2);
+    L.wsd_bf = take(H * Is * 2);
+    L.wr_bf = take(E * H * 2);
+    L.xhat = take(t * H * 2);
+    L.xhat_perm = take(R * H * 2);
+    L.dout_perm = take(R * H * 2);
     L.total = off;
     return L;
 }
@@ -573,14 +552,18 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
     const int T = a.T, H = c.hidden, I = c.moe_inter, E = c.n_routed, k = c.top_k;
     const int Is = c.n_shared * c.moe_inter;
     const bool sh = Is > 0;
+    const int R = T * k;
     const BwdLayout L = bwd_layout(c, T);
     auto at = [&](size_t o) { return static_cast<uint8_t*>(ws) + o; };
+    auto bf = [&](size_t o) { return reinterpret_cast<__nv_bfloat16*>(at(o)); };
+    auto f32 = [&](size_t o) { return reinterpret_cast<float*>(at(o)); };
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(L.ctrl));
     int32_t* perm_src = reinterpret_cast<int32_t*>(at(L.perm_src));
     int32_t* inv_pos = reinterpret_cast<int32_t*>(at(L.inv_pos));
     MTile* mtiles = reinterpret_cast<MTile*>(at(L.mtiles));
     uint8_t* xq = at(L.xq);
-    float* xs = reinterpret_cast<float*>(at(L.xs));
+    float* xs = f32(L.xs);
+    const __nv_bfloat16* dout = static_cast<const __nv_bfloat16*>(a.dout);
     cudaError_t e;
 #define BWD_TRY(x)                             \
     do {                                       \
@@ -593,11 +576,10 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
     };
     BWD_TRY(mark(MOE_STAGE_ROUTE, true));
 
-    // forward quantities: activation codes, the router's logits, the permutation, g and u
+    // ---- forward quantities: activation codes, the router's logits, the permutation, g and u
     BWD_TRY(launch_quant_act(a.x, T, H, xq, xs, NormArgs{}, st));
     BWD_TRY(launch_route_large(c, a.x, T, a.W->w_router, a.W->router_bias, reinterpret_cast<int32_t*>(at(L.ids)),
-                               reinterpret_cast<float*>(at(L.w)), reinterpret_cast<float*>(at(L.logits)), L.splits,
-                               NormArgs{}, st));
+                               f32(L.w), f32(L.logits), L.splits, NormArgs{}, st));
     BWD_TRY(launch_permute(c, a.topk_ids, T, reinterpret_cast<int32_t*>(at(L.offsets)), perm_src, inv_pos, nullptr,
                            nullptr, mtiles, reinterpret_cast<int32_t*>(at(L.perm_hist)), ctrl, st));
     BWD_TRY(launch_gather_rows(T, H, k, perm_src, xq, at(L.xq_perm), &ctrl->status, st));
@@ -622,13 +604,13 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         g.s_up = a.W->s_up;
         g.ss_gate = a.W->ss_gate;
         g.ss_up = a.W->ss_up;
-        g.g_out_r = reinterpret_cast<float*>(at(L.g_r));
-        g.u_out_r = reinterpret_cast<float*>(at(L.u_r));
-        g.g_out_s = reinterpret_cast<float*>(at(L.g_s));
-        g.u_out_s = reinterpret_cast<float*>(at(L.u_s));
+        g.g_out_r = f32(L.g_r);
+        g.u_out_r = f32(L.u_r);
+        g.g_out_s = f32(L.g_s);
+        g.u_out_s = f32(L.u_s);
         g.status = &ctrl->status;
         TmaMaps m = {};
-        if (!tmap_u8_2d(&m.a_r, at(L.xq_perm), (uint64_t)T * k, H, 128, 128) ||
+        if (!tmap_u8_2d(&m.a_r, at(L.xq_perm), (uint64_t)R, H, 128, 128) ||
             !tmap_u8_2d(&m.b0_r, a.W->w_gate, (uint64_t)E * I, H, 128, 128) ||
             !tmap_u8_2d(&m.b1_r, a.W->w_up, (uint64_t)E * I, H, 128, 128))
             return cudaErrorInvalidValue;
@@ -637,84 +619,90 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
             return cudaErrorInvalidValue;
         BWD_TRY(launch_expert_gemm(g, m, st));
     }
+    // ---- bf16 operands of the contractions: weights dequantised, xhat, gathered rows
+    const long EIH = (long)E * I * H;
+    dequant_bf16_kernel<<<grid_for(EIH, 16), 256, 0, st>>>(a.W->w_gate, a.W->s_gate, E, I, H, bf(L.wg_bf));
+    dequant_bf16_kernel<<<grid_for(EIH, 16), 256, 0, st>>>(a.W->w_up, a.W->s_up, E, I, H, bf(L.wu_bf));
+    dequant_bf16_kernel<<<grid_for(EIH, 16), 256, 0, st>>>(a.W->w_down, a.W->s_down, E, H, I, bf(L.wd_bf));
+    if (sh) {
+        const long sIH = (long)Is * H;
+        dequant_bf16_kernel<<<grid_for(sIH, 16), 256, 0, st>>>(a.W->ws_gate, a.W->ss_gate, 1, Is, H, bf(L.wsg_bf));
+        dequant_bf16_kernel<<<grid_for(sIH, 16), 256, 0, st>>>(a.W->ws_up, a.W->ss_up, 1, Is, H, bf(L.wsu_bf));
+        dequant_bf16_kernel<<<grid_for(sIH, 16), 256, 0, st>>>(a.W->ws_down, a.W->ss_down, 1, H, Is, bf(L.wsd_bf));
+    }
+    f32_to_bf16_kernel<<<grid_for((long)E * H, 2), 256, 0, st>>>(a.W->w_router, (long)E * H, bf(L.wr_bf));
+    xhat_kernel<<<grid_for((long)T * H, 16), 256, 0, st>>>(xq, xs, T, H, bf(L.xhat));
+    gather_bf16_kernel<<<cdiv(R, 8), 256, 0, st>>>(bf(L.xhat), H, perm_src, k, R, bf(L.xhat_perm));
+    gather_bf16_kernel<<<cdiv(R, 8), 256, 0, st>>>(dout, H, perm_src, k, R, bf(L.dout_perm));
+    BWD_TRY(cudaGetLastError());
     BWD_TRY(mark(MOE_STAGE_ROUTE, false));
     BWD_TRY(mark(MOE_STAGE_PERMUTE, true));
 
-    BwdGemm b = {};
-    b.T = T;
-    b.k = k;
-    b.E = E;
-    b.H = H;
-    b.perm_src = perm_src;
+    Gemm b = {};
     b.mtiles = mtiles;
     b.ctrl = ctrl;
     b.offsets = reinterpret_cast<int32_t*>(at(L.offsets));
-    b.dout = static_cast<const __nv_bfloat16*>(a.dout);
-    b.topk_w = a.topk_w;
-    b.x = static_cast<const __nv_bfloat16*>(a.x);
-    b.xq = xq;
-    b.xs = xs;
-    b.wr = a.W->w_router;
-    b.dlogit = reinterpret_cast<float*>(at(L.dlogit));
     const unsigned mt_grid = (unsigned)L.max_mtiles;
 
-    // dau = Wd^T dout (routed rows, then the shared experts' tokens)
-    BwdGemm d = b;
-    d.routed = 1;
-    d.grouping = 1;
-    d.Iw = I;
-    d.N = I;
-    d.K = H;
-    d.w0 = a.W->w_down;
-    d.s0 = a.W->s_down;
-    d.w_estride = (size_t)H * I;
-    d.s_estride = (size_t)(H / 128) * (I / 128);
-    d.c0 = reinterpret_cast<float*>(at(L.dau_r));
-    BWD_TRY(run_gemm<F_DDOWN>(d, dim3(mt_grid, cdiv(I, kBN)), st));
-    if (sh) {
-        BwdGemm ds = b;
-        ds.routed = 0;
-        ds.grouping = 0;
-        ds.Iw = Is;
-        ds.M = T;
-        ds.N = Is;
-        ds.K = H;
-        ds.w0 = a.W->ws_down;
-        ds.s0 = a.W->ss_down;
-        ds.c0 = reinterpret_cast<float*>(at(L.dau_s));
-        // a single group: the tile's rows are tokens m0 + m (row0 stays 0, m0 from blockIdx.x)
-        BWD_TRY(run_gemm<F_DDOWN>(ds, dim3(cdiv(T, kBM), cdiv(Is, kBN)), st));
+    // ---- dau = Wd^T dout: routed rows (tiles of the permutation), then the shared experts
+    {
+        Gemm d = b;
+        d.grouping = 1;
+        d.N = I;
+        d.K = H;
+        d.A = bf(L.dout_perm);
+        d.lda = H;
+        d.B = bf(L.wd_bf);
+        d.ldb = I;
+        d.b_estride = (size_t)H * I;
+        d.C = f32(L.dau_r);
+        d.ldc = I;
+        BWD_TRY(run_gemm<false>(d, dim3(mt_grid, cdiv(I, kBN)), st));
+        if (sh) {
+            Gemm ds = b;
+            ds.grouping = 0;
+            ds.M = T;
+            ds.N = Is;
+            ds.K = H;
+            ds.A = dout;
+            ds.lda = H;
+            ds.B = bf(L.wsd_bf);
+            ds.ldb = Is;
+            ds.C = f32(L.dau_s);
+            ds.ldc = Is;
+            BWD_TRY(run_gemm<false>(ds, dim3(cdiv(T, kBM), cdiv(Is, kBN)), st));
+        }
     }
-    // SwiGLU backward: ahat, dgu, dw
+    // ---- SwiGLU backward: w ahat, dgu, dw
     {
         SwigluBwd s;
-        s.rows = T * k;
+        s.rows = R;
         s.Iw = I;
         s.routed = 1;
-        s.g = reinterpret_cast<float*>(at(L.g_r));
-        s.u = reinterpret_cast<float*>(at(L.u_r));
-        s.dau = reinterpret_cast<float*>(at(L.dau_r));
+        s.g = f32(L.g_r);
+        s.u = f32(L.u_r);
+        s.dau = f32(L.dau_r);
         s.perm_src = perm_src;
         s.topk_w = a.topk_w;
-        s.ahat = reinterpret_cast<__nv_bfloat16*>(at(L.ahat_r));
-        s.dgu = reinterpret_cast<__nv_bfloat16*>(at(L.dgu_r));
-        s.dw = reinterpret_cast<float*>(at(L.dw));
+        s.wahat = bf(L.wahat_r);
+        s.dgu = bf(L.dgu_r);
+        s.dw = f32(L.dw);
         swiglu_bwd_kernel<<<cdiv(s.rows, 8), 256, 0, st>>>(s);
         BWD_TRY(cudaGetLastError());
         if (sh) {
             s.rows = T;
             s.Iw = Is;
             s.routed = 0;
-            s.g = reinterpret_cast<float*>(at(L.g_s));
-            s.u = reinterpret_cast<float*>(at(L.u_s));
-            s.dau = reinterpret_cast<float*>(at(L.dau_s));
-            s.ahat = reinterpret_cast<__nv_bfloat16*>(at(L.ahat_s));
-            s.dgu = reinterpret_cast<__nv_bfloat16*>(at(L.dgu_s));
+            s.g = f32(L.g_s);
+            s.u = f32(L.u_s);
+            s.dau = f32(L.dau_s);
+            s.wahat = bf(L.wahat_s);
+            s.dgu = bf(L.dgu_s);
             swiglu_bwd_kernel<<<cdiv(s.rows, 8), 256, 0, st>>>(s);
             BWD_TRY(cudaGetLastError());
         }
     }
-    // router: dlogit, dbias
+    // ---- router: dlogit, dbias
     {
         RouterBwd r;
         r.T = T;
@@ -722,122 +710,142 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         r.k = k;
         r.splits = L.splits;
         r.scale = c.routed_scaling_factor;
-        r.part = reinterpret_cast<float*>(at(L.logits));
+        r.part = f32(L.logits);
         r.bias = a.W->router_bias;
         r.ids = a.topk_ids;
-        r.dw = reinterpret_cast<float*>(at(L.dw));
-        r.dlogit = reinterpret_cast<float*>(at(L.dlogit));
+        r.dw = f32(L.dw);
+        r.dlogit = f32(L.dlogit);
+        r.dlogit_bf = bf(L.dlogit_bf);
         router_bwd_kernel<<<cdiv(T, 8), 256, 0, st>>>(r);
         BWD_TRY(cudaGetLastError());
         if (a.dbias) {
-            dbias_kernel<<<cdiv(E, 32), 1024, 0, st>>>(T, E, b.dlogit, a.dbias);
+            dbias_kernel<<<cdiv(E, 32), 1024, 0, st>>>(T, E, f32(L.dlogit), a.dbias);
             BWD_TRY(cudaGetLastError());
         }
     }
     BWD_TRY(mark(MOE_STAGE_PERMUTE, false));
-    // dx: router term, then the routed rows and the shared experts
+    // ---- dx: router term, then the routed rows and the shared experts, then their sum
     {
         BWD_TRY(mark(MOE_STAGE_COMBINE, true));
-        BwdGemm x = b;
+        Gemm x = b;
         x.grouping = 0;
         x.M = T;
         x.N = H;
         x.K = E;
-        x.c0 = a.dx;
-        BWD_TRY(run_gemm<F_DXR>(x, dim3(cdiv(T, kBM), cdiv(H, kBN)), st));
-        BwdGemm g = b;
-        g.routed = 1;
+        x.A = bf(L.dlogit_bf);
+        x.lda = E;
+        x.B = bf(L.wr_bf);
+        x.ldb = H;
+        x.C = a.dx;
+        x.ldc = H;
+        BWD_TRY(run_gemm<false>(x, dim3(cdiv(T, kBM), cdiv(H, kBN)), st));
+        Gemm g = b;
         g.grouping = 1;
-        g.Iw = I;
         g.N = H;
         g.K = 2 * I;
-        g.dgu = reinterpret_cast<__nv_bfloat16*>(at(L.dgu_r));
-        g.w0 = a.W->w_gate;
-        g.w1 = a.W->w_up;
-        g.s0 = a.W->s_gate;
-        g.s1 = a.W->s_up;
-        g.w_estride = (size_t)I * H;
-        g.s_estride = (size_t)(I / 128) * (H / 128);
-        g.c0 = reinterpret_cast<float*>(at(L.dx_perm));
+        g.A = bf(L.dgu_r);
+        g.lda = 2 * I;
+        g.B = bf(L.wg_bf);
+        g.B2 = bf(L.wu_bf);
+        g.ksplit = I;
+        g.ldb = H;
+        g.b_estride = (size_t)I * H;
+        g.C = f32(L.dx_perm);
+        g.ldc = H;
         BWD_TRY(mark(MOE_STAGE_GATE_UP, true));
-        BWD_TRY(run_gemm<F_DGU>(g, dim3(mt_grid, cdiv(H, kBN)), st));
+        BWD_TRY(run_gemm<false>(g, dim3(mt_grid, cdiv(H, kBN)), st));
         BWD_TRY(mark(MOE_STAGE_GATE_UP, false));
         if (sh) {
-            BwdGemm gs = b;
-            gs.routed = 0;
+            Gemm gs = b;
             gs.grouping = 0;
-            gs.Iw = Is;
             gs.M = T;
             gs.N = H;
             gs.K = 2 * Is;
-            gs.dgu = reinterpret_cast<__nv_bfloat16*>(at(L.dgu_s));
-            gs.w0 = a.W->ws_gate;
-            gs.w1 = a.W->ws_up;
-            gs.s0 = a.W->ss_gate;
-            gs.s1 = a.W->ss_up;
-            gs.c0 = reinterpret_cast<float*>(at(L.dx_s));
-            BWD_TRY(run_gemm<F_DGU>(gs, dim3(cdiv(T, kBM), cdiv(H, kBN)), st));
+            gs.A = bf(L.dgu_s);
+            gs.lda = 2 * Is;
+            gs.B = bf(L.wsg_bf);
+            gs.B2 = bf(L.wsu_bf);
+            gs.ksplit = Is;
+            gs.ldb = H;
+            gs.C = f32(L.dx_s);
+            gs.ldc = H;
+            BWD_TRY(run_gemm<false>(gs, dim3(cdiv(T, kBM), cdiv(H, kBN)), st));
         }
         const long n4 = (long)T * (H / 4);
-        dx_combine_kernel<<<cdiv(n4, 256), 256, 0, st>>>(T, H, k, inv_pos, reinterpret_cast<float*>(at(L.dx_perm)),
-                                                        sh ? reinterpret_cast<float*>(at(L.dx_s)) : nullptr, a.dx);
+        dx_combine_kernel<<<cdiv(n4, 256), 256, 0, st>>>(T, H, k, inv_pos, f32(L.dx_perm), sh ? f32(L.dx_s) : nullptr,
+                                                        a.dx);
         BWD_TRY(cudaGetLastError());
         BWD_TRY(mark(MOE_STAGE_COMBINE, false));
     }
+    // ---- weight gradients: down, gate/up (routed per expert, shared over all tokens), router
     BWD_TRY(mark(MOE_STAGE_DOWN, true));
-    // weight gradients: down, gate/up (routed per expert, shared over all tokens), router
     {
-        BwdGemm w = b;
-        w.routed = 1;
+        Gemm w = b;  // dWd_e[h, i] = sum_r dout_perm[r, h] wahat[r, i]
         w.grouping = 2;
-        w.Iw = I;
         w.M = H;
         w.N = I;
-        w.ahat = reinterpret_cast<__nv_bfloat16*>(at(L.ahat_r));
-        w.c0 = a.dw_down;
+        w.A = bf(L.dout_perm);
+        w.lda = H;
+        w.B = bf(L.wahat_r);
+        w.ldb = I;
+        w.C = a.dw_down;
+        w.ldc = I;
         w.c_estride = (size_t)H * I;
-        BWD_TRY(run_gemm<F_WDOWN>(w, dim3(cdiv(I, kBN), cdiv(H, kBM), E), st));
-        BwdGemm u = b;
-        u.routed = 1;
+        BWD_TRY(run_gemm<true>(w, dim3(cdiv(I, kBN), cdiv(H, kBM), E), st));
+        Gemm u = b;  // [dWg_e; dWu_e][i, h] = sum_r dgu[r, i] xhat_perm[r, h]
         u.grouping = 2;
-        u.Iw = I;
         u.M = 2 * I;
         u.N = H;
-        u.dgu = reinterpret_cast<__nv_bfloat16*>(at(L.dgu_r));
-        u.c0 = a.dw_gate;
-        u.c1 = a.dw_up;
+        u.A = bf(L.dgu_r);
+        u.lda = 2 * I;
+        u.B = bf(L.xhat_perm);
+        u.ldb = H;
+        u.C = a.dw_gate;
+        u.C2 = a.dw_up;
+        u.msplit = I;
+        u.ldc = H;
         u.c_estride = (size_t)I * H;
-        BWD_TRY(run_gemm<F_WGU>(u, dim3(cdiv(H, kBN), cdiv(2 * I, kBM), E), st));
+        BWD_TRY(run_gemm<true>(u, dim3(cdiv(H, kBN), cdiv(2 * I, kBM), E), st));
         if (sh) {
-            BwdGemm ws_ = b;
-            ws_.routed = 0;
-            ws_.grouping = 0;
-            ws_.Iw = Is;
-            ws_.M = H;
-            ws_.N = Is;
-            ws_.K = T;
-            ws_.ahat = reinterpret_cast<__nv_bfloat16*>(at(L.ahat_s));
-            ws_.c0 = a.dws_down;
-            BWD_TRY(run_gemm<F_WDOWN>(ws_, dim3(cdiv(Is, kBN), cdiv(H, kBM), 1), st));
-            BwdGemm us = b;
-            us.routed = 0;
-            us.grouping = 0;
-            us.Iw = Is;
-            us.M = 2 * Is;
-            us.N = H;
-            us.K = T;
-            us.dgu = reinterpret_cast<__nv_bfloat16*>(at(L.dgu_s));
-            us.c0 = a.dws_gate;
-            us.c1 = a.dws_up;
-            BWD_TRY(run_gemm<F_WGU>(us, dim3(cdiv(H, kBN), cdiv(2 * Is, kBM), 1), st));
+            Gemm wsd = b;
+            wsd.grouping = 0;
+            wsd.M = H;
+            wsd.N = Is;
+            wsd.K = T;
+            wsd.A = dout;
+            wsd.lda = H;
+            wsd.B = bf(L.wahat_s);
+            wsd.ldb = Is;
+            wsd.C = a.dws_down;
+            wsd.ldc = Is;
+            BWD_TRY(run_gemm<true>(wsd, dim3(cdiv(Is, kBN), cdiv(H, kBM), 1), st));
+            Gemm wsu = b;
+            wsu.grouping = 0;
+            wsu.M = 2 * Is;
+            wsu.N = H;
+            wsu.K = T;
+            wsu.A = bf(L.dgu_s);
+            wsu.lda = 2 * Is;
+            wsu.B = bf(L.xhat);
+            wsu.ldb = H;
+            wsu.C = a.dws_gate;
+            wsu.C2 = a.dws_up;
+            wsu.msplit = Is;
+            wsu.ldc = H;
+            BWD_TRY(run_gemm<true>(wsu, dim3(cdiv(H, kBN), cdiv(2 * Is, kBM), 1), st));
         }
-        BwdGemm r = b;
+        Gemm r = b;  // dWr[e, h] = sum_t dlogit[t, e] x[t, h]
         r.grouping = 0;
         r.M = E;
         r.N = H;
         r.K = T;
-        r.c0 = a.dw_router;
-        BWD_TRY(run_gemm<F_WR>(r, dim3(cdiv(H, kBN), cdiv(E, kBM), 1), st));
+        r.A = bf(L.dlogit_bf);
+        r.lda = E;
+        r.B = static_cast<const __nv_bfloat16*>(a.x);
+        r.ldb = H;
+        r.C = a.dw_router;
+        r.ldc = H;
+        BWD_TRY(run_gemm<true>(r, dim3(cdiv(H, kBN), cdiv(E, kBM), 1), st));
     }
     BWD_TRY(mark(MOE_STAGE_DOWN, false));
 #undef BWD_TRY

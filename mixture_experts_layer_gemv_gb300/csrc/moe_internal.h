@@ -230,9 +230,11 @@ cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, con
 // Workspace regions of the layer backward (byte offsets), for T tokens.
 struct BwdLayout {
     size_t ctrl, logits, ids, w, xq, xs, offsets, perm_src, inv_pos, perm_hist, mtiles, xq_perm;
-    size_t g_r, u_r, dau_r, ahat_r, dgu_r, dx_perm;  // routed rows: fp32 [R, I] x3, bf16 [R, I], [R, 2I], fp32 [R, H]
-    size_t g_s, u_s, dau_s, ahat_s, dgu_s, dx_s;     // shared experts' tokens, the same with Is
-    size_t dw, dlogit;                               // fp32 [T k], [T, E]
+    size_t g_r, u_r, dau_r, wahat_r, dgu_r, dx_perm;  // routed rows: fp32 [R, I] x3, bf16 [R, I], [R, 2I], fp32 [R, H]
+    size_t g_s, u_s, dau_s, wahat_s, dgu_s, dx_s;     // shared experts' tokens, the same with Is
+    size_t dw, dlogit, dlogit_bf;                     // fp32 [T k], fp32 and bf16 [T, E]
+    size_t wg_bf, wu_bf, wd_bf, wsg_bf, wsu_bf, wsd_bf, wr_bf;  // bf16 weights (dequantised FP8; router)
+    size_t xhat, xhat_perm, dout_perm;                // bf16 [T, H], [R, H], [R, H]
     size_t total;
     int splits, max_mtiles;
 };
