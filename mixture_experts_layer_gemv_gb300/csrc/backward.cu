@@ -270,6 +270,43 @@ __global__ void __launch_bounds__(256) dequant_bf16_kernel(const uint8_t* q, con
     }
 }
 
+// Transposed dequantisation for the tcgen05 dgrad operands: for each of nmat matrices
+// q [R, Cc] of E4M3 codes (fp32 scales per 128 x 128 block), out[c, col0 + r] =
+// bf16(dec(q[r, c]) * scale) in an output matrix [Cc, out_ld]. 64 x 64 tiles through
+// shared memory: reads of 64-byte row pieces, writes of 128-byte row pieces.
+__global__ void __launch_bounds__(256) dequant_t_kernel(const uint8_t* q, const float* s, int R, int Cc, int out_ld,
+                                                        int col0, __nv_bfloat16* out) {
+    __shared__ __nv_bfloat16 tile[64][64 + 8];
+    const int mat = blockIdx.z, r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+    const uint8_t* qm = q + (size_t)mat * R * Cc;
+    const float* sm = s + (size_t)mat * (R / kBlk) * (Cc / kBlk);
+    {  // read: thread -> row r0 + tid/4, 16 columns from c0 + (tid%4)*16
+        const int r = threadIdx.x >> 2, c = (threadIdx.x & 3) * 16;
+        const uint4 v = *reinterpret_cast<const uint4*>(qm + (size_t)(r0 + r) * Cc + c0 + c);
+        const float sc = sm[(size_t)((r0 + r) / kBlk) * (Cc / kBlk) + (c0 + c) / kBlk];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f01 = __half22float2(
+                __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFF), __NV_E4M3)));
+            const float2 f23 = __half22float2(
+                __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3)));
+            tile[c + 4 * i][r] = __float2bfloat16_rn(f01.x * sc);
+            tile[c + 4 * i + 1][r] = __float2bfloat16_rn(f01.y * sc);
+            tile[c + 4 * i + 2][r] = __float2bfloat16_rn(f23.x * sc);
+            tile[c + 4 * i + 3][r] = __float2bfloat16_rn(f23.y * sc);
+        }
+    }
+    __syncthreads();
+    {  // write: thread -> output row c0 + tid/4, 16 values from r0 + (tid%4)*16
+        const int c = threadIdx.x >> 2, r = (threadIdx.x & 3) * 16;
+        const uint4* src = reinterpret_cast<const uint4*>(&tile[c][r]);
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)mat * Cc * out_ld + (size_t)(c0 + c) * out_ld + col0 + r0 + r);
+        dst[0] = src[0];
+        dst[1] = src[1];
+    }
+}
+
 // xhat[t, :] = dec(xq[t, :]) * xs[t, block] in bf16 (exact: a 3-bit significand times 2^k).
 __global__ void __launch_bounds__(256) xhat_kernel(const uint8_t* xq, const float* xs, long T, int H,
                                                    __nv_bfloat16* out) {
@@ -533,12 +570,10 @@ BwdLayout bwd_layout(const moe_config_t& c, int64_t T) {
     L.dw = take(R * 4);
     L.dlogit = take(t * E * 4);
     L.dlogit_bf = take(t * E * 2);
-    L.wg_bf = take(E * I * H * 2);
-    L.wu_bf = take(E * I * H * 2);
-    L.wd_bf = take(E * H * I * 2);
-    L.wsg_bf = take(Is * H * 2);
-    L.wsu_bf = take(Is * H * 2);
-    L.wsd_bf = take(H * Is * 2);
+    L.wdT = take(E * I * H * 2);
+    L.wguT = take(E * H * 2 * I * 2);
+    L.wsdT = take(Is * H * 2);
+    L.wsguT = take(H * 2 * Is * 2);
     L.wr_bf = take(E * H * 2);
     L.xhat = take(t * H * 2);
     L.xhat_perm = take(R * H * 2);
@@ -620,15 +655,18 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         BWD_TRY(launch_expert_gemm(g, m, st));
     }
     // ---- bf16 operands of the contractions: weights dequantised, xhat, gathered rows
-    const long EIH = (long)E * I * H;
-    dequant_bf16_kernel<<<grid_for(EIH, 16), 256, 0, st>>>(a.W->w_gate, a.W->s_gate, E, I, H, bf(L.wg_bf));
-    dequant_bf16_kernel<<<grid_for(EIH, 16), 256, 0, st>>>(a.W->w_up, a.W->s_up, E, I, H, bf(L.wu_bf));
-    dequant_bf16_kernel<<<grid_for(EIH, 16), 256, 0, st>>>(a.W->w_down, a.W->s_down, E, H, I, bf(L.wd_bf));
+    // weights, dequantised and transposed for the tcgen05 dgrad (K contiguous):
+    //   WdT [E][I][H] (dau = dout Wd), WguT [E][H][2I] ([Wg; Wu] stacked along K for dx)
+    dequant_t_kernel<<<dim3(I / 64, H / 64, E), 256, 0, st>>>(a.W->w_down, a.W->s_down, H, I, H, 0, bf(L.wdT));
+    dequant_t_kernel<<<dim3(H / 64, I / 64, E), 256, 0, st>>>(a.W->w_gate, a.W->s_gate, I, H, 2 * I, 0, bf(L.wguT));
+    dequant_t_kernel<<<dim3(H / 64, I / 64, E), 256, 0, st>>>(a.W->w_up, a.W->s_up, I, H, 2 * I, I, bf(L.wguT));
     if (sh) {
-        const long sIH = (long)Is * H;
-        dequant_bf16_kernel<<<grid_for(sIH, 16), 256, 0, st>>>(a.W->ws_gate, a.W->ss_gate, 1, Is, H, bf(L.wsg_bf));
-        dequant_bf16_kernel<<<grid_for(sIH, 16), 256, 0, st>>>(a.W->ws_up, a.W->ss_up, 1, Is, H, bf(L.wsu_bf));
-        dequant_bf16_kernel<<<grid_for(sIH, 16), 256, 0, st>>>(a.W->ws_down, a.W->ss_down, 1, H, Is, bf(L.wsd_bf));
+        dequant_t_kernel<<<dim3(Is / 64, H / 64, 1), 256, 0, st>>>(a.W->ws_down, a.W->ss_down, H, Is, H, 0,
+                                                                 bf(L.wsdT));
+        dequant_t_kernel<<<dim3(H / 64, Is / 64, 1), 256, 0, st>>>(a.W->ws_gate, a.W->ss_gate, Is, H, 2 * Is, 0,
+                                                                 bf(L.wsguT));
+        dequant_t_kernel<<<dim3(H / 64, Is / 64, 1), 256, 0, st>>>(a.W->ws_up, a.W->ss_up, Is, H, 2 * Is, Is,
+                                                                 bf(L.wsguT));
     }
     f32_to_bf16_kernel<<<grid_for((long)E * H, 2), 256, 0, st>>>(a.W->w_router, (long)E * H, bf(L.wr_bf));
     xhat_kernel<<<grid_for((long)T * H, 16), 256, 0, st>>>(xq, xs, T, H, bf(L.xhat));
@@ -645,34 +683,11 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
     const unsigned mt_grid = (unsigned)L.max_mtiles;
 
     // ---- dau = Wd^T dout: routed rows (tiles of the permutation), then the shared experts
-    {
-        Gemm d = b;
-        d.grouping = 1;
-        d.N = I;
-        d.K = H;
-        d.A = bf(L.dout_perm);
-        d.lda = H;
-        d.B = bf(L.wd_bf);
-        d.ldb = I;
-        d.b_estride = (size_t)H * I;
-        d.C = f32(L.dau_r);
-        d.ldc = I;
-        BWD_TRY(run_gemm<false>(d, dim3(mt_grid, cdiv(I, kBN)), st));
-        if (sh) {
-            Gemm ds = b;
-            ds.grouping = 0;
-            ds.M = T;
-            ds.N = Is;
-            ds.K = H;
-            ds.A = dout;
-            ds.lda = H;
-            ds.B = bf(L.wsd_bf);
-            ds.ldb = Is;
-            ds.C = f32(L.dau_s);
-            ds.ldc = Is;
-            BWD_TRY(run_gemm<false>(ds, dim3(cdiv(T, kBM), cdiv(Is, kBN)), st));
-        }
-    }
+    BWD_TRY(launch_bwd_tc(bf(L.dout_perm), (uint64_t)R, bf(L.wdT), (uint64_t)E, H, I, 1, 0, mtiles, ctrl,
+                          f32(L.dau_r), &ctrl->status, st));
+    if (sh)
+        BWD_TRY(launch_bwd_tc(dout, (uint64_t)T, bf(L.wsdT), 1, H, Is, 0, T, mtiles, ctrl, f32(L.dau_s),
+                              &ctrl->status, st));
     // ---- SwiGLU backward: w ahat, dgu, dw
     {
         SwigluBwd s;
@@ -739,38 +754,13 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         x.C = a.dx;
         x.ldc = H;
         BWD_TRY(run_gemm<false>(x, dim3(cdiv(T, kBM), cdiv(H, kBN)), st));
-        Gemm g = b;
-        g.grouping = 1;
-        g.N = H;
-        g.K = 2 * I;
-        g.A = bf(L.dgu_r);
-        g.lda = 2 * I;
-        g.B = bf(L.wg_bf);
-        g.B2 = bf(L.wu_bf);
-        g.ksplit = I;
-        g.ldb = H;
-        g.b_estride = (size_t)I * H;
-        g.C = f32(L.dx_perm);
-        g.ldc = H;
         BWD_TRY(mark(MOE_STAGE_GATE_UP, true));
-        BWD_TRY(run_gemm<false>(g, dim3(mt_grid, cdiv(H, kBN)), st));
+        BWD_TRY(launch_bwd_tc(bf(L.dgu_r), (uint64_t)R, bf(L.wguT), (uint64_t)E, 2 * I, H, 1, 0, mtiles, ctrl,
+                              f32(L.dx_perm), &ctrl->status, st));
         BWD_TRY(mark(MOE_STAGE_GATE_UP, false));
-        if (sh) {
-            Gemm gs = b;
-            gs.grouping = 0;
-            gs.M = T;
-            gs.N = H;
-            gs.K = 2 * Is;
-            gs.A = bf(L.dgu_s);
-            gs.lda = 2 * Is;
-            gs.B = bf(L.wsg_bf);
-            gs.B2 = bf(L.wsu_bf);
-            gs.ksplit = Is;
-            gs.ldb = H;
-            gs.C = f32(L.dx_s);
-            gs.ldc = H;
-            BWD_TRY(run_gemm<false>(gs, dim3(cdiv(T, kBM), cdiv(H, kBN)), st));
-        }
+        if (sh)
+            BWD_TRY(launch_bwd_tc(bf(L.dgu_s), (uint64_t)T, bf(L.wsguT), 1, 2 * Is, H, 0, T, mtiles, ctrl,
+                                  f32(L.dx_s), &ctrl->status, st));
         const long n4 = (long)T * (H / 4);
         dx_combine_kernel<<<cdiv(n4, 256), 256, 0, st>>>(T, H, k, inv_pos, f32(L.dx_perm), sh ? f32(L.dx_s) : nullptr,
                                                         a.dx);

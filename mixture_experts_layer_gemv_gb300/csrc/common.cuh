@@ -318,6 +318,15 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D(tmem, fp32) (+)= A(smem desc) * B(smem desc)^T, bf16 inputs, one thread issues.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -433,6 +442,14 @@ __host__ __device__ constexpr uint32_t idesc_mx_f32(int M, int N, int sf_id) {
            | (1u << 23)                     // scale factors: UE8M0
            | ((uint32_t)(M >> 4) << 24)     // M / 16
            | ((uint32_t)sf_id << 29);       // A scale-factor byte
+}
+
+// Instruction descriptor of kind::f16: bf16 x bf16 -> fp32, both operands K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                        // D format fp32
+           | (1u << 7) | (1u << 10)         // A, B: bf16 (the same type for both)
+           | ((uint32_t)(N >> 3) << 17)     // N / 8
+           | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
 
 // Instruction descriptor: E4M3 x E4M3 -> fp32, both operands K-major, M x N.

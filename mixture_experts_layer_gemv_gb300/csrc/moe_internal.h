@@ -138,6 +138,8 @@ struct alignas(64) TmaMap {
 
 // 2-D tensor map of an 8-bit row-major [rows, cols] tensor with a box of
 // box_rows x box_cols bytes and 128-byte swizzle (cached per address/shape/box).
+bool tmap_bf16_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                  uint32_t box_rows);
 bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows);
 
 // Upper bound on the CTAs of the weight-streaming kernels (sizes the hand-off slots).
@@ -233,7 +235,7 @@ struct BwdLayout {
     size_t g_r, u_r, dau_r, wahat_r, dgu_r, dx_perm;  // routed rows: fp32 [R, I] x3, bf16 [R, I], [R, 2I], fp32 [R, H]
     size_t g_s, u_s, dau_s, wahat_s, dgu_s, dx_s;     // shared experts' tokens, the same with Is
     size_t dw, dlogit, dlogit_bf;                     // fp32 [T k], fp32 and bf16 [T, E]
-    size_t wg_bf, wu_bf, wd_bf, wsg_bf, wsu_bf, wsd_bf, wr_bf;  // bf16 weights (dequantised FP8; router)
+    size_t wdT, wguT, wsdT, wsguT, wr_bf;  // bf16 weights: dequantised and transposed (K contiguous); router
     size_t xhat, xhat_perm, dout_perm;                // bf16 [T, H], [R, H], [R, H]
     size_t total;
     int splits, max_mtiles;
@@ -250,6 +252,9 @@ struct BwdArgs {
     const moe_stage_events_t* ev = nullptr;  // optional: events around the parts (moe_backward_profiled)
 };
 cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, cudaStream_t st);
+// The backward's dgrad on the tcgen05 tensor cores (bwd_tc.cu): C[r, :] = A[r, :] Bt_e^T.
+cudaError_t launch_bwd_tc(const void* A, uint64_t rows_a, const void* Bt, uint64_t n_mat, int K, int N, int routed,
+                          int rows, const MTile* mtiles, const Ctrl* ctrl, float* C, int* status, cudaStream_t st);
 
 int stream_grid();
 int down_stages(int I, int Is);

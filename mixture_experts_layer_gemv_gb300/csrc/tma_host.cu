@@ -34,7 +34,7 @@ using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint64_t, uint32_t, uint32
 std::mutex g_mu;
 std::map<Key, CUtensorMap> g_cache;
 
-// kind 0: u8 with 128-byte swizzle; 1: fp32, no swizzle
+// kind 0: u8 with 128-byte swizzle; 1: fp32, no swizzle; 2: bf16 with 128-byte swizzle
 bool encode_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch_bytes, uint32_t box_cols,
                uint32_t box_rows, int kind) {
     static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "opaque map size");
@@ -56,8 +56,9 @@ bool encode_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r =
-        fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+        fn(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : kind == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+           2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           kind == 1 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     {
@@ -70,6 +71,12 @@ bool encode_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint
 }
 
 }  // namespace
+
+// bf16 [rows, cols], dense rows, 128-byte swizzle (box_cols must be 64: 128 bytes)
+bool tmap_bf16_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                  uint32_t box_rows) {
+    return encode_2d(out, base, rows, cols, cols * 2, box_cols, box_rows, 2);
+}
 
 // u8 [rows, cols], dense rows, 128-byte swizzle (box_cols must be 128)
 bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
