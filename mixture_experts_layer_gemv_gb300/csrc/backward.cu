@@ -307,6 +307,63 @@ __global__ void __launch_bounds__(256) dequant_t_kernel(const uint8_t* q, const 
     }
 }
 
+// The weight gradients' column layout: expert e's permuted rows occupy columns
+// [poff[e], poff[e] + cnt_e) of the transposed operands, poff[e] = sum over e' < e of
+// cnt_e' rounded up to 64, and the columns up to poff[e + 1] are padding (map -1).
+// One block per expert; block E - 1 also writes poff[E].
+__global__ void __launch_bounds__(256) pad_map_kernel(int E, const int32_t* offsets, int32_t* poff, int32_t* pmap) {
+    const int e = blockIdx.x;
+    int base = 0;
+    for (int i = 0; i < e; ++i) base += (offsets[i + 1] - offsets[i] + 63) & ~63;
+    const int o = offsets[e], cnt = offsets[e + 1] - o, padded = (cnt + 63) & ~63;
+    for (int j = threadIdx.x; j < padded; j += blockDim.x) pmap[base + j] = j < cnt ? o + j : -1;
+    if (threadIdx.x == 0) {
+        poff[e] = base;
+        if (e == E - 1) poff[E] = base + padded;
+    }
+}
+
+// dst[c, j] = src[row(j), c] for the columns j < ncols (ncols_dev when given, else
+// ncols), with row(j) = map[j] (or j when map is null and j < nsrc), and 0 where row(j)
+// < 0 or j >= nsrc: bf16, src [*, C] rows, dst [C, ldd]. 64 x 64 tiles through shared
+// memory; C and the column tiles multiples of 16 and 64.
+__global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16* src, int C, const int32_t* map, int nsrc,
+                                                        int ncols, const int32_t* ncols_dev, __nv_bfloat16* dst,
+                                                        long ldd) {
+    __shared__ __nv_bfloat16 tile[64][64 + 8];
+    const int j0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
+    const int nc = ncols_dev ? *ncols_dev : ncols;
+    if (j0 >= nc) return;
+    {  // read: column j0 + tid/4 (a source row), 16 channels from c0 + (tid%4)*16
+        const int jj = threadIdx.x >> 2, cc = (threadIdx.x & 3) * 16;
+        const int j = j0 + jj;
+        int row = -1;
+        if (j < nc) row = map ? map[j] : (j < nsrc ? j : -1);
+        uint4 a = make_uint4(0, 0, 0, 0), b = a;
+        if (row >= 0 && c0 + cc < C) {
+            const uint4* sp = reinterpret_cast<const uint4*>(src + (size_t)row * C + c0 + cc);
+            a = sp[0];
+            b = sp[1];
+        }
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            tile[cc + 2 * i][jj] = __ushort_as_bfloat16((unsigned short)(w[i] & 0xFFFF));
+            tile[cc + 2 * i + 1][jj] = __ushort_as_bfloat16((unsigned short)(w[i] >> 16));
+        }
+    }
+    __syncthreads();
+    {  // write: row c0 + tid/4 of dst, 16 columns from j0 + (tid%4)*16
+        const int c = threadIdx.x >> 2, jc = (threadIdx.x & 3) * 16;
+        if (c0 + c < C) {
+            const uint4* tp = reinterpret_cast<const uint4*>(&tile[c][jc]);
+            uint4* dp = reinterpret_cast<uint4*>(dst + (size_t)(c0 + c) * ldd + j0 + jc);
+            dp[0] = tp[0];
+            dp[1] = tp[1];
+        }
+    }
+}
+
 // xhat[t, :] = dec(xq[t, :]) * xs[t, block] in bf16 (exact: a 3-bit significand times 2^k).
 __global__ void __launch_bounds__(256) xhat_kernel(const uint8_t* xq, const float* xs, long T, int H,
                                                    __nv_bfloat16* out) {
@@ -578,6 +635,23 @@ BwdLayout bwd_layout(const moe_config_t& c, int64_t T) {
     L.xhat = take(t * H * 2);
     L.xhat_perm = take(R * H * 2);
     L.dout_perm = take(R * H * 2);
+    // the weight gradients' transposed operands: routed rows in padded expert segments
+    // (Rp columns), tokens padded to Tp
+    L.Rp = (int)(((R + 63) & ~size_t(63)) + 64 * E);
+    L.Tp = (int)((t + 63) & ~size_t(63));
+    const size_t Rp = (size_t)L.Rp, Tp = (size_t)L.Tp;
+    L.poff = take((E + 1) * 4);
+    L.pmap = take(Rp * 4);
+    L.dout_permT = take(H * Rp * 2);
+    L.wahatT = take(I * Rp * 2);
+    L.dguT = take(2 * I * Rp * 2);
+    L.xhat_permT = take(H * Rp * 2);
+    L.doutT = take(H * Tp * 2);
+    L.wahat_sT = take(Is * Tp * 2);
+    L.dgu_sT = take(2 * Is * Tp * 2);
+    L.xhatT = take(H * Tp * 2);
+    L.dlogitT = take(E * Tp * 2);
+    L.xT = take(H * Tp * 2);
     L.total = off;
     return L;
 }
@@ -767,75 +841,46 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         BWD_TRY(cudaGetLastError());
         BWD_TRY(mark(MOE_STAGE_COMBINE, false));
     }
-    // ---- weight gradients: down, gate/up (routed per expert, shared over all tokens), router
+    // ---- weight gradients on the tcgen05 tensor cores: dWd_e = dout_perm^T (w ahat),
+    // [dWg_e; dWu_e] = [dg | du]^T xhat_perm (routed, per expert over its padded columns),
+    // the same over tokens for the shared experts, and dWr = dlogit^T x
     BWD_TRY(mark(MOE_STAGE_DOWN, true));
     {
-        Gemm w = b;  // dWd_e[h, i] = sum_r dout_perm[r, h] wahat[r, i]
-        w.grouping = 2;
-        w.M = H;
-        w.N = I;
-        w.A = bf(L.dout_perm);
-        w.lda = H;
-        w.B = bf(L.wahat_r);
-        w.ldb = I;
-        w.C = a.dw_down;
-        w.ldc = I;
-        w.c_estride = (size_t)H * I;
-        BWD_TRY(run_gemm<true>(w, dim3(cdiv(I, kBN), cdiv(H, kBM), E), st));
-        Gemm u = b;  // [dWg_e; dWu_e][i, h] = sum_r dgu[r, i] xhat_perm[r, h]
-        u.grouping = 2;
-        u.M = 2 * I;
-        u.N = H;
-        u.A = bf(L.dgu_r);
-        u.lda = 2 * I;
-        u.B = bf(L.xhat_perm);
-        u.ldb = H;
-        u.C = a.dw_gate;
-        u.C2 = a.dw_up;
-        u.msplit = I;
-        u.ldc = H;
-        u.c_estride = (size_t)I * H;
-        BWD_TRY(run_gemm<true>(u, dim3(cdiv(H, kBN), cdiv(2 * I, kBM), E), st));
+        int32_t* poff = reinterpret_cast<int32_t*>(at(L.poff));
+        int32_t* pmap = reinterpret_cast<int32_t*>(at(L.pmap));
+        pad_map_kernel<<<E, 256, 0, st>>>(E, reinterpret_cast<int32_t*>(at(L.offsets)), poff, pmap);
+        const long Rp = L.Rp, Tp = L.Tp;
+        auto tr = [&](const __nv_bfloat16* src, int C, const int32_t* map, int nsrc, int ncols, const int32_t* ncd,
+                      size_t dst, long ldd) {
+            transpose_kernel<<<dim3(cdiv(ldd, 64), cdiv(C, 64)), 256, 0, st>>>(src, C, map, nsrc, ncols, ncd, bf(dst),
+                                                                                ldd);
+        };
+        const int32_t* nc_r = poff + E;  // the routed columns in use
+        tr(bf(L.dout_perm), H, pmap, R, 0, nc_r, L.dout_permT, Rp);
+        tr(bf(L.wahat_r), I, pmap, R, 0, nc_r, L.wahatT, Rp);
+        tr(bf(L.dgu_r), 2 * I, pmap, R, 0, nc_r, L.dguT, Rp);
+        tr(bf(L.xhat_perm), H, pmap, R, 0, nc_r, L.xhat_permT, Rp);
+        BWD_TRY(cudaGetLastError());
+        BWD_TRY(launch_bwd_tc_wgrad(bf(L.dout_permT), H, bf(L.wahatT), I, (uint64_t)Rp, poff, E, 0, a.dw_down,
+                                    nullptr, 0, (size_t)H * I, &ctrl->status, st));
+        BWD_TRY(launch_bwd_tc_wgrad(bf(L.dguT), 2 * I, bf(L.xhat_permT), H, (uint64_t)Rp, poff, E, 0, a.dw_gate,
+                                    a.dw_up, I, (size_t)I * H, &ctrl->status, st));
         if (sh) {
-            Gemm wsd = b;
-            wsd.grouping = 0;
-            wsd.M = H;
-            wsd.N = Is;
-            wsd.K = T;
-            wsd.A = dout;
-            wsd.lda = H;
-            wsd.B = bf(L.wahat_s);
-            wsd.ldb = Is;
-            wsd.C = a.dws_down;
-            wsd.ldc = Is;
-            BWD_TRY(run_gemm<true>(wsd, dim3(cdiv(Is, kBN), cdiv(H, kBM), 1), st));
-            Gemm wsu = b;
-            wsu.grouping = 0;
-            wsu.M = 2 * Is;
-            wsu.N = H;
-            wsu.K = T;
-            wsu.A = bf(L.dgu_s);
-            wsu.lda = 2 * Is;
-            wsu.B = bf(L.xhat);
-            wsu.ldb = H;
-            wsu.C = a.dws_gate;
-            wsu.C2 = a.dws_up;
-            wsu.msplit = Is;
-            wsu.ldc = H;
-            BWD_TRY(run_gemm<true>(wsu, dim3(cdiv(H, kBN), cdiv(2 * Is, kBM), 1), st));
+            tr(dout, H, nullptr, T, (int)Tp, nullptr, L.doutT, Tp);
+            tr(bf(L.wahat_s), Is, nullptr, T, (int)Tp, nullptr, L.wahat_sT, Tp);
+            tr(bf(L.dgu_s), 2 * Is, nullptr, T, (int)Tp, nullptr, L.dgu_sT, Tp);
+            tr(bf(L.xhat), H, nullptr, T, (int)Tp, nullptr, L.xhatT, Tp);
+            BWD_TRY(cudaGetLastError());
+            BWD_TRY(launch_bwd_tc_wgrad(bf(L.doutT), H, bf(L.wahat_sT), Is, (uint64_t)Tp, nullptr, 1, (int)Tp,
+                                        a.dws_down, nullptr, 0, 0, &ctrl->status, st));
+            BWD_TRY(launch_bwd_tc_wgrad(bf(L.dgu_sT), 2 * Is, bf(L.xhatT), H, (uint64_t)Tp, nullptr, 1, (int)Tp,
+                                        a.dws_gate, a.dws_up, Is, 0, &ctrl->status, st));
         }
-        Gemm r = b;  // dWr[e, h] = sum_t dlogit[t, e] x[t, h]
-        r.grouping = 0;
-        r.M = E;
-        r.N = H;
-        r.K = T;
-        r.A = bf(L.dlogit_bf);
-        r.lda = E;
-        r.B = static_cast<const __nv_bfloat16*>(a.x);
-        r.ldb = H;
-        r.C = a.dw_router;
-        r.ldc = H;
-        BWD_TRY(run_gemm<true>(r, dim3(cdiv(H, kBN), cdiv(E, kBM), 1), st));
+        tr(bf(L.dlogit_bf), E, nullptr, T, (int)Tp, nullptr, L.dlogitT, Tp);
+        tr(static_cast<const __nv_bfloat16*>(a.x), H, nullptr, T, (int)Tp, nullptr, L.xT, Tp);
+        BWD_TRY(cudaGetLastError());
+        BWD_TRY(launch_bwd_tc_wgrad(bf(L.dlogitT), E, bf(L.xT), H, (uint64_t)Tp, nullptr, 1, (int)Tp, a.dw_router,
+                                    nullptr, 0, 0, &ctrl->status, st));
     }
     BWD_TRY(mark(MOE_STAGE_DOWN, false));
 #undef BWD_TRY

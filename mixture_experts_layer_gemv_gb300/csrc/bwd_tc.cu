@@ -6,6 +6,11 @@
 // Bt_e: the expert's weights transposed and dequantised to bf16, [N, K] (K contiguous),
 //    stacked over experts as [E * N, K].
 // Used for dau = Wd^T dout (K = H, N = I) and dx_r = [Wg; Wu]^T [dg | du] (K = 2I, N = H).
+// The weight gradients use the same kernel with transposed operands: C_e[m, n] =
+// sum_j At[m, j] Bt[n, j] over an expert's columns j (its rows, laid out with each
+// expert's segment starting at a multiple of 64 and zero-padded to one, so every K block
+// is whole and every TMA offset aligned): dWd_e = (dout_perm^T)(w ahat), [dWg_e; dWu_e]
+// = (dgu^T)(xhat_perm), and over tokens for the shared experts and the router.
 //
 // Tiles of 128 rows x 256 columns; a tile's whole K accumulates in one TMEM accumulator,
 // and two accumulators (512 columns) let one tile's epilogue overlap the next tile's
@@ -35,33 +40,58 @@ constexpr int kTStage = kTSA + kTSB;
 constexpr uint32_t kTTmemCols = 512;            // two 128 x 256 fp32 accumulators
 constexpr uint32_t kTIdesc = idesc_bf16_f32(kTM, kTN);
 
+// mode 0: dgrad over the permutation's tiles; 1: dgrad over rows [0, rows); 2: wgrad per
+// expert (K range [poff[e], poff[e+1]) of the transposed operands); 3: wgrad, one group
+// with K = K (a multiple of 64).
 struct TcParams {
-    int K, N;         // reduction length, output width (Bt_e has N rows)
-    int routed;       // 1: tiles of the permutation (rows row0.., B of the tile's expert); 0: one group
-    int rows;         // rows of A in the one-group case
+    int mode;
+    int K, N;         // dgrad: reduction length and output width (Bt_e has N rows)
+    int M;            // wgrad: output rows (rows of At)
+    int rows;         // dgrad mode 1: rows of A
+    int groups;       // wgrad mode 2: experts
     const MTile* mtiles;
     const Ctrl* ctrl;
-    float* C;         // [rows, N] fp32
+    const int32_t* poff;  // wgrad mode 2: [groups + 1] padded column offsets
+    float *C, *C2;    // output rows >= msplit go to C2 (row - msplit); C2 == nullptr: none
+    int msplit;
+    long ldc;
+    size_t c_estride; // per-group stride of C and C2 (wgrad)
     int* status;
 };
 
 struct TcItem {
-    int row0, nrows, brow, ncol;
+    int row0, nrows, brow, ncol, k0, kb, e;
 };
 
-__device__ __forceinline__ TcItem tc_item(const TcParams& p, int nt_per, int item) {
+__device__ __forceinline__ TcItem tc_item(const TcParams& p, int n_mt, int nt_per, int item) {
     TcItem it;
-    const int mt = item / nt_per, nt = item % nt_per;
+    const int g = item / (n_mt * nt_per), rest = item % (n_mt * nt_per);
+    const int mt = rest / nt_per, nt = rest % nt_per;
     it.ncol = nt * kTN;
-    if (p.routed) {
+    it.e = 0;
+    it.k0 = 0;
+    if (p.mode == 0) {
         const MTile m = p.mtiles[mt];
         it.row0 = m.row0;
         it.nrows = m.nrows;
         it.brow = m.expert * p.N + it.ncol;
-    } else {
+        it.kb = p.K / kTK;
+    } else if (p.mode == 1) {
         it.row0 = mt * kTM;
         it.nrows = min(kTM, p.rows - it.row0);
         it.brow = it.ncol;
+        it.kb = p.K / kTK;
+    } else {
+        it.row0 = mt * kTM;
+        it.nrows = min(kTM, p.M - it.row0);
+        it.brow = it.ncol;
+        if (p.mode == 2) {
+            it.e = g;
+            it.k0 = p.poff[g];
+            it.kb = (p.poff[g + 1] - it.k0) / kTK;
+        } else {
+            it.kb = p.K / kTK;
+        }
     }
     return it;
 }
@@ -102,36 +132,33 @@ __global__ void __launch_bounds__(kTThreads, 1)
     pdl_launch_dependents();
 
     const int nt_per = (p.N + kTN - 1) / kTN;
-    const int n_mt = p.routed ? p.ctrl->n_mtiles : (p.rows + kTM - 1) / kTM;
-    const int n_items = n_mt * nt_per;
-    const int Kb = p.K / kTK;
-    const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const int total = my_items * Kb;
+    const int n_mt = p.mode == 0 ? p.ctrl->n_mtiles
+                   : p.mode == 1 ? (p.rows + kTM - 1) / kTM
+                                 : (p.M + kTM - 1) / kTM;
+    const int n_items = n_mt * nt_per * (p.mode == 2 ? p.groups : 1);
 
     if (warp == kTProdWarp) {
         // ----------------------------------------------------------- TMA producer
-        if (lane == 0 && total > 0) {
+        if (lane == 0 && (int)blockIdx.x < n_items) {
             prefetch_tmap(&tm_a);
             prefetch_tmap(&tm_b);
-            int n = 0, item = blockIdx.x;
-            TcItem it = tc_item(p, nt_per, item);
-            int kb = 0;
-            for (; n < total; ++n) {
-                const int s = n % kTStages;
-                if (n >= kTStages && !mbar_wait_bounded(&empty[s], ((n / kTStages) - 1) & 1)) {
-                    set_status(p.status, kStatusTimeout);
-                    break;
-                }
-                uint8_t* st = smem + s * kTStage;
-                const int x = kb * kTK;
-                mbar_arrive_expect_tx(&full[s], kTStage);
-                tma_load_2d(st, &tm_a, x, it.row0, &full[s]);
-                tma_load_2d(st + kTSA, &tm_b, x, it.brow, &full[s]);
-                tma_load_2d(st + kTSA + kTSB / 2, &tm_b, x, it.brow + kTN / 2, &full[s]);
-                if (++kb == Kb) {
-                    kb = 0;
-                    item += gridDim.x;
-                    if (item < n_items) it = tc_item(p, nt_per, item);
+            int n = 0;
+            bool stop = false;
+            for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
+                const TcItem it = tc_item(p, n_mt, nt_per, item);
+                for (int kb = 0; kb < it.kb; ++kb, ++n) {
+                    const int s = n % kTStages;
+                    if (n >= kTStages && !mbar_wait_bounded(&empty[s], ((n / kTStages) - 1) & 1)) {
+                        set_status(p.status, kStatusTimeout);
+                        stop = true;
+                        break;
+                    }
+                    uint8_t* st = smem + s * kTStage;
+                    const int x = it.k0 + kb * kTK;
+                    mbar_arrive_expect_tx(&full[s], kTStage);
+                    tma_load_2d(st, &tm_a, x, it.row0, &full[s]);
+                    tma_load_2d(st + kTSA, &tm_b, x, it.brow, &full[s]);
+                    tma_load_2d(st + kTSA + kTSB / 2, &tm_b, x, it.brow + kTN / 2, &full[s]);
                 }
             }
             // copies still in flight land before this CTA may exit
@@ -141,8 +168,9 @@ __global__ void __launch_bounds__(kTThreads, 1)
     } else if (warp == kTMmaWarp) {
         // -------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            int n = 0;
-            for (int t = 0; t < my_items; ++t) {
+            int n = 0, t = 0;
+            for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++t) {
+                const int kbs = tc_item(p, n_mt, nt_per, item).kb;
                 const int b = t & 1;
                 if (t >= 2 && !mbar_wait_bounded(&acc_empty[b], ((t >> 1) - 1) & 1)) {
                     set_status(p.status, kStatusTimeout);
@@ -150,7 +178,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 }
                 tc_fence_after();
                 bool stop = false;
-                for (int kb = 0; kb < Kb; ++kb, ++n) {
+                for (int kb = 0; kb < kbs; ++kb, ++n) {
                     const int s = n % kTStages;
                     if (!mbar_wait_bounded(&full[s], (n / kTStages) & 1)) {
                         set_status(p.status, kStatusTimeout);
@@ -168,10 +196,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     tc_commit(&empty[s]);
                 }
                 if (stop) break;
-                tc_commit(&acc_full[b]);
+                tc_commit(&acc_full[b]);  // with no K blocks (an expert without rows) it arrives at once
             }
             // every MMA issued has completed before the CTA frees tensor memory
-            if (n > 0) {
+            if (t > 0) {
                 tc_commit(fin);
                 mbar_wait_bounded(fin, 0);
             }
@@ -184,7 +212,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
         bool ok = true;
         int t = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++t) {
-            const TcItem it = tc_item(p, nt_per, item);
+            const TcItem it = tc_item(p, n_mt, nt_per, item);
             const int b = t & 1;
             if (ok && !mbar_wait_bounded(&acc_full[b], (t >> 1) & 1)) ok = false;
             ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
@@ -201,15 +229,21 @@ __global__ void __launch_bounds__(kTThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[b]);  // the tile after next may start
             if (!ok || row >= it.nrows) continue;
-            float* dst = p.C + (size_t)(it.row0 + row) * p.N + it.ncol + 128 * wg;
+            const int mrow = it.row0 + row;
+            float* crow = (p.C2 && mrow >= p.msplit)
+                              ? p.C2 + (size_t)it.e * p.c_estride + (size_t)(mrow - p.msplit) * p.ldc
+                              : p.C + (size_t)it.e * p.c_estride + (size_t)mrow * p.ldc;
+            float* dst = crow + it.ncol + 128 * wg;
             const int ncols = min(128, p.N - it.ncol - 128 * wg);
+            const bool zero = it.kb == 0;  // no K blocks: the accumulator was never written
             const float* vs[4] = {v0, v1, v2, v3};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 if (4 * c >= ncols) break;
                 const float* v = vs[c >> 3];
                 const int j = 4 * (c & 7);
-                reinterpret_cast<float4*>(dst)[c] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                reinterpret_cast<float4*>(dst)[c] =
+                    zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
             }
         }
         if (!ok) set_status(p.status, kStatusTimeout);
@@ -224,16 +258,11 @@ __global__ void __launch_bounds__(kTThreads, 1)
 
 size_t tc_smem() { return (size_t)kTStages * kTStage + 1024 + (2 * kTStages + 5) * 8 + 16; }
 
-}  // namespace
-
-// C[r, :] = A[r, :] . Bt_e^T for the rows of the permutation's tiles (routed) or rows
-// [0, rows) (one group, Bt = its only matrix). A: bf16 [rows_a, K]; Bt: bf16 [n_mat * N, K];
-// K a multiple of 64, N a multiple of 8; C: fp32 [rows, N].
-cudaError_t launch_bwd_tc(const void* A, uint64_t rows_a, const void* Bt, uint64_t n_mat, int K, int N, int routed,
-                          int rows, const MTile* mtiles, const Ctrl* ctrl, float* C, int* status, cudaStream_t st) {
+// A: bf16 [a_rows, cols], B: bf16 [b_rows, cols], both K contiguous.
+cudaError_t launch_tc(const TcParams& p, const void* A, uint64_t a_rows, uint64_t cols, const void* B, uint64_t b_rows,
+                      cudaStream_t st) {
     TmaMap ta, tb;
-    if (!tmap_bf16_2d(&ta, A, rows_a, (uint64_t)K, kTK, kTM) ||
-        !tmap_bf16_2d(&tb, Bt, n_mat * (uint64_t)N, (uint64_t)K, kTK, kTN / 2))
+    if (!tmap_bf16_2d(&ta, A, a_rows, cols, kTK, kTM) || !tmap_bf16_2d(&tb, B, b_rows, cols, kTK, kTN / 2))
         return cudaErrorInvalidValue;
     static bool smem_set = false;
     const size_t smem = tc_smem();
@@ -243,15 +272,6 @@ cudaError_t launch_bwd_tc(const void* A, uint64_t rows_a, const void* Bt, uint64
         if (e != cudaSuccess) return e;
         smem_set = true;
     }
-    TcParams p;
-    p.K = K;
-    p.N = N;
-    p.routed = routed;
-    p.rows = rows;
-    p.mtiles = mtiles;
-    p.ctrl = ctrl;
-    p.C = C;
-    p.status = status;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(num_sms(), kMaxStreamCtas));
     cfg.blockDim = dim3(kTThreads);
@@ -263,6 +283,49 @@ cudaError_t launch_bwd_tc(const void* A, uint64_t rows_a, const void* Bt, uint64
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, bwd_tc_kernel, p, ta, tb);
+}
+
+}  // namespace
+
+// dgrad: C[r, :] = A[r, :] . Bt_e^T for the rows of the permutation's tiles (routed) or rows
+// [0, rows) (one group, Bt = its only matrix). A: bf16 [rows_a, K]; Bt: bf16 [n_mat * N, K];
+// K a multiple of 64, N a multiple of 8; C: fp32 [rows, N].
+cudaError_t launch_bwd_tc(const void* A, uint64_t rows_a, const void* Bt, uint64_t n_mat, int K, int N, int routed,
+                          int rows, const MTile* mtiles, const Ctrl* ctrl, float* C, int* status, cudaStream_t st) {
+    TcParams p = {};
+    p.mode = routed ? 0 : 1;
+    p.K = K;
+    p.N = N;
+    p.rows = rows;
+    p.mtiles = mtiles;
+    p.ctrl = ctrl;
+    p.C = C;
+    p.ldc = N;
+    p.status = status;
+    return launch_tc(p, A, rows_a, (uint64_t)K, Bt, n_mat * (uint64_t)N, st);
+}
+
+// wgrad: C_g[m, n] = sum_j At[m, j] Bt[n, j] over the columns j of group g: [poff[g],
+// poff[g+1]) (poff != nullptr: groups of them, each a multiple of 64) or [0, K) (one
+// group). At: bf16 [M, cols]; Bt: bf16 [N, cols]; C_g = C + g * c_estride, [M, N] rows of
+// N (rows >= msplit to C2 when given).
+cudaError_t launch_bwd_tc_wgrad(const void* At, int M, const void* Bt, int N, uint64_t cols, const int32_t* poff,
+                                int groups, int K, float* C, float* C2, int msplit, size_t c_estride, int* status,
+                                cudaStream_t st) {
+    TcParams p = {};
+    p.mode = poff ? 2 : 3;
+    p.K = K;
+    p.N = N;
+    p.M = M;
+    p.groups = groups;
+    p.poff = poff;
+    p.C = C;
+    p.C2 = C2;
+    p.msplit = msplit;
+    p.ldc = N;
+    p.c_estride = c_estride;
+    p.status = status;
+    return launch_tc(p, At, (uint64_t)M, cols, Bt, (uint64_t)N, st);
 }
 
 }  // namespace moe

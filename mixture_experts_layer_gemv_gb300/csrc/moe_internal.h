@@ -237,6 +237,10 @@ struct BwdLayout {
     size_t dw, dlogit, dlogit_bf;                     // fp32 [T k], fp32 and bf16 [T, E]
     size_t wdT, wguT, wsdT, wsguT, wr_bf;  // bf16 weights: dequantised and transposed (K contiguous); router
     size_t xhat, xhat_perm, dout_perm;                // bf16 [T, H], [R, H], [R, H]
+    size_t poff, pmap;                                // int32 [E + 1], [Rp]: padded expert columns
+    size_t dout_permT, wahatT, dguT, xhat_permT;      // bf16 [H | I | 2I | H, Rp]
+    size_t doutT, wahat_sT, dgu_sT, xhatT, dlogitT, xT;  // bf16 [H | Is | 2Is | H | E | H, Tp]
+    int Rp, Tp;                                       // padded column counts (multiples of 64)
     size_t total;
     int splits, max_mtiles;
 };
@@ -252,7 +256,11 @@ struct BwdArgs {
     const moe_stage_events_t* ev = nullptr;  // optional: events around the parts (moe_backward_profiled)
 };
 cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, cudaStream_t st);
-// The backward's dgrad on the tcgen05 tensor cores (bwd_tc.cu): C[r, :] = A[r, :] Bt_e^T.
+// The backward's contractions on the tcgen05 tensor cores (bwd_tc.cu): dgrad C[r, :] =
+// A[r, :] Bt_e^T; wgrad C_g = At Bt^T over the columns of group g.
+cudaError_t launch_bwd_tc_wgrad(const void* At, int M, const void* Bt, int N, uint64_t cols, const int32_t* poff,
+                                int groups, int K, float* C, float* C2, int msplit, size_t c_estride, int* status,
+                                cudaStream_t st);
 cudaError_t launch_bwd_tc(const void* A, uint64_t rows_a, const void* Bt, uint64_t n_mat, int K, int N, int routed,
                           int rows, const MTile* mtiles, const Ctrl* ctrl, float* C, int* status, cudaStream_t st);
 
