@@ -19,7 +19,10 @@
 //               B boxes of 128 rows (128-byte swizzle), a 4-stage ring
 //   warp 8      MMA issuer (one thread): per K block 4 tcgen05.mma M=128 N=256 K=16
 //   warps 0-7   epilogue: warp w reads lanes 32*(w%4).. and column half w/4 of the
-//               accumulator, releases it, and stores the rows in fp32.
+//               accumulator, releases it, and stores the rows in fp32 through a per-warp
+//               shared-memory block, so that each store instruction writes 128-byte
+//               pieces of 4 rows (the weight gradients' short K makes the stores the
+//               bottleneck otherwise).
 #include <algorithm>
 
 #include "gemm_common.cuh"
@@ -106,6 +109,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     uint64_t* acc_empty = acc_full + 2;     // [2]
     uint64_t* fin = acc_empty + 2;          // the MMA warp's last commit
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(fin + 1);
+    float* s_epi = reinterpret_cast<float*>(s_tmem + 4);  // [8 warps][32 rows][33]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -207,7 +211,6 @@ __global__ void __launch_bounds__(kTThreads, 1)
     } else {
         // ---------------------------------------------------------------- epilogue
         const int q4 = warp & 3, wg = warp >> 2;
-        const int row = 32 * q4 + lane;
         const uint32_t t_row = tmem + ((uint32_t)(32 * q4) << 16);
         bool ok = true;
         int t = 0;
@@ -228,23 +231,36 @@ __global__ void __launch_bounds__(kTThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[b]);  // the tile after next may start
-            if (!ok || row >= it.nrows) continue;
-            const int mrow = it.row0 + row;
-            float* crow = (p.C2 && mrow >= p.msplit)
-                              ? p.C2 + (size_t)it.e * p.c_estride + (size_t)(mrow - p.msplit) * p.ldc
-                              : p.C + (size_t)it.e * p.c_estride + (size_t)mrow * p.ldc;
-            float* dst = crow + it.ncol + 128 * wg;
-            const int ncols = min(128, p.N - it.ncol - 128 * wg);
+            if (!ok) continue;
+            // rows 32*q4 + rr of the tile, columns ncol + 128*wg + 32*c + 4*(lane%8)..: each store
+            // instruction covers 4 rows x 128 bytes
             const bool zero = it.kb == 0;  // no K blocks: the accumulator was never written
-            const float* vs[4] = {v0, v1, v2, v3};
+            float* sb = s_epi + warp * 32 * 33;
+            const int rsub = lane >> 3, cc = (lane & 7) * 4;
+            auto put = [&](const float (&v)[32], int c) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                if (4 * c >= ncols) break;
-                const float* v = vs[c >> 3];
-                const int j = 4 * (c & 7);
-                reinterpret_cast<float4*>(dst)[c] =
-                    zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-            }
+                for (int j = 0; j < 32; ++j) sb[lane * 33 + j] = zero ? 0.f : v[j];
+                __syncwarp();
+                const int col = it.ncol + 128 * wg + 32 * c + cc;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int rr = 4 * q + rsub;
+                    const int trow = 32 * q4 + rr;
+                    if (trow < it.nrows && col < p.N) {
+                        const int mrow = it.row0 + trow;
+                        float* crow = (p.C2 && mrow >= p.msplit)
+                                          ? p.C2 + (size_t)it.e * p.c_estride + (size_t)(mrow - p.msplit) * p.ldc
+                                          : p.C + (size_t)it.e * p.c_estride + (size_t)mrow * p.ldc;
+                        const float* r = sb + rr * 33 + cc;
+                        *reinterpret_cast<float4*>(crow + col) = make_float4(r[0], r[1], r[2], r[3]);
+                    }
+                }
+                __syncwarp();
+            };
+            put(v0, 0);
+            put(v1, 1);
+            put(v2, 2);
+            put(v3, 3);
         }
         if (!ok) set_status(p.status, kStatusTimeout);
     }
@@ -256,7 +272,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
 }
 
-size_t tc_smem() { return (size_t)kTStages * kTStage + 1024 + (2 * kTStages + 5) * 8 + 16; }
+size_t tc_smem() { return (size_t)kTStages * kTStage + 1024 + (2 * kTStages + 5) * 8 + 16 + kTEpiWarps * 32 * 33 * 4; }
 
 // A: bf16 [a_rows, cols], B: bf16 [b_rows, cols], both K contiguous.
 cudaError_t launch_tc(const TcParams& p, const void* A, uint64_t a_rows, uint64_t cols, const void* B, uint64_t b_rows,
