@@ -380,20 +380,23 @@ def cpu_oracle_rate(wl, budget_s: float, weights=None, mx: bool = False):
 
 def _backward_launches(cfg) -> int:
     """Kernels per moe_backward call: the forward recompute (activation quant, router GEMM,
-    top-k, permutation count + scatter, row gather, g/u GEMM), then dgrad of down, SwiGLU,
-    router and dbias backward, router dx, dgrad of gate/up, the dx sum and the three
-    weight-gradient GEMMs (down, gate/up, router); the shared experts add five."""
-    return 17 + (5 if cfg.n_shared > 0 else 0)
+    top-k, permutation count + scatter, row gather, g/u GEMM, 7), the bf16 operands (3
+    weight dequant-transposes, router weights, xhat, two row gathers, 7), dgrad of down,
+    SwiGLU, router and dbias backward, router dx, dgrad of gate/up, the dx sum (7), and
+    the weight gradients (padded column map, 4 transposes, down and gate/up GEMMs; router:
+    2 transposes and a GEMM, 10); the shared experts add 12 (3 dequant-transposes, dgrad
+    of down and of gate/up, SwiGLU, 4 transposes, two weight-gradient GEMMs)."""
+    return 31 + (12 if cfg.n_shared > 0 else 0)
 
 
 def _backward_flops(cfg, T: int) -> dict:
     H, I, E, k, Is = cfg.hidden, cfg.moe_inter, cfg.n_routed, cfg.top_k, cfg.shared_inter
     R = T * k
-    dgrad_gu_routed = 2 * R * 2 * I * H
-    total = (2 * R * H * I + dgrad_gu_routed + 2 * R * H * I + 2 * R * 2 * I * H      # routed dgrad + wgrad
+    gu_routed = 2 * R * 2 * I * H  # the gate/up contraction of the routed rows (dgrad or wgrad)
+    total = (2 * R * H * I + gu_routed + 2 * R * H * I + gu_routed                    # routed dgrad + wgrad
              + 2 * T * (H * Is + 2 * Is * H) * 2                                       # shared dgrad + wgrad
              + 2 * 2 * T * E * H)                                                      # router dx + dWr
-    return {"dgrad_gate_up_routed": dgrad_gu_routed, "backward_bf16": total}
+    return {"wgrad_gate_up_routed": gu_routed, "backward_bf16": total}
 
 
 def cpu_oracle_backward_rate(wl, budget_s: float, weights, x, ids, w, dout):
@@ -474,8 +477,8 @@ def main_backward(args, dist, rank, world):
         routes.append((ids, w))
     ws = B.alloc_workspace_backward(cfg, T, dev)
     grads = B.alloc_grads(cfg, T, dev)
-    names = {"recompute": "route", "dgrad_down": "permute", "dgrad_gate_up_routed": "gate_up",
-             "dx_rest": "combine", "wgrad": "down"}
+    names = {"recompute_and_operands": "route", "dgrad_down_swiglu_router": "permute", "dx": "combine",
+             "wgrad": "down", "wgrad_gate_up_routed": "gate_up"}
     prof = []
     for _ in range(args.steps):
         evs = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in B.STAGES}
@@ -541,19 +544,19 @@ def main_backward(args, dist, rank, world):
     fl = _backward_flops(cfg, T)
     peaks = _peaks()
     bf16_peak = peaks["bf16_tflops"] if peaks else 1900.0
-    k_us = stages["dgrad_gate_up_routed"]
-    k_tf = fl["dgrad_gate_up_routed"] / (k_us * 1e-6) / 1e12
+    k_us = stages["wgrad_gate_up_routed"]
+    k_tf = fl["wgrad_gate_up_routed"] / (k_us * 1e-6) / 1e12
     tok_s = world * T / (ms * 1e-3)
     line = {
         "metric": metric, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 x bf16 -> f32 (g, u recomputed e4m3 x e4m3 -> f32)",
         "data": "synthetic", "config": config,
-        "roofline": {"bound": "tensor", "kernel": "bwd_gemm_kernel<1> (dgrad of gate/up, routed experts)",
+        "roofline": {"bound": "tensor", "kernel": "bwd_tc_kernel (weight gradient of gate/up, routed experts)",
                      "achieved": round(k_tf, 1), "peak": round(bf16_peak, 1), "unit": "TFLOP/s",
                      "frac": round(k_tf / bf16_peak, 4), "traffic": None,
                      "peak_source": "measured bf16 burst" if peaks else "fallback",
-                     "launch_us": k_us, "flops_per_launch": fl["dgrad_gate_up_routed"]},
+                     "launch_us": k_us, "flops_per_launch": fl["wgrad_gate_up_routed"]},
         "backward_tflops": round(fl["backward_bf16"] / (ms * 1e-3) / 1e12, 1),
         "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * cfg.hidden * 2 * 2 + T * cfg.top_k * 8,

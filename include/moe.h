@@ -292,9 +292,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const void* x_bf16, int32_t T
 
 /* moe_backward with CUDA events around its parts, in the slots of moe_stage_events_t:
  * ROUTE: the forward recompute (activation codes, router logits, permutation, row
- * gather, g and u); PERMUTE: dgrad of down, SwiGLU and router backward; GATE_UP: the
- * routed experts' dgrad of gate/up alone; COMBINE: the other dx terms and their sum;
- * DOWN: the weight gradients. */
+ * gather, g and u) and the bf16 operands (weights dequantised and transposed, xhat,
+ * gathered rows); PERMUTE: dgrad of down, SwiGLU and router backward; COMBINE: the dx
+ * terms and their sum; DOWN: the weight gradients, which contain GATE_UP: the routed
+ * experts' weight gradient of gate/up alone. */
 moe_status_t moe_backward_profiled(const moe_config_t* cfg, const void* x_bf16, int32_t T,
                                    const moe_weights_t* weights, const int32_t* topk_ids, const float* topk_w,
                                    const void* dout_bf16, float* dx, float* dw_gate, float* dw_up, float* dw_down,

@@ -828,10 +828,8 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         x.C = a.dx;
         x.ldc = H;
         BWD_TRY(run_gemm<false>(x, dim3(cdiv(T, kBM), cdiv(H, kBN)), st));
-        BWD_TRY(mark(MOE_STAGE_GATE_UP, true));
         BWD_TRY(launch_bwd_tc(bf(L.dgu_r), (uint64_t)R, bf(L.wguT), (uint64_t)E, 2 * I, H, 1, 0, mtiles, ctrl,
                               f32(L.dx_perm), &ctrl->status, st));
-        BWD_TRY(mark(MOE_STAGE_GATE_UP, false));
         if (sh)
             BWD_TRY(launch_bwd_tc(bf(L.dgu_s), (uint64_t)T, bf(L.wsguT), 1, 2 * Is, H, 0, T, mtiles, ctrl,
                                   f32(L.dx_s), &ctrl->status, st));
@@ -863,8 +861,10 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         BWD_TRY(cudaGetLastError());
         BWD_TRY(launch_bwd_tc_wgrad(bf(L.dout_permT), H, bf(L.wahatT), I, (uint64_t)Rp, poff, E, 0, a.dw_down,
                                     nullptr, 0, (size_t)H * I, &ctrl->status, st));
+        BWD_TRY(mark(MOE_STAGE_GATE_UP, true));
         BWD_TRY(launch_bwd_tc_wgrad(bf(L.dguT), 2 * I, bf(L.xhat_permT), H, (uint64_t)Rp, poff, E, 0, a.dw_gate,
                                     a.dw_up, I, (size_t)I * H, &ctrl->status, st));
+        BWD_TRY(mark(MOE_STAGE_GATE_UP, false));
         if (sh) {
             tr(dout, H, nullptr, T, (int)Tp, nullptr, L.doutT, Tp);
             tr(bf(L.wahat_s), Is, nullptr, T, (int)Tp, nullptr, L.wahat_sT, Tp);
