@@ -122,3 +122,36 @@ def test_backward_prefill_shape_sampled_tokens():
     assert abs(float(db.sum())) <= 1e-3 * float(db.abs().sum()) + 1e-6
     for k, v in g.items():
         assert bool(torch.isfinite(v).all()), k
+
+
+@pytest.mark.parametrize("name", ["dsv2_zipf_t2048", "dsv2_decode_t64"])
+def test_backward_dsv2_shape_sampled_tokens(name):
+    # E = 160 (two 128-row tiles of the router's weight gradient), I = 1536 (six 256-column
+    # tiles), two shared experts; the load-imbalance workload adds the router bias
+    wl = WORKLOADS[name]
+    cfg, T = wl.cfg, wl.T
+    W = make_weights(cfg, wl.seed, "cuda", zipf=wl.zipf_bias)
+    x = make_tokens(cfg, T, 300, "cuda")
+    ids, w = _route(cfg, x, W)
+    dout = _dout(cfg, T, 13)
+    g = B.backward(cfg, x, W, ids, w, dout)
+    torch.cuda.synchronize()
+    rows = np.unique(np.array([0, 5, T // 2, T - 1]))
+    ref = _oracle(cfg, W, x, ids, w, dout, rows=rows, dx_only=True)
+    _close("dx (sampled tokens)", g["dx"][rows].cpu().double().numpy(), ref["dx"])
+    db = g["dbias"].double()
+    assert abs(float(db.sum())) <= 1e-3 * float(db.abs().sum()) + 1e-6
+
+
+def test_backward_invalid_expert_id_is_reported_not_faulted():
+    cfg = MoEConfig(512, 256, 16, 4, 2, 4, 1.0, 1)
+    W = make_weights(cfg, 5, "cuda")
+    x = make_tokens(cfg, 16, 6, "cuda")
+    ids, w = _route(cfg, x, W)
+    ids[3, 1] = 99  # >= n_routed
+    dout = _dout(cfg, 16, 7)
+    ws = B.alloc_workspace_backward(cfg, 16)
+    g = B.alloc_grads(cfg, 16)
+    B.moe_backward(cfg, x, W, ids, w, dout, g, ws)
+    assert B.moe_read_device_status(ws) == -1  # MOE_ERR_INVALID_ARG
+    assert B.moe_read_device_status(ws) == 0
