@@ -63,6 +63,26 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     const int e = blockIdx.x;
     const int H = p.H, T = p.T, Hb = H / kBlk;
     constexpr bool norm = kNorm;
+
+    // A warp's slice of the router row (and of gamma) sits in registers, up to 8 float4
+    // per lane per chunk of 256 float4; the first chunk is loaded before the wait, since
+    // the weights do not come from the previous kernel.
+    const int slice = H / kRouteWarps;
+    const int n4 = slice / 4;  // float4 per warp slice
+    const float4* wrow = reinterpret_cast<const float4*>(p.wr + (size_t)e * H + warp * slice);
+    const uint2* grow = norm ? reinterpret_cast<const uint2*>(p.gamma + warp * slice) : nullptr;
+    float4 wv[8];
+    uint2 gv[8];
+    auto load_w = [&](int c0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = c0 + lane + 32 * j;
+            wv[j] = i < n4 ? __ldg(wrow + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[j] = norm && i < n4 ? __ldg(grow + i) : make_uint2(0, 0);
+        }
+    };
+    load_w(0);
+    const float bias_e = p.bias ? __ldg(p.bias + e) : 0.f;
     pdl_wait();  // x and the workspace are free (the previous kernel in the stream is done)
     pdl_launch_dependents();
 
@@ -76,24 +96,12 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     }
 
     // ---- N: logits[:, e], K split over the CTA's warps (H/8 is a multiple of 16).
-    // A warp's router slice sits in registers (up to 8 float4 per lane per chunk) and
-    // four tokens' activations are loaded before any FMA, so a warp waits for one
+    // Four tokens' activations are loaded before any FMA, so a warp waits for one
     // memory round trip per chunk and four tokens, not one per load.
-    const int slice = H / kRouteWarps;
-    const int n4 = slice / 4;  // float4 per warp slice
-    const float4* wrow = reinterpret_cast<const float4*>(p.wr + (size_t)e * H + warp * slice);
     for (int t = lane; t < T; t += 32) s_part[warp][t] = 0.f;
     __syncwarp();
-    const uint2* grow = norm ? reinterpret_cast<const uint2*>(p.gamma + warp * slice) : nullptr;
     for (int c0 = 0; c0 < n4; c0 += 32 * 8) {
-        float4 wv[8];
-        uint2 gv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int i = c0 + lane + 32 * j;
-            wv[j] = i < n4 ? __ldg(wrow + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            gv[j] = norm && i < n4 ? __ldg(grow + i) : make_uint2(0, 0);
-        }
+        if (c0 > 0) load_w(c0);
         for (int t = 0; t < T; t += 4) {
             uint2 xv[4][8];
 #pragma unroll
@@ -135,7 +143,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
         float l = 0.f;
 #pragma unroll
         for (int w = 0; w < kRouteWarps; ++w) l += s_part[w][t];
-        if (p.bias) l += p.bias[e];
+        if (p.bias) l += bias_e;
         p.logits[(size_t)t * p.E + e] = l;
     }
 

@@ -1,6 +1,6 @@
-// Device building blocks of expert selection shared by the router kernels
-// (route.cu) and the fused small-T layer kernel (moe_fused.cu): group-limited
-// top-k of one token by one warp, and the in-CTA counting-sort permutation.
+// Device building blocks of expert selection shared by the router kernels (route.cu):
+// group-limited top-k of one token by one warp, and the in-CTA counting-sort
+// permutation.
 #pragma once
 
 #include <climits>
@@ -137,6 +137,47 @@ __device__ inline void small_permute(const int32_t* s_ids, int n, int E, int* s_
                                      int* s_goff, int* s_rank, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
                                      RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl) {
     const int lane = threadIdx.x & 31;
+    if (n <= 32) {
+        // One warp, no CTA barrier: a slot's row is the number of slots with a smaller id
+        // plus its rank among the equal ids before it (the order of the general path
+        // below), and a row group starts at every kGroupRows-th row of an expert, so its
+        // index counts the group starts of smaller ids. The offsets come from counts.
+        if (threadIdx.x < 32) {
+            const int e = lane < n ? s_ids[lane] : INT_MAX;
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int rin = __popc(peers & ((1u << lane) - 1u));
+            const int start = lane < n && e >= 0 && rin % kGroupRows == 0;
+            int below = 0, gbelow = 0;
+            for (int j = 0; j < n; ++j) {
+                const int ej = __shfl_sync(0xffffffffu, e, j);
+                const int sj = __shfl_sync(0xffffffffu, start, j);
+                below += ej >= 0 && ej < e;
+                gbelow += (ej >= 0 && ej < e) & sj;
+            }
+            const int pos = below + rin, gi = gbelow + rin / kGroupRows;
+            if (lane < n && e >= 0) {
+                perm_src[pos] = lane;
+                inv_pos[lane] = pos;
+                group_of_row[pos] = gi;
+            }
+            if (start) {
+                RowGroup rg;
+                rg.expert = e;
+                rg.row_begin = pos;
+                rg.nrows = min(kGroupRows, __popc(peers) - rin);
+                rg.pad = 0;
+                groups[gi] = rg;
+            }
+            const int ng = __popc(__ballot_sync(0xffffffffu, start));
+            if (lane == 0) ctrl->n_routed_groups = ng;
+        }
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+            int c = 0;
+            for (int f = 0; f < n; ++f) c += s_ids[f] >= 0 && s_ids[f] < e;
+            offsets[e] = c;
+        }
+        return;
+    }
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
     __syncthreads();
     if (threadIdx.x < 32) {
