@@ -40,21 +40,21 @@ namespace {
 
 using namespace stream;
 
-// ng: routed row groups (the permutation's count)
-__device__ __forceinline__ TileSpace gateup_space(const StreamArgs& a, int ng, int P) {
-    return make_space(ng * (a.I / kTile), a.H / kBlk, a.n_shared_groups * (a.Is / kTile), a.H / kBlk, P);
+__device__ __forceinline__ TileSpace gateup_space(const StreamArgs& a, int P) {
+    return TileSpace{a.ctrl->n_routed_groups * (a.I / kTile), a.H / kBlk, a.n_shared_groups * (a.Is / kTile),
+                     a.H / kBlk, P};
 }
-__device__ __forceinline__ Plan gateup_plan(const StreamArgs& a, int ng) {
-    return make_plan(ng * (a.I / kTile), a.H / kBlk, a.n_shared_groups * (a.Is / kTile), a.H / kBlk, a.grid_gu,
-                     a.max_parts);
+__device__ __forceinline__ Plan gateup_plan(const StreamArgs& a) {
+    const TileSpace t = gateup_space(a, 1);
+    return make_plan(t.n_r, t.kc_r, t.n_s, t.kc_s, a.grid_gu, a.max_parts);
 }
-__device__ __forceinline__ TileSpace down_space(const StreamArgs& a, int ng, int P) {
+__device__ __forceinline__ TileSpace down_space(const StreamArgs& a, int P) {
     const int slices = a.H / kTile;
-    return make_space(ng * slices, a.I / kBlk, a.n_shared_groups * slices, a.Is / kBlk, P);
+    return TileSpace{a.ctrl->n_routed_groups * slices, a.I / kBlk, a.n_shared_groups * slices, a.Is / kBlk, P};
 }
-__device__ __forceinline__ Plan down_plan(const StreamArgs& a, int ng) {
-    const int slices = a.H / kTile;
-    return make_plan(ng * slices, a.I / kBlk, a.n_shared_groups * slices, a.Is / kBlk, a.grid_d, a.max_parts);
+__device__ __forceinline__ Plan down_plan(const StreamArgs& a) {
+    const TileSpace t = down_space(a, 1);
+    return make_plan(t.n_r, t.kc_r, t.n_s, t.kc_s, a.grid_d, a.max_parts);
 }
 
 __device__ __forceinline__ uint32_t ldg32(const uint8_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
@@ -109,9 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
 
     const int slices_r = a.I / kTile, slices_s = a.Is / kTile;
-    const int ng = a.ctrl->n_routed_groups;
-    const Plan pl = gateup_plan(a, ng);
-    const TileSpace ts = gateup_space(a, ng, pl.P);
+    const Plan pl = gateup_plan(a);
+    const TileSpace ts = gateup_space(a, pl.P);
     const Range rg = make_range(ts, pl.nb, blockIdx.x);
     if (blockIdx.x >= pl.nb || rg.u1 <= rg.u0) return;
     const Partials pt{{a.g_r, a.u_r}, {a.gb_r, a.ub_r}, (long)a.T * a.k, a.I};
@@ -307,9 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (this kernel's predecessor) got past its own wait; down weights depend on nothing
     // else, so the tile table is built and the producer streams weights before the
     // gate/up results exist.
-    const int ng = a.ctrl->n_routed_groups;
-    const Plan pl = down_plan(a, ng);
-    const TileSpace ts = down_space(a, ng, pl.P);
+    const Plan pl = down_plan(a);
+    const TileSpace ts = down_space(a, pl.P);
     const Range rg = make_range(ts, pl.nb, blockIdx.x);
     const bool active = blockIdx.x < pl.nb && rg.u1 > rg.u0;
     __shared__ TileRec s_tab[kMaxTab];
@@ -354,11 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    const Plan pl_gu = gateup_plan(a, ng);
     pdl_wait();  // the gate/up tiles are complete
     pdl_launch_dependents();
     if (!active) return;
 
+    const Plan pl_gu = gateup_plan(a);
     const Partials gu_r{{a.g_r, a.u_r}, {a.gb_r, a.ub_r}, (long)a.T * a.k, a.I};
     const Partials gu_s{{a.g_s, a.u_s}, {a.gb_s, a.ub_s}, (long)a.T, a.Is};
     const Partials pt{{a.y_r, nullptr}, {a.yb_r, nullptr}, (long)a.T * a.k, H};
@@ -484,11 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // rounding; or, for the stage API, the bf16 expert rows y_perm / y_shared themselves.
 // Each thread owns 4 consecutive hidden channels of one token (or one row).
 __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a) {
-    // The routing was complete before the down kernel (this kernel's predecessor) got
-    // past its own wait, so the plan and the first rows' positions are read before this
-    // kernel's wait; the down tiles are read after it.
+    pdl_wait();  // the down tiles are complete
+    pdl_launch_dependents();
     const int H = a.H;
-    const Plan pl = down_plan(a, a.ctrl->n_routed_groups);
+    const Plan pl = down_plan(a);
     const int H4 = H / 4;
     const int Tk = a.T * a.k;
     const Partials pt{{a.y_r, nullptr}, {a.yb_r, nullptr}, (long)Tk, H};
@@ -505,32 +502,18 @@ __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a)
     };
 
     if (a.fuse_combine) {
-        const int n = a.T * H4;
-        // permuted positions of slots j0..j0+7 of token tok (-1: none or out of range)
-        auto slots = [&](int tok, int j0, int (&r)[8]) {
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                r[jj] = j0 + jj < a.k ? a.inv_pos[tok * a.k + j0 + jj] : -1;
-                if ((unsigned)r[jj] >= (unsigned)Tk) r[jj] = -1;
-            }
-        };
-        const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
-        int r0[8];
-        if (i0 < n) slots(i0 / H4, 0, r0);
-        pdl_wait();  // the down tiles are complete
-        pdl_launch_dependents();
-        for (int i = i0; i < n; i += gridDim.x * blockDim.x) {
-            const int tok = i / H4, h = (i - tok * H4) * 4;
+        const long n = (long)a.T * H4;
+        for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+            const int tok = (int)(i / H4), h = (int)(i % H4) * 4;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             // up to 8 expert rows at a time: their positions, then all their loads, then
             // the sums in slot order
             for (int j0 = 0; j0 < a.k; j0 += 8) {
                 int r[8];
-                if (i == i0 && j0 == 0) {
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) r[jj] = r0[jj];
-                } else {
-                    slots(tok, j0, r);
+                for (int jj = 0; jj < 8; ++jj) {
+                    r[jj] = j0 + jj < a.k ? a.inv_pos[tok * a.k + j0 + jj] : -1;
+                    if ((unsigned)r[jj] >= (unsigned)Tk) r[jj] = -1;
                 }
                 float4 y[8];
 #pragma unroll
@@ -579,8 +562,6 @@ __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a)
             store4(a.out + (size_t)tok * H + h, v);
         }
     } else {
-        pdl_wait();  // the down tiles are complete
-        pdl_launch_dependents();
         const long nr = (long)Tk * H4, ns = a.n_shared_groups > 0 ? (long)a.T * H4 : 0;
         for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nr + ns; i += (long)gridDim.x * blockDim.x) {
             if (i < nr) {
@@ -635,15 +616,6 @@ cudaError_t set_smem(const void* fn, size_t bytes, size_t* done) {
 int stream_grid() { return std::min(num_sms(), kMaxStreamCtas); }
 
 int down_stages(int I, int Is) { return stages_down(std::max(I, Is)); }
-
-bool stream_fits(const moe_config_t& c, int64_t T) {
-    const int64_t Hb = c.hidden / kBlk, Ib = c.moe_inter / kBlk, Isb = (int64_t)c.n_shared * Ib;
-    const int64_t rows = T * c.top_k;
-    const int64_t groups = std::min<int64_t>(rows, (rows + kGroupRows - 1) / kGroupRows + c.n_routed);
-    const int64_t sgroups = c.n_shared > 0 ? (T + kGroupRows - 1) / kGroupRows : 0;
-    const int64_t U = groups * Ib * Hb + sgroups * Isb * Hb;  // most units either stage can have
-    return U < kMaxStreamUnits && T * (c.hidden / 4) < (int64_t)INT32_MAX;
-}
 
 int stream_max_parts(const moe_config_t& c, int64_t T) {
     // fewest units either streaming stage can have for T tokens, spread over the most

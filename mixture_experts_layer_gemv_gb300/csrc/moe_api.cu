@@ -629,7 +629,6 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_bf16, int32_t
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_T(cfg, T));
     if (T == 0) return MOE_OK;
-    if (!use_gemm(*cfg, T) && !stream_fits(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
     MOE_TRY(check_weights(cfg, weights, false));
     const void* req[] = {x_bf16, expert_offsets, perm_src, topk_w, y_perm_bf16};
     for (const void* p : req)
@@ -686,7 +685,6 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_T(cfg, T));
     if (T == 0) return MOE_OK;
-    if (!use_gemm(*cfg, T) && !stream_fits(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
     MOE_TRY(check_weights(cfg, weights, true));
     if (!x_bf16 || !out_bf16 || !aligned16(x_bf16) || !aligned16(out_bf16)) return MOE_ERR_INVALID_ARG;
     if ((residual_bf16 && !aligned16(residual_bf16)) || (topk_ids_out && !aligned4(topk_ids_out)))
@@ -818,7 +816,6 @@ moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16
     MOE_TRY(check_T(cfg, T));
     if (!gemm_mx_supported(*cfg)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;
-    if (T <= kSmallT && !stream_fits(*cfg, T)) return MOE_ERR_UNSUPPORTED_SHAPE;
     MOE_TRY(check_weights_mx(cfg, weights));
     if (!x_bf16 || !out_bf16 || !aligned16(x_bf16) || !aligned16(out_bf16)) return MOE_ERR_INVALID_ARG;
     if ((residual_bf16 && !aligned16(residual_bf16)) || (topk_ids_out && !aligned4(topk_ids_out)))

@@ -144,10 +144,6 @@ bool tmap_u8_2d(TmaMap* out, const void* base, uint64_t rows, uint64_t cols, uin
 
 // Upper bound on the CTAs of the weight-streaming kernels (sizes the hand-off slots).
 constexpr int kMaxStreamCtas = 512;
-// The streaming kernels index units, tiles and output elements with 32-bit integers:
-// a stage of kMaxStreamUnits units or more, or an output of 2^31 elements or more, is
-// refused (stream_fits).
-constexpr int kMaxStreamUnits = 1 << 30;
 
 constexpr size_t kCtrlRegionBytes = sizeof(Ctrl);
 
@@ -270,7 +266,6 @@ cudaError_t launch_bwd_tc(const void* A, uint64_t rows_a, const void* Bt, uint64
 
 int stream_grid();
 int down_stages(int I, int Is);
-bool stream_fits(const moe_config_t& c, int64_t T);  // within the streaming kernels' 32-bit indexing
 int stream_max_parts(const moe_config_t& c, int64_t T);  // K parts the workspace provides for
 cudaError_t launch_gateup_stream(const StreamArgs& a, const uint8_t* w_gate, const uint8_t* w_up, int E,
                                  cudaStream_t st);

@@ -52,7 +52,7 @@ struct RouteSmallParams {
 template <bool kNorm, bool kMX>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmallParams p) {
     __shared__ float s_part[kRouteWarps][kSmallT];
-    __shared__ float s_gs[kRouteWarps][kMaxE];
+    __shared__ alignas(16) float s_gs[kRouteWarps][kMaxE];
     __shared__ int32_t s_ids[kSmallT * 16];
     __shared__ int s_rank[kSmallT * 16];
     __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_gcnt[kMaxE], s_goff[kMaxE];
@@ -65,8 +65,10 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     constexpr bool norm = kNorm;
 
     // A warp's slice of the router row (and of gamma) sits in registers, up to 8 float4
-    // per lane per chunk of 256 float4; the first chunk is loaded before the wait, since
-    // the weights do not come from the previous kernel.
+    // per lane per chunk of 256 float4. Nothing is read before the wait: this is the
+    // layer's first kernel, and the one before it in the stream (the caller's) may have
+    // written any of the inputs, the weights included; its writes are visible only
+    // after the wait.
     const int slice = H / kRouteWarps;
     const int n4 = slice / 4;  // float4 per warp slice
     const float4* wrow = reinterpret_cast<const float4*>(p.wr + (size_t)e * H + warp * slice);
@@ -81,10 +83,10 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
             gv[j] = norm && i < n4 ? __ldg(grow + i) : make_uint2(0, 0);
         }
     };
+    pdl_wait();  // the previous kernel in the stream is done: inputs written, workspace free
+    pdl_launch_dependents();
     load_w(0);
     const float bias_e = p.bias ? __ldg(p.bias + e) : 0.f;
-    pdl_wait();  // x and the workspace are free (the previous kernel in the stream is done)
-    pdl_launch_dependents();
 
     // ---- M (optional): every CTA derives the same 1/rms of each token itself
     if (norm) {
@@ -181,15 +183,22 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     if (!s_last) return;
     __threadfence();
 
-    for (int t = warp; t < T; t += kRouteWarps) {
-        float lg[kMaxE / 32];
+    if (T == 1 && p.E <= (int)blockDim.x) {
+        // one token: the whole CTA ranks the experts (s_gs as scratch)
+        unsigned* scratch = reinterpret_cast<unsigned*>(&s_gs[0][0]);
+        cta_topk1(p.logits, p.E, p.G, p.Gk, p.k, p.scale, scratch, scratch + kMaxE,
+                  reinterpret_cast<float*>(scratch + kMaxE + 32), p.ids, p.w, s_ids);
+    } else {
+        for (int t = warp; t < T; t += kRouteWarps) {
+            float lg[kMaxE / 32];
 #pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i) {
-            const int ee = lane + 32 * i;
-            lg[i] = ee < p.E ? __ldcg(p.logits + (size_t)t * p.E + ee) : -INFINITY;
+            for (int i = 0; i < kMaxE / 32; ++i) {
+                const int ee = lane + 32 * i;
+                lg[i] = ee < p.E ? __ldcg(p.logits + (size_t)t * p.E + ee) : -INFINITY;
+            }
+            topk_warp(lg, p.E, p.G, p.Gk, p.k, p.scale, s_gs[warp], p.ids + (size_t)t * p.k, p.w + (size_t)t * p.k,
+                      s_ids + t * p.k);
         }
-        topk_warp(lg, p.E, p.G, p.Gk, p.k, p.scale, s_gs[warp], p.ids + (size_t)t * p.k, p.w + (size_t)t * p.k,
-                  s_ids + t * p.k);
     }
     __syncthreads();
     if (p.offsets)

@@ -98,6 +98,68 @@ __device__ inline void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, in
     __syncwarp();
 }
 
+// Inverse of float_key.
+__device__ __forceinline__ float key_float(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// The same selection and weights as topk_warp for a single token, computed by a whole
+// CTA of at least E threads (thread e holds expert e): group scores by shared-memory
+// atomicMax, the kept groups by counting the groups that beat each one, and every
+// candidate's rank by one pass over the candidates' keys (ties to the lower index), so
+// slot j holds the j-th best; no rounds of warp-wide arg-max. The softmax sum runs per
+// warp, then over the warps (another order than topk_warp's, so w may differ in the
+// last bit). Scratch: key[kMaxE] (16-byte aligned), gkey[32], part[32].
+__device__ inline void cta_topk1(const float* lg, int E, int G, int Gk, int k, float scale, unsigned* key_s,
+                                 unsigned* gkey, float* part, int32_t* ids_out, float* w_out, int32_t* ids_smem) {
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5, nw = blockDim.x >> 5;
+    const int per = E / G;
+    const float l = e < E ? __ldcg(lg + e) : -INFINITY;
+    const unsigned key = e < E ? float_key(l) : 0u;
+    if (e < 32) gkey[e] = 0u;
+    __syncthreads();
+    if (e < E) atomicMax(&gkey[e / per], key);
+    __syncthreads();
+    unsigned mkey = 0u;  // the best logit's key
+    for (int h = 0; h < G; ++h) mkey = max(mkey, gkey[h]);
+    bool cand = false;
+    if (e < E) {
+        const int g = e / per;
+        const unsigned gk = gkey[g];
+        int beaten = 0;
+        for (int h = 0; h < G; ++h) {
+            const unsigned o = gkey[h];
+            beaten += (o > gk) || (o == gk && h < g);
+        }
+        cand = beaten < Gk;
+    }
+    if (e < kMaxE) key_s[e] = cand ? key : 0u;  // a real key is never 0
+    const float mx = key_float(mkey);
+    float z = e < E ? expf(l - mx) : 0.f;
+    z = warp_sum(z);
+    if (lane == 0) part[warp] = z;
+    __syncthreads();
+    if (cand) {
+        int rank = 0;
+        const uint4* kv = reinterpret_cast<const uint4*>(key_s);
+        for (int j4 = 0; j4 < (E + 3) / 4; ++j4) {
+            const uint4 o = kv[j4];
+            const int j = 4 * j4;
+            rank += (o.x > key) || (o.x == key && j < e);
+            rank += (o.y > key) || (o.y == key && j + 1 < e);
+            rank += (o.z > key) || (o.z == key && j + 2 < e);
+            rank += (o.w > key) || (o.w == key && j + 3 < e);
+        }
+        if (rank < k) {
+            float Z = 0.f;
+            for (int w = 0; w < nw; ++w) Z += part[w];
+            ids_out[rank] = e;
+            if (ids_smem) ids_smem[rank] = e;
+            w_out[rank] = expf(l - mx) / Z * scale;
+        }
+    }
+}
+
 // Exclusive scan of n (<= 256) ints in shared memory by one warp; returns the total.
 __device__ inline int warp_exclusive_scan256(int* v, int n) {
     const int lane = threadIdx.x & 31;

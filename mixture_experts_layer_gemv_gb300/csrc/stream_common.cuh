@@ -1,12 +1,6 @@
-// Device building blocks of the weight-streaming expert kernels (expert_stream.cu):
-// unit/tile decomposition, launch plans, TMA-box dot products and the A/B partial-sum
-// buffers.
-//
-// The unit and tile arithmetic runs at the start of every CTA, on the critical path of
-// a decode step, so it is 32-bit (the host refuses stages of kMaxStreamUnits units or
-// more) and takes each part's K range from a table instead of dividing again: a 64-bit
-// division is a long dependent chain of instructions, and a tile decoded with them took
-// thousands of cycles.
+// Device building blocks of the weight-streaming expert kernels (expert_stream.cu)
+// and the fused small-T layer kernel (moe_fused.cu): unit/tile decomposition,
+// launch plans, TMA-box dot products and the A/B partial-sum buffers.
 #pragma once
 
 #include <algorithm>
@@ -30,78 +24,108 @@ constexpr int kBRows = 2048;                // the unit's activation rows (8 x k
 constexpr int kStagesGU = 5;
 constexpr int kMaxStagesD = 10;
 
-constexpr int kMaxParts = 4;
-
 // The unit sequence of a stage. Output rows come in "rows" of 128 (row group x 128-row
 // slice): n_r routed rows with kc_r K blocks each, then n_s shared rows with kc_s.
-// Each row's K blocks are split into P contiguous parts, part p holding blocks
-// [lo[p], lo[p+1]) with lo[p] = p * kc / P; a tile is one (row, part) and a unit one
-// (tile, K block). Units are ordered row-major, K block fastest.
+// Each row's K blocks are split into P contiguous parts; a tile is one (row, part) and
+// a unit one (tile, K block). Units are ordered row-major, K block fastest.
 struct TileSpace {
     int n_r, kc_r, n_s, kc_s, P;
-    int lo_r[kMaxParts + 1], lo_s[kMaxParts + 1];
-    __device__ int total() const { return n_r * kc_r + n_s * kc_s; }
-    // lo[p] of the routed (shared = 0) or shared rows, p <= P
-    __device__ __forceinline__ int lo(int shared, int p) const {
-        int v = 0;
-#pragma unroll
-        for (int q = 0; q <= kMaxParts; ++q)
-            if (q == p) v = shared ? lo_s[q] : lo_r[q];
-        return v;
+    __device__ long total() const { return (long)n_r * kc_r + (long)n_s * kc_s; }
+    __device__ int kc_of(long t) const { return t < (long)n_r * P ? kc_r : kc_s; }
+    // first K block of part p of a row with kc blocks
+    __device__ int part_lo(int kc, int p) const { return (int)((long)p * kc / P); }
+    __device__ long start(long t) const {
+        if (t < (long)n_r * P) return (t / P) * kc_r + part_lo(kc_r, (int)(t % P));
+        const long v = t - (long)n_r * P;
+        return (long)n_r * kc_r + (v / P) * kc_s + part_lo(kc_s, (int)(v % P));
     }
-    // tile of unit u; *kb receives its K block within the row
-    __device__ int tile_of(int u, int* kb) const {
-        const int shared = u >= n_r * kc_r;
-        const int v = shared ? u - n_r * kc_r : u;
-        const int kc = shared ? kc_s : kc_r;
-        const int row = v / kc, kin = v - row * kc;
-        int p = 0;
-#pragma unroll
-        for (int q = 1; q < kMaxParts; ++q)
-            if (q < P && kin >= lo(shared, q)) p = q;
+    __device__ int len(long t) const {
+        const int kc = kc_of(t), p = (int)(t % P);
+        return part_lo(kc, p + 1) - part_lo(kc, p);
+    }
+    // tile of unit u; *kb receives its absolute K block
+    __device__ long tile_of(long u, int* kb) const {
+        long row, base_t;
+        int kc, kin;
+        if (u < (long)n_r * kc_r) {
+            row = u / kc_r;
+            kin = (int)(u % kc_r);
+            kc = kc_r;
+            base_t = 0;
+        } else {
+            const long v = u - (long)n_r * kc_r;
+            row = v / kc_s;
+            kin = (int)(v % kc_s);
+            kc = kc_s;
+            base_t = (long)n_r * P;
+        }
         *kb = kin;
-        return (shared ? n_r * P : 0) + row * P + p;
+        const int p = (int)(((long)(kin + 1) * P - 1) / kc);  // part whose range holds kin
+        return base_t + row * P + p;
     }
 };
-
-__device__ __forceinline__ TileSpace make_space(int n_r, int kc_r, int n_s, int kc_s, int P) {
-    TileSpace t;
-    t.n_r = n_r;
-    t.kc_r = kc_r;
-    t.n_s = n_s;
-    t.kc_s = kc_s;
-    t.P = P;
-#pragma unroll
-    for (int q = 0; q <= kMaxParts; ++q) {
-        t.lo_r[q] = q * kc_r / P;
-        t.lo_s[q] = q * kc_s / P;
-    }
-    return t;
-}
 
 // Launch plan shared by a streaming kernel and the kernels that read its tiles: the
 // number of active CTAs and the K-part count P, so that every part fits in a range.
 struct Plan {
     int nb, P;
 };
+constexpr int kMaxParts = 4;
 __device__ __forceinline__ Plan make_plan(int n_r, int kc_r, int n_s, int kc_s, int grid, int max_parts) {
-    const int U = n_r * kc_r + n_s * kc_s;
+    const long U = (long)n_r * kc_r + (long)n_s * kc_s;
     Plan pl;
-    pl.nb = max(1, min(grid, U));
+    pl.nb = (int)std::max<long>(1, std::min<long>(grid, U));
     int kcmax = 0, kcmin = INT_MAX;  // over the kinds that have rows
     if (n_r > 0) kcmax = kcmin = kc_r;
     if (n_s > 0) {
-        kcmax = max(kcmax, kc_s);
-        kcmin = min(kcmin, kc_s);
+        kcmax = std::max(kcmax, kc_s);
+        kcmin = std::min(kcmin, kc_s);
     }
     if (kcmax == 0) kcmax = kcmin = 1;
-    const int L = max(1, U / pl.nb);
-    int P = (kcmax + L - 1) / L;
-    P = max(1, min(P, min(max_parts, kcmin)));
-    const int need = (kcmax + P - 1) / P;  // longest part
-    if (need > L) pl.nb = max(1, U / need);
+    const long L = std::max<long>(1, U / pl.nb);
+    int P = (int)((kcmax + L - 1) / L);
+    P = std::max(1, std::min(P, std::min(max_parts, kcmin)));
+    const long need = (kcmax + P - 1) / P;  // longest part
+    if (need > L) pl.nb = (int)std::max<long>(1, U / need);
     pl.P = P;
     return pl;
+}
+
+// A tile decoded: which row group, which 128-row slice of the output, which K part.
+struct TileInfo {
+    int shared;     // 1: shared experts
+    int expert;     // routed expert id (routed tiles)
+    int group;      // routed row-group index (routed tiles)
+    int row_begin;  // permuted row (routed) or token (shared) of column 0
+    int nrows;      // activation columns, <= 8
+    int slice;      // 128-row slice index within the matrix
+    int part;       // K part
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const TileSpace& ts, long t, int slices_r, int slices_s,
+                                                const RowGroup* groups, int T) {
+    TileInfo ti;
+    ti.part = (int)(t % ts.P);
+    if (t < (long)ts.n_r * ts.P) {
+        const long row = t / ts.P;
+        const int gi = (int)(row / slices_r);
+        const RowGroup rg = groups[gi];
+        ti.shared = 0;
+        ti.expert = rg.expert;
+        ti.group = gi;
+        ti.row_begin = rg.row_begin;
+        ti.nrows = rg.nrows;
+        ti.slice = (int)(row % slices_r);
+    } else {
+        const long row = (t - (long)ts.n_r * ts.P) / ts.P;
+        ti.shared = 1;
+        ti.expert = -1;
+        ti.group = -1;
+        ti.row_begin = (int)(row / slices_s) * kGroupRows;
+        ti.nrows = min(kGroupRows, T - ti.row_begin);
+        ti.slice = (int)(row % slices_s);
+    }
+    return ti;
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -159,10 +183,8 @@ __device__ __forceinline__ void box_dot_mx(float (&c)[4][4], const uint8_t* box,
     }
 }
 
-// A CTA's contiguous share [u0, u1) of the units: CTA b of nb takes U / nb units, one
-// more for the first U % nb.
 struct Range {
-    int U, u0, u1, first_tile;
+    long U, u0, u1, first_tile;
     int nb, b, kb0;
 };
 
@@ -171,16 +193,15 @@ __device__ __forceinline__ Range make_range(const TileSpace& ts, int nb, int b) 
     r.U = ts.total();
     r.nb = nb;
     r.b = b;
-    const int q = r.U / nb, rem = r.U - q * nb;
-    r.u0 = b < nb ? b * q + min(b, rem) : 0;
-    r.u1 = b < nb ? r.u0 + q + (b < rem ? 1 : 0) : 0;
+    r.u0 = b < nb ? (long)b * r.U / nb : 0;
+    r.u1 = b < nb ? (long)(b + 1) * r.U / nb : 0;
     r.kb0 = 0;
     r.first_tile = (b < nb && r.u1 > r.u0) ? ts.tile_of(r.u0, &r.kb0) : 0;
     return r;
 }
 
 // One tile of a CTA's unit range, decoded once before the streaming loops so that
-// neither the producer nor the consumers stall on descriptor loads or index
+// neither the producer nor the consumers stall on descriptor loads or 64-bit index
 // arithmetic at tile boundaries.
 struct TileRec {
     int shared, expert, group, row_begin, nrows, slice, part;
@@ -197,53 +218,38 @@ struct TileRec {
 constexpr int kMaxTab = 96;
 constexpr size_t kTabBytes = (size_t)kMaxTab * sizeof(TileRec);
 
-// Tile t of range rg: its row group (routed rows: groups[gi] for row gi * slices_r +
-// slice; shared rows: tokens 8 sg .. 8 sg + 7 for row sg * slices_s + slice), its K part
-// and the part's units inside the range.
-__device__ inline TileRec make_rec(const TileSpace& ts, const Range& rg, int t, int slices_r, int slices_s,
+__device__ inline TileRec make_rec(const TileSpace& ts, const Range& rg, long t, int slices_r, int slices_s,
                                    const RowGroup* groups, int T, int k, const int32_t* perm_src,
                                    const float* topk_w) {
     TileRec r;
-    const int shared = t >= ts.n_r * ts.P;
-    const int v = shared ? t - ts.n_r * ts.P : t;
-    const int row = v / ts.P, p = v - row * ts.P;
-    const int slices = shared ? slices_s : slices_r;
-    const int gi = row / slices;
-    r.shared = shared;
-    r.slice = row - gi * slices;
-    r.part = p;
-    if (shared) {
-        r.expert = -1;
-        r.group = -1;
-        r.row_begin = gi * kGroupRows;
-        r.nrows = min(kGroupRows, T - r.row_begin);
-    } else {
-        const RowGroup g = groups[gi];
-        r.expert = g.expert;
-        r.group = gi;
-        r.row_begin = g.row_begin;
-        r.nrows = g.nrows;
-    }
-    const int kc = shared ? ts.kc_s : ts.kc_r;
-    const int plo = ts.lo(shared, p), phi = ts.lo(shared, p + 1);
-    const int st = (shared ? ts.n_r * ts.kc_r : 0) + row * kc + plo;  // the tile's first unit
-    const int len = phi - plo;
-    const int lo = st > rg.u0 ? st : rg.u0, hi = st + len < rg.u1 ? st + len : rg.u1;
-    r.kb0 = plo + (lo - st);
-    r.n = hi - lo;
+    const TileInfo ti = decode_tile(ts, t, slices_r, slices_s, groups, T);
+    r.shared = ti.shared;
+    r.expert = ti.expert;
+    r.group = ti.group;
+    r.row_begin = ti.row_begin;
+    r.nrows = ti.nrows;
+    r.slice = ti.slice;
+    r.part = ti.part;
+    const long st = ts.start(t), len = ts.len(t);
+    const long lo = st > rg.u0 ? st : rg.u0, hi = st + len < rg.u1 ? st + len : rg.u1;
+    int kbs;
+    ts.tile_of(st, &kbs);
+    r.kb0 = kbs + (int)(lo - st);
+    r.n = (int)(hi - lo);
     r.hs = st >= rg.u0;
     r.he = st + len <= rg.u1;
     r.pad = 0;
     const int Tk = T * k;
     int f[kGroupRows];
 #pragma unroll
-    for (int c = 0; c < kGroupRows; ++c) f[c] = (c < r.nrows && !shared) ? perm_src[r.row_begin + c] : -1;
+    for (int c = 0; c < kGroupRows; ++c)
+        f[c] = (c < ti.nrows && !ti.shared) ? perm_src[ti.row_begin + c] : -1;
 #pragma unroll
     for (int c = 0; c < kGroupRows; ++c) {
         if (topk_w) {
-            r.w[c] = c >= r.nrows ? 0.f : shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? topk_w[f[c]] : 0.f);
+            r.w[c] = c >= ti.nrows ? 0.f : ti.shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? topk_w[f[c]] : 0.f);
         } else {
-            r.tok[c] = c >= r.nrows ? -1 : shared ? r.row_begin + c : ((unsigned)f[c] < (unsigned)Tk ? f[c] / k : -1);
+            r.tok[c] = c >= ti.nrows ? -1 : ti.shared ? ti.row_begin + c : ((unsigned)f[c] < (unsigned)Tk ? f[c] / k : -1);
         }
     }
     return r;
@@ -255,8 +261,8 @@ __device__ inline int build_table(TileRec* tab, const TileSpace& ts, const Range
                                   const RowGroup* groups, int T, int k, const int32_t* perm_src, const float* topk_w,
                                   int tid, int nthreads) {
     int kbl;
-    const int last = ts.tile_of(rg.u1 - 1, &kbl);
-    const int n = last - rg.first_tile + 1;
+    const long last = ts.tile_of(rg.u1 - 1, &kbl);
+    const int n = (int)(last - rg.first_tile + 1);
     for (int i = tid; i < n && i < kMaxTab; i += nthreads)
         tab[i] = make_rec(ts, rg, rg.first_tile + i, slices_r, slices_s, groups, T, k, perm_src, topk_w);
     return n;
@@ -272,8 +278,35 @@ struct Partials {
 };
 
 // Store this warp's share of a tile: vals[m][i] is row warp*16 + g + 8*(i>=2),
-// column 2*t4 + (i&1) of matrix m. The CTA holding the tile's first unit writes A (and
-// zeros to B when it also holds the last); a CTA holding the rest writes B.
+// column 2*t4 + (i&1) of matrix m.
+template <int NMAT>
+__device__ __forceinline__ void store_tile(const float (&vals)[NMAT][4], const TileSpace& ts, const Range& rg, long t,
+                                           const TileInfo& ti, const Partials& pt) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
+    const long st = ts.start(t);
+    const bool holds_start = st >= rg.u0;
+    const bool holds_end = st + ts.len(t) <= rg.u1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int col = 2 * t4 + (i & 1);
+        if (col >= ti.nrows) continue;
+        const int row = warp * 16 + g + (i >= 2 ? 8 : 0);
+        const size_t o = ((size_t)ti.part * pt.rows + ti.row_begin + col) * pt.N + ti.slice * kTile + row;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            if (holds_start) {
+                pt.A[m][o] = vals[m][i];
+                if (holds_end) pt.B[m][o] = 0.f;
+            } else {
+                pt.B[m][o] = vals[m][i];
+            }
+        }
+    }
+}
+
+// Sum over the P parts of A + B at four consecutive channels col4.. of output row
+// `orow` of matrix m.
+// store_tile with the tile described by a TileRec
 template <int NMAT>
 __device__ __forceinline__ void store_rec(const float (&vals)[NMAT][4], const TileRec& r, const Partials& pt) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
@@ -295,8 +328,6 @@ __device__ __forceinline__ void store_rec(const float (&vals)[NMAT][4], const Ti
     }
 }
 
-// Sum over the P parts of A + B at four consecutive channels col4.. of output row
-// `orow` of matrix m.
 __device__ __forceinline__ float4 read4(const Partials& pt, int P, int m, long orow, int col4) {
     // all 2P loads first, then the sums in part order: one memory round trip
     float4 a[kMaxParts], b[kMaxParts];
