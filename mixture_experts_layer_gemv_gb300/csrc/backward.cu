@@ -253,23 +253,6 @@ __global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const Gemm p) {
 }
 
 // ---------------------------------------------------------------- operand preparation
-// nmat matrices [rows, cols] of E4M3 codes with fp32 scales per 128 x 128 block ->
-// bf16 (dec(code) * scale, one rounding), 16 values per thread.
-__global__ void __launch_bounds__(256) dequant_bf16_kernel(const uint8_t* q, const float* s, long nmat, int rows,
-                                                           int cols, __nv_bfloat16* out) {
-    const long per = (long)rows * cols / 16;
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nmat * per; i += (long)gridDim.x * blockDim.x) {
-        const long mat = i / per, off = (i % per) * 16;
-        const int r = (int)(off / cols), c = (int)(off % cols);
-        const float sc = s[(size_t)mat * (rows / kBlk) * (cols / kBlk) + (size_t)(r / kBlk) * (cols / kBlk) + c / kBlk];
-        uint4 lo, hi;
-        e4m3x16_to_bf16(*reinterpret_cast<const uint4*>(q + (size_t)mat * rows * cols + off), sc, lo, hi);
-        uint4* d = reinterpret_cast<uint4*>(out + (size_t)mat * rows * cols + off);
-        d[0] = lo;
-        d[1] = hi;
-    }
-}
-
 // Transposed dequantisation for the tcgen05 dgrad operands: for each of nmat matrices
 // q [R, Cc] of E4M3 codes (fp32 scales per 128 x 128 block), out[c, col0 + r] =
 // bf16(dec(q[r, c]) * scale) in an output matrix [Cc, out_ld]. 64 x 64 tiles through
@@ -754,7 +737,6 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
     b.mtiles = mtiles;
     b.ctrl = ctrl;
     b.offsets = reinterpret_cast<int32_t*>(at(L.offsets));
-    const unsigned mt_grid = (unsigned)L.max_mtiles;
 
     // ---- dau = Wd^T dout: routed rows (tiles of the permutation), then the shared experts
     BWD_TRY(launch_bwd_tc(bf(L.dout_perm), (uint64_t)R, bf(L.wdT), (uint64_t)E, H, I, 1, 0, mtiles, ctrl,
