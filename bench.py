@@ -350,7 +350,7 @@ def run_ours(args, dist, rank, world):
     }
 
 
-def cpu_oracle_rate(wl, budget_s: float, weights=None, mx: bool = False):
+def cpu_oracle_rate(wl, limit_s: float, weights=None, mx: bool = False):
     """Time the oracle (as it stands) on a bounded sample of the workload: independent
     T-token layer calls' worth of tokens, all host cores. Returns (us per layer call, cores, sample)."""
     import oracle
@@ -371,7 +371,7 @@ def cpu_oracle_rate(wl, budget_s: float, weights=None, mx: bool = False):
         ids, w, _, _ = oracle.route(cfg, x, Wc["w_router"], Wc["router_bias"])
         run_tokens(cfg, OW, x, ids, w)
         done += n_tok
-        if time.perf_counter() - t0 > budget_s:
+        if time.perf_counter() - t0 > limit_s:
             break
     el = time.perf_counter() - t0
     us_per_token = el / done * 1e6
@@ -399,7 +399,7 @@ def _backward_flops(cfg, T: int) -> dict:
     return {"wgrad_gate_up_routed": gu_routed, "backward_bf16": total}
 
 
-def cpu_oracle_backward_rate(wl, budget_s: float, weights, x, ids, w, dout):
+def cpu_oracle_backward_rate(wl, limit_s: float, weights, x, ids, w, dout):
     """The oracle backward as it stands, dx of a bounded sample of tokens (the weight
     gradients are sums over whole experts, whose fp64 arrays do not fit at this shape).
     Returns (tokens/s, cores, sample description)."""
@@ -417,9 +417,9 @@ def cpu_oracle_backward_rate(wl, budget_s: float, weights, x, ids, w, dout):
         oracle.backward(cfg, Wo, x[rows], ids_h[rows], w_h[rows], dout_h[rows], wr, b, dx_only=True)
         done += n
         el = time.perf_counter() - t0
-        if el > budget_s or done >= wl.T:
+        if el > limit_s or done >= wl.T:
             break
-        n = max(1, min(2 * n, int(n * (budget_s - el) / max(el, 1e-3))))
+        n = max(1, min(2 * n, int(n * (limit_s - el) / max(el, 1e-3))))
     return done / el, oracle.num_threads(), f"dx of {done} tokens of the workload (router, experts, shared)"
 
 
@@ -446,8 +446,8 @@ def main_backward(args, dist, rank, world):
         ids, w, _, _ = oracle.route(cfg, xc, Wc["w_router"], Wc["router_bias"])
         g = torch.Generator(device="cpu").manual_seed(1234)
         dout = torch.randn((T, cfg.hidden), generator=g).to(torch.bfloat16)
-        budget = max(5.0, min(60.0, args.cpu_budget))
-        rate, cores, sample = cpu_oracle_backward_rate(wl, budget, Wc, xc, torch.from_numpy(ids),
+        cap = max(5.0, min(60.0, args.cpu_seconds))
+        rate, cores, sample = cpu_oracle_backward_rate(wl, cap, Wc, xc, torch.from_numpy(ids),
                                                        torch.from_numpy(w), dout)
         line = {"impl": "reference", "metric": metric, "value": round(rate, 3), "unit": "tokens/s", "n_gpus": 1,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(T / rate * 1e3, 3),
@@ -565,7 +565,7 @@ def main_backward(args, dist, rank, world):
         "device_status": status,
     }
     if not args.no_cpu_baseline:
-        rate, cores, sample = cpu_oracle_backward_rate(wl, args.cpu_budget, W, xs[0], routes[0][0], routes[0][1],
+        rate, cores, sample = cpu_oracle_backward_rate(wl, args.cpu_seconds, W, xs[0], routes[0][0], routes[0][1],
                                                        dout)
         line["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
@@ -583,7 +583,7 @@ def main():
     ap.add_argument("--workload", default="dsv2_decode_t1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--replicas", type=int, default=0)
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mx", action="store_true", help="the MXFP8 variant (E8M0 scales per 32 K)")
     ap.add_argument("--backward", action="store_true",
@@ -611,8 +611,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        budget = max(5.0, min(60.0, args.cpu_budget))
-        us, cores, sample = cpu_oracle_rate(wl, budget, mx=args.mx)
+        cap = max(5.0, min(60.0, args.cpu_seconds))
+        us, cores, sample = cpu_oracle_rate(wl, cap, mx=args.mx)
         value = us if t1_metric else 1e6 / us * 1.0
         unit = "us/layer" if t1_metric else "tokens/s"
         line = {"impl": "reference", "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": 1,
@@ -674,7 +674,7 @@ def main():
         "gpu_launches": r["launches"], "clocks": r["clocks"], "device_status": r["status"],
     }
     if not args.no_cpu_baseline:
-        us_cpu, cores, sample = cpu_oracle_rate(wl, args.cpu_budget, r["weights"], mx=args.mx)
+        us_cpu, cores, sample = cpu_oracle_rate(wl, args.cpu_seconds, r["weights"], mx=args.mx)
         cv = us_cpu if t1_metric else 1e6 / us_cpu
         line["cpu_baseline"] = {"value": round(cv, 3), "unit": unit, "cores": cores, "kind": "oracle",
                                 "sample": sample}

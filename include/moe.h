@@ -120,7 +120,7 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 /* Device-side error word of ws: copies it to the host (synchronising `stream`), clears
  * it, and returns MOE_OK or the recorded error (MOE_ERR_DEVICE_TIMEOUT when a bounded
  * wait inside a kernel gave up; such a kernel skips its remaining work and returns
- * instead of hanging). Every bounded wait has an iteration budget; none traps. */
+ * instead of hanging). Every bounded wait has an iteration limit; none traps. */
 moe_status_t moe_read_device_status(void* ws, void* stream);
 
 /* Activation quantisation, the FP8 operand of the expert GEMMs: per token and block of

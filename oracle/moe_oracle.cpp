@@ -15,7 +15,7 @@
 //   Q1/Q2 shared experts (fused into one MLP of width n_shared * moe_inter)
 //   R  combine: h = shared_out + sum of routed (+ residual when one is given)
 // The FP8 activation quantisation (one power-of-two scale per token and 128
-// channels) is this build's reading of the pages' "FP8 block-scaled MoE GEMMs"
+// channels) is the reading taken here of the pages' "FP8 block-scaled MoE GEMMs"
 // (README "Results") and of "MXFP8 input quantization" (the DeepSeek-V4.1 Flash
 // lecture, "Rounds 12-15" table); the scale form follows the pages' quantiser with
 // UE8M0 (power-of-two) scale factors (README "Layout", quant/fp8_block_quant.py).

@@ -2,8 +2,8 @@
 
 The backward differentiates L = sum(dout * out) for the layer with the expert choice
 held fixed (selection is piecewise constant) and the routing weights w = s * p_e
-recomputed from x (Mixture-of-Kittens, Table 1 "Backward"; the formulas are this
-build's reading, not printed on the pages). It is pinned by central finite
+recomputed from x (Mixture-of-Kittens, Table 1 "Backward"; the formulas are the
+reading taken here, not printed on the pages). It is pinned by central finite
 differences of the oracle's own forward with fixed ids (a separate code path: a
 mistake in a chain-rule term changes the analytic gradient but not the forward), by
 linearity in dout, by the routing weights' scale s = 0 limit, and by the FP8
