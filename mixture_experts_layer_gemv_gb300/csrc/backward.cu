@@ -1,6 +1,6 @@
 // The layer's backward: gradients of sum(dout * out) with the forward's expert choice
-// held fixed (the Mixture-of-Kittens page's training workload, Table 1 "Backward";
-// "expert FFNs" forward and backward). The FP8 quantisers are straight-through and the
+// held fixed (the Mixture-of-Kittens page's training workload: Table 1's backward
+// columns, and the abstract's training of the expert MLPs). The FP8 quantisers are straight-through and the
 // weights enter at their dequantised FP8 values. Per routed row r = (t, j), expert e,
 // routing weight w = s * p_e, with g, u, ahat the forward's values:
 //   dau = Wd_e^T dout_t                       (unweighted)        dgrad of the down GEMM

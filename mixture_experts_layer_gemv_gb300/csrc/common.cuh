@@ -137,7 +137,8 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 
 // ------------------------------------------------- stage M: RMSNorm x gamma
 // x = h * rstd * gamma with rstd = 1 / sqrt(mean(h^2) + eps), rounded once to bf16
-// ("M . RMSNorm h x gamma4", DSV2-236B-MegaKernel stage flowchart, MoE subgraph).
+// (stage M of the DSV2-236B-MegaKernel stage flowchart, MoE subgraph: the hidden state
+// normalised and scaled by its gamma before the router).
 // Every kernel that reads a normalised activation derives it from the raw row with
 // these functions (rstd always from warp_row_sumsq), so all of them see the same
 // bf16 values.

@@ -1,8 +1,8 @@
 // Stages P1/P2 and Q1/Q2 of the MoE layer in the MXFP8 variant: E4M3 codes with one
 // UE8M0 (power-of-two) scale per row and 32 consecutive K, for weights and activations
-// ("MXFP8 routed experts", Mixture-of-Kittens Table 2; the DeepSeek-V4.1 Flash
-// lecture's "block_fp8 -> mxfp8" conversion that lets the GEMMs "go straight into the
-// Blackwell MXFP8 kernel", "Round 1->2").
+// (Mixture-of-Kittens Table 2, its MXFP8 routed-expert rows; the DeepSeek-V4.1 Flash
+// lecture, "Round 1->2": converting the weights' 128-block scales to the MX layout
+// so that the GEMMs run on Blackwell's block-scaled MXFP8 MMA).
 //
 // Such scales go through the tensor core (tcgen05.mma kind::mxf8f6f4, scale factors in
 // tensor memory), so a tile's whole K reduction accumulates in one TMEM accumulator and

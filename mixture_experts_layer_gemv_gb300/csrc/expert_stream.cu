@@ -1,8 +1,8 @@
 // Stages P1/P2 and Q1/Q2 of the DeepSeek-V2 MoE layer ("DSV2-236B-MegaKernel",
 // README stage flowchart, MoE subgraph) in the weight-streaming regime, where each
 // expert sees at most a few tokens and every FP8 weight byte is used by at most 8
-// activation rows: bound by HBM bandwidth ("decode is a GEMV", the DeepSeek-V4.1
-// Flash Kernel Journey lecture, "Skill 5").
+// activation rows: bound by HBM bandwidth (decode is a matrix-vector product: the
+// DeepSeek-V4.1 Flash Kernel Journey lecture, "Skill 5").
 //
 // Work decomposition (stream-K). A tile is 128 output rows of one matrix (gate and up
 // together for P1/Q1) for one row group of <= 8 activation rows; a unit is one tile

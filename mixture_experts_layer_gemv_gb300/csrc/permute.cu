@@ -1,7 +1,8 @@
 // Token permutation by expert: a deterministic, stable counting sort of the
 // T*k (token, slot) pairs, done on the device so that expert counts and offsets
 // never travel to the host (MoK abstract: no CPU-GPU synchronisation; the
-// DeepSeek-V4.1 Flash lecture's "router emits the layout the experts need").
+// DeepSeek-V4.1 Flash lecture, "Rounds 12-15": the router produces the data layout
+// the expert GEMMs consume).
 //
 // Two launches over segments of 1024 flat indices, one CTA of 8 warps each:
 // permute_count_kernel writes every segment's expert histogram; permute_scatter_kernel

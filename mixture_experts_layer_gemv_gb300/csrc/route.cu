@@ -7,9 +7,9 @@
 //    fp32 router row, K split across warps), every CTA quantises a share of x, and
 //    the last CTA to arrive (an atomic arrival counter, no waiting) runs the
 //    per-token softmax/top-k and, for the fused forward, the expert permutation and
-//    the row-group work list. The README's stage O does the selection with
-//    "ballot + popc + ctz"; here groups and experts are ranked (count of better
-//    candidates, ties to the lower index) with a ballot-compacted candidate list.
+//    the row-group work list. The README's stage O selects with warp ballots and
+//    bit counts; here groups and experts are ranked (count of better candidates, ties
+//    to the lower index) with a ballot-compacted candidate list.
 //  * large T: a tiled fp32 SIMT GEMM for the logits (split-K partials, summed in a
 //    fixed order), then one warp per token for softmax/top-k.
 #include <algorithm>

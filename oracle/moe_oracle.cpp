@@ -15,9 +15,9 @@
 //   Q1/Q2 shared experts (fused into one MLP of width n_shared * moe_inter)
 //   R  combine: h = shared_out + sum of routed (+ residual when one is given)
 // The FP8 activation quantisation (one power-of-two scale per token and 128
-// channels) is the reading taken here of the pages' "FP8 block-scaled MoE GEMMs"
-// (README "Results") and of "MXFP8 input quantization" (the DeepSeek-V4.1 Flash
-// lecture, "Rounds 12-15" table); the scale form follows the pages' quantiser with
+// channels) is the reading taken here of the pages' FP8 block-scaled expert GEMMs
+// (README "Results") and of the quantisation of the experts' inputs to MXFP8 (the
+// DeepSeek-V4.1 Flash lecture, "Rounds 12-15" table); the scale form follows the pages' quantiser with
 // UE8M0 (power-of-two) scale factors (README "Layout", quant/fp8_block_quant.py).
 //
 // Parity pins (tests/test_oracle_*.py) tie every function below to something other
@@ -167,8 +167,8 @@ void orc_round_bf16(const double* v, int n, uint16_t* out) {
 }
 
 // ------------------------------------------------------------------ M: RMSNorm
-// Stage M in front of the router ("RMSNorm h x gamma4", DSV2-236B-MegaKernel stage
-// flowchart, MoE subgraph): per token row,
+// Stage M in front of the router (DSV2-236B-MegaKernel stage flowchart, MoE
+// subgraph: the hidden state normalised and scaled by its gamma): per token row,
 //   x[h] = h[h] / sqrt(mean over the row of h^2 + eps) * gamma[h],
 // computed in fp64 and rounded once to bf16. x_exact (optional) receives the value
 // before that rounding.
@@ -421,9 +421,10 @@ void orc_forward_tokens(const orc_cfg_t* c, const orc_weights_t* W, const uint16
 // ------------------------------------------------------------------ MXFP8
 // The MXFP8 variant of the expert MLPs: E4M3 codes with one UE8M0 (power-of-two)
 // scale per 32 consecutive values along K, for the weights (per output row) and the
-// activations (per token) alike ("MXFP8 routed experts", Mixture-of-Kittens Table 2;
-// the "block_fp8 -> mxfp8" load-time scale conversion and "MXFP8 input quantization"
-// of the DeepSeek-V4.1 Flash lecture, "Round 1->2" and "Rounds 12-15").
+// activations (per token) alike (Mixture-of-Kittens Table 2, its MXFP8 routed-expert
+// rows; the DeepSeek-V4.1 Flash lecture's conversion of the weights' block scales to
+// the MX layout at load time and its MXFP8 quantisation of the experts' inputs,
+// "Round 1->2" and "Rounds 12-15").
 // An E8M0 byte b encodes 2^(b-127); 0xFF is NaN.
 double orc_e8m0_decode(uint8_t b) {
     if (b == 0xFF) return std::numeric_limits<double>::quiet_NaN();
