@@ -64,8 +64,9 @@ typedef struct moe_weights {
     const float *w_router, *router_bias;
 } moe_weights_t;
 
-/* One layer's weights in the MXFP8 variant ("MXFP8 routed experts", Mixture-of-Kittens
- * Table 2; "block_fp8 -> mxfp8", DeepSeek-V4.1 Flash lecture): E4M3 codes as in
+/* One layer's weights in the MXFP8 variant (Mixture-of-Kittens Table 2, its MXFP8
+ * routed-expert rows; the DeepSeek-V4.1 Flash lecture's conversion of block scales to
+ * the MX layout): E4M3 codes as in
  * moe_weights_t, with one UE8M0 scale byte b (value 2^(b-127)) per row and 32
  * consecutive K instead of the fp32 128x128 block scales:
  *   s_gate, s_up   [E, I, H/32]   s_down [E, H, I/32]
@@ -132,8 +133,8 @@ moe_status_t moe_read_device_status(void* ws, void* stream);
 moe_status_t moe_quant_act(const void* x_bf16, int32_t T, int32_t H, uint8_t* xq, float* xs,
                            void* stream);
 
-/* Stage M: RMSNorm in front of the router ("M . RMSNorm h x gamma4 -> 5120",
- * DSV2-236B-MegaKernel stage flowchart, MoE subgraph). Per token row t:
+/* Stage M: RMSNorm in front of the router (DSV2-236B-MegaKernel stage flowchart, MoE
+ * subgraph: the hidden state normalised and scaled by gamma). Per token row t:
  *   x[t][i] = bf16( h[t][i] * rstd[t] * gamma[i] ),  rstd[t] = 1 / sqrt(mean_i h[t][i]^2 + eps),
  * the mean and 1/rms in fp32, one round-to-nearest-even to bf16 per element.
  *   h_bf16 [T, H], gamma_bf16 [H] -> x_bf16 [T, H] (must not alias h).
@@ -183,8 +184,8 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const void* x_bf16, int3
  *   inv_pos        int32 [T*k]: permuted position of each flat index
  * Within one expert the pairs keep ascending f. Ids outside [0, E) are an error the
  * library does not check on the device: they must come from moe_route.
- * ("router emits the layout the experts need": DeepSeek-V4.1 Flash lecture, "Rounds
- * 12-15" table; MoK's GPU-side dispatch scheduling, abstract.) */
+ * (The router produces the layout the expert GEMMs consume: DeepSeek-V4.1 Flash
+ * lecture, "Rounds 12-15" table; MoK's GPU-side dispatch scheduling, abstract.) */
 moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32_t T,
                          int32_t* expert_offsets, int32_t* perm_src, int32_t* inv_pos,
                          void* ws, size_t ws_bytes, void* stream);
@@ -202,7 +203,8 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* x_bf16, int32_t
                             void* y_shared_bf16, void* ws, size_t ws_bytes, void* stream);
 
 /* Stage R's local part: out[t] = sum_j y_perm[inv_pos[t*k + j]] + y_shared[t] (+ residual[t]),
- * summed in fp32, rounded once to bf16 (README flowchart: "h += shared_out + routed").
+ * summed in fp32, rounded once to bf16 (README flowchart, stage R: the shared and routed
+ * outputs added into h).
  * y_shared / residual may be NULL (treated as zero). out must not alias the inputs. */
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm_bf16, const int32_t* inv_pos,
                          const void* y_shared_bf16, const void* residual_bf16, int32_t T,
@@ -228,7 +230,8 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
  *                                     moe_forward with residual = h)
  * h_bf16 [T, H] is the hidden state before the norm; out_bf16 must not alias it.
  * The normalised activation is formed inside the router and quantisation kernels
- * (README flowchart: "M . RMSNorm h x gamma4", then N..R, "h += shared_out + routed"). */
+ * (README flowchart: stage M, then N..R, and stage R adds the shared and routed outputs
+ * into h). */
 moe_status_t moe_forward_rmsnorm(const moe_config_t* cfg, const void* h_bf16, int32_t T, const void* gamma_bf16,
                                  float eps, const moe_weights_t* weights, void* out_bf16, int32_t* topk_ids_out,
                                  void* ws, size_t ws_bytes, void* stream);

@@ -1,5 +1,6 @@
 // Stage R's local part of the DeepSeek-V2 MoE layer ("DSV2-236B-MegaKernel",
-// README stage flowchart: h += shared_out + routed): a sorted-segment gather.
+// README stage flowchart: the shared and routed outputs added into h): a sorted-segment
+// gather.
 // Token t sums its k weighted expert rows (found through inv_pos), the shared
 // experts' row and the optional residual in fp32, in a fixed order, and rounds
 // once to bf16. No atomics, so the result is deterministic.

@@ -537,8 +537,8 @@ void orc_forward_tokens_mx(const orc_cfg_t* c, const orc_weights_mx_t* W, const 
 
 // ---------------------------------------------------------------- backward
 // The layer's backward for an output gradient dout[T][H]: the training workload of the
-// Mixture-of-Kittens page (Table 1, "Backward" columns; "expert FFNs" forward and
-// backward), for one layer on one device. The forward's expert choice (ids) is held
+// Mixture-of-Kittens page (Table 1's backward columns; the abstract's training of the
+// expert MLPs), for one layer on one device. The forward's expert choice (ids) is held
 // fixed: selection is piecewise constant in the inputs, so gradients reach the router
 // only through the routing weights of the kept experts, w = s * p_e.
 // Reading taken here (the pages give no formulas): the FP8 quantisers are

@@ -1,7 +1,7 @@
 """Stage M (RMSNorm x gamma in front of the router) through the C ABI, against the oracle.
 
-"M . RMSNorm h x gamma4 -> 5120" (DSV2-236B-MegaKernel, stage flowchart, MoE
-subgraph), then the layer N..R with the residual h: out = h + layer(RMSNorm(h)).
+Stage M of the DSV2-236B-MegaKernel stage flowchart (MoE subgraph), the hidden
+state normalised and scaled by gamma before the router, then the layer N..R with the residual h: out = h + layer(RMSNorm(h)).
 
 Bars: moe_rmsnorm's bf16 values equal the oracle's, except where the oracle's exact
 value lies so close to a rounding midpoint (1e-5 relative) that fp32 arithmetic may

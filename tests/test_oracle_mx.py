@@ -2,9 +2,9 @@
 MXFP8 expert MLP / layer.
 
 The variant stores E4M3 codes with one UE8M0 (power-of-two) scale per 32 consecutive
-values along K, for weights and activations ("MXFP8 routed experts", Mixture-of-Kittens
-Table 2; "block_fp8 -> mxfp8" conversion and "MXFP8 input quantization", DeepSeek-V4.1
-Flash lecture). Pinned by torch's float8_e8m0fnu / float8_e4m3fn conversions (library
+values along K, for weights and activations (Mixture-of-Kittens Table 2, its MXFP8
+routed-expert rows; the DeepSeek-V4.1 Flash lecture's conversion of block scales to the
+MX layout and its MXFP8 quantisation of the experts' inputs). Pinned by torch's float8_e8m0fnu / float8_e4m3fn conversions (library
 routines), the agreement with the per-128 quantiser when the four 32-blocks of a
 128-block share their maximum, a hand-worked MLP (tests/golden/mx_swiglu_hand.txt) and
 torch fp64 matmuls on dequantised weights.

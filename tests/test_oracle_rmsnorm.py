@@ -1,7 +1,7 @@
 """Pins of the oracle's stage M (RMSNorm in front of the router) and its bf16 rounding.
 
-"M . RMSNorm h x gamma4 -> 5120" (DSV2-236B-MegaKernel, stage flowchart, MoE
-subgraph): x = h / sqrt(mean(h^2) + eps) * gamma per token row, rounded once to
+Stage M of the DSV2-236B-MegaKernel stage flowchart (MoE subgraph), the hidden
+state normalised and scaled by gamma before the router: x = h / sqrt(mean(h^2) + eps) * gamma per token row, rounded once to
 bf16. Pinned by a hand-worked row (tests/golden/rmsnorm_hand.txt), closed forms
 (a constant row normalises to +-1), invariances the definition implies (scaling h by
 a power of two, gamma by a power of two), torch's float32 -> bf16 conversion for the
