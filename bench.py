@@ -31,7 +31,6 @@ sys.path.insert(0, ROOT)
 from mixture_experts_layer_gemv_gb300.synth import (WORKLOADS, make_tokens, make_weights, make_weights_mx,  # noqa: E402
                                                     replicate_weights)
 
-L2_BYTES = 129 * 1024 * 1024
 
 
 def _peaks():
@@ -212,34 +211,96 @@ NCU_TRAFFIC_BYTES = {
 }
 
 
-def run_ours(args, dist, rank, world):
+def l2_bytes() -> int:
+    """L2 size of the current device (cudaDeviceProp::l2CacheSize), 129 MB without one."""
+    if torch.cuda.is_available():
+        try:
+            return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+        except (AttributeError, RuntimeError):
+            pass
+    return 129 * 1024 * 1024
+
+
+def n_replicas(cfg, T: int, mx: bool = False, forced: int = 0) -> int:
+    """Stacked layer replicas rotated through so consecutive steps never find their
+    weights in L2: enough that R layers' touched bytes exceed 4x the L2 size."""
+    if forced:
+        return forced
+    touched = _algorithmic_layer_bytes(cfg, min(cfg.n_routed, T * cfg.top_k), T, mx)
+    return max(1, min(8, (4 * l2_bytes()) // max(1, touched) + 1))
+
+
+def l2_note(cfg, T: int, mx: bool = False, forced: int = 0) -> str:
+    R = n_replicas(cfg, T, mx, forced)
+    mb = l2_bytes() / 2 ** 20
+    if R == 1:
+        return f"one layer's weights exceed the {mb:.0f} MiB L2 every step (inputs > L2)"
+    return f"{R} stacked layer replicas rotated so weights stream from HBM (inputs > L2 of {mb:.0f} MiB)"
+
+
+def _timed_graph_loop(step, steps: int, period: int, stream):
+    """Time exactly `steps` calls of step(i) on the device, replayed from CUDA graphs so
+    that host launch overhead is not in the timed region: one graph of `period` calls
+    (the rotation period of inputs and weights) replayed steps // period times, and one
+    of the remaining steps % period calls. Returns (ms per step, "graph" or "eager")."""
+    graphs = []
+    mode = "graph"
+    try:
+        with torch.cuda.stream(stream):
+            for n in ([period] if steps >= period else []) + ([steps % period] if steps % period else []):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                    for i in range(n):
+                        step(i, stream.cuda_stream)
+                graphs.append((n, g))
+        for _, g in graphs:  # one untimed replay each
+            g.replay()
+        torch.cuda.synchronize()
+    except RuntimeError:
+        graphs, mode = [], "eager"
+        torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        if graphs:
+            full = steps // period if steps >= period else 0
+            for _ in range(full):
+                graphs[0][1].replay()
+            if steps % period:
+                graphs[-1][1].replay()
+        else:
+            for i in range(steps):
+                step(i, stream.cuda_stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps, mode
+
+
+def measure(wl, args, steps: int, warmup: int, dist, rank: int, world: int, prof_steps: int = 200):
+    """One workload on this GPU: the layer timed unprofiled (graph replays of plain
+    moe_forward calls), then per-stage CUDA events on a separate pass, then the end-to-end
+    time through the public API with host buffers. Returns a dict of figures."""
     import ctypes
+    import math
 
     from mixture_experts_layer_gemv_gb300 import binding as B
-    from mixture_experts_layer_gemv_gb300 import build as lib_build
 
-    if rank == 0 or not os.path.exists(lib_build.LIB):
-        lib_build.build()
-    _barrier(dist)
     lib = B.lib()
     dev = torch.device("cuda", torch.cuda.current_device())
-    wl = WORKLOADS[args.workload]
     cfg, T = wl.cfg, wl.T
     mx = args.mx
     W0 = (make_weights_mx if mx else make_weights)(cfg, wl.seed, dev, zipf=wl.zipf_bias)
-    touched_bytes = _algorithmic_layer_bytes(cfg, min(cfg.n_routed, T * cfg.top_k), T, args.mx)
-    # enough stacked layer replicas that consecutive steps never find their weights in L2
-    R = args.replicas or max(1, min(8, (4 * L2_BYTES) // max(1, touched_bytes) + 1))
+    R = n_replicas(cfg, T, mx, args.replicas)
     layers = [W0] + [replicate_weights(W0) for _ in range(R - 1)]
-    P = max(R, 8)
+    P = max(R, 8) if T <= 64 else 2
     xs = [make_tokens(cfg, T, replica_seed(wl.seed, rank, i), dev, name=f"x_step{i}") for i in range(P)]
     ws = (B.alloc_workspace_mx if mx else B.alloc_workspace)(cfg, T, dev)
     out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=dev)
     ids = torch.empty((T, cfg.top_k), dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
-    st = stream.cuda_stream
+    stream = torch.cuda.Stream(dev)
+    period = P * R // math.gcd(P, R)
 
-    # argument structs built once: the timed loop is one C call per step
     cstruct = B.config_struct(cfg)
     wstructs = [(B.weights_mx_struct if mx else B.weights_struct)(Wl) for Wl in layers]
     fwd = lib.moe_forward_mx if mx else lib.moe_forward
@@ -250,7 +311,7 @@ def run_ours(args, dist, rank, world):
     x_ptrs = [x.data_ptr() for x in xs]
     out_p, ws_p, ws_n = out.data_ptr(), ws.data_ptr(), ws.numel()
 
-    def step(i, ev=None):
+    def step(i, st, ev=None):
         if ev is None:
             r = fwd(c_ref, x_ptrs[i % P], T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st)
         else:
@@ -258,96 +319,152 @@ def run_ours(args, dist, rank, world):
         if r != 0:
             raise B.MoeError("moe_forward", r, B.status_string(r))
 
-    # touched experts per step (for the roofline numerator): from the routing itself
+    # touched experts per step (the roofline numerator), from the routing itself
     touched = []
-    for i in range(P):
+    for i in range(min(P, 4)):
         fwd_py(cfg, xs[i], layers[i % R], out, topk_ids_out=ids, ws=ws)
         touched.append(int(torch.unique(ids).numel()))
     torch.cuda.synchronize()
 
-    # per-stage CUDA events on every `stride`-th timed step
-    stride = max(1, args.steps // 256)
-    n_prof = (args.steps + stride - 1) // stride
+    with ClockSampler(dev.index) as clk:
+        clk.wait_first_sample()
+        for i in range(warmup):
+            step(i, stream.cuda_stream)
+        torch.cuda.synchronize()
+        _barrier(dist)
+        torch.cuda.synchronize()
+        ms, timing = _timed_graph_loop(step, steps, period, stream)
+        # the sampler sees at least one sample under load: keep the GPU busy for >= 0.3 s
+        # when the timed region itself was shorter (these steps are not timed)
+        extra = int(0.3 / max(ms * 1e-3, 1e-6)) if steps * ms < 300 else 0
+        for i in range(min(extra, 20000)):
+            step(i, stream.cuda_stream)
+        torch.cuda.synchronize()
+    _barrier(dist)
+    ms = _max_over_ranks(dist, ms)
+    status = B.moe_read_device_status(ws, stream)
+
+    # per-stage events: a separate, untimed pass
+    n_prof = max(1, min(prof_steps, steps))
     prof = []
     for _ in range(n_prof):
         evs = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in B.STAGES}
-        for a, b in evs.values():
-            a.record()
-            b.record()
+        with torch.cuda.stream(stream):
+            for a, b in evs.values():  # torch times only events it has recorded itself
+                a.record(stream)
+                b.record(stream)
         s_ev = B.moe_stage_events_t()
         for j, n in enumerate(B.STAGES):
             s_ev.start[j] = evs[n][0].cuda_event
             s_ev.stop[j] = evs[n][1].cuda_event
         prof.append((evs, s_ev))
     torch.cuda.synchronize()
-
-    with ClockSampler(dev.index) as clk:
-        clk.wait_first_sample()
-        for i in range(args.warmup):
-            step(i)
-        torch.cuda.synchronize()
-        _barrier(dist)
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for i in range(args.steps):
-            step(i, prof[i // stride][1] if i % stride == 0 else None)
-        t1.record()
-        torch.cuda.synchronize()
-    _barrier(dist)
+    for i in range(n_prof):
+        step(i, stream.cuda_stream, prof[i][1])
     torch.cuda.synchronize()
-    ms = _max_over_ranks(dist, t0.elapsed_time(t1) / args.steps)
     stage_us = {}
-    # small T: the router also permutes
     recorded = ("route", "gate_up", "down", "combine") if T <= 64 else B.STAGES
     for n in recorded:
         v = [evs[n][0].elapsed_time(evs[n][1]) * 1e3 for evs, _ in prof]
         if max(v) > 0:
-            stage_us[n] = round(statistics.mean(v), 3)
-    gu_ms = stage_us["gate_up"] / 1e3
-    status = B.moe_read_device_status(ws)
+            stage_us[n] = round(statistics.median(v), 3)
 
-    # end to end through the C ABI with host buffers: pinned x in, out back, every step
+    # end to end through the public API (the Python binding's moe_forward, one call per
+    # step) with host buffers: pinned x copied in and the output copied back every step
     xh = [x.cpu().pin_memory() for x in xs]
     oh = torch.empty((T, cfg.hidden), dtype=torch.bfloat16).pin_memory()
     xd = torch.empty_like(xs[0])
-    xd_p = xd.data_ptr()
 
     def e2e_step(i):
         xd.copy_(xh[i % P], non_blocking=True)
-        r = fwd(c_ref, xd_p, T, w_refs[i % R], None, out_p, None, ws_p, ws_n, st)
-        if r != 0:
-            raise B.MoeError("moe_forward", r, B.status_string(r))
+        fwd_py(cfg, xd, layers[i % R], out, ws=ws, stream=stream)
         oh.copy_(out, non_blocking=True)
 
-    for i in range(args.warmup):
-        e2e_step(i)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        _barrier(dist)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            e2e_step(i)
+        e1.record(stream)
     torch.cuda.synchronize()
-    _barrier(dist)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / args.steps)
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / steps)
 
     n_touched = statistics.mean(touched)
-    gu_bytes = _algorithmic_gateup_bytes(cfg, round(n_touched), T, mx)
     peaks = _peaks()
-    peak_gbs = peaks["hbm_gbs"] if peaks else 6800.0
-    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
-    layer_bytes = _algorithmic_layer_bytes(cfg, round(n_touched), T, mx)
-    tokens_per_s = _sum_over_ranks(dist, T / (ms * 1e-3))
-    return {
-        "cfg": cfg, "T": T, "ms": ms, "e2e_ms": e2e_ms, "gu_ms": gu_ms, "gu_bytes": gu_bytes,
-        "achieved": achieved, "peak": peak_gbs, "peak_src": "measured" if peaks else "fallback",
-        "layer_bytes": layer_bytes, "tokens_per_s": tokens_per_s, "clocks": clk.summary(), "status": status,
-        "replicas": R, "n_touched": n_touched, "launches": _launches_per_step(cfg, T, mx) * args.steps, "weights": W0,
-        "stage_us": stage_us, "prof_steps": n_prof,
-    }
+    res = {"cfg": cfg, "T": T, "ms": ms, "timing": timing, "e2e_ms": e2e_ms, "stage_us": stage_us,
+           "prof_steps": n_prof, "clocks": clk.summary(), "status": status, "replicas": R, "n_touched": n_touched,
+           "launches": _launches_per_step(cfg, T, mx) * steps, "weights": W0,
+           "tokens_per_s": _sum_over_ranks(dist, T / (ms * 1e-3)),
+           "peak_gbs": peaks["hbm_gbs"] if peaks else 6800.0, "peak_src": "measured" if peaks else "fallback",
+           "layer_bytes": _algorithmic_layer_bytes(cfg, round(n_touched), T, mx)}
+    del layers, W0, xs, ws
+    return res
+
+
+def summarise(r, wl, args, world: int) -> dict:
+    """The JSON figures of one measured workload: value in the metric's unit for its
+    regime (us/layer at T <= 64, tokens/s above), the roofline of the dominant kernel
+    and of the whole layer, e2e, stage times and clocks."""
+    cfg, T, mx = wl.cfg, wl.T, args.mx
+    us = r["ms"] * 1e3
+    small = T <= 64
+    if small:
+        value, unit, hib = us, "us/layer", False
+        e2e_value = r["e2e_ms"] * 1e3
+    else:
+        value, unit, hib = r["tokens_per_s"], "tokens/s", True
+        e2e_value = world * T / (r["e2e_ms"] * 1e-3)
+    peaks = _peaks()
+    layer_gbs = r["layer_bytes"] / (r["ms"] * 1e-3) / 1e9
+    gu_us = r["stage_us"].get("gate_up")
+    out = {"value": round(value, 3), "unit": unit, "higher_is_better": hib, "ms_per_step": round(r["ms"], 5),
+           "us_per_layer": round(us, 3), "tokens_per_s": round(r["tokens_per_s"], 1), "timing": r["timing"],
+           "layer_hbm_gbs": round(layer_gbs, 1), "layer_hbm_frac": round(layer_gbs / r["peak_gbs"], 4),
+           "layer_bytes": r["layer_bytes"], "experts_touched_per_step": r["n_touched"]}
+    if (mx and T > 64) or _gemm_path(cfg, T):
+        # contraction on the FP8 tensor cores: peak = measured bf16 burst x nominal FP8/bf16 ratio (2)
+        fp8_peak = 2.0 * peaks["bf16_tflops"] if peaks else 2.0 * 1900.0
+        gu_tflops = _gateup_flops(cfg, T) / (gu_us * 1e-6) / 1e12
+        kname = "expert_gemm_mx_kernel<0>" if mx else "expert_gemm_kernel<0>"
+        out["roofline"] = {"bound": "tensor", "kernel": f"{kname} (gate/up grouped GEMM)",
+                           "achieved": round(gu_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                           "frac": round(gu_tflops / fp8_peak, 4),
+                           "traffic": NCU_TRAFFIC_BYTES.get((wl.name, kname)),
+                           "peak_source": ("measured bf16 burst x2 (nominal fp8/bf16)" if peaks else "fallback x2"),
+                           "launch_us": gu_us, "flops_per_launch": _gateup_flops(cfg, T)}
+        layer_tflops = _layer_flops(cfg, T) / (r["ms"] * 1e-3) / 1e12
+        out["layer_tflops"] = round(layer_tflops, 1)
+        out["layer_tensor_frac"] = round(layer_tflops / fp8_peak, 4)
+    else:
+        gu_bytes = _algorithmic_gateup_bytes(cfg, round(r["n_touched"]), T, mx)
+        achieved = gu_bytes / (gu_us * 1e-6) / 1e9
+        kname = "gateup_stream_kernel<true>" if mx else "gateup_stream_kernel"
+        out["roofline"] = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": r["peak_gbs"],
+                           "unit": "GB/s", "frac": round(achieved / r["peak_gbs"], 4),
+                           "traffic": NCU_TRAFFIC_BYTES.get((wl.name, kname)), "peak_source": r["peak_src"],
+                           "launch_us": gu_us, "bytes_per_launch": gu_bytes}
+    out["e2e"] = {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": T * cfg.hidden * 2,
+                  "d2h_bytes_per_step": T * cfg.hidden * 2}
+    out.update({"stages_us": r["stage_us"], "stage_events": f"separate untimed pass of {r['prof_steps']} steps",
+                "gpu_launches": r["launches"], "clocks": r["clocks"], "device_status": r["status"],
+                "l2": l2_note(cfg, T, mx, args.replicas)})
+    return out
+
+
+def workload_config(wl, args, world: int) -> dict:
+    cfg, T = wl.cfg, wl.T
+    return {"workload": f"{wl.name}: {wl.description}", "T": T, "hidden": cfg.hidden,
+            "moe_inter": cfg.moe_inter, "n_routed": cfg.n_routed, "n_group": cfg.n_group,
+            "topk_group": cfg.topk_group, "top_k": cfg.top_k,
+            "routed_scaling_factor": cfg.routed_scaling_factor, "n_shared": cfg.n_shared,
+            "weights": ("MXFP8: E4M3, E8M0 scale per row and 32 K" if args.mx else
+                        "FP8 E4M3, fp32 per-128x128 block scales"), "parallelism": f"replicas x{world}",
+            "l2": l2_note(cfg, T, args.mx, args.replicas)}
 
 
 def cpu_oracle_rate(wl, limit_s: float, weights=None, mx: bool = False):
@@ -585,6 +702,9 @@ def main():
     ap.add_argument("--replicas", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sub-cpu-seconds", type=float, default=5.0,
+                    help="oracle time cap for each of the extra workloads in the default run")
+    ap.add_argument("--only", action="store_true", help="the named workload alone (no extra workloads)")
     ap.add_argument("--mx", action="store_true", help="the MXFP8 variant (E8M0 scales per 32 K)")
     ap.add_argument("--backward", action="store_true",
                     help="the layer backward (moe_backward) instead of the forward; use with --workload prefill_t4096")
@@ -599,25 +719,20 @@ def main():
     cfg, T = wl.cfg, wl.T
     if args.steps <= 0:
         args.steps = {1: 20000, 8: 20000, 64: 2000}.get(T, 200)
-    t1_metric = T <= 64
+    small = T <= 64
     metric = "MoE layer µs at T=1 (% HBM roofline); tokens/s at T=4096 (% FP8 TC peak)"
-    config = {"workload": f"{wl.name}: {wl.description}", "T": T, "hidden": cfg.hidden,
-              "moe_inter": cfg.moe_inter, "n_routed": cfg.n_routed, "n_group": cfg.n_group,
-              "topk_group": cfg.topk_group, "top_k": cfg.top_k,
-              "routed_scaling_factor": cfg.routed_scaling_factor, "n_shared": cfg.n_shared,
-              "weights": ("MXFP8: E4M3, E8M0 scale per row and 32 K" if args.mx else
-                          "FP8 E4M3, fp32 per-128x128 block scales"), "parallelism": f"replicas x{world}"}
+    config = workload_config(wl, args, world)
 
     if args.impl == "reference":
         if rank != 0:
             return
         cap = max(5.0, min(60.0, args.cpu_seconds))
-        us, cores, sample = cpu_oracle_rate(wl, cap, mx=args.mx)
-        value = us if t1_metric else 1e6 / us * 1.0
-        unit = "us/layer" if t1_metric else "tokens/s"
+        us_tok, cores, sample = cpu_oracle_rate(wl, cap, mx=args.mx)
+        value = us_tok * T if small else 1e6 / us_tok
+        unit = "us/layer" if small else "tokens/s"
         line = {"impl": "reference", "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": 1,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
-                "higher_is_better": not t1_metric, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_tok * T / 1e3, 3),
+                "higher_is_better": not small, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": cores, "kind": "oracle",
                                  "sample": sample},
@@ -625,60 +740,47 @@ def main():
         print(json.dumps(line))
         return
 
-    r = run_ours(args, dist, rank, world)
-    if rank != 0:
-        return
-    us = r["ms"] * 1e3
-    if t1_metric:
-        value, unit, hib = us, "us/layer", False
-        e2e_value = r["e2e_ms"] * 1e3
-    else:
-        value, unit, hib = r["tokens_per_s"], "tokens/s", True
-        e2e_value = world * T / (r["e2e_ms"] * 1e-3)
-    config["l2"] = f"{r['replicas']} stacked layer replicas rotated so weights stream from HBM (inputs > L2)"
-    peaks = _peaks()
-    if (args.mx and T > 64) or _gemm_path(cfg, T):
-        # contraction on the FP8 tensor cores: peak = measured bf16 burst x nominal FP8/bf16 ratio (2)
-        fp8_peak = 2.0 * peaks["bf16_tflops"] if peaks else 2.0 * 1900.0
-        gu_tflops = _gateup_flops(cfg, T) / (r["gu_ms"] * 1e-3) / 1e12
-        kname = "expert_gemm_mx_kernel<0>" if args.mx else "expert_gemm_kernel<0>"
-        roofline = {"bound": "tensor", "kernel": f"{kname} (gate/up grouped GEMM)",
-                    "achieved": round(gu_tflops, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                    "frac": round(gu_tflops / fp8_peak, 4),
-                    "traffic": NCU_TRAFFIC_BYTES.get((wl.name, kname)),
-                    "peak_source": ("measured bf16 burst x2 (nominal fp8/bf16)" if peaks else "fallback x2"),
-                    "launch_us": round(r["gu_ms"] * 1e3, 3), "flops_per_launch": _gateup_flops(cfg, T)}
-        layer_tflops = _layer_flops(cfg, T) / (r["ms"] * 1e-3) / 1e12
-        extra = {"layer_tflops": round(layer_tflops, 1), "layer_tensor_frac": round(layer_tflops / fp8_peak, 4)}
-    else:
-        kname = "gateup_stream_kernel<true>" if args.mx else "gateup_stream_kernel"
-        roofline = {"bound": "hbm", "kernel": kname, "achieved": round(r["achieved"], 1),
-                    "peak": r["peak"], "unit": "GB/s", "frac": round(r["achieved"] / r["peak"], 4),
-                    "traffic": NCU_TRAFFIC_BYTES.get((wl.name, kname)),
-                    "peak_source": r["peak_src"], "launch_us": round(r["gu_ms"] * 1e3, 3),
-                    "bytes_per_launch": r["gu_bytes"]}
-        extra = {}
-    line = {
-        "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(r["ms"], 5), "higher_is_better": hib, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 (bf16 out)", "data": "synthetic", "config": config,
-        "layer_hbm_gbs": round(r["layer_bytes"] / (r["ms"] * 1e-3) / 1e9, 1),
-        "layer_hbm_frac": round(r["layer_bytes"] / (r["ms"] * 1e-3) / 1e9 / r["peak"], 4),
-        "tokens_per_s": round(r["tokens_per_s"], 1),
-        "experts_touched_per_step": r["n_touched"],
-        "roofline": roofline,
-        "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": T * cfg.hidden * 2,
-                "d2h_bytes_per_step": T * cfg.hidden * 2},
-        **extra,
-        "stages_us": r["stage_us"], "stage_events_on_steps": r["prof_steps"],
-        "gpu_launches": r["launches"], "clocks": r["clocks"], "device_status": r["status"],
-    }
-    if not args.no_cpu_baseline:
-        us_cpu, cores, sample = cpu_oracle_rate(wl, args.cpu_seconds, r["weights"], mx=args.mx)
-        cv = us_cpu if t1_metric else 1e6 / us_cpu
-        line["cpu_baseline"] = {"value": round(cv, 3), "unit": unit, "cores": cores, "kind": "oracle",
-                                "sample": sample}
-    print(json.dumps(line))
+    from mixture_experts_layer_gemv_gb300 import build as lib_build
+    if rank == 0 or not os.path.exists(lib_build.LIB):
+        lib_build.build()
+    _barrier(dist)
+    r = measure(wl, args, args.steps, args.warmup, dist, rank, world)
+    head = summarise(r, wl, args, world)
+
+    def cpu_leg(wl_, weights, seconds):
+        us_tok, cores, sample = cpu_oracle_rate(wl_, seconds, weights, mx=args.mx)
+        small_ = wl_.T <= 64
+        return {"value": round(us_tok * wl_.T if small_ else 1e6 / us_tok, 3),
+                "unit": "us/layer" if small_ else "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    line = {"metric": metric, "value": head.pop("value"), "unit": head.pop("unit"), "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"),
+            "higher_is_better": head.pop("higher_is_better"), "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 x e4m3 -> f32 (bf16 out)", "data": "synthetic", "config": config}
+    head.pop("l2")
+    line.update(head)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_leg(wl, r["weights"], args.cpu_seconds)
+    r = None
+    # the metric's other workloads, each timed the same way at its own size (untimed by the
+    # headline: the headline's timed region covers only the headline workload)
+    if not args.only and args.workload == "dsv2_decode_t1" and not args.mx:
+        subs = {}
+        for name, steps2 in (("dsv2_decode_t64", 200), ("prefill_t4096", 50), ("dsv2_zipf_t2048", 50)):
+            torch.cuda.empty_cache()
+            wl2 = WORKLOADS[name]
+            r2 = measure(wl2, args, steps2, max(3, min(args.warmup, 10)), dist, rank, world, prof_steps=50)
+            s2 = summarise(r2, wl2, args, world)
+            s2["config"] = workload_config(wl2, args, world)
+            s2.pop("l2")
+            s2["steps"], s2["warmup"] = steps2, max(3, min(args.warmup, 10))
+            if rank == 0 and not args.no_cpu_baseline:
+                s2["cpu_baseline"] = cpu_leg(wl2, r2["weights"], args.sub_cpu_seconds)
+            subs[name] = s2
+            r2 = None
+        line["workloads"] = subs
+    if rank == 0:
+        print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
 
