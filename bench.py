@@ -467,6 +467,59 @@ def workload_config(wl, args, world: int) -> dict:
             "l2": l2_note(cfg, T, args.mx, args.replicas)}
 
 
+def trace_timeline(wl, args, steps: int = 48) -> dict:
+    """Where a decode layer's time goes: moe_forward_trace replayed back to back from a
+    CUDA graph (as the timed loop runs), one stamp array per step. Per kernel and event,
+    the earliest, median and latest CTA stamp in us after the router's first CTA start,
+    medians over the steps; plus the step-to-step period."""
+    import ctypes
+
+    from mixture_experts_layer_gemv_gb300 import binding as B
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg, T = wl.cfg, wl.T
+    W0 = make_weights(cfg, wl.seed, dev, zipf=wl.zipf_bias)
+    R = n_replicas(cfg, T, False, args.replicas)
+    layers = [W0] + [replicate_weights(W0) for _ in range(R - 1)]
+    x = make_tokens(cfg, T, wl.seed, dev)
+    ws = B.alloc_workspace(cfg, T, dev)
+    out = torch.empty((T, cfg.hidden), dtype=torch.bfloat16, device=dev)
+    tr = torch.zeros((steps, B.TRACE_WORDS), dtype=torch.int64, device=dev)
+    stream = torch.cuda.Stream(dev)
+    c_ref = ctypes.byref(B.config_struct(cfg))
+    wst = [B.weights_struct(Wl) for Wl in layers]
+    lib = B.lib()
+
+    def step(i, st):
+        r = lib.moe_forward_trace(c_ref, x.data_ptr(), T, ctypes.byref(wst[i % R]), None, out.data_ptr(),
+                                  ws.data_ptr(), ws.numel(), st, tr[i].data_ptr())
+        if r != 0:
+            raise B.MoeError("moe_forward_trace", r, B.status_string(r))
+
+    for i in range(steps):
+        step(i, stream.cuda_stream)
+    torch.cuda.synchronize()
+    tr.zero_()
+    _timed_graph_loop(step, steps, steps, stream)
+    t = tr.view(steps, 4, B.TRACE_CTAS, 4).cpu().numpy().astype(np.float64)
+    res = {}
+    t0 = np.array([t[s, 0, :, 0][t[s, 0, :, 0] > 0].min() for s in range(steps)])
+    period = np.diff(t0)
+    res["step_period_us"] = round(float(np.median(period)) / 1e3, 3)
+    for k, kn in enumerate(B.TRACE_KERNELS):
+        for e, en in enumerate(B.TRACE_EVENTS):
+            vals = []
+            for s in range(1, steps):  # the first replay's predecessor differs
+                v = t[s, k, :, e]
+                v = v[v > 0]
+                if v.size:
+                    vals.append(((v.min() - t0[s]) / 1e3, (np.median(v) - t0[s]) / 1e3, (v.max() - t0[s]) / 1e3))
+            if vals:
+                a = np.median(np.array(vals), axis=0)
+                res[f"{kn}.{en}"] = [round(float(q), 2) for q in a]
+    return res
+
+
 def cpu_oracle_rate(wl, limit_s: float, weights=None, mx: bool = False):
     """Time the oracle (as it stands) on a bounded sample of the workload: independent
     T-token layer calls' worth of tokens, all host cores. Returns (us per layer call, cores, sample)."""
@@ -705,6 +758,8 @@ def main():
     ap.add_argument("--sub-cpu-seconds", type=float, default=5.0,
                     help="oracle time cap for each of the extra workloads in the default run")
     ap.add_argument("--only", action="store_true", help="the named workload alone (no extra workloads)")
+    ap.add_argument("--trace", action="store_true",
+                    help="print the decode kernels' per-CTA timeline (moe_forward_trace) instead of timing")
     ap.add_argument("--mx", action="store_true", help="the MXFP8 variant (E8M0 scales per 32 K)")
     ap.add_argument("--backward", action="store_true",
                     help="the layer backward (moe_backward) instead of the forward; use with --workload prefill_t4096")
@@ -744,6 +799,10 @@ def main():
     if rank == 0 or not os.path.exists(lib_build.LIB):
         lib_build.build()
     _barrier(dist)
+    if args.trace:
+        if rank == 0:
+            print(json.dumps({"workload": wl.name, "trace_us": trace_timeline(wl, args)}))
+        return
     r = measure(wl, args, args.steps, args.warmup, dist, rank, world)
     head = summarise(r, wl, args, world)
 

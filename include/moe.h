@@ -225,6 +225,22 @@ moe_status_t moe_forward_profiled(const moe_config_t* cfg, const void* x_bf16, i
                                   void* out_bf16, int32_t* topk_ids_out, void* ws, size_t ws_bytes,
                                   void* stream, const moe_stage_events_t* events);
 
+/* moe_forward with per-CTA timestamps, for attributing the layer's time to its kernels
+ * the way the DSV2-236B-MegaKernel README's per-stage table does (that page stamps each
+ * stage with in-kernel clocks). trace is a DEVICE array of MOE_TRACE_WORDS uint64 owned by
+ * the caller (16-byte aligned; NULL returns MOE_ERR_INVALID_ARG). The call writes
+ *   trace[(kernel * MOE_TRACE_CTAS + cta) * 4 + event] = GPU global timer (ns)
+ * for kernel 0 router (+ top-k and permutation), 1 gate/up, 2 down, 3 combine; event 0
+ * CTA start, 1 its wait for the previous kernel returned, 2 first data consumed (router:
+ * logits stored; down: first operand built), 3 CTA done. Only the decode kernels (T <= 64)
+ * stamp; entries no CTA writes keep their previous contents, so clear the array first.
+ * The stamps cost a few stores per CTA; the results equal moe_forward's. */
+#define MOE_TRACE_CTAS 512
+#define MOE_TRACE_WORDS (4 * MOE_TRACE_CTAS * 4)
+moe_status_t moe_forward_trace(const moe_config_t* cfg, const void* x_bf16, int32_t T,
+                               const moe_weights_t* weights, const void* residual_bf16, void* out_bf16,
+                               void* ws, size_t ws_bytes, void* stream, uint64_t* trace);
+
 /* Stages M..R of the MoE block in one call, the residual stream in and out:
  *   out = h + layer(RMSNorm(h))      (stage M as in moe_rmsnorm, the layer as in
  *                                     moe_forward with residual = h)

@@ -77,6 +77,7 @@ _SIGNATURES = {
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P]),
     "moe_forward": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_profiled": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "moe_forward_trace": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_workspace_size_mx": (_SZ, [_P, _I32]),
     "moe_quant_act_mx": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "moe_forward_mx": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -235,6 +236,22 @@ def moe_forward(cfg, x, weights, out, residual=None, topk_ids_out=None, ws=None,
         return
     _check("moe_forward", lib().moe_forward(ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W), _ptr(residual),
                                             _ptr(out), _ptr(topk_ids_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+TRACE_CTAS = 512
+TRACE_WORDS = 4 * TRACE_CTAS * 4
+TRACE_KERNELS = ("route", "gate_up", "down", "combine")
+TRACE_EVENTS = ("start", "wait_done", "first_data", "done")
+
+
+def moe_forward_trace(cfg, x, weights, out, trace, residual=None, ws=None, stream=None) -> None:
+    """moe_forward that also writes per-CTA global-timer stamps into trace (int64 device
+    tensor of TRACE_WORDS): trace.view(4, TRACE_CTAS, 4)[kernel, cta, event] in ns."""
+    c = config_struct(cfg)
+    W = weights_struct(weights)
+    _check("moe_forward_trace", lib().moe_forward_trace(ctypes.byref(c), _ptr(x), x.shape[0], ctypes.byref(W),
+                                                        _ptr(residual), _ptr(out), _ptr(ws), ws.numel(),
+                                                        _stream(stream), _ptr(trace)))
 
 
 def _events_struct(events):

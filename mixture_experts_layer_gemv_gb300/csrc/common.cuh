@@ -233,6 +233,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Trace stamps (moe_forward_trace): trace[(kernel * kTraceCtas + cta) * 4 + event] = the
+// global timer in ns; kernel 0 route, 1 gate/up, 2 down, 3 combine; event 0 CTA entry,
+// 1 dependency wait returned, 2 first data consumed, 3 CTA done. Null: nothing recorded.
+constexpr int kTraceCtas = 512;
+__device__ __forceinline__ void trace_stamp(uint64_t* tr, int kernel, int ev) {
+    if (tr != nullptr && blockIdx.x < (unsigned)kTraceCtas)
+        tr[((size_t)kernel * kTraceCtas + blockIdx.x) * 4 + ev] = globaltimer_ns();
+}
+
 // Upper bound on the wall time of one wait; no legitimate wait in this library comes
 // near it (the longest are TMA copies from HBM, microseconds).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -249,6 +258,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
         if ((i & 15) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
     return false;
+}
+
+// mbar_wait_bounded for a whole warp: lane 0 alone polls the barrier (32 lanes polling one
+// mbarrier contend with the thread that fills the stages) and the warp then synchronises,
+// which orders the other lanes' reads of the stage after lane 0's observation of the
+// completed phase. Every lane gets the same result. Call with the whole warp.
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // 2-D tiled TMA load of box {x (inner, bytes of an 8-bit tensor), y (rows)} into

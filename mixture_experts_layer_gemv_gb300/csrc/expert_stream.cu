@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int H = a.H, Hb = H / kBlk;
+    if (tid == 0) trace_stamp(a.trace, 1, 0);
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     pdl_wait();  // routing, activation codes and the work list are complete
     pdl_launch_dependents();
+    if (tid == 0) trace_stamp(a.trace, 1, 1);
 
     const int slices_r = a.I / kTile, slices_s = a.Is / kTile;
     const Plan pl = gateup_plan(a);
@@ -253,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     box_dot(cu, st + kBox, st + 2 * kBox + g * kRowPitch, bv, warp, g, t4);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[s]);
+                    if (tid == 0 && i == 0 && j == 0) trace_stamp(a.trace, 1, 2);
                 }
                 acc[0][0] = fmaf(cg[0], swg * sx0, acc[0][0]);
                 acc[0][1] = fmaf(cg[1], swg * sx1, acc[0][1]);
@@ -270,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!failed) store_rec<2>(acc, r, r.shared ? pts : pt);
     }
+    if (tid == 0) trace_stamp(a.trace, 1, 3);
 }
 
 // ======================================================================= down
@@ -292,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = lane >> 2, t4 = lane & 3;
     const int H = a.H, Ib = a.I / kBlk, Isb = a.Is / kBlk;
     const int slices = H / kTile;
+    if (tid == 0) trace_stamp(a.trace, 2, 0);
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -354,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     pdl_wait();  // the gate/up tiles are complete
     pdl_launch_dependents();
+    if (tid == 0) trace_stamp(a.trace, 2, 1);
     if (!active) return;
 
     const Plan pl_gu = gateup_plan(a);
@@ -403,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (grp != cur_group) {
             named_bar(1, kConsThreads);  // every warp is done with the previous operand
             build_operand(r);
+            if (tid == 0 && i == 0) trace_stamp(a.trace, 2, 2);
             cur_group = grp;
         }
         const float* swr = nullptr;
@@ -475,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_rec<1>(vals, r, r.shared ? pts : pt);
         }
     }
+    if (tid == 0) trace_stamp(a.trace, 2, 3);
 }
 
 // ==================================================================== combine
@@ -482,8 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // rounding; or, for the stage API, the bf16 expert rows y_perm / y_shared themselves.
 // Each thread owns 4 consecutive hidden channels of one token (or one row).
 __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a) {
+    if (threadIdx.x == 0) trace_stamp(a.trace, 3, 0);
     pdl_wait();  // the down tiles are complete
     pdl_launch_dependents();
+    if (threadIdx.x == 0) trace_stamp(a.trace, 3, 1);
     const int H = a.H;
     const Plan pl = down_plan(a);
     const int H4 = H / 4;
@@ -561,6 +571,7 @@ __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a)
             }
             store4(a.out + (size_t)tok * H + h, v);
         }
+        if (threadIdx.x == 0) trace_stamp(a.trace, 3, 3);
     } else {
         const long nr = (long)Tk * H4, ns = a.n_shared_groups > 0 ? (long)a.T * H4 : 0;
         for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nr + ns; i += (long)gridDim.x * blockDim.x) {

@@ -21,6 +21,8 @@ int num_sms() {
     return n;
 }
 
+static_assert(kTraceCtas == MOE_TRACE_CTAS, "trace layout of moe.h");
+
 static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 int router_splits_for(const moe_config_t& c, int64_t T) {
@@ -681,7 +683,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm_bf16, const
 static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, int32_t T,
                                  const moe_weights_t* weights, const void* residual_bf16, void* out_bf16,
                                  int32_t* topk_ids_out, void* ws, size_t ws_bytes, void* stream,
-                                 const moe_stage_events_t* events, NormArgs nm) {
+                                 const moe_stage_events_t* events, NormArgs nm, uint64_t* trace = nullptr) {
     MOE_TRY(check_cfg(cfg));
     MOE_TRY(check_T(cfg, T));
     if (T == 0) return MOE_OK;
@@ -705,7 +707,7 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
         MOE_CUDA(launch_route_small(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
                                     at<float>(ws, L.logits), at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
                                     at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups,
-                                    at<int32_t>(ws, L.group_of_row), ctrl, nm, st));
+                                    at<int32_t>(ws, L.group_of_row), ctrl, nm, st, nullptr, trace));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
     } else {
         if (nm.gamma) {
@@ -744,6 +746,7 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
     a.fuse_combine = 1;
     a.residual = static_cast<const __nv_bfloat16*>(residual_bf16);
     a.out = static_cast<__nv_bfloat16*>(out_bf16);
+    a.trace = trace;
     MOE_TRY(mark.begin(MOE_STAGE_GATE_UP));
     MOE_CUDA(launch_gateup_stream(a, weights->w_gate, weights->w_up, cfg->n_routed, st));
     MOE_TRY(mark.end(MOE_STAGE_GATE_UP));
@@ -772,6 +775,14 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x_bf16, int32_t T,
                          size_t ws_bytes, void* stream) {
     return forward_impl(cfg, x_bf16, T, weights, residual_bf16, out_bf16, topk_ids_out, ws, ws_bytes, stream,
                         nullptr, NormArgs{});
+}
+
+moe_status_t moe_forward_trace(const moe_config_t* cfg, const void* x_bf16, int32_t T, const moe_weights_t* weights,
+                               const void* residual_bf16, void* out_bf16, void* ws, size_t ws_bytes, void* stream,
+                               uint64_t* trace) {
+    if (!trace || !aligned16(trace)) return MOE_ERR_INVALID_ARG;
+    return forward_impl(cfg, x_bf16, T, weights, residual_bf16, out_bf16, nullptr, ws, ws_bytes, stream, nullptr,
+                        NormArgs{}, trace);
 }
 
 moe_status_t moe_forward_rmsnorm_profiled(const moe_config_t* cfg, const void* h_bf16, int32_t T,

@@ -112,7 +112,8 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
                                const float* bias, int32_t* ids, float* w, float* logits,
                                uint8_t* xq, float* xs, int32_t* offsets, int32_t* perm_src,
                                int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl,
-                               const NormArgs& nm, cudaStream_t st, uint8_t* xs8 = nullptr);
+                               const NormArgs& nm, cudaStream_t st, uint8_t* xs8 = nullptr,
+                               uint64_t* trace = nullptr);
 
 // Large-T route: router GEMM (split-K partials) + softmax/top-k per token. With
 // nm.gamma the router reads stage M's output on the fly (nm.rstd from launch_rmsnorm).
@@ -182,6 +183,7 @@ struct StreamArgs {
     const __nv_bfloat16* residual;
     __nv_bfloat16* out;
     int* status;
+    uint64_t* trace;  // per-CTA timer stamps (moe_forward_trace) or null
 };
 
 struct GemmArgs {
@@ -272,7 +274,6 @@ cudaError_t launch_gateup_stream(const StreamArgs& a, const uint8_t* w_gate, con
 cudaError_t launch_down_stream(const StreamArgs& a, const uint8_t* w_down, const uint8_t* ws_down, int E,
                                cudaStream_t st);
 cudaError_t launch_stream_combine(const StreamArgs& a, cudaStream_t st);
-
 cudaError_t launch_combine(int T, int H, int k, const __nv_bfloat16* y_perm, const int32_t* inv_pos,
                            const __nv_bfloat16* y_shared, const __nv_bfloat16* residual,
                            __nv_bfloat16* out, cudaStream_t st);

@@ -45,6 +45,7 @@ struct RouteSmallParams {
     const uint16_t* gamma;  // stage M in front of the router when not null
     float eps;
     uint8_t* xs8;           // MXFP8: E8M0 scales [T, H/32] (xs unused)
+    uint64_t* trace;        // per-CTA timer stamps or null
 };
 
 // kNorm: stage M in front of the router (p.gamma != nullptr); kMX: x quantised per 32
@@ -83,8 +84,10 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
             gv[j] = norm && i < n4 ? __ldg(grow + i) : make_uint2(0, 0);
         }
     };
+    trace_stamp(p.trace, 0, 0);
     pdl_wait();  // the previous kernel in the stream is done: inputs written, workspace free
     pdl_launch_dependents();
+    trace_stamp(p.trace, 0, 1);
     load_w(0);
     const float bias_e = p.bias ? __ldg(p.bias + e) : 0.f;
 
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
         if (p.bias) l += bias_e;
         p.logits[(size_t)t * p.E + e] = l;
     }
+    trace_stamp(p.trace, 0, 2);
 
     // ---- activation quantisation: this CTA's share of the T*H/128 blocks
     for (int b = blockIdx.x * kRouteWarps + warp; b < T * Hb; b += gridDim.x * kRouteWarps) {
@@ -180,7 +184,10 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
         s_last = (prev == gridDim.x - 1);
     }
     __syncthreads();
-    if (!s_last) return;
+    if (!s_last) {
+        trace_stamp(p.trace, 0, 3);
+        return;
+    }
     __threadfence();
 
     if (T == 1 && p.E <= (int)blockDim.x) {
@@ -205,6 +212,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
         small_permute(s_ids, T * p.k, p.E, s_cnt, s_off, s_gcnt, s_goff, s_rank, p.offsets, p.perm_src, p.inv_pos,
                       p.groups, p.group_of_row, p.ctrl);
     if (threadIdx.x == 0) p.ctrl->route_arrived = 0u;
+    trace_stamp(p.trace, 0, 3);
 }
 
 // ---------------------------------------------------------------- large T
@@ -507,7 +515,7 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
                                const float* bias, int32_t* ids, float* w, float* logits, uint8_t* xq,
                                float* xs, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
                                RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl, const NormArgs& nm,
-                               cudaStream_t st, uint8_t* xs8) {
+                               cudaStream_t st, uint8_t* xs8, uint64_t* trace) {
     RouteSmallParams p;
     p.H = c.hidden;
     p.E = c.n_routed;
@@ -533,6 +541,7 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
     p.gamma = nm.gamma;
     p.eps = nm.eps;
     p.xs8 = nullptr;
+    p.trace = trace;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.n_routed);
     cfg.blockDim = dim3(kRouteWarps * 32);
