@@ -41,7 +41,7 @@ namespace {
 using namespace stream;
 
 __device__ __forceinline__ TileSpace gateup_space(const StreamArgs& a, int P) {
-    return TileSpace{a.ctrl->n_routed_groups * (a.I / kTile), a.H / kBlk, a.n_shared_groups * (a.Is / kTile),
+    return TileSpace{routed_groups(a.ctrl) * (a.I / kTile), a.H / kBlk, a.n_shared_groups * (a.Is / kTile),
                      a.H / kBlk, P};
 }
 __device__ __forceinline__ Plan gateup_plan(const StreamArgs& a) {
@@ -50,7 +50,7 @@ __device__ __forceinline__ Plan gateup_plan(const StreamArgs& a) {
 }
 __device__ __forceinline__ TileSpace down_space(const StreamArgs& a, int P) {
     const int slices = a.H / kTile;
-    return TileSpace{a.ctrl->n_routed_groups * slices, a.I / kBlk, a.n_shared_groups * slices, a.Is / kBlk, P};
+    return TileSpace{routed_groups(a.ctrl) * slices, a.I / kBlk, a.n_shared_groups * slices, a.Is / kBlk, P};
 }
 __device__ __forceinline__ Plan down_plan(const StreamArgs& a) {
     const TileSpace t = down_space(a, 1);

@@ -371,3 +371,28 @@ def test_grouped_gemm_expert_segments_on_tile_boundaries():
             y_ref, _ = oracle.expert_row(cfg, OW, xc[tok], int(ids[tok, j]), float(w[tok, j]))
             assert_out_close(y_perm[inv[tok * k + j]], y_ref, f"row ({tok},{j}) expert {ids[tok, j]}")
         assert_out_close(y_sh[tok], oracle.shared_row(cfg, OW, xc[tok]), f"shared {tok}")
+
+
+@pytest.mark.parametrize("name", ["dsv2_decode_t1", "dsv2_decode_t64", "tiny_t8"])
+def test_back_to_back_forwards_on_one_workspace(name):
+    # 60 forwards enqueued back to back on one workspace, no synchronisation between them,
+    # alternating two inputs whose routings differ, so that a kernel reading the previous
+    # call's routing data (a stale work list, permutation or weight) would change its
+    # output: every call must equal the same input's result computed alone
+    wl, W, x, _ = _layer(name)
+    xb = make_tokens(wl.cfg, wl.T, wl.seed + 77, "cuda", name="x_other")
+    ws = B.alloc_workspace(wl.cfg, wl.T)
+    refs = []
+    for xi in (x, xb):
+        o = torch.empty_like(xi)
+        B.moe_forward(wl.cfg, xi, W, o, ws=ws)
+        torch.cuda.synchronize()
+        refs.append(o)
+    assert not torch.equal(refs[0], refs[1])
+    outs = [torch.empty_like(x) for _ in range(60)]
+    for i, o in enumerate(outs):
+        B.moe_forward(wl.cfg, x if i % 2 == 0 else xb, W, o, ws=ws)
+    torch.cuda.synchronize()
+    assert B.moe_read_device_status(ws) == 0
+    bad = [i for i, o in enumerate(outs) if not torch.equal(o, refs[i % 2])]
+    assert not bad, f"calls {bad[:10]} differ from their input's result"
