@@ -119,10 +119,30 @@ size_t moe_workspace_size(const moe_config_t* cfg, int32_t max_tokens);
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Device-side error word of ws: copies it to the host (synchronising `stream`), clears
- * it, and returns MOE_OK or the recorded error (MOE_ERR_DEVICE_TIMEOUT when a bounded
- * wait inside a kernel gave up; such a kernel skips its remaining work and returns
- * instead of hanging). Every bounded wait has an iteration limit; none traps. */
+ * it, and returns MOE_OK or the recorded error:
+ *   MOE_ERR_DEVICE_TIMEOUT  a bounded wait inside a kernel gave up (that kernel skips its
+ *                           remaining work and returns instead of hanging; every bounded
+ *                           wait has a time and an iteration limit, none traps);
+ *   MOE_ERR_INVALID_ARG     a kernel met invalid device data and left it out: an expert id
+ *                           outside [0, E) given to moe_permute, a perm_src entry outside
+ *                           [0, T*k), or expert offsets that do not cover the permuted rows.
+ * A timeout takes precedence when both were recorded. The outputs of a call that recorded
+ * an error are unspecified. */
 moe_status_t moe_read_device_status(void* ws, void* stream);
+
+/* Failure-detection test hook (the pages have no counterpart; a test uses it to make a
+ * device-side wait run out on purpose, in the permitted form: a flag that nothing sets).
+ * Sets the workspace's fault-injection word for the calls that follow on it,
+ * asynchronously on `stream`:
+ *   MOE_INJECT_SKIP_GATEUP_LOADS  the decode gate/up kernel (T <= 64 tokens) issues no
+ *       copies, so its consumers' bounded waits run out (after about one second) with
+ *       nothing in flight; such a call records MOE_ERR_DEVICE_TIMEOUT
+ *       (moe_read_device_status) and its outputs are unspecified;
+ *   0  clears it.
+ * Other words of the workspace are not touched. Errors: MOE_ERR_WORKSPACE (ws NULL or
+ * ws_bytes below the control region), MOE_ERR_INVALID_ARG (an unknown bit). */
+#define MOE_INJECT_SKIP_GATEUP_LOADS 1u
+moe_status_t moe_debug_set(void* ws, size_t ws_bytes, uint32_t inject, void* stream);
 
 /* Activation quantisation, the FP8 operand of the expert GEMMs: per token and block of
  * 128 channels, scale = the smallest power of two 2^k with amax <= 448 * 2^k
@@ -182,8 +202,10 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const void* x_bf16, int3
  *   expert_offsets int32 [E+1]: pairs routed to experts < e (exclusive prefix sum)
  *   perm_src       int32 [T*k]: flat index of the pair at each permuted position
  *   inv_pos        int32 [T*k]: permuted position of each flat index
- * Within one expert the pairs keep ascending f. Ids outside [0, E) are an error the
- * library does not check on the device: they must come from moe_route.
+ * Within one expert the pairs keep ascending f. An id outside [0, E) is checked on the
+ * device: its pair is left out of the permutation and the workspace status records it
+ * (moe_read_device_status then returns MOE_ERR_INVALID_ARG); ids from moe_route are
+ * always valid.
  * (The router produces the layout the expert GEMMs consume: DeepSeek-V4.1 Flash
  * lecture, "Rounds 12-15" table; MoK's GPU-side dispatch scheduling, abstract.) */
 moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, int32_t T,

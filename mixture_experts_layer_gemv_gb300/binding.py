@@ -59,6 +59,7 @@ _SIGNATURES = {
     "moe_workspace_size": (_SZ, [_P, _I32]),
     "moe_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
     "moe_read_device_status": (ctypes.c_int, [_P, _P]),
+    "moe_debug_set": (ctypes.c_int, [_P, _SZ, ctypes.c_uint32, _P]),
     "moe_backward_workspace_size": (_SZ, [_P, _I32]),
     "moe_backward": (ctypes.c_int, [_P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                     _P]),
@@ -154,6 +155,16 @@ def alloc_workspace(cfg: MoEConfig, max_tokens: int, device="cuda") -> torch.Ten
     ws = torch.empty(n, dtype=torch.uint8, device=device)
     moe_workspace_init(ws)
     return ws
+
+
+INJECT_SKIP_GATEUP_LOADS = 1
+
+
+def moe_debug_set(ws: torch.Tensor, inject: int = 0, stream=None) -> None:
+    """Failure-detection test hook: the fault-injection bits for the calls that follow on
+    ws (see moe.h); 0 clears them."""
+    _check("moe_debug_set", lib().moe_debug_set(_ptr(ws), ws.numel() * ws.element_size(), int(inject),
+                                                _stream(stream)))
 
 
 def moe_read_device_status(ws: torch.Tensor, stream=None) -> int:

@@ -480,6 +480,10 @@ __host__ __device__ constexpr uint32_t idesc_f8_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
 
+// Fault-injection bits of Ctrl::inject (failure-detection tests): the decode gate/up
+// kernel's producer issues no copies, so its consumers' bounded waits run out.
+enum : unsigned { kInjectSkipGateupLoads = 1u };
+
 // ----------------------------------------------------------- status word
 // kStatusTimeout: a bounded wait gave up; kStatusBadId: an expert id outside [0, E)
 // reached the permutation (the offending item is skipped).

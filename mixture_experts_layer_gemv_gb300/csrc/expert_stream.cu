@@ -77,12 +77,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int H = a.H, Hb = H / kBlk;
     if (tid == 0) trace_stamp(a.trace, 1, 0);
 
+    // the fault-injection word the host wrote before the call (read while the router runs)
+    __shared__ unsigned s_inject;
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCons);
         }
         fence_mbar_init();
+        s_inject = __ldcg(&a.ctrl->inject);
     }
     for (int s = 0; s < S; ++s)  // activation rows beyond a group's size are read but masked
         for (int i = tid; i < kBRows / 16; i += kThreads)
@@ -131,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kCons) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
+        // failure-detection tests: issue nothing, so that every consumer wait runs out
+        if (s_inject & kInjectSkipGateupLoads) return;
         int s = 0, ph = 0;
         long q = 0;  // units issued
         bool stop = false;

@@ -2,6 +2,7 @@
 // the launch sequence of each entry point. No entry point allocates memory or
 // synchronises the host, except moe_read_device_status (documented).
 #include <algorithm>
+#include <cstddef>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -453,6 +454,16 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
     MOE_CUDA(cudaMemsetAsync(ws, 0, ws_bytes < kCtrlRegionBytes ? ws_bytes : kCtrlRegionBytes,
                              (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status_t moe_debug_set(void* ws, size_t ws_bytes, uint32_t inject, void* stream) {
+    static_assert(kInjectSkipGateupLoads == MOE_INJECT_SKIP_GATEUP_LOADS, "inject bit of moe.h");
+    if (!ws || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
+    if (inject & ~kInjectSkipGateupLoads) return MOE_ERR_INVALID_ARG;
+    const uint32_t word = inject;  // staged by the copy before it returns
+    MOE_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(ws) + offsetof(Ctrl, inject), &word, sizeof(word),
+                             cudaMemcpyHostToDevice, (cudaStream_t)stream));
     return MOE_OK;
 }
 

@@ -23,7 +23,8 @@ struct Ctrl {
     unsigned route_arrived;  // last-block-done counter of the fused router
     int n_routed_groups;     // work descriptors written by the permutation
     int n_mtiles;            // 128-row token tiles of the routed experts (grouped GEMM)
-    int pad[60];
+    unsigned inject;         // fault injection for failure-detection tests (moe_debug_set), normally 0
+    int pad[59];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 

@@ -93,15 +93,10 @@ __device__ __forceinline__ Plan make_plan(int n_r, int kc_r, int n_s, int kc_s, 
 
 // The routing data the tile decoders read (the work list, perm_src, topk_w, the group
 // count) is written by the router kernel. The down kernel decodes its tiles before its own
-// dependency wait: that data was complete before the gate/up kernel's wait returned, and
-// the down kernel is launched only after that, but the SM's L1 may still hold lines of the
-// same workspace addresses from the previous call. So it is read through L2
-// (ld.global.cg), where the router's writes are.
-__device__ __forceinline__ RowGroup ldcg_group(const RowGroup* p) {
-    const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
-    return RowGroup{v.x, v.y, v.z, v.w};
-}
-__device__ __forceinline__ int routed_groups(const Ctrl* c) { return __ldcg(&c->n_routed_groups); }
+// dependency wait: the router had completed, its writes visible, before the gate/up
+// kernel's wait returned, and the down kernel is launched only after every gate/up CTA
+// has passed that wait.
+__device__ __forceinline__ int routed_groups(const Ctrl* c) { return c->n_routed_groups; }
 
 // A tile decoded: which row group, which 128-row slice of the output, which K part.
 struct TileInfo {
@@ -121,7 +116,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TileSpace& ts, long t, int
     if (t < (long)ts.n_r * ts.P) {
         const long row = t / ts.P;
         const int gi = (int)(row / slices_r);
-        const RowGroup rg = ldcg_group(groups + gi);
+        const RowGroup rg = groups[gi];
         ti.shared = 0;
         ti.expert = rg.expert;
         ti.group = gi;
@@ -255,11 +250,11 @@ __device__ inline TileRec make_rec(const TileSpace& ts, const Range& rg, long t,
     int f[kGroupRows];
 #pragma unroll
     for (int c = 0; c < kGroupRows; ++c)
-        f[c] = (c < ti.nrows && !ti.shared) ? __ldcg(perm_src + ti.row_begin + c) : -1;
+        f[c] = (c < ti.nrows && !ti.shared) ? perm_src[ti.row_begin + c] : -1;
 #pragma unroll
     for (int c = 0; c < kGroupRows; ++c) {
         if (topk_w) {
-            r.w[c] = c >= ti.nrows ? 0.f : ti.shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? __ldcg(topk_w + f[c]) : 0.f);
+            r.w[c] = c >= ti.nrows ? 0.f : ti.shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? topk_w[f[c]] : 0.f);
         } else {
             r.tok[c] = c >= ti.nrows ? -1 : ti.shared ? ti.row_begin + c : ((unsigned)f[c] < (unsigned)Tk ? f[c] / k : -1);
         }

@@ -114,3 +114,11 @@ def test_backward_workspace_and_argument_checks(L):
                           None, None, None, None, 0, None) == -1
     assert L.moe_backward(ctypes.byref(c), None, 8, ctypes.byref(w), None, None, None, None, None, None, None,
                           None, None, None, None, None, None, 0, None) == -1
+
+
+def test_debug_set_checks_its_arguments_before_any_device_work():
+    from mixture_experts_layer_gemv_gb300 import binding as B
+    lib = B.lib()
+    assert lib.moe_debug_set(None, 4096, 0, None) == -3                 # MOE_ERR_WORKSPACE
+    assert lib.moe_debug_set(ctypes.c_void_p(4096), 16, 0, None) == -3  # below the control region
+    assert lib.moe_debug_set(ctypes.c_void_p(4096), 4096, 2, None) == -1  # unknown inject bit
