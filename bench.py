@@ -496,6 +496,7 @@ def trace_timeline(wl, args, steps: int = 48) -> dict:
         if r != 0:
             raise B.MoeError("moe_forward_trace", r, B.status_string(r))
 
+    torch.cuda.synchronize()  # weights, tokens and the workspace's init (current stream) before `stream`
     for i in range(steps):
         step(i, stream.cuda_stream)
     torch.cuda.synchronize()

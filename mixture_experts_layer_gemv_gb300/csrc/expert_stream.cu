@@ -40,28 +40,34 @@ namespace {
 
 using namespace stream;
 
-__device__ __forceinline__ TileSpace gateup_space(const StreamArgs& a, int P) {
-    return TileSpace{routed_groups(a.ctrl) * (a.I / kTile), a.H / kBlk, a.n_shared_groups * (a.Is / kTile),
-                     a.H / kBlk, P};
+template <typename Ix>
+__device__ __forceinline__ TileSpace<Ix> gateup_space(const StreamArgs& a, int ng, int P) {
+    return TileSpace<Ix>{(Ix)ng * (a.I / kTile), a.H / kBlk, (Ix)a.n_shared_groups * (a.Is / kTile), a.H / kBlk, P};
 }
-__device__ __forceinline__ Plan gateup_plan(const StreamArgs& a) {
-    const TileSpace t = gateup_space(a, 1);
-    return make_plan(t.n_r, t.kc_r, t.n_s, t.kc_s, a.grid_gu, a.max_parts);
+template <typename Ix>
+__device__ __forceinline__ Plan gateup_plan(const StreamArgs& a, int ng) {
+    return make_plan<Ix>((Ix)ng * (a.I / kTile), a.H / kBlk, (Ix)a.n_shared_groups * (a.Is / kTile), a.H / kBlk,
+                         a.grid_gu, a.max_parts);
 }
-__device__ __forceinline__ TileSpace down_space(const StreamArgs& a, int P) {
+template <typename Ix>
+__device__ __forceinline__ TileSpace<Ix> down_space(const StreamArgs& a, int ng, int P) {
     const int slices = a.H / kTile;
-    return TileSpace{routed_groups(a.ctrl) * slices, a.I / kBlk, a.n_shared_groups * slices, a.Is / kBlk, P};
+    return TileSpace<Ix>{(Ix)ng * slices, a.I / kBlk, (Ix)a.n_shared_groups * slices, a.Is / kBlk, P};
 }
-__device__ __forceinline__ Plan down_plan(const StreamArgs& a) {
-    const TileSpace t = down_space(a, 1);
-    return make_plan(t.n_r, t.kc_r, t.n_s, t.kc_s, a.grid_d, a.max_parts);
+template <typename Ix>
+__device__ __forceinline__ Plan down_plan(const StreamArgs& a, int ng) {
+    const int slices = a.H / kTile;
+    return make_plan<Ix>((Ix)ng * slices, a.I / kBlk, (Ix)a.n_shared_groups * slices, a.Is / kBlk, a.grid_d,
+                         a.max_parts);
 }
 
 __device__ __forceinline__ uint32_t ldg32(const uint8_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
 
 // ================================================================== gate / up
 // kMX: MXFP8 weights and activations (E8M0 scales per row / token and 32 K)
-template <bool kMX>
+// kLocal: the routing is derived here from the router's logits (local_route); only the
+// int-indexed instantiations have it
+template <bool kMX, typename Ix, bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
     gateup_stream_kernel(const StreamArgs a, const __grid_constant__ TmaMap tm_g, const __grid_constant__ TmaMap tm_u,
                          const __grid_constant__ TmaMap tm_sg, const __grid_constant__ TmaMap tm_su) {
@@ -113,22 +119,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     if (tid == 0) trace_stamp(a.trace, 1, 1);
 
+    // the routing data in one round of loads, then the plan and this CTA's tiles, with
+    // the token of every activation row, from shared memory
+    __shared__ RouteSmem s_route;
+    RouteView rv;
+    if constexpr (kLocal) {
+        __shared__ LocalRouteSmem s_local;
+        rv = local_route(&s_route, &s_local, a, blockIdx.x == 0, false, tid, kThreads);
+    } else {
+        rv = load_route(&s_route, a.ctrl, a.groups, a.max_groups, a.perm_src, nullptr, a.T * a.k, a.E, a.status, tid,
+                        kThreads);
+    }
     const int slices_r = a.I / kTile, slices_s = a.Is / kTile;
-    const Plan pl = gateup_plan(a);
-    const TileSpace ts = gateup_space(a, pl.P);
-    const Range rg = make_range(ts, pl.nb, blockIdx.x);
+    const Plan pl = gateup_plan<Ix>(a, rv.n_groups);
+    const TileSpace<Ix> ts = gateup_space<Ix>(a, rv.n_groups, pl.P);
+    const Range<Ix> rg = make_range(ts, pl.nb, blockIdx.x);
     if (blockIdx.x >= pl.nb || rg.u1 <= rg.u0) return;
     const Partials pt{{a.g_r, a.u_r}, {a.gb_r, a.ub_r}, (long)a.T * a.k, a.I};
     const Partials pts{{a.g_s, a.u_s}, {a.gb_s, a.ub_s}, (long)a.T, a.Is};
-    // this CTA's tiles, with the token of every activation row
     __shared__ TileRec s_tab[kMaxTab];
-    const int ntiles = build_table(s_tab, ts, rg, slices_r, slices_s, a.groups, a.T, a.k, a.perm_src, nullptr,
-                                   tid, kThreads);
+    const int ntiles = build_table(s_tab, ts, rg, slices_r, slices_s, rv, a.T, a.k, tid, kThreads);
     __syncthreads();
     auto rec = [&](int i) {
-        return i < kMaxTab ? s_tab[i]
-                           : make_rec(ts, rg, rg.first_tile + i, slices_r, slices_s, a.groups, a.T, a.k, a.perm_src,
-                                      nullptr);
+        return i < kMaxTab ? s_tab[i] : make_rec_far(ts, rg, rg.first_tile + (Ix)i, slices_r, slices_s, rv, a.T, a.k);
     };
 
     if (warp == kCons) {
@@ -136,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane != 0) return;
         // failure-detection tests: issue nothing, so that every consumer wait runs out
         if (s_inject & kInjectSkipGateupLoads) return;
+        const uint64_t wpol = l2_policy_evict_first();  // used when a.stream_once
         int s = 0, ph = 0;
         long q = 0;  // units issued
         bool stop = false;
@@ -160,8 +174,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = r.kb0 + j;
                 uint8_t* st = smem + s * SB;
                 mbar_arrive_expect_tx(&full[s], 2 * kBox + nrow * kBlk);
-                tma_load_2d(st, mg, kb * kBlk, y, &full[s]);
-                tma_load_2d(st + kBox, mu, kb * kBlk, y, &full[s]);
+                if (a.stream_once) {
+                    tma_load_2d_hint(st, mg, kb * kBlk, y, &full[s], wpol);
+                    tma_load_2d_hint(st + kBox, mu, kb * kBlk, y, &full[s], wpol);
+                } else {
+                    tma_load_2d(st, mg, kb * kBlk, y, &full[s]);
+                    tma_load_2d(st + kBox, mu, kb * kBlk, y, &full[s]);
+                }
 #pragma unroll
                 for (int c = 0; c < kGroupRows; ++c)
                     if (xrow[c]) bulk_load(st + 2 * kBox + c * kRowPitch, xrow[c] + kb * kBlk, kBlk, &full[s]);
@@ -282,7 +301,161 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ======================================================================= down
+// One round of the down operand build of a row group. Four (task, K part) slots of
+// partial sums: slot q holds part q % PP of task t0 + (q / PP) * kCons, where a task is
+// the 128 values of one activation row's gate/up block and PP (1, 2 or 4) is the part
+// count P rounded up, so a round covers 4 / PP tasks. Every load of the round is issued
+// before any arithmetic (one memory round trip); then per task the parts are summed in
+// part order (A + B of each), a = SiLU(g) * u is formed and quantised per 128 values
+// (MXFP8: per 32) into the shared-memory operand.
 template <bool kMX>
+__device__ __forceinline__ void operand_round(const Partials& src, int P, int PP, int row_begin, int Nb, int ntask,
+                                              int t0, uint8_t* s_hq, int hp, float* s_hs, int Nmax) {
+    const int lane = threadIdx.x & 31;
+    float4 ga[4], gb[4], ua[4], ub[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int task = t0 + (q / PP) * kCons, p = q % PP;
+        if (task < ntask && p < P) {
+            const int col = task / Nb, kbq = task % Nb;
+            const size_t o = ((size_t)p * src.rows + row_begin + col) * src.N + kbq * kTile + 4 * lane;
+            ga[q] = __ldcg(reinterpret_cast<const float4*>(src.A[0] + o));
+            gb[q] = __ldcg(reinterpret_cast<const float4*>(src.B[0] + o));
+            ua[q] = __ldcg(reinterpret_cast<const float4*>(src.A[1] + o));
+            ub[q] = __ldcg(reinterpret_cast<const float4*>(src.B[1] + o));
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int task = t0 + b * kCons;
+        if (b * PP >= 4 || task >= ntask) break;  // warp-uniform
+        const int col = task / Nb, kbq = task % Nb;
+        float4 gv = make_float4(0.f, 0.f, 0.f, 0.f), uv = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)  // this task's slots in part order
+            if (q / PP == b && q % PP < P) {
+                gv.x += ga[q].x + gb[q].x;
+                gv.y += ga[q].y + gb[q].y;
+                gv.z += ga[q].z + gb[q].z;
+                gv.w += ga[q].w + gb[q].w;
+                uv.x += ua[q].x + ub[q].x;
+                uv.y += ua[q].y + ub[q].y;
+                uv.z += ua[q].z + ub[q].z;
+                uv.w += ua[q].w + ub[q].w;
+            }
+        const float h0 = silu_mul(gv.x, uv.x), h1 = silu_mul(gv.y, uv.y);
+        const float h2 = silu_mul(gv.z, uv.z), h3 = silu_mul(gv.w, uv.w);
+        if constexpr (kMX) {  // per 32 values: E8M0 bytes [8][Nmax/32] in place of s_hs
+            uint32_t s8;
+            const uint32_t code = warp_quant_mx32(h0, h1, h2, h3, &s8);
+            reinterpret_cast<uint32_t*>(s_hq + col * hp + kbq * kBlk)[lane] = code;
+            if ((lane & 7) == 0)
+                reinterpret_cast<uint8_t*>(s_hs)[col * (Nmax / 32) + kbq * 4 + (lane >> 3)] = (uint8_t)s8;
+        } else {
+            float sc;
+            const uint32_t code = warp_quant_block128(h0, h1, h2, h3, &sc);
+            reinterpret_cast<uint32_t*>(s_hq + col * hp + kbq * kBlk)[lane] = code;
+            if (lane == 0) s_hs[col * (Nmax / kBlk) + kbq] = sc;
+        }
+    }
+}
+
+// Positions of token tok's routed rows j0 .. j0 + RB - 1 in the permuted order (-1 beyond
+// top_k, or outside [0, T*k)), read through L2.
+template <int RB>
+__device__ __forceinline__ void combine_pos(const StreamArgs& a, int tok, int j0, int (&r)[RB]) {
+    const int Tk = a.T * a.k;
+#pragma unroll
+    for (int jj = 0; jj < RB; ++jj) {
+        r[jj] = j0 + jj < a.k ? __ldcg(a.inv_pos + tok * a.k + j0 + jj) : -1;
+        if ((unsigned)r[jj] >= (unsigned)Tk) r[jj] = -1;
+    }
+}
+
+// Combine of one token's four channels h..h+3: the k routed rows' down outputs in slot
+// order (each row's K parts summed in order, A + B), then the shared row, then the
+// residual, in fp32. r0: the positions of the first RB slots (combine_pos). RB rows at a
+// time: all their loads (with the shared row's, in the first batch), then the sums in
+// slot order; the result does not depend on RB.
+template <int RB>
+__device__ __forceinline__ float4 combine4(const StreamArgs& a, const Partials& pt, const Partials& pts, int P,
+                                           int tok, int h, const int (&r0)[RB]) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f), ys = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool shared = a.n_shared_groups > 0;
+    for (int j0 = 0; j0 < a.k; j0 += RB) {
+        int r[RB];
+        if (j0 == 0) {
+#pragma unroll
+            for (int jj = 0; jj < RB; ++jj) r[jj] = r0[jj];
+        } else {
+            combine_pos<RB>(a, tok, j0, r);
+        }
+        float4 y[RB];
+#pragma unroll
+        for (int jj = 0; jj < RB; ++jj) y[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p = 0; p < P; ++p) {
+            float4 ya[RB], yb[RB], sa, sb;
+#pragma unroll
+            for (int jj = 0; jj < RB; ++jj)
+                if (r[jj] >= 0) {
+                    const size_t o = ((size_t)p * pt.rows + r[jj]) * pt.N + h;
+                    ya[jj] = __ldcg(reinterpret_cast<const float4*>(pt.A[0] + o));
+                    yb[jj] = __ldcg(reinterpret_cast<const float4*>(pt.B[0] + o));
+                }
+            if (j0 == 0 && shared) {
+                const size_t o = ((size_t)p * pts.rows + tok) * pts.N + h;
+                sa = __ldcg(reinterpret_cast<const float4*>(pts.A[0] + o));
+                sb = __ldcg(reinterpret_cast<const float4*>(pts.B[0] + o));
+            }
+#pragma unroll
+            for (int jj = 0; jj < RB; ++jj)
+                if (r[jj] >= 0) {
+                    y[jj].x += ya[jj].x + yb[jj].x;
+                    y[jj].y += ya[jj].y + yb[jj].y;
+                    y[jj].z += ya[jj].z + yb[jj].z;
+                    y[jj].w += ya[jj].w + yb[jj].w;
+                }
+            if (j0 == 0 && shared) {
+                ys.x += sa.x + sb.x;
+                ys.y += sa.y + sb.y;
+                ys.z += sa.z + sb.z;
+                ys.w += sa.w + sb.w;
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < RB; ++jj)
+            if (r[jj] >= 0) {
+                v.x += y[jj].x;
+                v.y += y[jj].y;
+                v.z += y[jj].z;
+                v.w += y[jj].w;
+            }
+    }
+    if (shared) {
+        v.x += ys.x;
+        v.y += ys.y;
+        v.z += ys.z;
+        v.w += ys.w;
+    }
+    if (a.residual) {
+        const uint2 rr = *reinterpret_cast<const uint2*>(a.residual + (size_t)tok * a.H + h);
+        v.x += __uint_as_float(rr.x << 16);
+        v.y += __uint_as_float(rr.x & 0xFFFF0000u);
+        v.z += __uint_as_float(rr.y << 16);
+        v.w += __uint_as_float(rr.y & 0xFFFF0000u);
+    }
+    return v;
+}
+
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&lo);
+    o.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = o;
+}
+
+template <bool kMX, typename Ix, bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
     down_stream_kernel(const StreamArgs a, const __grid_constant__ TmaMap tm_d, const __grid_constant__ TmaMap tm_sd) {
     extern __shared__ uint8_t smem_raw[];
@@ -296,6 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* s_hq = reinterpret_cast<uint8_t*>(empty + S);               // [8][hp] FP8 operand
     float* s_hs = reinterpret_cast<float*>(s_hq + kGroupRows * hp);      // [8][Nmax/128] its scales
     __shared__ float s_w[kGroupRows];
+    __shared__ RouteSmem s_route;
+    __shared__ TileRec s_tab[kMaxTab];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
@@ -310,31 +485,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_mbar_init();
     }
-    __syncthreads();
 
-    // The work list comes from the router, which completed before the gate/up kernel
+    // The routing data come from the router, which completed before the gate/up kernel
     // (this kernel's predecessor) got past its own wait; down weights depend on nothing
     // else, so the tile table is built and the producer streams weights before the
-    // gate/up results exist.
-    const Plan pl = down_plan(a);
-    const TileSpace ts = down_space(a, pl.P);
-    const Range rg = make_range(ts, pl.nb, blockIdx.x);
+    // gate/up results exist (load_route and local_route read through L2 and end with
+    // __syncthreads).
+    RouteView rv;
+    if constexpr (kLocal) {
+        __shared__ LocalRouteSmem s_local;
+        rv = local_route(&s_route, &s_local, a, false, true, tid, kThreads);
+    } else {
+        rv = load_route(&s_route, a.ctrl, a.groups, a.max_groups, a.perm_src, a.topk_w, a.T * a.k, a.E, a.status,
+                        tid, kThreads);
+    }
+    const Plan pl = down_plan<Ix>(a, rv.n_groups);
+    const Plan pl_gu = gateup_plan<Ix>(a, rv.n_groups);  // the K parts of the gate/up partials
+    const TileSpace<Ix> ts = down_space<Ix>(a, rv.n_groups, pl.P);
+    const Range<Ix> rg = make_range(ts, pl.nb, blockIdx.x);
     const bool active = blockIdx.x < pl.nb && rg.u1 > rg.u0;
-    __shared__ TileRec s_tab[kMaxTab];
-    const int ntiles = active ? build_table(s_tab, ts, rg, slices, slices, a.groups, a.T, a.k, a.perm_src,
-                                            a.topk_w, tid, kThreads)
-                              : 0;
+    const int ntiles = active ? build_table(s_tab, ts, rg, slices, slices, rv, a.T, a.k, tid, kThreads) : 0;
     __syncthreads();
     auto rec = [&](int i) {
-        return i < kMaxTab ? s_tab[i]
-                           : make_rec(ts, rg, rg.first_tile + i, slices, slices, a.groups, a.T, a.k, a.perm_src,
-                                      a.topk_w);
+        return i < kMaxTab ? s_tab[i] : make_rec_far(ts, rg, rg.first_tile + (Ix)i, slices, slices, rv, a.T, a.k);
     };
 
     if (warp == kCons) {
         if (lane == 0 && active) {
             prefetch_tmap(&tm_d);
             if (a.Is > 0) prefetch_tmap(&tm_sd);
+            const uint64_t wpol = l2_policy_evict_first();  // used when a.stream_once
             int s = 0, ph = 0;
             long q = 0;  // units issued
             bool stop = false;
@@ -349,7 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], kBox);
-                    tma_load_2d(smem + s * SB, md, (r.kb0 + j) * kBlk, y, &full[s]);
+                    if (a.stream_once)
+                        tma_load_2d_hint(smem + s * SB, md, (r.kb0 + j) * kBlk, y, &full[s], wpol);
+                    else
+                        tma_load_2d(smem + s * SB, md, (r.kb0 + j) * kBlk, y, &full[s]);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1;
@@ -367,7 +550,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) trace_stamp(a.trace, 2, 1);
     if (!active) return;
 
-    const Plan pl_gu = gateup_plan(a);
     const Partials gu_r{{a.g_r, a.u_r}, {a.gb_r, a.ub_r}, (long)a.T * a.k, a.I};
     const Partials gu_s{{a.g_s, a.u_s}, {a.gb_s, a.ub_s}, (long)a.T, a.Is};
     const Partials pt{{a.y_r, nullptr}, {a.yb_r, nullptr}, (long)a.T * a.k, H};
@@ -375,31 +557,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;
 
     // FP8 operand of one row group: a = SiLU(g) * u from the gate/up tiles, quantised
-    // per 128 values (one gate/up slice = one down K block)
+    // per 128 values (one gate/up slice = one down K block); as many tasks per warp and
+    // round as 16 float4 registers of partial sums hold
     auto build_operand = [&](const TileRec& q) {
         const int N = q.shared ? a.Is : a.I;
         const int Nb = N / kBlk;
         const Partials& src = q.shared ? gu_s : gu_r;
-        for (int task = warp; task < q.nrows * Nb; task += kCons) {
-            const int col = task / Nb, kbq = task % Nb;
-            const long orow = q.row_begin + col;
-            const float4 gv = read4(src, pl_gu.P, 0, orow, kbq * kTile + 4 * lane);
-            const float4 uv = read4(src, pl_gu.P, 1, orow, kbq * kTile + 4 * lane);
-            const float h0 = silu_mul(gv.x, uv.x), h1 = silu_mul(gv.y, uv.y);
-            const float h2 = silu_mul(gv.z, uv.z), h3 = silu_mul(gv.w, uv.w);
-            if constexpr (kMX) {  // per 32 values: E8M0 bytes [8][Nmax/32] in place of s_hs
-                uint32_t s8;
-                const uint32_t code = warp_quant_mx32(h0, h1, h2, h3, &s8);
-                reinterpret_cast<uint32_t*>(s_hq + col * hp + kbq * kBlk)[lane] = code;
-                if ((lane & 7) == 0)
-                    reinterpret_cast<uint8_t*>(s_hs)[col * (Nmax / 32) + kbq * 4 + (lane >> 3)] = (uint8_t)s8;
-            } else {
-                float sc;
-                const uint32_t code = warp_quant_block128(h0, h1, h2, h3, &sc);
-                reinterpret_cast<uint32_t*>(s_hq + col * hp + kbq * kBlk)[lane] = code;
-                if (lane == 0) s_hs[col * (Nmax / kBlk) + kbq] = sc;
-            }
-        }
+        const int ntask = q.nrows * Nb, P = pl_gu.P;
+        const int PP = P <= 1 ? 1 : (P <= 2 ? 2 : 4);
+        for (int t0 = warp; t0 < ntask; t0 += kCons * (4 / PP))
+            operand_round<kMX>(src, P, PP, q.row_begin, Nb, ntask, t0, s_hq, hp, s_hs, Nmax);
         if (tid < kGroupRows) s_w[tid] = q.w[tid];
         named_bar(1, kConsThreads);
     };
@@ -496,85 +663,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Each thread owns 4 consecutive hidden channels of one token (or one row).
 __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a) {
     if (threadIdx.x == 0) trace_stamp(a.trace, 3, 0);
+    // Before the dependency wait, what was written two or more kernels back, through L2:
+    // the row-group count (for the down stage's K-part count) and this thread's first
+    // token's row positions.
+    const int down_P = down_plan<long long>(a, __ldcg(&a.ctrl->n_routed_groups)).P;
+    const int H = a.H;
+    const int H4 = H / 4;
+    const int Tk = a.T * a.k;
+    const long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x, stride = (long)gridDim.x * blockDim.x;
+    int r0[8];
+    if (a.fuse_combine && i0 < (long)a.T * H4) combine_pos<8>(a, (int)(i0 / H4), 0, r0);
     pdl_wait();  // the down tiles are complete
     pdl_launch_dependents();
     if (threadIdx.x == 0) trace_stamp(a.trace, 3, 1);
-    const int H = a.H;
-    const Plan pl = down_plan(a);
-    const int H4 = H / 4;
-    const int Tk = a.T * a.k;
     const Partials pt{{a.y_r, nullptr}, {a.yb_r, nullptr}, (long)Tk, H};
     const Partials pts{{a.y_s, nullptr}, {a.yb_s, nullptr}, (long)a.T, H};
-    // the down output of permuted row r (routed) or token tok (shared), channels h..h+3
-    auto routed4 = [&](int r, int h) -> float4 { return read4(pt, pl.P, 0, r, h); };
-    auto shared4 = [&](int tok, int h) -> float4 { return read4(pts, pl.P, 0, tok, h); };
-    auto store4 = [](__nv_bfloat16* dst, float4 v) {
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-        uint2 o;
-        o.x = *reinterpret_cast<const uint32_t*>(&lo);
-        o.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(dst) = o;
-    };
-
     if (a.fuse_combine) {
         const long n = (long)a.T * H4;
-        for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        for (long i = i0; i < n; i += stride) {
             const int tok = (int)(i / H4), h = (int)(i % H4) * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            // up to 8 expert rows at a time: their positions, then all their loads, then
-            // the sums in slot order
-            for (int j0 = 0; j0 < a.k; j0 += 8) {
-                int r[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    r[jj] = j0 + jj < a.k ? a.inv_pos[tok * a.k + j0 + jj] : -1;
-                    if ((unsigned)r[jj] >= (unsigned)Tk) r[jj] = -1;
-                }
-                float4 y[8];
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) y[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int p = 0; p < pl.P; ++p) {
-                    float4 ya[8], yb[8];
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj)
-                        if (r[jj] >= 0) {
-                            const size_t o = ((size_t)p * pt.rows + r[jj]) * pt.N + h;
-                            ya[jj] = __ldcg(reinterpret_cast<const float4*>(pt.A[0] + o));
-                            yb[jj] = __ldcg(reinterpret_cast<const float4*>(pt.B[0] + o));
-                        }
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj)
-                        if (r[jj] >= 0) {
-                            y[jj].x += ya[jj].x + yb[jj].x;
-                            y[jj].y += ya[jj].y + yb[jj].y;
-                            y[jj].z += ya[jj].z + yb[jj].z;
-                            y[jj].w += ya[jj].w + yb[jj].w;
-                        }
-                }
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    if (r[jj] >= 0) {
-                        v.x += y[jj].x;
-                        v.y += y[jj].y;
-                        v.z += y[jj].z;
-                        v.w += y[jj].w;
-                    }
-            }
-            if (a.n_shared_groups > 0) {
-                const float4 y = shared4(tok, h);
-                v.x += y.x;
-                v.y += y.y;
-                v.z += y.z;
-                v.w += y.w;
-            }
-            if (a.residual) {
-                const uint2 rr = *reinterpret_cast<const uint2*>(a.residual + (size_t)tok * H + h);
-                v.x += __uint_as_float(rr.x << 16);
-                v.y += __uint_as_float(rr.x & 0xFFFF0000u);
-                v.z += __uint_as_float(rr.y << 16);
-                v.w += __uint_as_float(rr.y & 0xFFFF0000u);
-            }
-            store4(a.out + (size_t)tok * H + h, v);
+            if (i != i0) combine_pos<8>(a, tok, 0, r0);
+            store_bf16x4(a.out + (size_t)tok * H + h, combine4<8>(a, pt, pts, down_P, tok, h, r0));
         }
         if (threadIdx.x == 0) trace_stamp(a.trace, 3, 3);
     } else {
@@ -582,21 +691,24 @@ __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a)
         for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nr + ns; i += (long)gridDim.x * blockDim.x) {
             if (i < nr) {
                 const int r = (int)(i / H4), h = (int)(i % H4) * 4;
-                store4(a.y_perm + (size_t)r * H + h, routed4(r, h));
+                store_bf16x4(a.y_perm + (size_t)r * H + h, read4(pt, down_P, 0, r, h));
             } else {
                 const long j = i - nr;
                 const int tok = (int)(j / H4), h = (int)(j % H4) * 4;
-                store4(a.y_shared + (size_t)tok * H + h, shared4(tok, h));
+                store_bf16x4(a.y_shared + (size_t)tok * H + h, read4(pts, down_P, 0, tok, h));
             }
         }
     }
 }
 
 size_t smem_gateup() { return (size_t)kStagesGU * (2 * kBox + kBRows) + 2 * kStagesGU * 8 + 1024; }
+// Static shared memory of the down kernel beside its dynamic ring and operand: the tile
+// table, the routing copies and small scalars.
+constexpr long kDownStaticSmem = (long)kTabBytes + (long)sizeof(RouteSmem) + (long)sizeof(LocalRouteSmem) + 256;
 // Down-kernel ring depth: as many 16 KB stages (up to 10) as fit beside the FP8 operand.
 int stages_down(int Nmax) {
     const long operand = (long)kGroupRows * (Nmax + 16) + (long)kGroupRows * (Nmax / kBlk) * 4;
-    const long room = 227L * 1024 - 1024 - operand - (long)kTabBytes - 64;
+    const long room = 227L * 1024 - 1024 - operand - kDownStaticSmem - 64;
     return (int)std::max<long>(2, std::min<long>(kMaxStagesD, room / (kBox + 16)));
 }
 size_t smem_down(int Nmax) {
@@ -647,9 +759,13 @@ int stream_max_parts(const moe_config_t& c, int64_t T) {
 
 cudaError_t launch_gateup_stream(const StreamArgs& a, const uint8_t* w_gate, const uint8_t* w_up, int E,
                                  cudaStream_t st) {
-    static size_t smem_set[2] = {0, 0};
-    const void* kern = a.mx ? (const void*)gateup_stream_kernel<true> : (const void*)gateup_stream_kernel<false>;
-    cudaError_t e = set_smem(kern, smem_gateup(), &smem_set[a.mx ? 1 : 0]);
+    static size_t smem_set[6] = {0, 0, 0, 0, 0, 0};
+    using K = void (*)(const StreamArgs, const TmaMap, const TmaMap, const TmaMap, const TmaMap);
+    const K kerns[6] = {gateup_stream_kernel<false, int, false>,       gateup_stream_kernel<true, int, false>,
+                        gateup_stream_kernel<false, long long, false>, gateup_stream_kernel<true, long long, false>,
+                        gateup_stream_kernel<false, int, true>,        gateup_stream_kernel<true, int, true>};
+    const int v = a.local_route ? 4 + (a.mx ? 1 : 0) : (a.mx ? 1 : 0) + (a.wide ? 2 : 0);
+    cudaError_t e = set_smem((const void*)kerns[v], smem_gateup(), &smem_set[v]);
     if (e != cudaSuccess) return e;
     TmaMap tg{}, tu{}, tsg{}, tsu{};
     if (!tmap_u8_2d(&tg, w_gate, (uint64_t)E * a.I, a.H, kBlk, kTile) ||
@@ -658,22 +774,24 @@ cudaError_t launch_gateup_stream(const StreamArgs& a, const uint8_t* w_gate, con
     if (a.Is > 0 && (!tmap_u8_2d(&tsg, a.ws_gate, a.Is, a.H, kBlk, kTile) ||
                      !tmap_u8_2d(&tsu, a.ws_up, a.Is, a.H, kBlk, kTile)))
         return cudaErrorInvalidValue;
-    return a.mx ? launch_pdl(gateup_stream_kernel<true>, a.grid_gu, kThreads, smem_gateup(), st, a, tg, tu, tsg, tsu)
-                : launch_pdl(gateup_stream_kernel<false>, a.grid_gu, kThreads, smem_gateup(), st, a, tg, tu, tsg, tsu);
+    return launch_pdl(kerns[v], a.grid_gu, kThreads, smem_gateup(), st, a, tg, tu, tsg, tsu);
 }
 
 cudaError_t launch_down_stream(const StreamArgs& a, const uint8_t* w_down, const uint8_t* ws_down, int E,
                                cudaStream_t st) {
-    static size_t smem_set[2] = {0, 0};
+    static size_t smem_set[6] = {0, 0, 0, 0, 0, 0};
     const size_t smem = smem_down(std::max(a.I, a.Is));
-    const void* kern = a.mx ? (const void*)down_stream_kernel<true> : (const void*)down_stream_kernel<false>;
-    cudaError_t e = set_smem(kern, smem, &smem_set[a.mx ? 1 : 0]);
+    using K = void (*)(const StreamArgs, const TmaMap, const TmaMap);
+    const K kerns[6] = {down_stream_kernel<false, int, false>,       down_stream_kernel<true, int, false>,
+                        down_stream_kernel<false, long long, false>, down_stream_kernel<true, long long, false>,
+                        down_stream_kernel<false, int, true>,        down_stream_kernel<true, int, true>};
+    const int v = a.local_route ? 4 + (a.mx ? 1 : 0) : (a.mx ? 1 : 0) + (a.wide ? 2 : 0);
+    cudaError_t e = set_smem((const void*)kerns[v], smem, &smem_set[v]);
     if (e != cudaSuccess) return e;
     TmaMap td{}, tsd{};
     if (!tmap_u8_2d(&td, w_down, (uint64_t)E * a.H, a.I, kBlk, kTile)) return cudaErrorInvalidValue;
     if (a.Is > 0 && !tmap_u8_2d(&tsd, ws_down, a.H, a.Is, kBlk, kTile)) return cudaErrorInvalidValue;
-    return a.mx ? launch_pdl(down_stream_kernel<true>, a.grid_d, kThreads, smem, st, a, td, tsd)
-                : launch_pdl(down_stream_kernel<false>, a.grid_d, kThreads, smem, st, a, td, tsd);
+    return launch_pdl(kerns[v], a.grid_d, kThreads, smem, st, a, td, tsd);
 }
 
 cudaError_t launch_stream_combine(const StreamArgs& a, cudaStream_t st) {

@@ -185,6 +185,16 @@ T* at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+// The streaming kernels need 64-bit unit indices: the most units a stage can have (every
+// row group and shared group times the 128-row slices of its matrix times its K blocks,
+// the same count for gate/up and down), times the CTAs, may pass 2^31.
+bool stream_wide(const moe_config_t* c, int32_t T, const WsLayout& L) {
+    const int64_t sgroups = c->n_shared > 0 ? (T + kGroupRows - 1) / kGroupRows : 0;
+    const int64_t units = ((int64_t)L.max_groups * (c->moe_inter / kBlk) +
+                           sgroups * ((int64_t)c->n_shared * c->moe_inter / kBlk)) * (c->hidden / kBlk);
+    return units > (int64_t)INT32_MAX / (2 * kMaxStreamCtas);
+}
+
 StreamArgs stream_args(const moe_config_t* c, int32_t T, const moe_weights_t* W, const WsLayout& L, void* ws,
                        const int32_t* perm_src, const float* topk_w) {
     StreamArgs a = {};
@@ -193,11 +203,17 @@ StreamArgs stream_args(const moe_config_t* c, int32_t T, const moe_weights_t* W,
     a.Is = c->n_shared * c->moe_inter;
     a.T = T;
     a.k = c->top_k;
+    a.E = c->n_routed;
     a.n_shared_groups = c->n_shared > 0 ? (T + kGroupRows - 1) / kGroupRows : 0;
     a.grid_gu = stream_grid();
     a.grid_d = stream_grid();
     a.stages_d = down_stages(a.I, a.Is);
     a.max_parts = stream_max_parts(*c, T);
+    a.max_groups = L.max_groups;
+    a.wide = stream_wide(c, T, L) ? 1 : 0;
+    // up to 8 tokens every routed expert's rows form one row group and the shared experts'
+    // tokens another, so each weight byte is streamed exactly once
+    a.stream_once = T <= kGroupRows ? 1 : 0;
     a.ctrl = at<Ctrl>(ws, L.ctrl);
     a.groups = at<RowGroup>(ws, L.groups);
     a.group_of_row = at<int32_t>(ws, L.group_of_row);
@@ -228,6 +244,24 @@ StreamArgs stream_args(const moe_config_t* c, int32_t T, const moe_weights_t* W,
     a.yb_s = at<float>(ws, L.yb_s);
     a.status = &at<Ctrl>(ws, L.ctrl)->status;
     return a;
+}
+
+// Routing inside the streaming kernels (T <= kLocalT): the router leaves logits only; the
+// gate/up kernel's CTA 0 publishes the selection and the permutation into the workspace.
+void set_local_route(StreamArgs* a, const moe_config_t* c, const WsLayout& L, void* ws) {
+    a->local_route = 1;
+    a->G = c->n_group;
+    a->Gk = c->topk_group;
+    a->scale = c->routed_scaling_factor;
+    a->logits = at<float>(ws, L.logits);
+    a->pub_ids = at<int32_t>(ws, L.ids);
+    a->pub_w = at<float>(ws, L.w);
+    a->pub_perm = at<int32_t>(ws, L.perm_src);
+    a->pub_inv = at<int32_t>(ws, L.inv_pos);
+    a->pub_offsets = at<int32_t>(ws, L.offsets);
+    a->pub_groups = at<RowGroup>(ws, L.groups);
+    a->pub_group_of_row = at<int32_t>(ws, L.group_of_row);
+    a->pub_n_groups = &at<Ctrl>(ws, L.ctrl)->n_routed_groups;
 }
 
 // The streaming kernels' arguments for MXFP8 weights (E8M0 scale rows).
@@ -713,12 +747,14 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
     Ctrl* ctrl = at<Ctrl>(ws, L.ctrl);
     RowGroup* groups = at<RowGroup>(ws, L.groups);
 
+    // the streaming kernels route (see set_local_route)
+    const bool local = T <= kLocalT && !stream_wide(cfg, T, L);
     MOE_TRY(mark.begin(MOE_STAGE_ROUTE));
     if (T <= kSmallT) {
         MOE_CUDA(launch_route_small(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
                                     at<float>(ws, L.logits), at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
                                     at<int32_t>(ws, L.offsets), perm_src, inv_pos, groups,
-                                    at<int32_t>(ws, L.group_of_row), ctrl, nm, st, nullptr, trace));
+                                    at<int32_t>(ws, L.group_of_row), ctrl, nm, st, nullptr, trace, !local));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
     } else {
         if (nm.gamma) {
@@ -755,6 +791,7 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
     }
     StreamArgs a = stream_args(cfg, T, weights, L, ws, perm_src, w);
     a.fuse_combine = 1;
+    if (local) set_local_route(&a, cfg, L, ws);
     a.residual = static_cast<const __nv_bfloat16*>(residual_bf16);
     a.out = static_cast<__nv_bfloat16*>(out_bf16);
     a.trace = trace;
@@ -856,13 +893,16 @@ moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16
     MOE_TRY(mark.begin(MOE_STAGE_ROUTE));
     if (T <= kSmallT) {
         // decode: the fused route (x quantised per 32), then the weight-streaming kernels
+        const bool local = T <= kLocalT && !stream_wide(cfg, T, L);  // the streaming kernels route
         MOE_CUDA(launch_route_small(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
                                     at<float>(ws, L.logits), at<uint8_t>(ws, L.xq), at<float>(ws, L.xs),
                                     at<int32_t>(ws, L.offsets), perm_src, inv_pos, at<RowGroup>(ws, L.groups),
-                                    at<int32_t>(ws, L.group_of_row), ctrl, NormArgs{}, st, at<uint8_t>(ws, L.xs8)));
+                                    at<int32_t>(ws, L.group_of_row), ctrl, NormArgs{}, st, at<uint8_t>(ws, L.xs8),
+                                    nullptr, !local));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
         StreamArgs a = stream_args_mx(cfg, T, weights, L, ws, perm_src, w);
         a.fuse_combine = 1;
+        if (local) set_local_route(&a, cfg, L, ws);
         a.residual = static_cast<const __nv_bfloat16*>(residual_bf16);
         a.out = static_cast<__nv_bfloat16*>(out_bf16);
         MOE_TRY(mark.begin(MOE_STAGE_GATE_UP));

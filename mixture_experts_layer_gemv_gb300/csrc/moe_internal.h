@@ -15,6 +15,10 @@ namespace moe {
 constexpr int kGroupRows = 8;
 // Up to this many tokens the router + top-k + permutation run as one fused kernel.
 constexpr int kSmallT = 64;
+// Up to this many tokens the fused forward's streaming kernels derive the routing from the
+// router's logits themselves (every CTA the same selection), so the router has no serial
+// tail on the layer's critical path.
+constexpr int kLocalT = 8;
 
 // Control words at the start of the workspace (256 bytes, zeroed by
 // moe_workspace_init and returned to zero by every call that changes them).
@@ -31,7 +35,7 @@ static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 // One activation row group of the expert GEMVs: up to kGroupRows rows of one expert
 // (expert >= 0: permuted rows [row_begin, row_begin + nrows)) or of the shared experts
 // (expert == -1: tokens [row_begin, row_begin + nrows)).
-struct RowGroup {
+struct alignas(16) RowGroup {
     int expert;
     int row_begin;
     int nrows;
@@ -114,7 +118,7 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
                                uint8_t* xq, float* xs, int32_t* offsets, int32_t* perm_src,
                                int32_t* inv_pos, RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl,
                                const NormArgs& nm, cudaStream_t st, uint8_t* xs8 = nullptr,
-                               uint64_t* trace = nullptr);
+                               uint64_t* trace = nullptr, bool tail = true);
 
 // Large-T route: router GEMM (split-K partials) + softmax/top-k per token. With
 // nm.gamma the router reads stage M's output on the fly (nm.rstd from launch_rmsnorm).
@@ -150,9 +154,12 @@ constexpr int kMaxStreamCtas = 512;
 constexpr size_t kCtrlRegionBytes = sizeof(Ctrl);
 
 struct StreamArgs {
-    int H, I, Is, T, k, n_shared_groups;
+    int H, I, Is, T, k, E, n_shared_groups;
     int grid_gu, grid_d, stages_d;  // launch shapes (the readers of partial tiles need them)
     int max_parts;                  // K parts the A buffers have room for
+    int max_groups;                 // row-group capacity of the workspace
+    int wide;                       // 1: unit indices may exceed 2^31 (64-bit tile arithmetic)
+    int stream_once;                // 1: every weight byte is read by one row group (T <= 8): evict-first loads
     const Ctrl* ctrl;
     const RowGroup* groups;
     const int32_t* group_of_row;  // [T*k] row group of each permuted row
@@ -179,6 +186,22 @@ struct StreamArgs {
     const uint8_t* xs8;
     // combine
     int fuse_combine;  // 1: out (bf16) = sum of rows + shared (+ residual); 0: y_perm / y_shared (bf16)
+    // Routing derived inside every streaming CTA (local_route = 1, up to kLocalT tokens):
+    // the router leaves logits [T, E] only; each gate/up and down CTA runs top-k and the
+    // permutation itself, and gate/up CTA 0 publishes them (ids, weights, perm_src, inv_pos,
+    // offsets, row groups and their count) for the combine and the caller.
+    int local_route;
+    int G, Gk;
+    float scale;
+    const float* logits;
+    int32_t* pub_ids;
+    float* pub_w;
+    int32_t* pub_perm;
+    int32_t* pub_inv;
+    int32_t* pub_offsets;
+    RowGroup* pub_groups;
+    int32_t* pub_group_of_row;
+    int* pub_n_groups;
     __nv_bfloat16* y_perm;
     __nv_bfloat16* y_shared;
     const __nv_bfloat16* residual;

@@ -46,6 +46,7 @@ struct RouteSmallParams {
     float eps;
     uint8_t* xs8;           // MXFP8: E8M0 scales [T, H/32] (xs unused)
     uint64_t* trace;        // per-CTA timer stamps or null
+    int tail;               // 1: the last CTA runs top-k and the permutation; 0: logits and x codes only
 };
 
 // kNorm: stage M in front of the router (p.gamma != nullptr); kMX: x quantised per 32
@@ -176,7 +177,12 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
         }
     }
 
-    // ---- last CTA to arrive: O (softmax + top-k) and the permutation
+    // ---- last CTA to arrive: O (softmax + top-k) and the permutation; with p.tail = 0
+    // the kernels that follow derive the selection from the logits themselves
+    if (!p.tail) {
+        trace_stamp(p.trace, 0, 3);
+        return;
+    }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
     __syncthreads();
     if (p.offsets)
         small_permute(s_ids, T * p.k, p.E, s_cnt, s_off, s_gcnt, s_goff, s_rank, p.offsets, p.perm_src, p.inv_pos,
-                      p.groups, p.group_of_row, p.ctrl);
+                      p.groups, p.group_of_row, &p.ctrl->n_routed_groups);
     if (threadIdx.x == 0) p.ctrl->route_arrived = 0u;
     trace_stamp(p.trace, 0, 3);
 }
@@ -515,8 +521,9 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
                                const float* bias, int32_t* ids, float* w, float* logits, uint8_t* xq,
                                float* xs, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
                                RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl, const NormArgs& nm,
-                               cudaStream_t st, uint8_t* xs8, uint64_t* trace) {
+                               cudaStream_t st, uint8_t* xs8, uint64_t* trace, bool tail) {
     RouteSmallParams p;
+    p.tail = tail ? 1 : 0;
     p.H = c.hidden;
     p.E = c.n_routed;
     p.G = c.n_group;

@@ -197,7 +197,7 @@ __device__ inline int warp_exclusive_scan256(int* v, int n) {
 // s_rank holds n ints of scratch.
 __device__ inline void small_permute(const int32_t* s_ids, int n, int E, int* s_cnt, int* s_off, int* s_gcnt,
                                      int* s_goff, int* s_rank, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
-                                     RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl) {
+                                     RowGroup* groups, int32_t* group_of_row, int* n_groups) {
     const int lane = threadIdx.x & 31;
     if (n <= 32) {
         // One warp, no CTA barrier: a slot's row is the number of slots with a smaller id
@@ -231,7 +231,7 @@ __device__ inline void small_permute(const int32_t* s_ids, int n, int E, int* s_
                 groups[gi] = rg;
             }
             const int ng = __popc(__ballot_sync(0xffffffffu, start));
-            if (lane == 0) ctrl->n_routed_groups = ng;
+            if (lane == 0) *n_groups = ng;
         }
         for (int e = threadIdx.x; e <= E; e += blockDim.x) {
             int c = 0;
@@ -267,7 +267,7 @@ __device__ inline void small_permute(const int32_t* s_ids, int n, int E, int* s_
         const int gtot = warp_exclusive_scan256(s_goff, E);
         if (threadIdx.x == 0) {
             s_off[E] = tot;
-            ctrl->n_routed_groups = gtot;
+            *n_groups = gtot;
         }
     }
     __syncthreads();

@@ -1,6 +1,6 @@
-// Device building blocks of the weight-streaming expert kernels (expert_stream.cu)
-// and the fused small-T layer kernel (moe_fused.cu): unit/tile decomposition,
-// launch plans, TMA-box dot products and the A/B partial-sum buffers.
+// Device building blocks of the weight-streaming expert kernels (expert_stream.cu):
+// unit/tile decomposition, launch plans, the routing data in shared memory, TMA-box dot
+// products and the A/B partial-sum buffers.
 #pragma once
 
 #include <algorithm>
@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "moe_internal.h"
+#include "route_common.cuh"
 
 namespace moe {
 namespace stream {
@@ -27,40 +28,46 @@ constexpr int kMaxStagesD = 10;
 // The unit sequence of a stage. Output rows come in "rows" of 128 (row group x 128-row
 // slice): n_r routed rows with kc_r K blocks each, then n_s shared rows with kc_s.
 // Each row's K blocks are split into P contiguous parts; a tile is one (row, part) and
-// a unit one (tile, K block). Units are ordered row-major, K block fastest.
+// a unit one (tile, K block). Units are ordered row-major, K block fastest. Ix is the
+// index type of units and tiles: int whenever the host has bounded the unit count
+// below 2^31 (every decode shape), long long otherwise.
+template <typename Ix>
 struct TileSpace {
-    int n_r, kc_r, n_s, kc_s, P;
-    __device__ long total() const { return (long)n_r * kc_r + (long)n_s * kc_s; }
-    __device__ int kc_of(long t) const { return t < (long)n_r * P ? kc_r : kc_s; }
+    Ix n_r;
+    int kc_r;
+    Ix n_s;
+    int kc_s, P;
+    __device__ Ix total() const { return n_r * kc_r + n_s * kc_s; }
+    __device__ int kc_of(Ix t) const { return t < n_r * P ? kc_r : kc_s; }
     // first K block of part p of a row with kc blocks
-    __device__ int part_lo(int kc, int p) const { return (int)((long)p * kc / P); }
-    __device__ long start(long t) const {
-        if (t < (long)n_r * P) return (t / P) * kc_r + part_lo(kc_r, (int)(t % P));
-        const long v = t - (long)n_r * P;
-        return (long)n_r * kc_r + (v / P) * kc_s + part_lo(kc_s, (int)(v % P));
+    __device__ int part_lo(int kc, int p) const { return p * kc / P; }
+    __device__ Ix start(Ix t) const {
+        if (t < n_r * P) return (t / P) * kc_r + part_lo(kc_r, (int)(t % P));
+        const Ix v = t - n_r * P;
+        return n_r * kc_r + (v / P) * kc_s + part_lo(kc_s, (int)(v % P));
     }
-    __device__ int len(long t) const {
+    __device__ int len(Ix t) const {
         const int kc = kc_of(t), p = (int)(t % P);
         return part_lo(kc, p + 1) - part_lo(kc, p);
     }
     // tile of unit u; *kb receives its absolute K block
-    __device__ long tile_of(long u, int* kb) const {
-        long row, base_t;
+    __device__ Ix tile_of(Ix u, int* kb) const {
+        Ix row, base_t;
         int kc, kin;
-        if (u < (long)n_r * kc_r) {
+        if (u < n_r * kc_r) {
             row = u / kc_r;
             kin = (int)(u % kc_r);
             kc = kc_r;
             base_t = 0;
         } else {
-            const long v = u - (long)n_r * kc_r;
+            const Ix v = u - n_r * kc_r;
             row = v / kc_s;
             kin = (int)(v % kc_s);
             kc = kc_s;
-            base_t = (long)n_r * P;
+            base_t = n_r * P;
         }
         *kb = kin;
-        const int p = (int)(((long)(kin + 1) * P - 1) / kc);  // part whose range holds kin
+        const int p = ((kin + 1) * P - 1) / kc;  // part whose range holds kin
         return base_t + row * P + p;
     }
 };
@@ -71,10 +78,12 @@ struct Plan {
     int nb, P;
 };
 constexpr int kMaxParts = 4;
-__device__ __forceinline__ Plan make_plan(int n_r, int kc_r, int n_s, int kc_s, int grid, int max_parts) {
-    const long U = (long)n_r * kc_r + (long)n_s * kc_s;
+template <typename Ix>
+__device__ __forceinline__ Plan make_plan(Ix n_r, int kc_r, Ix n_s, int kc_s, int grid, int max_parts) {
+    const Ix U = n_r * kc_r + n_s * kc_s;
     Plan pl;
-    pl.nb = (int)std::max<long>(1, std::min<long>(grid, U));
+    pl.nb = (int)(U < (Ix)grid ? U : (Ix)grid);
+    if (pl.nb < 1) pl.nb = 1;
     int kcmax = 0, kcmin = INT_MAX;  // over the kinds that have rows
     if (n_r > 0) kcmax = kcmin = kc_r;
     if (n_s > 0) {
@@ -82,21 +91,174 @@ __device__ __forceinline__ Plan make_plan(int n_r, int kc_r, int n_s, int kc_s, 
         kcmin = std::min(kcmin, kc_s);
     }
     if (kcmax == 0) kcmax = kcmin = 1;
-    const long L = std::max<long>(1, U / pl.nb);
+    const Ix L = std::max<Ix>(1, U / pl.nb);
     int P = (int)((kcmax + L - 1) / L);
     P = std::max(1, std::min(P, std::min(max_parts, kcmin)));
-    const long need = (kcmax + P - 1) / P;  // longest part
-    if (need > L) pl.nb = (int)std::max<long>(1, U / need);
+    const int need = (kcmax + P - 1) / P;  // longest part
+    if (need > L) pl.nb = (int)std::max<Ix>(1, U / need);
     pl.P = P;
     return pl;
 }
 
-// The routing data the tile decoders read (the work list, perm_src, topk_w, the group
-// count) is written by the router kernel. The down kernel decodes its tiles before its own
-// dependency wait: the router had completed, its writes visible, before the gate/up
-// kernel's wait returned, and the down kernel is launched only after every gate/up CTA
-// has passed that wait.
-__device__ __forceinline__ int routed_groups(const Ctrl* c) { return c->n_routed_groups; }
+// The routing data the tile decoders read (the row groups, perm_src, topk_w and the group
+// count), written by the router kernel (or the row-group kernel of the stage API) two or
+// more kernels before the streaming kernels. The down kernel decodes its tiles before its
+// own dependency wait: the router had completed, its writes performed at device scope,
+// before the gate/up kernel's wait returned, and the down kernel is launched only after
+// every gate/up CTA has passed that wait. Those reads go through L2 (ld.global.cg), the
+// device's point of coherence, so no line an earlier kernel left in this SM's L1 can
+// answer them.
+constexpr int kMaxGroupsSmem = 256;  // row groups copied into shared memory
+constexpr int kMaxRowsSmem = 512;    // routed rows (T*k) whose source slot and weight are copied
+
+// 16-byte aligned: the row groups are copied with 16-byte vector stores.
+struct alignas(16) RouteSmem {
+    RowGroup groups[kMaxGroupsSmem];
+    int32_t perm[kMaxRowsSmem];
+    float w[kMaxRowsSmem];
+    int n_groups;
+};
+
+// Where a decoder finds the routing data: shared-memory copies (smem = 1), or the
+// workspace itself when it does not fit (read through L2).
+struct RouteView {
+    const RowGroup* groups;
+    const int32_t* perm;
+    const float* w;  // null: token ids wanted (gate/up); else routing weights (down)
+    int n_groups;
+    int smem;
+    int E, R;     // routed experts, routed rows (T*k): the bounds of a valid record
+    int* status;  // device status word (kStatusBadId for a record out of bounds)
+};
+
+// A row group as the decoders use it. A record outside the routing's bounds (an expert
+// id outside [0, E), rows outside [0, T*k), none or more than kGroupRows of them) is read
+// as an empty group of expert 0 and reported, so that no weight, scale or partial-sum
+// address is ever formed from it.
+__device__ __forceinline__ RowGroup route_group(const RouteView& v, int gi) {
+    RowGroup g;
+    if (v.smem) {
+        g = v.groups[gi];
+    } else {
+        const int4 q = __ldcg(reinterpret_cast<const int4*>(v.groups) + gi);
+        g = RowGroup{q.x, q.y, q.z, q.w};
+    }
+    if ((unsigned)g.expert >= (unsigned)v.E || g.nrows < 1 || g.nrows > kGroupRows || g.row_begin < 0 ||
+        g.row_begin > v.R - g.nrows) {
+        set_status(v.status, kStatusBadId);
+        g = RowGroup{0, 0, 0, 0};
+    }
+    return g;
+}
+__device__ __forceinline__ int route_perm(const RouteView& v, int r) { return v.smem ? v.perm[r] : __ldcg(v.perm + r); }
+__device__ __forceinline__ float route_w(const RouteView& v, int f) { return v.smem ? v.w[f] : __ldcg(v.w + f); }
+
+// Gather the routing data into s with one round of loads (all threads tid < nthreads;
+// ends with __syncthreads). max_groups: the workspace's row-group capacity.
+__device__ inline RouteView load_route(RouteSmem* s, const Ctrl* ctrl, const RowGroup* groups, int max_groups,
+                                       const int32_t* perm_src, const float* topk_w, int R, int E, int* status,
+                                       int tid, int nthreads) {
+    // every load is issued before any store (one memory round trip): with nthreads >= 256
+    // a thread copies at most one row group and two rows
+    const bool fits = max_groups <= kMaxGroupsSmem && R <= kMaxRowsSmem && 2 * nthreads >= kMaxRowsSmem &&
+                      nthreads >= kMaxGroupsSmem;
+    if (tid == 0) s->n_groups = min(max(__ldcg(&ctrl->n_routed_groups), 0), max_groups);
+    if (fits) {
+        const int i1 = tid + nthreads;
+        const bool hg = tid < max_groups, h0 = tid < R, h1 = i1 < R;
+        const int4 g = hg ? __ldcg(reinterpret_cast<const int4*>(groups) + tid) : make_int4(0, 0, 0, 0);
+        const int p0 = h0 ? __ldcg(perm_src + tid) : 0, p1 = h1 ? __ldcg(perm_src + i1) : 0;
+        const float w0 = topk_w && h0 ? __ldcg(topk_w + tid) : 0.f, w1 = topk_w && h1 ? __ldcg(topk_w + i1) : 0.f;
+        if (hg) reinterpret_cast<int4*>(s->groups)[tid] = g;
+        if (h0) {
+            s->perm[tid] = p0;
+            s->w[tid] = w0;
+        }
+        if (h1) {
+            s->perm[i1] = p1;
+            s->w[i1] = w1;
+        }
+    }
+    __syncthreads();
+    RouteView v;
+    v.n_groups = s->n_groups;
+    v.smem = fits ? 1 : 0;
+    v.groups = fits ? s->groups : groups;
+    v.perm = fits ? s->perm : perm_src;
+    v.w = topk_w ? (fits ? s->w : topk_w) : nullptr;
+    v.E = E;
+    v.R = R;
+    v.status = status;
+    return v;
+}
+
+// Scratch of local_route: the CTA-wide top-k's keys, group keys and partial sums, the T*k
+// selected ids, inverse positions, the counting sort's ranks and per-expert counts,
+// offsets and group offsets.
+constexpr int kLocalRows = kLocalT * 16;  // T*k slots (top_k <= 16)
+struct alignas(16) LocalRouteSmem {
+    unsigned key[routing::kMaxE];  // first: read as uint4
+    unsigned gkey[32];
+    float part[32];
+    int32_t ids[kLocalRows];
+    int32_t inv[kLocalRows];
+    int32_t rank[kLocalRows];
+    int32_t gor[kLocalRows];
+    int32_t cnt[routing::kMaxE], gcnt[routing::kMaxE], goff[routing::kMaxE];
+    int32_t off[routing::kMaxE + 1];
+    int32_t offsets[routing::kMaxE + 1];
+};
+
+// The routing of T <= kLocalT tokens derived by one CTA from the router's logits (read
+// through L2): softmax and group-limited top-k of each token by one warp (the router's own
+// function, so every CTA makes the same selection), then the stable counting sort of the
+// T*k slots and the row groups, in shared memory. publish (gate/up CTA 0): the result is
+// also written to the workspace for the combine kernel and the caller. All nthreads
+// threads call it; it ends with __syncthreads. want_w: the view carries the routing
+// weights (down) rather than token ids (gate/up).
+__device__ inline RouteView local_route(RouteSmem* s, LocalRouteSmem* L, const StreamArgs& a, bool publish,
+                                        bool want_w, int tid, int nthreads) {
+    using namespace routing;
+    const int warp = tid >> 5, lane = tid & 31, T = a.T, k = a.k, E = a.E, n = T * k;
+    if (T == 1 && E <= nthreads) {
+        // one token: the whole CTA ranks the experts (the router's one-token selection)
+        cta_topk1(a.logits, E, a.G, a.Gk, k, a.scale, L->key, L->gkey, L->part, L->ids, s->w, nullptr);
+    } else if (warp < T) {
+        float lg[kMaxE / 32];
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i) {
+            const int e = lane + 32 * i;
+            lg[i] = e < E ? __ldcg(a.logits + (size_t)warp * E + e) : -INFINITY;
+        }
+        topk_warp(lg, E, a.G, a.Gk, k, a.scale, nullptr, L->ids + warp * k, s->w + warp * k, nullptr);
+    }
+    __syncthreads();
+    small_permute(L->ids, n, E, L->cnt, L->off, L->gcnt, L->goff, L->rank, L->offsets, s->perm, L->inv, s->groups,
+                  L->gor, &s->n_groups);
+    __syncthreads();
+    if (publish) {
+        for (int i = tid; i < n; i += nthreads) {
+            a.pub_ids[i] = L->ids[i];
+            a.pub_w[i] = s->w[i];
+            a.pub_perm[i] = s->perm[i];
+            a.pub_inv[i] = L->inv[i];
+            a.pub_group_of_row[i] = L->gor[i];
+        }
+        for (int e = tid; e <= E; e += nthreads) a.pub_offsets[e] = L->offsets[e];
+        for (int g = tid; g < s->n_groups; g += nthreads) a.pub_groups[g] = s->groups[g];
+        if (tid == 0) *a.pub_n_groups = s->n_groups;
+    }
+    RouteView v;
+    v.n_groups = s->n_groups;
+    v.smem = 1;
+    v.groups = s->groups;
+    v.perm = s->perm;
+    v.w = want_w ? s->w : nullptr;
+    v.E = E;
+    v.R = n;
+    v.status = a.status;
+    return v;
+}
 
 // A tile decoded: which row group, which 128-row slice of the output, which K part.
 struct TileInfo {
@@ -109,14 +271,15 @@ struct TileInfo {
     int part;       // K part
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const TileSpace& ts, long t, int slices_r, int slices_s,
-                                                const RowGroup* groups, int T) {
+template <typename Ix>
+__device__ __forceinline__ TileInfo decode_tile(const TileSpace<Ix>& ts, Ix t, int slices_r, int slices_s,
+                                                const RouteView& rv, int T) {
     TileInfo ti;
     ti.part = (int)(t % ts.P);
-    if (t < (long)ts.n_r * ts.P) {
-        const long row = t / ts.P;
+    if (t < ts.n_r * ts.P) {
+        const Ix row = t / ts.P;
         const int gi = (int)(row / slices_r);
-        const RowGroup rg = groups[gi];
+        const RowGroup rg = route_group(rv, gi);
         ti.shared = 0;
         ti.expert = rg.expert;
         ti.group = gi;
@@ -124,7 +287,7 @@ __device__ __forceinline__ TileInfo decode_tile(const TileSpace& ts, long t, int
         ti.nrows = rg.nrows;
         ti.slice = (int)(row % slices_r);
     } else {
-        const long row = (t - (long)ts.n_r * ts.P) / ts.P;
+        const Ix row = (t - ts.n_r * ts.P) / ts.P;
         ti.shared = 1;
         ti.expert = -1;
         ti.group = -1;
@@ -190,25 +353,28 @@ __device__ __forceinline__ void box_dot_mx(float (&c)[4][4], const uint8_t* box,
     }
 }
 
+template <typename Ix>
 struct Range {
-    long U, u0, u1, first_tile;
+    Ix U, u0, u1, first_tile;
     int nb, b, kb0;
 };
 
-__device__ __forceinline__ Range make_range(const TileSpace& ts, int nb, int b) {
-    Range r;
+template <typename Ix>
+__device__ __forceinline__ Range<Ix> make_range(const TileSpace<Ix>& ts, int nb, int b) {
+    Range<Ix> r;
     r.U = ts.total();
     r.nb = nb;
     r.b = b;
-    r.u0 = b < nb ? (long)b * r.U / nb : 0;
-    r.u1 = b < nb ? (long)(b + 1) * r.U / nb : 0;
+    // b * U fits the index type (the host bounds units x CTAs for int indices)
+    r.u0 = b < nb ? (Ix)b * r.U / nb : 0;
+    r.u1 = b < nb ? (Ix)(b + 1) * r.U / nb : 0;
     r.kb0 = 0;
     r.first_tile = (b < nb && r.u1 > r.u0) ? ts.tile_of(r.u0, &r.kb0) : 0;
     return r;
 }
 
 // One tile of a CTA's unit range, decoded once before the streaming loops so that
-// neither the producer nor the consumers stall on descriptor loads or 64-bit index
+// neither the producer nor the consumers stall on descriptor loads or index
 // arithmetic at tile boundaries.
 struct TileRec {
     int shared, expert, group, row_begin, nrows, slice, part;
@@ -225,11 +391,11 @@ struct TileRec {
 constexpr int kMaxTab = 96;
 constexpr size_t kTabBytes = (size_t)kMaxTab * sizeof(TileRec);
 
-__device__ inline TileRec make_rec(const TileSpace& ts, const Range& rg, long t, int slices_r, int slices_s,
-                                   const RowGroup* groups, int T, int k, const int32_t* perm_src,
-                                   const float* topk_w) {
+template <typename Ix>
+__device__ inline TileRec make_rec(const TileSpace<Ix>& ts, const Range<Ix>& rg, Ix t, int slices_r, int slices_s,
+                                   const RouteView& rv, int T, int k) {
     TileRec r;
-    const TileInfo ti = decode_tile(ts, t, slices_r, slices_s, groups, T);
+    const TileInfo ti = decode_tile(ts, t, slices_r, slices_s, rv, T);
     r.shared = ti.shared;
     r.expert = ti.expert;
     r.group = ti.group;
@@ -237,8 +403,9 @@ __device__ inline TileRec make_rec(const TileSpace& ts, const Range& rg, long t,
     r.nrows = ti.nrows;
     r.slice = ti.slice;
     r.part = ti.part;
-    const long st = ts.start(t), len = ts.len(t);
-    const long lo = st > rg.u0 ? st : rg.u0, hi = st + len < rg.u1 ? st + len : rg.u1;
+    const Ix st = ts.start(t);
+    const int len = ts.len(t);
+    const Ix lo = st > rg.u0 ? st : rg.u0, hi = st + len < rg.u1 ? st + len : rg.u1;
     int kbs;
     ts.tile_of(st, &kbs);
     r.kb0 = kbs + (int)(lo - st);
@@ -249,12 +416,11 @@ __device__ inline TileRec make_rec(const TileSpace& ts, const Range& rg, long t,
     const int Tk = T * k;
     int f[kGroupRows];
 #pragma unroll
-    for (int c = 0; c < kGroupRows; ++c)
-        f[c] = (c < ti.nrows && !ti.shared) ? perm_src[ti.row_begin + c] : -1;
+    for (int c = 0; c < kGroupRows; ++c) f[c] = (c < ti.nrows && !ti.shared) ? route_perm(rv, ti.row_begin + c) : -1;
 #pragma unroll
     for (int c = 0; c < kGroupRows; ++c) {
-        if (topk_w) {
-            r.w[c] = c >= ti.nrows ? 0.f : ti.shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? topk_w[f[c]] : 0.f);
+        if (rv.w) {
+            r.w[c] = c >= ti.nrows ? 0.f : ti.shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? route_w(rv, f[c]) : 0.f);
         } else {
             r.tok[c] = c >= ti.nrows ? -1 : ti.shared ? ti.row_begin + c : ((unsigned)f[c] < (unsigned)Tk ? f[c] / k : -1);
         }
@@ -262,16 +428,24 @@ __device__ inline TileRec make_rec(const TileSpace& ts, const Range& rg, long t,
     return r;
 }
 
+// make_rec kept out of line, for tiles beyond the table (decoded when reached): keeps the
+// streaming loops' register footprint that of a table lookup.
+template <typename Ix>
+__device__ __noinline__ TileRec make_rec_far(const TileSpace<Ix>& ts, const Range<Ix>& rg, Ix t, int slices_r,
+                                             int slices_s, const RouteView& rv, int T, int k) {
+    return make_rec(ts, rg, t, slices_r, slices_s, rv, T, k);
+}
+
 // Decode the tiles of range rg into tab (cooperatively, threads tid of nthreads); the
 // first kMaxTab are stored, the rest are decoded when reached. Returns the tile count.
-__device__ inline int build_table(TileRec* tab, const TileSpace& ts, const Range& rg, int slices_r, int slices_s,
-                                  const RowGroup* groups, int T, int k, const int32_t* perm_src, const float* topk_w,
-                                  int tid, int nthreads) {
+template <typename Ix>
+__device__ inline int build_table(TileRec* tab, const TileSpace<Ix>& ts, const Range<Ix>& rg, int slices_r,
+                                  int slices_s, const RouteView& rv, int T, int k, int tid, int nthreads) {
     int kbl;
-    const long last = ts.tile_of(rg.u1 - 1, &kbl);
+    const Ix last = ts.tile_of(rg.u1 - 1, &kbl);
     const int n = (int)(last - rg.first_tile + 1);
     for (int i = tid; i < n && i < kMaxTab; i += nthreads)
-        tab[i] = make_rec(ts, rg, rg.first_tile + i, slices_r, slices_s, groups, T, k, perm_src, topk_w);
+        tab[i] = make_rec(ts, rg, rg.first_tile + (Ix)i, slices_r, slices_s, rv, T, k);
     return n;
 }
 
@@ -284,36 +458,9 @@ struct Partials {
     int N;      // row length
 };
 
-// Store this warp's share of a tile: vals[m][i] is row warp*16 + g + 8*(i>=2),
-// column 2*t4 + (i&1) of matrix m.
-template <int NMAT>
-__device__ __forceinline__ void store_tile(const float (&vals)[NMAT][4], const TileSpace& ts, const Range& rg, long t,
-                                           const TileInfo& ti, const Partials& pt) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
-    const long st = ts.start(t);
-    const bool holds_start = st >= rg.u0;
-    const bool holds_end = st + ts.len(t) <= rg.u1;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int col = 2 * t4 + (i & 1);
-        if (col >= ti.nrows) continue;
-        const int row = warp * 16 + g + (i >= 2 ? 8 : 0);
-        const size_t o = ((size_t)ti.part * pt.rows + ti.row_begin + col) * pt.N + ti.slice * kTile + row;
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-            if (holds_start) {
-                pt.A[m][o] = vals[m][i];
-                if (holds_end) pt.B[m][o] = 0.f;
-            } else {
-                pt.B[m][o] = vals[m][i];
-            }
-        }
-    }
-}
-
-// Sum over the P parts of A + B at four consecutive channels col4.. of output row
-// `orow` of matrix m.
-// store_tile with the tile described by a TileRec
+// Store this warp's share of the tile described by r: vals[m][i] is row warp*16 + g +
+// 8*(i>=2), column 2*t4 + (i&1) of matrix m. The range holding the tile's first unit
+// writes A (and zeros into B when it also holds the last unit); the other writes B.
 template <int NMAT>
 __device__ __forceinline__ void store_rec(const float (&vals)[NMAT][4], const TileRec& r, const Partials& pt) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t4 = lane & 3;
@@ -335,6 +482,8 @@ __device__ __forceinline__ void store_rec(const float (&vals)[NMAT][4], const Ti
     }
 }
 
+// Sum over the P parts of A + B at four consecutive channels col4.. of output row
+// `orow` of matrix m.
 __device__ __forceinline__ float4 read4(const Partials& pt, int P, int m, long orow, int col4) {
     // all 2P loads first, then the sums in part order: one memory round trip
     float4 a[kMaxParts], b[kMaxParts];
