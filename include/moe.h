@@ -125,7 +125,10 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
  *                           wait has a time and an iteration limit, none traps);
  *   MOE_ERR_INVALID_ARG     a kernel met invalid device data and left it out: an expert id
  *                           outside [0, E) given to moe_permute, a perm_src entry outside
- *                           [0, T*k), or expert offsets that do not cover the permuted rows.
+ *                           [0, T*k), expert offsets that do not cover the permuted rows, or
+ *                           a row-group work record outside the routing's bounds (in a build
+ *                           with -DMOE_DEBUG also: a weight-streaming or grouped-GEMM tile
+ *                           outside its K range, slice, part or rows).
  * A timeout takes precedence when both were recorded. The outputs of a call that recorded
  * an error are unspecified. */
 moe_status_t moe_read_device_status(void* ws, void* stream);

@@ -16,7 +16,8 @@ import torch
 from .synth import MoEConfig
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libmoe_gb300.so")
+# MOE_GB300_LIB: another build of the library (the MOE_DEBUG build, for instance)
+LIB_PATH = os.environ.get("MOE_GB300_LIB") or os.path.join(PKG, "libmoe_gb300.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "moe.h")
 
 MOE_OK = 0

@@ -1,6 +1,6 @@
 """Build libmoe_gb300.so from csrc/*.cu for sm_103a (in-tree, no cmake).
 
-    python -m mixture_experts_layer_gemv_gb300.build
+    python -m mixture_experts_layer_gemv_gb300.build [--debug]
 """
 from __future__ import annotations
 
@@ -15,6 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
+DEBUG_LIB = os.path.join(PKG, "libmoe_gb300_debug.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-I" + INCLUDE]
@@ -36,21 +37,28 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib_path: str = None) -> bool:
+    lib_path = lib_path or LIB
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """debug: the MOE_DEBUG build (device-side checks of the tile decompositions' invariants,
+    reported in the status word), as libmoe_gb300_debug.so beside the library."""
+    lib_path = DEBUG_LIB if debug else LIB
+    build_dir = BUILD + "_debug" if debug else BUILD
+    if debug:
+        extra_flags = (*extra_flags, "-DMOE_DEBUG")
+    if not force and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,15 +69,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True,
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv,
                 extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []))

@@ -43,6 +43,17 @@ __device__ __forceinline__ Item decode_item(const GemmArgs& a, int n_mt_r, int i
         it.nrows = min(kGM, a.T - it.row0);
         it.ntile = v % a.nt_s;
     }
+#ifdef MOE_DEBUG
+    // debug builds: a tile must lie inside its A tensor (a tile that does not is reported
+    // and computed as rows 0.. of expert 0, none of them stored)
+    if (it.nrows < 0 || it.nrows > kGM || it.row0 < 0 || it.row0 + it.nrows > (it.shared ? a.T : a.T * a.k) ||
+        (!it.shared && it.expert < 0)) {
+        set_status(a.status, kStatusBadId);
+        it.row0 = 0;
+        it.nrows = 0;
+        it.expert = it.shared ? -1 : 0;
+    }
+#endif
     return it;
 }
 

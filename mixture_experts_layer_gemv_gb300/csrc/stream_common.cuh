@@ -414,15 +414,32 @@ __device__ inline TileRec make_rec(const TileSpace<Ix>& ts, const Range<Ix>& rg,
     r.he = st + len <= rg.u1;
     r.pad = 0;
     const int Tk = T * k;
+#ifdef MOE_DEBUG
+    // debug builds: the decomposition's invariants for every tile (a tile that breaks one
+    // is reported and streams nothing)
+    {
+        const int kc = ts.kc_of(t), slices = ti.shared ? slices_s : slices_r;
+        const bool ok = r.n >= 1 && r.kb0 >= 0 && r.kb0 + r.n <= kc && r.part >= 0 && r.part < ts.P &&
+                        r.slice >= 0 && r.slice < slices && r.row_begin >= 0 && r.nrows >= 0 &&
+                        r.nrows <= kGroupRows && r.row_begin + r.nrows <= (ti.shared ? T : Tk);
+        if (!ok) {
+            set_status(rv.status, kStatusBadId);
+            r.n = 0;
+            r.nrows = 0;
+            r.row_begin = 0;
+            r.expert = ti.shared ? -1 : 0;
+        }
+    }
+#endif
     int f[kGroupRows];
 #pragma unroll
-    for (int c = 0; c < kGroupRows; ++c) f[c] = (c < ti.nrows && !ti.shared) ? route_perm(rv, ti.row_begin + c) : -1;
+    for (int c = 0; c < kGroupRows; ++c) f[c] = (c < r.nrows && !r.shared) ? route_perm(rv, r.row_begin + c) : -1;
 #pragma unroll
     for (int c = 0; c < kGroupRows; ++c) {
         if (rv.w) {
-            r.w[c] = c >= ti.nrows ? 0.f : ti.shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? route_w(rv, f[c]) : 0.f);
+            r.w[c] = c >= r.nrows ? 0.f : r.shared ? 1.f : ((unsigned)f[c] < (unsigned)Tk ? route_w(rv, f[c]) : 0.f);
         } else {
-            r.tok[c] = c >= ti.nrows ? -1 : ti.shared ? ti.row_begin + c : ((unsigned)f[c] < (unsigned)Tk ? f[c] / k : -1);
+            r.tok[c] = c >= r.nrows ? -1 : r.shared ? r.row_begin + c : ((unsigned)f[c] < (unsigned)Tk ? f[c] / k : -1);
         }
     }
     return r;
