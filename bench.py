@@ -181,12 +181,13 @@ def _launches_per_step(cfg, T: int, mx: bool = False) -> int:
     # small T: fused route + permutation, gate/up, down, combine (both variants)
     if T <= 64:
         return 4
-    # grouped GEMM: router GEMM, top-k, activation quant, permutation (count + scatter), row gather,
-    # gate/up, down, combine
+    # grouped GEMM: router weight split, router GEMM, top-k, activation quant, permutation (count +
+    # scatter), row gather, gate/up, down, combine
     if mx or _gemm_path(cfg, T):
-        return 9
-    # streaming fallback: router GEMM, top-k, activation quant, permutation (2), gate/up, down, combine
-    return 8
+        return 10
+    # streaming fallback: router weight split, router GEMM, top-k, activation quant, permutation (2),
+    # gate/up, down, combine
+    return 9
 
 
 def _gateup_flops(cfg, T: int) -> int:

@@ -585,6 +585,7 @@ BwdLayout bwd_layout(const moe_config_t& c, int64_t T) {
     L.max_mtiles = (int)((R + 127) / 128 + std::min(E, R));
     L.ctrl = take(kCtrlRegionBytes);
     L.logits = take((size_t)L.splits * t * E * 4);
+    L.router_w3 = take(router_w3_bytes(c));
     L.ids = take(R * 4);
     L.w = take(R * 4);
     L.xq = take(t * H);
@@ -671,7 +672,8 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
     // ---- forward quantities: activation codes, the router's logits, the permutation, g and u
     BWD_TRY(launch_quant_act(a.x, T, H, xq, xs, NormArgs{}, st));
     BWD_TRY(launch_route_large(c, a.x, T, a.W->w_router, a.W->router_bias, reinterpret_cast<int32_t*>(at(L.ids)),
-                               f32(L.w), f32(L.logits), L.splits, NormArgs{}, st));
+                               f32(L.w), f32(L.logits), L.splits, NormArgs{}, reinterpret_cast<uint16_t*>(at(L.router_w3)),
+                               &ctrl->status, st));
     BWD_TRY(launch_permute(c, a.topk_ids, T, reinterpret_cast<int32_t*>(at(L.offsets)), perm_src, inv_pos, nullptr,
                            nullptr, mtiles, reinterpret_cast<int32_t*>(at(L.perm_hist)), ctrl, st));
     BWD_TRY(launch_gather_rows(T, H, k, perm_src, xq, at(L.xq_perm), &ctrl->status, st));

@@ -28,8 +28,8 @@ static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 int router_splits_for(const moe_config_t& c, int64_t T) {
     if (T <= kSmallT) return 1;  // the fused small-T route kernel
-    const int64_t tiles = (T + 63) / 64;     // router CTAs: 64 tokens x all experts each
-    int64_t s = (304 + tiles - 1) / tiles;  // aim at two CTAs per SM of a 152-SM part
+    const int64_t tiles = (T + 127) / 128;  // router CTAs: 128 tokens x all experts each
+    int64_t s = 152 / tiles;                // at most one CTA per SM of a 152-SM part
     const int64_t hb = c.hidden / 128;
     if (s > 8) s = 8;
     if (s > hb) s = hb;
@@ -112,6 +112,7 @@ WsLayout ws_layout(const moe_config_t& c, int64_t T, bool mx) {
     }
     L.y_perm = take(t * k * H * 2);
     L.y_shared = take(t * H * 2);
+    L.router_w3 = T > kSmallT ? take(router_w3_bytes(c)) : 0;
     L.total = off;
     return L;
 }
@@ -634,7 +635,8 @@ static moe_status_t route_impl(const moe_config_t* cfg, const void* x_bf16, int3
             MOE_CUDA(launch_rmsnorm(x_bf16, T, cfg->hidden, nm, nullptr, st));
         }
         MOE_CUDA(launch_route_large(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
-                                    L.router_splits, nm, st));
+                                    L.router_splits, nm, at<uint16_t>(ws, L.router_w3), &at<Ctrl>(ws, L.ctrl)->status,
+                                    st));
     }
     return MOE_OK;
 }
@@ -762,7 +764,8 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
             MOE_CUDA(launch_rmsnorm(x_bf16, T, cfg->hidden, nm, nullptr, st));
         }
         MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
-                                    at<float>(ws, L.logits), L.router_splits, nm, st));
+                                    at<float>(ws, L.logits), L.router_splits, nm, at<uint16_t>(ws, L.router_w3),
+                                    &ctrl->status, st));
         MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), nm, st));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
         MOE_TRY(mark.begin(MOE_STAGE_PERMUTE));
@@ -920,7 +923,8 @@ moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16
         return MOE_OK;
     }
     MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
-                                at<float>(ws, L.logits), L.router_splits, NormArgs{}, st));
+                                at<float>(ws, L.logits), L.router_splits, NormArgs{}, at<uint16_t>(ws, L.router_w3),
+                                &ctrl->status, st));
     MOE_CUDA(launch_quant_act_mx(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs8), NormArgs{},
                                  st));
     MOE_TRY(mark.end(MOE_STAGE_ROUTE));

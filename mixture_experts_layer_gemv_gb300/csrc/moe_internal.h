@@ -82,6 +82,7 @@ struct WsLayout {
     size_t hs8_r, hs8_s;   //                and of the intermediate [T*k, I/32], [T, Is/32]
     size_t y_perm;     // bf16 [T*k, H]
     size_t y_shared;   // bf16 [T, H]
+    size_t router_w3;  // bf16 [3][Ep][H]: the router weights' three-way split (large T)
     size_t total;
     int router_splits;
     int max_groups;
@@ -120,11 +121,17 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
                                const NormArgs& nm, cudaStream_t st, uint8_t* xs8 = nullptr,
                                uint64_t* trace = nullptr, bool tail = true);
 
-// Large-T route: router GEMM (split-K partials) + softmax/top-k per token. With
-// nm.gamma the router reads stage M's output on the fly (nm.rstd from launch_rmsnorm).
+// Large-T route: router GEMM (split-K partials) + softmax/top-k per token. Without
+// stage M the GEMM runs on tcgen05 and w3 (router_w3_bytes) receives the weights'
+// three-way bf16 split; with nm.gamma the router applies stage M on the fly (nm.rstd
+// from launch_rmsnorm) on mma.sync and w3 is not used. logits: [splits, T, E] fp32.
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, int splits,
-                               const NormArgs& nm, cudaStream_t st);
+                               const NormArgs& nm, uint16_t* w3, int* status, cudaStream_t st);
+// bytes of the three-way split router weights: bf16 [3][E rounded up to 16][H]
+inline size_t router_w3_bytes(const moe_config_t& c) {
+    return (size_t)3 * ((c.n_routed + 15) & ~15) * c.hidden * 2;
+}
 
 // Stable counting sort of the T*k pairs by expert; writes row groups when groups != nullptr.
 // seg_hist: int32 [permute_segments(T*k), E] scratch.
@@ -258,6 +265,7 @@ cudaError_t launch_gather_rows(int T, int H, int k, const int32_t* perm_src, con
 // Workspace regions of the layer backward (byte offsets), for T tokens.
 struct BwdLayout {
     size_t ctrl, logits, ids, w, xq, xs, offsets, perm_src, inv_pos, perm_hist, mtiles, xq_perm;
+    size_t router_w3;                                 // bf16 [3][Ep][H]: split router weights
     size_t g_r, u_r, dau_r, wahat_r, dgu_r, dx_perm;  // routed rows: fp32 [R, I] x3, bf16 [R, I], [R, 2I], fp32 [R, H]
     size_t g_s, u_s, dau_s, wahat_s, dgu_s, dx_s;     // shared experts' tokens, the same with Is
     size_t dw, dlogit, dlogit_bf;                     // fp32 [T k], fp32 and bf16 [T, E]

@@ -222,13 +222,15 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
 }
 
 // ---------------------------------------------------------------- large T
-// ---- large T: router GEMM on the tensor cores. x is exact in bf16; each fp32 router
-// weight is split as w = hi + mid + lo, three bf16 values (|w - hi - mid - lo| <=
-// 2^-27 |w|, the precision of the fp32 weight itself), and the three products go
+// ---- large T with stage M in front: router GEMM on mma.sync. x is normalised while it
+// is staged (the normalised rows exist nowhere else) and is then exact in bf16; each
+// fp32 router weight is split as w = hi + mid + lo, three bf16 values (|w - hi - mid -
+// lo| <= 2^-27 |w|, the precision of the fp32 weight itself), and the three products go
 // through mma.m16n8k16 (bf16 x bf16, fp32 accumulation). A CTA takes 64 tokens x all
 // experts over a range of K (split-K partials, summed in fixed order by topk_kernel),
 // in 64-wide K steps: the next step's x and router values are loaded into registers
-// while the current step's MMAs run.
+// while the current step's MMAs run. Without stage M the router runs on tcgen05
+// (router_tc_kernel below).
 constexpr int kRM = 64;      // token rows per CTA
 constexpr int kRK = 64;      // K per step
 constexpr int kRPitch = 72;  // bf16 per shared-memory row: 64 + 8 (rows in distinct banks)
@@ -238,7 +240,7 @@ struct RouterMmaParams {
     const uint16_t* x;
     const float* wr;
     float* part;            // [splits, T, E]
-    const uint16_t* gamma;  // stage M applied to x when not null (with rstd [T])
+    const uint16_t* gamma;  // stage M applied to x (with rstd [T])
     const float* rstd;
 };
 
@@ -264,7 +266,7 @@ __device__ __forceinline__ void split3(float w, uint16_t& hi, uint16_t& mid, uin
     lo = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
 }
 
-template <int NTW, bool kNorm>  // 8-wide expert tiles per warp: Ep = 16 * NTW; stage M on load
+template <int NTW>  // 8-wide expert tiles per warp: Ep = 16 * NTW
 __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
     extern __shared__ uint4 smem_r[];
     uint16_t* sx = reinterpret_cast<uint16_t*>(smem_r);  // [64][kRPitch]
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
     uint4 gx[2];       // gamma of those columns (stage M)
     float rs[2];       // 1/rms of those rows
     float4 wv[nw4];    // router tile: Ep rows x 64 fp32
-    constexpr bool norm = kNorm;
+    constexpr bool norm = true;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
         const int t = m0 + ((tid + 256 * q) >> 3);
@@ -372,6 +374,226 @@ __global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
             if (e0 < p.E) out[(size_t)t * p.E + e0] = acc[j][2 * h];
             if (e0 + 1 < p.E) out[(size_t)t * p.E + e0 + 1] = acc[j][2 * h + 1];
         }
+    }
+}
+
+// ---- large T: router GEMM on the tcgen05 tensor cores (kind::f16, fp32 in tensor memory).
+// The fp32 router weights are split once per call into three bf16 parts (router_split_
+// kernel: hi + mid + lo, as split3), stacked as [3][Ep][H] with zero rows from E to Ep;
+// x is exact in bf16. A CTA takes 128 tokens x all experts over a range of K (split-K
+// partials, summed in fixed order by topk_kernel), in 64-wide K steps: per step the three
+// parts' products (12 MMAs of M=128, N=Ep, K=16, the small parts first) accumulate in a
+// fresh TMEM accumulator (the tensor core truncates small products against a large
+// accumulator), which the epilogue adds into fp32 registers while the tensor core fills
+// the other accumulator with the next step. Warp 9: TMA producer (an x box of 128 rows
+// and the three parts' boxes of Ep rows per step); warp 8: MMA issuer; warps 0-7:
+// epilogue (warp w reads lanes 32*(w%4).. and the 16-column chunks c = w/4, w/4+2, ...).
+constexpr int kRTM = 128;            // tokens per CTA (MMA M)
+constexpr int kRTK = 64;             // bf16 per K step (128 bytes)
+constexpr int kRTEpi = 8;
+constexpr int kRTMma = kRTEpi;
+constexpr int kRTProd = kRTEpi + 1;
+constexpr int kRTThreads = (kRTEpi + 2) * 32;
+constexpr int kRTSA = kRTM * kRTK * 2;   // 16 KB x box
+
+// TMEM columns per accumulator buffer: the power of two >= Ep (two buffers per CTA)
+__host__ __device__ constexpr uint32_t rt_buf_cols(int Ep) {
+    uint32_t c = 16;
+    while (c < (uint32_t)Ep) c <<= 1;
+    return c;
+}
+
+struct RouterTcParams {
+    int T, E, Ep, H, k_per_split, n_mt, stages;
+    float* part;  // [splits, T, E]
+    int* status;
+};
+
+__global__ void __launch_bounds__(256) router_split_kernel(const float* wr, int E, int Ep, int H, uint16_t* out) {
+    const size_t plane = (size_t)Ep * H, n4 = plane / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t o = 4 * i;
+        const int e = (int)(o / H);
+        const float4 v = e < E ? __ldg(reinterpret_cast<const float4*>(wr) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float w4[4] = {v.x, v.y, v.z, v.w};
+        uint16_t h[4], m[4], l[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) split3(w4[u], h[u], m[u], l[u]);
+        *reinterpret_cast<uint2*>(out + o) = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+        *reinterpret_cast<uint2*>(out + plane + o) =
+            make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
+        *reinterpret_cast<uint2*>(out + 2 * plane + o) =
+            make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
+    }
+}
+
+template <int NCH>  // 16-column chunks of the accumulator: Ep = 16 * NCH
+__global__ void __launch_bounds__(kRTThreads, 1)
+    router_tc_kernel(const RouterTcParams p, const __grid_constant__ TmaMap tm_x, const __grid_constant__ TmaMap tm_w) {
+    constexpr int Ep = 16 * NCH;
+    constexpr int kSB = 3 * Ep * kRTK * 2;  // the three parts' boxes
+    constexpr int kStage = kRTSA + kSB;     // a multiple of 1024 (Ep is a multiple of 16)
+    constexpr int kMyCh = (NCH + 1) / 2;    // chunks per epilogue thread (at most)
+    static_assert(kRTM * (Ep + 4) * 4 <= 2 * kStage, "the output block is staged in the (at least two) stages");
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kRTM, Ep);
+    constexpr uint32_t kBuf = rt_buf_cols(Ep);
+    constexpr uint32_t kAlloc = 2 * kBuf < 32 ? 32 : 2 * kBuf;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kStage);
+    uint64_t* empty = full + S;
+    uint64_t* acc_full = empty + S;   // [2]
+    uint64_t* acc_empty = acc_full + 2;  // [2]
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int mt = blockIdx.x % p.n_mt, split = blockIdx.x / p.n_mt;
+    const int k0 = split * p.k_per_split, k1 = min(p.H, k0 + p.k_per_split);
+    const int nsteps = k1 > k0 ? (k1 - k0) / kRTK : 0;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kRTEpi);
+        }
+        fence_mbar_init();
+    }
+    if (warp == kRTMma) {
+        tmem_alloc(s_tmem, kAlloc);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    if (warp == kRTProd) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && nsteps > 0) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_w);
+            int n = 0;
+            for (; n < nsteps; ++n) {
+                const int s = n % S;
+                if (n >= S && !mbar_wait_bounded(&empty[s], ((n / S) - 1) & 1)) {
+                    set_status(p.status, kStatusTimeout);
+                    break;
+                }
+                uint8_t* st = smem + s * kStage;
+                const int x = k0 + n * kRTK;
+                mbar_arrive_expect_tx(&full[s], kStage);
+                tma_load_2d(st, &tm_x, x, mt * kRTM, &full[s]);
+#pragma unroll
+                for (int part = 0; part < 3; ++part)
+                    tma_load_2d(st + kRTSA + part * Ep * kRTK * 2, &tm_w, x, part * Ep, &full[s]);
+            }
+            // copies still in flight land before this CTA may exit
+            for (int q = n > S ? n - S : 0; q < n; ++q) mbar_wait_bounded(&full[q % S], (q / S) & 1);
+        }
+    } else if (warp == kRTMma) {
+        // -------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int n = 0;
+            for (; n < nsteps; ++n) {
+                const int s = n % S, b = n & 1;
+                if ((n >= 2 && !mbar_wait_bounded(&acc_empty[b], ((n >> 1) - 1) & 1)) ||
+                    !mbar_wait_bounded(&full[s], (n / S) & 1)) {
+                    set_status(p.status, kStatusTimeout);
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t* st = smem + s * kStage;
+                const uint64_t da = smem_desc_sw128(st);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)  // 4 x K=16 (32 bytes) inside the 128-byte swizzled rows
+#pragma unroll
+                    for (int part = 2; part >= 0; --part) {  // small parts first
+                        const uint64_t db = smem_desc_sw128(st + kRTSA + part * Ep * kRTK * 2);
+                        tc_mma_bf16(tmem + b * kBuf, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), kIdesc,
+                                    (k | (2 - part)) != 0);
+                    }
+                tc_commit(&empty[s]);
+                tc_commit(&acc_full[b]);
+            }
+            // every MMA issued has completed before the CTA frees tensor memory
+            if (n > 0) mbar_wait_bounded(&acc_full[(n - 1) & 1], ((n - 1) >> 1) & 1);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int q4 = warp & 3, half = warp >> 2;
+        const int row = 32 * q4 + lane;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * q4) << 16);
+        float acc[kMyCh][16];
+#pragma unroll
+        for (int c = 0; c < kMyCh; ++c)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[c][j] = 0.f;
+        bool ok = true;
+        for (int n = 0; n < nsteps; ++n) {
+            const int b = n & 1;
+            if (ok && !mbar_wait_bounded(&acc_full[b], (n >> 1) & 1)) ok = false;
+            ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+            tc_fence_after();
+            if (ok) {
+#pragma unroll
+                for (int c = 0; c < kMyCh; ++c) {
+                    const int ch = half + 2 * c;
+                    if (ch < NCH) {
+                        float v[16];
+                        tmem_ld16(t_row + b * kBuf + 16 * ch, v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[c][j] += v[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
+        }
+        if (!ok) set_status(p.status, kStatusTimeout);
+        // The CTA's partial logits are one contiguous [rows, E] block of part: stage them
+        // in shared memory (the stages are free: every copy was consumed by an MMA that
+        // has completed) with a row pitch of Ep + 4 floats, so that a warp's 16-byte
+        // stores of 32 rows fall in distinct banks, then store the block coalesced.
+        constexpr int kPitch = Ep + 4;
+        float* stg = reinterpret_cast<float*>(smem);
+#pragma unroll
+        for (int c = 0; c < kMyCh; ++c) {
+            const int ch = half + 2 * c;
+            if (ch < NCH)
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4*>(stg + row * kPitch + 16 * ch + j) =
+                        make_float4(acc[c][j], acc[c][j + 1], acc[c][j + 2], acc[c][j + 3]);
+        }
+        named_bar(1, kRTEpi * 32);
+        const int rows = min(kRTM, p.T - mt * kRTM), E = p.E;
+        float* out = p.part + ((size_t)split * p.T + (size_t)mt * kRTM) * E;
+        if ((E & 3) == 0) {
+            const int q = E >> 2, n = rows * q;
+            for (int i = tid; i < n; i += kRTEpi * 32) {
+                const int r = i / q, c4 = i - r * q;
+                reinterpret_cast<float4*>(out)[i] = *reinterpret_cast<const float4*>(stg + r * kPitch + 4 * c4);
+            }
+        } else {
+            const int n = rows * E;
+            for (int i = tid; i < n; i += kRTEpi * 32) {
+                const int r = i / E;
+                out[i] = stg[r * kPitch + (i - r * E)];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kRTMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kAlloc);
     }
 }
 
@@ -569,49 +791,105 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
 
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, int splits,
-                               const NormArgs& nm, cudaStream_t st) {
-    RouterMmaParams g;
-    g.H = c.hidden;
-    g.E = c.n_routed;
-    g.Ep = (c.n_routed + 15) & ~15;
-    g.T = T;
-    const int Hb = c.hidden / kBlk;
-    g.k_per_split = ((Hb + splits - 1) / splits) * kBlk;
-    g.x = static_cast<const uint16_t*>(x);
-    g.wr = w_router;
-    g.part = logits;
-    g.gamma = nm.gamma;
-    g.rstd = nm.rstd;
-    const size_t smem = ((size_t)kRM + 3 * (size_t)g.Ep) * kRPitch * sizeof(uint16_t);
-    const dim3 grid((T + kRM - 1) / kRM, splits);
-    auto run = [&](auto kern) -> cudaError_t {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        kern<<<grid, 256, smem, st>>>(g);
-        return cudaGetLastError();
-    };
+                               const NormArgs& nm, uint16_t* w3, int* status, cudaStream_t st) {
+    const int H = c.hidden, E = c.n_routed, Ep = (E + 15) & ~15;
+    const int Hb = H / kBlk;
+    const int k_per_split = ((Hb + splits - 1) / splits) * kBlk;
     cudaError_t e2 = cudaErrorInvalidValue;
-    auto pick = [&](auto ntw) -> cudaError_t {
-        constexpr int N = decltype(ntw)::value;
-        return g.gamma ? run(router_mma_kernel<N, true>) : run(router_mma_kernel<N, false>);
-    };
-    switch (g.Ep / 16) {  // n_routed <= 256
-        case 1: e2 = pick(std::integral_constant<int, 1>{}); break;
-        case 2: e2 = pick(std::integral_constant<int, 2>{}); break;
-        case 3: e2 = pick(std::integral_constant<int, 3>{}); break;
-        case 4: e2 = pick(std::integral_constant<int, 4>{}); break;
-        case 5: e2 = pick(std::integral_constant<int, 5>{}); break;
-        case 6: e2 = pick(std::integral_constant<int, 6>{}); break;
-        case 7: e2 = pick(std::integral_constant<int, 7>{}); break;
-        case 8: e2 = pick(std::integral_constant<int, 8>{}); break;
-        case 9: e2 = pick(std::integral_constant<int, 9>{}); break;
-        case 10: e2 = pick(std::integral_constant<int, 10>{}); break;
-        case 11: e2 = pick(std::integral_constant<int, 11>{}); break;
-        case 12: e2 = pick(std::integral_constant<int, 12>{}); break;
-        case 13: e2 = pick(std::integral_constant<int, 13>{}); break;
-        case 14: e2 = pick(std::integral_constant<int, 14>{}); break;
-        case 15: e2 = pick(std::integral_constant<int, 15>{}); break;
-        case 16: e2 = pick(std::integral_constant<int, 16>{}); break;
+    if (!nm.gamma) {
+        // tcgen05 path: split the router weights, then the GEMM
+        if (!w3) return cudaErrorInvalidValue;
+        {
+            const size_t n4 = (size_t)Ep * H / 4;
+            const unsigned blocks = (unsigned)std::min<size_t>(1024, (n4 + 255) / 256);
+            router_split_kernel<<<blocks, 256, 0, st>>>(w_router, E, Ep, H, w3);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        TmaMap tx, tw;
+        if (!tmap_bf16_2d(&tx, x, (uint64_t)T, (uint64_t)H, kRTK, kRTM) ||
+            !tmap_bf16_2d(&tw, w3, (uint64_t)3 * Ep, (uint64_t)H, kRTK, (uint32_t)Ep))
+            return cudaErrorInvalidValue;
+        RouterTcParams p;
+        p.T = T;
+        p.E = E;
+        p.Ep = Ep;
+        p.H = H;
+        p.k_per_split = k_per_split;
+        p.n_mt = (T + kRTM - 1) / kRTM;
+        p.part = logits;
+        p.status = status;
+        const size_t stage = (size_t)kRTSA + 3 * (size_t)Ep * kRTK * 2;
+        const size_t room = 227 * 1024 - 1024 - 256;
+        p.stages = (int)std::min<size_t>(4, room / stage);
+        if (p.stages < 2) return cudaErrorInvalidValue;
+        const size_t smem = 1024 + (size_t)p.stages * stage + 256;
+        auto run = [&](auto kern) -> cudaError_t {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            kern<<<p.n_mt * splits, kRTThreads, smem, st>>>(p, tx, tw);
+            return cudaGetLastError();
+        };
+        auto pick = [&](auto nch) -> cudaError_t { return run(router_tc_kernel<decltype(nch)::value>); };
+        switch (Ep / 16) {  // n_routed <= 256
+            case 1: e2 = pick(std::integral_constant<int, 1>{}); break;
+            case 2: e2 = pick(std::integral_constant<int, 2>{}); break;
+            case 3: e2 = pick(std::integral_constant<int, 3>{}); break;
+            case 4: e2 = pick(std::integral_constant<int, 4>{}); break;
+            case 5: e2 = pick(std::integral_constant<int, 5>{}); break;
+            case 6: e2 = pick(std::integral_constant<int, 6>{}); break;
+            case 7: e2 = pick(std::integral_constant<int, 7>{}); break;
+            case 8: e2 = pick(std::integral_constant<int, 8>{}); break;
+            case 9: e2 = pick(std::integral_constant<int, 9>{}); break;
+            case 10: e2 = pick(std::integral_constant<int, 10>{}); break;
+            case 11: e2 = pick(std::integral_constant<int, 11>{}); break;
+            case 12: e2 = pick(std::integral_constant<int, 12>{}); break;
+            case 13: e2 = pick(std::integral_constant<int, 13>{}); break;
+            case 14: e2 = pick(std::integral_constant<int, 14>{}); break;
+            case 15: e2 = pick(std::integral_constant<int, 15>{}); break;
+            case 16: e2 = pick(std::integral_constant<int, 16>{}); break;
+        }
+    } else {
+        // stage M in front: the normalised x exists only in registers, so the router
+        // applies it while staging x in shared memory (mma.sync path)
+        RouterMmaParams g;
+        g.H = H;
+        g.E = E;
+        g.Ep = Ep;
+        g.T = T;
+        g.k_per_split = k_per_split;
+        g.x = static_cast<const uint16_t*>(x);
+        g.wr = w_router;
+        g.part = logits;
+        g.gamma = nm.gamma;
+        g.rstd = nm.rstd;
+        const size_t smem = ((size_t)kRM + 3 * (size_t)g.Ep) * kRPitch * sizeof(uint16_t);
+        const dim3 grid((T + kRM - 1) / kRM, splits);
+        auto run = [&](auto kern) -> cudaError_t {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            kern<<<grid, 256, smem, st>>>(g);
+            return cudaGetLastError();
+        };
+        auto pick = [&](auto ntw) -> cudaError_t { return run(router_mma_kernel<decltype(ntw)::value>); };
+        switch (g.Ep / 16) {  // n_routed <= 256
+            case 1: e2 = pick(std::integral_constant<int, 1>{}); break;
+            case 2: e2 = pick(std::integral_constant<int, 2>{}); break;
+            case 3: e2 = pick(std::integral_constant<int, 3>{}); break;
+            case 4: e2 = pick(std::integral_constant<int, 4>{}); break;
+            case 5: e2 = pick(std::integral_constant<int, 5>{}); break;
+            case 6: e2 = pick(std::integral_constant<int, 6>{}); break;
+            case 7: e2 = pick(std::integral_constant<int, 7>{}); break;
+            case 8: e2 = pick(std::integral_constant<int, 8>{}); break;
+            case 9: e2 = pick(std::integral_constant<int, 9>{}); break;
+            case 10: e2 = pick(std::integral_constant<int, 10>{}); break;
+            case 11: e2 = pick(std::integral_constant<int, 11>{}); break;
+            case 12: e2 = pick(std::integral_constant<int, 12>{}); break;
+            case 13: e2 = pick(std::integral_constant<int, 13>{}); break;
+            case 14: e2 = pick(std::integral_constant<int, 14>{}); break;
+            case 15: e2 = pick(std::integral_constant<int, 15>{}); break;
+            case 16: e2 = pick(std::integral_constant<int, 16>{}); break;
+        }
     }
     if (e2 != cudaSuccess) return e2;
     cudaError_t err = cudaGetLastError();
