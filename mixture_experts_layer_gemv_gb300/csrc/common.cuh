@@ -131,6 +131,17 @@ __device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint3
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
+// (a0, a1) = (v0 * c + a0, v1 * c + a1) in one packed FP32 instruction (fma.rn.f32x2:
+// each lane rounds once, as fmaf does); halves the issue slots of a scale promotion.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, float c) {
+    unsigned long long A, V, C, D;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(V) : "f"(v0), "f"(v1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(C) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(V), "l"(C), "l"(A));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(D));
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
     return __uint_as_float((uint32_t)b << 16);
 }

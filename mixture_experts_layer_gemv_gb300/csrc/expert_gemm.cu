@@ -14,7 +14,7 @@
 //     acc[m][n] += D_kb[m][n] * s_x[m][kb] * s_w[n-block][kb],
 // while the tensor core fills the other accumulator with the next K block.
 //
-// One CTA of 10 warps per SM, persistent over tiles, warp-specialised:
+// One CTA of 12 warps per SM, persistent over tiles, warp-specialised:
 //   warp 9      TMA producer: per K block an A box (128 rows x 128 B) and two B boxes
 //               (128 rows x 128 B) into a 4-stage ring; a stage is refilled as soon as
 //               the MMAs that read it have completed
@@ -23,6 +23,15 @@
 //   warps 0-7   epilogue: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and, with
 //               g = w/4, columns [64g, 64g+64) of gate and of up (or [128g, 128g+128) of
 //               down), so each thread keeps a 128-float accumulator row in registers
+//   warps 10-11 idle (they complete the third warpgroup)
+// Registers: the CTA is launched with 168 per thread (three warps on each of the four
+// 16K-register sub-partition files); the third warpgroup (MMA, producer, idle) then
+// gives back all but 56 of its registers (setmaxnreg) and the two epilogue warpgroups
+// grow to 224, room for the accumulator row plus a 64-column TMEM slice.
+// Per K block an epilogue thread loads its two 64-column halves from TMEM in turn, each
+// followed by its multiply-adds (packed FP32 pairs), and then releases the accumulator
+// to the MMA warp. (Releasing it before the second half's multiply-adds measured
+// slower: 1.05 against 1.03 ms for the T=4096 gate/up GEMM.)
 // Activation scales come from global memory (row-major, one row per thread) and the
 // weight scales of the tile's row blocks too; both are loaded one K block ahead.
 // Epilogue at the end of a tile: gate/up -> a = SiLU(g) * u, quantised per 128 values
@@ -41,7 +50,11 @@ constexpr int kGStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = kEpiWarps;
 constexpr int kProducerWarp = kEpiWarps + 1;
-constexpr int kGThreads = (kEpiWarps + 2) * 32;
+constexpr int kGThreads = (kEpiWarps + 4) * 32;  // + a warpgroup: MMA, producer, two idle warps
+constexpr int kLaunchRegs = 168;                  // per thread at launch (__launch_bounds__ below)
+constexpr int kEpiRegs = 224, kCtlRegs = 56;      // after the split
+static_assert(kEpiWarps * 32 * kEpiRegs + 128 * kCtlRegs == kGThreads * kLaunchRegs,
+              "the register split hands over exactly what the launch holds");
 constexpr int kSA = kGM * kBlk;           // 16 KB A tile
 constexpr int kSB = kGN * kBlk;           // 32 KB B tile
 constexpr int kStageBytes = kSA + kSB;    // a multiple of 1024 (128-byte swizzle atoms)
@@ -104,6 +117,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // K blocks this CTA runs, over all its items
     const int total = items_in(0, n_r) * (a.K_r / kBlk) + items_in(n_r, n_items) * (a.K_s / kBlk);
 
+    if (warp >= kEpiWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
     if (warp == kProducerWarp) {
         // ----------------------------------------------------------- TMA producer
         if (lane == 0 && total > 0) {
@@ -158,7 +173,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
             // every MMA issued has completed before the CTA frees tensor memory
             if (n > 0) mbar_wait_bounded(&acc_full[(n - 1) & 1], ((n - 1) >> 1) & 1);
         }
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
         // ---------------------------------------------------------------- epilogue
         const int q4 = warp & 3;          // TMEM lane quadrant: rows 32q .. 32q+31
         const int wg = warp >> 2;         // column half
@@ -212,20 +229,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 // tcgen05.ld is warp-collective: the whole warp reads, or none of it
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
+                // half h: gate/up: 0 = gate cols 64wg.., 1 = up cols 128+64wg..; down: cols 128wg + 64h
+                const uint32_t tb = t_row + (uint32_t)(b * kGN);
                 if (ok) {
-                    const uint32_t tb = t_row + (uint32_t)(b * kGN);
+                    float v[64];
+                    tmem_ld64(tb + (gateup ? 64 * wg : 128 * wg), v);
 #pragma unroll
-                    for (int h = 0; h < 8; ++h) {
-                        // gate/up: chunks 0-3 = gate cols 64wg.., chunks 4-7 = up cols 128+64wg..
-                        // down: chunks 0-7 = cols 128wg..
-                        const int col = gateup ? (h < 4 ? 64 * wg + 16 * h : 128 + 64 * wg + 16 * (h - 4))
-                                               : 128 * wg + 16 * h;
-                        float v[16];
-                        tmem_ld16(tb + col, v);
-                        const float c = (gateup && h >= 4) ? c1 : c0;
+                    for (int j = 0; j < 64; j += 2) fma2(acc[j], acc[j + 1], v[j], v[j + 1], c0);
+                    tmem_ld64(tb + (gateup ? 128 + 64 * wg : 128 * wg + 64), v);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[16 * h + j] = fmaf(v[j], c, acc[16 * h + j]);
-                    }
+                    for (int j = 0; j < 64; j += 2) fma2(acc[64 + j], acc[64 + j + 1], v[j], v[j + 1], c1);
                 }
                 tc_fence_before();
                 __syncwarp();
