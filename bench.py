@@ -178,9 +178,10 @@ def _gemm_path(cfg, T: int) -> bool:
 
 
 def _launches_per_step(cfg, T: int, mx: bool = False) -> int:
-    # small T: fused route + permutation, gate/up, down, combine (both variants)
+    # small T: route (+ top-k and permutation up to 8 tokens), gate/up, down, combine (both
+    # variants); above 8 tokens top-k and the permutation are two kernels of their own
     if T <= 64:
-        return 4
+        return 4 if T <= 8 else 6
     # grouped GEMM: router weight split, router GEMM, top-k, activation quant, permutation (count +
     # scatter), row gather, gate/up, down, combine
     if mx or _gemm_path(cfg, T):

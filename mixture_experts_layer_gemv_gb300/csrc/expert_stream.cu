@@ -149,7 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane != 0) return;
         // failure-detection tests: issue nothing, so that every consumer wait runs out
         if (s_inject & kInjectSkipGateupLoads) return;
-        const uint64_t wpol = l2_policy_evict_first();  // used when a.stream_once
+        // Evict-first: the routed experts' weights always (a row group's pass over them is
+        // not followed by another soon enough to hit in L2, and the partial sums that the
+        // down kernel and the combine read back should outlive them), the shared experts'
+        // only when no other row group reads them again (up to 8 tokens).
+        const uint64_t wpol = l2_policy_evict_first();
         int s = 0, ph = 0;
         long q = 0;  // units issued
         bool stop = false;
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = r.kb0 + j;
                 uint8_t* st = smem + s * SB;
                 mbar_arrive_expect_tx(&full[s], 2 * kBox + nrow * kBlk);
-                if (a.stream_once) {
+                if (a.stream_once || !r.shared) {
                     tma_load_2d_hint(st, mg, kb * kBlk, y, &full[s], wpol);
                     tma_load_2d_hint(st + kBox, mu, kb * kBlk, y, &full[s], wpol);
                 } else {
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && active) {
             prefetch_tmap(&tm_d);
             if (a.Is > 0) prefetch_tmap(&tm_sd);
-            const uint64_t wpol = l2_policy_evict_first();  // used when a.stream_once
+            const uint64_t wpol = l2_policy_evict_first();  // the routed experts' weights, or all up to 8 tokens
             int s = 0, ph = 0;
             long q = 0;  // units issued
             bool stop = false;
@@ -529,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], kBox);
-                    if (a.stream_once)
+                    if (a.stream_once || !r.shared)
                         tma_load_2d_hint(smem + s * SB, md, (r.kb0 + j) * kBlk, y, &full[s], wpol);
                     else
                         tma_load_2d(smem + s * SB, md, (r.kb0 + j) * kBlk, y, &full[s]);

@@ -167,6 +167,7 @@ struct StreamArgs {
     int max_groups;                 // row-group capacity of the workspace
     int wide;                       // 1: unit indices may exceed 2^31 (64-bit tile arithmetic)
     int stream_once;                // 1: every weight byte is read by one row group (T <= 8): evict-first loads
+                                    // of the shared experts too (the routed experts' always)
     const Ctrl* ctrl;
     const RowGroup* groups;
     const int32_t* group_of_row;  // [T*k] row group of each permuted row

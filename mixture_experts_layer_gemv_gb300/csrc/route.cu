@@ -22,6 +22,7 @@ namespace moe {
 namespace {
 
 constexpr int kRouteWarps = 8;
+constexpr int kTailNT = 4;  // tokens per warp in the last CTA's top-k (T > 1)
 
 using namespace routing;
 
@@ -51,8 +52,9 @@ struct RouteSmallParams {
 
 // kNorm: stage M in front of the router (p.gamma != nullptr); kMX: x quantised per 32
 // values with E8M0 scales (p.xs8) instead of per 128 with fp32 scales (p.xs)
+// (Two CTAs per SM without stage M: the 160 CTAs of a 160-expert layer in one wave.)
 template <bool kNorm, bool kMX>
-__global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmallParams p) {
+__global__ void __launch_bounds__(kRouteWarps * 32, kNorm ? 1 : 2) route_small_kernel(RouteSmallParams p) {
     __shared__ float s_part[kRouteWarps][kSmallT];
     __shared__ alignas(16) float s_gs[kRouteWarps][kMaxE];
     __shared__ int32_t s_ids[kSmallT * 16];
@@ -202,15 +204,27 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_small_kernel(RouteSmal
         cta_topk1(p.logits, p.E, p.G, p.Gk, p.k, p.scale, scratch, scratch + kMaxE,
                   reinterpret_cast<float*>(scratch + kMaxE + 32), p.ids, p.w, s_ids);
     } else {
-        for (int t = warp; t < T; t += kRouteWarps) {
-            float lg[kMaxE / 32];
+        // kTailNT tokens per warp side by side (tokens t0 + q * kRouteWarps), all their
+        // logits loaded at once
+        for (int t0 = warp; t0 < T; t0 += kRouteWarps * kTailNT) {
+            float lg[kTailNT][kMaxE / 32];
+            int32_t* io[kTailNT];
+            float* wo[kTailNT];
+            int32_t* so[kTailNT];
 #pragma unroll
-            for (int i = 0; i < kMaxE / 32; ++i) {
-                const int ee = lane + 32 * i;
-                lg[i] = ee < p.E ? __ldcg(p.logits + (size_t)t * p.E + ee) : -INFINITY;
+            for (int q = 0; q < kTailNT; ++q) {
+                const int t = t0 + q * kRouteWarps;
+                const bool valid = t < T;
+#pragma unroll
+                for (int i = 0; i < kMaxE / 32; ++i) {
+                    const int ee = lane + 32 * i;
+                    lg[q][i] = valid && ee < p.E ? __ldcg(p.logits + (size_t)t * p.E + ee) : -INFINITY;
+                }
+                io[q] = valid ? p.ids + (size_t)t * p.k : nullptr;
+                wo[q] = valid ? p.w + (size_t)t * p.k : nullptr;
+                so[q] = valid ? s_ids + t * p.k : nullptr;
             }
-            topk_warp(lg, p.E, p.G, p.Gk, p.k, p.scale, s_gs[warp], p.ids + (size_t)t * p.k, p.w + (size_t)t * p.k,
-                      s_ids + t * p.k);
+            topk_warp_n<kTailNT>(lg, p.E, p.G, p.Gk, p.k, p.scale, io, wo, so);
         }
     }
     __syncthreads();
@@ -608,6 +622,8 @@ struct TopkParams {
 
 __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
     __shared__ float s_gs[8][kMaxE];
+    pdl_wait();  // the logits (launched with programmatic serialization after the small-T router)
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.T) return;
@@ -626,6 +642,23 @@ __global__ void __launch_bounds__(256) topk_kernel(TopkParams p) {
     }
     topk_warp(lg, p.E, p.G, p.Gk, p.k, p.scale, s_gs[warp], p.ids + (size_t)t * p.k, p.w + (size_t)t * p.k,
               nullptr);
+}
+
+// The permutation and row-group work list of up to kSmallT tokens from topk_kernel's ids,
+// by one CTA (the small-T router's tail, split off when its last CTA would rank more
+// than one token per warp).
+__global__ void __launch_bounds__(256) route_permute_kernel(const int32_t* ids, int n, int E, int32_t* offsets,
+                                                            int32_t* perm_src, int32_t* inv_pos, RowGroup* groups,
+                                                            int32_t* group_of_row, int* n_groups) {
+    __shared__ int32_t s_ids[kSmallT * 16];
+    __shared__ int s_rank[kSmallT * 16];
+    __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_gcnt[kMaxE], s_goff[kMaxE];
+    pdl_wait();  // topk_kernel's ids
+    pdl_launch_dependents();
+    for (int f = threadIdx.x; f < n; f += blockDim.x) s_ids[f] = ids[f];
+    __syncthreads();
+    small_permute(s_ids, n, E, s_cnt, s_off, s_gcnt, s_goff, s_rank, offsets, perm_src, inv_pos, groups, group_of_row,
+                  n_groups);
 }
 
 // x [T, H] bf16 -> xq codes + scales. Each thread takes 32 consecutive values. Per-128
@@ -744,8 +777,12 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
                                float* xs, int32_t* offsets, int32_t* perm_src, int32_t* inv_pos,
                                RowGroup* groups, int32_t* group_of_row, Ctrl* ctrl, const NormArgs& nm,
                                cudaStream_t st, uint8_t* xs8, uint64_t* trace, bool tail) {
+    // Above kRouteWarps tokens the last CTA would rank several tokens per warp on one SM
+    // (~3 us each): the router then leaves the logits, and top-k (one warp per token
+    // over T/8 CTAs) and the permutation run as two chained kernels.
+    const bool split = tail && offsets != nullptr && T > kRouteWarps;
     RouteSmallParams p;
-    p.tail = tail ? 1 : 0;
+    p.tail = tail && !split ? 1 : 0;
     p.H = c.hidden;
     p.E = c.n_routed;
     p.G = c.n_group;
@@ -780,13 +817,36 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cudaError_t e;
     if (xs8) {
         p.xs8 = xs8;
-        return nm.gamma ? cudaLaunchKernelEx(&cfg, route_small_kernel<true, true>, p)
-                        : cudaLaunchKernelEx(&cfg, route_small_kernel<false, true>, p);
+        e = nm.gamma ? cudaLaunchKernelEx(&cfg, route_small_kernel<true, true>, p)
+                     : cudaLaunchKernelEx(&cfg, route_small_kernel<false, true>, p);
+    } else {
+        e = nm.gamma ? cudaLaunchKernelEx(&cfg, route_small_kernel<true, false>, p)
+                     : cudaLaunchKernelEx(&cfg, route_small_kernel<false, false>, p);
     }
-    return nm.gamma ? cudaLaunchKernelEx(&cfg, route_small_kernel<true, false>, p)
-                    : cudaLaunchKernelEx(&cfg, route_small_kernel<false, false>, p);
+    if (e != cudaSuccess || !split) return e;
+    TopkParams t;
+    t.E = c.n_routed;
+    t.G = c.n_group;
+    t.Gk = c.topk_group;
+    t.k = c.top_k;
+    t.T = T;
+    t.splits = 1;
+    t.scale = c.routed_scaling_factor;
+    t.part = logits;
+    t.bias = nullptr;  // the router's logits include it
+    t.ids = ids;
+    t.w = w;
+    cfg.gridDim = dim3((T + 7) / 8);
+    cfg.blockDim = dim3(256);
+    e = cudaLaunchKernelEx(&cfg, topk_kernel, t);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(1);
+    return cudaLaunchKernelEx(&cfg, route_permute_kernel, static_cast<const int32_t*>(ids), T * c.top_k,
+                              (int)c.n_routed, offsets, perm_src, inv_pos, groups, group_of_row,
+                              &ctrl->n_routed_groups);
 }
 
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,

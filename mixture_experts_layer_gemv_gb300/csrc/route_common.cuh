@@ -29,15 +29,26 @@ __device__ __forceinline__ unsigned float_key(float f) {
 // groups beat it (higher score, or equal score and lower index). The experts are then
 // taken in top_k rounds of a warp-wide arg-max over the members of kept groups (ties
 // to the lower index), so slot j holds the j-th best: the greedy order.
-__device__ inline void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, int Gk, int k, float scale,
-                                 float* scratch, int32_t* ids_out, float* w_out, int32_t* ids_smem) {
-    (void)scratch;
+//
+// topk_warp_n runs NT tokens through the same steps side by side in one warp (token q's
+// logits in lg[q]; its outputs through ids_out[q], w_out[q], ids_smem[q], each skipped when
+// null): every token's arithmetic is exactly topk_warp's, and the NT independent chains of
+// warp-wide reductions overlap their latencies.
+template <int NT>
+__device__ inline void topk_warp_n(const float (&lg)[NT][kMaxE / 32], int E, int G, int Gk, int k, float scale,
+                                   int32_t* const (&ids_out)[NT], float* const (&w_out)[NT],
+                                   int32_t* const (&ids_smem)[NT]) {
     const int lane = threadIdx.x & 31;
     const int per = E / G;
-    float mx = -INFINITY;
+    float mx[NT];
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) mx = fmaxf(mx, lg[i]);
-    mx = warp_max(mx);
+    for (int q = 0; q < NT; ++q) {
+        mx[q] = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i) mx[q] = fmaxf(mx[q], lg[q][i]);
+    }
+#pragma unroll
+    for (int q = 0; q < NT; ++q) mx[q] = warp_max(mx[q]);
     // group scores: lane g keeps the best key of group g
     int gid[kMaxE / 32];
 #pragma unroll
@@ -45,57 +56,96 @@ __device__ inline void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, in
         const int e = lane + 32 * i;
         gid[i] = e < E ? e / per : -1;
     }
-    unsigned gkey = 0u;
+    unsigned gkey[NT];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) gkey[q] = 0u;
     for (int gi = 0; gi < G; ++gi) {
-        unsigned m = 0u;
 #pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i)
-            if (gid[i] == gi) m = max(m, float_key(lg[i]));
-        m = __reduce_max_sync(0xffffffffu, m);
-        if (lane == gi) gkey = m;
-    }
-    int beaten = 0;
-    for (int h = 0; h < G; ++h) {
-        const unsigned o = __shfl_sync(0xffffffffu, gkey, h);
-        beaten += (o > gkey) || (o == gkey && h < lane);
-    }
-    const unsigned kept = __ballot_sync(0xffffffffu, lane < G && beaten < Gk);
-    // candidates: experts of kept groups, as keys (0: none; a real key is never 0)
-    unsigned ck[kMaxE / 32];
+        for (int q = 0; q < NT; ++q) {
+            unsigned m = 0u;
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) ck[i] = (gid[i] >= 0 && ((kept >> gid[i]) & 1u)) ? float_key(lg[i]) : 0u;
-    float lsel = 0.f;  // lane j < k: logit of the j-th choice
-    for (int j = 0; j < k; ++j) {
-        unsigned bk = 0u;
-#pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i) bk = max(bk, ck[i]);
-        const unsigned top = __reduce_max_sync(0xffffffffu, bk);
-        unsigned be = 0xffffffffu;  // this lane's lowest expert holding the top key
-#pragma unroll
-        for (int i = kMaxE / 32 - 1; i >= 0; --i)
-            if (ck[i] == top) be = (unsigned)(lane + 32 * i);
-        be = __reduce_min_sync(0xffffffffu, be);
-#pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i)
-            if ((unsigned)(lane + 32 * i) == be) ck[i] = 0u;  // the owner removes the winner
-        const int owner = (int)(be & 31u), slot = (int)(be >> 5);
-        float lw = 0.f;
-#pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i)
-            if (i == slot) lw = lg[i];
-        lw = __shfl_sync(0xffffffffu, lw, owner);
-        if (lane == j) lsel = lw;
-        if (lane == 0) {
-            ids_out[j] = (int)be;
-            if (ids_smem) ids_smem[j] = (int)be;
+            for (int i = 0; i < kMaxE / 32; ++i)
+                if (gid[i] == gi) m = max(m, float_key(lg[q][i]));
+            m = __reduce_max_sync(0xffffffffu, m);
+            if (lane == gi) gkey[q] = m;
         }
     }
-    float z = 0.f;
+    int beaten[NT];
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) z += (lane + 32 * i < E) ? expf(lg[i] - mx) : 0.f;
-    z = warp_sum(z);
-    if (lane < k) w_out[lane] = expf(lsel - mx) / z * scale;
+    for (int q = 0; q < NT; ++q) beaten[q] = 0;
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const unsigned o = __shfl_sync(0xffffffffu, gkey[q], h);
+            beaten[q] += (o > gkey[q]) || (o == gkey[q] && h < lane);
+        }
+    }
+    // candidates: experts of kept groups, as keys (0: none; a real key is never 0)
+    unsigned ck[NT][kMaxE / 32];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        const unsigned kept = __ballot_sync(0xffffffffu, lane < G && beaten[q] < Gk);
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i)
+            ck[q][i] = (gid[i] >= 0 && ((kept >> gid[i]) & 1u)) ? float_key(lg[q][i]) : 0u;
+    }
+    float lsel[NT];  // lane j < k: logit of the j-th choice
+#pragma unroll
+    for (int q = 0; q < NT; ++q) lsel[q] = 0.f;
+    for (int j = 0; j < k; ++j) {
+        unsigned top[NT], be[NT];
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            unsigned bk = 0u;
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i) bk = max(bk, ck[q][i]);
+            top[q] = __reduce_max_sync(0xffffffffu, bk);
+        }
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            be[q] = 0xffffffffu;  // this lane's lowest expert holding the top key
+#pragma unroll
+            for (int i = kMaxE / 32 - 1; i >= 0; --i)
+                if (ck[q][i] == top[q]) be[q] = (unsigned)(lane + 32 * i);
+            be[q] = __reduce_min_sync(0xffffffffu, be[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i)
+                if ((unsigned)(lane + 32 * i) == be[q]) ck[q][i] = 0u;  // the owner removes the winner
+            const int owner = (int)(be[q] & 31u), slot = (int)(be[q] >> 5);
+            float lw = 0.f;
+#pragma unroll
+            for (int i = 0; i < kMaxE / 32; ++i)
+                if (i == slot) lw = lg[q][i];
+            lw = __shfl_sync(0xffffffffu, lw, owner);
+            if (lane == j) lsel[q] = lw;
+            if (lane == 0) {
+                if (ids_out[q]) ids_out[q][j] = (int)be[q];
+                if (ids_smem[q]) ids_smem[q][j] = (int)be[q];
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        float z = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i) z += (lane + 32 * i < E) ? expf(lg[q][i] - mx[q]) : 0.f;
+        z = warp_sum(z);
+        if (lane < k && w_out[q]) w_out[q][lane] = expf(lsel[q] - mx[q]) / z * scale;
+    }
     __syncwarp();
+}
+
+__device__ inline void topk_warp(const float (&lg)[kMaxE / 32], int E, int G, int Gk, int k, float scale,
+                                 float* scratch, int32_t* ids_out, float* w_out, int32_t* ids_smem) {
+    (void)scratch;
+    const float(&l1)[1][kMaxE / 32] = *reinterpret_cast<const float(*)[1][kMaxE / 32]>(&lg);
+    int32_t* const io[1] = {ids_out};
+    float* const wo[1] = {w_out};
+    int32_t* const so[1] = {ids_smem};
+    topk_warp_n<1>(l1, E, G, Gk, k, scale, io, wo, so);
 }
 
 // Inverse of float_key.
