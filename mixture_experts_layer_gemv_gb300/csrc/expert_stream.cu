@@ -490,19 +490,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
 
-    // The routing data come from the router, which completed before the gate/up kernel
-    // (this kernel's predecessor) got past its own wait; down weights depend on nothing
-    // else, so the tile table is built and the producer streams weights before the
-    // gate/up results exist (load_route and local_route read through L2 and end with
-    // __syncthreads).
-    RouteView rv;
-    if constexpr (kLocal) {
-        __shared__ LocalRouteSmem s_local;
-        rv = local_route(&s_route, &s_local, a, false, true, tid, kThreads);
-    } else {
-        rv = load_route(&s_route, a.ctrl, a.groups, a.max_groups, a.perm_src, a.topk_w, a.T * a.k, a.E, a.status,
-                        tid, kThreads);
-    }
+    // The routing data come from the router kernels, which completed before the gate/up
+    // kernel (this kernel's predecessor) got past its own wait; down weights depend on
+    // nothing else, so the tile table is built and the producer streams weights before
+    // the gate/up results exist (load_route reads through L2 and ends with
+    // __syncthreads). With routing inside the streaming kernels (up to 8 tokens) gate/up
+    // CTA 0 published it: it is read after the wait (deriving it again here from the
+    // logits took ~4 us per CTA, and these CTAs start only as gate/up CTAs retire).
+    if constexpr (kLocal) pdl_wait();
+    const RouteView rv = load_route(&s_route, a.ctrl, a.groups, a.max_groups, a.perm_src, a.topk_w, a.T * a.k, a.E,
+                                    a.status, tid, kThreads);
     const Plan pl = down_plan<Ix>(a, rv.n_groups);
     const Plan pl_gu = gateup_plan<Ix>(a, rv.n_groups);  // the K parts of the gate/up partials
     const TileSpace<Ix> ts = down_space<Ix>(a, rv.n_groups, pl.P);
@@ -708,7 +705,7 @@ __global__ void __launch_bounds__(256) stream_combine_kernel(const StreamArgs a)
 size_t smem_gateup() { return (size_t)kStagesGU * (2 * kBox + kBRows) + 2 * kStagesGU * 8 + 1024; }
 // Static shared memory of the down kernel beside its dynamic ring and operand: the tile
 // table, the routing copies and small scalars.
-constexpr long kDownStaticSmem = (long)kTabBytes + (long)sizeof(RouteSmem) + (long)sizeof(LocalRouteSmem) + 256;
+constexpr long kDownStaticSmem = (long)kTabBytes + (long)sizeof(RouteSmem) + 256;
 // Down-kernel ring depth: as many 16 KB stages (up to 10) as fit beside the FP8 operand.
 int stages_down(int Nmax) {
     const long operand = (long)kGroupRows * (Nmax + 16) + (long)kGroupRows * (Nmax / kBlk) * 4;
