@@ -15,10 +15,10 @@
 // The forward's g and u are recomputed by the grouped tcgen05 FP8 GEMM (mode 2, same
 // tiles and arithmetic as the forward, so ahat is bit-identical to what the forward's
 // down GEMM consumed). The contractions of the backward run in bf16 with fp32
-// accumulation on the mma.sync tensor path: one grouped GEMM kernel, specialised per
-// operand access pattern, with the FP8 weights and activations decoded to bf16 (exact
-// for activations, one bf16 rounding for weight x block scale) while they are staged
-// in shared memory.
+// accumulation on the tcgen05 tensor cores (bwd_tc.cu), on operands prepared here: the
+// FP8 weights decoded to bf16 and transposed so that K is contiguous (one bf16 rounding
+// of weight x block scale), the activations decoded exactly, rows gathered into expert
+// order, and the transposed operands of the weight gradients.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -49,207 +49,6 @@ __device__ __forceinline__ void e4m3x16_to_bf16(uint4 q, float s, uint4& lo, uin
     }
     lo = make_uint4(o[0], o[1], o[2], o[3]);
     hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-constexpr int kBM = 128, kBN = 128, kBK = 32;
-constexpr int kStages = 4;
-constexpr int kAPitch = kBK + 8;   // bf16 per A row, [m][k] layout (k contiguous)
-constexpr int kTPitch = kBN + 8;   // bf16 per row of the [k][m] and [k][n] layouts
-constexpr int kGThr = 256;         // 8 warps: 2 along M (64 rows) x 4 along N (32 columns)
-constexpr int kAStage = kBM * kAPitch;  // bf16 per A stage (the larger of the two layouts)
-constexpr int kBStage = kBK * kTPitch;
-static_assert(kAStage >= kBK * kTPitch, "an A stage holds either layout");
-constexpr size_t kGemmSmem = (size_t)kStages * (kAStage + kBStage) * 2;
-
-// A bf16 GEMM over row-major operands, per group: C[m, n] = sum_k A(m, k) B(k, n).
-// A is [rows][lda] with k contiguous (dgrad: rows are the output rows) or, with
-// kACols, [k rows][lda] with m contiguous (wgrad: the K index runs over token rows);
-// B is [k][ldb] with n contiguous, its rows >= ksplit taken from B2 (two stacked
-// matrices). Groups: one (grouping 0), the permutation's 128-row tiles of an expert
-// (1: rows row0.., B of that expert), or one expert's K range of rows (2: C of that
-// expert).
-struct Gemm {
-    int M, N, K;
-    int grouping;
-    const MTile* mtiles;
-    const Ctrl* ctrl;
-    const int32_t* offsets;
-    const __nv_bfloat16* A;
-    long lda;
-    const __nv_bfloat16 *B, *B2;
-    int ksplit;
-    long ldb;
-    size_t b_estride;
-    float *C, *C2;  // output rows m >= msplit go to C2 (row m - msplit)
-    int msplit;
-    long ldc;
-    size_t c_estride;
-};
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
-                 "r"(pred ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// One 128 x 128 output tile: a kStages-deep ring of cp.async copies (16 bytes each, out of
-// range chunks zero-filled) and ldmatrix fragments (.trans for the [k][*] layouts).
-template <bool kACols>
-__global__ void __launch_bounds__(kGThr) bwd_gemm_kernel(const Gemm p) {
-    extern __shared__ __align__(16) uint8_t smem_g[];
-    __nv_bfloat16* As = reinterpret_cast<__nv_bfloat16*>(smem_g);
-    __nv_bfloat16* Bs = As + kStages * kAStage;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    int e = 0, m0, mv, n0, kbase = 0, kv = p.K, rowbase;
-    if (kACols) {  // wgrad: N tiles on x, M tiles on y, the group on z
-        n0 = blockIdx.x * kBN;
-        m0 = blockIdx.y * kBM;
-        mv = min(kBM, p.M - m0);
-        rowbase = 0;
-        if (p.grouping == 2) {
-            e = blockIdx.z;
-            kbase = p.offsets[e];
-            kv = p.offsets[e + 1] - kbase;
-        }
-    } else {
-        n0 = blockIdx.y * kBN;
-        if (p.grouping == 1) {
-            if ((int)blockIdx.x >= p.ctrl->n_mtiles) return;
-            const MTile t = p.mtiles[blockIdx.x];
-            e = t.expert;
-            m0 = 0;
-            mv = t.nrows;
-            rowbase = t.row0;
-        } else {
-            m0 = blockIdx.x * kBM;
-            mv = min(kBM, p.M - m0);
-            rowbase = m0;
-        }
-    }
-    if (mv <= 0 || n0 >= p.N) return;
-    const __nv_bfloat16* Bm = p.B + (size_t)e * p.b_estride;
-    const __nv_bfloat16* Bm2 = p.B2 ? p.B2 + (size_t)e * p.b_estride : nullptr;
-
-    auto load_stage = [&](int slot, int kt) {
-        const int kb = kt * kBK;
-        __nv_bfloat16* as = As + slot * kAStage;
-        __nv_bfloat16* bs = Bs + slot * kBStage;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int c = tid + kGThr * q;
-            if (!kACols) {  // 128 rows x 4 chunks of 8 k
-                const int m = c >> 2, kc = (c & 3) * 8;
-                const bool ok = m < mv && kb + kc < kv;
-                const __nv_bfloat16* src = ok ? p.A + (size_t)(rowbase + m) * p.lda + kb + kc : p.A;
-                cp_async16(as + m * kAPitch + kc, src, ok);
-            } else {        // 32 k rows x 16 chunks of 8 m
-                const int kk = c >> 4, mc = (c & 15) * 8;
-                const bool ok = kb + kk < kv && m0 + mc < p.M;
-                const __nv_bfloat16* src = ok ? p.A + (size_t)(kbase + kb + kk) * p.lda + m0 + mc : p.A;
-                cp_async16(as + kk * kTPitch + mc, src, ok);
-            }
-            {  // B: 32 k rows x 16 chunks of 8 n
-                const int kk = c >> 4, nc = (c & 15) * 8;
-                const int kr = kb + kk;
-                const bool ok = kr < kv && n0 + nc < p.N;
-                const bool second = Bm2 && kr >= p.ksplit;
-                const __nv_bfloat16* src =
-                    ok ? (second ? Bm2 + (size_t)(kbase + kr - p.ksplit) * p.ldb : Bm + (size_t)(kbase + kr) * p.ldb) +
-                             n0 + nc
-                       : p.B;
-                cp_async16(bs + kk * kTPitch + nc, src, ok);
-            }
-        }
-    };
-
-    float acc[4][4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
-    const int wm = warp & 1, wn = warp >> 1;
-    const int nk = (kv + kBK - 1) / kBK;
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (s < nk) load_stage(s, s);
-        cp_async_commit();
-    }
-    for (int kt = 0; kt < nk; ++kt) {
-        cp_async_wait<kStages - 2>();  // stage kt has landed (this thread's copies)
-        __syncthreads();               // ... and everyone's; stage kt-1 is free again
-        const int nxt = kt + kStages - 1;
-        if (nxt < nk) load_stage(nxt % kStages, nxt);
-        cp_async_commit();
-        const __nv_bfloat16* as = As + (kt % kStages) * kAStage;
-        const __nv_bfloat16* bs = Bs + (kt % kStages) * kBStage;
-#pragma unroll
-        for (int ks = 0; ks < kBK; ks += 16) {
-            uint32_t af[4][4], bf[2][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (kACols)  // matrices (m 0-7 | 8-15) x (k 0-7 | 8-15) from rows k of [k][m]
-                    ldsm_x4_t(af[i], as + (ks + (lane & 7) + ((lane >> 4) & 1) * 8) * kTPitch + wm * 64 + i * 16 +
-                                         ((lane >> 3) & 1) * 8);
-                else
-                    ldsm_x4(af[i], as + (wm * 64 + i * 16 + (lane & 15)) * kAPitch + ks + (lane >> 4) * 8);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-                ldsm_x4_t(bf[j], bs + (ks + (lane & 15)) * kTPitch + wn * 32 + j * 16 + (lane >> 4) * 8);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mma_bf16(acc[i][j], af[i], bf[j >> 1][2 * (j & 1)], bf[j >> 1][2 * (j & 1) + 1]);
-        }
-    }
-    cp_async_wait<0>();
-
-    // ---- epilogue: fp32 rows of C
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int m = wm * 64 + i * 16 + (lane >> 2) + 8 * h;
-            if (m >= mv) continue;
-            float* crow;
-            if (!kACols) {
-                crow = p.C + (size_t)(rowbase + m) * p.ldc;
-            } else {
-                const int mm = m0 + m;
-                crow = (p.C2 && mm >= p.msplit) ? p.C2 + (size_t)e * p.c_estride + (size_t)(mm - p.msplit) * p.ldc
-                                                : p.C + (size_t)e * p.c_estride + (size_t)mm * p.ldc;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int n = n0 + wn * 32 + j * 8 + (lane & 3) * 2;
-                if (n < p.N) *reinterpret_cast<float2*>(crow + n) = make_float2(acc[i][j][2 * h], acc[i][j][2 * h + 1]);
-            }
-        }
 }
 
 // ---------------------------------------------------------------- operand preparation
@@ -373,11 +172,17 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const __nv_bfloat16* s
     for (int c = lane; c < H / 8; c += 32) d4[c] = good ? __ldg(s4 + c) : make_uint4(0, 0, 0, 0);
 }
 
-__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* src, long n, __nv_bfloat16* dst) {
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n / 2; i += (long)gridDim.x * blockDim.x) {
-        const float2 v = reinterpret_cast<const float2*>(src)[i];
-        reinterpret_cast<uint32_t*>(dst)[i] = pack_bf16x2(v.x, v.y);
-    }
+// dst [C, R] bf16 = src [R, C] fp32 transposed (the router weights as the K-contiguous
+// operand of dx's router term: K = E), 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) f32_to_bf16_t_kernel(const float* src, int R, int C, __nv_bfloat16* dst) {
+    __shared__ float tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int i = ty; i < 32; i += 8)
+        if (r0 + i < R && c0 + tx < C) tile[i][tx] = src[(size_t)(r0 + i) * C + c0 + tx];
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8)
+        if (c0 + i < C && r0 + tx < R) dst[(size_t)(c0 + i) * R + r0 + tx] = __float2bfloat16_rn(tile[tx][i]);
 }
 
 // SwiGLU backward and the quantised intermediate, one warp per row (routed rows or
@@ -552,20 +357,6 @@ __global__ void __launch_bounds__(256) dx_combine_kernel(int T, int H, int k, co
     *reinterpret_cast<float4*>(dx + (size_t)t * H + h) = acc;
 }
 
-template <bool kACols>
-cudaError_t run_gemm(const Gemm& p, dim3 grid, cudaStream_t st) {
-    if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[kACols]) {
-        const cudaError_t e = cudaFuncSetAttribute((const void*)bwd_gemm_kernel<kACols>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-        if (e != cudaSuccess) return e;
-        attr_set[kACols] = true;
-    }
-    bwd_gemm_kernel<kACols><<<grid, kGThr, kGemmSmem, st>>>(p);
-    return cudaGetLastError();
-}
-
 unsigned cdiv(long a, long b) { return (unsigned)((a + b - 1) / b); }
 unsigned grid_for(long n, int per_thread) { return (unsigned)std::min<long>(4096, std::max<long>(1, cdiv(n / per_thread, 256))); }
 
@@ -672,7 +463,7 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
     // ---- forward quantities: activation codes, the router's logits, the permutation, g and u
     BWD_TRY(launch_quant_act(a.x, T, H, xq, xs, NormArgs{}, st));
     BWD_TRY(launch_route_large(c, a.x, T, a.W->w_router, a.W->router_bias, reinterpret_cast<int32_t*>(at(L.ids)),
-                               f32(L.w), f32(L.logits), L.splits, NormArgs{}, reinterpret_cast<uint16_t*>(at(L.router_w3)),
+                               f32(L.w), f32(L.logits), L.splits, reinterpret_cast<uint16_t*>(at(L.router_w3)),
                                &ctrl->status, st));
     BWD_TRY(launch_permute(c, a.topk_ids, T, reinterpret_cast<int32_t*>(at(L.offsets)), perm_src, inv_pos, nullptr,
                            nullptr, mtiles, reinterpret_cast<int32_t*>(at(L.perm_hist)), ctrl, st));
@@ -727,18 +518,13 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
         dequant_t_kernel<<<dim3(H / 64, Is / 64, 1), 256, 0, st>>>(a.W->ws_up, a.W->ss_up, Is, H, 2 * Is, Is,
                                                                  bf(L.wsguT));
     }
-    f32_to_bf16_kernel<<<grid_for((long)E * H, 2), 256, 0, st>>>(a.W->w_router, (long)E * H, bf(L.wr_bf));
+    f32_to_bf16_t_kernel<<<dim3(cdiv(H, 32), cdiv(E, 32)), 256, 0, st>>>(a.W->w_router, E, H, bf(L.wr_bf));
     xhat_kernel<<<grid_for((long)T * H, 16), 256, 0, st>>>(xq, xs, T, H, bf(L.xhat));
     gather_bf16_kernel<<<cdiv(R, 8), 256, 0, st>>>(bf(L.xhat), H, perm_src, k, R, bf(L.xhat_perm));
     gather_bf16_kernel<<<cdiv(R, 8), 256, 0, st>>>(dout, H, perm_src, k, R, bf(L.dout_perm));
     BWD_TRY(cudaGetLastError());
     BWD_TRY(mark(MOE_STAGE_ROUTE, false));
     BWD_TRY(mark(MOE_STAGE_PERMUTE, true));
-
-    Gemm b = {};
-    b.mtiles = mtiles;
-    b.ctrl = ctrl;
-    b.offsets = reinterpret_cast<int32_t*>(at(L.offsets));
 
     // ---- dau = Wd^T dout: routed rows (tiles of the permutation), then the shared experts
     BWD_TRY(launch_bwd_tc(bf(L.dout_perm), (uint64_t)R, bf(L.wdT), (uint64_t)E, H, I, 1, 0, mtiles, ctrl,
@@ -800,18 +586,9 @@ cudaError_t launch_backward(const moe_config_t& c, const BwdArgs& a, void* ws, c
     // ---- dx: router term, then the routed rows and the shared experts, then their sum
     {
         BWD_TRY(mark(MOE_STAGE_COMBINE, true));
-        Gemm x = b;
-        x.grouping = 0;
-        x.M = T;
-        x.N = H;
-        x.K = E;
-        x.A = bf(L.dlogit_bf);
-        x.lda = E;
-        x.B = bf(L.wr_bf);
-        x.ldb = H;
-        x.C = a.dx;
-        x.ldc = H;
-        BWD_TRY(run_gemm<false>(x, dim3(cdiv(T, kBM), cdiv(H, kBN)), st));
+        // dx = dlogit [T, E] . Wr: K = E in 64-wide steps (columns past E read as zeros)
+        BWD_TRY(launch_bwd_tc_wgrad(bf(L.dlogit_bf), T, bf(L.wr_bf), H, (uint64_t)E, nullptr, 1, (E + 63) / 64 * 64,
+                                    a.dx, nullptr, 0, 0, &ctrl->status, st));
         BWD_TRY(launch_bwd_tc(bf(L.dgu_r), (uint64_t)R, bf(L.wguT), (uint64_t)E, 2 * I, H, 1, 0, mtiles, ctrl,
                               f32(L.dx_perm), &ctrl->status, st));
         if (sh)

@@ -630,12 +630,14 @@ static moe_status_t route_impl(const moe_config_t* cfg, const void* x_bf16, int3
                                     at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), nullptr, nullptr, nullptr, nullptr,
                                     nullptr, at<Ctrl>(ws, L.ctrl), nm, st));
     } else {
-        if (nm.gamma) {
+        const void* xr = x_bf16;
+        if (nm.gamma) {  // the normalised rows, in the y_perm region (free until the expert GEMMs)
             nm.rstd = at<float>(ws, L.rstd);
-            MOE_CUDA(launch_rmsnorm(x_bf16, T, cfg->hidden, nm, nullptr, st));
+            MOE_CUDA(launch_rmsnorm(x_bf16, T, cfg->hidden, nm, at<uint16_t>(ws, L.y_perm), st));
+            xr = at<uint16_t>(ws, L.y_perm);
         }
-        MOE_CUDA(launch_route_large(*cfg, x_bf16, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
-                                    L.router_splits, nm, at<uint16_t>(ws, L.router_w3), &at<Ctrl>(ws, L.ctrl)->status,
+        MOE_CUDA(launch_route_large(*cfg, xr, T, w_router, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
+                                    L.router_splits, at<uint16_t>(ws, L.router_w3), &at<Ctrl>(ws, L.ctrl)->status,
                                     st));
     }
     return MOE_OK;
@@ -759,12 +761,14 @@ static moe_status_t forward_impl(const moe_config_t* cfg, const void* x_bf16, in
                                     at<int32_t>(ws, L.group_of_row), ctrl, nm, st, nullptr, trace, !local));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
     } else {
-        if (nm.gamma) {
+        const void* xr = x_bf16;
+        if (nm.gamma) {  // the normalised rows, in the y_perm region (free until the expert GEMMs)
             nm.rstd = at<float>(ws, L.rstd);
-            MOE_CUDA(launch_rmsnorm(x_bf16, T, cfg->hidden, nm, nullptr, st));
+            MOE_CUDA(launch_rmsnorm(x_bf16, T, cfg->hidden, nm, at<uint16_t>(ws, L.y_perm), st));
+            xr = at<uint16_t>(ws, L.y_perm);
         }
-        MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
-                                    at<float>(ws, L.logits), L.router_splits, nm, at<uint16_t>(ws, L.router_w3),
+        MOE_CUDA(launch_route_large(*cfg, xr, T, weights->w_router, weights->router_bias, ids, w,
+                                    at<float>(ws, L.logits), L.router_splits, at<uint16_t>(ws, L.router_w3),
                                     &ctrl->status, st));
         MOE_CUDA(launch_quant_act(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<float>(ws, L.xs), nm, st));
         MOE_TRY(mark.end(MOE_STAGE_ROUTE));
@@ -923,7 +927,7 @@ moe_status_t moe_forward_mx_profiled(const moe_config_t* cfg, const void* x_bf16
         return MOE_OK;
     }
     MOE_CUDA(launch_route_large(*cfg, x_bf16, T, weights->w_router, weights->router_bias, ids, w,
-                                at<float>(ws, L.logits), L.router_splits, NormArgs{}, at<uint16_t>(ws, L.router_w3),
+                                at<float>(ws, L.logits), L.router_splits, at<uint16_t>(ws, L.router_w3),
                                 &ctrl->status, st));
     MOE_CUDA(launch_quant_act_mx(x_bf16, T, cfg->hidden, at<uint8_t>(ws, L.xq), at<uint8_t>(ws, L.xs8), NormArgs{},
                                  st));

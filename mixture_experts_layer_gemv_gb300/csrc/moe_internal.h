@@ -121,13 +121,12 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
                                const NormArgs& nm, cudaStream_t st, uint8_t* xs8 = nullptr,
                                uint64_t* trace = nullptr, bool tail = true);
 
-// Large-T route: router GEMM (split-K partials) + softmax/top-k per token. Without
-// stage M the GEMM runs on tcgen05 and w3 (router_w3_bytes) receives the weights'
-// three-way bf16 split; with nm.gamma the router applies stage M on the fly (nm.rstd
-// from launch_rmsnorm) on mma.sync and w3 is not used. logits: [splits, T, E] fp32.
+// Large-T route: router GEMM on tcgen05 (split-K partials) + softmax/top-k per token;
+// w3 (router_w3_bytes) receives the weights' three-way bf16 split. With stage M the
+// caller passes the normalised rows (launch_rmsnorm's x_out). logits: [splits, T, E] fp32.
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, int splits,
-                               const NormArgs& nm, uint16_t* w3, int* status, cudaStream_t st);
+                               uint16_t* w3, int* status, cudaStream_t st);
 // bytes of the three-way split router weights: bf16 [3][E rounded up to 16][H]
 inline size_t router_w3_bytes(const moe_config_t& c) {
     return (size_t)3 * ((c.n_routed + 15) & ~15) * c.hidden * 2;

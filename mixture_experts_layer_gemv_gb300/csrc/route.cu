@@ -236,40 +236,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32, kNorm ? 1 : 2) route_small_k
 }
 
 // ---------------------------------------------------------------- large T
-// ---- large T with stage M in front: router GEMM on mma.sync. x is normalised while it
-// is staged (the normalised rows exist nowhere else) and is then exact in bf16; each
-// fp32 router weight is split as w = hi + mid + lo, three bf16 values (|w - hi - mid -
-// lo| <= 2^-27 |w|, the precision of the fp32 weight itself), and the three products go
-// through mma.m16n8k16 (bf16 x bf16, fp32 accumulation). A CTA takes 64 tokens x all
-// experts over a range of K (split-K partials, summed in fixed order by topk_kernel),
-// in 64-wide K steps: the next step's x and router values are loaded into registers
-// while the current step's MMAs run. Without stage M the router runs on tcgen05
-// (router_tc_kernel below).
-constexpr int kRM = 64;      // token rows per CTA
-constexpr int kRK = 64;      // K per step
-constexpr int kRPitch = 72;  // bf16 per shared-memory row: 64 + 8 (rows in distinct banks)
-
-struct RouterMmaParams {
-    int H, E, Ep, T, k_per_split;
-    const uint16_t* x;
-    const float* wr;
-    float* part;            // [splits, T, E]
-    const uint16_t* gamma;  // stage M applied to x (with rstd [T])
-    const float* rstd;
-};
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
-
-// w -> (hi, mid, lo), each the bf16 rounding of what the previous parts leave
+// w -> (hi, mid, lo), each the bf16 rounding of what the previous parts leave:
+// |w - hi - mid - lo| <= 2^-27 |w|, the precision of the fp32 weight itself, so that with
+// x exact in bf16 the three bf16 products reproduce the fp32 router GEMM.
 __device__ __forceinline__ void split3(float w, uint16_t& hi, uint16_t& mid, uint16_t& lo) {
     const __nv_bfloat16 h = __float2bfloat16_rn(w);
     const float r1 = w - __bfloat162float(h);
@@ -278,117 +247,6 @@ __device__ __forceinline__ void split3(float w, uint16_t& hi, uint16_t& mid, uin
     hi = __bfloat16_as_ushort(h);
     mid = __bfloat16_as_ushort(m);
     lo = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
-}
-
-template <int NTW>  // 8-wide expert tiles per warp: Ep = 16 * NTW
-__global__ void __launch_bounds__(256) router_mma_kernel(RouterMmaParams p) {
-    extern __shared__ uint4 smem_r[];
-    uint16_t* sx = reinterpret_cast<uint16_t*>(smem_r);  // [64][kRPitch]
-    uint16_t* sw = sx + kRM * kRPitch;                    // [3][Ep][kRPitch]: hi, mid, lo
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    const int m0 = blockIdx.x * kRM;
-    const int k0 = blockIdx.y * p.k_per_split, k1 = min(p.H, k0 + p.k_per_split);
-    const int mt = warp & 3, nh = warp >> 2;  // 16-row tile, half of the experts
-    constexpr int nw4 = NTW;                  // router float4 per thread per step: Ep * 16 / 256
-    const size_t wplane = (size_t)p.Ep * kRPitch;
-    float acc[NTW][4];
-#pragma unroll
-    for (int j = 0; j < NTW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-    uint4 xr[2];       // x tile: 64 rows x 64 bf16 = 512 uint4, 2 per thread
-    uint4 gx[2];       // gamma of those columns (stage M)
-    float rs[2];       // 1/rms of those rows
-    float4 wv[nw4];    // router tile: Ep rows x 64 fp32
-    constexpr bool norm = true;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const int t = m0 + ((tid + 256 * q) >> 3);
-        rs[q] = norm && t < p.T ? p.rstd[t] : 0.f;
-    }
-    auto load = [&](int kk) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int i = tid + 256 * q, r = i >> 3, c = i & 7, t = m0 + r;
-            xr[q] = t < p.T ? __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H + kk) + c)
-                            : make_uint4(0, 0, 0, 0);
-            if (norm) gx[q] = __ldg(reinterpret_cast<const uint4*>(p.gamma + kk) + c);
-        }
-#pragma unroll
-        for (int q = 0; q < nw4; ++q) {
-            const int i = tid + 256 * q, e = i >> 4, c = i & 15;
-            wv[q] = e < p.E ? __ldg(reinterpret_cast<const float4*>(p.wr + (size_t)e * p.H + kk) + c)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    auto store = [&]() {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int i = tid + 256 * q, r = i >> 3, c = i & 7;
-            *reinterpret_cast<uint4*>(sx + r * kRPitch + c * 8) = norm ? rms_apply8(xr[q], rs[q], gx[q]) : xr[q];
-        }
-#pragma unroll
-        for (int q = 0; q < nw4; ++q) {
-            const int i = tid + 256 * q, e = i >> 4, c = i & 15;
-            const float w4[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
-            uint16_t h[4], m[4], l[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) split3(w4[u], h[u], m[u], l[u]);
-            uint16_t* d = sw + e * kRPitch + c * 4;
-            *reinterpret_cast<uint2*>(d) = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
-            *reinterpret_cast<uint2*>(d + wplane) =
-                make_uint2(m[0] | ((uint32_t)m[1] << 16), m[2] | ((uint32_t)m[3] << 16));
-            *reinterpret_cast<uint2*>(d + 2 * wplane) =
-                make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
-        }
-    };
-
-    if (k0 < k1) load(k0);
-    for (int kk = k0; kk < k1; kk += kRK) {
-        store();
-        __syncthreads();
-        if (kk + kRK < k1) load(kk + kRK);  // in flight during this step's MMAs
-        // The tensor core aligns the products of one MMA to its accumulator's exponent and
-        // truncates, so each K step accumulates in a fresh (small) register block that is
-        // then added to the running sum with an ordinary fp32 add.
-        uint32_t af[kRK / 16][4];
-#pragma unroll
-        for (int k16 = 0; k16 < kRK / 16; ++k16) {
-            const uint16_t* ar = sx + (mt * 16 + g) * kRPitch + k16 * 16 + 2 * t4;
-            af[k16][0] = lds32(ar);
-            af[k16][1] = lds32(ar + 8 * kRPitch);
-            af[k16][2] = lds32(ar + 8);
-            af[k16][3] = lds32(ar + 8 * kRPitch + 8);
-        }
-        float d[NTW][4];
-#pragma unroll
-        for (int j = 0; j < NTW; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-#pragma unroll
-        for (int k16 = 0; k16 < kRK / 16; ++k16)
-#pragma unroll
-            for (int part = 2; part >= 0; --part)  // small parts first
-#pragma unroll
-                for (int j = 0; j < NTW; ++j) {  // independent accumulators interleave
-                    const uint16_t* b = sw + part * wplane + ((nh * NTW + j) * 8 + g) * kRPitch + k16 * 16 + 2 * t4;
-                    mma_bf16_16816(d[j], af[k16][0], af[k16][1], af[k16][2], af[k16][3], lds32(b), lds32(b + 8));
-                }
-#pragma unroll
-        for (int j = 0; j < NTW; ++j)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[j][q] += d[j][q];
-        __syncthreads();
-    }
-    float* out = p.part + (size_t)blockIdx.y * p.T * p.E;
-#pragma unroll
-    for (int j = 0; j < NTW; ++j) {
-        const int e0 = (nh * NTW + j) * 8 + 2 * t4;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int t = m0 + mt * 16 + g + 8 * h;
-            if (t >= p.T) continue;
-            if (e0 < p.E) out[(size_t)t * p.E + e0] = acc[j][2 * h];
-            if (e0 + 1 < p.E) out[(size_t)t * p.E + e0 + 1] = acc[j][2 * h + 1];
-        }
-    }
 }
 
 // ---- large T: router GEMM on the tcgen05 tensor cores (kind::f16, fp32 in tensor memory).
@@ -851,105 +709,62 @@ cudaError_t launch_route_small(const moe_config_t& c, const void* x, int T, cons
 
 cudaError_t launch_route_large(const moe_config_t& c, const void* x, int T, const float* w_router,
                                const float* bias, int32_t* ids, float* w, float* logits, int splits,
-                               const NormArgs& nm, uint16_t* w3, int* status, cudaStream_t st) {
+                               uint16_t* w3, int* status, cudaStream_t st) {
     const int H = c.hidden, E = c.n_routed, Ep = (E + 15) & ~15;
     const int Hb = H / kBlk;
     const int k_per_split = ((Hb + splits - 1) / splits) * kBlk;
     cudaError_t e2 = cudaErrorInvalidValue;
-    if (!nm.gamma) {
-        // tcgen05 path: split the router weights, then the GEMM
-        if (!w3) return cudaErrorInvalidValue;
-        {
-            const size_t n4 = (size_t)Ep * H / 4;
-            const unsigned blocks = (unsigned)std::min<size_t>(1024, (n4 + 255) / 256);
-            router_split_kernel<<<blocks, 256, 0, st>>>(w_router, E, Ep, H, w3);
-            const cudaError_t e = cudaGetLastError();
-            if (e != cudaSuccess) return e;
-        }
-        TmaMap tx, tw;
-        if (!tmap_bf16_2d(&tx, x, (uint64_t)T, (uint64_t)H, kRTK, kRTM) ||
-            !tmap_bf16_2d(&tw, w3, (uint64_t)3 * Ep, (uint64_t)H, kRTK, (uint32_t)Ep))
-            return cudaErrorInvalidValue;
-        RouterTcParams p;
-        p.T = T;
-        p.E = E;
-        p.Ep = Ep;
-        p.H = H;
-        p.k_per_split = k_per_split;
-        p.n_mt = (T + kRTM - 1) / kRTM;
-        p.part = logits;
-        p.status = status;
-        const size_t stage = (size_t)kRTSA + 3 * (size_t)Ep * kRTK * 2;
-        const size_t room = 227 * 1024 - 1024 - 256;
-        p.stages = (int)std::min<size_t>(4, room / stage);
-        if (p.stages < 2) return cudaErrorInvalidValue;
-        const size_t smem = 1024 + (size_t)p.stages * stage + 256;
-        auto run = [&](auto kern) -> cudaError_t {
-            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            kern<<<p.n_mt * splits, kRTThreads, smem, st>>>(p, tx, tw);
-            return cudaGetLastError();
-        };
-        auto pick = [&](auto nch) -> cudaError_t { return run(router_tc_kernel<decltype(nch)::value>); };
-        switch (Ep / 16) {  // n_routed <= 256
-            case 1: e2 = pick(std::integral_constant<int, 1>{}); break;
-            case 2: e2 = pick(std::integral_constant<int, 2>{}); break;
-            case 3: e2 = pick(std::integral_constant<int, 3>{}); break;
-            case 4: e2 = pick(std::integral_constant<int, 4>{}); break;
-            case 5: e2 = pick(std::integral_constant<int, 5>{}); break;
-            case 6: e2 = pick(std::integral_constant<int, 6>{}); break;
-            case 7: e2 = pick(std::integral_constant<int, 7>{}); break;
-            case 8: e2 = pick(std::integral_constant<int, 8>{}); break;
-            case 9: e2 = pick(std::integral_constant<int, 9>{}); break;
-            case 10: e2 = pick(std::integral_constant<int, 10>{}); break;
-            case 11: e2 = pick(std::integral_constant<int, 11>{}); break;
-            case 12: e2 = pick(std::integral_constant<int, 12>{}); break;
-            case 13: e2 = pick(std::integral_constant<int, 13>{}); break;
-            case 14: e2 = pick(std::integral_constant<int, 14>{}); break;
-            case 15: e2 = pick(std::integral_constant<int, 15>{}); break;
-            case 16: e2 = pick(std::integral_constant<int, 16>{}); break;
-        }
-    } else {
-        // stage M in front: the normalised x exists only in registers, so the router
-        // applies it while staging x in shared memory (mma.sync path)
-        RouterMmaParams g;
-        g.H = H;
-        g.E = E;
-        g.Ep = Ep;
-        g.T = T;
-        g.k_per_split = k_per_split;
-        g.x = static_cast<const uint16_t*>(x);
-        g.wr = w_router;
-        g.part = logits;
-        g.gamma = nm.gamma;
-        g.rstd = nm.rstd;
-        const size_t smem = ((size_t)kRM + 3 * (size_t)g.Ep) * kRPitch * sizeof(uint16_t);
-        const dim3 grid((T + kRM - 1) / kRM, splits);
-        auto run = [&](auto kern) -> cudaError_t {
-            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            kern<<<grid, 256, smem, st>>>(g);
-            return cudaGetLastError();
-        };
-        auto pick = [&](auto ntw) -> cudaError_t { return run(router_mma_kernel<decltype(ntw)::value>); };
-        switch (g.Ep / 16) {  // n_routed <= 256
-            case 1: e2 = pick(std::integral_constant<int, 1>{}); break;
-            case 2: e2 = pick(std::integral_constant<int, 2>{}); break;
-            case 3: e2 = pick(std::integral_constant<int, 3>{}); break;
-            case 4: e2 = pick(std::integral_constant<int, 4>{}); break;
-            case 5: e2 = pick(std::integral_constant<int, 5>{}); break;
-            case 6: e2 = pick(std::integral_constant<int, 6>{}); break;
-            case 7: e2 = pick(std::integral_constant<int, 7>{}); break;
-            case 8: e2 = pick(std::integral_constant<int, 8>{}); break;
-            case 9: e2 = pick(std::integral_constant<int, 9>{}); break;
-            case 10: e2 = pick(std::integral_constant<int, 10>{}); break;
-            case 11: e2 = pick(std::integral_constant<int, 11>{}); break;
-            case 12: e2 = pick(std::integral_constant<int, 12>{}); break;
-            case 13: e2 = pick(std::integral_constant<int, 13>{}); break;
-            case 14: e2 = pick(std::integral_constant<int, 14>{}); break;
-            case 15: e2 = pick(std::integral_constant<int, 15>{}); break;
-            case 16: e2 = pick(std::integral_constant<int, 16>{}); break;
-        }
+    // split the router weights, then the GEMM
+    if (!w3) return cudaErrorInvalidValue;
+    {
+        const size_t n4 = (size_t)Ep * H / 4;
+        const unsigned blocks = (unsigned)std::min<size_t>(1024, (n4 + 255) / 256);
+        router_split_kernel<<<blocks, 256, 0, st>>>(w_router, E, Ep, H, w3);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    TmaMap tx, tw;
+    if (!tmap_bf16_2d(&tx, x, (uint64_t)T, (uint64_t)H, kRTK, kRTM) ||
+        !tmap_bf16_2d(&tw, w3, (uint64_t)3 * Ep, (uint64_t)H, kRTK, (uint32_t)Ep))
+        return cudaErrorInvalidValue;
+    RouterTcParams p;
+    p.T = T;
+    p.E = E;
+    p.Ep = Ep;
+    p.H = H;
+    p.k_per_split = k_per_split;
+    p.n_mt = (T + kRTM - 1) / kRTM;
+    p.part = logits;
+    p.status = status;
+    const size_t stage = (size_t)kRTSA + 3 * (size_t)Ep * kRTK * 2;
+    const size_t room = 227 * 1024 - 1024 - 256;
+    p.stages = (int)std::min<size_t>(4, room / stage);
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + (size_t)p.stages * stage + 256;
+    auto run = [&](auto kern) -> cudaError_t {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kern<<<p.n_mt * splits, kRTThreads, smem, st>>>(p, tx, tw);
+        return cudaGetLastError();
+    };
+    auto pick = [&](auto nch) -> cudaError_t { return run(router_tc_kernel<decltype(nch)::value>); };
+    switch (Ep / 16) {  // n_routed <= 256
+        case 1: e2 = pick(std::integral_constant<int, 1>{}); break;
+        case 2: e2 = pick(std::integral_constant<int, 2>{}); break;
+        case 3: e2 = pick(std::integral_constant<int, 3>{}); break;
+        case 4: e2 = pick(std::integral_constant<int, 4>{}); break;
+        case 5: e2 = pick(std::integral_constant<int, 5>{}); break;
+        case 6: e2 = pick(std::integral_constant<int, 6>{}); break;
+        case 7: e2 = pick(std::integral_constant<int, 7>{}); break;
+        case 8: e2 = pick(std::integral_constant<int, 8>{}); break;
+        case 9: e2 = pick(std::integral_constant<int, 9>{}); break;
+        case 10: e2 = pick(std::integral_constant<int, 10>{}); break;
+        case 11: e2 = pick(std::integral_constant<int, 11>{}); break;
+        case 12: e2 = pick(std::integral_constant<int, 12>{}); break;
+        case 13: e2 = pick(std::integral_constant<int, 13>{}); break;
+        case 14: e2 = pick(std::integral_constant<int, 14>{}); break;
+        case 15: e2 = pick(std::integral_constant<int, 15>{}); break;
+        case 16: e2 = pick(std::integral_constant<int, 16>{}); break;
     }
     if (e2 != cudaSuccess) return e2;
     cudaError_t err = cudaGetLastError();
