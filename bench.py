@@ -208,6 +208,7 @@ def _layer_flops(cfg, T: int) -> int:
 # the current kernel exists.
 NCU_TRAFFIC_BYTES = {
     ("dsv2_decode_t1", "gateup_stream_kernel"): 135_087_360,   # 130.11 MB read + 4.98 MB written
+    ("dsv2_decode_t64", "gateup_stream_kernel"): 2_369_053_448,  # 2.3621 GB read + 6.9 MB written
     ("dsv2_zipf_t2048", "expert_gemm_kernel<0>"): 2_713_453_440,  # 2.6908 GB read + 22.7 MB written
     ("prefill_t4096", "expert_gemm_kernel<0>"): 2_619_613_920,  # 2.5478 GB read + 71.8 MB written
     ("prefill_t4096", "expert_gemm_mx_kernel<0>"): 2_705_107_000,  # 2.6330 GB read + 72.2 MB written
