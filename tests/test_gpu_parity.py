@@ -67,6 +67,27 @@ def test_route_ids_bit_exact(name):
     assert B.moe_read_device_status(ws) == 0
 
 
+# The large-T router on tcgen05 at expert counts that are not multiples of 16 (zero rows
+# up to the MMA's N) or of 4 (the partial logits stored one float at a time), the largest
+# count (256: 16 column chunks per epilogue thread), ragged token tiles and several K splits.
+@pytest.mark.parametrize("E,G,Gk,k,T,H", [(18, 3, 2, 4, 65, 512), (36, 4, 2, 6, 600, 512),
+                                          (20, 4, 4, 3, 300, 1024), (256, 8, 4, 8, 130, 512)])
+def test_large_t_router_ids_bit_exact(E, G, Gk, k, T, H):
+    cfg = MoEConfig(H, 256, E, G, Gk, k, 2.5, 1)
+    wr, _ = make_router(cfg, 50 + E, "cuda")
+    bias = (torch.arange(E, device="cuda", dtype=torch.float32) % 5) * 1e-3
+    x = make_tokens(cfg, T, 51 + T, "cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = B.alloc_workspace(cfg, T)
+    B.moe_route(cfg, x, wr, bias, ids, w, ws)
+    torch.cuda.synchronize()
+    ids_o, w_o, p_o, margin = oracle.route(cfg, x.cpu(), wr.cpu(), bias.cpu())
+    ids_eff, w_eff, _ = effective_routing(cfg, ids.cpu().numpy(), ids_o, p_o, margin)
+    np.testing.assert_allclose(w.cpu().numpy(), w_eff, rtol=2e-5, atol=1e-7)
+    assert B.moe_read_device_status(ws) == 0
+
+
 # ------------------------------------------------------------- permutation
 @pytest.mark.parametrize("T,E,k", [(1, 160, 6), (37, 16, 4), (64, 160, 6), (4096, 64, 8), (2048, 160, 6),
                                    (5000, 256, 16)])
